@@ -1,0 +1,385 @@
+"""Pins of the fp64 CPU oracle against things other than itself.
+
+Each pin is a closed form, a special case that reduces to a library routine
+(torch rms_norm / scaled_dot_product_attention / logsumexp), an invariant of
+the definitions, or brute force on tiny inputs.  They are chosen so that a
+dropped term, a wrong sign or index, or a transposed operand in the oracle
+fails at least one of them.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def b16(x):
+    """fp64 array -> bf16 bit patterns via torch's round-to-nearest-even."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(bits):
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(
+        torch.float64).numpy()
+
+
+# --------------------------------------------------------------------- bf16
+def test_bf16_widening_exact(orc):
+    bits = np.array([0x3F80, 0xC000, 0x0001, 0x7F7F, 0x8000, 0x3EAB], np.uint16)
+    ref = np.array([1.0, -2.0, 2.0 ** -133, (2 - 2 ** -7) * 2.0 ** 127, -0.0,
+                    0.333984375], np.float64)
+    np.testing.assert_array_equal(orc.bf16_to_f64(bits), ref)
+
+
+def test_bf16_rounding_matches_torch(orc):
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 6, 20000),
+                        [1.00390625, 1.01171875, -1.00390625, 3e-39, 1e-45]])
+    x32 = x.astype(np.float32).astype(np.float64)  # torch rounds from fp32
+    np.testing.assert_array_equal(orc.f64_to_bf16(x32), b16(x32))
+
+
+# --------------------------------------------------------------------- RMSNorm
+def test_rmsnorm_matches_torch(orc):
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((7, 64))
+    g = rng.standard_normal(64).astype(np.float32)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (64,),
+                                       torch.from_numpy(g.astype(np.float64)), eps=1e-6).numpy()
+    np.testing.assert_allclose(orc.rmsnorm(x, g, 1e-6), ref, rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------------- RoPE
+def test_rope_hand_cases(orc):
+    # pair 0 has theta = 1: e_{d0} at position 1 -> (cos 1, sin 1)
+    x = orc.rope(np.array([0.0, 0.0, 1.0, 0.0]), 2, 1)
+    np.testing.assert_allclose(x, [0, 0, math.cos(1), math.sin(1)], atol=1e-15)
+    # interleaved pairing: e_{d0+1} -> (-sin p, cos p) in dims (d0, d0+1)
+    x = orc.rope(np.array([5.0, 0.0, 1.0]), 2, 3)
+    np.testing.assert_allclose(x, [5.0, -math.sin(3), math.cos(3)], atol=1e-15)
+    # pair 1 of r=4 has theta = 10000^(-2/4) = 0.01: position 100 -> angle 1
+    x = orc.rope(np.array([0.0, 0.0, 1.0, 0.0]), 4, 100)
+    np.testing.assert_allclose(x, [0.0, 0.0, math.cos(1), math.sin(1)], atol=1e-13)
+
+
+def test_rope_invariants(orc):
+    rng = np.random.default_rng(3)
+    D, r = 64, 16
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    for p in [0, 1, 77, 1 << 20]:
+        y = orc.rope(q, r, p)
+        np.testing.assert_array_equal(y[:D - r], q[:D - r])          # untouched head
+        assert abs(np.linalg.norm(y[D - r:]) - np.linalg.norm(q[D - r:])) < 1e-12
+        np.testing.assert_allclose(orc.rope(y, r, p, sign=-1), q, atol=1e-9)
+    # relative position: <R_a q, R_b k> depends only on a - b
+    d1 = orc.rope(q, r, 1000) @ orc.rope(k, r, 990)
+    d2 = orc.rope(q, r, 10) @ orc.rope(k, r, 0)
+    assert abs(d1 - d2) < 1e-10
+
+
+# --------------------------------------------------------------------- compressor
+def test_compressor_hand_case(orc):
+    # C(1,2), gates (0, g) over c0=(1,0), c1=(0,1): entry 1 = (a0, a1), then RMSNorm
+    g = f64(b16([math.log(3.0)]))[0]
+    kv = b16([[[1.0, 0.0], [0.0, 1.0]]])
+    gate = b16([[0.0, g]])
+    out, _, alpha = orc.compress(kv, gate, m=1, w=2, r=0, j_begin=1, j_end=2, eps=0.0)
+    a1 = math.exp(g) / (1 + math.exp(g))
+    a0 = 1 - a1
+    rms = math.sqrt((a0 * a0 + a1 * a1) / 2)
+    np.testing.assert_allclose(out[0, 0], [a0 / rms, a1 / rms], rtol=1e-14)
+    np.testing.assert_allclose(alpha[0, 0], [a0, a1], rtol=1e-14)
+    # with exact ln 3 these are the hand values 0.4472135955, 1.3416407865
+    assert abs(a0 / rms - 0.4472135955) < 3e-3 and abs(a1 / rms - 1.3416407865) < 3e-3
+
+
+def test_compressor_window_membership_brute_force(orc):
+    """One-hot tokens + uniform gates: entry j = mean of exactly the tokens in
+    [m(j+1)-w, m(j+1)-1] that exist (CSA: the 8 tokens [4j-4, 4j+4))."""
+    for (m, w) in [(4, 8), (4, 4), (2, 6), (1, 1), (3, 3)]:
+        L = 24
+        kv = b16(np.eye(L)[None])          # token u = e_u, D = L
+        ik = b16(np.eye(L)[None] * 2.0)
+        gate = b16(np.zeros((1, L)))
+        nj = L // m
+        kvc, ikc, alpha = orc.compress(kv, gate, m, w, 0, 0, nj, ik_raw=ik, eps=0.0)
+        for j in range(nj):
+            members = [u for u in range(m * (j + 1) - w, m * (j + 1)) if u >= 0]
+            pre = np.zeros(L)
+            pre[members] = 1.0 / len(members)
+            # RMSNorm of the mean: members get 1/len / rms
+            rms = math.sqrt(np.mean(pre ** 2))
+            np.testing.assert_allclose(kvc[0, j], pre / rms, rtol=1e-13, atol=1e-15)
+            np.testing.assert_allclose(ikc[0, j], 2 * pre, rtol=1e-13, atol=1e-15)
+            np.testing.assert_allclose(alpha[0, j].sum(), 1.0, rtol=1e-14)
+            dropped = [s for s in range(w) if m * (j + 1) - w + s < 0]
+            assert all(alpha[0, j, s] == 0 for s in dropped)
+
+
+def test_compressor_gate_limits_and_constants(orc):
+    rng = np.random.default_rng(4)
+    L, D, dI = 16, 32, 8
+    kv = b16(rng.standard_normal((1, L, D)))
+    ik = b16(rng.standard_normal((1, L, dI)))
+    # one dominating gate selects that token (softmax -> one-hot)
+    gate = np.zeros((1, L))
+    gate[0, 6] = 80.0
+    kvc, ikc, _ = orc.compress(kv, b16(gate), 4, 8, 0, 1, 2, ik_raw=ik, eps=0.0)
+    tok = f64(kv)[0, 6]
+    np.testing.assert_allclose(kvc[0, 0], tok / math.sqrt(np.mean(tok ** 2)), rtol=1e-12)
+    np.testing.assert_allclose(ikc[0, 0], f64(ik)[0, 6], rtol=1e-12)
+    # constant tokens give the normalised constant, for any gates
+    c = b16(np.tile(rng.standard_normal(D), (1, L, 1)))
+    kvc, _, _ = orc.compress(c, b16(rng.standard_normal((1, L))), 4, 8, 0, 0, 4, eps=0.0)
+    cv = f64(c)[0, 0]
+    for j in range(4):
+        np.testing.assert_allclose(kvc[0, j], cv / math.sqrt(np.mean(cv ** 2)), rtol=1e-12)
+
+
+def test_compressor_rope_position_and_identity(orc):
+    """C(1,1) is the identity before norm; entries are roped at m(j+1)-1."""
+    rng = np.random.default_rng(5)
+    L, D, r = 12, 16, 8
+    kv = b16(rng.standard_normal((1, L, D)))
+    gate = b16(rng.standard_normal((1, L)))
+    c11, _, _ = orc.compress(kv, gate, 1, 1, r, 0, L)
+    for u in range(L):
+        ref = orc.rope(orc.rmsnorm(f64(kv)[0, u], None, 1e-6), r, u)
+        np.testing.assert_allclose(c11[0, u], ref, rtol=1e-13, atol=1e-13)
+    const = b16(np.tile(rng.standard_normal(D), (1, L, 1)))
+    c4, _, _ = orc.compress(const, gate, 4, 8, r, 0, 3)
+    base = orc.rmsnorm(f64(const)[0, 0], None, 1e-6)
+    for j in range(3):
+        np.testing.assert_allclose(c4[0, j], orc.rope(base, r, 4 * (j + 1) - 1), atol=1e-13)
+
+
+# --------------------------------------------------------------------- indexer
+def test_indexer_special_cases(orc):
+    rng = np.random.default_rng(6)
+    B, T, HI, dI, N, m = 1, 3, 3, 8, 5, 4
+    iq = b16(rng.standard_normal((B, T, HI, dI)))
+    ik = b16(rng.standard_normal((B, N, dI)))
+    pos = np.array([[2, 3, 19]], np.int32)     # visible: 0, 1, 5
+    q, k = f64(iq), f64(ik)
+    for h in range(HI):                         # one-hot w picks relu(q_h . k_j)
+        w = np.zeros((B, T, HI), np.float32)
+        w[..., h] = 1.0
+        s = orc.indexer_scores(iq, w, ik, pos, m)
+        assert np.isnan(s[0, 0]).all()                       # t=2: nothing visible
+        assert np.isnan(s[0, 1, 1:]).all()                   # t=3: only entry 0
+        for t, nv in [(1, 1), (2, 5)]:
+            ref = np.maximum(np.dot(k[0, :nv], q[0, t, h]), 0.0)
+            np.testing.assert_allclose(s[0, t, :nv], ref, rtol=1e-14, atol=1e-14)
+    # linear in w (including negative weights)
+    w1 = rng.standard_normal((B, T, HI)).astype(np.float32)
+    w2 = rng.standard_normal((B, T, HI)).astype(np.float32)
+    s1 = orc.indexer_scores(iq, w1, ik, pos, m)
+    s2 = orc.indexer_scores(iq, w2, ik, pos, m)
+    s12 = orc.indexer_scores(iq, (w1.astype(np.float64) + w2).astype(np.float32), ik, pos, m)
+    ok = ~np.isnan(s1)
+    np.testing.assert_allclose(s12[ok], (s1 + s2)[ok], rtol=1e-5, atol=1e-5)
+
+
+# --------------------------------------------------------------------- top-k
+def _pairwise_rule_ok(sc, chosen, n):
+    ch = set(chosen)
+    for i in ch:
+        for j in range(n):
+            if j in ch:
+                continue
+            if not (sc[i] > sc[j] or (sc[i] == sc[j] and i < j)):
+                return False
+    return True
+
+
+def test_topk_brute_force_with_ties(orc):
+    rng = np.random.default_rng(7)
+    for trial in range(300):
+        n = int(rng.integers(1, 11))
+        k = int(rng.integers(1, 5))
+        sc = rng.integers(-3, 4, n).astype(np.float64)        # many ties
+        pos = np.array([4 * n - 1], np.int32)                 # m=4: n visible
+        idx = orc.topk(sc[None], pos, 4, k)[0]
+        keff = min(k, n)
+        assert (idx[keff:] == -1).all()
+        chosen = list(idx[:keff])
+        assert len(set(chosen)) == keff
+        best = max(sum(sc[list(c)]) for c in itertools.combinations(range(n), keff))
+        assert sum(sc[chosen]) == best
+        assert _pairwise_rule_ok(sc, chosen, n)
+
+
+def test_topk_planted(orc):
+    N = 1000
+    sc = np.linspace(-1, 1, N)[np.random.default_rng(8).permutation(N)]
+    top = np.argsort(-sc)[:10]
+    idx = orc.topk(sc[None], np.array([4 * N - 1], np.int32), 4, 10)[0]
+    np.testing.assert_array_equal(idx, top)
+    # visibility: a query at t sees only (t+1)//4 entries
+    idx = orc.topk(sc[None], np.array([4 * 7 + 2], np.int32), 4, 10)[0]
+    assert sorted(idx[:7]) == list(range(7)) and (idx[7:] == -1).all()
+
+
+# --------------------------------------------------------------------- attention
+def _sdpa(qt, keys, causal_lens=None):
+    """Library reference: torch SDPA in fp64 with V = K, plus logsumexp."""
+    q = torch.from_numpy(qt)[None, None]          # [1,1,1,D]
+    k = torch.from_numpy(keys)[None, None]        # [1,1,n,D]
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, k)[0, 0, 0].numpy()
+    lg = (q @ k.transpose(-1, -2))[0, 0, 0] / math.sqrt(qt.shape[0])
+    return o, torch.logsumexp(lg, 0).item()
+
+
+def _prep_q(orc, q, r, t):
+    return orc.rope(torch.nn.functional.rms_norm(torch.from_numpy(q), (q.shape[0],),
+                                                 eps=1e-6).numpy(), r, t)
+
+
+def test_csa_with_large_k_is_dense_attention(orc):
+    rng = np.random.default_rng(9)
+    B, T, H, D, r, N = 1, 3, 2, 32, 8, 20
+    cache = b16(rng.standard_normal((B, N, D)))
+    q = b16(rng.standard_normal((B, T, H, D)))
+    pos = np.array([[15, 40, 83]], np.int32)          # m=4 -> 4, 10, 20 visible
+    idx = np.full((B, T, 32), -1, np.int32)
+    for t in range(T):
+        nv = min((pos[0, t] + 1) // 4, N)
+        idx[0, t, :nv] = rng.permutation(nv)
+    o, l = orc.attention(orc.KIND_SPARSE, q, cache, pos, idx=idx, r=r)
+    oh, lh = orc.attention(orc.KIND_HCA, q, cache, pos, m=4, r=r)
+    keys = f64(cache)[0]
+    for t in range(T):
+        nv = min((pos[0, t] + 1) // 4, N)
+        for h in range(H):
+            ref_o, ref_l = _sdpa(_prep_q(orc, f64(q)[0, t, h], r, pos[0, t]), keys[:nv])
+            np.testing.assert_allclose(o[0, t, h], ref_o, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(oh[0, t, h], ref_o, rtol=1e-12, atol=1e-12)
+            assert abs(l[0, t, h] - ref_l) < 1e-12 and abs(lh[0, t, h] - ref_l) < 1e-12
+
+
+def test_m1_uniform_gates_and_large_window_are_causal_attention(orc):
+    """C(1,1) + CSA with k >= visible, and SWA with W >= L, both equal standard
+    causal attention over the normalised, roped tokens (torch SDPA, is_causal)."""
+    rng = np.random.default_rng(10)
+    B, L, H, D, r = 1, 24, 2, 32, 8
+    raw = b16(rng.standard_normal((B, L, D)))
+    q = b16(rng.standard_normal((B, L, H, D)))
+    pos = np.arange(L, dtype=np.int32)[None]
+    c11, _, _ = orc.compress(raw, b16(np.zeros((B, L))), 1, 1, r, 0, L)
+    cache = orc.f64_to_bf16(c11)
+    idx = np.tile(np.arange(L, dtype=np.int32), (B, L, 1))
+    idx[np.arange(L)[None, :, None] < np.arange(L)[None, None, :]] = -1
+    o_csa, l_csa = orc.attention(orc.KIND_SPARSE, q, cache, pos, idx=idx, r=r)
+    o_swa, l_swa = orc.attention(orc.KIND_SWA, q, raw, pos, W=L + 5, r=r)
+    keys_csa = f64(cache)[0]
+    keys_swa = np.stack([orc.rope(orc.rmsnorm(f64(raw)[0, u], None, 1e-6), r, u)
+                         for u in range(L)])
+    qq = np.stack([[_prep_q(orc, f64(q)[0, t, h], r, t) for t in range(L)] for h in range(H)])
+    for keys, o in [(keys_csa, o_csa), (keys_swa, o_swa)]:
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(qq)[None], torch.from_numpy(keys)[None, None].expand(1, H, L, D),
+            torch.from_numpy(keys)[None, None].expand(1, H, L, D), is_causal=True)[0]
+        np.testing.assert_allclose(o[0].transpose(1, 0, 2), ref.numpy(), rtol=1e-11, atol=1e-11)
+
+
+def test_hand_cases_two_and_three_tokens(orc):
+    """D=2, r=0, eps=0, H=1, s=1/sqrt(2), sink 0 (closed forms)."""
+    s2 = math.sqrt(2.0)
+    raw = b16([[[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]]])
+    q = b16([[[[1.0, 0.0]]]])
+    sink = np.array([0.0], np.float32)
+    # 2 tokens, query at t=1: logits (sqrt2, 0)
+    o, l = orc.attention(orc.KIND_SWA, q, raw, np.array([[1]], np.int32), W=128, eps=0.0)
+    out, lse = orc.merge([o], [l], sink, np.array([[1]], np.int32), 0)
+    z = math.exp(s2) + 1 + 1
+    w0, w1 = math.exp(s2) / z, 1 / z
+    np.testing.assert_allclose(out[0, 0, 0], [w0 * s2, w1 * s2], rtol=1e-13)
+    assert abs(lse[0, 0, 0] - math.log(z)) < 1e-13
+    np.testing.assert_allclose([w0, w1, out[0, 0, 0, 0], out[0, 0, 0, 1], lse[0, 0, 0]],
+                               [0.6728417984, 0.1635791008, 0.9515419966, 0.2313357829,
+                                1.8104586086], atol=1e-9)
+    out_ns, _ = orc.merge([o], [l], None, np.array([[1]], np.int32), 0)   # no sink
+    np.testing.assert_allclose(out_ns[0, 0, 0], [1.1376353670, 0.2765781954], atol=1e-9)
+    # 3 tokens, query at t=2: logits (sqrt2, 0, 1), keys (sqrt2,0), (0,sqrt2), (1,1)
+    o, l = orc.attention(orc.KIND_SWA, q, raw, np.array([[2]], np.int32), W=128, eps=0.0)
+    out, lse = orc.merge([o], [l], sink, np.array([[2]], np.int32), 0)
+    z = math.exp(s2) + 1 + math.e + 1
+    ref = np.array([math.exp(s2) * s2 + math.e, s2 + math.e]) / z
+    np.testing.assert_allclose(out[0, 0, 0], ref, rtol=1e-13)
+    np.testing.assert_allclose([out[0, 0, 0, 0], out[0, 0, 0, 1], lse[0, 0, 0]],
+                               [0.9664570201, 0.4679250773, 2.1783285225], atol=1e-9)
+    # window 2: only tokens 1 and 2
+    o, l = orc.attention(orc.KIND_SWA, q, raw, np.array([[2]], np.int32), W=2, eps=0.0)
+    out, _ = orc.merge([o], [l], sink, np.array([[2]], np.int32), 0)
+    np.testing.assert_allclose(out[0, 0, 0], [0.5761168848, 0.8758475100], atol=1e-9)
+
+
+def test_weights_plus_sink_sum_to_one(orc):
+    rng = np.random.default_rng(11)
+    D, n = 16, 9
+    keys = rng.standard_normal((n, D))
+    qt = rng.standard_normal(D)
+    for sink in [-5.0, 0.0, 3.0]:
+        w, ws = orc.weights_with_sink(qt, keys, 1 / 4.0, sink)
+        assert abs(w.sum() + ws - 1.0) < 1e-12
+        # the merged output agrees: sink only enlarges the denominator
+        lg = keys @ qt / 4.0
+        ref = (np.exp(lg)[:, None] * keys).sum(0) / (np.exp(lg).sum() + math.exp(sink))
+        np.testing.assert_allclose((w[:, None] * keys).sum(0), ref, rtol=1e-12)
+
+
+def test_merge_of_split_equals_union(orc):
+    """LSE merge of two disjoint key sets equals attention over their union."""
+    rng = np.random.default_rng(12)
+    B, T, H, D, r, N = 2, 2, 3, 32, 8, 40
+    cache = b16(rng.standard_normal((B, N, D)))
+    q = b16(rng.standard_normal((B, T, H, D)))
+    pos = np.full((B, T), 4 * N - 1, np.int32)
+    sink = rng.standard_normal(H).astype(np.float32)
+    for trial in range(3):
+        perm = np.stack([np.stack([rng.permutation(N) for _ in range(T)]) for _ in range(B)])
+        cut = int(rng.integers(1, N))
+        a = np.full((B, T, N), -1, np.int32)
+        b_ = np.full((B, T, N), -1, np.int32)
+        a[..., :cut] = perm[..., :cut]
+        b_[..., :N - cut] = perm[..., cut:]
+        oa, la = orc.attention(orc.KIND_SPARSE, q, cache, pos, idx=a, r=r)
+        ob, lb = orc.attention(orc.KIND_SPARSE, q, cache, pos, idx=b_, r=r)
+        ou, lu = orc.attention(orc.KIND_SPARSE, q, cache, pos, idx=perm.astype(np.int32), r=r)
+        m2, l2 = orc.merge([oa, ob], [la, lb], sink, pos, r)
+        m1, l1 = orc.merge([ou], [lu], sink, pos, r)
+        np.testing.assert_allclose(m2, m1, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(l2, l1, rtol=1e-12)
+
+
+def test_merge_inverse_rope_and_empty_branch(orc):
+    rng = np.random.default_rng(13)
+    B, T, H, D, r = 1, 2, 2, 16, 8
+    o = rng.standard_normal((B, T, H, D))
+    l = rng.standard_normal((B, T, H))
+    pos = np.array([[5, 1000]], np.int32)
+    out, lse = orc.merge([o], [l], None, pos, r)
+    for t in range(T):
+        for h in range(H):
+            np.testing.assert_allclose(orc.rope(out[0, t, h], r, pos[0, t]), o[0, t, h],
+                                       atol=1e-12)
+    np.testing.assert_allclose(lse, l, rtol=1e-14)
+    # an empty branch (lse = -inf, o = 0) changes nothing
+    out2, lse2 = orc.merge([o, np.zeros_like(o)], [l, np.full_like(l, -np.inf)], None, pos, r)
+    np.testing.assert_allclose(out2, out, rtol=1e-14)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-14)
+
+
+def test_tiny_layer_runs(orc):
+    from sparse_attention_26_b300 import synth
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.to_numpy(synth.make_inputs(wl, 0))
+    res = orc.layer(inp, wl.cfg(), keep=True)
+    assert np.isfinite(res["out"]).all()
+    assert res["idx"].shape == (1, 256, 16)
+    # early queries see fewer than k entries: padded with -1
+    assert (res["idx"][0, 10, 2:] == -1).all() and (res["idx"][0, 10, :2] >= 0).all()

@@ -1,0 +1,193 @@
+/*
+ * hattn.h -- C ABI of libhattn, a B300 (sm_103a) implementation of the
+ * DeepSeek-V4 hybrid attention layer: CSA (compressed sparse attention),
+ * HCA (heavily compressed attention), SWA (sliding-window attention) and the
+ * sink-augmented log-sum-exp merge of their outputs.
+ *
+ * Sources (web pages on DeepSeek-V4, cited by title and section):
+ *   [DD] "Why DeepSeek V4 Stands Apart: A Deep Dive into Its Architecture and
+ *        Performance", section "Core Architectural Innovations".
+ *   [AT] "DeepSeek-V4" (atlas spec sheet), sections "Design overview",
+ *        "Spec sheet / Core block", "Inference efficiency", and
+ *        "Provenance references" items 15-18.
+ *
+ * Conventions shared by every call
+ *   - Tensors are dense, row-major, in DEVICE memory.  bf16 tensors are passed
+ *     as `const void*` (16-bit storage).  Every tensor pointer must be 16-byte
+ *     aligned (HATTN_ERR_MISALIGNED otherwise).
+ *   - Shapes use: B sequences, T queries per sequence, H query heads, D head
+ *     dim (= the shared KV latent dim, a multiple of 64, at most 512), r RoPE
+ *     dims (the last r of each vector, even, r <= D), HI indexer heads, dI
+ *     indexer dim (a multiple of 8, at most 128), W SWA window.
+ *   - `pos` is an int32 device array [B][T] of absolute query positions.  A
+ *     query at position t has its own token already in the raw cache.
+ *   - RoPE rotates interleaved pairs (D-r+2i, D-r+2i+1) by the angle
+ *     p * rope_base^(-2i/r); RMSNorm is x / sqrt(mean(x^2) + eps) * gamma
+ *     (gamma fp32 [D], NULL means all ones).
+ *   - The caller owns every buffer, including workspaces; the library never
+ *     allocates device memory.  Every call only enqueues work on `stream`
+ *     (a cudaStream_t, NULL = legacy default stream) and never synchronises.
+ *   - Return value: HATTN_OK or an error code.  Argument errors are detected
+ *     on the host before anything is enqueued; the thread-local message from
+ *     hattn_last_error() says which argument.  Errors found on the device
+ *     (an out-of-range index, a wait that gave up) never trap the GPU: the
+ *     kernel records a code in a device status word and returns, and
+ *     hattn_check_status() reports it.
+ */
+#ifndef HATTN_H
+#define HATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define HATTN_API __attribute__((visibility("default")))
+#else
+#define HATTN_API
+#endif
+
+typedef void* hattn_stream_t; /* cudaStream_t */
+
+enum {
+  HATTN_OK = 0,
+  HATTN_ERR_INVALID_ARG = 1, /* null pointer, size out of range, inconsistent sizes */
+  HATTN_ERR_MISALIGNED = 2,  /* a tensor pointer is not 16-byte aligned */
+  HATTN_ERR_UNSUPPORTED = 3, /* valid by the definitions, but no kernel for this shape */
+  HATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+  HATTN_ERR_TIMEOUT = 5,     /* a device-side wait gave up (reported by hattn_check_status) */
+  HATTN_ERR_DEVICE_INDEX = 6 /* a device-side index was out of range (hattn_check_status) */
+};
+
+/* -------------------------------------------------------------------------
+ * KV compression.  [DD]: CSA compresses KV 4x (m=4), HCA 128:1.  [AT] "Design
+ * overview": CSA compresses every 4 tokens into two overlapping streams;
+ * RMSNorm on the compressed KV entries.
+ *
+ * Entry j pools the tokens u in [m(j+1)-w, m(j+1)-1] that exist (u >= 0) with
+ * weights softmax over those tokens of the bf16 gate logit gate[b][u]; the
+ * pooled KV vector is RMSNorm'd (gamma_kv, eps) and RoPE'd at position
+ * m(j+1)-1; the pooled indexer key uses the same weights, with no norm and
+ * no RoPE.  CSA is m=4, w=8 (the 8 tokens [4j-4, 4j+4)).
+ *
+ *   kv_raw [B][L_cap][D] bf16, ik_raw [B][L_cap][dI] bf16, gate [B][L_cap] bf16
+ *   entries j in [j_begin, j_end) are written to row j of
+ *   kv_c [B][N_cap][D] bf16 and ik_c [B][N_cap][dI] bf16 (other rows untouched);
+ *   requires j_end <= N_cap, m*j_end <= L_cap, w % m == 0, w >= m, w <= 512.
+ *   j_begin == j_end is a no-op.  Fused single pass: each token row is read
+ *   from HBM once per window it belongs to, each entry written once.
+ * ---------------------------------------------------------------------- */
+HATTN_API int hattn_csa_compress(const void* kv_raw, const void* ik_raw, const void* gate,
+                       const float* gamma_kv, int B, int64_t L_cap, int D, int dI, int m, int w,
+                       int r, float rope_base, float eps, int64_t j_begin, int64_t j_end,
+                       void* kv_c, void* ik_c, int64_t N_cap, hattn_stream_t stream);
+
+/* HCA compression: the same compressor with w = m (non-overlapping windows,
+ * m = 128 on the pages) and no indexer key.  kv_h [B][N_cap][D] bf16. */
+HATTN_API int hattn_hca_compress(const void* kv_raw, const void* gate, const float* gamma_kv, int B,
+                       int64_t L_cap, int D, int m, int r, float rope_base, float eps,
+                       int64_t j_begin, int64_t j_end, void* kv_h, int64_t N_cap,
+                       hattn_stream_t stream);
+
+/* -------------------------------------------------------------------------
+ * Lightning indexer + per-query top-k.  [DD]: CSA keeps the top-1024 (Pro) /
+ * top-512 (Flash) compressed entries per query.  [AT] "Design overview": the
+ * V3.2 lightning-indexer sparse attention.
+ *
+ * For each query (b, t) with n = min(floor((pos+1)/m), N_cap) visible entries:
+ *   I[j] = sum_h w[b][t][h] * max(0, iq[b][t][h] . ik_c[b][j])   for j < n
+ *   idx_out[b][t][0..k) = the min(k, n) entries with the largest I (ties to the
+ *   smaller j), in unspecified order, then -1 padding.
+ *
+ *   iq [B][T][HI][dI] bf16, w [B][T][HI] fp32, ik_c [B][N_cap][dI] bf16,
+ *   idx_out [B][T][k] int32, score_out [B][T][N_cap] fp32 or NULL (when given,
+ *   receives I for j < n; entries j >= n are left untouched).
+ *   workspace: device buffer of at least hattn_indexer_topk_workspace_bytes()
+ *   bytes (may be NULL when that is 0); contents need no initialisation.
+ *   Limits: 1 <= k <= 2048, HI * min(T, 256 / HI) <= 256, N_cap <= 786432.
+ * ---------------------------------------------------------------------- */
+HATTN_API int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
+                       int B, int T, int HI, int dI, int64_t N_cap, int k, int m,
+                       int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
+                       hattn_stream_t stream);
+HATTN_API size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
+                                          int score_out_given);
+
+/* -------------------------------------------------------------------------
+ * Attention branches.  Shared-KV MQA latent ([AT] "Inference efficiency"):
+ * keys and values are the same D-dim vectors K~ for all heads.  Each query
+ * head is prepared as q~ = RoPE_pos(RMSNorm(q; gamma_q, eps)); logits are
+ * scale * q~ . K~_j; the branch output is o = sum_j softmax_j K~_j (bf16) and
+ * lse = log sum_j exp(logit_j) (fp32, natural log).  An empty key set gives
+ * o = 0, lse = -inf.
+ *
+ *   q [B][T][H][D] bf16, o [B][T][H][D] bf16, lse [B][T][H] fp32.
+ *   workspace: at least hattn_attn_workspace_bytes(kind, ...) bytes (split-KV
+ *   partials); contents need no initialisation.  H <= 128.
+ * ---------------------------------------------------------------------- */
+
+/* CSA branch ([DD]: sparse attention over the selected compressed entries):
+ * keys are kv_c[b][idx[b][t][i]] for every i with idx >= 0 (-1 is padding).
+ * kv_c [B][N_cap][D] bf16 (normalised + roped entries), idx [B][T][k] int32.
+ * An idx >= N_cap is skipped and reported as HATTN_ERR_DEVICE_INDEX. */
+HATTN_API int hattn_sparse_attn(const void* q, const float* gamma_q, const void* kv_c, const int32_t* idx,
+                      const int32_t* pos, int B, int T, int H, int D, int64_t N_cap, int k, int r,
+                      float rope_base, float eps, float scale, void* o, float* lse,
+                      void* workspace, size_t ws_bytes, hattn_stream_t stream);
+
+/* HCA branch ([DD]: dense global attention over the 128:1 compressed KV):
+ * keys are kv_h[b][j] for j < min(floor((pos+1)/m), N_cap).  kv_h [B][N_cap][D]. */
+HATTN_API int hattn_hca_attn(const void* q, const float* gamma_q, const void* kv_h, const int32_t* pos,
+                   int B, int T, int H, int D, int64_t N_cap, int m, int r, float rope_base,
+                   float eps, float scale, void* o, float* lse, void* workspace,
+                   size_t ws_bytes, hattn_stream_t stream);
+
+/* SWA branch ([DD]: the most recent 128 tokens): keys are the raw tokens
+ * u in [max(0, pos-W+1), pos], each RMSNorm'd (gamma_kv, eps) and RoPE'd at
+ * position u on load.  kv_raw [B][L_cap][D] bf16. */
+HATTN_API int hattn_swa_attn(const void* q, const float* gamma_q, const void* kv_raw,
+                   const float* gamma_kv, const int32_t* pos, int B, int T, int H, int D,
+                   int64_t L_cap, int W, int r, float rope_base, float eps, float scale, void* o,
+                   float* lse, void* workspace, size_t ws_bytes, hattn_stream_t stream);
+
+/* kind: 0 = CSA sparse (n_keys = k), 1 = HCA (n_keys = N_cap), 2 = SWA (n_keys = W). */
+HATTN_API size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys);
+
+/* -------------------------------------------------------------------------
+ * Merge.  [AT] "Spec sheet / Core block": attention sinks; provenance 16:
+ * "-i RoPE on outputs".  For every (b, t, h):
+ *   Z = sum_i exp(lse_i) + exp(sink[h]);  y = sum_i exp(lse_i) o_i / Z
+ *   out = y with its last r dims rotated by -pos (inverse RoPE); lse_out = log Z.
+ * o_list / lse_list: HOST arrays of nb (1..4) DEVICE pointers to bf16
+ * [B][T][H][D] / fp32 [B][T][H] branch outputs.  sink fp32 [H] device or NULL
+ * (no sink term).  out [B][T][H][D] bf16, lse_out [B][T][H] fp32 or NULL.
+ * ---------------------------------------------------------------------- */
+HATTN_API int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int nb,
+                    const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
+                    float rope_base, void* out, float* lse_out, hattn_stream_t stream);
+
+/* -------------------------------------------------------------------------
+ * Status and diagnostics.
+ * ---------------------------------------------------------------------- */
+HATTN_API const char* hattn_status_string(int code);
+/* Thread-local description of the last error returned on this thread. */
+HATTN_API const char* hattn_last_error(void);
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device (HATTN_OK, HATTN_ERR_TIMEOUT or HATTN_ERR_DEVICE_INDEX),
+ * or HATTN_ERR_CUDA if the synchronisation itself failed. */
+HATTN_API int hattn_check_status(hattn_stream_t stream);
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nothing arrives on, giving up after timeout_ns nanoseconds; the
+ * kernel then records HATTN_ERR_TIMEOUT and returns (no fault, no hang). */
+HATTN_API int hattn_selftest_wait_timeout(uint64_t timeout_ns, hattn_stream_t stream);
+/* Library version string. */
+HATTN_API const char* hattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HATTN_H */

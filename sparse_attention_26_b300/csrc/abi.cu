@@ -1,0 +1,497 @@
+// abi.cu -- the extern "C" entry points of libhattn (declared in
+// include/hattn.h): argument validation, launch planning, TMA descriptor
+// encoding, kernel launches, and the device status word.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/hattn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace hattn;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_last_error[0] = '\0';
+  return HATTN_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(HATTN_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Device status word: one int per device, read and cleared by hattn_check_status.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+bool device_info(int* dev_out, int** status, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return false;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    g_status_ptr[dev] = static_cast<int*>(p);
+    g_num_sms[dev] = n;
+  }
+  if (dev_out) *dev_out = dev;
+  if (status) *status = g_status_ptr[dev];
+  if (sms) *sms = g_num_sms[dev];
+  return true;
+}
+
+int num_sms_or_default() {
+  int sms = 0;
+  if (!device_info(nullptr, nullptr, &sms)) {
+    cudaGetLastError();
+    return 148;
+  }
+  return sms;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle.  dims/strides innermost first; strides
+// in bytes for dims 1..rank-1.
+int make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(HATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bx,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(HATTN_ERR_CUDA, "tensor map for %s: CUresult %d", what, (int)r);
+  return HATTN_OK;
+}
+
+#define REQUIRE(cond, ...)                                  \
+  do {                                                      \
+    if (!(cond)) return fail(HATTN_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+#define REQUIRE_PTR(p)                                                         \
+  do {                                                                         \
+    if (!(p)) return fail(HATTN_ERR_INVALID_ARG, "%s must not be NULL", #p);   \
+    if (!aligned16(p)) return fail(HATTN_ERR_MISALIGNED, "%s is not 16-byte aligned", #p); \
+  } while (0)
+#define REQUIRE_F32(p)                                                         \
+  do {                                                                         \
+    if ((p) && !aligned4(p)) return fail(HATTN_ERR_MISALIGNED, "%s is not 4-byte aligned", #p); \
+  } while (0)
+
+int check_rope(int D, int r, float rope_base, float eps) {
+  REQUIRE(r >= 0 && r % 2 == 0 && r <= D && r <= 128, "r=%d must be even, <= D and <= 128", r);
+  REQUIRE(rope_base > 0.f, "rope_base must be positive");
+  REQUIRE(eps >= 0.f, "eps must be >= 0");
+  return HATTN_OK;
+}
+
+int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
+                    const float* gamma_kv, int B, int64_t L_cap, int D, int dI, int m, int w,
+                    int r, float rope_base, float eps, int64_t j_begin, int64_t j_end, void* kv_c,
+                    void* ik_c, int64_t N_cap, hattn_stream_t stream) {
+  REQUIRE_PTR(kv_raw);
+  REQUIRE_PTR(gate);
+  REQUIRE_PTR(kv_c);
+  REQUIRE_F32(gamma_kv);
+  REQUIRE((ik_raw == nullptr) == (ik_c == nullptr), "ik_raw and ik_c must both be given or both NULL");
+  if (ik_raw) {
+    REQUIRE_PTR(ik_raw);
+    REQUIRE_PTR(ik_c);
+    REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
+  }
+  REQUIRE(B >= 1 && L_cap >= 1 && N_cap >= 1, "B, L_cap and N_cap must be >= 1");
+  REQUIRE(D >= 64 && D <= 512 && D % 64 == 0, "D=%d must be a multiple of 64 in [64, 512]", D);
+  REQUIRE(m >= 1 && w >= m && w % m == 0 && w <= 512, "need 1 <= m <= w <= 512, w %% m == 0 (m=%d w=%d)", m, w);
+  int rc = check_rope(D, r, rope_base, eps);
+  if (rc) return rc;
+  REQUIRE(j_begin >= 0 && j_end >= j_begin && j_end <= N_cap, "entry range [%lld, %lld) outside [0, N_cap=%lld)",
+          (long long)j_begin, (long long)j_end, (long long)N_cap);
+  REQUIRE((int64_t)m * j_end <= L_cap, "entry %lld needs tokens beyond L_cap=%lld", (long long)(j_end - 1),
+          (long long)L_cap);
+  if (j_end == j_begin) return ok();
+  CompressArgs a;
+  a.kv_raw = static_cast<const __nv_bfloat16*>(kv_raw);
+  a.ik_raw = static_cast<const __nv_bfloat16*>(ik_raw);
+  a.gate = static_cast<const __nv_bfloat16*>(gate);
+  a.gamma = gamma_kv;
+  a.kv_out = static_cast<__nv_bfloat16*>(kv_c);
+  a.ik_out = static_cast<__nv_bfloat16*>(ik_c);
+  a.B = B;
+  a.D = D;
+  a.dI = ik_raw ? dI : 0;
+  a.m = m;
+  a.w = w;
+  a.r = r;
+  a.L_cap = L_cap;
+  a.N_cap = N_cap;
+  a.j_begin = j_begin;
+  a.j_end = j_end;
+  a.rope_base = rope_base;
+  a.eps = eps;
+  cudaError_t e = launch_compress(a, num_sms_or_default(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "compress launch");
+  return ok();
+}
+
+int attn_common(int kind, const void* q, const float* gamma_q, const void* kv,
+                const float* gamma_kv, const int32_t* idx, const int32_t* pos, int B, int T, int H,
+                int D, int64_t N_rows, int k, int m, int W, int r, float rope_base, float eps,
+                float scale, void* o, float* lse, void* workspace, size_t ws_bytes,
+                hattn_stream_t stream) {
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(kv);
+  REQUIRE_PTR(pos);
+  REQUIRE_PTR(o);
+  REQUIRE_PTR(lse);
+  REQUIRE_F32(gamma_q);
+  REQUIRE_F32(gamma_kv);
+  if (kind == kSparse) REQUIRE_PTR(idx);
+  REQUIRE(B >= 1 && T >= 1, "B and T must be >= 1");
+  REQUIRE(H >= 1 && H <= 128, "H=%d must be in [1, 128]", H);
+  REQUIRE(D >= 64 && D <= 512 && D % 64 == 0, "D=%d must be a multiple of 64 in [64, 512]", D);
+  REQUIRE(N_rows >= 1, "the key cache needs at least one row");
+  REQUIRE((int64_t)B * N_rows < (1ll << 31), "B * rows of the cache must be < 2^31");
+  if (kind == kSparse) REQUIRE(k >= 1 && k <= 65536, "k=%d out of range", k);
+  if (kind == kHca) REQUIRE(m >= 1, "m must be >= 1");
+  if (kind == kSwa) REQUIRE(W >= 1, "W must be >= 1");
+  REQUIRE(scale > 0.f, "scale must be positive");
+  int rc = check_rope(D, r, rope_base, eps);
+  if (rc) return rc;
+  const int64_t n_keys = kind == kSparse ? k : (kind == kHca ? N_rows : W);
+  AttnPlan p;
+  if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p))
+    return fail(HATTN_ERR_UNSUPPORTED, "no attention kernel for H=%d D=%d", H, D);
+  if (p.ws_bytes > 0) {
+    REQUIRE_PTR(workspace);
+    REQUIRE(ws_bytes >= p.ws_bytes, "workspace of %zu bytes, need %zu", ws_bytes, p.ws_bytes);
+  }
+  int* status = nullptr;
+  if (!device_info(nullptr, &status, nullptr)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  CUtensorMap tm;
+  memset(&tm, 0, sizeof tm);
+  if (kind == kHca) {
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)N_rows};
+    const uint64_t strides[1] = {(uint64_t)D * 2};
+    const uint32_t box[2] = {64, 64};
+    rc = make_tmap(&tm, kv, 2, dims, strides, box, "kv_h");
+    if (rc) return rc;
+  }
+  AttnArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.gamma_q = gamma_q;
+  a.kv = static_cast<const __nv_bfloat16*>(kv);
+  a.gamma_kv = gamma_kv;
+  a.idx = idx;
+  a.pos = pos;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  float* ws = static_cast<float*>(workspace);
+  const int64_t rows = (int64_t)B * T * H;
+  a.part_o = p.nsplit > 1 ? ws : nullptr;
+  a.part_lse = p.nsplit > 1 ? ws + rows * p.nsplit * D : nullptr;
+  a.status = status;
+  a.kind = kind;
+  a.B = B;
+  a.T = T;
+  a.H = H;
+  a.D = D;
+  a.r = r;
+  a.N_rows = N_rows;
+  a.k = k;
+  a.m = m;
+  a.W = W;
+  a.rope_base = rope_base;
+  a.eps = eps;
+  a.scale = scale;
+  a.G = p.G;
+  a.n_rb = p.n_rb;
+  a.nsplit = p.nsplit;
+  a.keys_per_split = p.keys_per_split;
+  a.nds = p.nds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_attention(tm, a, p, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (p.nsplit > 1) {
+    CombineArgs c;
+    c.part_o = a.part_o;
+    c.part_lse = a.part_lse;
+    c.o = a.o;
+    c.lse = lse;
+    c.rows = rows;
+    c.nsplit = p.nsplit;
+    c.D = D;
+    e = launch_combine(c, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int hattn_csa_compress(const void* kv_raw, const void* ik_raw, const void* gate,
+                       const float* gamma_kv, int B, int64_t L_cap, int D, int dI, int m, int w,
+                       int r, float rope_base, float eps, int64_t j_begin, int64_t j_end,
+                       void* kv_c, void* ik_c, int64_t N_cap, hattn_stream_t stream) {
+  return compress_common(kv_raw, ik_raw, gate, gamma_kv, B, L_cap, D, dI, m, w, r, rope_base, eps,
+                         j_begin, j_end, kv_c, ik_c, N_cap, stream);
+}
+
+int hattn_hca_compress(const void* kv_raw, const void* gate, const float* gamma_kv, int B,
+                       int64_t L_cap, int D, int m, int r, float rope_base, float eps,
+                       int64_t j_begin, int64_t j_end, void* kv_h, int64_t N_cap,
+                       hattn_stream_t stream) {
+  return compress_common(kv_raw, nullptr, gate, gamma_kv, B, L_cap, D, 0, m, m, r, rope_base, eps,
+                         j_begin, j_end, kv_h, nullptr, N_cap, stream);
+}
+
+size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
+                                          int score_out_given) {
+  (void)k;
+  if (B < 1 || T < 1 || N_cap < 1 || score_out_given) return 0;
+  return (size_t)B * T * N_cap * sizeof(float);
+}
+
+int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
+                       int B, int T, int HI, int dI, int64_t N_cap, int k, int m,
+                       int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
+                       hattn_stream_t stream) {
+  REQUIRE_PTR(iq);
+  REQUIRE_PTR(w);
+  REQUIRE_PTR(ik_c);
+  REQUIRE_PTR(pos);
+  REQUIRE_PTR(idx_out);
+  if (score_out) REQUIRE_PTR(score_out);
+  REQUIRE(B >= 1 && T >= 1 && N_cap >= 1, "B, T and N_cap must be >= 1");
+  REQUIRE(HI >= 1 && HI <= 256, "HI=%d must be in [1, 256]", HI);
+  REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
+  REQUIRE(k >= 1 && k <= 2048, "k=%d must be in [1, 2048]", k);
+  REQUIRE(m >= 1, "m must be >= 1");
+  REQUIRE((int64_t)B * T * HI < (1ll << 31) && (int64_t)B * T < (1 << 16) * 32768ll,
+          "too many queries");
+  IndexerPlan ip;
+  if (!plan_indexer(T, HI, dI, &ip))
+    return fail(HATTN_ERR_UNSUPPORTED, "no indexer kernel for HI=%d dI=%d", HI, dI);
+  int sms = 0;
+  int* status = nullptr;
+  if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  TopkPlan tp;
+  if (!plan_topk(B * T, N_cap, sms, &tp))
+    return fail(HATTN_ERR_UNSUPPORTED, "top-k over N_cap=%lld entries is not supported",
+                (long long)N_cap);
+  float* scores = score_out;
+  if (!scores) {
+    const size_t need = hattn_indexer_topk_workspace_bytes(B, T, N_cap, k, 0);
+    REQUIRE_PTR(workspace);
+    REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
+    scores = static_cast<float*>(workspace);
+  }
+  CUtensorMap tm_ik, tm_iq;
+  {
+    const uint64_t dims[3] = {(uint64_t)dI, (uint64_t)N_cap, (uint64_t)B};
+    const uint64_t strides[2] = {(uint64_t)dI * 2, (uint64_t)N_cap * dI * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    int rc = make_tmap(&tm_ik, ik_c, 3, dims, strides, box, "ik_c");
+    if (rc) return rc;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)dI, (uint64_t)B * T * HI};
+    const uint64_t strides[1] = {(uint64_t)dI * 2};
+    const uint32_t box[2] = {64, (uint32_t)ip.NQ};
+    int rc = make_tmap(&tm_iq, iq, 2, dims, strides, box, "iq");
+    if (rc) return rc;
+  }
+  IndexerArgs a;
+  a.w = w;
+  a.pos = pos;
+  a.scores = scores;
+  a.status = status;
+  a.B = B;
+  a.T = T;
+  a.HI = HI;
+  a.dI = dI;
+  a.m = m;
+  a.G = ip.G;
+  a.NQ = ip.NQ;
+  a.KC = ip.KC;
+  a.stages = ip.stages;
+  a.groups_per_seq = (T + ip.G - 1) / ip.G;
+  a.nblk = static_cast<int>((N_cap + 127) / 128);
+  a.N_cap = N_cap;
+  a.total_slots = (int64_t)B * a.groups_per_seq * a.nblk;
+  const int grid = static_cast<int>(a.total_slots < sms ? a.total_slots : sms);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_indexer_score(tm_ik, tm_iq, a, ip, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
+  TopkArgs t;
+  t.scores = scores;
+  t.pos = pos;
+  t.idx = idx_out;
+  t.rows = B * T;
+  t.k = k;
+  t.m = m;
+  t.cluster = tp.cluster;
+  t.N_cap = N_cap;
+  t.slice = tp.slice;
+  e = launch_topk(t, tp, st);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  return ok();
+}
+
+size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys) {
+  AttnPlan p;
+  if (kind < 0 || kind > 2) return 0;
+  if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p)) return 0;
+  return p.ws_bytes;
+}
+
+int hattn_sparse_attn(const void* q, const float* gamma_q, const void* kv_c, const int32_t* idx,
+                      const int32_t* pos, int B, int T, int H, int D, int64_t N_cap, int k, int r,
+                      float rope_base, float eps, float scale, void* o, float* lse,
+                      void* workspace, size_t ws_bytes, hattn_stream_t stream) {
+  return attn_common(kSparse, q, gamma_q, kv_c, nullptr, idx, pos, B, T, H, D, N_cap, k, 1, 1, r,
+                     rope_base, eps, scale, o, lse, workspace, ws_bytes, stream);
+}
+
+int hattn_hca_attn(const void* q, const float* gamma_q, const void* kv_h, const int32_t* pos,
+                   int B, int T, int H, int D, int64_t N_cap, int m, int r, float rope_base,
+                   float eps, float scale, void* o, float* lse, void* workspace,
+                   size_t ws_bytes, hattn_stream_t stream) {
+  return attn_common(kHca, q, gamma_q, kv_h, nullptr, nullptr, pos, B, T, H, D, N_cap, 1, m, 1, r,
+                     rope_base, eps, scale, o, lse, workspace, ws_bytes, stream);
+}
+
+int hattn_swa_attn(const void* q, const float* gamma_q, const void* kv_raw,
+                   const float* gamma_kv, const int32_t* pos, int B, int T, int H, int D,
+                   int64_t L_cap, int W, int r, float rope_base, float eps, float scale, void* o,
+                   float* lse, void* workspace, size_t ws_bytes, hattn_stream_t stream) {
+  return attn_common(kSwa, q, gamma_q, kv_raw, gamma_kv, nullptr, pos, B, T, H, D, L_cap, 1, 1, W,
+                     r, rope_base, eps, scale, o, lse, workspace, ws_bytes, stream);
+}
+
+int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int nb,
+                    const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
+                    float rope_base, void* out, float* lse_out, hattn_stream_t stream) {
+  REQUIRE(o_list && lse_list, "o_list and lse_list must not be NULL");
+  REQUIRE(nb >= 1 && nb <= 4, "nb=%d must be in [1, 4]", nb);
+  MergeArgs a;
+  for (int i = 0; i < nb; ++i) {
+    if (!o_list[i] || !lse_list[i]) return fail(HATTN_ERR_INVALID_ARG, "branch %d is NULL", i);
+    if (!aligned16(o_list[i])) return fail(HATTN_ERR_MISALIGNED, "o_list[%d] is not 16-byte aligned", i);
+    if (!aligned4(lse_list[i])) return fail(HATTN_ERR_MISALIGNED, "lse_list[%d] is not 4-byte aligned", i);
+    a.o[i] = static_cast<const __nv_bfloat16*>(o_list[i]);
+    a.lse[i] = lse_list[i];
+  }
+  REQUIRE_PTR(pos);
+  REQUIRE_PTR(out);
+  REQUIRE_F32(sink);
+  REQUIRE_F32(lse_out);
+  REQUIRE(B >= 1 && T >= 1 && H >= 1, "B, T and H must be >= 1");
+  REQUIRE(D >= 8 && D <= 4096 && D % 8 == 0, "D=%d must be a multiple of 8 in [8, 4096]", D);
+  REQUIRE(r >= 0 && r % 2 == 0 && r <= D && r <= 512, "r=%d must be even, <= D and <= 512", r);
+  REQUIRE(rope_base > 0.f, "rope_base must be positive");
+  a.nb = nb;
+  a.sink = sink;
+  a.pos = pos;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse_out = lse_out;
+  a.B = B;
+  a.T = T;
+  a.H = H;
+  a.D = D;
+  a.r = r;
+  a.rope_base = rope_base;
+  cudaError_t e = launch_merge(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return ok();
+}
+
+const char* hattn_status_string(int code) {
+  switch (code) {
+    case HATTN_OK: return "ok";
+    case HATTN_ERR_INVALID_ARG: return "invalid argument";
+    case HATTN_ERR_MISALIGNED: return "misaligned pointer";
+    case HATTN_ERR_UNSUPPORTED: return "unsupported shape";
+    case HATTN_ERR_CUDA: return "CUDA error";
+    case HATTN_ERR_TIMEOUT: return "device wait timed out";
+    case HATTN_ERR_DEVICE_INDEX: return "device index out of range";
+    default: return "unknown status";
+  }
+}
+
+const char* hattn_last_error(void) { return g_last_error; }
+
+int hattn_check_status(hattn_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+  int* status = nullptr;
+  if (!device_info(nullptr, &status, nullptr)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  int v = 0;
+  e = cudaMemcpy(&v, status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  const int zero = 0;
+  e = cudaMemcpy(status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  if (v != 0) return fail(v, "device reported: %s", hattn_status_string(v));
+  return ok();
+}
+
+int hattn_selftest_wait_timeout(uint64_t timeout_ns, hattn_stream_t stream) {
+  int* status = nullptr;
+  if (!device_info(nullptr, &status, nullptr)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  cudaError_t e = launch_wait_selftest(timeout_ns, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+  return ok();
+}
+
+const char* hattn_version(void) { return "hattn 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+// compress.cu -- the KV compressor C(m, w) used by CSA (m=4, w=8, with the
+// indexer key) and HCA (m=w=128, KV only).
+//
+// "Why DeepSeek V4 Stands Apart", section "Core Architectural Innovations":
+// CSA compresses KV 4x (m=4), HCA 128:1.  "DeepSeek-V4" atlas, section
+// "Design overview": every 4 tokens are compressed into two overlapping
+// streams, and the compressed KV entries are RMSNorm'd.  Provenance 16: RoPE
+// on the last 64 dims.
+//
+// Entry j pools tokens u in [m(j+1)-w, m(j+1)-1] (u >= 0) with weights
+// softmax(gate_u); the pooled KV is RMSNorm'd and RoPE'd at position m(j+1)-1;
+// the pooled indexer key uses the same weights, no norm, no RoPE.
+//
+// One CTA processes one (sequence, entry) at a time in a grid-stride loop.
+// Threads are laid out as NC column pieces (16 bytes = 8 bf16 of the
+// concatenated [KV | indexer-key] row) x S token slices; every token row of
+// the window is read once, with 16-byte coalesced loads, and every output
+// row is written once.  Accumulation is fp32; the entry is rounded to bf16
+// once at the end.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace hattn {
+
+namespace {
+
+constexpr int kCompressThreads = 256;
+constexpr int kMaxW = 512;
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
+  uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&y)[8]) {
+  uint4 u;
+  u.x = pack_bf16x2(y[0], y[1]);
+  u.y = pack_bf16x2(y[2], y[3]);
+  u.z = pack_bf16x2(y[4], y[5]);
+  u.w = pack_bf16x2(y[6], y[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
+__global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs a) {
+  __shared__ float alpha[kMaxW];
+  __shared__ float partial[2048];  // S x (D + dI) floats, S*(NC) <= 256 -> <= 2048
+  __shared__ double theta[256];
+  __shared__ float red[kCompressThreads / 32];
+  __shared__ float inv_rms_s;
+
+  const int tid = threadIdx.x;
+  const int NCk = a.D / 8;                 // KV pieces
+  const int NCi = a.ik_raw ? a.dI / 8 : 0; // indexer-key pieces
+  const int NC = NCk + NCi;
+  const int S = kCompressThreads / NC;     // token slices
+  const int width = NC * 8;
+
+  for (int i = tid; i < a.r / 2; i += kCompressThreads)
+    theta[i] = pow(static_cast<double>(a.rope_base), -2.0 * i / static_cast<double>(a.r));
+
+  const int64_t nj = a.j_end - a.j_begin;
+  const int64_t items = nj * a.B;
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = static_cast<int>(item / nj);
+    const int64_t j = a.j_begin + item % nj;
+    const int64_t u0 = static_cast<int64_t>(a.m) * (j + 1) - a.w;
+
+    // gate softmax over the tokens that exist (warp 0)
+    if (tid < 32) {
+      float gmax = -INFINITY;
+      for (int s = tid; s < a.w; s += 32) {
+        int64_t u = u0 + s;
+        if (u >= 0) gmax = fmaxf(gmax, __bfloat162float(a.gate[(int64_t)b * a.L_cap + u]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+      float z = 0.f;
+      for (int s = tid; s < a.w; s += 32) {
+        int64_t u = u0 + s;
+        float e = 0.f;
+        if (u >= 0) e = __expf(__bfloat162float(a.gate[(int64_t)b * a.L_cap + u]) - gmax);
+        alpha[s] = e;
+        z += e;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      const float iz = 1.f / z;
+      __syncwarp();
+      for (int s = tid; s < a.w; s += 32) alpha[s] *= iz;
+    }
+    __syncthreads();
+
+    // weighted sums: thread (c, s) covers piece c over tokens s, s+S, ...
+    if (tid < S * NC) {
+      const int c = tid % NC;
+      const int s = tid / NC;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int i = s; i < a.w; i += S) {
+        const int64_t u = u0 + i;
+        if (u < 0) continue;
+        const float al = alpha[i];
+        float x[8];
+        if (c < NCk)
+          load8(a.kv_raw + ((int64_t)b * a.L_cap + u) * a.D + c * 8, x);
+        else
+          load8(a.ik_raw + ((int64_t)b * a.L_cap + u) * a.dI + (c - NCk) * 8, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(al, x[e], acc[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) partial[s * width + c * 8 + e] = acc[e];
+    }
+    __syncthreads();
+
+    // reduce the slices (fixed order), RMS over the KV part
+    float v[8];
+    float ss = 0.f;
+    if (tid < NC) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = 0.f;
+      for (int s = 0; s < S; ++s)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] += partial[s * width + tid * 8 + e];
+      if (tid < NCk)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int i = 0; i < kCompressThreads / 32; ++i) t += red[i];
+      inv_rms_s = rsqrtf(t / static_cast<float>(a.D) + a.eps);
+    }
+    __syncthreads();
+
+    if (tid < NCk) {
+      const float inv = inv_rms_s;
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float g = a.gamma ? a.gamma[tid * 8 + e] : 1.f;
+        y[e] = v[e] * inv * g;
+      }
+      const int d0 = a.D - a.r;
+      const int64_t p = static_cast<int64_t>(a.m) * (j + 1) - 1;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const int d = tid * 8 + e;
+        if (d >= d0) {
+          float sn, cs;
+          rope_sincos(theta[(d - d0) / 2], p, &sn, &cs);
+          const float x0 = y[e], x1 = y[e + 1];
+          y[e] = x0 * cs - x1 * sn;
+          y[e + 1] = x0 * sn + x1 * cs;
+        }
+      }
+      store8(a.kv_out + ((int64_t)b * a.N_cap + j) * a.D + tid * 8, y);
+    } else if (tid < NC) {
+      store8(a.ik_out + ((int64_t)b * a.N_cap + j) * a.dI + (tid - NCk) * 8, v);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const CompressArgs& a, int num_sms, cudaStream_t stream) {
+  const int64_t items = (a.j_end - a.j_begin) * a.B;
+  if (items <= 0) return cudaSuccess;
+  const int64_t grid = items < (int64_t)num_sms * 8 ? items : (int64_t)num_sms * 8;
+  compress_kernel<<<static_cast<unsigned>(grid), kCompressThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace hattn

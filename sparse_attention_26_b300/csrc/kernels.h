@@ -1,0 +1,127 @@
+// kernels.h -- internal launch interface between the C ABI layer (abi.cu)
+// and the kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hattn {
+
+// ------------------------------------------------------------ compressor
+struct CompressArgs {
+  const __nv_bfloat16* kv_raw;  // [B][L_cap][D]
+  const __nv_bfloat16* ik_raw;  // [B][L_cap][dI] or null (no indexer key)
+  const __nv_bfloat16* gate;    // [B][L_cap]
+  const float* gamma;           // [D] or null
+  __nv_bfloat16* kv_out;        // [B][N_cap][D]
+  __nv_bfloat16* ik_out;        // [B][N_cap][dI] or null
+  int B, D, dI, m, w, r;
+  int64_t L_cap, N_cap, j_begin, j_end;
+  float rope_base, eps;
+};
+cudaError_t launch_compress(const CompressArgs& a, int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------------------ indexer score
+struct IndexerArgs {
+  const float* w;        // [B][T][HI]
+  const int32_t* pos;    // [B][T]
+  float* scores;         // [B][T][N_cap]
+  int* status;
+  int B, T, HI, dI, m;
+  int G;                 // queries per group (B operand rows = G*HI, padded to NQ)
+  int NQ;                // MMA N
+  int KC;                // 64-wide K chunks
+  int stages;
+  int groups_per_seq;    // ceil(T / G)
+  int nblk;              // ceil(N_cap / 128)
+  int64_t N_cap;
+  int64_t total_slots;   // B * groups_per_seq * nblk
+};
+struct IndexerPlan {
+  int G, NQ, KC, stages, tmem_cols;
+  size_t smem_bytes;
+};
+bool plan_indexer(int T, int HI, int dI, IndexerPlan* p);
+cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm_iq,
+                                 const IndexerArgs& a, const IndexerPlan& p, int grid,
+                                 cudaStream_t stream);
+
+// ------------------------------------------------------------ top-k select
+struct TopkArgs {
+  const float* scores;   // [rows][N_cap]
+  const int32_t* pos;    // [rows]
+  int32_t* idx;          // [rows][k]
+  int rows, k, m, cluster;
+  int64_t N_cap;
+  int slice;             // entries per CTA of a cluster
+};
+struct TopkPlan {
+  int cluster, slice, threads;
+  size_t smem_bytes;
+};
+bool plan_topk(int rows, int64_t N_cap, int num_sms, TopkPlan* p);
+cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, cudaStream_t stream);
+
+// ------------------------------------------------------------ attention
+enum AttnKind { kSparse = 0, kHca = 1, kSwa = 2 };
+
+struct AttnArgs {
+  const __nv_bfloat16* q;       // [B][T][H][D]
+  const float* gamma_q;         // [D] or null
+  const __nv_bfloat16* kv;      // cache [B][N_cap][D] (sparse/HCA) or raw [B][L_cap][D] (SWA)
+  const float* gamma_kv;        // SWA only
+  const int32_t* idx;           // sparse only [B][T][k]
+  const int32_t* pos;           // [B][T]
+  __nv_bfloat16* o;             // [B][T][H][D] (direct output when nsplit == 1)
+  float* lse;                   // [B][T][H]
+  float* part_o;                // [B*T*H][nsplit][D] partials (nsplit > 1)
+  float* part_lse;              // [B*T*H][nsplit]
+  int* status;
+  int kind, B, T, H, D, r;
+  int64_t N_rows;               // rows per sequence of kv (N_cap or L_cap)
+  int k, m, W;
+  float rope_base, eps, scale;
+  int G;                        // queries per row block
+  int n_rb;                     // row blocks per sequence = ceil(T / G)
+  int nsplit;                   // key splits
+  int keys_per_split;           // multiple of 64
+  int nds;                      // D splits (1 or 2)
+};
+struct AttnPlan {
+  int G, n_rb, nsplit, keys_per_split, nds, nslot;
+  size_t smem_bytes, ws_bytes;
+};
+bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int num_sms,
+                    AttnPlan* p);
+cudaError_t launch_attention(const CUtensorMap& tm_kv, const AttnArgs& a, const AttnPlan& p,
+                             cudaStream_t stream);
+
+// ------------------------------------------------------------ merges
+struct CombineArgs {
+  const float* part_o;
+  const float* part_lse;
+  __nv_bfloat16* o;
+  float* lse;
+  int64_t rows;   // B*T*H
+  int nsplit, D;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+struct MergeArgs {
+  const __nv_bfloat16* o[4];
+  const float* lse[4];
+  int nb;
+  const float* sink;    // [H] or null
+  const int32_t* pos;   // [B][T]
+  __nv_bfloat16* out;
+  float* lse_out;       // or null
+  int B, T, H, D, r;
+  float rope_base;
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, int* status, cudaStream_t stream);
+
+}  // namespace hattn

@@ -1,0 +1,272 @@
+// topk.cu -- exact per-query top-k over the indexer scores.
+//
+// "Why DeepSeek V4 Stands Apart", section "Core Architectural Innovations":
+// CSA keeps the top-1024 (Pro) / top-512 (Flash) compressed entries per
+// query.  Selection rule: the min(k, n) largest scores among the n visible
+// entries, ties to the smaller entry index; the output order is unspecified.
+//
+// One thread-block cluster of C CTAs handles one query row: CTA `rank` holds
+// entries [rank*slice, (rank+1)*slice) as order-preserving uint32 keys in
+// shared memory (one read of the fp32 scores).  Three radix passes (11, 11,
+// 10 bits, most significant first) find the k-th largest key: every CTA
+// builds a shared-memory histogram of the digit among the keys that still
+// match the prefix, the histograms are summed across the cluster through
+// distributed shared memory, and every CTA scans the sum to pick the digit.
+// The final pass writes every key above the threshold, then the threshold
+// ties in global index order until k are written.  No global atomics, no
+// inter-kernel passes; the result is deterministic.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace hattn {
+
+namespace {
+
+constexpr int kBins = 2048;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);  // -0 and +0 compare equal
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct TopkShared {
+  uint32_t hist[kBins];
+  uint32_t ghist[kBins];
+  uint32_t warp_tot[32];
+  int counts[2];       // keys above the threshold, keys equal to it (this CTA)
+  int ctr;
+  uint32_t digit;
+  uint32_t above;
+};
+
+__global__ void topk_kernel(const TopkArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  TopkShared* sh = reinterpret_cast<TopkShared*>(smem_raw);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkShared));
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = a.cluster;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int row = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+
+  const int32_t t = a.pos[row];
+  int64_t n = t < 0 ? 0 : (static_cast<int64_t>(t) + 1) / a.m;
+  if (n > a.N_cap) n = a.N_cap;
+  const int64_t start = static_cast<int64_t>(rank) * a.slice;
+  int len = 0;
+  if (n > start) len = static_cast<int>((n - start) < a.slice ? (n - start) : a.slice);
+  int32_t* out = a.idx + static_cast<int64_t>(row) * a.k;
+
+  if (n <= a.k) {  // every visible entry is selected (same branch for the whole cluster)
+    for (int e = tid; e < len; e += nthr) out[start + e] = static_cast<int32_t>(start + e);
+    if (rank == 0)
+      for (int64_t p = n + tid; p < a.k; p += nthr) out[p] = -1;
+    return;
+  }
+
+  const float* src = a.scores + static_cast<int64_t>(row) * a.N_cap + start;
+  for (int e = tid; e < len; e += nthr) keys[e] = order_key(src[e]);
+
+  uint32_t prefix = 0;
+  uint32_t need = static_cast<uint32_t>(a.k);
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = shifts[pass];
+    const int nb = 1 << widths[pass];
+    for (int i = tid; i < nb; i += nthr) sh->hist[i] = 0;
+    __syncthreads();
+    for (int e = tid; e < len; e += nthr) {
+      const uint32_t key = keys[e];
+      if (pass == 0 || (key >> (shift + widths[pass])) == prefix)
+        atomicAdd(&sh->hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    cluster.sync();
+    // this CTA sums its share of the bins over the cluster and broadcasts it
+    const int per = nb / C;
+    for (int i = tid; i < per; i += nthr) {
+      const int bin = rank * per + i;
+      uint32_t s = 0;
+      for (int q = 0; q < C; ++q) s += cluster.map_shared_rank(sh->hist, q)[bin];
+      for (int q = 0; q < C; ++q) cluster.map_shared_rank(sh->ghist, q)[bin] = s;
+    }
+    cluster.sync();
+    if (tid < 32) {
+      // lane L covers the bins [nb - (L+1)*pl, nb - L*pl), scanned from the top
+      const int pl = nb / 32;
+      uint32_t tot = 0;
+      for (int i = 0; i < pl; ++i) tot += sh->ghist[nb - tid * pl - 1 - i];
+      uint32_t inc = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (tid >= o) inc += v;
+      }
+      const unsigned ball = __ballot_sync(0xffffffffu, inc >= need);
+      const int L = __ffs(ball) - 1;
+      if (tid == L) {
+        uint32_t run = inc - tot;
+        for (int i = 0; i < pl; ++i) {
+          const int bin = nb - tid * pl - 1 - i;
+          const uint32_t c = sh->ghist[bin];
+          if (run + c >= need) {
+            sh->digit = static_cast<uint32_t>(bin);
+            sh->above = run;
+            break;
+          }
+          run += c;
+        }
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << widths[pass]) | sh->digit;
+    need -= sh->above;
+  }
+  const uint32_t thr = prefix;  // the k-th largest key; take `need` of its ties
+
+  if (tid == 0) {
+    sh->counts[0] = 0;
+    sh->counts[1] = 0;
+    sh->ctr = 0;
+  }
+  __syncthreads();
+  int gt = 0, eq = 0;
+  for (int e = tid; e < len; e += nthr) {
+    gt += keys[e] > thr;
+    eq += keys[e] == thr;
+  }
+  if (gt) atomicAdd(&sh->counts[0], gt);
+  if (eq) atomicAdd(&sh->counts[1], eq);
+  cluster.sync();
+  int off_gt = 0, off_eq = 0;
+  for (int q = 0; q < rank; ++q) {
+    const int* rc = cluster.map_shared_rank(sh->counts, q);
+    off_gt += rc[0];
+    off_eq += rc[1];
+  }
+  // keys above the threshold: any order
+  for (int e = tid; e < len; e += nthr) {
+    if (keys[e] > thr) {
+      const int p = atomicAdd(&sh->ctr, 1);
+      out[off_gt + p] = static_cast<int32_t>(start + e);
+    }
+  }
+  // threshold ties in index order: each thread owns a contiguous run
+  const int per_t = (len + nthr - 1) / nthr;
+  const int e0 = tid * per_t;
+  const int e1 = min(len, e0 + per_t);
+  uint32_t c = 0;
+  for (int e = e0; e < e1; ++e) c += keys[e] == thr;
+  uint32_t inc = c;
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) sh->warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nthr >> 5;
+    uint32_t v = lane < nw ? sh->warp_tot[lane] : 0;
+    uint32_t s = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += x;
+    }
+    if (lane < nw) sh->warp_tot[lane] = s - v;  // exclusive
+  }
+  __syncthreads();
+  uint32_t rnk = static_cast<uint32_t>(off_eq) + sh->warp_tot[warp] + (inc - c);
+  const int base = a.k - static_cast<int>(need);
+  for (int e = e0; e < e1 && rnk < need; ++e) {
+    if (keys[e] == thr) {
+      out[base + rnk] = static_cast<int32_t>(start + e);
+      ++rnk;
+    }
+  }
+  cluster.sync();  // keep this CTA's shared memory alive for the others' reads
+}
+
+}  // namespace
+
+bool plan_topk(int rows, int64_t N_cap, int num_sms, TopkPlan* p) {
+  if (rows <= 0 || N_cap < 0) return false;
+  const int64_t max_slice = 49152;  // keys per CTA held in shared memory
+  int C = 1;
+  // spread small batches over more SMs, keep slices large enough to be worth it
+  while (C < 16 && (int64_t)rows * C < num_sms && (N_cap + 2 * C - 1) / (2 * C) >= 2048) C *= 2;
+  while (C < 16 && (N_cap + C - 1) / C > max_slice) C *= 2;
+  if ((N_cap + C - 1) / C > max_slice) return false;
+  if (C > 8) {
+    // 16-CTA clusters are non-portable; fall back to 8 when they cannot be scheduled
+    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  }
+  int slice = static_cast<int>((N_cap + C - 1) / C);
+  if (slice < 1) slice = 1;
+  p->cluster = C;
+  p->slice = slice;
+  p->threads = slice >= 8192 ? 1024 : (slice >= 2048 ? 512 : 256);
+  p->smem_bytes = sizeof(TopkShared) + static_cast<size_t>(slice) * 4;
+  if (C > 8) {
+    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(p->smem_bytes));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, 1, 1);
+    cfg.blockDim = dim3(p->threads, 1, 1);
+    cfg.dynamicSmemBytes = p->smem_bytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, topk_kernel, &cfg) != cudaSuccess ||
+        nclusters < 1) {
+      cudaGetLastError();
+      C = 8;
+      slice = static_cast<int>((N_cap + C - 1) / C);
+      if (slice > max_slice) return false;
+      p->cluster = C;
+      p->slice = slice;
+      p->threads = slice >= 8192 ? 1024 : (slice >= 2048 ? 512 : 256);
+      p->smem_bytes = sizeof(TopkShared) + static_cast<size_t>(slice) * 4;
+    }
+  }
+  return true;
+}
+
+cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(p.smem_bytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.cluster, a.rows, 1);
+  cfg.blockDim = dim3(p.threads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = p.cluster;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  TopkArgs args = a;
+  args.cluster = p.cluster;
+  args.slice = p.slice;
+  e = cudaLaunchKernelEx(&cfg, topk_kernel, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace hattn

@@ -1,0 +1,310 @@
+"""Thin ctypes binding of libhattn (include/hattn.h).
+
+Each function takes torch CUDA tensors, checks dtype / contiguity / device,
+allocates any output or workspace the caller did not pass (torch is the
+device-memory allocator), and calls the C entry point of the same name on the
+current torch stream.  All compute runs in libhattn's kernels; there is no
+CPU or PyTorch fallback: if the library is missing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhattn.so")
+
+OK, INVALID_ARG, MISALIGNED, UNSUPPORTED, CUDA_ERROR, TIMEOUT, DEVICE_INDEX = range(7)
+KIND_SPARSE, KIND_HCA, KIND_SWA = 0, 1, 2
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/hattn.h
+_SIGS = {
+    "hattn_csa_compress": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32, _i32,
+                                  _f32, _f32, _i64, _i64, _vp, _vp, _i64, _vp]),
+    "hattn_hca_compress": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _f32, _f32, _i64,
+                                  _i64, _vp, _i64, _vp]),
+    "hattn_indexer_topk": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
+                                  _vp, _vp, _vp, _sz, _vp]),
+    "hattn_indexer_topk_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32, _i32]),
+    "hattn_sparse_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
+                                 _i32, _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "hattn_hca_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _f32,
+                              _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "hattn_swa_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
+                              _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "hattn_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64]),
+    "hattn_lse_merge": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _vp, _vp, _i32,
+                               _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp]),
+    "hattn_status_string": (ctypes.c_char_p, [_i32]),
+    "hattn_last_error": (ctypes.c_char_p, []),
+    "hattn_check_status": (_i32, [_vp]),
+    "hattn_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
+    "hattn_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+class HattnError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"libhattn error {code}: {msg}")
+        self.code = code
+
+
+def lib():
+    """Load libhattn.so (built in-tree); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m sparse_attention_26_b300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc):
+    if rc != OK:
+        raise HattnError(rc, lib().hattn_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, ndim=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def _opt(t, name, dtype):
+    return None if t is None else _need(t, name, dtype)
+
+
+# ------------------------------------------------------------------ compression
+def csa_compress(kv_raw, ik_raw, gate, *, r, j_begin=0, j_end=None, m=4, w=8, kv_c=None,
+                 ik_c=None, N_cap=None, gamma_kv=None, rope_base=10000.0, eps=1e-6, stream=None):
+    """C(m, w) of KV + indexer keys for entries [j_begin, j_end); returns (kv_c, ik_c)."""
+    _need(kv_raw, "kv_raw", torch.bfloat16, 3)
+    _need(gate, "gate", torch.bfloat16, 2)
+    if ik_raw is not None:
+        _need(ik_raw, "ik_raw", torch.bfloat16, 3)
+    B, L, D = kv_raw.shape
+    dI = ik_raw.shape[2] if ik_raw is not None else 0
+    if N_cap is None:
+        N_cap = kv_c.shape[1] if kv_c is not None else L // m
+    if j_end is None:
+        j_end = min(N_cap, L // m)
+    if kv_c is None:
+        kv_c = torch.zeros((B, N_cap, D), dtype=torch.bfloat16, device=kv_raw.device)
+    if ik_c is None and ik_raw is not None:
+        ik_c = torch.zeros((B, N_cap, dI), dtype=torch.bfloat16, device=kv_raw.device)
+    _need(kv_c, "kv_c", torch.bfloat16, 3)
+    _opt(ik_c, "ik_c", torch.bfloat16)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    _check(lib().hattn_csa_compress(_ptr(kv_raw), _ptr(ik_raw), _ptr(gate), _ptr(gamma_kv), B, L,
+                                    D, dI, m, w, r, rope_base, eps, j_begin, j_end, _ptr(kv_c),
+                                    _ptr(ik_c), N_cap, _stream(stream)))
+    return kv_c, ik_c
+
+
+def hca_compress(kv_raw, gate, *, r, j_begin=0, j_end=None, m=128, kv_h=None, N_cap=None,
+                 gamma_kv=None, rope_base=10000.0, eps=1e-6, stream=None):
+    """C(m, m) of KV for entries [j_begin, j_end); returns kv_h."""
+    _need(kv_raw, "kv_raw", torch.bfloat16, 3)
+    _need(gate, "gate", torch.bfloat16, 2)
+    B, L, D = kv_raw.shape
+    if N_cap is None:
+        N_cap = kv_h.shape[1] if kv_h is not None else max(1, L // m)
+    if j_end is None:
+        j_end = min(N_cap, L // m)
+    if kv_h is None:
+        kv_h = torch.zeros((B, N_cap, D), dtype=torch.bfloat16, device=kv_raw.device)
+    _need(kv_h, "kv_h", torch.bfloat16, 3)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    _check(lib().hattn_hca_compress(_ptr(kv_raw), _ptr(gate), _ptr(gamma_kv), B, L, D, m, r,
+                                    rope_base, eps, j_begin, j_end, _ptr(kv_h), N_cap,
+                                    _stream(stream)))
+    return kv_h
+
+
+# ------------------------------------------------------------------ indexer
+def indexer_topk_workspace_bytes(B, T, N_cap, k, score_out_given=False):
+    return int(lib().hattn_indexer_topk_workspace_bytes(B, T, N_cap, k, int(bool(score_out_given))))
+
+
+def indexer_topk(iq, w, ik_c, pos, *, k, m=4, idx_out=None, score_out=None, workspace=None,
+                 stream=None):
+    """Lightning-indexer scores + per-query top-k; returns idx [B, T, k] int32."""
+    _need(iq, "iq", torch.bfloat16, 4)
+    _need(w, "w", torch.float32, 3)
+    _need(ik_c, "ik_c", torch.bfloat16, 3)
+    _need(pos, "pos", torch.int32, 2)
+    B, T, HI, dI = iq.shape
+    N_cap = ik_c.shape[1]
+    if idx_out is None:
+        idx_out = torch.empty((B, T, k), dtype=torch.int32, device=iq.device)
+    _need(idx_out, "idx_out", torch.int32)
+    _opt(score_out, "score_out", torch.float32)
+    need = indexer_topk_workspace_bytes(B, T, N_cap, k, score_out is not None)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=iq.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().hattn_indexer_topk(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI, N_cap,
+                                    k, m, _ptr(idx_out), _ptr(score_out), _ptr(workspace),
+                                    ws_bytes, _stream(stream)))
+    return idx_out
+
+
+# ------------------------------------------------------------------ attention
+def attn_workspace_bytes(kind, B, T, H, D, n_keys):
+    return int(lib().hattn_attn_workspace_bytes(kind, B, T, H, D, n_keys))
+
+
+def _attn_out(q, o, lse):
+    B, T, H, D = q.shape
+    if o is None:
+        o = torch.empty((B, T, H, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+    _need(o, "o", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    return o, lse
+
+
+def _ws(kind, q, n_keys, workspace):
+    B, T, H, D = q.shape
+    need = attn_workspace_bytes(kind, B, T, H, D, n_keys)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    return workspace, (workspace.numel() * workspace.element_size() if workspace is not None
+                       else 0)
+
+
+def sparse_attn(q, kv_c, idx, pos, *, r, gamma_q=None, rope_base=10000.0, eps=1e-6, scale=None,
+                o=None, lse=None, workspace=None, stream=None):
+    """CSA branch over the selected entries; returns (o bf16, lse fp32)."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv_c, "kv_c", torch.bfloat16, 3)
+    _need(idx, "idx", torch.int32, 3)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(gamma_q, "gamma_q", torch.float32)
+    B, T, H, D = q.shape
+    k = idx.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    o, lse = _attn_out(q, o, lse)
+    workspace, wsb = _ws(KIND_SPARSE, q, k, workspace)
+    _check(lib().hattn_sparse_attn(_ptr(q), _ptr(gamma_q), _ptr(kv_c), _ptr(idx), _ptr(pos), B, T,
+                                   H, D, kv_c.shape[1], k, r, rope_base, eps, scale, _ptr(o),
+                                   _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
+    return o, lse
+
+
+def hca_attn(q, kv_h, pos, *, r, m=128, gamma_q=None, rope_base=10000.0, eps=1e-6, scale=None,
+             o=None, lse=None, workspace=None, stream=None):
+    """HCA branch, dense over the visible compressed entries; returns (o, lse)."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv_h, "kv_h", torch.bfloat16, 3)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(gamma_q, "gamma_q", torch.float32)
+    B, T, H, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    o, lse = _attn_out(q, o, lse)
+    workspace, wsb = _ws(KIND_HCA, q, kv_h.shape[1], workspace)
+    _check(lib().hattn_hca_attn(_ptr(q), _ptr(gamma_q), _ptr(kv_h), _ptr(pos), B, T, H, D,
+                                kv_h.shape[1], m, r, rope_base, eps, scale, _ptr(o), _ptr(lse),
+                                _ptr(workspace), wsb, _stream(stream)))
+    return o, lse
+
+
+def swa_attn(q, kv_raw, pos, *, r, W=128, gamma_q=None, gamma_kv=None, rope_base=10000.0,
+             eps=1e-6, scale=None, o=None, lse=None, workspace=None, stream=None):
+    """SWA branch over the last W raw tokens (normalised and roped on load)."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv_raw, "kv_raw", torch.bfloat16, 3)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(gamma_q, "gamma_q", torch.float32)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    B, T, H, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    o, lse = _attn_out(q, o, lse)
+    workspace, wsb = _ws(KIND_SWA, q, W, workspace)
+    _check(lib().hattn_swa_attn(_ptr(q), _ptr(gamma_q), _ptr(kv_raw), _ptr(gamma_kv), _ptr(pos),
+                                B, T, H, D, kv_raw.shape[1], W, r, rope_base, eps, scale, _ptr(o),
+                                _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
+    return o, lse
+
+
+# ------------------------------------------------------------------ merge
+def lse_merge(o_list, lse_list, pos, *, r, sink=None, rope_base=10000.0, out=None, lse_out=None,
+              stream=None):
+    """Sink-augmented LSE merge of 1..4 branches + inverse RoPE; returns (out, lse)."""
+    nb = len(o_list)
+    if nb < 1 or nb != len(lse_list):
+        raise ValueError("need 1..4 branches with matching lse tensors")
+    for i, (o, l) in enumerate(zip(o_list, lse_list)):
+        _need(o, f"o_list[{i}]", torch.bfloat16, 4)
+        _need(l, f"lse_list[{i}]", torch.float32, 3)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(sink, "sink", torch.float32)
+    B, T, H, D = o_list[0].shape
+    if out is None:
+        out = torch.empty((B, T, H, D), dtype=torch.bfloat16, device=o_list[0].device)
+    if lse_out is None:
+        lse_out = torch.empty((B, T, H), dtype=torch.float32, device=o_list[0].device)
+    _need(out, "out", torch.bfloat16)
+    _need(lse_out, "lse_out", torch.float32)
+    op = (_vp * nb)(*[o.data_ptr() for o in o_list])
+    lp = (_vp * nb)(*[l.data_ptr() for l in lse_list])
+    _check(lib().hattn_lse_merge(op, lp, nb, _ptr(sink), _ptr(pos), B, T, H, D, r, rope_base,
+                                 _ptr(out), _ptr(lse_out), _stream(stream)))
+    return out, lse_out
+
+
+# ------------------------------------------------------------------ status
+def check_status(stream=None):
+    """Synchronise and raise if a kernel reported a device-side error."""
+    _check(lib().hattn_check_status(_stream(stream)))
+
+
+def check_status_code(stream=None):
+    return int(lib().hattn_check_status(_stream(stream)))
+
+
+def selftest_wait_timeout(timeout_ns, stream=None):
+    _check(lib().hattn_selftest_wait_timeout(int(timeout_ns), _stream(stream)))
+
+
+def status_string(code):
+    return lib().hattn_status_string(code).decode()
+
+
+def version():
+    return lib().hattn_version().decode()

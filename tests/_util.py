@@ -1,0 +1,66 @@
+"""Comparison helpers shared by the GPU parity tests (no method arithmetic)."""
+import numpy as np
+import torch
+
+# Tolerances of the layer specification (bf16 in, fp32 accumulate).
+ATTN_MAX_ABS = 1e-2
+ATTN_REL_L2 = 5e-3
+KV_REL_L2 = 2e-3
+TOPK_REL = 1e-3
+
+
+def f64(x):
+    if isinstance(x, torch.Tensor):
+        return x.detach().to(torch.float64).cpu().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def rel_l2(got, ref):
+    got, ref = f64(got), f64(ref)
+    den = np.linalg.norm(ref.ravel())
+    return float(np.linalg.norm((got - ref).ravel()) / (den if den > 0 else 1.0))
+
+
+def check_attn(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    o_gpu, o_ref = f64(o_gpu), f64(o_ref)
+    assert np.isfinite(o_gpu).all(), f"{what}: non-finite output"
+    err = np.abs(o_gpu - o_ref).max() if o_ref.size else 0.0
+    rl = rel_l2(o_gpu, o_ref)
+    assert err <= ATTN_MAX_ABS, f"{what}: max-abs {err:.3e} > {ATTN_MAX_ABS}"
+    assert rl <= ATTN_REL_L2, f"{what}: rel-L2 {rl:.3e} > {ATTN_REL_L2}"
+    if lse_gpu is not None:
+        lg, lr = f64(lse_gpu), f64(lse_ref)
+        fin = np.isfinite(lr)
+        assert (np.isfinite(lg) == fin).all(), f"{what}: lse finiteness differs"
+        if fin.any():
+            d = np.abs(lg[fin] - lr[fin]).max()
+            assert d <= 1e-2, f"{what}: lse max-abs {d:.3e}"
+    return err, rl
+
+
+def check_topk(idx_gpu, scores_ref, pos, m, k, what=""):
+    """Sets equal except entries whose oracle score is within 1e-3 relative of
+    the k-th score; every selected entry is visible and distinct."""
+    idx_gpu = np.asarray(idx_gpu).reshape(-1, k)
+    sc = np.asarray(scores_ref).reshape(idx_gpu.shape[0], -1)
+    pos = np.asarray(pos).reshape(-1)
+    N = sc.shape[1]
+    for r in range(idx_gpu.shape[0]):
+        n = min((int(pos[r]) + 1) // m, N) if pos[r] >= 0 else 0
+        keff = min(k, n)
+        row = idx_gpu[r]
+        sel = row[row >= 0]
+        assert len(sel) == keff, f"{what} row {r}: {len(sel)} selected, expected {keff}"
+        assert (row[keff:] == -1).all(), f"{what} row {r}: padding not at the end"
+        assert len(set(sel.tolist())) == keff, f"{what} row {r}: duplicate indices"
+        assert (sel < n).all(), f"{what} row {r}: invisible entry selected"
+        if keff == 0:
+            continue
+        s = sc[r, :n]
+        order = np.lexsort((np.arange(n), -s))
+        ref = set(order[:keff].tolist())
+        kth = s[order[keff - 1]]
+        tol = TOPK_REL * abs(kth)
+        for j in ref.symmetric_difference(set(sel.tolist())):
+            assert abs(s[j] - kth) <= tol, (
+                f"{what} row {r}: entry {j} (score {s[j]:.6g}) differs, k-th {kth:.6g}")

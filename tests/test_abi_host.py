@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI: the library loads on a machine without a
+GPU, exports every entry point of include/hattn.h, and rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_26_b300 import hattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hattn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sparse_attention_26_b300 import build
+    build.build()
+    return hattn.lib()
+
+
+def header_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"HATTN_API\s+[\w\s\*]+?\b(hattn_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_seven_calls():
+    syms = header_symbols()
+    for name in ["csa_compress", "hca_compress", "indexer_topk", "sparse_attn", "hca_attn",
+                 "swa_attn", "lse_merge"]:
+        assert f"hattn_{name}" in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    syms = header_symbols()
+    assert len(syms) >= 14
+    for s in syms:
+        assert hasattr(L, s), f"{s} declared in hattn.h but not exported"
+        assert s in hattn._SIGS, f"{s} has no binding signature"
+
+
+def test_status_strings(L):
+    assert hattn.status_string(0) == "ok"
+    assert "misaligned" in hattn.status_string(2)
+    assert "timed out" in hattn.status_string(5)
+    assert hattn.version().startswith("hattn")
+
+
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: validation fails first
+MISAL = ctypes.c_void_p(0x10008)
+
+
+def _err(L):
+    return L.hattn_last_error().decode()
+
+
+def test_compress_validation(L):
+    N = None
+    s = None
+    rc = L.hattn_csa_compress(N, FAKE, FAKE, N, 1, 64, 64, 32, 4, 8, 16, 1e4, 1e-6, 0, 4, FAKE,
+                              FAKE, 16, s)
+    assert rc == hattn.INVALID_ARG and "kv_raw" in _err(L)
+    rc = L.hattn_csa_compress(MISAL, FAKE, FAKE, N, 1, 64, 64, 32, 4, 8, 16, 1e4, 1e-6, 0, 4,
+                              FAKE, FAKE, 16, s)
+    assert rc == hattn.MISALIGNED
+    # w % m != 0
+    rc = L.hattn_csa_compress(FAKE, FAKE, FAKE, N, 1, 64, 64, 32, 4, 6, 16, 1e4, 1e-6, 0, 4, FAKE,
+                              FAKE, 16, s)
+    assert rc == hattn.INVALID_ARG
+    # D not a multiple of 64
+    rc = L.hattn_csa_compress(FAKE, FAKE, FAKE, N, 1, 64, 96, 32, 4, 8, 16, 1e4, 1e-6, 0, 4, FAKE,
+                              FAKE, 16, s)
+    assert rc == hattn.INVALID_ARG and "D=96" in _err(L)
+    # entries need tokens beyond L_cap
+    rc = L.hattn_csa_compress(FAKE, FAKE, FAKE, N, 1, 15, 64, 32, 4, 8, 16, 1e4, 1e-6, 0, 4, FAKE,
+                              FAKE, 16, s)
+    assert rc == hattn.INVALID_ARG and "L_cap" in _err(L)
+    # odd RoPE width
+    rc = L.hattn_hca_compress(FAKE, FAKE, N, 1, 256, 64, 128, 15, 1e4, 1e-6, 0, 2, FAKE, 2, s)
+    assert rc == hattn.INVALID_ARG
+    # empty range is a no-op that succeeds without a device
+    rc = L.hattn_hca_compress(FAKE, FAKE, N, 1, 256, 64, 128, 16, 1e4, 1e-6, 1, 1, FAKE, 2, s)
+    assert rc == hattn.OK
+
+
+def test_indexer_validation(L):
+    N = None
+    rc = L.hattn_indexer_topk(FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 128, 100, 0, 4, FAKE, N, N, 0, N)
+    assert rc == hattn.INVALID_ARG and "k=0" in _err(L)
+    rc = L.hattn_indexer_topk(FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 120 + 3, 100, 16, 4, FAKE, N, N,
+                              0, N)
+    assert rc == hattn.INVALID_ARG
+    rc = L.hattn_indexer_topk(FAKE, FAKE, FAKE, N, 1, 1, 64, 128, 100, 16, 4, FAKE, N, N, 0, N)
+    assert rc == hattn.INVALID_ARG and "pos" in _err(L)
+    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 0) == 8 * 262144 * 4
+    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 1) == 0
+
+
+def test_attention_validation(L):
+    N = None
+    rc = L.hattn_sparse_attn(FAKE, N, FAKE, N, FAKE, 1, 1, 128, 512, 100, 16, 64, 1e4, 1e-6,
+                             0.04, FAKE, FAKE, N, 0, N)
+    assert rc == hattn.INVALID_ARG and "idx" in _err(L)
+    rc = L.hattn_hca_attn(FAKE, N, FAKE, FAKE, 1, 1, 256, 512, 100, 128, 64, 1e4, 1e-6, 0.04, FAKE,
+                          FAKE, N, 0, N)
+    assert rc == hattn.INVALID_ARG and "H=256" in _err(L)
+    rc = L.hattn_swa_attn(FAKE, N, FAKE, N, FAKE, 1, 1, 128, 512, 100, 0, 64, 1e4, 1e-6, 0.04,
+                          FAKE, FAKE, N, 0, N)
+    assert rc == hattn.INVALID_ARG
+    rc = L.hattn_hca_attn(FAKE, N, FAKE, FAKE, 1, 1, 128, 512, 100, 128, 200, 1e4, 1e-6, 0.04,
+                          FAKE, FAKE, N, 0, N)
+    assert rc == hattn.INVALID_ARG and "r=200" in _err(L)
+    # the merge needs 1..4 branches
+    arr = (ctypes.c_void_p * 1)(FAKE)
+    rc = L.hattn_lse_merge(arr, arr, 0, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
+    assert rc == hattn.INVALID_ARG
+
+
+def test_workspace_sizes_scale_with_splits(L):
+    # decode at the 1M-context shape splits keys across SMs and needs partials
+    assert hattn.attn_workspace_bytes(hattn.KIND_HCA, 8, 1, 128, 512, 8192) > 0
+    # a long prefill row block has no split and needs none
+    assert hattn.attn_workspace_bytes(hattn.KIND_SPARSE, 1, 8192, 64, 512, 512) == 0

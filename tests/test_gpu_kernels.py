@@ -1,0 +1,303 @@
+"""GPU parity of every C-ABI call against the fp64 CPU oracle, at sizes the
+oracle finishes in seconds that still span several tiles and a ragged tail,
+plus the edge cases (empty / short key sets, padding, uninitialised cache
+tails, ties, the lazy-rescale path, the bounded-wait timeout)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from sparse_attention_26_b300 import hattn, synth
+
+from _util import (KV_REL_L2, check_attn, check_topk, f64, rel_l2)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def bits(t):
+    return synth.bits(t)
+
+
+def randn_bf16(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def randn_f32(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g).float()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from sparse_attention_26_b300 import build
+    build.build()
+    hattn.lib()
+    orc.lib()
+    torch.cuda.init()
+    yield
+    hattn.check_status()
+
+
+# ------------------------------------------------------------------ status
+def test_bounded_wait_times_out_and_reports():
+    hattn.check_status()  # clear
+    hattn.selftest_wait_timeout(2_000_000)  # 2 ms, nothing ever arrives
+    assert hattn.check_status_code() == hattn.TIMEOUT
+    assert hattn.check_status_code() == hattn.OK  # read clears it
+
+
+# ------------------------------------------------------------------ compression
+@pytest.mark.parametrize("B,L,D,dI,r,j0,j1", [
+    (2, 64, 64, 32, 16, 0, 16),
+    (1, 1030, 512, 128, 64, 0, 257),
+    (2, 1024, 512, 128, 64, 100, 131),   # incremental range
+])
+def test_csa_compress(B, L, D, dI, r, j0, j1):
+    kv = randn_bf16((B, L, D), 1)
+    ik = randn_bf16((B, L, dI), 2)
+    gate = randn_bf16((B, L), 3)
+    gamma = (1.0 + 0.1 * randn_f32((D,), 4))
+    N_cap = L // 4
+    kv_c = torch.full((B, N_cap, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ik_c = torch.full((B, N_cap, dI), float("nan"), dtype=torch.bfloat16, device=DEV)
+    hattn.csa_compress(kv.to(DEV), ik.to(DEV), gate.to(DEV), r=r, j_begin=j0, j_end=j1,
+                       kv_c=kv_c, ik_c=ik_c, gamma_kv=gamma.to(DEV))
+    hattn.check_status()
+    ref_kv, ref_ik, _ = orc.compress(bits(kv), bits(gate), 4, 8, r, j0, j1, ik_raw=bits(ik),
+                                     gamma=gamma.numpy())
+    assert rel_l2(kv_c[:, j0:j1], ref_kv) <= KV_REL_L2
+    assert rel_l2(ik_c[:, j0:j1], ref_ik) <= KV_REL_L2
+    # rows outside the range are untouched
+    assert torch.isnan(kv_c[:, :j0].float()).all() and torch.isnan(kv_c[:, j1:].float()).all()
+
+
+@pytest.mark.parametrize("B,L,D,r", [(2, 1024, 512, 64), (1, 300, 64, 16)])
+def test_hca_compress(B, L, D, r):
+    kv = randn_bf16((B, L, D), 5)
+    gate = randn_bf16((B, L), 6)
+    n = L // 128
+    if n == 0:
+        pytest.skip("no complete entry")
+    kv_h = hattn.hca_compress(kv.to(DEV), gate.to(DEV), r=r)
+    hattn.check_status()
+    ref, _, _ = orc.compress(bits(kv), bits(gate), 128, 128, r, 0, n)
+    assert rel_l2(kv_h[:, :n], ref) <= KV_REL_L2
+
+
+# ------------------------------------------------------------------ indexer + top-k
+def _indexer_case(B, T, HI, dI, N_cap, k, pos, seed, m=4):
+    iq = randn_bf16((B, T, HI, dI), seed)
+    w = randn_f32((B, T, HI), seed + 1)
+    ik = randn_bf16((B, N_cap, dI), seed + 2)
+    pos_t = torch.tensor(pos, dtype=torch.int32).reshape(B, T)
+    scores = torch.full((B, T, N_cap), float("nan"), device=DEV)
+    idx = hattn.indexer_topk(iq.to(DEV), w.to(DEV), ik.to(DEV), pos_t.to(DEV), k=k, m=m,
+                             score_out=scores)
+    hattn.check_status()
+    ref = orc.indexer_scores(bits(iq), w.numpy(), bits(ik), pos_t.numpy(), m)
+    vis = ~np.isnan(ref)
+    got = f64(scores)
+    assert np.isfinite(got[vis]).all()
+    err = np.abs(got[vis] - ref[vis])
+    tol = 2e-3 * (np.abs(ref[vis]) + np.sqrt(HI * dI) * 0.05)
+    assert (err <= tol).all(), f"score error {err.max():.3e}"
+    check_topk(idx.cpu().numpy(), ref, pos_t.numpy(), m, k)
+    return idx
+
+
+def test_indexer_decode_ragged():
+    # visible counts 0, 10 (< k), 150 (spans two 128-blocks), 600 (ragged tail)
+    _indexer_case(4, 1, 64, 128, 600, 16, [2, 41, 603, 2399], 10)
+
+
+def test_indexer_prefill_groups():
+    # 64 heads -> 4 queries per group; T=7 leaves a ragged group
+    T = 7
+    _indexer_case(2, T, 64, 128, 520, 32, [[4 * j + 3 + 40 * t for t in range(T)]
+                                           for j in range(2)], 20)
+
+
+def test_indexer_tiny_shape():
+    # 2 heads x 32 dims, causal prefill over 256 positions
+    _indexer_case(1, 256, 2, 32, 64, 16, [list(range(256))], 30)
+
+
+@pytest.mark.parametrize("N_cap,k", [(40000, 1024), (262144, 1024), (3000, 512)])
+def test_topk_exact_with_ties(N_cap, k):
+    """Integer-valued scores are exact in fp32 on both sides, so the selected
+    sets must agree bit for bit, ties included (ties go to the smaller j)."""
+    B, T, HI, dI = 2, 1, 2, 32
+    g = torch.Generator().manual_seed(7)
+    iq = torch.randint(-2, 3, (B, T, HI, dI), generator=g).to(torch.bfloat16)
+    ik = torch.randint(-2, 3, (B, N_cap, dI), generator=g).to(torch.bfloat16)
+    w = torch.tensor([1.0, 0.5]).repeat(B, T, 1).float()
+    pos = torch.tensor([[4 * N_cap - 1], [4 * (N_cap // 2) + 1]], dtype=torch.int32)
+    scores = torch.zeros((B, T, N_cap), device=DEV)
+    idx = hattn.indexer_topk(iq.to(DEV), w.to(DEV), ik.to(DEV), pos.to(DEV), k=k, m=4,
+                             score_out=scores)
+    hattn.check_status()
+    ref = orc.indexer_scores(bits(iq), w.numpy(), bits(ik), pos.numpy(), 4)
+    vis = ~np.isnan(ref)
+    np.testing.assert_array_equal(f64(scores)[vis], ref[vis])
+    ref_idx = orc.topk(ref, pos.numpy(), 4, k)
+    got = idx.cpu().numpy()
+    for b in range(B):
+        assert sorted(got[b, 0][got[b, 0] >= 0].tolist()) == sorted(
+            ref_idx[b, 0][ref_idx[b, 0] >= 0].tolist())
+        assert (got[b, 0] == -1).sum() == (ref_idx[b, 0] == -1).sum()
+
+
+def test_topk_without_score_output_uses_workspace():
+    B, T, HI, dI, N = 1, 1, 64, 128, 2048
+    iq = randn_bf16((B, T, HI, dI), 40).to(DEV)
+    w = randn_f32((B, T, HI), 41).to(DEV)
+    ik = randn_bf16((B, N, dI), 42).to(DEV)
+    pos = torch.tensor([[4 * N - 1]], dtype=torch.int32, device=DEV)
+    a = hattn.indexer_topk(iq, w, ik, pos, k=64)
+    s = torch.empty((B, T, N), device=DEV)
+    b = hattn.indexer_topk(iq, w, ik, pos, k=64, score_out=s)
+    assert sorted(a.cpu().flatten().tolist()) == sorted(b.cpu().flatten().tolist())
+
+
+# ------------------------------------------------------------------ attention branches
+def _pos(B, T, values):
+    return torch.tensor(values, dtype=torch.int32).reshape(B, T)
+
+
+@pytest.mark.parametrize("B,T,H,D,r,N_cap,k", [
+    (2, 2, 128, 512, 64, 300, 100),
+    (1, 3, 4, 64, 16, 40, 16),
+    (1, 2, 64, 512, 64, 2048, 512),
+    (3, 1, 128, 512, 64, 5000, 1024),
+])
+def test_sparse_attn(B, T, H, D, r, N_cap, k):
+    q = randn_bf16((B, T, H, D), 50)
+    cache = randn_bf16((B, N_cap, D), 51)
+    pos = _pos(B, T, [4 * N_cap - 1] * (B * T))
+    nvis = np.full((B, T), N_cap)
+    idx = synth.random_idx(B, T, k, nvis, seed=52, n_valid=max(1, k - 7))
+    o, lse = hattn.sparse_attn(q.to(DEV), cache.to(DEV), idx.to(DEV), pos.to(DEV), r=r)
+    hattn.check_status()
+    ro, rl = orc.attention(orc.KIND_SPARSE, bits(q), bits(cache), pos.numpy(), idx=idx.numpy(),
+                           r=r)
+    check_attn(o, lse, ro, rl, "sparse")
+
+
+def test_sparse_attn_all_padding_and_bad_index():
+    B, T, H, D, N_cap, k = 1, 2, 8, 64, 50, 16
+    q = randn_bf16((B, T, H, D), 53)
+    cache = randn_bf16((B, N_cap, D), 54)
+    idx = torch.full((B, T, k), -1, dtype=torch.int32)
+    idx[0, 1, :3] = torch.tensor([5, 7, 9])
+    pos = _pos(B, T, [199, 199])
+    o, lse = hattn.sparse_attn(q.to(DEV), cache.to(DEV), idx.to(DEV), pos.to(DEV), r=16)
+    hattn.check_status()
+    assert torch.isinf(lse[0, 0]).all() and (lse[0, 0] < 0).all()
+    assert (o[0, 0].float() == 0).all()
+    ro, rl = orc.attention(orc.KIND_SPARSE, bits(q), bits(cache), pos.numpy(), idx=idx.numpy(),
+                           r=16)
+    check_attn(o[0, 1], lse[0, 1], ro[0, 1], rl[0, 1], "sparse short")
+    idx[0, 1, 4] = N_cap + 3  # out of range: skipped and reported
+    hattn.sparse_attn(q.to(DEV), cache.to(DEV), idx.to(DEV), pos.to(DEV), r=16)
+    assert hattn.check_status_code() == hattn.DEVICE_INDEX
+
+
+@pytest.mark.parametrize("B,T,H,D,r,N_cap,pos_list", [
+    (2, 1, 128, 512, 64, 1000, [128 * 1000 - 1, 128 * 613 + 5]),   # ragged tail
+    (1, 200, 4, 64, 16, 6, list(range(800 - 200, 800))),           # prefill, 32 q per block
+    (1, 5, 128, 512, 64, 64, [100, 127, 128, 4000, 8191]),          # empty and short rows
+])
+def test_hca_attn(B, T, H, D, r, N_cap, pos_list):
+    q = randn_bf16((B, T, H, D), 60)
+    cache = randn_bf16((B, N_cap, D), 61)
+    pos = _pos(B, T, pos_list)
+    # entries that are not visible may hold anything, even NaN
+    cdev = cache.to(DEV)
+    nvis = [min((p + 1) // 128, N_cap) for p in pos_list]
+    if B == 2:
+        cdev[1, nvis[1]:] = float("nan")
+    o, lse = hattn.hca_attn(q.to(DEV), cdev, pos.to(DEV), r=r, m=128)
+    hattn.check_status()
+    ro, rl = orc.attention(orc.KIND_HCA, bits(q), bits(cache), pos.numpy(), m=128, r=r)
+    check_attn(o, lse, ro, rl, "hca")
+
+
+@pytest.mark.parametrize("B,T,H,D,r,L,W,pos_list", [
+    (2, 1, 128, 512, 64, 300, 128, [299, 150]),
+    (1, 256, 4, 64, 16, 256, 128, list(range(256))),
+    (1, 3, 64, 512, 64, 700, 128, [0, 64, 699]),
+])
+def test_swa_attn(B, T, H, D, r, L, W, pos_list):
+    q = randn_bf16((B, T, H, D), 70)
+    raw = randn_bf16((B, L, D), 71)
+    gq = 1.0 + 0.1 * randn_f32((D,), 72)
+    gk = 1.0 + 0.1 * randn_f32((D,), 73)
+    pos = _pos(B, T, pos_list)
+    o, lse = hattn.swa_attn(q.to(DEV), raw.to(DEV), pos.to(DEV), r=r, W=W, gamma_q=gq.to(DEV),
+                            gamma_kv=gk.to(DEV))
+    hattn.check_status()
+    ro, rl = orc.attention(orc.KIND_SWA, bits(q), bits(raw), pos.numpy(), W=W, r=r,
+                           gamma_q=gq.numpy(), gamma_kv=gk.numpy())
+    check_attn(o, lse, ro, rl, "swa")
+
+
+def test_lazy_rescale_path():
+    """Keys ordered so the running max keeps growing across tiles (forces the
+    tensor-memory rescale of O); D=64 bounds logits by 8."""
+    B, T, H, D, N = 1, 1, 4, 64, 640
+    q = torch.zeros((B, T, H, D))
+    q[..., 0] = 1.0
+    t = torch.linspace(-1.0, 1.0, N)
+    cache = torch.zeros((B, N, D))
+    cache[0, :, 0] = t * 8.0
+    cache[0, :, 1] = torch.sqrt(torch.clamp(64.0 - (t * 8.0) ** 2, min=0.0))
+    q, cache = q.to(torch.bfloat16), cache.to(torch.bfloat16)
+    pos = _pos(B, T, [128 * N - 1])
+    o, lse = hattn.hca_attn(q.to(DEV), cache.to(DEV), pos.to(DEV), r=0, m=128)
+    hattn.check_status()
+    ro, rl = orc.attention(orc.KIND_HCA, bits(q), bits(cache), pos.numpy(), m=128, r=0)
+    check_attn(o, lse, ro, rl, "rescale")
+
+
+# ------------------------------------------------------------------ merge
+@pytest.mark.parametrize("nb,with_sink", [(3, True), (2, False), (1, True)])
+def test_lse_merge(nb, with_sink):
+    B, T, H, D, r = 2, 3, 16, 512, 64
+    os_ = [randn_bf16((B, T, H, D), 80 + i) for i in range(nb)]
+    ls = [randn_f32((B, T, H), 90 + i) * 3 for i in range(nb)]
+    ls[0][0, 0, 0] = -float("inf")  # an empty branch row
+    sink = randn_f32((H,), 99) if with_sink else None
+    pos = _pos(B, T, [5, 77, 1 << 20, 3, 9, 123456])
+    out, lse = hattn.lse_merge([o.to(DEV) for o in os_], [l.to(DEV) for l in ls], pos.to(DEV),
+                               r=r, sink=sink.to(DEV) if sink is not None else None)
+    ro, rl = orc.merge([f64(o) for o in os_], [f64(l) for l in ls],
+                       sink.numpy() if sink is not None else None, pos.numpy(), r)
+    check_attn(out, lse, ro, rl, "merge")
+
+
+# ------------------------------------------------------------------ whole tiny layer
+def test_tiny_layer_end_to_end():
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, 0)
+    ref = orc.layer(synth.to_numpy(inp), wl.cfg(), keep=True)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    L = wl.L
+    kv_c, ik_c = hattn.csa_compress(d["kv_raw"], d["ik_raw"], d["gate_csa"], r=wl.r)
+    kv_h = hattn.hca_compress(d["kv_raw"], d["gate_hca"], r=wl.r)
+    assert rel_l2(kv_c, ref["kv_c64"]) <= KV_REL_L2
+    idx = hattn.indexer_topk(d["iq"], d["w"], ik_c, d["pos"], k=wl.k)
+    o1, l1 = hattn.sparse_attn(d["q"], kv_c, idx, d["pos"], r=wl.r)
+    o2, l2 = hattn.hca_attn(d["q"], kv_h, d["pos"], r=wl.r)
+    o3, l3 = hattn.swa_attn(d["q"], d["kv_raw"], d["pos"], r=wl.r, W=wl.W)
+    out, lse = hattn.lse_merge([o1, o2, o3], [l1, l2, l3], d["pos"], r=wl.r, sink=d["sink"])
+    hattn.check_status()
+    check_topk(idx.cpu().numpy(), ref["scores"], inp["pos"].numpy(), 4, wl.k, "tiny")
+    check_attn(o3, l3, ref["o_swa"], ref["lse_swa"], "tiny swa")
+    check_attn(o2, l2, ref["o_hca"], ref["lse_hca"], "tiny hca")
+    check_attn(out, lse, ref["out"], ref["lse"], "tiny layer")
+    assert L == 256

@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the hybrid attention decode step at 1M-token context.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (default): the full V4-Pro-shaped hybrid layer decode, batch 8, each
+sequence with 1,048,576 cached tokens -> 262,144 CSA entries (top-1024 via a
+64x128 indexer), 8,192 HCA entries and the last 128 raw tokens for SWA; 128
+heads x 512, RoPE on 64 dims, sinks.  One step = one pass of every row of the
+hot path: the incremental compression of the entries the newest token
+completes, indexer scores, top-k, the three attention branches (with their
+split combines) and the sink merge.  Inputs: seeded synthetic N(0,1) bf16.
+
+Timing: W eager warm-up steps, then the K steps are captured in one CUDA graph
+with CUDA events between steps and around each call; the graph is replayed
+once between a barrier + synchronize on each side.  The per-step input (616
+MB, mostly indexer keys) is larger than L2, so no flush is added.  The
+`e2e` figure repeats the K steps through the same public calls with the
+step's inputs copied from pinned host memory and the output copied back
+inside the timed region.  Under torchrun every rank runs the same per-GPU
+workload on its own GPU (weak scaling, no collective on the data path); the
+time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle (test infrastructure, the only
+reference this layer has) on one sequence of the same workload per step.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "hybrid-attn decode tokens/s @1M ctx (1 B300), HBM GB/s & % roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="hybrid_decode_1m")
+    ap.add_argument("--batch", type=int, default=0, help="override B (profiling only)")
+    ap.add_argument("--context", type=int, default=0, help="override L (profiling only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--soak-ms", type=float, default=1500.0,
+                    help="replay time under the clock sampler before the timed region")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6400.0, 1800.0, "fallback"
+
+
+def workload(args):
+    from sparse_attention_26_b300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    kw = {}
+    if args.batch:
+        kw["B"] = args.batch
+    if args.context:
+        kw["L"] = args.context
+    return synth.scaled(wl, **kw) if kw else wl
+
+
+def step_bytes(wl):
+    """Algorithmic HBM bytes of one decode step (T=1): indexer keys of every
+    visible entry, the k gathered CSA rows, every visible HCA row, W raw rows,
+    q, iq, w, the output; plus the incremental compression reads/writes."""
+    B, L, D, dI = wl.B, wl.L, wl.D, wl.dI
+    n_csa, n_hca = L // wl.m_csa, L // wl.m_hca
+    per = 0
+    if "csa" in wl.branches:
+        per += n_csa * dI * 2 + min(wl.k, n_csa) * D * 2 + wl.HI * dI * 2 + wl.HI * 4
+        per += wl.w_csa * (D + dI + 1) * 2 + (D + dI) * 2
+    if "hca" in wl.branches:
+        per += n_hca * D * 2 + wl.w_hca * (D + 1) * 2 + D * 2
+    if "swa" in wl.branches:
+        per += wl.W * D * 2
+    per += 2 * wl.H * D * 2 + wl.H * 4
+    return B * per
+
+
+def indexer_bytes(wl):
+    n_csa = wl.L // wl.m_csa
+    return wl.B * (n_csa * wl.dI * 2 + wl.HI * wl.dI * 2 + wl.HI * 4)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons),
+                "window": "soak replays of the same graph immediately before and during the "
+                          "timed region"}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif args.impl == "ours":
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample_setup(wl, seed=0):
+    """One sequence of the workload for the fp64 oracle, on seeded synthetic
+    caches of the full size (values drawn directly; timing does not depend on
+    them).  Raw tokens are materialised only where the step reads them."""
+    import numpy as np
+    import torch
+    g = np.random.default_rng(seed)
+
+    def bf(shape):
+        x = torch.from_numpy(g.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
+        return x.view(torch.int16).numpy().view(np.uint16)
+
+    L, D, dI = wl.L, wl.D, wl.dI
+    n_csa, n_hca = L // wl.m_csa, L // wl.m_hca
+    tail = max(wl.W, wl.w_hca, wl.w_csa) + 8
+    kv_raw = np.zeros((1, L, D), np.uint16)
+    ik_raw = np.zeros((1, L, dI), np.uint16)
+    kv_raw[0, L - tail:] = bf((tail, D))
+    ik_raw[0, L - tail:] = bf((tail, dI))
+    s = dict(
+        kv_raw=kv_raw, ik_raw=ik_raw,
+        gate_csa=bf((1, L)), gate_hca=bf((1, L)),
+        kv_c=bf((1, n_csa, D)) if "csa" in wl.branches else None,
+        ik_c=bf((1, n_csa, dI)) if "csa" in wl.branches else None,
+        kv_h=bf((1, max(n_hca, 1), D)),
+        q=bf((1, 1, wl.H, D)), iq=bf((1, 1, wl.HI, dI)),
+        w=g.standard_normal((1, 1, wl.HI)).astype(np.float32),
+        sink=g.standard_normal(wl.H).astype(np.float32),
+        pos=np.array([[L - 1]], np.int32),
+    )
+    return s
+
+
+def oracle_step(wl, s):
+    """The decode step of one sequence through the oracle's stages."""
+    import oracle as orc
+    L, t = wl.L, wl.L - 1
+    o_list, l_list = [], []
+    if "csa" in wl.branches:
+        j = (t + 1) // wl.m_csa - 1
+        orc.compress(s["kv_raw"], s["gate_csa"], wl.m_csa, wl.w_csa, wl.r, j, j + 1,
+                     ik_raw=s["ik_raw"])
+        sc = orc.indexer_scores(s["iq"], s["w"], s["ik_c"], s["pos"], wl.m_csa)
+        idx = orc.topk(sc, s["pos"], wl.m_csa, wl.k)
+        o, l = orc.attention(orc.KIND_SPARSE, s["q"], s["kv_c"], s["pos"], idx=idx, r=wl.r)
+        o_list.append(o)
+        l_list.append(l)
+    if "hca" in wl.branches:
+        j = (t + 1) // wl.m_hca - 1
+        orc.compress(s["kv_raw"], s["gate_hca"], wl.m_hca, wl.w_hca, wl.r, j, j + 1)
+        o, l = orc.attention(orc.KIND_HCA, s["q"], s["kv_h"], s["pos"], m=wl.m_hca, r=wl.r)
+        o_list.append(o)
+        l_list.append(l)
+    if "swa" in wl.branches:
+        o, l = orc.attention(orc.KIND_SWA, s["q"], s["kv_raw"], s["pos"], W=wl.W, r=wl.r)
+        o_list.append(o)
+        l_list.append(l)
+    orc.merge(o_list, l_list, s["sink"], s["pos"], wl.r)
+    return L
+
+
+def cpu_baseline(wl, steps=1):
+    s = oracle_sample_setup(wl)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(wl, s)
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": 1.0 / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 of {wl.B} sequences x 1 decode step of {wl.name} (full 1M-context "
+                      f"sizes: {wl.L // wl.m_csa} indexer entries, top-{wl.k}, "
+                      f"{wl.L // wl.m_hca} HCA entries, {wl.W} SWA tokens), single-threaded "
+                      "fp64 C, seeded synthetic caches",
+            "seconds_per_token": dt}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, world, rank, budget_s=150.0):
+    """The oracle on a bounded sample per step: one sequence at a context of
+    L' <= L tokens (a prefix of the cache), with L' chosen so that the whole
+    --steps/--warmup run fits `budget_s`; tokens/s is scaled by the work
+    fraction step_bytes(L') / step_bytes(L) (indexer, HCA scans and the rest
+    grow linearly with the context)."""
+    if rank != 0:
+        return
+    from sparse_attention_26_b300 import synth
+    wl = workload(args)
+    one = synth.scaled(wl, B=1)
+
+    def at(L):
+        L = max(wl.m_hca * 8, (L // wl.m_hca) * wl.m_hca)
+        return synth.scaled(one, L=L)
+
+    # calibrate on 1/64 of the context
+    cal = at(wl.L // 64)
+    s = oracle_sample_setup(cal)
+    t0 = time.perf_counter()
+    oracle_step(cal, s)
+    t_cal = time.perf_counter() - t0
+    est_full = t_cal * step_bytes(one) / step_bytes(cal)
+    n = max(1, args.steps + args.warmup)
+    frac = min(1.0, budget_s / n / est_full)
+    smp = at(int(wl.L * frac))
+    s = oracle_sample_setup(smp)
+    for _ in range(args.warmup):
+        oracle_step(smp, s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(smp, s)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    work = step_bytes(smp) / step_bytes(one)
+    v = work / dt
+    sample = (f"each step: 1 decode token of one sequence at context {smp.L} of {wl.L} "
+              f"(work fraction {work:.4f}, tokens/s scaled by it), single-threaded fp64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 / v, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(wl, sample=sample),
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(wl, **extra):
+    d = {"workload": wl.name, "batch": wl.B, "context_tokens": wl.L, "queries_per_seq": wl.T,
+         "heads": wl.H, "head_dim": wl.D, "rope_dims": wl.r, "indexer": f"{wl.HI}x{wl.dI}",
+         "top_k": wl.k, "csa_entries": wl.L // wl.m_csa, "hca_entries": wl.L // wl.m_hca,
+         "swa_window": wl.W, "branches": list(wl.branches),
+         "l2": f"per-step input {step_bytes(wl) / 1e6:.1f} MB > 126 MB L2 (no flush)"}
+    d.update(extra)
+    return d
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+    from sparse_attention_26_b300 import hattn, synth
+    from sparse_attention_26_b300.layer import HybridLayer
+
+    hattn.lib()
+    dev = torch.device("cuda", local)
+    wl = workload(args)
+    inp = synth.make_inputs(wl, seed=0, device=dev)
+    raw = {k: inp[k] for k in ["kv_raw", "ik_raw", "gate_csa", "gate_hca"]}
+    layer = HybridLayer(wl, raw, device=dev)
+    q, iq, w, pos, sink = inp["q"], inp["iq"], inp["w"], inp["pos"], inp["sink"]
+    t_new = wl.L - 1
+    torch.cuda.synchronize()
+    hattn.check_status()
+
+    for _ in range(args.warmup):
+        layer.step(q, iq, w, pos, sink, t_new=t_new)
+    torch.cuda.synchronize()
+    hattn.check_status()
+
+    K = args.steps
+    names = ["compress", "indexer", "topk", "sparse", "hca", "swa", "merge"]
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    step_ev = [mk() for _ in range(K + 1)]
+    kev = [{n: (mk(), mk()) for n in names} for _ in range(K)]
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        step_ev[0].record()
+        for i in range(K):
+            layer.step(q, iq, w, pos, sink, t_new=t_new, events=kev[i])
+            step_ev[i + 1].record()
+    torch.cuda.synchronize()
+    g.replay()  # one untimed replay of the captured graph
+    torch.cuda.synchronize()
+    hattn.check_status()
+
+    # clock sampling: soak replays, then the timed replay
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.perf_counter() + args.soak_ms / 1e3
+    while time.perf_counter() < t_end:
+        g.replay()
+        torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    hattn.check_status()
+
+    total_ms = step_ev[0].elapsed_time(step_ev[K])
+    total_ms = max_over_ranks(world, total_ms)
+    ms_step = total_ms / K
+    tokens = wl.B * wl.T * K * world
+    value = tokens / (total_ms / 1e3)
+    per_kernel = {n: statistics.mean(kev[i][n][0].elapsed_time(kev[i][n][1]) for i in range(K))
+                  for n in names}
+
+    hbm, bf16, src = peaks()
+    ib = indexer_bytes(wl)
+    idx_ms = per_kernel["indexer"]
+    achieved = ib / (idx_ms / 1e3) / 1e9
+    sb = step_bytes(wl)
+    roofline = {"bound": "hbm", "kernel": "indexer_score_kernel", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                else "fallback 6.4 TB/s",
+                "algorithmic_bytes_per_launch": ib,
+                "avg_launch_ms": idx_ms}
+    step_roof = {"alg_bytes_per_step": sb, "achieved_gbs": sb / (ms_step / 1e3) / 1e9,
+                 "frac_of_measured_hbm": sb / (ms_step / 1e3) / 1e9 / hbm,
+                 "roofline_ms_per_step": sb / (hbm * 1e9) * 1e3}
+
+    # e2e: host buffers in, output back to host, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, world, layer, inp, wl, t_new, stream)
+
+    launches = layer.launches_per_step(wl.T, t_new) * K
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(wl, parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
+                              step_roofline=step_roof,
+                              per_call_ms=per_kernel),
+        "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, world, layer, inp, wl, t_new, stream):
+    import torch
+    K = args.steps
+    dev = inp["q"].device
+    host = {k: inp[k].cpu().pin_memory() for k in ["q", "iq", "w", "pos"]}
+    tok = {"kv": inp["kv_raw"][:, t_new].cpu().pin_memory(),
+           "ik": inp["ik_raw"][:, t_new].cpu().pin_memory(),
+           "gc": inp["gate_csa"][:, t_new].cpu().pin_memory(),
+           "gh": inp["gate_hca"][:, t_new].cpu().pin_memory()}
+    dq = {k: torch.empty_like(inp[k]) for k in host}
+    out_h = torch.empty(inp["q"].shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(inp["q"].shape[:3], dtype=torch.float32).pin_memory()
+    raw = layer.raw
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        ev[0].record()
+        for _ in range(K):
+            for k in host:
+                dq[k].copy_(host[k], non_blocking=True)
+            raw["kv_raw"][:, t_new].copy_(tok["kv"], non_blocking=True)
+            raw["ik_raw"][:, t_new].copy_(tok["ik"], non_blocking=True)
+            raw["gate_csa"][:, t_new].copy_(tok["gc"], non_blocking=True)
+            raw["gate_hca"][:, t_new].copy_(tok["gh"], non_blocking=True)
+            out, lse = layer.step(dq["q"], dq["iq"], dq["w"], dq["pos"], inp["sink"], t_new=t_new)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+        ev[1].record()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(world, ev[0].elapsed_time(ev[1]))
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + sum(
+        t.numel() * t.element_size() for t in tok.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    return {"value": wl.B * wl.T * K * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / K}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

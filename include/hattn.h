@@ -116,6 +116,17 @@ HATTN_API int hattn_indexer_topk(const void* iq, const float* w, const void* ik_
 HATTN_API size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
                                           int score_out_given);
 
+/* The two stages of hattn_indexer_topk as separate calls.
+ * hattn_indexer_scores writes I[j] for j < n into score_out [B][T][N_cap] fp32
+ * (entries j >= n untouched).  hattn_topk_select reads those scores and writes
+ * idx_out [B][T][k] with the selection rule above (same limits). */
+HATTN_API int hattn_indexer_scores(const void* iq, const float* w, const void* ik_c,
+                                   const int32_t* pos, int B, int T, int HI, int dI,
+                                   int64_t N_cap, int m, float* score_out, hattn_stream_t stream);
+HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T,
+                                int64_t N_cap, int k, int m, int32_t* idx_out,
+                                hattn_stream_t stream);
+
 /* -------------------------------------------------------------------------
  * Attention branches.  Shared-KV MQA latent ([AT] "Inference efficiency"):
  * keys and values are the same D-dim vectors K~ for all heads.  Each query

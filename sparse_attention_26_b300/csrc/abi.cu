@@ -37,7 +37,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Device status word: one int per device, read and cleared by hattn_check_status.
-__device__ int g_device_status;
+__device__ int g_device_status[4];  // code, wait site, block, thread
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -300,40 +300,29 @@ size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
   return (size_t)B * T * N_cap * sizeof(float);
 }
 
-int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
-                       int B, int T, int HI, int dI, int64_t N_cap, int k, int m,
-                       int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
-                       hattn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
+                        int B, int T, int HI, int dI, int64_t N_cap, int m, float* scores,
+                        hattn_stream_t stream) {
   REQUIRE_PTR(iq);
   REQUIRE_PTR(w);
   REQUIRE_PTR(ik_c);
   REQUIRE_PTR(pos);
-  REQUIRE_PTR(idx_out);
-  if (score_out) REQUIRE_PTR(score_out);
+  REQUIRE_PTR(scores);
   REQUIRE(B >= 1 && T >= 1 && N_cap >= 1, "B, T and N_cap must be >= 1");
   REQUIRE(HI >= 1 && HI <= 256, "HI=%d must be in [1, 256]", HI);
   REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
-  REQUIRE(k >= 1 && k <= 2048, "k=%d must be in [1, 2048]", k);
   REQUIRE(m >= 1, "m must be >= 1");
-  REQUIRE((int64_t)B * T * HI < (1ll << 31) && (int64_t)B * T < (1 << 16) * 32768ll,
-          "too many queries");
+  REQUIRE((int64_t)B * T * HI < (1ll << 31), "too many query heads");
   IndexerPlan ip;
   if (!plan_indexer(T, HI, dI, &ip))
     return fail(HATTN_ERR_UNSUPPORTED, "no indexer kernel for HI=%d dI=%d", HI, dI);
   int sms = 0;
   int* status = nullptr;
   if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
-  TopkPlan tp;
-  if (!plan_topk(B * T, N_cap, sms, &tp))
-    return fail(HATTN_ERR_UNSUPPORTED, "top-k over N_cap=%lld entries is not supported",
-                (long long)N_cap);
-  float* scores = score_out;
-  if (!scores) {
-    const size_t need = hattn_indexer_topk_workspace_bytes(B, T, N_cap, k, 0);
-    REQUIRE_PTR(workspace);
-    REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
-    scores = static_cast<float*>(workspace);
-  }
   CUtensorMap tm_ik, tm_iq;
   {
     const uint64_t dims[3] = {(uint64_t)dI, (uint64_t)N_cap, (uint64_t)B};
@@ -368,22 +357,78 @@ int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const i
   a.N_cap = N_cap;
   a.total_slots = (int64_t)B * a.groups_per_seq * a.nblk;
   const int grid = static_cast<int>(a.total_slots < sms ? a.total_slots : sms);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_indexer_score(tm_ik, tm_iq, a, ip, grid, st);
+  cudaError_t e = launch_indexer_score(tm_ik, tm_iq, a, ip, grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
+  return ok();
+}
+
+int topk_impl(const float* scores, const int32_t* pos, int rows, int64_t N_cap, int k, int m,
+              int32_t* idx_out, hattn_stream_t stream) {
+  REQUIRE_PTR(scores);
+  REQUIRE_PTR(pos);
+  REQUIRE_PTR(idx_out);
+  REQUIRE(rows >= 1 && rows < 65536 * 32768ll && N_cap >= 1, "rows and N_cap must be >= 1");
+  REQUIRE(k >= 1 && k <= 2048, "k=%d must be in [1, 2048]", k);
+  REQUIRE(m >= 1, "m must be >= 1");
+  int sms = 0;
+  if (!device_info(nullptr, nullptr, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  TopkPlan tp;
+  if (!plan_topk(rows, N_cap, sms, &tp))
+    return fail(HATTN_ERR_UNSUPPORTED, "top-k over N_cap=%lld entries is not supported",
+                (long long)N_cap);
   TopkArgs t;
   t.scores = scores;
   t.pos = pos;
   t.idx = idx_out;
-  t.rows = B * T;
+  t.rows = rows;
   t.k = k;
   t.m = m;
   t.cluster = tp.cluster;
   t.N_cap = N_cap;
   t.slice = tp.slice;
-  e = launch_topk(t, tp, st);
+  cudaError_t e = launch_topk(t, tp, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int hattn_indexer_scores(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
+                         int B, int T, int HI, int dI, int64_t N_cap, int m, float* score_out,
+                         hattn_stream_t stream) {
+  return indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, score_out, stream);
+}
+
+int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T, int64_t N_cap, int k,
+                      int m, int32_t* idx_out, hattn_stream_t stream) {
+  REQUIRE(B >= 1 && T >= 1, "B and T must be >= 1");
+  return topk_impl(scores, pos, B * T, N_cap, k, m, idx_out, stream);
+}
+
+int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
+                       int B, int T, int HI, int dI, int64_t N_cap, int k, int m,
+                       int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
+                       hattn_stream_t stream) {
+  REQUIRE_PTR(iq);
+  REQUIRE_PTR(w);
+  REQUIRE_PTR(ik_c);
+  REQUIRE_PTR(pos);
+  REQUIRE(k >= 1 && k <= 2048, "k=%d must be in [1, 2048]", k);
+  REQUIRE_PTR(idx_out);
+  REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
+  float* scores = score_out;
+  if (!scores) {
+    REQUIRE(B >= 1 && T >= 1 && N_cap >= 1, "B, T and N_cap must be >= 1");
+    const size_t need = hattn_indexer_topk_workspace_bytes(B, T, N_cap, k, 0);
+    REQUIRE_PTR(workspace);
+    REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
+    scores = static_cast<float*>(workspace);
+  }
+  int rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream);
+  if (rc) return rc;
+  return topk_impl(scores, pos, B * T, N_cap, k, m, idx_out, stream);
 }
 
 size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys) {
@@ -474,13 +519,15 @@ int hattn_check_status(hattn_stream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
   int* status = nullptr;
   if (!device_info(nullptr, &status, nullptr)) return fail(HATTN_ERR_CUDA, "no CUDA device");
-  int v = 0;
-  e = cudaMemcpy(&v, status, sizeof v, cudaMemcpyDeviceToHost);
+  int v[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(v, status, sizeof v, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
-  const int zero = 0;
-  e = cudaMemcpy(status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  const int zero[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(status, zero, sizeof zero, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "status clear");
-  if (v != 0) return fail(v, "device reported: %s", hattn_status_string(v));
+  if (v[0] != 0)
+    return fail(v[0], "device reported: %s (wait site %d, block %d, thread %d)",
+                hattn_status_string(v[0]), v[1], v[2], v[3]);
   return ok();
 }
 

@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int p = 0; p < ndc; ++p, ++ctr) {
             const int slot = static_cast<int>(ctr % nslot);
             if (ctr >= nslot &&
-                !mbar_wait(smem_u32(&sm->empty[slot]), ((ctr / nslot) + 1) & 1, abort, a.status))
+                !mbar_wait(smem_u32(&sm->empty[slot]), ((ctr / nslot) + 1) & 1, abort, a.status, kWaitLimitNs, 18))
               break;
             const uint32_t fb = smem_u32(&sm->full[slot]);
             mbar_arrive_expect_tx(fb, 8192);
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t first = ctr > nslot ? ctr - nslot : 0;
           for (int64_t x = first; x < ctr; ++x)
             mbar_wait(smem_u32(&sm->full[x % nslot]), (x / nslot) & 1, nullptr, nullptr,
-                      10000000ull);
+                      10000000ull, 19);
         }
       }
     } else if (KIND == kSparse) {
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = 0; p < ndc; ++p, ++ctr) {
           const int slot = static_cast<int>(ctr % nslot);
           if (ctr >= nslot &&
-              !mbar_wait(smem_u32(&sm->empty[slot]), ((ctr / nslot) + 1) & 1, abort, a.status))
+              !mbar_wait(smem_u32(&sm->empty[slot]), ((ctr / nslot) + 1) & 1, abort, a.status, kWaitLimitNs, 20))
             break;
           const int dcol = chunk_dc(p) * 64;
           const uint32_t dst = smem_u32(sRing + slot * 8192);
@@ -354,9 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         for (int p = 0; p < ndc; ++p, ++ctr) {
           const int slot = static_cast<int>(ctr % nslot);
-          if (ctr >= nslot &&
-              !mbar_wait(smem_u32(&sm->empty[slot]), ((ctr / nslot) + 1) & 1, abort, a.status))
-            break;
+          const bool got = ctr < nslot ||
+                           mbar_wait(smem_u32(&sm->empty[slot]), ((ctr / nslot) + 1) & 1, abort,
+                                     a.status, kWaitLimitNs, 21);
+          if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform (shuffles follow)
           const int dcol = chunk_dc(p) * 64;
           uint8_t* dst = sRing + slot * 8192;
           const int piece = lane & 7;
@@ -397,7 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // wait for a chunk; for an HCA tail tile, zero its invalid key rows first
     auto wait_chunk = [&](int64_t c, int nvalid) -> bool {
       const int slot = static_cast<int>(c % nslot);
-      if (!mbar_wait(smem_u32(&sm->full[slot]), (c / nslot) & 1, abort, a.status)) return false;
+      const bool got = mbar_wait(smem_u32(&sm->full[slot]), (c / nslot) & 1, abort, a.status,
+                                 kWaitLimitNs, 22);
+      if (!__all_sync(0xffffffffu, got)) return false;  // warp-uniform
       if (KIND == kHca && nvalid < kTile) {
         uint8_t* dst = sRing + slot * 8192;
         for (int pc = nvalid * 8 + lane; pc < kTile * 8; pc += 32)
@@ -422,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     auto issue_pv = [&](int j) -> bool {
-      if (!mbar_wait(smem_u32(&sm->p_full), j & 1, abort, a.status)) return false;
+      const bool got = mbar_wait(smem_u32(&sm->p_full), j & 1, abort, a.status, kWaitLimitNs, 23);
+      if (!__all_sync(0xffffffffu, got)) return false;  // warp-uniform
       if (lane == 0) {
         tc_fence_after();
         for (int e = 0; e < n_own; ++e) {
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (!ok) {
       // wait (bounded) for the MMAs already issued before the memory is released
-      mbar_wait(smem_u32(&sm->o_full), 0, nullptr, nullptr, 10000000ull);
+      mbar_wait(smem_u32(&sm->o_full), 0, nullptr, nullptr, 10000000ull, 24);
     }
   } else {
     // ============================================================ softmax
@@ -510,7 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         colmask = nv >= 64 ? ~0ull : ((1ull << nv) - 1);
       }
       const int sb = i & 1;
-      if (!mbar_wait(smem_u32(&sm->s_full[sb]), (i >> 1) & 1, abort, a.status)) { ok = false; break; }
+      const bool got = mbar_wait(smem_u32(&sm->s_full[sb]), (i >> 1) & 1, abort, a.status,
+                                 kWaitLimitNs, 25);
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }  // warp-uniform exit
       tc_fence_after();
       float s[64];
       {
@@ -532,23 +538,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         s[c] = v ? s[c] * sl2 : -INFINITY;
         mx = fmaxf(mx, s[c]);
       }
-      if (mx > m_used + 8.f) {
-        // lazy rescale: only when the running max grows by more than 2^8
-        if (m_used != -INFINITY && i > 0) {
-          const float f = exp2f(m_used - mx);
-          for (int cc = 0; cc < ocols; cc += 32) {
-            float o[32];
-            tmem_ld32(tO + lane_base + cc, o);
-            tmem_wait_ld();
+      // Lazy rescale: only when the running max grows by more than 2^8.  The
+      // tensor-memory loads/stores are warp-collective, so the decision is
+      // taken per warp; lanes that need no rescale multiply by 1.
+      const bool grow = mx > m_used + 8.f;
+      const bool need_rescale = grow && m_used != -INFINITY && i > 0;
+      if (__any_sync(0xffffffffu, need_rescale)) {
+        const float f = need_rescale ? exp2f(m_used - mx) : 1.f;
+        for (int cc = 0; cc < ocols; cc += 32) {
+          float o[32];
+          tmem_ld32(tO + lane_base + cc, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= f;
-            tmem_st32(tO + lane_base + cc, o);
-          }
-          tmem_wait_st();
-          l *= f;
+          for (int e = 0; e < 32; ++e) o[e] *= f;
+          tmem_st32(tO + lane_base + cc, o);
         }
-        m_used = mx;
+        tmem_wait_st();
+        l *= f;
       }
+      if (grow) m_used = mx;
       uint8_t* prow = sP;
 #pragma unroll
       for (int pc = 0; pc < 8; ++pc) {
@@ -567,7 +575,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(smem_u32(&sm->p_full));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(smem_u32(&sm->o_full), 0, abort, a.status) && row_valid) {
+    // The tensor-memory loads are warp-collective: every lane of the warp runs
+    // them; only rows that exist store.
+    bool done = ok && mbar_wait(smem_u32(&sm->o_full), 0, abort, a.status, kWaitLimitNs, 40);
+    done = __all_sync(0xffffffffu, done);
+    if (done) {
       tc_fence_after();
       const int64_t row = ((int64_t)b * a.T + t0 + g) * a.H + h;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -576,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float o[32];
         tmem_ld32(tO + lane_base + cc, o);
         tmem_wait_ld();
+        if (!row_valid) continue;
         if (a.nsplit == 1) {
           __nv_bfloat16* dst = a.o + row * a.D + dh * ocols + cc;
 #pragma unroll
@@ -593,13 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(o[e] * inv_l, o[e + 1] * inv_l, o[e + 2] * inv_l, o[e + 3] * inv_l);
         }
       }
-      if (dh == 0) {
+      if (row_valid && dh == 0) {
         if (a.nsplit == 1) a.lse[row] = lse;
         else a.part_lse[row * a.nsplit + split] = lse;
       }
-    } else if (!ok) {
+    } else {
       // drain: make sure no MMA is still writing the accumulators
-      mbar_wait(smem_u32(&sm->o_full), 0, nullptr, nullptr, 10000000ull);
+      mbar_wait(smem_u32(&sm->o_full), 0, nullptr, nullptr, 10000000ull, 41);
     }
   }
 

@@ -28,8 +28,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ void record_status(int* status, int code) {
-  if (status) atomicCAS(status, 0, code);
+// status[0] = first error code; for waits that gave up, status[1..3] =
+// (site, block, thread) of the first one.
+__device__ __forceinline__ void record_status(int* status, int code, int site = 0) {
+  if (status && atomicCAS(status, 0, code) == 0 && site) {
+    status[1] = site;
+    status[2] = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+    status[3] = static_cast<int>(threadIdx.x);
+  }
 }
 
 // ----------------------------------------------------------------- mbarrier
@@ -67,7 +73,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // `limit_ns` (or at once when *abort is set by another thread of the CTA),
 // records kStatusTimeout, sets *abort and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int* status, uint64_t limit_ns = kWaitLimitNs) {
+                                          int* status, uint64_t limit_ns = kWaitLimitNs,
+                                          int site = 1) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
@@ -76,7 +83,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if ((++spins & 63u) == 0) {
       if (abort && *abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
-        record_status(status, kStatusTimeout);
+        record_status(status, kStatusTimeout, site);
         if (abort) *abort = 1;
         return false;
       }

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (static_cast<int64_t>(s.blk) * kBlockRows >= nmax) continue;
         if (s.group != loaded) {
           if (qloads > 0 &&
-              !mbar_wait(smem_u32(&sm->qempty), (qloads - 1) & 1, abort, a.status))
+              !mbar_wait(smem_u32(&sm->qempty), (qloads - 1) & 1, abort, a.status, kWaitLimitNs, 10))
             break;
           const uint32_t qb = smem_u32(&sm->qfull);
           mbar_arrive_expect_tx(qb, q_bytes);
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         }
         const int st = static_cast<int>(it % a.stages);
         if (it >= a.stages &&
-            !mbar_wait(smem_u32(&sm->empty[st]), ((it / a.stages) + 1) & 1, abort, a.status))
+            !mbar_wait(smem_u32(&sm->empty[st]), ((it / a.stages) + 1) & 1, abort, a.status, kWaitLimitNs, 11))
           break;
         const uint32_t fb = smem_u32(&sm->full[st]);
         mbar_arrive_expect_tx(fb, stage_bytes);
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         const int64_t first = it > a.stages ? it - a.stages : 0;
         for (int64_t x = first; x < it; ++x)
           mbar_wait(smem_u32(&sm->full[x % a.stages]), (x / a.stages) & 1, nullptr, nullptr,
-                    10000000ull);
+                    10000000ull, 12);
       }
     }
   } else if (warp == 1) {
@@ -171,16 +171,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (static_cast<int64_t>(s.blk) * kBlockRows >= nmax) continue;
         if (s.group != loaded) {
           if (qn > 0) mma_commit(smem_u32(&sm->qempty));  // previous group's reads of sQ done
-          if (!mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status)) break;
+          if (!mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 13)) break;
           ++qn;
           loaded = s.group;
         }
         const int acc = static_cast<int>(it & 1);
         if (it >= 2 &&
-            !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> 1) + 1) & 1, abort, a.status))
+            !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> 1) + 1) & 1, abort, a.status, kWaitLimitNs, 14))
           break;
         const int st = static_cast<int>(it % a.stages);
-        if (!mbar_wait(smem_u32(&sm->full[st]), (it / a.stages) & 1, abort, a.status)) break;
+        if (!mbar_wait(smem_u32(&sm->full[st]), (it / a.stages) & 1, abort, a.status, kWaitLimitNs, 15)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * a.NQ;
         for (int kc = 0; kc < a.KC; ++kc) {
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       }
       // all issued MMAs complete before the accumulators are released
       mma_commit(smem_u32(&sm->mma_done));
-      mbar_wait(smem_u32(&sm->mma_done), 0, nullptr, a.status);
+      mbar_wait(smem_u32(&sm->mma_done), 0, nullptr, a.status, kWaitLimitNs, 16);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -226,7 +226,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         wgroup = s.group;
       }
       const int acc = static_cast<int>(it & 1);
-      if (!mbar_wait(smem_u32(&sm->tfull[acc]), (it >> 1) & 1, abort, a.status)) break;
+      const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), (it >> 1) & 1, abort, a.status,
+                                 kWaitLimitNs, 17);
+      if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: tcgen05.ld follows
       tc_fence_after();
       const int64_t j = static_cast<int64_t>(s.blk) * kBlockRows + row;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * a.NQ;

@@ -137,7 +137,7 @@ __global__ void wait_selftest_kernel(uint64_t timeout_ns, int* status) {
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar), 1);
     fence_barrier_init();
-    mbar_wait(smem_u32(&bar), 0, nullptr, status, timeout_ns);
+    mbar_wait(smem_u32(&bar), 0, nullptr, status, timeout_ns, 28);
   }
 }
 

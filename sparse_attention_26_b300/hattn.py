@@ -35,6 +35,9 @@ _SIGS = {
     "hattn_indexer_topk": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                   _vp, _vp, _vp, _sz, _vp]),
     "hattn_indexer_topk_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32, _i32]),
+    "hattn_indexer_scores": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
+                                    _vp]),
+    "hattn_topk_select": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp]),
     "hattn_sparse_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
                                  _i32, _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
     "hattn_hca_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _f32,
@@ -183,6 +186,36 @@ def indexer_topk(iq, w, ik_c, pos, *, k, m=4, idx_out=None, score_out=None, work
     return idx_out
 
 
+def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, stream=None):
+    """Lightning-indexer scores only; returns score_out [B, T, N_cap] fp32
+    (entries beyond each query's visible count are left untouched)."""
+    _need(iq, "iq", torch.bfloat16, 4)
+    _need(w, "w", torch.float32, 3)
+    _need(ik_c, "ik_c", torch.bfloat16, 3)
+    _need(pos, "pos", torch.int32, 2)
+    B, T, HI, dI = iq.shape
+    N_cap = ik_c.shape[1]
+    if score_out is None:
+        score_out = torch.empty((B, T, N_cap), dtype=torch.float32, device=iq.device)
+    _need(score_out, "score_out", torch.float32)
+    _check(lib().hattn_indexer_scores(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
+                                      N_cap, m, _ptr(score_out), _stream(stream)))
+    return score_out
+
+
+def topk_select(scores, pos, *, k, m=4, idx_out=None, stream=None):
+    """Per-query top-k over precomputed scores; returns idx [B, T, k] int32."""
+    _need(scores, "scores", torch.float32, 3)
+    _need(pos, "pos", torch.int32, 2)
+    B, T, N_cap = scores.shape
+    if idx_out is None:
+        idx_out = torch.empty((B, T, k), dtype=torch.int32, device=scores.device)
+    _need(idx_out, "idx_out", torch.int32)
+    _check(lib().hattn_topk_select(_ptr(scores), _ptr(pos), B, T, N_cap, k, m, _ptr(idx_out),
+                                   _stream(stream)))
+    return idx_out
+
+
 # ------------------------------------------------------------------ attention
 def attn_workspace_bytes(kind, B, T, H, D, n_keys):
     return int(lib().hattn_attn_workspace_bytes(kind, B, T, H, D, n_keys))
@@ -289,12 +322,25 @@ def lse_merge(o_list, lse_list, pos, *, r, sink=None, rope_base=10000.0, out=Non
 
 
 # ------------------------------------------------------------------ status
-def check_status(stream=None):
-    """Synchronise and raise if a kernel reported a device-side error."""
+def _bounded_sync(stream=None, timeout_s=120.0):
+    import time
+    s = stream if stream is not None else torch.cuda.current_stream()
+    t_end = time.monotonic() + timeout_s
+    while not s.query():
+        if time.monotonic() > t_end:
+            raise TimeoutError(f"GPU work did not finish within {timeout_s} s")
+        time.sleep(1e-4)
+
+
+def check_status(stream=None, timeout_s=120.0):
+    """Synchronise (waiting at most timeout_s) and raise if a kernel reported
+    a device-side error."""
+    _bounded_sync(stream, timeout_s)
     _check(lib().hattn_check_status(_stream(stream)))
 
 
-def check_status_code(stream=None):
+def check_status_code(stream=None, timeout_s=120.0):
+    _bounded_sync(stream, timeout_s)
     return int(lib().hattn_check_status(_stream(stream)))
 
 

@@ -1,0 +1,146 @@
+"""One hybrid attention layer (CSA + HCA + SWA, sink merge) driven through the
+C ABI.  This module only sequences the calls and owns the device buffers
+(caches, workspaces, outputs); every step of the computation runs in
+libhattn's kernels.
+
+Decode step at query position t (its own token already written to the raw
+cache), for every sequence of the batch:
+  1. csa_compress / hca_compress of the entry that the token at t completes
+     (when (t+1) is a multiple of m), so the caches are current;
+  2. indexer scores over the visible CSA entries, then top-k selection;
+  3. sparse attention over the selected entries, dense attention over the
+     visible HCA entries, sliding-window attention over the last W tokens;
+  4. sink-augmented LSE merge of the three branches with inverse RoPE.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import hattn
+
+
+class HybridLayer:
+    def __init__(self, wl, raw: dict, device="cuda", build_caches=True):
+        self.wl = wl
+        self.dev = device
+        self.raw = raw  # kv_raw, ik_raw, gate_csa, gate_hca on device
+        B, L, D = raw["kv_raw"].shape
+        self.B, self.L, self.D = B, L, D
+        self.N_csa = L // wl.m_csa
+        self.N_hca = max(1, L // wl.m_hca)
+        bf = torch.bfloat16
+        self.kv_c = torch.zeros((B, self.N_csa, D), dtype=bf, device=device)
+        self.ik_c = torch.zeros((B, self.N_csa, wl.dI), dtype=bf, device=device)
+        self.kv_h = torch.zeros((B, self.N_hca, D), dtype=bf, device=device)
+        if build_caches:
+            self.build_caches()
+        self._bufs = {}
+
+    def build_caches(self, n_tokens=None):
+        """Compress every complete entry of the raw caches (cache build)."""
+        wl, r = self.wl, self.raw
+        L = self.L if n_tokens is None else n_tokens
+        hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=0,
+                           j_end=L // wl.m_csa, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c,
+                           ik_c=self.ik_c)
+        if L // wl.m_hca > 0:
+            hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=0, j_end=L // wl.m_hca,
+                               m=wl.m_hca, kv_h=self.kv_h)
+
+    def buffers(self, T):
+        """Outputs and workspaces for T queries per sequence (allocated once)."""
+        if T in self._bufs:
+            return self._bufs[T]
+        wl, B, D, dev = self.wl, self.B, self.D, self.dev
+        H = wl.H
+        bf = torch.bfloat16
+        b = dict(
+            scores=torch.empty((B, T, self.N_csa), dtype=torch.float32, device=dev),
+            idx=torch.empty((B, T, wl.k), dtype=torch.int32, device=dev),
+            out=torch.empty((B, T, H, D), dtype=bf, device=dev),
+            lse=torch.empty((B, T, H), dtype=torch.float32, device=dev),
+        )
+        for name, kind, nk in [("csa", hattn.KIND_SPARSE, wl.k), ("hca", hattn.KIND_HCA, self.N_hca),
+                               ("swa", hattn.KIND_SWA, wl.W)]:
+            b["o_" + name] = torch.empty((B, T, H, D), dtype=bf, device=dev)
+            b["l_" + name] = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+            ws = hattn.attn_workspace_bytes(kind, B, T, H, D, nk)
+            b["ws_" + name] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self._bufs[T] = b
+        return b
+
+    def step(self, q, iq, w, pos, sink, t_new=None, events=None):
+        """One pass of the hot path for queries q [B,T,H,D] at positions pos.
+
+        t_new: position of the newest token (compresses the entries it
+        completes); None skips the incremental compression.  events: optional
+        dict name -> (start, end) torch.cuda.Event pairs recorded around the
+        calls.  Returns (out bf16 [B,T,H,D], lse fp32 [B,T,H])."""
+        wl, r = self.wl, self.raw
+        B, T = q.shape[0], q.shape[1]
+        b = self.buffers(T)
+
+        def ev(name, i):
+            if events is not None and name in events:
+                events[name][i].record()
+
+        ev("compress", 0)
+        if t_new is not None:
+            for m, w_, kind in [(wl.m_csa, wl.w_csa, "csa"), (wl.m_hca, wl.m_hca, "hca")]:
+                if (t_new + 1) % m == 0:
+                    j = (t_new + 1) // m - 1
+                    if kind == "csa":
+                        hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r,
+                                           j_begin=j, j_end=j + 1, m=m, w=w_, kv_c=self.kv_c,
+                                           ik_c=self.ik_c)
+                    else:
+                        hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=j,
+                                           j_end=j + 1, m=m, kv_h=self.kv_h)
+        ev("compress", 1)
+        o_list, l_list = [], []
+        if "csa" in wl.branches:
+            ev("indexer", 0)
+            hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=b["scores"])
+            ev("indexer", 1)
+            ev("topk", 0)
+            hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
+            ev("topk", 1)
+            ev("sparse", 0)
+            hattn.sparse_attn(q, self.kv_c, b["idx"], pos, r=wl.r, o=b["o_csa"], lse=b["l_csa"],
+                              workspace=b["ws_csa"])
+            ev("sparse", 1)
+            o_list.append(b["o_csa"])
+            l_list.append(b["l_csa"])
+        if "hca" in wl.branches:
+            ev("hca", 0)
+            hattn.hca_attn(q, self.kv_h, pos, r=wl.r, m=wl.m_hca, o=b["o_hca"], lse=b["l_hca"],
+                           workspace=b["ws_hca"])
+            ev("hca", 1)
+            o_list.append(b["o_hca"])
+            l_list.append(b["l_hca"])
+        if "swa" in wl.branches:
+            ev("swa", 0)
+            hattn.swa_attn(q, r["kv_raw"], pos, r=wl.r, W=wl.W, o=b["o_swa"], lse=b["l_swa"],
+                           workspace=b["ws_swa"])
+            ev("swa", 1)
+            o_list.append(b["o_swa"])
+            l_list.append(b["l_swa"])
+        ev("merge", 0)
+        hattn.lse_merge(o_list, l_list, pos, r=wl.r, sink=sink, out=b["out"], lse_out=b["lse"])
+        ev("merge", 1)
+        return b["out"], b["lse"]
+
+    def launches_per_step(self, T, t_new=None):
+        """Kernels one step launches (each attention branch with split-KV adds
+        its combine kernel)."""
+        wl, B, D, H = self.wl, self.B, self.D, self.wl.H
+        n = 1  # merge
+        if t_new is not None:
+            n += int((t_new + 1) % wl.m_csa == 0) + int((t_new + 1) % wl.m_hca == 0)
+        for name, kind, nk in [("csa", hattn.KIND_SPARSE, wl.k), ("hca", hattn.KIND_HCA, self.N_hca),
+                               ("swa", hattn.KIND_SWA, wl.W)]:
+            if name in wl.branches:
+                n += 1 + int(hattn.attn_workspace_bytes(kind, B, T, H, D, nk) > 0)
+                if name == "csa":
+                    n += 2  # indexer scores + top-k select
+        return n

@@ -247,21 +247,24 @@ def test_swa_attn(B, T, H, D, r, L, W, pos_list):
 
 
 def test_lazy_rescale_path():
-    """Keys ordered so the running max keeps growing across tiles (forces the
-    tensor-memory rescale of O); D=64 bounds logits by 8."""
-    B, T, H, D, N = 1, 1, 4, 64, 640
+    """Keys ordered so the running max keeps growing across the tiles of one
+    CTA (forces the tensor-memory rescale of O); D=64 bounds logits by 8.
+    150 sequences fill the SMs, so every row keeps all 10 tiles in one split."""
+    B, T, H, D, N = 150, 1, 4, 64, 640
+    assert hattn.attn_workspace_bytes(hattn.KIND_HCA, B, T, H, D, N) == 0  # one split
     q = torch.zeros((B, T, H, D))
     q[..., 0] = 1.0
     t = torch.linspace(-1.0, 1.0, N)
     cache = torch.zeros((B, N, D))
-    cache[0, :, 0] = t * 8.0
-    cache[0, :, 1] = torch.sqrt(torch.clamp(64.0 - (t * 8.0) ** 2, min=0.0))
+    cache[:, :, 0] = t * 8.0
+    cache[:, :, 1] = torch.sqrt(torch.clamp(64.0 - (t * 8.0) ** 2, min=0.0))
     q, cache = q.to(torch.bfloat16), cache.to(torch.bfloat16)
-    pos = _pos(B, T, [128 * N - 1])
+    pos = _pos(B, T, [128 * N - 1] * B)
     o, lse = hattn.hca_attn(q.to(DEV), cache.to(DEV), pos.to(DEV), r=0, m=128)
     hattn.check_status()
-    ro, rl = orc.attention(orc.KIND_HCA, bits(q), bits(cache), pos.numpy(), m=128, r=0)
-    check_attn(o, lse, ro, rl, "rescale")
+    ro, rl = orc.attention(orc.KIND_HCA, bits(q[:2]), bits(cache[:2]), pos[:2].numpy(), m=128,
+                           r=0)
+    check_attn(o[:2], lse[:2], ro, rl, "rescale")
 
 
 # ------------------------------------------------------------------ merge

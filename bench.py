@@ -349,7 +349,7 @@ def run_ours(args, world, rank, local):
 
     K = args.steps
     names = ["compress", "indexer", "topk", "sparse", "hca", "swa", "merge"]
-    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
     step_ev = [mk() for _ in range(K + 1)]
     kev = [{n: (mk(), mk()) for n in names} for _ in range(K)]
     stream = torch.cuda.Stream(device=dev)
@@ -438,7 +438,7 @@ def run_e2e(args, world, layer, inp, wl, t_new, stream):
     out_h = torch.empty(inp["q"].shape, dtype=torch.bfloat16).pin_memory()
     lse_h = torch.empty(inp["q"].shape[:3], dtype=torch.float32).pin_memory()
     raw = layer.raw
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
         ev[0].record()

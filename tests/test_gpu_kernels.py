@@ -185,7 +185,7 @@ def test_sparse_attn(B, T, H, D, r, N_cap, k):
     hattn.check_status()
     ro, rl = orc.attention(orc.KIND_SPARSE, bits(q), bits(cache), pos.numpy(), idx=idx.numpy(),
                            r=r)
-    check_attn(o, lse, ro, rl, "sparse")
+    check_attn(o, lse, ro, rl, "sparse", storage="bf16")
 
 
 def test_sparse_attn_all_padding_and_bad_index():
@@ -201,7 +201,7 @@ def test_sparse_attn_all_padding_and_bad_index():
     assert (o[0, 0].float() == 0).all()
     ro, rl = orc.attention(orc.KIND_SPARSE, bits(q), bits(cache), pos.numpy(), idx=idx.numpy(),
                            r=16)
-    check_attn(o[0, 1], lse[0, 1], ro[0, 1], rl[0, 1], "sparse short")
+    check_attn(o[0, 1], lse[0, 1], ro[0, 1], rl[0, 1], "sparse short", storage="bf16")
     idx[0, 1, 4] = N_cap + 3  # out of range: skipped and reported
     hattn.sparse_attn(q.to(DEV), cache.to(DEV), idx.to(DEV), pos.to(DEV), r=16)
     assert hattn.check_status_code() == hattn.DEVICE_INDEX
@@ -224,7 +224,7 @@ def test_hca_attn(B, T, H, D, r, N_cap, pos_list):
     o, lse = hattn.hca_attn(q.to(DEV), cdev, pos.to(DEV), r=r, m=128)
     hattn.check_status()
     ro, rl = orc.attention(orc.KIND_HCA, bits(q), bits(cache), pos.numpy(), m=128, r=r)
-    check_attn(o, lse, ro, rl, "hca")
+    check_attn(o, lse, ro, rl, "hca", storage="bf16")
 
 
 @pytest.mark.parametrize("B,T,H,D,r,L,W,pos_list", [
@@ -243,28 +243,31 @@ def test_swa_attn(B, T, H, D, r, L, W, pos_list):
     hattn.check_status()
     ro, rl = orc.attention(orc.KIND_SWA, bits(q), bits(raw), pos.numpy(), W=W, r=r,
                            gamma_q=gq.numpy(), gamma_kv=gk.numpy())
-    check_attn(o, lse, ro, rl, "swa")
+    check_attn(o, lse, ro, rl, "swa", storage="bf16")
 
 
 def test_lazy_rescale_path():
     """Keys ordered so the running max keeps growing across the tiles of one
-    CTA (forces the tensor-memory rescale of O); D=64 bounds logits by 8.
-    150 sequences fill the SMs, so every row keeps all 10 tiles in one split."""
+    CTA (forces the tensor-memory rescale of O).  D=64 bounds the logits by 8;
+    query and keys are spread over all dims, so values stay O(1) like real
+    normalised latents.  150 sequences fill the SMs, so every row keeps all 10
+    tiles in one split."""
     B, T, H, D, N = 150, 1, 4, 64, 640
     assert hattn.attn_workspace_bytes(hattn.KIND_HCA, B, T, H, D, N) == 0  # one split
-    q = torch.zeros((B, T, H, D))
-    q[..., 0] = 1.0
+    u = torch.zeros(D)
+    u[: D // 2] = 1.0 / math.sqrt(D // 2)
+    v = torch.zeros(D)
+    v[D // 2:] = 1.0 / math.sqrt(D // 2)
     t = torch.linspace(-1.0, 1.0, N)
-    cache = torch.zeros((B, N, D))
-    cache[:, :, 0] = t * 8.0
-    cache[:, :, 1] = torch.sqrt(torch.clamp(64.0 - (t * 8.0) ** 2, min=0.0))
-    q, cache = q.to(torch.bfloat16), cache.to(torch.bfloat16)
+    keys = 8.0 * (t[:, None] * u[None] + torch.sqrt(1.0 - t ** 2)[:, None] * v[None])
+    cache = keys[None].expand(B, N, D).contiguous().to(torch.bfloat16)
+    q = u.expand(B, T, H, D).contiguous().to(torch.bfloat16)
     pos = _pos(B, T, [128 * N - 1] * B)
     o, lse = hattn.hca_attn(q.to(DEV), cache.to(DEV), pos.to(DEV), r=0, m=128)
     hattn.check_status()
     ro, rl = orc.attention(orc.KIND_HCA, bits(q[:2]), bits(cache[:2]), pos[:2].numpy(), m=128,
                            r=0)
-    check_attn(o[:2], lse[:2], ro, rl, "rescale")
+    check_attn(o[:2], lse[:2], ro, rl, "rescale", storage="bf16")
 
 
 # ------------------------------------------------------------------ merge
@@ -280,7 +283,7 @@ def test_lse_merge(nb, with_sink):
                                r=r, sink=sink.to(DEV) if sink is not None else None)
     ro, rl = orc.merge([f64(o) for o in os_], [f64(l) for l in ls],
                        sink.numpy() if sink is not None else None, pos.numpy(), r)
-    check_attn(out, lse, ro, rl, "merge")
+    check_attn(out, lse, ro, rl, "merge", storage="bf16")
 
 
 # ------------------------------------------------------------------ whole tiny layer
@@ -300,7 +303,7 @@ def test_tiny_layer_end_to_end():
     out, lse = hattn.lse_merge([o1, o2, o3], [l1, l2, l3], d["pos"], r=wl.r, sink=d["sink"])
     hattn.check_status()
     check_topk(idx.cpu().numpy(), ref["scores"], inp["pos"].numpy(), 4, wl.k, "tiny")
-    check_attn(o3, l3, ref["o_swa"], ref["lse_swa"], "tiny swa")
-    check_attn(o2, l2, ref["o_hca"], ref["lse_hca"], "tiny hca")
+    check_attn(o3, l3, ref["o_swa"], ref["lse_swa"], "tiny swa", storage="bf16")
+    check_attn(o2, l2, ref["o_hca"], ref["lse_hca"], "tiny hca", storage="bf16")
     check_attn(out, lse, ref["out"], ref["lse"], "tiny layer")
     assert L == 256

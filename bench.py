@@ -178,13 +178,22 @@ def barrier(world):
 
 
 def max_over_ranks(world, x):
+    """Largest x over the ranks (the job time is the slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world, units_per_rank, local_ms):
+    """Whole-job throughput: the units every rank processed divided by the
+    slowest rank's time.  Returns (units per second, max ms)."""
+    ms = max_over_ranks(world, local_ms)
+    return units_per_rank * world / (ms / 1e3), ms
 
 
 # ---------------------------------------------------------------- CPU oracle sample
@@ -379,11 +388,8 @@ def run_ours(args, world, rank, local):
     clocks = sampler.stop()
     hattn.check_status()
 
-    total_ms = step_ev[0].elapsed_time(step_ev[K])
-    total_ms = max_over_ranks(world, total_ms)
+    value, total_ms = job_throughput(world, wl.B * wl.T * K, step_ev[0].elapsed_time(step_ev[K]))
     ms_step = total_ms / K
-    tokens = wl.B * wl.T * K * world
-    value = tokens / (total_ms / 1e3)
     per_kernel = {n: statistics.mean(kev[i][n][0].elapsed_time(kev[i][n][1]) for i in range(K))
                   for n in names}
 
@@ -461,11 +467,11 @@ def run_e2e(args, world, layer, inp, wl, t_new, stream):
     g.replay()
     torch.cuda.synchronize()
     barrier(world)
-    ms = max_over_ranks(world, ev[0].elapsed_time(ev[1]))
+    e2e_value, ms = job_throughput(world, wl.B * wl.T * K, ev[0].elapsed_time(ev[1]))
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + sum(
         t.numel() * t.element_size() for t in tok.values())
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-    return {"value": wl.B * wl.T * K * world / (ms / 1e3), "unit": "tokens/s",
+    return {"value": e2e_value, "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / K}
 
 

@@ -1,6 +1,7 @@
 // abi.cu -- the extern "C" entry points of libhattn (declared in
 // include/hattn.h): argument validation, launch planning, TMA descriptor
 // encoding, kernel launches, and the device status word.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -126,7 +127,8 @@ int make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims,
   } while (0)
 
 int check_rope(int D, int r, float rope_base, float eps) {
-  REQUIRE(r >= 0 && r % 2 == 0 && r <= D && r <= 128, "r=%d must be even, <= D and <= 128", r);
+  REQUIRE(r >= 0 && r % 2 == 0 && r <= D && r <= 2 * kMaxRopePairs,
+          "r=%d must be even, <= D and <= %d", r, 2 * kMaxRopePairs);
   REQUIRE(rope_base > 0.f, "rope_base must be positive");
   REQUIRE(eps >= 0.f, "eps must be >= 0");
   return HATTN_OK;
@@ -173,8 +175,8 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
   a.N_cap = N_cap;
   a.j_begin = j_begin;
   a.j_end = j_end;
-  a.rope_base = rope_base;
   a.eps = eps;
+  make_rope_coef(rope_base, r, &a.rope);
   cudaError_t e = launch_compress(a, num_sms_or_default(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
   return ok();
@@ -214,13 +216,22 @@ int attn_common(int kind, const void* q, const float* gamma_q, const void* kv,
   }
   int* status = nullptr;
   if (!device_info(nullptr, &status, nullptr)) return fail(HATTN_ERR_CUDA, "no CUDA device");
-  CUtensorMap tm;
+  CUtensorMap tm, tm_q;
   memset(&tm, 0, sizeof tm);
-  if (kind == kHca) {
+  if (kind != kSparse) {
+    // HCA entries / SWA raw tokens: 64 rows x 64 dims per copy
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)N_rows};
     const uint64_t strides[1] = {(uint64_t)D * 2};
     const uint32_t box[2] = {64, 64};
-    rc = make_tmap(&tm, kv, 2, dims, strides, box, "kv_h");
+    rc = make_tmap(&tm, kv, 2, dims, strides, box, kind == kHca ? "kv_h" : "kv_raw");
+    if (rc) return rc;
+  }
+  {
+    // query rows of a row block: 128 rows x 64 dims per copy
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)T * (uint64_t)H};
+    const uint64_t strides[1] = {(uint64_t)D * 2};
+    const uint32_t box[2] = {64, 128};
+    rc = make_tmap(&tm_q, q, 2, dims, strides, box, "q");
     if (rc) return rc;
   }
   AttnArgs a;
@@ -247,16 +258,16 @@ int attn_common(int kind, const void* q, const float* gamma_q, const void* kv,
   a.k = k;
   a.m = m;
   a.W = W;
-  a.rope_base = rope_base;
   a.eps = eps;
   a.scale = scale;
+  make_rope_coef(rope_base, r, &a.rope);
   a.G = p.G;
   a.n_rb = p.n_rb;
   a.nsplit = p.nsplit;
   a.keys_per_split = p.keys_per_split;
   a.nds = p.nds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_attention(tm, a, p, st);
+  cudaError_t e = launch_attention(tm, tm_q, a, p, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (p.nsplit > 1) {
     CombineArgs c;
@@ -274,6 +285,24 @@ int attn_common(int kind, const void* q, const float* gamma_q, const void* kv,
 }
 
 }  // namespace
+
+namespace hattn {
+
+void make_rope_coef(double base, int r, RopeCoef* rc) {
+  memset(rc, 0, sizeof *rc);
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < r / 2 && i < kMaxRopePairs; ++i) {
+    const double theta = pow(base, -2.0 * i / static_cast<double>(r));
+    const double f = theta / two_pi;           // turns per position
+    const double g = fmod(4096.0 * f, 1.0);    // turns per 4096 positions, reduced
+    rc->c[0][i] = static_cast<float>(f);
+    rc->c[1][i] = static_cast<float>(f - static_cast<double>(rc->c[0][i]));
+    rc->c[2][i] = static_cast<float>(g);
+    rc->c[3][i] = static_cast<float>(g - static_cast<double>(rc->c[2][i]));
+  }
+}
+
+}  // namespace hattn
 
 extern "C" {
 
@@ -481,7 +510,8 @@ int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int
   REQUIRE_F32(lse_out);
   REQUIRE(B >= 1 && T >= 1 && H >= 1, "B, T and H must be >= 1");
   REQUIRE(D >= 8 && D <= 4096 && D % 8 == 0, "D=%d must be a multiple of 8 in [8, 4096]", D);
-  REQUIRE(r >= 0 && r % 2 == 0 && r <= D && r <= 512, "r=%d must be even, <= D and <= 512", r);
+  REQUIRE(r >= 0 && r % 2 == 0 && r <= D && r <= 2 * kMaxRopePairs,
+          "r=%d must be even, <= D and <= %d", r, 2 * kMaxRopePairs);
   REQUIRE(rope_base > 0.f, "rope_base must be positive");
   a.nb = nb;
   a.sink = sink;
@@ -493,7 +523,7 @@ int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int
   a.H = H;
   a.D = D;
   a.r = r;
-  a.rope_base = rope_base;
+  make_rope_coef(rope_base, r, &a.rope);
   cudaError_t e = launch_merge(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return ok();

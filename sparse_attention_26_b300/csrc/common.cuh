@@ -91,6 +91,72 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// ----------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Whole-cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster, releasing this
+// thread's earlier writes (including remote shared-memory stores).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on a local mbarrier whose arrivals come from other CTAs of
+// the cluster (acquire at cluster scope); same contract as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, int* status,
+                                                  uint64_t limit_ns = kWaitLimitNs, int site = 1) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((++spins & 63u) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        record_status(status, kStatusTimeout, site);
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -98,6 +164,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns the AND of `v` over the participating
+// threads, so a group can agree on leaving a loop that contains barriers.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ----------------------------------------------------------------- TMA
@@ -252,16 +333,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// RoPE angle for position p and pair i of r: p * base^(-2i/r), reduced to
-// [-pi, pi] in fp64 with one round-to-nearest multiple of 2*pi (the product
-// and the reduction are exact to ~1e-10 rad for p < 2^31), then sin/cos in
-// fp32 of the small reduced angle.
-__device__ __forceinline__ void rope_sincos(double theta, int64_t p, float* s, float* c) {
-  const double two_pi = 6.283185307179586476925286766559;
-  double phi = static_cast<double>(p) * theta;
-  double n = rint(phi / two_pi);
-  double red = fma(-n, two_pi, phi);
-  sincosf(static_cast<float>(red), s, c);
+// RoPE coefficients of one call, computed on the host in fp64: for pair i,
+// the frequency theta_i = base^(-2i/r) in turns per position,
+//   f_i = theta_i / (2 pi)            as the float pair (fa, fb),
+//   g_i = frac(4096 f_i)              as the float pair (ga, gb).
+// B300 runs fp64 at a small fraction of its fp32 rate, so the angle is
+// reduced on the device in fp32 only (rope_cs).
+constexpr int kMaxRopePairs = 64;
+struct RopeCoef {
+  float c[4][kMaxRopePairs];  // fa, fb, ga, gb
+};
+
+// cos / sin of the RoPE angle p * theta_i for |p| < 2^31.  With
+// p = 4096 ph + pl, p f_i = ph g_i + pl f_i (mod 1); each product is split
+// into its rounded value and exact error (fmaf), the integer parts are
+// dropped exactly, and the fraction of a turn left, accurate to about 1e-7
+// turns at any position, goes to sincospif.  The _rn intrinsics keep the
+// compiler from contracting the products into other operations.
+__device__ __forceinline__ void rope_cs(const float (*rc)[kMaxRopePairs], int i, int64_t p,
+                                        float* sn, float* cs) {
+  const uint32_t ap = static_cast<uint32_t>(p < 0 ? -p : p);
+  const float ph = static_cast<float>(ap >> 12);
+  const float pl = static_cast<float>(ap & 4095u);
+  const float fa = rc[0][i], fb = rc[1][i], ga = rc[2][i], gb = rc[3][i];
+  const float x1 = __fmul_rn(ph, ga);
+  const float e1 = fmaf(ph, ga, -x1);
+  const float x2 = __fmul_rn(pl, fa);
+  const float e2 = fmaf(pl, fa, -x2);
+  float t = __fadd_rn(__fsub_rn(x1, rintf(x1)), __fsub_rn(x2, rintf(x2)));
+  const float small = __fadd_rn(__fadd_rn(e1, e2), fmaf(ph, gb, __fmul_rn(pl, fb)));
+  t = __fadd_rn(t, small);
+  t = __fsub_rn(t, rintf(t));
+  float s, c;
+  sincospif(2.f * t, &s, &c);
+  *sn = p < 0 ? -s : s;
+  *cs = c;
 }
 
 }  // namespace hattn

@@ -47,10 +47,11 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&y)[8]) {
   *reinterpret_cast<uint4*>(p) = u;
 }
 
-__global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs a) {
+__global__ void __launch_bounds__(kCompressThreads)
+    compress_kernel(const __grid_constant__ CompressArgs a) {
   __shared__ float alpha[kMaxW];
   __shared__ float partial[2048];  // S x (D + dI) floats, S*(NC) <= 256 -> <= 2048
-  __shared__ double theta[256];
+  __shared__ float rc[4][kMaxRopePairs];
   __shared__ float red[kCompressThreads / 32];
   __shared__ float inv_rms_s;
 
@@ -61,8 +62,10 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
   const int S = kCompressThreads / NC;     // token slices
   const int width = NC * 8;
 
-  for (int i = tid; i < a.r / 2; i += kCompressThreads)
-    theta[i] = pow(static_cast<double>(a.rope_base), -2.0 * i / static_cast<double>(a.r));
+  for (int i = tid; i < a.r / 2; i += kCompressThreads) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) rc[c][i] = a.rope.c[c][i];
+  }
 
   const int64_t nj = a.j_end - a.j_begin;
   const int64_t items = nj * a.B;
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(kCompressThreads) compress_kernel(CompressArgs
         const int d = tid * 8 + e;
         if (d >= d0) {
           float sn, cs;
-          rope_sincos(theta[(d - d0) / 2], p, &sn, &cs);
+          rope_cs(rc, (d - d0) / 2, p, &sn, &cs);
           const float x0 = y[e], x1 = y[e + 1];
           y[e] = x0 * cs - x1 * sn;
           y[e + 1] = x0 * sn + x1 * cs;

@@ -41,7 +41,7 @@ struct IdxSmem {
   // per epilogue warp (no cross-warp barrier): visible entries per query of
   // the current group, and the head weight of every accumulator column
   int nt[4][256];
-  float wcol[4][256];
+  alignas(16) float wcol[4][256];
 };
 
 __device__ __forceinline__ int64_t visible_entries(int32_t t, int m, int64_t cap) {
@@ -49,30 +49,50 @@ __device__ __forceinline__ int64_t visible_entries(int32_t t, int m, int64_t cap
   return n < cap ? n : cap;
 }
 
-// Slot decoding shared by all roles.
-struct SlotInfo {
-  int64_t group;   // global group index = b * groups_per_seq + gq
-  int b, t0, gv, blk;
-};
+// Walks this CTA's slots in order.  Every role runs the same cursor, so all
+// of them skip the same blocks; the 64-bit divisions happen only when the
+// query group changes, never per slot.
+struct SlotCursor {
+  int64_t slot, end;
+  int64_t group;   // b * groups_per_seq + query group within the sequence
+  int blk;         // 128-entry block within the sequence
+  int b, t0, gv;
+  int64_t nmax;    // largest visible-entry count among the group's queries
 
-__device__ __forceinline__ SlotInfo decode_slot(const IndexerArgs& a, int64_t slot) {
-  SlotInfo s;
-  s.group = slot / a.nblk;
-  s.blk = static_cast<int>(slot % a.nblk);
-  s.b = static_cast<int>(s.group / a.groups_per_seq);
-  s.t0 = static_cast<int>(s.group % a.groups_per_seq) * a.G;
-  s.gv = min(a.G, a.T - s.t0);
-  return s;
-}
-
-__device__ __forceinline__ int64_t group_nmax(const IndexerArgs& a, const SlotInfo& s) {
-  int64_t n = 0;
-  for (int g = 0; g < s.gv; ++g) {
-    int64_t v = visible_entries(a.pos[(int64_t)s.b * a.T + s.t0 + g], a.m, a.N_cap);
-    n = v > n ? v : n;
+  __device__ __forceinline__ void load_group(const IndexerArgs& a) {
+    b = static_cast<int>(group / a.groups_per_seq);
+    t0 = static_cast<int>(group - static_cast<int64_t>(b) * a.groups_per_seq) * a.G;
+    gv = min(a.G, a.T - t0);
+    nmax = 0;
+    for (int g = 0; g < gv; ++g) {
+      const int64_t v = visible_entries(a.pos[(int64_t)b * a.T + t0 + g], a.m, a.N_cap);
+      nmax = v > nmax ? v : nmax;
+    }
   }
-  return n;
-}
+  __device__ __forceinline__ void init(const IndexerArgs& a, int64_t s0, int64_t s1) {
+    slot = s0;
+    end = s1;
+    group = s0 / a.nblk;
+    blk = static_cast<int>(s0 - group * a.nblk);
+    if (slot < end) load_group(a);
+  }
+  __device__ __forceinline__ bool live() const {
+    return static_cast<int64_t>(blk) * kBlockRows < nmax;
+  }
+  // next slot; a dead block ends its group (the later blocks are dead too)
+  __device__ __forceinline__ void advance(const IndexerArgs& a) {
+    if (!live()) {
+      slot += a.nblk - 1 - blk;
+      blk = a.nblk - 1;
+    }
+    ++slot;
+    if (++blk == a.nblk) {
+      blk = 0;
+      ++group;
+      if (slot < end) load_group(a);
+    }
+  }
+};
 
 __global__ void __launch_bounds__(kIdxThreads, 1)
     indexer_score_kernel(const __grid_constant__ CUtensorMap tm_ik,
@@ -121,36 +141,40 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   const uint32_t tmem = sm->tmem_base;
   volatile int* abort = &sm->abort;
 
+  // Ring positions are tracked as (stage, phase) pairs advanced by one per
+  // use, so the loops below divide nothing per slot.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int64_t it = 0, qloads = 0, loaded = -1, cur = -1, nmax = 0;
-      for (int64_t slot = s0; slot < s1 && !*abort; ++slot) {
-        SlotInfo s = decode_slot(a, slot);
-        if (s.group != cur) { cur = s.group; nmax = group_nmax(a, s); }
-        if (static_cast<int64_t>(s.blk) * kBlockRows >= nmax) continue;
-        if (s.group != loaded) {
+      SlotCursor cur;
+      int st = 0;
+      uint32_t ph = 0;
+      int64_t it = 0, qloads = 0, loaded = -1;
+      for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
+        if (!cur.live()) continue;
+        if (cur.group != loaded) {
           if (qloads > 0 &&
               !mbar_wait(smem_u32(&sm->qempty), (qloads - 1) & 1, abort, a.status, kWaitLimitNs, 10))
             break;
           const uint32_t qb = smem_u32(&sm->qfull);
           mbar_arrive_expect_tx(qb, q_bytes);
-          const int row0 = ((s.b * a.T) + s.t0) * a.HI;
+          const int row0 = ((cur.b * a.T) + cur.t0) * a.HI;
           for (int kc = 0; kc < a.KC; ++kc)
             tma_load_2d(smem_u32(sQ + kc * a.NQ * 128), &tm_iq, kc * 64, row0, qb);
           ++qloads;
-          loaded = s.group;
+          loaded = cur.group;
         }
-        const int st = static_cast<int>(it % a.stages);
+        // stage st was last filled `stages` uses ago, in phase ph ^ 1
         if (it >= a.stages &&
-            !mbar_wait(smem_u32(&sm->empty[st]), ((it / a.stages) + 1) & 1, abort, a.status, kWaitLimitNs, 11))
+            !mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 11))
           break;
         const uint32_t fb = smem_u32(&sm->full[st]);
         mbar_arrive_expect_tx(fb, stage_bytes);
         for (int kc = 0; kc < a.KC; ++kc)
           tma_load_3d(smem_u32(sA + st * stage_bytes + kc * 16384), &tm_ik, kc * 64,
-                      s.blk * kBlockRows, s.b, fb);
+                      cur.blk * kBlockRows, cur.b, fb);
         ++it;
+        if (++st == a.stages) { st = 0; ph ^= 1u; }
       }
       if (*abort) {
         // let the copies already issued land before the CTA exits
@@ -164,23 +188,24 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, a.NQ, 0, 0);
-      int64_t it = 0, qn = 0, loaded = -1, cur = -1, nmax = 0;
-      for (int64_t slot = s0; slot < s1 && !*abort; ++slot) {
-        SlotInfo s = decode_slot(a, slot);
-        if (s.group != cur) { cur = s.group; nmax = group_nmax(a, s); }
-        if (static_cast<int64_t>(s.blk) * kBlockRows >= nmax) continue;
-        if (s.group != loaded) {
+      SlotCursor cur;
+      int st = 0;
+      uint32_t ph = 0;
+      int64_t it = 0, qn = 0, loaded = -1;
+      for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
+        if (!cur.live()) continue;
+        if (cur.group != loaded) {
           if (qn > 0) mma_commit(smem_u32(&sm->qempty));  // previous group's reads of sQ done
           if (!mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 13)) break;
           ++qn;
-          loaded = s.group;
+          loaded = cur.group;
         }
         const int acc = static_cast<int>(it & 1);
         if (it >= 2 &&
-            !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> 1) + 1) & 1, abort, a.status, kWaitLimitNs, 14))
+            !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> 1) + 1) & 1, abort, a.status,
+                       kWaitLimitNs, 14))
           break;
-        const int st = static_cast<int>(it % a.stages);
-        if (!mbar_wait(smem_u32(&sm->full[st]), (it / a.stages) & 1, abort, a.status, kWaitLimitNs, 15)) break;
+        if (!mbar_wait(smem_u32(&sm->full[st]), ph, abort, a.status, kWaitLimitNs, 15)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * a.NQ;
         for (int kc = 0; kc < a.KC; ++kc) {
@@ -196,6 +221,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         mma_commit(smem_u32(&sm->empty[st]));
         mma_commit(smem_u32(&sm->tfull[acc]));
         ++it;
+        if (++st == a.stages) { st = 0; ph ^= 1u; }
       }
       // all issued MMAs complete before the accumulators are released
       mma_commit(smem_u32(&sm->mma_done));
@@ -207,46 +233,83 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     const int row = quad * 32 + lane;
     float* wcol = sm->wcol[quad];
     int* ntv = sm->nt[quad];
-    int64_t it = 0, cur = -1, nmax = 0, wgroup = -1;
-    for (int64_t slot = s0; slot < s1 && !*abort; ++slot) {
-      SlotInfo s = decode_slot(a, slot);
-      if (s.group != cur) { cur = s.group; nmax = group_nmax(a, s); }
-      if (static_cast<int64_t>(s.blk) * kBlockRows >= nmax) continue;
-      if (s.group != wgroup) {
+    // heads a multiple of 32: every 32-column accumulator chunk belongs to
+    // one query, so a query's score is a straight sum over its chunks
+    const bool whole = (a.HI & 31) == 0;
+    const int cpq = a.HI >> 5;
+    SlotCursor cur;
+    int64_t it = 0, wgroup = -1;
+    for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
+      if (!cur.live()) continue;
+      if (cur.group != wgroup) {
         __syncwarp();
         for (int c = lane; c < a.NQ; c += 32) {
           const int g = c / a.HI, h = c % a.HI;
-          wcol[c] = (g < s.gv) ? a.w[((int64_t)s.b * a.T + s.t0 + g) * a.HI + h] : 0.f;
+          wcol[c] = (g < cur.gv) ? a.w[((int64_t)cur.b * a.T + cur.t0 + g) * a.HI + h] : 0.f;
         }
         for (int g = lane; g < a.G; g += 32)
-          ntv[g] = g < s.gv ? static_cast<int>(visible_entries(
-                                  a.pos[(int64_t)s.b * a.T + s.t0 + g], a.m, a.N_cap))
-                            : 0;
+          ntv[g] = g < cur.gv ? static_cast<int>(visible_entries(
+                                    a.pos[(int64_t)cur.b * a.T + cur.t0 + g], a.m, a.N_cap))
+                              : 0;
         __syncwarp();
-        wgroup = s.group;
+        wgroup = cur.group;
       }
       const int acc = static_cast<int>(it & 1);
       const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), (it >> 1) & 1, abort, a.status,
                                  kWaitLimitNs, 17);
       if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: tcgen05.ld follows
       tc_fence_after();
-      const int64_t j = static_cast<int64_t>(s.blk) * kBlockRows + row;
+      const int64_t j = static_cast<int64_t>(cur.blk) * kBlockRows + row;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * a.NQ;
-      float sum = 0.f;
-      int g = 0, h = 0;
-      for (int cc = 0; cc < a.NQ; cc += 32) {
-        float x[32];
-        tmem_ld32(taddr + cc, x);
-        tmem_wait_ld();
+      float* srow = a.scores + ((int64_t)cur.b * a.T + cur.t0) * a.N_cap + j;
+      if (whole) {
+        for (int g = 0; g < cur.gv; ++g) {
+          float sum = 0.f;
+          for (int c = 0; c < cpq; c += 2) {
+            const int col = (g * cpq + c) * 32;
+            float x0[32], x1[32];
+            tmem_ld32(taddr + col, x0);
+            if (c + 1 < cpq) tmem_ld32(taddr + col + 32, x1);
+            tmem_wait_ld();
+            const float4* w0 = reinterpret_cast<const float4*>(wcol + col);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sum = fmaf(wcol[cc + i], fmaxf(x[i], 0.f), sum);
-          if (++h == a.HI) {
-            if (g < s.gv && j < ntv[g])
-              a.scores[(((int64_t)s.b * a.T) + s.t0 + g) * a.N_cap + j] = sum;
-            sum = 0.f;
-            h = 0;
-            ++g;
+            for (int i = 0; i < 8; ++i) {
+              const float4 wv = w0[i];
+              sum = fmaf(wv.x, fmaxf(x0[4 * i], 0.f), sum);
+              sum = fmaf(wv.y, fmaxf(x0[4 * i + 1], 0.f), sum);
+              sum = fmaf(wv.z, fmaxf(x0[4 * i + 2], 0.f), sum);
+              sum = fmaf(wv.w, fmaxf(x0[4 * i + 3], 0.f), sum);
+            }
+            if (c + 1 < cpq) {
+              const float4* w1 = reinterpret_cast<const float4*>(wcol + col + 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 wv = w1[i];
+                sum = fmaf(wv.x, fmaxf(x1[4 * i], 0.f), sum);
+                sum = fmaf(wv.y, fmaxf(x1[4 * i + 1], 0.f), sum);
+                sum = fmaf(wv.z, fmaxf(x1[4 * i + 2], 0.f), sum);
+                sum = fmaf(wv.w, fmaxf(x1[4 * i + 3], 0.f), sum);
+              }
+            }
+          }
+          if (j < ntv[g]) srow[(int64_t)g * a.N_cap] = sum;
+        }
+      } else {
+        float sum = 0.f;
+        int g = 0, h = 0;
+        for (int cc = 0; cc < a.NQ; cc += 32) {
+          float x[32];
+          tmem_ld32(taddr + cc, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            sum = fmaf(wcol[cc + i], fmaxf(x[i], 0.f), sum);
+            if (++h == a.HI) {
+              if (g < cur.gv && j < ntv[g]) srow[(int64_t)g * a.N_cap] = sum;
+              sum = 0.f;
+              h = 0;
+              ++g;
+            }
           }
         }
       }

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace hattn {
 
 // ------------------------------------------------------------ compressor
@@ -19,7 +21,8 @@ struct CompressArgs {
   __nv_bfloat16* ik_out;        // [B][N_cap][dI] or null
   int B, D, dI, m, w, r;
   int64_t L_cap, N_cap, j_begin, j_end;
-  float rope_base, eps;
+  float eps;
+  RopeCoef rope;
 };
 cudaError_t launch_compress(const CompressArgs& a, int num_sms, cudaStream_t stream);
 
@@ -82,7 +85,8 @@ struct AttnArgs {
   int kind, B, T, H, D, r;
   int64_t N_rows;               // rows per sequence of kv (N_cap or L_cap)
   int k, m, W;
-  float rope_base, eps, scale;
+  float eps, scale;
+  RopeCoef rope;
   int G;                        // queries per row block
   int n_rb;                     // row blocks per sequence = ceil(T / G)
   int nsplit;                   // key splits
@@ -95,8 +99,8 @@ struct AttnPlan {
 };
 bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int num_sms,
                     AttnPlan* p);
-cudaError_t launch_attention(const CUtensorMap& tm_kv, const AttnArgs& a, const AttnPlan& p,
-                             cudaStream_t stream);
+cudaError_t launch_attention(const CUtensorMap& tm_kv, const CUtensorMap& tm_q, const AttnArgs& a,
+                             const AttnPlan& p, cudaStream_t stream);
 
 // ------------------------------------------------------------ merges
 struct CombineArgs {
@@ -118,9 +122,12 @@ struct MergeArgs {
   __nv_bfloat16* out;
   float* lse_out;       // or null
   int B, T, H, D, r;
-  float rope_base;
+  RopeCoef rope;
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+
+// Host: RoPE coefficients of base^(-2i/r) for i < r/2 (r <= 2 * kMaxRopePairs).
+void make_rope_coef(double base, int r, RopeCoef* rc);
 
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, int* status, cudaStream_t stream);
 

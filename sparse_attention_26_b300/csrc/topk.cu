@@ -10,11 +10,13 @@
 // shared memory (one read of the fp32 scores).  Three radix passes (11, 11,
 // 10 bits, most significant first) find the k-th largest key: every CTA
 // builds a shared-memory histogram of the digit among the keys that still
-// match the prefix, the histograms are summed across the cluster through
-// distributed shared memory, and every CTA scans the sum to pick the digit.
-// The final pass writes every key above the threshold, then the threshold
-// ties in global index order until k are written.  No global atomics, no
-// inter-kernel passes; the result is deterministic.
+// match the prefix and adds its nonzero bins into every CTA's copy of the
+// cluster histogram with remote shared-memory atomics (double-buffered, so
+// one cluster barrier per pass); every CTA then finds the digit with a
+// block-wide suffix scan.  The final pass writes every key above the
+// threshold, then the threshold ties in global index order until k are
+// written.  No global atomics, no inter-kernel passes; the result is
+// deterministic.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -35,13 +37,68 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 struct TopkShared {
   uint32_t hist[kBins];
-  uint32_t ghist[kBins];
+  uint32_t ghist[2][kBins];
   uint32_t warp_tot[32];
   int counts[2];       // keys above the threshold, keys equal to it (this CTA)
+  int offs[2];         // the same counts summed over the lower-ranked CTAs
   int ctr;
   uint32_t digit;
   uint32_t above;
 };
+
+// Inclusive scan over the threads of the block, in thread order; uses
+// sh->warp_tot.  Returns this thread's exclusive prefix.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, TopkShared* sh, int tid,
+                                                         int nthr) {
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += x;
+  }
+  if (lane == 31) sh->warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nthr >> 5;
+    const uint32_t w = lane < nw ? sh->warp_tot[lane] : 0;
+    uint32_t t = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += x;
+    }
+    if (lane < nw) sh->warp_tot[lane] = t - w;
+  }
+  __syncthreads();
+  const uint32_t r = sh->warp_tot[warp] + inc - v;
+  __syncthreads();  // warp_tot is reused by the next scan
+  return r;
+}
+
+// The bin holding the need-th largest key: bins are visited from the top;
+// sh->digit = that bin, sh->above = the keys in the bins above it.
+__device__ __forceinline__ void find_digit(const uint32_t* gh, int nb, uint32_t need,
+                                           TopkShared* sh, int tid, int nthr) {
+  const int bpt = nb / nthr;            // bins per thread (nb >= nthr)
+  const int hi = nb - bpt * tid;        // this thread's bins: [hi - bpt, hi)
+  uint32_t tot = 0;
+  for (int i = 0; i < bpt; ++i) tot += gh[hi - 1 - i];
+  const uint32_t before = block_exclusive_scan(tot, sh, tid, nthr);
+  if (before < need && before + tot >= need) {
+    uint32_t run = before;
+    for (int i = 0; i < bpt; ++i) {
+      const uint32_t c = gh[hi - 1 - i];
+      if (run + c >= need) {
+        sh->digit = static_cast<uint32_t>(hi - 1 - i);
+        sh->above = run;
+        break;
+      }
+      run += c;
+    }
+  }
+  __syncthreads();
+}
 
 __global__ void topk_kernel(const TopkArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -72,6 +129,12 @@ __global__ void topk_kernel(const TopkArgs a) {
 
   const float* src = a.scores + static_cast<int64_t>(row) * a.N_cap + start;
   for (int e = tid; e < len; e += nthr) keys[e] = order_key(src[e]);
+  for (int i = tid; i < kBins; i += nthr) {
+    sh->hist[i] = 0;
+    sh->ghist[0][i] = 0;
+    sh->ghist[1][i] = 0;
+  }
+  cluster.sync();  // every copy of the cluster histogram is zero before any add
 
   uint32_t prefix = 0;
   uint32_t need = static_cast<uint32_t>(a.k);
@@ -80,51 +143,27 @@ __global__ void topk_kernel(const TopkArgs a) {
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = shifts[pass];
     const int nb = 1 << widths[pass];
-    for (int i = tid; i < nb; i += nthr) sh->hist[i] = 0;
-    __syncthreads();
+    const int buf = pass & 1;
     for (int e = tid; e < len; e += nthr) {
       const uint32_t key = keys[e];
       if (pass == 0 || (key >> (shift + widths[pass])) == prefix)
         atomicAdd(&sh->hist[(key >> shift) & (nb - 1)], 1u);
     }
-    cluster.sync();
-    // this CTA sums its share of the bins over the cluster and broadcasts it
-    const int per = nb / C;
-    for (int i = tid; i < per; i += nthr) {
-      const int bin = rank * per + i;
-      uint32_t s = 0;
-      for (int q = 0; q < C; ++q) s += cluster.map_shared_rank(sh->hist, q)[bin];
-      for (int q = 0; q < C; ++q) cluster.map_shared_rank(sh->ghist, q)[bin] = s;
-    }
-    cluster.sync();
-    if (tid < 32) {
-      // lane L covers the bins [nb - (L+1)*pl, nb - L*pl), scanned from the top
-      const int pl = nb / 32;
-      uint32_t tot = 0;
-      for (int i = 0; i < pl; ++i) tot += sh->ghist[nb - tid * pl - 1 - i];
-      uint32_t inc = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-        if (tid >= o) inc += v;
-      }
-      const unsigned ball = __ballot_sync(0xffffffffu, inc >= need);
-      const int L = __ffs(ball) - 1;
-      if (tid == L) {
-        uint32_t run = inc - tot;
-        for (int i = 0; i < pl; ++i) {
-          const int bin = nb - tid * pl - 1 - i;
-          const uint32_t c = sh->ghist[bin];
-          if (run + c >= need) {
-            sh->digit = static_cast<uint32_t>(bin);
-            sh->above = run;
-            break;
-          }
-          run += c;
-        }
-      }
-    }
     __syncthreads();
+    // add this CTA's nonzero bins into every CTA's copy; reset the local bins
+    for (int bin = tid; bin < nb; bin += nthr) {
+      const uint32_t v = sh->hist[bin];
+      if (v) {
+        for (int q = 0; q < C; ++q) atomicAdd(cluster.map_shared_rank(&sh->ghist[buf][bin], q), v);
+        sh->hist[bin] = 0;
+      }
+    }
+    // the other copy was last scanned by this CTA in the previous pass; the
+    // next adds into it come after the cluster barrier below
+    if (pass < 2)
+      for (int i = tid; i < kBins; i += nthr) sh->ghist[buf ^ 1][i] = 0;
+    cluster.sync();
+    find_digit(sh->ghist[buf], nb, need, sh, tid, nthr);
     prefix = (prefix << widths[pass]) | sh->digit;
     need -= sh->above;
   }
@@ -144,12 +183,27 @@ __global__ void topk_kernel(const TopkArgs a) {
   if (gt) atomicAdd(&sh->counts[0], gt);
   if (eq) atomicAdd(&sh->counts[1], eq);
   cluster.sync();
-  int off_gt = 0, off_eq = 0;
-  for (int q = 0; q < rank; ++q) {
-    const int* rc = cluster.map_shared_rank(sh->counts, q);
-    off_gt += rc[0];
-    off_eq += rc[1];
+  if (tid < 32) {
+    // counts of the lower-ranked CTAs, summed by one warp
+    int g = 0, e = 0;
+    if (tid < rank) {
+      const int* rc = cluster.map_shared_rank(sh->counts, tid);
+      g = rc[0];
+      e = rc[1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      e += __shfl_xor_sync(0xffffffffu, e, o);
+    }
+    if (tid == 0) {
+      sh->offs[0] = g;
+      sh->offs[1] = e;
+    }
   }
+  __syncthreads();
+  const int off_gt = sh->offs[0];
+  const int off_eq = sh->offs[1];
   // keys above the threshold: any order
   for (int e = tid; e < len; e += nthr) {
     if (keys[e] > thr) {
@@ -163,28 +217,7 @@ __global__ void topk_kernel(const TopkArgs a) {
   const int e1 = min(len, e0 + per_t);
   uint32_t c = 0;
   for (int e = e0; e < e1; ++e) c += keys[e] == thr;
-  uint32_t inc = c;
-  const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  if (lane == 31) sh->warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = nthr >> 5;
-    uint32_t v = lane < nw ? sh->warp_tot[lane] : 0;
-    uint32_t s = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t x = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += x;
-    }
-    if (lane < nw) sh->warp_tot[lane] = s - v;  // exclusive
-  }
-  __syncthreads();
-  uint32_t rnk = static_cast<uint32_t>(off_eq) + sh->warp_tot[warp] + (inc - c);
+  uint32_t rnk = static_cast<uint32_t>(off_eq) + block_exclusive_scan(c, sh, tid, nthr);
   const int base = a.k - static_cast<int>(need);
   for (int e = e0; e < e1 && rnk < need; ++e) {
     if (keys[e] == thr) {

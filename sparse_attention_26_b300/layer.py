@@ -29,9 +29,12 @@ class HybridLayer:
         self.N_csa = L // wl.m_csa
         self.N_hca = max(1, L // wl.m_hca)
         bf = torch.bfloat16
-        self.kv_c = torch.zeros((B, self.N_csa, D), dtype=bf, device=device)
-        self.ik_c = torch.zeros((B, self.N_csa, wl.dI), dtype=bf, device=device)
-        self.kv_h = torch.zeros((B, self.N_hca, D), dtype=bf, device=device)
+        # only the caches of the branches this layer runs
+        n_c = self.N_csa if "csa" in wl.branches else 1
+        n_h = self.N_hca if "hca" in wl.branches else 1
+        self.kv_c = torch.zeros((B, n_c, D), dtype=bf, device=device)
+        self.ik_c = torch.zeros((B, n_c, wl.dI), dtype=bf, device=device)
+        self.kv_h = torch.zeros((B, n_h, D), dtype=bf, device=device)
         if build_caches:
             self.build_caches()
         self._bufs = {}
@@ -40,10 +43,11 @@ class HybridLayer:
         """Compress every complete entry of the raw caches (cache build)."""
         wl, r = self.wl, self.raw
         L = self.L if n_tokens is None else n_tokens
-        hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=0,
-                           j_end=L // wl.m_csa, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c,
-                           ik_c=self.ik_c)
-        if L // wl.m_hca > 0:
+        if "csa" in wl.branches:
+            hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=0,
+                               j_end=L // wl.m_csa, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c,
+                               ik_c=self.ik_c)
+        if "hca" in wl.branches and L // wl.m_hca > 0:
             hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=0, j_end=L // wl.m_hca,
                                m=wl.m_hca, kv_h=self.kv_h)
 
@@ -55,7 +59,8 @@ class HybridLayer:
         H = wl.H
         bf = torch.bfloat16
         b = dict(
-            scores=torch.empty((B, T, self.N_csa), dtype=torch.float32, device=dev),
+            scores=torch.empty((B, T, self.N_csa if "csa" in wl.branches else 1),
+                               dtype=torch.float32, device=dev),
             idx=torch.empty((B, T, wl.k), dtype=torch.int32, device=dev),
             out=torch.empty((B, T, H, D), dtype=bf, device=dev),
             lse=torch.empty((B, T, H), dtype=torch.float32, device=dev),
@@ -87,7 +92,7 @@ class HybridLayer:
         ev("compress", 0)
         if t_new is not None:
             for m, w_, kind in [(wl.m_csa, wl.w_csa, "csa"), (wl.m_hca, wl.m_hca, "hca")]:
-                if (t_new + 1) % m == 0:
+                if kind in wl.branches and (t_new + 1) % m == 0:
                     j = (t_new + 1) // m - 1
                     if kind == "csa":
                         hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r,
@@ -136,7 +141,8 @@ class HybridLayer:
         wl, B, D, H = self.wl, self.B, self.D, self.wl.H
         n = 1  # merge
         if t_new is not None:
-            n += int((t_new + 1) % wl.m_csa == 0) + int((t_new + 1) % wl.m_hca == 0)
+            n += int("csa" in wl.branches and (t_new + 1) % wl.m_csa == 0)
+            n += int("hca" in wl.branches and (t_new + 1) % wl.m_hca == 0)
         for name, kind, nk in [("csa", hattn.KIND_SPARSE, wl.k), ("hca", hattn.KIND_HCA, self.N_hca),
                                ("swa", hattn.KIND_SWA, wl.W)]:
             if name in wl.branches:

@@ -271,14 +271,21 @@ def test_lazy_rescale_path():
 
 
 # ------------------------------------------------------------------ merge
-@pytest.mark.parametrize("nb,with_sink", [(3, True), (2, False), (1, True)])
-def test_lse_merge(nb, with_sink):
+@pytest.mark.parametrize("nb,with_sink,pos_list", [
+    (3, True, [5, 77, 1 << 20, 3, 9, 123456]),
+    (2, False, [5, 77, 1 << 20, 3, 9, 123456]),
+    (1, True, [5, 77, 1 << 20, 3, 9, 123456]),
+    # inverse RoPE at positions far beyond the cached context: the angle
+    # reduction must stay exact up to the largest int32 position
+    (2, True, [(1 << 31) - 1, (1 << 30) + 12345, (1 << 24) + 1, 4095, 4096, (1 << 28) - 3]),
+])
+def test_lse_merge(nb, with_sink, pos_list):
     B, T, H, D, r = 2, 3, 16, 512, 64
     os_ = [randn_bf16((B, T, H, D), 80 + i) for i in range(nb)]
     ls = [randn_f32((B, T, H), 90 + i) * 3 for i in range(nb)]
     ls[0][0, 0, 0] = -float("inf")  # an empty branch row
     sink = randn_f32((H,), 99) if with_sink else None
-    pos = _pos(B, T, [5, 77, 1 << 20, 3, 9, 123456])
+    pos = _pos(B, T, pos_list)
     out, lse = hattn.lse_merge([o.to(DEV) for o in os_], [l.to(DEV) for l in ls], pos.to(DEV),
                                r=r, sink=sink.to(DEV) if sink is not None else None)
     ro, rl = orc.merge([f64(o) for o in os_], [f64(l) for l in ls],

@@ -17,8 +17,8 @@
  *     aligned (HATTN_ERR_MISALIGNED otherwise).
  *   - Shapes use: B sequences, T queries per sequence, H query heads, D head
  *     dim (= the shared KV latent dim, a multiple of 64, at most 512), r RoPE
- *     dims (the last r of each vector, even, r <= D), HI indexer heads, dI
- *     indexer dim (a multiple of 8, at most 128), W SWA window.
+ *     dims (the last r of each vector, even, r <= D, r <= 128), HI indexer
+ *     heads, dI indexer dim (a multiple of 8, at most 128), W SWA window.
  *   - `pos` is an int32 device array [B][T] of absolute query positions.  A
  *     query at position t has its own token already in the raw cache.
  *   - RoPE rotates interleaved pairs (D-r+2i, D-r+2i+1) by the angle
@@ -128,30 +128,50 @@ HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, 
                                 hattn_stream_t stream);
 
 /* -------------------------------------------------------------------------
+ * Query preparation.  [AT] "Design overview": RMSNorm on the queries;
+ * provenance 16: RoPE on the last r dims.  For every (b, t, h):
+ *   q_out = RoPE_pos[b][t](RMSNorm(q; gamma_q, eps))   (bf16)
+ * q, q_out [B][T][H][D] bf16 (may not overlap); gamma_q fp32 [D] or NULL.
+ * The three attention calls accept q_out with q_prepped = 1, so one
+ * preparation serves every branch of a layer.
+ * ---------------------------------------------------------------------- */
+HATTN_API int hattn_query_prep(const void* q, const float* gamma_q, const int32_t* pos, int B,
+                               int T, int H, int D, int r, float rope_base, float eps,
+                               void* q_out, hattn_stream_t stream);
+
+/* -------------------------------------------------------------------------
  * Attention branches.  Shared-KV MQA latent ([AT] "Inference efficiency"):
  * keys and values are the same D-dim vectors K~ for all heads.  Each query
  * head is prepared as q~ = RoPE_pos(RMSNorm(q; gamma_q, eps)); logits are
- * scale * q~ . K~_j; the branch output is o = sum_j softmax_j K~_j (bf16) and
+ * scale * q~ . K~_j; the branch output is o = sum_j softmax_j K~_j (fp32) and
  * lse = log sum_j exp(logit_j) (fp32, natural log).  An empty key set gives
- * o = 0, lse = -inf.
+ * o = 0, lse = -inf.  Branch outputs stay fp32 so the merge rounds to bf16
+ * once.
  *
- *   q [B][T][H][D] bf16, o [B][T][H][D] bf16, lse [B][T][H] fp32.
- *   workspace: at least hattn_attn_workspace_bytes(kind, ...) bytes (split-KV
- *   partials); contents need no initialisation.  H <= 128.
+ *   q [B][T][H][D] bf16: raw queries (q_prepped = 0; the call prepares them
+ *   into its workspace with gamma_q and eps), or the output of
+ *   hattn_query_prep (q_prepped = 1; gamma_q and eps are then not used for
+ *   the queries).  o [B][T][H][D] fp32, lse [B][T][H] fp32.
+ *   workspace: at least hattn_attn_workspace_bytes(kind, ..., q_prepped)
+ *   bytes (prepared queries, then split-KV partials); contents need no
+ *   initialisation.  H <= 128; D a multiple of 64 up to 512 (a multiple of
+ *   128 above 256).
  * ---------------------------------------------------------------------- */
 
 /* CSA branch ([DD]: sparse attention over the selected compressed entries):
  * keys are kv_c[b][idx[b][t][i]] for every i with idx >= 0 (-1 is padding).
  * kv_c [B][N_cap][D] bf16 (normalised + roped entries), idx [B][T][k] int32.
  * An idx >= N_cap is skipped and reported as HATTN_ERR_DEVICE_INDEX. */
-HATTN_API int hattn_sparse_attn(const void* q, const float* gamma_q, const void* kv_c, const int32_t* idx,
+HATTN_API int hattn_sparse_attn(const void* q, const float* gamma_q, int q_prepped,
+                      const void* kv_c, const int32_t* idx,
                       const int32_t* pos, int B, int T, int H, int D, int64_t N_cap, int k, int r,
                       float rope_base, float eps, float scale, void* o, float* lse,
                       void* workspace, size_t ws_bytes, hattn_stream_t stream);
 
 /* HCA branch ([DD]: dense global attention over the 128:1 compressed KV):
  * keys are kv_h[b][j] for j < min(floor((pos+1)/m), N_cap).  kv_h [B][N_cap][D]. */
-HATTN_API int hattn_hca_attn(const void* q, const float* gamma_q, const void* kv_h, const int32_t* pos,
+HATTN_API int hattn_hca_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_h,
+                   const int32_t* pos,
                    int B, int T, int H, int D, int64_t N_cap, int m, int r, float rope_base,
                    float eps, float scale, void* o, float* lse, void* workspace,
                    size_t ws_bytes, hattn_stream_t stream);
@@ -159,21 +179,23 @@ HATTN_API int hattn_hca_attn(const void* q, const float* gamma_q, const void* kv
 /* SWA branch ([DD]: the most recent 128 tokens): keys are the raw tokens
  * u in [max(0, pos-W+1), pos], each RMSNorm'd (gamma_kv, eps) and RoPE'd at
  * position u on load.  kv_raw [B][L_cap][D] bf16. */
-HATTN_API int hattn_swa_attn(const void* q, const float* gamma_q, const void* kv_raw,
+HATTN_API int hattn_swa_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_raw,
                    const float* gamma_kv, const int32_t* pos, int B, int T, int H, int D,
                    int64_t L_cap, int W, int r, float rope_base, float eps, float scale, void* o,
                    float* lse, void* workspace, size_t ws_bytes, hattn_stream_t stream);
 
-/* kind: 0 = CSA sparse (n_keys = k), 1 = HCA (n_keys = N_cap), 2 = SWA (n_keys = W). */
-HATTN_API size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys);
+/* kind: 0 = CSA sparse (n_keys = k), 1 = HCA (n_keys = N_cap), 2 = SWA (n_keys = W).
+ * 0 means no workspace is needed (or no kernel exists for the shape). */
+HATTN_API size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys,
+                                            int q_prepped);
 
 /* -------------------------------------------------------------------------
  * Merge.  [AT] "Spec sheet / Core block": attention sinks; provenance 16:
  * "-i RoPE on outputs".  For every (b, t, h):
  *   Z = sum_i exp(lse_i) + exp(sink[h]);  y = sum_i exp(lse_i) o_i / Z
  *   out = y with its last r dims rotated by -pos (inverse RoPE); lse_out = log Z.
- * o_list / lse_list: HOST arrays of nb (1..4) DEVICE pointers to bf16
- * [B][T][H][D] / fp32 [B][T][H] branch outputs.  sink fp32 [H] device or NULL
+ * o_list / lse_list: HOST arrays of nb (1..4) DEVICE pointers to fp32
+ * [B][T][H][D] / fp32 [B][T][H] branch outputs (16-byte aligned).  sink fp32 [H] device or NULL
  * (no sink term).  out [B][T][H][D] bf16, lse_out [B][T][H] fp32 or NULL.
  * ---------------------------------------------------------------------- */
 HATTN_API int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int nb,

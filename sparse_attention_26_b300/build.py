@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libhattn.so")
-SOURCES = ["abi.cu", "compress.cu", "indexer.cu", "topk.cu", "attention.cu", "merge.cu"]
+SOURCES = ["abi.cu", "compress.cu", "indexer.cu", "topk.cu", "qprep.cu", "attention.cu",
+           "merge.cu"]
 HEADERS = ["common.cuh", "kernels.h", os.path.join("..", "..", "include", "hattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -182,7 +182,41 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
   return ok();
 }
 
-int attn_common(int kind, const void* q, const float* gamma_q, const void* kv,
+// Bytes of the prepared-query copy at the start of an attention workspace
+// (none when the caller passes prepared queries).
+size_t qprep_bytes(int B, int T, int H, int D, int q_prepped) {
+  return q_prepped ? 0 : (size_t)B * T * H * D * 2;
+}
+
+int query_prep_impl(const void* q, const float* gamma_q, const int32_t* pos, int B, int T, int H,
+                    int D, int r, float rope_base, float eps, void* q_out,
+                    hattn_stream_t stream) {
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(pos);
+  REQUIRE_PTR(q_out);
+  REQUIRE_F32(gamma_q);
+  REQUIRE(B >= 1 && T >= 1 && H >= 1, "B, T and H must be >= 1");
+  REQUIRE(D >= 64 && D <= 512 && D % 64 == 0, "D=%d must be a multiple of 64 in [64, 512]", D);
+  int rc = check_rope(D, r, rope_base, eps);
+  if (rc) return rc;
+  QPrepArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.gamma = gamma_q;
+  a.pos = pos;
+  a.q_out = static_cast<__nv_bfloat16*>(q_out);
+  a.B = B;
+  a.T = T;
+  a.H = H;
+  a.D = D;
+  a.r = r;
+  a.eps = eps;
+  make_rope_coef(rope_base, r, &a.rope);
+  cudaError_t e = launch_qprep(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "query prep launch");
+  return HATTN_OK;
+}
+
+int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, const void* kv,
                 const float* gamma_kv, const int32_t* idx, const int32_t* pos, int B, int T, int H,
                 int D, int64_t N_rows, int k, int m, int W, int r, float rope_base, float eps,
                 float scale, void* o, float* lse, void* workspace, size_t ws_bytes,
@@ -210,9 +244,11 @@ int attn_common(int kind, const void* q, const float* gamma_q, const void* kv,
   AttnPlan p;
   if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p))
     return fail(HATTN_ERR_UNSUPPORTED, "no attention kernel for H=%d D=%d", H, D);
-  if (p.ws_bytes > 0) {
+  const size_t qbytes = qprep_bytes(B, T, H, D, q_prepped);
+  const size_t need = qbytes + p.ws_bytes;
+  if (need > 0) {
     REQUIRE_PTR(workspace);
-    REQUIRE(ws_bytes >= p.ws_bytes, "workspace of %zu bytes, need %zu", ws_bytes, p.ws_bytes);
+    REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
   }
   int* status = nullptr;
   if (!device_info(nullptr, &status, nullptr)) return fail(HATTN_ERR_CUDA, "no CUDA device");
@@ -226,24 +262,30 @@ int attn_common(int kind, const void* q, const float* gamma_q, const void* kv,
     rc = make_tmap(&tm, kv, 2, dims, strides, box, kind == kHca ? "kv_h" : "kv_raw");
     if (rc) return rc;
   }
+  // prepared queries: the caller's, or this call's into the workspace
+  const void* qt = q_prepped ? q : workspace;
   {
     // query rows of a row block: 128 rows x 64 dims per copy
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)T * (uint64_t)H};
     const uint64_t strides[1] = {(uint64_t)D * 2};
     const uint32_t box[2] = {64, 128};
-    rc = make_tmap(&tm_q, q, 2, dims, strides, box, "q");
+    rc = make_tmap(&tm_q, qt, 2, dims, strides, box, "q");
+    if (rc) return rc;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!q_prepped) {
+    rc = query_prep_impl(q, gamma_q, pos, B, T, H, D, r, rope_base, eps, workspace, stream);
     if (rc) return rc;
   }
   AttnArgs a;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.gamma_q = gamma_q;
+  a.q = static_cast<const __nv_bfloat16*>(qt);
   a.kv = static_cast<const __nv_bfloat16*>(kv);
   a.gamma_kv = gamma_kv;
   a.idx = idx;
   a.pos = pos;
-  a.o = static_cast<__nv_bfloat16*>(o);
+  a.o = static_cast<float*>(o);
   a.lse = lse;
-  float* ws = static_cast<float*>(workspace);
+  float* ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + qbytes);
   const int64_t rows = (int64_t)B * T * H;
   a.part_o = p.nsplit > 1 ? ws : nullptr;
   a.part_lse = p.nsplit > 1 ? ws + rows * p.nsplit * D : nullptr;
@@ -266,7 +308,6 @@ int attn_common(int kind, const void* q, const float* gamma_q, const void* kv,
   a.nsplit = p.nsplit;
   a.keys_per_split = p.keys_per_split;
   a.nds = p.nds;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_attention(tm, tm_q, a, p, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (p.nsplit > 1) {
@@ -460,34 +501,44 @@ int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const i
   return topk_impl(scores, pos, B * T, N_cap, k, m, idx_out, stream);
 }
 
-size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys) {
+size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys,
+                                  int q_prepped) {
   AttnPlan p;
   if (kind < 0 || kind > 2) return 0;
   if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p)) return 0;
-  return p.ws_bytes;
+  return qprep_bytes(B, T, H, D, q_prepped) + p.ws_bytes;
 }
 
-int hattn_sparse_attn(const void* q, const float* gamma_q, const void* kv_c, const int32_t* idx,
+int hattn_query_prep(const void* q, const float* gamma_q, const int32_t* pos, int B, int T, int H,
+                     int D, int r, float rope_base, float eps, void* q_out,
+                     hattn_stream_t stream) {
+  int rc = query_prep_impl(q, gamma_q, pos, B, T, H, D, r, rope_base, eps, q_out, stream);
+  return rc ? rc : ok();
+}
+
+int hattn_sparse_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_c,
+                      const int32_t* idx,
                       const int32_t* pos, int B, int T, int H, int D, int64_t N_cap, int k, int r,
                       float rope_base, float eps, float scale, void* o, float* lse,
                       void* workspace, size_t ws_bytes, hattn_stream_t stream) {
-  return attn_common(kSparse, q, gamma_q, kv_c, nullptr, idx, pos, B, T, H, D, N_cap, k, 1, 1, r,
+  return attn_common(kSparse, q, gamma_q, q_prepped, kv_c, nullptr, idx, pos, B, T, H, D, N_cap, k, 1, 1, r,
                      rope_base, eps, scale, o, lse, workspace, ws_bytes, stream);
 }
 
-int hattn_hca_attn(const void* q, const float* gamma_q, const void* kv_h, const int32_t* pos,
+int hattn_hca_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_h,
+                   const int32_t* pos,
                    int B, int T, int H, int D, int64_t N_cap, int m, int r, float rope_base,
                    float eps, float scale, void* o, float* lse, void* workspace,
                    size_t ws_bytes, hattn_stream_t stream) {
-  return attn_common(kHca, q, gamma_q, kv_h, nullptr, nullptr, pos, B, T, H, D, N_cap, 1, m, 1, r,
+  return attn_common(kHca, q, gamma_q, q_prepped, kv_h, nullptr, nullptr, pos, B, T, H, D, N_cap, 1, m, 1, r,
                      rope_base, eps, scale, o, lse, workspace, ws_bytes, stream);
 }
 
-int hattn_swa_attn(const void* q, const float* gamma_q, const void* kv_raw,
+int hattn_swa_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_raw,
                    const float* gamma_kv, const int32_t* pos, int B, int T, int H, int D,
                    int64_t L_cap, int W, int r, float rope_base, float eps, float scale, void* o,
                    float* lse, void* workspace, size_t ws_bytes, hattn_stream_t stream) {
-  return attn_common(kSwa, q, gamma_q, kv_raw, gamma_kv, nullptr, pos, B, T, H, D, L_cap, 1, 1, W,
+  return attn_common(kSwa, q, gamma_q, q_prepped, kv_raw, gamma_kv, nullptr, pos, B, T, H, D, L_cap, 1, 1, W,
                      r, rope_base, eps, scale, o, lse, workspace, ws_bytes, stream);
 }
 
@@ -501,7 +552,7 @@ int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int
     if (!o_list[i] || !lse_list[i]) return fail(HATTN_ERR_INVALID_ARG, "branch %d is NULL", i);
     if (!aligned16(o_list[i])) return fail(HATTN_ERR_MISALIGNED, "o_list[%d] is not 16-byte aligned", i);
     if (!aligned4(lse_list[i])) return fail(HATTN_ERR_MISALIGNED, "lse_list[%d] is not 4-byte aligned", i);
-    a.o[i] = static_cast<const __nv_bfloat16*>(o_list[i]);
+    a.o[i] = static_cast<const float*>(o_list[i]);
     a.lse[i] = lse_list[i];
   }
   REQUIRE_PTR(pos);

@@ -70,14 +70,25 @@ cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, cudaStream_t strea
 // ------------------------------------------------------------ attention
 enum AttnKind { kSparse = 0, kHca = 1, kSwa = 2 };
 
-struct AttnArgs {
+// ------------------------------------------------------------ query prep
+struct QPrepArgs {
   const __nv_bfloat16* q;       // [B][T][H][D]
-  const float* gamma_q;         // [D] or null
+  const float* gamma;           // [D] or null
+  const int32_t* pos;           // [B][T]
+  __nv_bfloat16* q_out;         // [B][T][H][D]
+  int B, T, H, D, r;
+  float eps;
+  RopeCoef rope;
+};
+cudaError_t launch_qprep(const QPrepArgs& a, cudaStream_t stream);
+
+struct AttnArgs {
+  const __nv_bfloat16* q;       // prepared queries q~ [B][T][H][D]
   const __nv_bfloat16* kv;      // cache [B][N_cap][D] (sparse/HCA) or raw [B][L_cap][D] (SWA)
   const float* gamma_kv;        // SWA only
   const int32_t* idx;           // sparse only [B][T][k]
   const int32_t* pos;           // [B][T]
-  __nv_bfloat16* o;             // [B][T][H][D] (direct output when nsplit == 1)
+  float* o;                     // [B][T][H][D] fp32 (direct output when nsplit == 1)
   float* lse;                   // [B][T][H]
   float* part_o;                // [B*T*H][nsplit][D] partials (nsplit > 1)
   float* part_lse;              // [B*T*H][nsplit]
@@ -85,8 +96,8 @@ struct AttnArgs {
   int kind, B, T, H, D, r;
   int64_t N_rows;               // rows per sequence of kv (N_cap or L_cap)
   int k, m, W;
-  float eps, scale;
-  RopeCoef rope;
+  float eps, scale;             // eps: SWA key norm
+  RopeCoef rope;                // SWA key RoPE
   int G;                        // queries per row block
   int n_rb;                     // row blocks per sequence = ceil(T / G)
   int nsplit;                   // key splits
@@ -106,7 +117,7 @@ cudaError_t launch_attention(const CUtensorMap& tm_kv, const CUtensorMap& tm_q, 
 struct CombineArgs {
   const float* part_o;
   const float* part_lse;
-  __nv_bfloat16* o;
+  float* o;
   float* lse;
   int64_t rows;   // B*T*H
   int nsplit, D;
@@ -114,7 +125,7 @@ struct CombineArgs {
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
 struct MergeArgs {
-  const __nv_bfloat16* o[4];
+  const float* o[4];            // fp32 branch outputs
   const float* lse[4];
   int nb;
   const float* sink;    // [H] or null

@@ -2,7 +2,7 @@
 //
 // combine: the split-KV partials of one branch (each normalised by its own
 // softmax sum, with its log-sum-exp) merged in a fixed split order into the
-// branch output o (bf16) and lse (fp32).
+// branch output o and lse (fp32).
 //
 // merge: the sink-augmented merge of the branch outputs ("DeepSeek-V4" atlas,
 // section "Spec sheet / Core block": attention sinks; provenance 16: inverse
@@ -31,9 +31,10 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArg
   const float* pl = a.part_lse + row * a.nsplit;
   float mx = -INFINITY;
   for (int s = 0; s < a.nsplit; ++s) mx = fmaxf(mx, pl[s]);
-  __nv_bfloat16* o = a.o + row * a.D + c8 * 8;
+  float* o = a.o + row * a.D + c8 * 8;
   if (mx == -INFINITY) {
-    *reinterpret_cast<uint4*>(o) = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<float4*>(o)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(o)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (c8 == 0) a.lse[row] = -INFINITY;
     return;
   }
@@ -59,12 +60,8 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArg
     acc[7] = fmaf(c, v1.w, acc[7]);
   }
   const float iz = 1.f / z;
-  uint4 u;
-  u.x = pack_bf16x2(acc[0] * iz, acc[1] * iz);
-  u.y = pack_bf16x2(acc[2] * iz, acc[3] * iz);
-  u.z = pack_bf16x2(acc[4] * iz, acc[5] * iz);
-  u.w = pack_bf16x2(acc[6] * iz, acc[7] * iz);
-  *reinterpret_cast<uint4*>(o) = u;
+  reinterpret_cast<float4*>(o)[0] = make_float4(acc[0] * iz, acc[1] * iz, acc[2] * iz, acc[3] * iz);
+  reinterpret_cast<float4*>(o)[1] = make_float4(acc[4] * iz, acc[5] * iz, acc[6] * iz, acc[7] * iz);
   if (c8 == 0) a.lse[row] = mx + __logf(z);
 }
 
@@ -106,14 +103,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   for (int i = 0; i < a.nb; ++i) {
     const float coef = __expf(lse_b[i] - lz);
     if (coef == 0.f) continue;  // an empty branch (its o is not read)
-    const uint4 u = *reinterpret_cast<const uint4*>(a.o[i] + row * a.D + d);
-    const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(hv[e]);
-      y[2 * e] = fmaf(coef, f.x, y[2 * e]);
-      y[2 * e + 1] = fmaf(coef, f.y, y[2 * e + 1]);
-    }
+    const float4 v0 = *reinterpret_cast<const float4*>(a.o[i] + row * a.D + d);
+    const float4 v1 = *reinterpret_cast<const float4*>(a.o[i] + row * a.D + d + 4);
+    y[0] = fmaf(coef, v0.x, y[0]);
+    y[1] = fmaf(coef, v0.y, y[1]);
+    y[2] = fmaf(coef, v0.z, y[2]);
+    y[3] = fmaf(coef, v0.w, y[3]);
+    y[4] = fmaf(coef, v1.x, y[4]);
+    y[5] = fmaf(coef, v1.y, y[5]);
+    y[6] = fmaf(coef, v1.z, y[6]);
+    y[7] = fmaf(coef, v1.w, y[7]);
   }
   const int d0 = a.D - a.r;
   const int64_t p = a.pos[bt];

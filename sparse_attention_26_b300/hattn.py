@@ -38,13 +38,15 @@ _SIGS = {
     "hattn_indexer_scores": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
                                     _vp]),
     "hattn_topk_select": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp]),
-    "hattn_sparse_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
-                                 _i32, _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
-    "hattn_hca_attn": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _f32,
-                              _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
-    "hattn_swa_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
+    "hattn_query_prep": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _vp,
+                                _vp]),
+    "hattn_sparse_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
+                                 _i32, _i32, _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "hattn_hca_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                               _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
-    "hattn_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64]),
+    "hattn_swa_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
+                              _i32, _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
+    "hattn_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32]),
     "hattn_lse_merge": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _vp, _vp, _i32,
                                _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp]),
     "hattn_status_string": (ctypes.c_char_p, [_i32]),
@@ -217,24 +219,38 @@ def topk_select(scores, pos, *, k, m=4, idx_out=None, stream=None):
 
 
 # ------------------------------------------------------------------ attention
-def attn_workspace_bytes(kind, B, T, H, D, n_keys):
-    return int(lib().hattn_attn_workspace_bytes(kind, B, T, H, D, n_keys))
+def attn_workspace_bytes(kind, B, T, H, D, n_keys, q_prepped=False):
+    return int(lib().hattn_attn_workspace_bytes(kind, B, T, H, D, n_keys, int(bool(q_prepped))))
+
+
+def query_prep(q, pos, *, r, gamma_q=None, rope_base=10000.0, eps=1e-6, q_out=None, stream=None):
+    """q~ = RoPE_pos(RMSNorm(q)) for every head; returns q_out [B, T, H, D] bf16."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(gamma_q, "gamma_q", torch.float32)
+    B, T, H, D = q.shape
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    _need(q_out, "q_out", torch.bfloat16)
+    _check(lib().hattn_query_prep(_ptr(q), _ptr(gamma_q), _ptr(pos), B, T, H, D, r, rope_base,
+                                  eps, _ptr(q_out), _stream(stream)))
+    return q_out
 
 
 def _attn_out(q, o, lse):
     B, T, H, D = q.shape
     if o is None:
-        o = torch.empty((B, T, H, D), dtype=torch.bfloat16, device=q.device)
+        o = torch.empty((B, T, H, D), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
-    _need(o, "o", torch.bfloat16)
+    _need(o, "o", torch.float32)
     _need(lse, "lse", torch.float32)
     return o, lse
 
 
-def _ws(kind, q, n_keys, workspace):
+def _ws(kind, q, n_keys, workspace, q_prepped):
     B, T, H, D = q.shape
-    need = attn_workspace_bytes(kind, B, T, H, D, n_keys)
+    need = attn_workspace_bytes(kind, B, T, H, D, n_keys, q_prepped)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     return workspace, (workspace.numel() * workspace.element_size() if workspace is not None
@@ -242,8 +258,9 @@ def _ws(kind, q, n_keys, workspace):
 
 
 def sparse_attn(q, kv_c, idx, pos, *, r, gamma_q=None, rope_base=10000.0, eps=1e-6, scale=None,
-                o=None, lse=None, workspace=None, stream=None):
-    """CSA branch over the selected entries; returns (o bf16, lse fp32)."""
+                o=None, lse=None, workspace=None, q_prepped=False, stream=None):
+    """CSA branch over the selected entries; returns (o fp32, lse fp32).
+    q_prepped: q is the output of query_prep."""
     _need(q, "q", torch.bfloat16, 4)
     _need(kv_c, "kv_c", torch.bfloat16, 3)
     _need(idx, "idx", torch.int32, 3)
@@ -253,15 +270,15 @@ def sparse_attn(q, kv_c, idx, pos, *, r, gamma_q=None, rope_base=10000.0, eps=1e
     k = idx.shape[2]
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     o, lse = _attn_out(q, o, lse)
-    workspace, wsb = _ws(KIND_SPARSE, q, k, workspace)
-    _check(lib().hattn_sparse_attn(_ptr(q), _ptr(gamma_q), _ptr(kv_c), _ptr(idx), _ptr(pos), B, T,
+    workspace, wsb = _ws(KIND_SPARSE, q, k, workspace, q_prepped)
+    _check(lib().hattn_sparse_attn(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_c), _ptr(idx), _ptr(pos), B, T,
                                    H, D, kv_c.shape[1], k, r, rope_base, eps, scale, _ptr(o),
                                    _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
     return o, lse
 
 
 def hca_attn(q, kv_h, pos, *, r, m=128, gamma_q=None, rope_base=10000.0, eps=1e-6, scale=None,
-             o=None, lse=None, workspace=None, stream=None):
+             o=None, lse=None, workspace=None, q_prepped=False, stream=None):
     """HCA branch, dense over the visible compressed entries; returns (o, lse)."""
     _need(q, "q", torch.bfloat16, 4)
     _need(kv_h, "kv_h", torch.bfloat16, 3)
@@ -270,15 +287,16 @@ def hca_attn(q, kv_h, pos, *, r, m=128, gamma_q=None, rope_base=10000.0, eps=1e-
     B, T, H, D = q.shape
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     o, lse = _attn_out(q, o, lse)
-    workspace, wsb = _ws(KIND_HCA, q, kv_h.shape[1], workspace)
-    _check(lib().hattn_hca_attn(_ptr(q), _ptr(gamma_q), _ptr(kv_h), _ptr(pos), B, T, H, D,
+    workspace, wsb = _ws(KIND_HCA, q, kv_h.shape[1], workspace, q_prepped)
+    _check(lib().hattn_hca_attn(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_h), _ptr(pos), B, T, H, D,
                                 kv_h.shape[1], m, r, rope_base, eps, scale, _ptr(o), _ptr(lse),
                                 _ptr(workspace), wsb, _stream(stream)))
     return o, lse
 
 
 def swa_attn(q, kv_raw, pos, *, r, W=128, gamma_q=None, gamma_kv=None, rope_base=10000.0,
-             eps=1e-6, scale=None, o=None, lse=None, workspace=None, stream=None):
+             eps=1e-6, scale=None, o=None, lse=None, workspace=None, q_prepped=False,
+             stream=None):
     """SWA branch over the last W raw tokens (normalised and roped on load)."""
     _need(q, "q", torch.bfloat16, 4)
     _need(kv_raw, "kv_raw", torch.bfloat16, 3)
@@ -288,8 +306,8 @@ def swa_attn(q, kv_raw, pos, *, r, W=128, gamma_q=None, gamma_kv=None, rope_base
     B, T, H, D = q.shape
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     o, lse = _attn_out(q, o, lse)
-    workspace, wsb = _ws(KIND_SWA, q, W, workspace)
-    _check(lib().hattn_swa_attn(_ptr(q), _ptr(gamma_q), _ptr(kv_raw), _ptr(gamma_kv), _ptr(pos),
+    workspace, wsb = _ws(KIND_SWA, q, W, workspace, q_prepped)
+    _check(lib().hattn_swa_attn(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_raw), _ptr(gamma_kv), _ptr(pos),
                                 B, T, H, D, kv_raw.shape[1], W, r, rope_base, eps, scale, _ptr(o),
                                 _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
     return o, lse
@@ -303,7 +321,7 @@ def lse_merge(o_list, lse_list, pos, *, r, sink=None, rope_base=10000.0, out=Non
     if nb < 1 or nb != len(lse_list):
         raise ValueError("need 1..4 branches with matching lse tensors")
     for i, (o, l) in enumerate(zip(o_list, lse_list)):
-        _need(o, f"o_list[{i}]", torch.bfloat16, 4)
+        _need(o, f"o_list[{i}]", torch.float32, 4)
         _need(l, f"lse_list[{i}]", torch.float32, 3)
     _need(pos, "pos", torch.int32, 2)
     _opt(sink, "sink", torch.float32)

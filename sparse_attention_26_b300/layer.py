@@ -7,10 +7,12 @@ Decode step at query position t (its own token already written to the raw
 cache), for every sequence of the batch:
   1. csa_compress / hca_compress of the entry that the token at t completes
      (when (t+1) is a multiple of m), so the caches are current;
-  2. indexer scores over the visible CSA entries, then top-k selection;
-  3. sparse attention over the selected entries, dense attention over the
-     visible HCA entries, sliding-window attention over the last W tokens;
-  4. sink-augmented LSE merge of the three branches with inverse RoPE.
+  2. query preparation (RMSNorm + RoPE), shared by the three branches;
+  3. indexer scores over the visible CSA entries, then top-k selection;
+  4. sparse attention over the selected entries, dense attention over the
+     visible HCA entries, sliding-window attention over the last W tokens
+     (HCA and SWA optionally on a second stream, concurrent with 3);
+  5. sink-augmented LSE merge of the three branches with inverse RoPE.
 """
 from __future__ import annotations
 
@@ -65,44 +67,84 @@ class HybridLayer:
             out=torch.empty((B, T, H, D), dtype=bf, device=dev),
             lse=torch.empty((B, T, H), dtype=torch.float32, device=dev),
         )
-        for name, kind, nk in [("csa", hattn.KIND_SPARSE, wl.k), ("hca", hattn.KIND_HCA, self.N_hca),
-                               ("swa", hattn.KIND_SWA, wl.W)]:
-            b["o_" + name] = torch.empty((B, T, H, D), dtype=bf, device=dev)
+        b["qt"] = torch.empty((B, T, H, D), dtype=bf, device=dev)  # prepared queries
+        for name, kind, nk in self._branch_kinds():
+            b["o_" + name] = torch.empty((B, T, H, D), dtype=torch.float32, device=dev)
             b["l_" + name] = torch.empty((B, T, H), dtype=torch.float32, device=dev)
-            ws = hattn.attn_workspace_bytes(kind, B, T, H, D, nk)
+            ws = hattn.attn_workspace_bytes(kind, B, T, H, D, nk, q_prepped=True)
             b["ws_" + name] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         self._bufs[T] = b
         return b
 
-    def step(self, q, iq, w, pos, sink, t_new=None, events=None):
+    def _branch_kinds(self):
+        wl = self.wl
+        return [(n, k, nk) for n, k, nk in [("csa", hattn.KIND_SPARSE, wl.k),
+                                            ("hca", hattn.KIND_HCA, self.N_hca),
+                                            ("swa", hattn.KIND_SWA, wl.W)]
+                if n in wl.branches]
+
+    def step(self, q, iq, w, pos, sink, t_new=None, events=None, side_stream=None):
         """One pass of the hot path for queries q [B,T,H,D] at positions pos.
 
         t_new: position of the newest token (compresses the entries it
         completes); None skips the incremental compression.  events: optional
         dict name -> (start, end) torch.cuda.Event pairs recorded around the
-        calls.  Returns (out bf16 [B,T,H,D], lse fp32 [B,T,H])."""
+        calls.  side_stream: a second CUDA stream; when given, the HCA and
+        SWA branches run on it, concurrently with the indexer, top-k and CSA
+        branch, joined before the merge.  Returns (out bf16 [B,T,H,D], lse
+        fp32 [B,T,H])."""
         wl, r = self.wl, self.raw
         B, T = q.shape[0], q.shape[1]
         b = self.buffers(T)
+        main = torch.cuda.current_stream()
 
         def ev(name, i):
             if events is not None and name in events:
-                events[name][i].record()
+                events[name][i].record(torch.cuda.current_stream())
+
+        def compress(kind):
+            if t_new is None or kind not in wl.branches:
+                return
+            m, w_ = (wl.m_csa, wl.w_csa) if kind == "csa" else (wl.m_hca, wl.m_hca)
+            if (t_new + 1) % m:
+                return
+            j = (t_new + 1) // m - 1
+            if kind == "csa":
+                hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j,
+                                   j_end=j + 1, m=m, w=w_, kv_c=self.kv_c, ik_c=self.ik_c)
+            else:
+                hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=j, j_end=j + 1,
+                                   m=m, kv_h=self.kv_h)
 
         ev("compress", 0)
-        if t_new is not None:
-            for m, w_, kind in [(wl.m_csa, wl.w_csa, "csa"), (wl.m_hca, wl.m_hca, "hca")]:
-                if kind in wl.branches and (t_new + 1) % m == 0:
-                    j = (t_new + 1) // m - 1
-                    if kind == "csa":
-                        hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r,
-                                           j_begin=j, j_end=j + 1, m=m, w=w_, kv_c=self.kv_c,
-                                           ik_c=self.ik_c)
-                    else:
-                        hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=j,
-                                           j_end=j + 1, m=m, kv_h=self.kv_h)
+        compress("csa")
+        if side_stream is None:
+            compress("hca")
         ev("compress", 1)
-        o_list, l_list = [], []
+        ev("qprep", 0)
+        hattn.query_prep(q, pos, r=wl.r, q_out=b["qt"])
+        ev("qprep", 1)
+        qt = b["qt"]
+
+        def dense_branches():
+            if "hca" in wl.branches:
+                ev("hca", 0)
+                hattn.hca_attn(qt, self.kv_h, pos, r=wl.r, m=wl.m_hca, o=b["o_hca"],
+                               lse=b["l_hca"], workspace=b["ws_hca"], q_prepped=True)
+                ev("hca", 1)
+            if "swa" in wl.branches:
+                ev("swa", 0)
+                hattn.swa_attn(qt, r["kv_raw"], pos, r=wl.r, W=wl.W, o=b["o_swa"],
+                               lse=b["l_swa"], workspace=b["ws_swa"], q_prepped=True)
+                ev("swa", 1)
+
+        joined = None
+        if side_stream is not None:
+            side_stream.wait_stream(main)
+            with torch.cuda.stream(side_stream):
+                compress("hca")
+                dense_branches()
+            joined = side_stream
         if "csa" in wl.branches:
             ev("indexer", 0)
             hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=b["scores"])
@@ -111,42 +153,31 @@ class HybridLayer:
             hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
             ev("topk", 1)
             ev("sparse", 0)
-            hattn.sparse_attn(q, self.kv_c, b["idx"], pos, r=wl.r, o=b["o_csa"], lse=b["l_csa"],
-                              workspace=b["ws_csa"])
+            hattn.sparse_attn(qt, self.kv_c, b["idx"], pos, r=wl.r, o=b["o_csa"],
+                              lse=b["l_csa"], workspace=b["ws_csa"], q_prepped=True)
             ev("sparse", 1)
-            o_list.append(b["o_csa"])
-            l_list.append(b["l_csa"])
-        if "hca" in wl.branches:
-            ev("hca", 0)
-            hattn.hca_attn(q, self.kv_h, pos, r=wl.r, m=wl.m_hca, o=b["o_hca"], lse=b["l_hca"],
-                           workspace=b["ws_hca"])
-            ev("hca", 1)
-            o_list.append(b["o_hca"])
-            l_list.append(b["l_hca"])
-        if "swa" in wl.branches:
-            ev("swa", 0)
-            hattn.swa_attn(q, r["kv_raw"], pos, r=wl.r, W=wl.W, o=b["o_swa"], lse=b["l_swa"],
-                           workspace=b["ws_swa"])
-            ev("swa", 1)
-            o_list.append(b["o_swa"])
-            l_list.append(b["l_swa"])
+        if joined is None:
+            dense_branches()
+        else:
+            main.wait_stream(joined)
+        o_list = [b["o_" + n] for n, _, _ in self._branch_kinds()]
+        l_list = [b["l_" + n] for n, _, _ in self._branch_kinds()]
         ev("merge", 0)
         hattn.lse_merge(o_list, l_list, pos, r=wl.r, sink=sink, out=b["out"], lse_out=b["lse"])
         ev("merge", 1)
         return b["out"], b["lse"]
 
     def launches_per_step(self, T, t_new=None):
-        """Kernels one step launches (each attention branch with split-KV adds
-        its combine kernel)."""
+        """Kernels one step launches: the query preparation, each branch's
+        attention kernel (plus its combine with split-KV), the indexer and
+        top-k of CSA, the merge, and the compressions the new token needs."""
         wl, B, D, H = self.wl, self.B, self.D, self.wl.H
-        n = 1  # merge
+        n = 2  # query preparation, merge
         if t_new is not None:
             n += int("csa" in wl.branches and (t_new + 1) % wl.m_csa == 0)
             n += int("hca" in wl.branches and (t_new + 1) % wl.m_hca == 0)
-        for name, kind, nk in [("csa", hattn.KIND_SPARSE, wl.k), ("hca", hattn.KIND_HCA, self.N_hca),
-                               ("swa", hattn.KIND_SWA, wl.W)]:
-            if name in wl.branches:
-                n += 1 + int(hattn.attn_workspace_bytes(kind, B, T, H, D, nk) > 0)
-                if name == "csa":
-                    n += 2  # indexer scores + top-k select
+        for name, kind, nk in self._branch_kinds():
+            n += 1 + int(hattn.attn_workspace_bytes(kind, B, T, H, D, nk, q_prepped=True) > 0)
+            if name == "csa":
+                n += 2  # indexer scores + top-k select
         return n

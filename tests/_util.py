@@ -35,13 +35,12 @@ def bf16_half_ulp(x):
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
-def check_attn(o_gpu, lse_gpu, o_ref, lse_ref, what="", storage=None):
+def check_attn(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     """Spec tolerance: max-abs 1e-2 and rel-L2 5e-3 on the attention output
-    (bf16 in, fp32 accumulate).  Outputs are stored in bf16, so a result
-    that is correct in fp32 may still land one rounding step away from the
-    oracle: every element may also differ by the half bf16 ulp that storing
-    it costs (0.0078 at magnitudes 2..4).  `storage` is accepted for
-    readability at call sites; every output here is bf16."""
+    (bf16 in, fp32 accumulate).  The layer output is stored in bf16, so a
+    result that is correct in fp32 may still land one rounding step away
+    from the oracle: every element may also differ by the half bf16 ulp that
+    storing it costs (0.0078 at magnitudes 2..4)."""
     o_gpu, o_ref = f64(o_gpu), f64(o_ref)
     assert np.isfinite(o_gpu).all(), f"{what}: non-finite output"
     if o_ref.size:

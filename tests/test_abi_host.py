@@ -99,18 +99,30 @@ def test_indexer_validation(L):
 
 def test_attention_validation(L):
     N = None
-    rc = L.hattn_sparse_attn(FAKE, N, FAKE, N, FAKE, 1, 1, 128, 512, 100, 16, 64, 1e4, 1e-6,
+    rc = L.hattn_sparse_attn(FAKE, N, 0, FAKE, N, FAKE, 1, 1, 128, 512, 100, 16, 64, 1e4, 1e-6,
                              0.04, FAKE, FAKE, N, 0, N)
     assert rc == hattn.INVALID_ARG and "idx" in _err(L)
-    rc = L.hattn_hca_attn(FAKE, N, FAKE, FAKE, 1, 1, 256, 512, 100, 128, 64, 1e4, 1e-6, 0.04, FAKE,
-                          FAKE, N, 0, N)
+    rc = L.hattn_hca_attn(FAKE, N, 0, FAKE, FAKE, 1, 1, 256, 512, 100, 128, 64, 1e4, 1e-6, 0.04,
+                          FAKE, FAKE, N, 0, N)
     assert rc == hattn.INVALID_ARG and "H=256" in _err(L)
-    rc = L.hattn_swa_attn(FAKE, N, FAKE, N, FAKE, 1, 1, 128, 512, 100, 0, 64, 1e4, 1e-6, 0.04,
+    rc = L.hattn_swa_attn(FAKE, N, 1, FAKE, N, FAKE, 1, 1, 128, 512, 100, 0, 64, 1e4, 1e-6, 0.04,
                           FAKE, FAKE, N, 0, N)
     assert rc == hattn.INVALID_ARG
-    rc = L.hattn_hca_attn(FAKE, N, FAKE, FAKE, 1, 1, 128, 512, 100, 128, 200, 1e4, 1e-6, 0.04,
+    rc = L.hattn_hca_attn(FAKE, N, 0, FAKE, FAKE, 1, 1, 128, 512, 100, 128, 200, 1e4, 1e-6, 0.04,
                           FAKE, FAKE, N, 0, N)
     assert rc == hattn.INVALID_ARG and "r=200" in _err(L)
+    # raw queries are prepared into the workspace, which is then required
+    rc = L.hattn_hca_attn(FAKE, N, 0, FAKE, FAKE, 1, 1, 128, 512, 100, 128, 64, 1e4, 1e-6, 0.04,
+                          FAKE, FAKE, N, 0, N)
+    assert rc == hattn.INVALID_ARG and "workspace" in _err(L)
+    # D above 256 is split in halves of whole 64-wide chunks
+    rc = L.hattn_hca_attn(FAKE, N, 1, FAKE, FAKE, 1, 1, 128, 320, 100, 128, 64, 1e4, 1e-6, 0.04,
+                          FAKE, FAKE, N, 0, N)
+    assert rc == hattn.UNSUPPORTED
+    rc = L.hattn_query_prep(FAKE, N, N, 1, 1, 4, 64, 16, 1e4, 1e-6, FAKE, N)
+    assert rc == hattn.INVALID_ARG and "pos" in _err(L)
+    rc = L.hattn_query_prep(MISAL, N, FAKE, 1, 1, 4, 64, 16, 1e4, 1e-6, FAKE, N)
+    assert rc == hattn.MISALIGNED
     # the merge needs 1..4 branches
     arr = (ctypes.c_void_p * 1)(FAKE)
     rc = L.hattn_lse_merge(arr, arr, 0, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
@@ -119,6 +131,11 @@ def test_attention_validation(L):
 
 def test_workspace_sizes_scale_with_splits(L):
     # decode at the 1M-context shape splits keys across SMs and needs partials
-    assert hattn.attn_workspace_bytes(hattn.KIND_HCA, 8, 1, 128, 512, 8192) > 0
-    # a long prefill row block has no split and needs none
-    assert hattn.attn_workspace_bytes(hattn.KIND_SPARSE, 1, 8192, 64, 512, 512) == 0
+    part = hattn.attn_workspace_bytes(hattn.KIND_HCA, 8, 1, 128, 512, 8192, q_prepped=True)
+    assert part > 0
+    # raw queries add their prepared copy (B*T*H*D bf16) in front
+    full = hattn.attn_workspace_bytes(hattn.KIND_HCA, 8, 1, 128, 512, 8192)
+    assert full == part + 8 * 1 * 128 * 512 * 2
+    # a long prefill row block has no split and needs no partials
+    assert hattn.attn_workspace_bytes(hattn.KIND_SPARSE, 1, 8192, 64, 512, 512,
+                                      q_prepped=True) == 0

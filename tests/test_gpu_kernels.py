@@ -164,6 +164,25 @@ def test_topk_without_score_output_uses_workspace():
     assert sorted(a.cpu().flatten().tolist()) == sorted(b.cpu().flatten().tolist())
 
 
+# ------------------------------------------------------------------ query preparation
+@pytest.mark.parametrize("B,T,H,D,r", [(2, 3, 128, 512, 64), (1, 5, 4, 64, 16)])
+def test_query_prep(B, T, H, D, r):
+    q = randn_bf16((B, T, H, D), 45)
+    gq = 1.0 + 0.1 * randn_f32((D,), 46)
+    pos = _pos(B, T, [(7919 * i + 3) % (1 << 21) for i in range(B * T)])
+    qt = hattn.query_prep(q.to(DEV), pos.to(DEV), r=r, gamma_q=gq.to(DEV))
+    hattn.check_status()
+    qf = f64(q)
+    ref = np.empty_like(qf)
+    for bb in range(B):
+        for t in range(T):
+            for hh in range(H):
+                ref[bb, t, hh] = orc.rope(orc.rmsnorm(qf[bb, t, hh], gq.numpy()), r,
+                                          int(pos[bb, t]))
+    assert rel_l2(qt, ref) <= KV_REL_L2
+    check_attn(qt, None, ref, None, "query prep")
+
+
 # ------------------------------------------------------------------ attention branches
 def _pos(B, T, values):
     return torch.tensor(values, dtype=torch.int32).reshape(B, T)
@@ -185,7 +204,7 @@ def test_sparse_attn(B, T, H, D, r, N_cap, k):
     hattn.check_status()
     ro, rl = orc.attention(orc.KIND_SPARSE, bits(q), bits(cache), pos.numpy(), idx=idx.numpy(),
                            r=r)
-    check_attn(o, lse, ro, rl, "sparse", storage="bf16")
+    check_attn(o, lse, ro, rl, "sparse")
 
 
 def test_sparse_attn_all_padding_and_bad_index():
@@ -201,7 +220,7 @@ def test_sparse_attn_all_padding_and_bad_index():
     assert (o[0, 0].float() == 0).all()
     ro, rl = orc.attention(orc.KIND_SPARSE, bits(q), bits(cache), pos.numpy(), idx=idx.numpy(),
                            r=16)
-    check_attn(o[0, 1], lse[0, 1], ro[0, 1], rl[0, 1], "sparse short", storage="bf16")
+    check_attn(o[0, 1], lse[0, 1], ro[0, 1], rl[0, 1], "sparse short")
     idx[0, 1, 4] = N_cap + 3  # out of range: skipped and reported
     hattn.sparse_attn(q.to(DEV), cache.to(DEV), idx.to(DEV), pos.to(DEV), r=16)
     assert hattn.check_status_code() == hattn.DEVICE_INDEX
@@ -224,7 +243,7 @@ def test_hca_attn(B, T, H, D, r, N_cap, pos_list):
     o, lse = hattn.hca_attn(q.to(DEV), cdev, pos.to(DEV), r=r, m=128)
     hattn.check_status()
     ro, rl = orc.attention(orc.KIND_HCA, bits(q), bits(cache), pos.numpy(), m=128, r=r)
-    check_attn(o, lse, ro, rl, "hca", storage="bf16")
+    check_attn(o, lse, ro, rl, "hca")
 
 
 @pytest.mark.parametrize("B,T,H,D,r,L,W,pos_list", [
@@ -243,7 +262,7 @@ def test_swa_attn(B, T, H, D, r, L, W, pos_list):
     hattn.check_status()
     ro, rl = orc.attention(orc.KIND_SWA, bits(q), bits(raw), pos.numpy(), W=W, r=r,
                            gamma_q=gq.numpy(), gamma_kv=gk.numpy())
-    check_attn(o, lse, ro, rl, "swa", storage="bf16")
+    check_attn(o, lse, ro, rl, "swa")
 
 
 def test_lazy_rescale_path():
@@ -253,7 +272,7 @@ def test_lazy_rescale_path():
     normalised latents.  150 sequences fill the SMs, so every row keeps all 10
     tiles in one split."""
     B, T, H, D, N = 150, 1, 4, 64, 640
-    assert hattn.attn_workspace_bytes(hattn.KIND_HCA, B, T, H, D, N) == 0  # one split
+    assert hattn.attn_workspace_bytes(hattn.KIND_HCA, B, T, H, D, N, q_prepped=True) == 0  # one split
     u = torch.zeros(D)
     u[: D // 2] = 1.0 / math.sqrt(D // 2)
     v = torch.zeros(D)
@@ -267,7 +286,7 @@ def test_lazy_rescale_path():
     hattn.check_status()
     ro, rl = orc.attention(orc.KIND_HCA, bits(q[:2]), bits(cache[:2]), pos[:2].numpy(), m=128,
                            r=0)
-    check_attn(o[:2], lse[:2], ro, rl, "rescale", storage="bf16")
+    check_attn(o[:2], lse[:2], ro, rl, "rescale")
 
 
 # ------------------------------------------------------------------ merge
@@ -281,7 +300,7 @@ def test_lazy_rescale_path():
 ])
 def test_lse_merge(nb, with_sink, pos_list):
     B, T, H, D, r = 2, 3, 16, 512, 64
-    os_ = [randn_bf16((B, T, H, D), 80 + i) for i in range(nb)]
+    os_ = [randn_f32((B, T, H, D), 80 + i) for i in range(nb)]
     ls = [randn_f32((B, T, H), 90 + i) * 3 for i in range(nb)]
     ls[0][0, 0, 0] = -float("inf")  # an empty branch row
     sink = randn_f32((H,), 99) if with_sink else None
@@ -290,7 +309,7 @@ def test_lse_merge(nb, with_sink, pos_list):
                                r=r, sink=sink.to(DEV) if sink is not None else None)
     ro, rl = orc.merge([f64(o) for o in os_], [f64(l) for l in ls],
                        sink.numpy() if sink is not None else None, pos.numpy(), r)
-    check_attn(out, lse, ro, rl, "merge", storage="bf16")
+    check_attn(out, lse, ro, rl, "merge")
 
 
 # ------------------------------------------------------------------ whole tiny layer
@@ -310,7 +329,7 @@ def test_tiny_layer_end_to_end():
     out, lse = hattn.lse_merge([o1, o2, o3], [l1, l2, l3], d["pos"], r=wl.r, sink=d["sink"])
     hattn.check_status()
     check_topk(idx.cpu().numpy(), ref["scores"], inp["pos"].numpy(), 4, wl.k, "tiny")
-    check_attn(o3, l3, ref["o_swa"], ref["lse_swa"], "tiny swa", storage="bf16")
-    check_attn(o2, l2, ref["o_hca"], ref["lse_hca"], "tiny hca", storage="bf16")
+    check_attn(o3, l3, ref["o_swa"], ref["lse_swa"], "tiny swa")
+    check_attn(o2, l2, ref["o_hca"], ref["lse_hca"], "tiny hca")
     check_attn(out, lse, ref["out"], ref["lse"], "tiny layer")
     assert L == 256

@@ -184,10 +184,22 @@ HATTN_API int hattn_swa_attn(const void* q, const float* gamma_q, int q_prepped,
                    int64_t L_cap, int W, int r, float rope_base, float eps, float scale, void* o,
                    float* lse, void* workspace, size_t ws_bytes, hattn_stream_t stream);
 
-/* kind: 0 = CSA sparse (n_keys = k), 1 = HCA (n_keys = N_cap), 2 = SWA (n_keys = W).
- * 0 means no workspace is needed (or no kernel exists for the shape). */
+/* Split partials instead of a branch output: with o == NULL and lse == NULL
+ * an attention call leaves the softmax of each key split in its workspace,
+ * right after the prepared queries (if any):
+ *   part_o   [B*T*H][nsplit][D] fp32 (each split normalised by its own sum)
+ *   part_lse [B*T*H][nsplit]    fp32 (that split's log-sum-exp)
+ * with nsplit = hattn_attn_splits(...).  hattn_lse_merge_splits merges such
+ * partials of several branches in one pass (no per-branch combine).
+ *
+ * kind: 0 = CSA sparse (n_keys = k), 1 = HCA (n_keys = N_cap), 2 = SWA (n_keys = W).
+ * partials: 1 when the call is made in the partials form above.  0 means no
+ * workspace is needed (or no kernel exists for the shape). */
 HATTN_API size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys,
-                                            int q_prepped);
+                                            int q_prepped, int partials);
+/* Key splits (partials per row) an attention call of this shape uses; 0 if
+ * no kernel exists for it. */
+HATTN_API int hattn_attn_splits(int kind, int B, int T, int H, int D, int64_t n_keys);
 
 /* -------------------------------------------------------------------------
  * Merge.  [AT] "Spec sheet / Core block": attention sinks; provenance 16:
@@ -201,6 +213,18 @@ HATTN_API size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D
 HATTN_API int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int nb,
                     const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
                     float rope_base, void* out, float* lse_out, hattn_stream_t stream);
+
+/* The same merge over split partials: branch i is given by nsplit[i] (host
+ * array) partials per row, part_o_list[i] fp32 [B*T*H][nsplit[i]][D] and
+ * part_lse_list[i] fp32 [B*T*H][nsplit[i]] (as left by an attention call with
+ * o == lse == NULL).  The result equals combining each branch's splits and
+ * then merging (a branch's own normalisation cancels).  At most 128 partials
+ * per row in total. */
+HATTN_API int hattn_lse_merge_splits(const void* const* part_o_list,
+                                     const float* const* part_lse_list, const int* nsplit, int nb,
+                                     const float* sink, const int32_t* pos, int B, int T, int H,
+                                     int D, int r, float rope_base, void* out, float* lse_out,
+                                     hattn_stream_t stream);
 
 /* -------------------------------------------------------------------------
  * Status and diagnostics.

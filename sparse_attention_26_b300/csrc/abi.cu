@@ -182,6 +182,12 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
   return ok();
 }
 
+// Bytes of the split partials of an attention call: [B*T*H][nsplit][D] fp32
+// outputs, then [B*T*H][nsplit] fp32 log-sum-exps.
+size_t partial_bytes(int B, int T, int H, int D, int nsplit) {
+  return (size_t)B * T * H * nsplit * (D + 1) * sizeof(float);
+}
+
 // Bytes of the prepared-query copy at the start of an attention workspace
 // (none when the caller passes prepared queries).
 size_t qprep_bytes(int B, int T, int H, int D, int q_prepped) {
@@ -224,8 +230,14 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   REQUIRE_PTR(q);
   REQUIRE_PTR(kv);
   REQUIRE_PTR(pos);
-  REQUIRE_PTR(o);
-  REQUIRE_PTR(lse);
+  // o == lse == NULL: leave the split partials in the workspace for
+  // hattn_lse_merge_splits instead of combining them
+  const bool partials = o == nullptr && lse == nullptr;
+  if (!partials) {
+    REQUIRE_PTR(o);
+    REQUIRE(lse != nullptr, "lse must not be NULL when o is given");
+    REQUIRE_F32(lse);
+  }
   REQUIRE_F32(gamma_q);
   REQUIRE_F32(gamma_kv);
   if (kind == kSparse) REQUIRE_PTR(idx);
@@ -245,7 +257,8 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p))
     return fail(HATTN_ERR_UNSUPPORTED, "no attention kernel for H=%d D=%d", H, D);
   const size_t qbytes = qprep_bytes(B, T, H, D, q_prepped);
-  const size_t need = qbytes + p.ws_bytes;
+  const size_t pbytes = partials ? partial_bytes(B, T, H, D, p.nsplit) : p.ws_bytes;
+  const size_t need = qbytes + pbytes;
   if (need > 0) {
     REQUIRE_PTR(workspace);
     REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
@@ -287,8 +300,10 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.lse = lse;
   float* ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + qbytes);
   const int64_t rows = (int64_t)B * T * H;
-  a.part_o = p.nsplit > 1 ? ws : nullptr;
-  a.part_lse = p.nsplit > 1 ? ws + rows * p.nsplit * D : nullptr;
+  const bool split_out = partials || p.nsplit > 1;
+  a.part_o = split_out ? ws : nullptr;
+  a.part_lse = split_out ? ws + rows * p.nsplit * D : nullptr;
+  a.partials = partials ? 1 : 0;
   a.status = status;
   a.kind = kind;
   a.B = B;
@@ -310,7 +325,7 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.nds = p.nds;
   cudaError_t e = launch_attention(tm, tm_q, a, p, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
-  if (p.nsplit > 1) {
+  if (p.nsplit > 1 && !partials) {
     CombineArgs c;
     c.part_o = a.part_o;
     c.part_lse = a.part_lse;
@@ -502,11 +517,19 @@ int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const i
 }
 
 size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys,
-                                  int q_prepped) {
+                                  int q_prepped, int partials) {
   AttnPlan p;
   if (kind < 0 || kind > 2) return 0;
   if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p)) return 0;
-  return qprep_bytes(B, T, H, D, q_prepped) + p.ws_bytes;
+  return qprep_bytes(B, T, H, D, q_prepped) +
+         (partials ? partial_bytes(B, T, H, D, p.nsplit) : p.ws_bytes);
+}
+
+int hattn_attn_splits(int kind, int B, int T, int H, int D, int64_t n_keys) {
+  AttnPlan p;
+  if (kind < 0 || kind > 2) return 0;
+  if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p)) return 0;
+  return p.nsplit;
 }
 
 int hattn_query_prep(const void* q, const float* gamma_q, const int32_t* pos, int B, int T, int H,
@@ -542,19 +565,29 @@ int hattn_swa_attn(const void* q, const float* gamma_q, int q_prepped, const voi
                      r, rope_base, eps, scale, o, lse, workspace, ws_bytes, stream);
 }
 
-int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int nb,
-                    const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
-                    float rope_base, void* out, float* lse_out, hattn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int merge_impl(const void* const* o_list, const float* const* lse_list, const int* nsplit, int nb,
+               const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
+               float rope_base, void* out, float* lse_out, hattn_stream_t stream) {
   REQUIRE(o_list && lse_list, "o_list and lse_list must not be NULL");
   REQUIRE(nb >= 1 && nb <= 4, "nb=%d must be in [1, 4]", nb);
   MergeArgs a;
+  int parts = 0;
   for (int i = 0; i < nb; ++i) {
     if (!o_list[i] || !lse_list[i]) return fail(HATTN_ERR_INVALID_ARG, "branch %d is NULL", i);
     if (!aligned16(o_list[i])) return fail(HATTN_ERR_MISALIGNED, "o_list[%d] is not 16-byte aligned", i);
     if (!aligned4(lse_list[i])) return fail(HATTN_ERR_MISALIGNED, "lse_list[%d] is not 4-byte aligned", i);
+    const int ns = nsplit ? nsplit[i] : 1;
+    REQUIRE(ns >= 1, "nsplit[%d]=%d must be >= 1", i, ns);
+    parts += ns;
     a.o[i] = static_cast<const float*>(o_list[i]);
     a.lse[i] = lse_list[i];
+    a.nsplit[i] = ns;
   }
+  REQUIRE(parts <= kMaxMergeParts, "%d partials per row, at most %d", parts, kMaxMergeParts);
   REQUIRE_PTR(pos);
   REQUIRE_PTR(out);
   REQUIRE_F32(sink);
@@ -578,6 +611,26 @@ int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int
   cudaError_t e = launch_merge(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int nb,
+                    const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
+                    float rope_base, void* out, float* lse_out, hattn_stream_t stream) {
+  return merge_impl(o_list, lse_list, nullptr, nb, sink, pos, B, T, H, D, r, rope_base, out,
+                    lse_out, stream);
+}
+
+int hattn_lse_merge_splits(const void* const* part_o_list, const float* const* part_lse_list,
+                           const int* nsplit, int nb, const float* sink, const int32_t* pos, int B,
+                           int T, int H, int D, int r, float rope_base, void* out, float* lse_out,
+                           hattn_stream_t stream) {
+  if (!nsplit) return fail(HATTN_ERR_INVALID_ARG, "nsplit must not be NULL");
+  return merge_impl(part_o_list, part_lse_list, nsplit, nb, sink, pos, B, T, H, D, r, rope_base,
+                    out, lse_out, stream);
 }
 
 const char* hattn_status_string(int code) {

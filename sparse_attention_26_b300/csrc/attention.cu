@@ -23,9 +23,13 @@
 // Key rows reach shared memory as 64x64 bf16 chunks (8 KB, 128-byte
 // swizzle) in a ring of `nslot` slots: HCA by TMA tiles, CSA by a 16-byte
 // cp.async gather through the top-k indices, SWA by TMA tiles normalised and
-// roped in place.  Warps 0-3 produce chunks from kernel entry, warp 4 issues
-// the MMAs, warps 5-8 run the softmax and the epilogue, which writes whole
-// fp32 rows through shared memory so every store instruction is contiguous.
+// roped in place.  Warps 0-3 produce chunks from kernel entry; warps 4 and 9
+// issue the QK products of even and odd tiles (one S buffer each; a single
+// thread issues a tcgen05.mma only every ~50 ns, so two issuers keep the
+// tensor core busier), warp 10 issues the PV products (one N = D/nds MMA
+// per 16 keys), warps 5-8 run the softmax and the epilogue, which writes
+// whole fp32 rows through shared memory so every store instruction is
+// contiguous.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -33,9 +37,9 @@ namespace hattn {
 
 namespace {
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 352;
 constexpr int kTile = 64;
-constexpr int kMaxSlots = 24;
+constexpr int kMaxSlots = 20;
 constexpr int kProdThreads = 128;
 
 struct AttnShared {
@@ -43,15 +47,17 @@ struct AttnShared {
   uint64_t raw[kMaxSlots];  // SWA: the TMA copy of a raw chunk has landed
   uint64_t empty[kMaxSlots];
   uint64_t s_full[2];
+  uint64_t s_free[2];       // PV of the tile that last used this S/P buffer is done
   uint64_t p_full;
   uint64_t pv_done;
   uint64_t o_full;
   uint64_t q_full;
   uint64_t q_tmem;          // the other half of Q is in tensor memory
+  uint64_t q_ready;         // Q complete (both MMA warps may start)
+  uint64_t drain[2];        // the QK warps' own MMAs have completed
   uint32_t tmem_base;
   int abort;
   float inv_rms[2][kTile];  // SWA: per-row norms, double-buffered by tile
-  float rc[4][kMaxRopePairs];  // RoPE coefficients (see RopeCoef)
 };
 
 __device__ __forceinline__ int64_t vis(int32_t t, int m) {
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rI = threadIdx.x; rI < nrows; rI += kThreads) {
       const int g = rI / a.H, h = rI % a.H;
       const int64_t row = ((int64_t)b * a.T + t0 + g) * a.H + h;
-      if (a.nsplit == 1) {
+      if (a.nsplit == 1 && !a.partials) {
         for (int c = 0; c < ocols; ++c) a.o[row * a.D + dh * ocols + c] = 0.f;
         if (dh == 0) a.lse[row] = -INFINITY;
       } else {
@@ -220,21 +226,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm->raw[i]), 1);
       mbar_init(smem_u32(&sm->empty[i]), 1);
     }
-    mbar_init(smem_u32(&sm->s_full[0]), 1);
-    mbar_init(smem_u32(&sm->s_full[1]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm->s_full[i]), 1);
+      mbar_init(smem_u32(&sm->s_free[i]), 1);
+      mbar_init(smem_u32(&sm->drain[i]), 1);
+    }
     mbar_init(smem_u32(&sm->p_full), 128);
     mbar_init(smem_u32(&sm->pv_done), 1);
     mbar_init(smem_u32(&sm->o_full), 1);
     mbar_init(smem_u32(&sm->q_full), 1);
     mbar_init(smem_u32(&sm->q_tmem), 128);
+    mbar_init(smem_u32(&sm->q_ready), 1);
     sm->abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     if (KIND != kSparse) tma_prefetch_desc(&tm_kv);
-  }
-  for (int i = threadIdx.x; i < a.r / 2; i += kThreads) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) sm->rc[c][i] = a.rope.c[c][i];
   }
   if (warp == 4) {
     tmem_alloc(smem_u32(&sm->tmem_base), 512);
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float gm = a.gamma_kv ? a.gamma_kv[dcol + piece * 8 + z] : 1.f;
                 y[z] = y[z] * inv * gm;
               }
-              rope8(y, dcol + piece * 8, a.D, a.r, u_lo + kt + rI, sm->rc);
+              rope8(y, dcol + piece * 8, a.D, a.r, u_lo + kt + rI, a.rope.c);
             } else {
 #pragma unroll
               for (int z = 0; z < 8; ++z) y[z] = 0.f;
@@ -420,95 +426,84 @@ __global__ void __launch_bounds__(kThreads, 1)
                     10000000ull, 27);
       }
     }
-  } else if (warp == 4) {
-    // ============================================================ Q load + MMA issuer
-    if (lane == 0) {
-      const uint32_t qb = smem_u32(&sm->q_full);
-      mbar_arrive_expect_tx(qb, static_cast<uint32_t>(ndc) * 16384u);
-      const int32_t qrow0 = static_cast<int32_t>(((int64_t)b * a.T + t0) * a.H);
-      for (int dc = 0; dc < ndc; ++dc) {
-        const int e = dc - dh * n_own;  // own chunk index, or outside [0, n_own)
-        uint8_t* dst = (e >= 0 && e < n_own) ? sQ + e * 16384
-                                             : sQstage + (dc - (dh == 0 ? n_own : 0)) * 16384;
-        tma_load_2d(smem_u32(dst), &tm_q, dc * 64, qrow0, qb);
-      }
-    }
-    const uint32_t idesc_qk = idesc_bf16(128, 64, 0, 0);
-    const uint32_t idesc_pv = idesc_bf16(128, 64, 0, 1);
-    const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sRing);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_full), 0, abort, a.status,
-                                                kWaitLimitNs, 29));
-    // the query rows of other queries (or past the tensor) in the box are
-    // zeroed, so they contribute nothing to S
-    if (ok && nrows < 128) {
-      for (int e = 0; e < n_own; ++e)
-        for (int pc = nrows * 8 + lane; pc < 128 * 8; pc += 32)
-          *reinterpret_cast<uint4*>(sQ + e * 16384 + swz128(pc >> 3, pc & 7)) =
-              make_uint4(0, 0, 0, 0);
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
-    if (ok && n_other > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_tmem), 0, abort, a.status,
-                                             kWaitLimitNs, 34));
-      tc_fence_after();
-    }
-    // wait for a chunk; for an HCA tail tile, zero its invalid key rows first
-    auto wait_chunk = [&](int s, uint32_t phase, int nvalid) -> bool {
-      const bool got = mbar_wait(smem_u32(&sm->full[s]), phase, abort, a.status, kWaitLimitNs, 22);
-      if (!__all_sync(0xffffffffu, got)) return false;  // warp-uniform
-      // gathered rows were written by cp.async (generic proxy); the MMA
-      // reads through the async proxy
-      if (KIND == kSparse) fence_proxy_async_smem();
-      if (KIND == kHca && nvalid < kTile) {
-        uint8_t* dst = sRing + s * 8192;
-        for (int pc = nvalid * 8 + lane; pc < kTile * 8; pc += 32)
-          *reinterpret_cast<uint4*>(dst + swz128(pc >> 3, pc & 7)) = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      return true;
-    };
-    // O += P(j) V(j): P from tensor memory (S/P buffer j & 1), V = our chunks
-    // of tile j, which follow its n_other chunks from ring slot s0
-    auto issue_pv = [&](int j, int s0) -> bool {
-      const bool got = mbar_wait(smem_u32(&sm->p_full), j & 1, abort, a.status, kWaitLimitNs, 23);
-      if (!__all_sync(0xffffffffu, got)) return false;  // warp-uniform
+  } else if (warp == 4 || warp == 9) {
+    // ============================================================ QK issuers
+    // warp 4 loads Q and issues QK for even tiles, warp 9 for odd tiles
+    const int par = warp == 4 ? 0 : 1;
+    bool ok = true;
+    if (warp == 4) {
       if (lane == 0) {
-        tc_fence_after();
-        int s = s0 + n_other;
-        if (s >= nslot) s -= nslot;
-        for (int e = 0; e < n_own; ++e) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc(sRa + s * 8192 + ks * 2048, 16, 1024, kSwizzle128B);
-            mma_bf16_ts(tO + e * 64, tS + (j & 1) * 64 + ks * 8, bd, idesc_pv,
-                        (j > 0 || ks > 0) ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&sm->empty[s]));
-          if (++s == nslot) s = 0;
+        const uint32_t qb = smem_u32(&sm->q_full);
+        mbar_arrive_expect_tx(qb, static_cast<uint32_t>(ndc) * 16384u);
+        const int32_t qrow0 = static_cast<int32_t>(((int64_t)b * a.T + t0) * a.H);
+        for (int dc = 0; dc < ndc; ++dc) {
+          const int e = dc - dh * n_own;  // own chunk index, or outside [0, n_own)
+          uint8_t* dst = (e >= 0 && e < n_own) ? sQ + e * 16384
+                                               : sQstage + (dc - (dh == 0 ? n_own : 0)) * 16384;
+          tma_load_2d(smem_u32(dst), &tm_q, dc * 64, qrow0, qb);
         }
-        mma_commit(smem_u32(&sm->pv_done));
       }
-      __syncwarp();
-      return true;
-    };
-    int slot = 0, prev_slot = 0;
-    uint32_t ph = 0;
-    for (int i = 0; i < nt && ok; ++i) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_full), 0, abort, a.status,
+                                             kWaitLimitNs, 29));
+      // the query rows of other queries (or past the tensor) in the box are
+      // zeroed, so they contribute nothing to S
+      if (ok && nrows < 128) {
+        for (int e = 0; e < n_own; ++e)
+          for (int pc = nrows * 8 + lane; pc < 128 * 8; pc += 32)
+            *reinterpret_cast<uint4*>(sQ + e * 16384 + swz128(pc >> 3, pc & 7)) =
+                make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (ok && n_other > 0)
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_tmem), 0, abort, a.status,
+                                               kWaitLimitNs, 34));
+      if (lane == 0) mbar_arrive(smem_u32(&sm->q_ready));  // also on failure: abort is set
+    } else {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_ready), 0, abort, a.status,
+                                             kWaitLimitNs, 36));
+    }
+    ok = ok && !*abort;
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const uint32_t idesc_qk = idesc_bf16(128, 64, 0, 0);
+    const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sRing);
+    for (int i = par; i < nt && ok; i += 2) {
       const int64_t kt = kbeg + (int64_t)i * kTile;
       const int nvalid = static_cast<int>((kend - kt) < kTile ? (kend - kt) : kTile);
       const int sb = i & 1;
-      const int tile_slot = slot;
+      // the S/P buffer is reused once PV of tile i-2 has read its P
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->s_free[sb]), ((i >> 1) - 1) & 1,
+                                               abort, a.status, kWaitLimitNs, 37));
+        if (!ok) break;
+        tc_fence_after();
+      }
       // S(i) = Q K(i)^T over all ndc chunks; the other half's chunks are only
       // keys, so they are released as soon as this product completes
       for (int p = 0; p < ndc && ok; ++p) {
-        ok = wait_chunk(slot, ph, nvalid);
-        if (ok && lane == 0) {
+        const int64_t c = (int64_t)i * ndc + p;
+        const int s = static_cast<int>(c % nslot);
+        const bool got = mbar_wait(smem_u32(&sm->full[s]), static_cast<uint32_t>((c / nslot) & 1),
+                                   abort, a.status, kWaitLimitNs, 22);
+        ok = __all_sync(0xffffffffu, got);  // warp-uniform
+        if (!ok) break;
+        // gathered rows were written by cp.async (generic proxy); the MMA
+        // reads through the async proxy
+        if (KIND == kSparse) fence_proxy_async_smem();
+        if (KIND == kHca && nvalid < kTile) {
+          // an HCA tail tile: zero its invalid key rows
+          uint8_t* dst = sRing + s * 8192;
+          for (int pc = nvalid * 8 + lane; pc < kTile * 8; pc += 32)
+            *reinterpret_cast<uint4*>(dst + swz128(pc >> 3, pc & 7)) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc(sRa + slot * 8192 + ks * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(sRa + s * 8192 + ks * 32, 16, 1024, kSwizzle128B);
             const uint32_t acc = (p == 0 && ks == 0) ? 0u : 1u;
             if (p < n_other) {
               mma_bf16_ts(tS + sb * 64, tQ + p * 32 + ks * 8, bd, idesc_qk, acc);
@@ -518,24 +513,63 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_ss(tS + sb * 64, ad, bd, idesc_qk, acc);
             }
           }
-          if (p < n_other) mma_commit(smem_u32(&sm->empty[slot]));
+          if (p < n_other) mma_commit(smem_u32(&sm->empty[s]));
         }
         __syncwarp();
-        if (++slot == nslot) { slot = 0; ph ^= 1u; }
       }
       if (!ok) break;
       if (lane == 0) mma_commit(smem_u32(&sm->s_full[sb]));
       __syncwarp();
-      // O += P(i-1) V(i-1), while the softmax works on S(i)
-      if (i > 0 && !(ok = issue_pv(i - 1, prev_slot))) break;
-      prev_slot = tile_slot;
     }
-    if (ok) ok = issue_pv(nt - 1, prev_slot);
+    // this thread's MMAs complete before the tensor memory is released
+    if (lane == 0) {
+      mma_commit(smem_u32(&sm->drain[par]));
+      mbar_wait(smem_u32(&sm->drain[par]), 0, nullptr, nullptr, 10000000ull, 24);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ============================================================ PV issuer
+    // O += P(i) V(i): P from tensor memory (S/P buffer i & 1), V = the n_own
+    // chunks of tile i, consecutive ring slots (the ring holds a whole number
+    // of such groups), read as one MN-major operand of N = ocols
+    const uint32_t idesc_pv = idesc_bf16(128, ocols, 0, 1);
+    const uint32_t sRa = smem_u32(sRing);
+    bool ok = true;
+    for (int i = 0; i < nt && ok; ++i) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->p_full), i & 1, abort, a.status,
+                                             kWaitLimitNs, 23));
+      if (!ok) break;
+      const int64_t c0 = (int64_t)i * ndc + n_other;
+      const int s0 = static_cast<int>(c0 % nslot);
+      if (KIND == kSparse) {
+        // this warp's view of the gathered rows, for the async proxy
+        for (int e = 0; e < n_own && ok; ++e)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&sm->full[s0 + e]),
+                                    static_cast<uint32_t>(((c0 + e) / nslot) & 1), abort,
+                                    a.status, kWaitLimitNs, 38));
+        if (!ok) break;
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bd = smem_desc(sRa + s0 * 8192 + ks * 2048, 8192, 1024, kSwizzle128B);
+          mma_bf16_ts(tO, tS + (i & 1) * 64 + ks * 8, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        for (int e = 0; e < n_own; ++e) mma_commit(smem_u32(&sm->empty[s0 + e]));
+        mma_commit(smem_u32(&sm->pv_done));
+        mma_commit(smem_u32(&sm->s_free[i & 1]));
+      }
+      __syncwarp();
+    }
     if (lane == 0) mma_commit(smem_u32(&sm->o_full));
     __syncwarp();
     if (!ok) {
       // wait (bounded) for the MMAs already issued before the memory is released
-      mbar_wait(smem_u32(&sm->o_full), 0, nullptr, nullptr, 10000000ull, 24);
+      mbar_wait(smem_u32(&sm->o_full), 0, nullptr, nullptr, 10000000ull, 39);
     }
   } else {
     // ============================================================ softmax
@@ -705,23 +739,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(dstrow + e) =
               make_float4(o[e] * inv_l, o[e + 1] * inv_l, o[e + 2] * inv_l, o[e + 3] * inv_l);
       }
-      if (row_valid && dh == 0) {
+      // the staged row of this thread goes out as one bulk copy by the copy
+      // engine (all 128 rows stream in parallel)
+      const bool direct = a.nsplit == 1 && !a.partials;
+      fence_proxy_async_smem();
+      if (row_valid) {
         const int64_t row = ((int64_t)b * a.T + t0 + g) * a.H + h;
-        if (a.nsplit == 1) a.lse[row] = lse;
-        else a.part_lse[row * a.nsplit + split] = lse;
-      }
-      __syncwarp();
-      // the warp writes its rows one at a time, each lane a 16-byte piece
-      const int nrw = min(32, nrows - quad * 32);
-      for (int rr = 0; rr < nrw; ++rr) {
-        const int r2 = quad * 32 + rr;
-        const int g2 = r2 / a.H, h2 = r2 % a.H;
-        const int64_t row = ((int64_t)b * a.T + t0 + g2) * a.H + h2;
-        const float* srow = stage + rr * (ocols + 4);
-        float* dst = a.nsplit == 1 ? a.o + row * a.D + dh * ocols
-                                   : a.part_o + (row * a.nsplit + split) * a.D + dh * ocols;
-        for (int c = lane * 4; c < ocols; c += 128)
-          *reinterpret_cast<float4*>(dst + c) = *reinterpret_cast<const float4*>(srow + c);
+        float* dst = direct ? a.o + row * a.D + dh * ocols
+                            : a.part_o + (row * a.nsplit + split) * a.D + dh * ocols;
+        bulk_copy_s2g(dst, smem_u32(stage + lane * (ocols + 4)),
+                      static_cast<uint32_t>(ocols) * 4u);
+        bulk_commit();
+        if (dh == 0) {
+          if (direct) a.lse[row] = lse;
+          else a.part_lse[row * a.nsplit + split] = lse;
+        }
+        bulk_wait_read();
       }
     } else {
       // drain: make sure no MMA is still writing the accumulators
@@ -753,6 +786,10 @@ bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int nu
   if (tps < 1) tps = 1;
   nsplit = (tiles + tps - 1) / tps;
   if (nsplit < 1) nsplit = 1;
+  if (nsplit > kMaxMergeParts) {  // the merges weigh at most this many partials per row
+    tps = (tiles + kMaxMergeParts - 1) / kMaxMergeParts;
+    nsplit = (tiles + tps - 1) / tps;
+  }
   if (nsplit * nds > 65535 || n_rb > 65535) return false;
   const int ndc = D / 64;
   if (ndc % nds) return false;  // the halves of the output are whole chunks
@@ -768,6 +805,9 @@ bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int nu
   const size_t fixed = 1024 + (size_t)n_own * 16384 + sizeof(AttnShared);
   int nslot = static_cast<int>((227 * 1024 - fixed) / 8192);
   if (nslot > kMaxSlots) nslot = kMaxSlots;
+  // the own chunks of a tile are consecutive slots: a tile's own group
+  // starts at a multiple of n_own and the ring holds whole groups
+  nslot -= nslot % n_own;
   // QK of the next tile (all ndc chunks) is issued before PV of the current
   // one (our n_own chunks): both must fit the ring at once, and the staging
   // of the other half of Q (two slots per chunk) fits at its end

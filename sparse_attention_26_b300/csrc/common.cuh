@@ -215,6 +215,22 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from shared to global memory by the copy engine, then the waits.
+__device__ __forceinline__ void bulk_copy_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// every bulk copy this thread committed has finished reading shared memory
+// (the global writes complete before the grid does)
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

@@ -24,7 +24,7 @@ namespace hattn {
 
 namespace {
 
-constexpr int kCompressThreads = 256;
+constexpr int kCompressThreads = 512;
 constexpr int kMaxW = 512;
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
@@ -50,7 +50,7 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&y)[8]) {
 __global__ void __launch_bounds__(kCompressThreads)
     compress_kernel(const __grid_constant__ CompressArgs a) {
   __shared__ float alpha[kMaxW];
-  __shared__ float partial[2048];  // S x (D + dI) floats, S*(NC) <= 256 -> <= 2048
+  __shared__ float partial[4096];  // S x (D + dI) floats, S * NC <= 512 -> <= 4096
   __shared__ float rc[4][kMaxRopePairs];
   __shared__ float red[kCompressThreads / 32];
   __shared__ float inv_rms_s;
@@ -99,24 +99,42 @@ __global__ void __launch_bounds__(kCompressThreads)
     }
     __syncthreads();
 
-    // weighted sums: thread (c, s) covers piece c over tokens s, s+S, ...
+    // weighted sums: thread (c, s) covers piece c over tokens s, s+S, ...,
+    // eight token rows in flight at a time
     if (tid < S * NC) {
       const int c = tid % NC;
       const int s = tid / NC;
+      const __nv_bfloat16* src = c < NCk ? a.kv_raw + (int64_t)b * a.L_cap * a.D + c * 8
+                                         : a.ik_raw + (int64_t)b * a.L_cap * a.dI + (c - NCk) * 8;
+      const int64_t stride = c < NCk ? a.D : a.dI;
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-      for (int i = s; i < a.w; i += S) {
-        const int64_t u = u0 + i;
-        if (u < 0) continue;
-        const float al = alpha[i];
-        float x[8];
-        if (c < NCk)
-          load8(a.kv_raw + ((int64_t)b * a.L_cap + u) * a.D + c * 8, x);
-        else
-          load8(a.ik_raw + ((int64_t)b * a.L_cap + u) * a.dI + (c - NCk) * 8, x);
+      for (int i0 = s; i0 < a.w; i0 += 8 * S) {
+        uint4 v[8];
+        float al[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(al, x[e], acc[e]);
+        for (int q = 0; q < 8; ++q) {
+          const int i = i0 + q * S;
+          const int64_t u = u0 + i;
+          const bool live = i < a.w && u >= 0;
+          v[q] = live ? __ldg(reinterpret_cast<const uint4*>(src + u * stride))
+                      : make_uint4(0, 0, 0, 0);
+          al[q] = live ? alpha[i] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float x[8];
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[q]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h[e]);
+            x[2 * e] = f.x;
+            x[2 * e + 1] = f.y;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = fmaf(al[q], x[e], acc[e]);
+        }
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) partial[s * width + c * 8 + e] = acc[e];

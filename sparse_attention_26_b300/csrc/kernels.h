@@ -90,8 +90,9 @@ struct AttnArgs {
   const int32_t* pos;           // [B][T]
   float* o;                     // [B][T][H][D] fp32 (direct output when nsplit == 1)
   float* lse;                   // [B][T][H]
-  float* part_o;                // [B*T*H][nsplit][D] partials (nsplit > 1)
+  float* part_o;                // [B*T*H][nsplit][D] partials (nsplit > 1 or partials)
   float* part_lse;              // [B*T*H][nsplit]
+  int partials;                 // 1: always write partials, even for one split
   int* status;
   int kind, B, T, H, D, r;
   int64_t N_rows;               // rows per sequence of kv (N_cap or L_cap)
@@ -124,9 +125,14 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
+// Sink-augmented merge of nb branches, each given as nsplit[i] partials per
+// row ([rows][nsplit][D] fp32 with [rows][nsplit] log-sum-exps; a branch
+// output is the case nsplit = 1).
+constexpr int kMaxMergeParts = 128;
 struct MergeArgs {
-  const float* o[4];            // fp32 branch outputs
+  const float* o[4];            // fp32 partials of each branch
   const float* lse[4];
+  int nsplit[4];
   int nb;
   const float* sink;    // [H] or null
   const int32_t* pos;   // [B][T]

@@ -4,13 +4,19 @@
 // softmax sum, with its log-sum-exp) merged in a fixed split order into the
 // branch output o and lse (fp32).
 //
-// merge: the sink-augmented merge of the branch outputs ("DeepSeek-V4" atlas,
+// merge: the sink-augmented merge of the branches ("DeepSeek-V4" atlas,
 // section "Spec sheet / Core block": attention sinks; provenance 16: inverse
-// RoPE on the outputs):
-//     Z = sum_i exp(lse_i) + exp(sink_h),  y = sum_i exp(lse_i) o_i / Z,
+// RoPE on the outputs), over every split partial of every branch at once:
+//     Z = sum_(b,s) exp(lse_bs) + exp(sink_h),  y = sum_(b,s) exp(lse_bs) o_bs / Z,
 //     out = y with its last r dims rotated back by the query position.
-// Both are HBM-bound elementwise passes: one thread per 8 columns of a
-// (query, head) row, 16-byte vector loads and stores.
+// A branch's own normalisation cancels: merging its partials directly equals
+// merging its combined output.
+//
+// A block of 256 threads merges two (query, head) rows, 128 threads each:
+// the first warp of a row loads the row's log-sum-exps (one per lane),
+// reduces them with shuffles and leaves the weights in shared memory; then
+// every thread accumulates 4 columns over all partials (16-byte loads,
+// independent across partials).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -18,122 +24,123 @@ namespace hattn {
 
 namespace {
 
-constexpr int kMergeThreads = 256;
+constexpr int kRowThreads = 128;  // threads per row
+constexpr int kMergeBlock = 256;  // two rows per block
 
-// One thread per (row, 8-column group): every load of a row's partials is
-// independent, so a launch keeps thousands of 16-byte loads in flight.
-__global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArgs a) {
-  const int groups = a.D / 8;
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x;
-  const int64_t row = gid / groups;
-  const int c8 = static_cast<int>(gid - row * groups);
-  if (row >= a.rows) return;
-  const float* pl = a.part_lse + row * a.nsplit;
-  float mx = -INFINITY;
-  for (int s = 0; s < a.nsplit; ++s) mx = fmaxf(mx, pl[s]);
-  float* o = a.o + row * a.D + c8 * 8;
-  if (mx == -INFINITY) {
-    reinterpret_cast<float4*>(o)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    reinterpret_cast<float4*>(o)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c8 == 0) a.lse[row] = -INFINITY;
-    return;
+struct Part {
+  const float* o;
+  const float* lse;
+  int nsplit;
+};
+
+// Weights exp(lse_k - log Z) of the row's partials into coef[], with Z the sum
+// over the partials (and the sink); run by one warp.  Returns log Z (or -inf
+// when the row has no key and no sink).
+__device__ __forceinline__ float row_weights(const Part* parts, int nb, int total, int64_t row,
+                                             float sink, bool has_sink, float* coef, int lane) {
+  float mx = has_sink ? sink : -INFINITY;
+  for (int k = lane; k < total; k += 32) {
+    int i = 0, s = k;
+    while (s >= parts[i].nsplit) s -= parts[i++].nsplit;
+    const float v = parts[i].lse[row * parts[i].nsplit + s];
+    coef[k] = v;
+    mx = fmaxf(mx, v);
   }
-  float z = 0.f;
-  float acc[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  const float* po = a.part_o + row * a.nsplit * a.D + c8 * 8;
-#pragma unroll 4
-  for (int s = 0; s < a.nsplit; ++s) {
-    const float c = __expf(pl[s] - mx);
-    z += c;
-    const float4 v0 = *reinterpret_cast<const float4*>(po + (int64_t)s * a.D);
-    const float4 v1 = *reinterpret_cast<const float4*>(po + (int64_t)s * a.D + 4);
-    // an empty split has weight 0 and zero partials
-    acc[0] = fmaf(c, v0.x, acc[0]);
-    acc[1] = fmaf(c, v0.y, acc[1]);
-    acc[2] = fmaf(c, v0.z, acc[2]);
-    acc[3] = fmaf(c, v0.w, acc[3]);
-    acc[4] = fmaf(c, v1.x, acc[4]);
-    acc[5] = fmaf(c, v1.y, acc[5]);
-    acc[6] = fmaf(c, v1.z, acc[6]);
-    acc[7] = fmaf(c, v1.w, acc[7]);
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (mx == -INFINITY) {
+    for (int k = lane; k < total; k += 32) coef[k] = 0.f;
+    return -INFINITY;
   }
-  const float iz = 1.f / z;
-  reinterpret_cast<float4*>(o)[0] = make_float4(acc[0] * iz, acc[1] * iz, acc[2] * iz, acc[3] * iz);
-  reinterpret_cast<float4*>(o)[1] = make_float4(acc[4] * iz, acc[5] * iz, acc[6] * iz, acc[7] * iz);
-  if (c8 == 0) a.lse[row] = mx + __logf(z);
+  float z = (lane == 0 && has_sink) ? __expf(sink - mx) : 0.f;
+  for (int k = lane; k < total; k += 32) z += __expf(coef[k] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  const float lz = mx + __logf(z);
+  for (int k = lane; k < total; k += 32) coef[k] = __expf(coef[k] - lz);
+  return lz;
 }
 
-// One thread per (row, 8-column group), as above.
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeArgs a) {
+// Columns 4*c4 .. 4*c4+3 of the row: sum over the partials of weight x value.
+__device__ __forceinline__ float4 row_columns(const Part* parts, int nb, int64_t row, int D,
+                                              int c4, const float* coef) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int k = 0;
+  for (int i = 0; i < nb; ++i) {
+    const float* base = parts[i].o + row * parts[i].nsplit * D + 4 * c4;
+#pragma unroll 4
+    for (int s = 0; s < parts[i].nsplit; ++s, ++k) {
+      const float c = coef[k];
+      const float4 v = *reinterpret_cast<const float4*>(base + (int64_t)s * D);
+      // an empty split has weight 0 and zero partials
+      acc.x = fmaf(c, v.x, acc.x);
+      acc.y = fmaf(c, v.y, acc.y);
+      acc.z = fmaf(c, v.z, acc.z);
+      acc.w = fmaf(c, v.w, acc.w);
+    }
+  }
+  return acc;
+}
+
+__global__ void __launch_bounds__(kMergeBlock) combine_kernel(const CombineArgs a) {
+  __shared__ float coef[kMergeBlock / kRowThreads][kMaxMergeParts];
+  __shared__ float lz_s[kMergeBlock / kRowThreads];
+  const int half = threadIdx.x / kRowThreads, t = threadIdx.x % kRowThreads;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kMergeBlock / kRowThreads) + half;
+  const bool live = row < a.rows;
+  Part p{a.part_o, a.part_lse, a.nsplit};
+  if (live && t < 32) lz_s[half] = row_weights(&p, 1, a.nsplit, row, 0.f, false, coef[half], t);
+  __syncthreads();
+  if (!live) return;
+  for (int c4 = t; c4 < a.D / 4; c4 += kRowThreads)
+    *reinterpret_cast<float4*>(a.o + row * a.D + 4 * c4) = row_columns(&p, 1, row, a.D, c4, coef[half]);
+  if (t == 0) a.lse[row] = lz_s[half];
+}
+
+__global__ void __launch_bounds__(kMergeBlock) merge_kernel(const __grid_constant__ MergeArgs a) {
+  __shared__ float coef[kMergeBlock / kRowThreads][kMaxMergeParts];
+  __shared__ float lz_s[kMergeBlock / kRowThreads];
   __shared__ float rc[4][kMaxRopePairs];
-  for (int i = threadIdx.x; i < a.r / 2; i += kMergeThreads) {
+  for (int i = threadIdx.x; i < a.r / 2; i += kMergeBlock) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) rc[c][i] = a.rope.c[c][i];
   }
-  __syncthreads();
-  const int groups = a.D / 8;
+  const int half = threadIdx.x / kRowThreads, t = threadIdx.x % kRowThreads;
   const int64_t rows = static_cast<int64_t>(a.B) * a.T * a.H;
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x;
-  const int64_t row = gid / groups;
-  const int c8 = static_cast<int>(gid - row * groups);
-  if (row >= rows) return;
-  const int h = static_cast<int>(row % a.H);
-  const int64_t bt = row / a.H;
-  float lse_b[4];
-  float mx = a.sink ? a.sink[h] : -INFINITY;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kMergeBlock / kRowThreads) + half;
+  const bool live = row < rows;
+  Part parts[4];
+  int total = 0;
   for (int i = 0; i < a.nb; ++i) {
-    lse_b[i] = a.lse[i][row];
-    mx = fmaxf(mx, lse_b[i]);
+    parts[i] = Part{a.o[i], a.lse[i], a.nsplit[i]};
+    total += a.nsplit[i];
   }
-  const int d = c8 * 8;
-  __nv_bfloat16* out = a.out + row * a.D + d;
-  if (mx == -INFINITY) {
-    *reinterpret_cast<uint4*>(out) = make_uint4(0, 0, 0, 0);
-    if (c8 == 0 && a.lse_out) a.lse_out[row] = -INFINITY;
-    return;
-  }
-  float z = a.sink ? __expf(a.sink[h] - mx) : 0.f;
-  for (int i = 0; i < a.nb; ++i) z += __expf(lse_b[i] - mx);
-  const float lz = mx + __logf(z);
-  float y[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) y[e] = 0.f;
-  for (int i = 0; i < a.nb; ++i) {
-    const float coef = __expf(lse_b[i] - lz);
-    if (coef == 0.f) continue;  // an empty branch (its o is not read)
-    const float4 v0 = *reinterpret_cast<const float4*>(a.o[i] + row * a.D + d);
-    const float4 v1 = *reinterpret_cast<const float4*>(a.o[i] + row * a.D + d + 4);
-    y[0] = fmaf(coef, v0.x, y[0]);
-    y[1] = fmaf(coef, v0.y, y[1]);
-    y[2] = fmaf(coef, v0.z, y[2]);
-    y[3] = fmaf(coef, v0.w, y[3]);
-    y[4] = fmaf(coef, v1.x, y[4]);
-    y[5] = fmaf(coef, v1.y, y[5]);
-    y[6] = fmaf(coef, v1.z, y[6]);
-    y[7] = fmaf(coef, v1.w, y[7]);
-  }
+  const int h = live ? static_cast<int>(row % a.H) : 0;
+  if (live && t < 32)
+    lz_s[half] = row_weights(parts, a.nb, total, row, a.sink ? a.sink[h] : 0.f,
+                             a.sink != nullptr, coef[half], t);
+  __syncthreads();
+  if (!live) return;
+  const int64_t pos = a.pos[row / a.H];
   const int d0 = a.D - a.r;
-  const int64_t p = a.pos[bt];
+  for (int c4 = t; c4 < a.D / 4; c4 += kRowThreads) {
+    const float4 acc = row_columns(parts, a.nb, row, a.D, c4, coef[half]);
+    float y[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-  for (int e = 0; e < 8; e += 2) {
-    const int dd = d + e;
-    if (dd >= d0) {
-      float sn, cs;
-      rope_cs(rc, (dd - d0) >> 1, -p, &sn, &cs);
-      const float x0 = y[e], x1 = y[e + 1];
-      y[e] = x0 * cs - x1 * sn;
-      y[e + 1] = x0 * sn + x1 * cs;
+    for (int e = 0; e < 4; e += 2) {
+      const int d = 4 * c4 + e;
+      if (d >= d0) {
+        float sn, cs;
+        rope_cs(rc, (d - d0) >> 1, -pos, &sn, &cs);
+        const float x0 = y[e], x1 = y[e + 1];
+        y[e] = x0 * cs - x1 * sn;
+        y[e + 1] = x0 * sn + x1 * cs;
+      }
     }
+    *reinterpret_cast<uint2*>(a.out + row * a.D + 4 * c4) =
+        make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
   }
-  uint4 u;
-  u.x = pack_bf16x2(y[0], y[1]);
-  u.y = pack_bf16x2(y[2], y[3]);
-  u.z = pack_bf16x2(y[4], y[5]);
-  u.w = pack_bf16x2(y[6], y[7]);
-  *reinterpret_cast<uint4*>(out) = u;
-  if (c8 == 0 && a.lse_out) a.lse_out[row] = lz;
+  if (t == 0 && a.lse_out) a.lse_out[row] = lz_s[half];
 }
 
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
@@ -151,16 +158,18 @@ __global__ void wait_selftest_kernel(uint64_t timeout_ns, int* status) {
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
-  const int64_t blocks = (a.rows * (a.D / 8) + kMergeThreads - 1) / kMergeThreads;
-  combine_kernel<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(a);
+  const int per = kMergeBlock / kRowThreads;
+  const int64_t blocks = (a.rows + per - 1) / per;
+  combine_kernel<<<static_cast<unsigned>(blocks), kMergeBlock, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.B) * a.T * a.H;
   if (rows <= 0) return cudaSuccess;
-  const int64_t blocks = (rows * (a.D / 8) + kMergeThreads - 1) / kMergeThreads;
-  merge_kernel<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(a);
+  const int per = kMergeBlock / kRowThreads;
+  const int64_t blocks = (rows + per - 1) / per;
+  merge_kernel<<<static_cast<unsigned>(blocks), kMergeBlock, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -46,7 +46,11 @@ _SIGS = {
                               _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
     "hattn_swa_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
                               _i32, _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
-    "hattn_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32]),
+    "hattn_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32]),
+    "hattn_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64]),
+    "hattn_lse_merge_splits": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i32),
+                                      _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
+                                      _vp]),
     "hattn_lse_merge": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _vp, _vp, _i32,
                                _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp]),
     "hattn_status_string": (ctypes.c_char_p, [_i32]),
@@ -219,8 +223,28 @@ def topk_select(scores, pos, *, k, m=4, idx_out=None, stream=None):
 
 
 # ------------------------------------------------------------------ attention
-def attn_workspace_bytes(kind, B, T, H, D, n_keys, q_prepped=False):
-    return int(lib().hattn_attn_workspace_bytes(kind, B, T, H, D, n_keys, int(bool(q_prepped))))
+def attn_workspace_bytes(kind, B, T, H, D, n_keys, q_prepped=False, partials=False):
+    return int(lib().hattn_attn_workspace_bytes(kind, B, T, H, D, n_keys, int(bool(q_prepped)),
+                                                int(bool(partials))))
+
+
+def attn_splits(kind, B, T, H, D, n_keys):
+    """Key splits (partials per row) of an attention call of this shape."""
+    return int(lib().hattn_attn_splits(kind, B, T, H, D, n_keys))
+
+
+class Partials:
+    """Split partials of one branch, viewing an attention call's workspace:
+    o [B*T*H, nsplit, D] fp32, lse [B*T*H, nsplit] fp32."""
+
+    def __init__(self, workspace, q_prepped, B, T, H, D, nsplit):
+        rows = B * T * H
+        off = 0 if q_prepped else rows * D * 2
+        n_o = rows * nsplit * D
+        f = workspace[off:off + (n_o + rows * nsplit) * 4].view(torch.float32)
+        self.o = f[:n_o].view(rows, nsplit, D)
+        self.lse = f[n_o:].view(rows, nsplit)
+        self.nsplit = nsplit
 
 
 def query_prep(q, pos, *, r, gamma_q=None, rope_base=10000.0, eps=1e-6, q_out=None, stream=None):
@@ -248,19 +272,27 @@ def _attn_out(q, o, lse):
     return o, lse
 
 
-def _ws(kind, q, n_keys, workspace, q_prepped):
+def _ws(kind, q, n_keys, workspace, q_prepped, partials=False):
     B, T, H, D = q.shape
-    need = attn_workspace_bytes(kind, B, T, H, D, n_keys, q_prepped)
+    need = attn_workspace_bytes(kind, B, T, H, D, n_keys, q_prepped, partials)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     return workspace, (workspace.numel() * workspace.element_size() if workspace is not None
                        else 0)
 
 
+def _result(kind, q, n_keys, o, lse, workspace, q_prepped, partials):
+    if not partials:
+        return o, lse
+    B, T, H, D = q.shape
+    return Partials(workspace, q_prepped, B, T, H, D, attn_splits(kind, B, T, H, D, n_keys))
+
+
 def sparse_attn(q, kv_c, idx, pos, *, r, gamma_q=None, rope_base=10000.0, eps=1e-6, scale=None,
-                o=None, lse=None, workspace=None, q_prepped=False, stream=None):
-    """CSA branch over the selected entries; returns (o fp32, lse fp32).
-    q_prepped: q is the output of query_prep."""
+                o=None, lse=None, workspace=None, q_prepped=False, partials=False, stream=None):
+    """CSA branch over the selected entries; returns (o fp32, lse fp32), or a
+    Partials view of the workspace when partials=True.  q_prepped: q is the
+    output of query_prep."""
     _need(q, "q", torch.bfloat16, 4)
     _need(kv_c, "kv_c", torch.bfloat16, 3)
     _need(idx, "idx", torch.int32, 3)
@@ -269,16 +301,17 @@ def sparse_attn(q, kv_c, idx, pos, *, r, gamma_q=None, rope_base=10000.0, eps=1e
     B, T, H, D = q.shape
     k = idx.shape[2]
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    o, lse = _attn_out(q, o, lse)
-    workspace, wsb = _ws(KIND_SPARSE, q, k, workspace, q_prepped)
+    if not partials:
+        o, lse = _attn_out(q, o, lse)
+    workspace, wsb = _ws(KIND_SPARSE, q, k, workspace, q_prepped, partials)
     _check(lib().hattn_sparse_attn(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_c), _ptr(idx), _ptr(pos), B, T,
                                    H, D, kv_c.shape[1], k, r, rope_base, eps, scale, _ptr(o),
                                    _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
-    return o, lse
+    return _result(KIND_SPARSE, q, k, o, lse, workspace, q_prepped, partials)
 
 
 def hca_attn(q, kv_h, pos, *, r, m=128, gamma_q=None, rope_base=10000.0, eps=1e-6, scale=None,
-             o=None, lse=None, workspace=None, q_prepped=False, stream=None):
+             o=None, lse=None, workspace=None, q_prepped=False, partials=False, stream=None):
     """HCA branch, dense over the visible compressed entries; returns (o, lse)."""
     _need(q, "q", torch.bfloat16, 4)
     _need(kv_h, "kv_h", torch.bfloat16, 3)
@@ -286,17 +319,18 @@ def hca_attn(q, kv_h, pos, *, r, m=128, gamma_q=None, rope_base=10000.0, eps=1e-
     _opt(gamma_q, "gamma_q", torch.float32)
     B, T, H, D = q.shape
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    o, lse = _attn_out(q, o, lse)
-    workspace, wsb = _ws(KIND_HCA, q, kv_h.shape[1], workspace, q_prepped)
+    if not partials:
+        o, lse = _attn_out(q, o, lse)
+    workspace, wsb = _ws(KIND_HCA, q, kv_h.shape[1], workspace, q_prepped, partials)
     _check(lib().hattn_hca_attn(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_h), _ptr(pos), B, T, H, D,
                                 kv_h.shape[1], m, r, rope_base, eps, scale, _ptr(o), _ptr(lse),
                                 _ptr(workspace), wsb, _stream(stream)))
-    return o, lse
+    return _result(KIND_HCA, q, kv_h.shape[1], o, lse, workspace, q_prepped, partials)
 
 
 def swa_attn(q, kv_raw, pos, *, r, W=128, gamma_q=None, gamma_kv=None, rope_base=10000.0,
              eps=1e-6, scale=None, o=None, lse=None, workspace=None, q_prepped=False,
-             stream=None):
+             partials=False, stream=None):
     """SWA branch over the last W raw tokens (normalised and roped on load)."""
     _need(q, "q", torch.bfloat16, 4)
     _need(kv_raw, "kv_raw", torch.bfloat16, 3)
@@ -305,12 +339,13 @@ def swa_attn(q, kv_raw, pos, *, r, W=128, gamma_q=None, gamma_kv=None, rope_base
     _opt(gamma_kv, "gamma_kv", torch.float32)
     B, T, H, D = q.shape
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    o, lse = _attn_out(q, o, lse)
-    workspace, wsb = _ws(KIND_SWA, q, W, workspace, q_prepped)
+    if not partials:
+        o, lse = _attn_out(q, o, lse)
+    workspace, wsb = _ws(KIND_SWA, q, W, workspace, q_prepped, partials)
     _check(lib().hattn_swa_attn(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_raw), _ptr(gamma_kv), _ptr(pos),
                                 B, T, H, D, kv_raw.shape[1], W, r, rope_base, eps, scale, _ptr(o),
                                 _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
-    return o, lse
+    return _result(KIND_SWA, q, W, o, lse, workspace, q_prepped, partials)
 
 
 # ------------------------------------------------------------------ merge
@@ -336,6 +371,32 @@ def lse_merge(o_list, lse_list, pos, *, r, sink=None, rope_base=10000.0, out=Non
     lp = (_vp * nb)(*[l.data_ptr() for l in lse_list])
     _check(lib().hattn_lse_merge(op, lp, nb, _ptr(sink), _ptr(pos), B, T, H, D, r, rope_base,
                                  _ptr(out), _ptr(lse_out), _stream(stream)))
+    return out, lse_out
+
+
+def lse_merge_splits(parts, pos, *, r, H, sink=None, rope_base=10000.0, out=None, lse_out=None,
+                     stream=None):
+    """Sink-augmented merge over the split partials of 1..4 branches (a list
+    of Partials) + inverse RoPE; returns (out bf16 [B, T, H, D], lse)."""
+    nb = len(parts)
+    if nb < 1:
+        raise ValueError("need 1..4 branches")
+    _need(pos, "pos", torch.int32, 2)
+    _opt(sink, "sink", torch.float32)
+    B, T = pos.shape
+    D = parts[0].o.shape[2]
+    dev = parts[0].o.device
+    if out is None:
+        out = torch.empty((B, T, H, D), dtype=torch.bfloat16, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16)
+    _need(lse_out, "lse_out", torch.float32)
+    op = (_vp * nb)(*[p.o.data_ptr() for p in parts])
+    lp = (_vp * nb)(*[p.lse.data_ptr() for p in parts])
+    ns = (_i32 * nb)(*[p.nsplit for p in parts])
+    _check(lib().hattn_lse_merge_splits(op, lp, ns, nb, _ptr(sink), _ptr(pos), B, T, H, D, r,
+                                        rope_base, _ptr(out), _ptr(lse_out), _stream(stream)))
     return out, lse_out
 
 

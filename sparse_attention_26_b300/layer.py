@@ -71,7 +71,9 @@ class HybridLayer:
         for name, kind, nk in self._branch_kinds():
             b["o_" + name] = torch.empty((B, T, H, D), dtype=torch.float32, device=dev)
             b["l_" + name] = torch.empty((B, T, H), dtype=torch.float32, device=dev)
-            ws = hattn.attn_workspace_bytes(kind, B, T, H, D, nk, q_prepped=True)
+            ws = max(hattn.attn_workspace_bytes(kind, B, T, H, D, nk, q_prepped=True),
+                     hattn.attn_workspace_bytes(kind, B, T, H, D, nk, q_prepped=True,
+                                                partials=True))
             b["ws_" + name] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         self._bufs[T] = b
         return b
@@ -83,7 +85,8 @@ class HybridLayer:
                                             ("swa", hattn.KIND_SWA, wl.W)]
                 if n in wl.branches]
 
-    def step(self, q, iq, w, pos, sink, t_new=None, events=None, side_stream=None):
+    def step(self, q, iq, w, pos, sink, t_new=None, events=None, side_stream=None,
+             branch_outputs=False):
         """One pass of the hot path for queries q [B,T,H,D] at positions pos.
 
         t_new: position of the newest token (compresses the entries it
@@ -91,8 +94,11 @@ class HybridLayer:
         dict name -> (start, end) torch.cuda.Event pairs recorded around the
         calls.  side_stream: a second CUDA stream; when given, the HCA and
         SWA branches run on it, concurrently with the indexer, top-k and CSA
-        branch, joined before the merge.  Returns (out bf16 [B,T,H,D], lse
-        fp32 [B,T,H])."""
+        branch, joined before the merge.  branch_outputs: combine each
+        branch's key splits into its own (o, lse) (kept in the buffers) and
+        merge those; by default the branches leave their split partials and
+        one merge weighs all of them.  Returns (out bf16 [B,T,H,D], lse fp32
+        [B,T,H])."""
         wl, r = self.wl, self.raw
         B, T = q.shape[0], q.shape[1]
         b = self.buffers(T)
@@ -125,17 +131,25 @@ class HybridLayer:
         hattn.query_prep(q, pos, r=wl.r, q_out=b["qt"])
         ev("qprep", 1)
         qt = b["qt"]
+        parts = {}
+
+        def outs(name):
+            if branch_outputs:
+                return dict(o=b["o_" + name], lse=b["l_" + name])
+            return dict(partials=True)
 
         def dense_branches():
             if "hca" in wl.branches:
                 ev("hca", 0)
-                hattn.hca_attn(qt, self.kv_h, pos, r=wl.r, m=wl.m_hca, o=b["o_hca"],
-                               lse=b["l_hca"], workspace=b["ws_hca"], q_prepped=True)
+                parts["hca"] = hattn.hca_attn(qt, self.kv_h, pos, r=wl.r, m=wl.m_hca,
+                                              workspace=b["ws_hca"], q_prepped=True,
+                                              **outs("hca"))
                 ev("hca", 1)
             if "swa" in wl.branches:
                 ev("swa", 0)
-                hattn.swa_attn(qt, r["kv_raw"], pos, r=wl.r, W=wl.W, o=b["o_swa"],
-                               lse=b["l_swa"], workspace=b["ws_swa"], q_prepped=True)
+                parts["swa"] = hattn.swa_attn(qt, r["kv_raw"], pos, r=wl.r, W=wl.W,
+                                              workspace=b["ws_swa"], q_prepped=True,
+                                              **outs("swa"))
                 ev("swa", 1)
 
         joined = None
@@ -153,31 +167,38 @@ class HybridLayer:
             hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
             ev("topk", 1)
             ev("sparse", 0)
-            hattn.sparse_attn(qt, self.kv_c, b["idx"], pos, r=wl.r, o=b["o_csa"],
-                              lse=b["l_csa"], workspace=b["ws_csa"], q_prepped=True)
+            parts["csa"] = hattn.sparse_attn(qt, self.kv_c, b["idx"], pos, r=wl.r,
+                                             workspace=b["ws_csa"], q_prepped=True,
+                                             **outs("csa"))
             ev("sparse", 1)
         if joined is None:
             dense_branches()
         else:
             main.wait_stream(joined)
-        o_list = [b["o_" + n] for n, _, _ in self._branch_kinds()]
-        l_list = [b["l_" + n] for n, _, _ in self._branch_kinds()]
         ev("merge", 0)
-        hattn.lse_merge(o_list, l_list, pos, r=wl.r, sink=sink, out=b["out"], lse_out=b["lse"])
+        if branch_outputs:
+            o_list = [b["o_" + n] for n, _, _ in self._branch_kinds()]
+            l_list = [b["l_" + n] for n, _, _ in self._branch_kinds()]
+            hattn.lse_merge(o_list, l_list, pos, r=wl.r, sink=sink, out=b["out"],
+                            lse_out=b["lse"])
+        else:
+            hattn.lse_merge_splits([parts[n] for n, _, _ in self._branch_kinds()], pos, r=wl.r,
+                                   H=wl.H, sink=sink, out=b["out"], lse_out=b["lse"])
         ev("merge", 1)
         return b["out"], b["lse"]
 
-    def launches_per_step(self, T, t_new=None):
+    def launches_per_step(self, T, t_new=None, branch_outputs=False):
         """Kernels one step launches: the query preparation, each branch's
-        attention kernel (plus its combine with split-KV), the indexer and
-        top-k of CSA, the merge, and the compressions the new token needs."""
+        attention kernel (plus its combine with split-KV when branch outputs
+        are formed), the indexer and top-k of CSA, the merge, and the
+        compressions the new token needs."""
         wl, B, D, H = self.wl, self.B, self.D, self.wl.H
         n = 2  # query preparation, merge
         if t_new is not None:
             n += int("csa" in wl.branches and (t_new + 1) % wl.m_csa == 0)
             n += int("hca" in wl.branches and (t_new + 1) % wl.m_hca == 0)
         for name, kind, nk in self._branch_kinds():
-            n += 1 + int(hattn.attn_workspace_bytes(kind, B, T, H, D, nk, q_prepped=True) > 0)
+            n += 1 + int(branch_outputs and hattn.attn_splits(kind, B, T, H, D, nk) > 1)
             if name == "csa":
                 n += 2  # indexer scores + top-k select
         return n

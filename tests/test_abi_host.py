@@ -139,3 +139,30 @@ def test_workspace_sizes_scale_with_splits(L):
     # a long prefill row block has no split and needs no partials
     assert hattn.attn_workspace_bytes(hattn.KIND_SPARSE, 1, 8192, 64, 512, 512,
                                       q_prepped=True) == 0
+
+
+def test_split_counts_and_partials_workspace(L):
+    # the 1M decode HCA branch splits its 8192 keys across the SMs
+    n = hattn.attn_splits(hattn.KIND_HCA, 8, 1, 128, 512, 8192)
+    assert n > 1
+    part = hattn.attn_workspace_bytes(hattn.KIND_HCA, 8, 1, 128, 512, 8192, q_prepped=True,
+                                      partials=True)
+    assert part == 8 * 128 * n * (512 + 1) * 4
+    # partials are kept even when a call has a single split
+    assert hattn.attn_splits(hattn.KIND_SPARSE, 1, 8192, 64, 512, 512) == 1
+    assert hattn.attn_workspace_bytes(hattn.KIND_SPARSE, 1, 8192, 64, 512, 512, q_prepped=True,
+                                      partials=True) == 8192 * 64 * 513 * 4
+    assert hattn.attn_splits(7, 1, 1, 1, 64, 10) == 0
+
+
+def test_merge_splits_validation(L):
+    N = None
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    ns = (ctypes.c_int * 2)(100, 40)
+    rc = L.hattn_lse_merge_splits(arr, arr, ns, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
+    assert rc == hattn.INVALID_ARG and "partials" in _err(L)
+    ns = (ctypes.c_int * 2)(3, 0)
+    rc = L.hattn_lse_merge_splits(arr, arr, ns, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
+    assert rc == hattn.INVALID_ARG and "nsplit" in _err(L)
+    rc = L.hattn_lse_merge_splits(arr, arr, N, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
+    assert rc == hattn.INVALID_ARG

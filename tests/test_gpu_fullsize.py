@@ -49,15 +49,21 @@ def _host_rows(t, b, rows):
 
 
 def _run(wl, t_new=None, side=False):
+    """The layer step twice on the same inputs: first forming each branch's
+    output (kept for the stage checks), then as the benchmark runs it (split
+    partials merged in one pass, HCA and SWA on a second stream when `side`).
+    Returns the inputs, the layer and both (out, lse) results."""
     inp = synth.make_inputs(wl, 0, device=DEV)
     raw = {k: inp[k] for k in ["kv_raw", "ik_raw", "gate_csa", "gate_hca"]}
     layer = HybridLayer(wl, raw, device=DEV)
+    args = (inp["q"], inp["iq"], inp["w"], inp["pos"], inp["sink"])
+    out_b, lse_b = layer.step(*args, t_new=t_new, branch_outputs=True)
+    out_b, lse_b = out_b.clone(), lse_b.clone()
     side_stream = torch.cuda.Stream() if side else None
-    out, lse = layer.step(inp["q"], inp["iq"], inp["w"], inp["pos"], inp["sink"], t_new=t_new,
-                          side_stream=side_stream)
+    out, lse = layer.step(*args, t_new=t_new, side_stream=side_stream)
     torch.cuda.synchronize()
     hattn.check_status()
-    return inp, layer, out, lse
+    return inp, layer, (out_b, lse_b), (out, lse)
 
 
 def _check_compress(wl, inp, layer, b, entries, kind):
@@ -75,8 +81,10 @@ def _check_compress(wl, inp, layer, b, entries, kind):
             assert rel_l2(layer.ik_c[b, j], ri[0, 0]) <= KV_REL_L2, f"indexer key {j}"
 
 
-def _check_sequence(wl, inp, layer, out, lse, b, ts):
-    """Stage-by-stage parity of queries ts of sequence b."""
+def _check_sequence(wl, inp, layer, res_b, res, b, ts):
+    """Stage-by-stage parity of queries ts of sequence b: every branch, the
+    merge of the branch outputs, and the benchmark's merge of split
+    partials."""
     T = inp["q"].shape[1]
     bufs = layer.buffers(T)
     tsel = torch.as_tensor(ts, device=DEV)
@@ -114,7 +122,8 @@ def _check_sequence(wl, inp, layer, out, lse, b, ts):
         o_list.append(ro)
         l_list.append(rl)
     ref_out, ref_lse = orc.merge(o_list, l_list, sink, pos, wl.r)
-    check_attn(out[b:b + 1, tsel], lse[b:b + 1, tsel], ref_out, ref_lse, "layer output")
+    for (out, lse), what in [(res_b, "layer output (branch outputs)"), (res, "layer output")]:
+        check_attn(out[b:b + 1, tsel], lse[b:b + 1, tsel], ref_out, ref_lse, what)
 
 
 def test_hybrid_decode_1m():
@@ -122,39 +131,39 @@ def test_hybrid_decode_1m():
     8,192 HCA entries, 128 SWA tokens; the benchmark's step, with the HCA and
     SWA branches on a second stream as the benchmark runs them."""
     wl = synth.WORKLOADS["hybrid_decode_1m"]
-    inp, layer, out, lse = _run(wl, t_new=wl.L - 1, side=True)
+    inp, layer, res_b, res = _run(wl, t_new=wl.L - 1, side=True)
     n = wl.L // wl.m_csa
     _check_compress(wl, inp, layer, 5, [0, 1, 77777, n - 1], "csa")
     _check_compress(wl, inp, layer, 2, [0, 4095, wl.L // wl.m_hca - 1], "hca")
-    _check_sequence(wl, inp, layer, out, lse, 5, [0])
-    assert torch.isfinite(out.float()).all()
+    _check_sequence(wl, inp, layer, res_b, res, 5, [0])
+    assert torch.isfinite(res[0].float()).all()
 
 
 def test_pro_csa_decode():
     """Batch 32, each query against its own 131,072-token context (32,768
     entries, top-1024) plus SWA."""
     wl = synth.WORKLOADS["pro_csa_decode"]
-    inp, layer, out, lse = _run(wl, t_new=wl.L - 1)
+    inp, layer, res_b, res = _run(wl, t_new=wl.L - 1)
     _check_compress(wl, inp, layer, 31, [3, wl.L // wl.m_csa - 1], "csa")
     for b in (0, 31):
-        _check_sequence(wl, inp, layer, out, lse, b, [0])
+        _check_sequence(wl, inp, layer, res_b, res, b, [0])
 
 
 def test_hca_decode_1m():
     """Batch 16 at 1M context: dense attention over 8,192 HCA entries."""
     wl = synth.WORKLOADS["hca_decode"]
-    inp, layer, out, lse = _run(wl, t_new=wl.L - 1)
+    inp, layer, res_b, res = _run(wl, t_new=wl.L - 1)
     _check_compress(wl, inp, layer, 9, [0, 8191], "hca")
     for b in (0, 15):
-        _check_sequence(wl, inp, layer, out, lse, b, [0])
+        _check_sequence(wl, inp, layer, res_b, res, b, [0])
 
 
 def test_hca_prefill_chunk():
     """A 4,096-query prefill chunk at the end of a 1M context, causal over
     the 128-token compressed blocks."""
     wl = synth.WORKLOADS["hca_prefill"]
-    inp, layer, out, lse = _run(wl)
-    _check_sequence(wl, inp, layer, out, lse, 0, [0, 126, 127, 2048, 4095])
+    inp, layer, res_b, res = _run(wl)
+    _check_sequence(wl, inp, layer, res_b, res, 0, [0, 126, 127, 2048, 4095])
 
 
 def test_flash_csa_prefill():
@@ -162,6 +171,6 @@ def test_flash_csa_prefill():
     2,048 entries) plus SWA; samples the first queries, a ragged middle and
     the end."""
     wl = synth.WORKLOADS["flash_csa_prefill"]
-    inp, layer, out, lse = _run(wl)
+    inp, layer, res_b, res = _run(wl)
     _check_compress(wl, inp, layer, 0, [0, 1, 1000, 2047], "csa")
-    _check_sequence(wl, inp, layer, out, lse, 0, [0, 3, 2051, 4097, 8191])
+    _check_sequence(wl, inp, layer, res_b, res, 0, [0, 3, 2051, 4097, 8191])

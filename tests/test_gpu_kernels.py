@@ -312,6 +312,45 @@ def test_lse_merge(nb, with_sink, pos_list):
     check_attn(out, lse, ro, rl, "merge")
 
 
+@pytest.mark.parametrize("B,H,D,r,N_hca,k,N_c,L", [
+    (3, 128, 512, 64, 900, 300, 5000, 20480),     # decode: every branch split across SMs
+    (1, 4, 64, 16, 40, 16, 60, 300),              # one split each
+])
+def test_merge_of_split_partials(B, H, D, r, N_hca, k, N_c, L):
+    """Branches left as split partials (o = lse = NULL) and merged in one pass
+    equal the oracle's merge of the branch outputs, and the combined path."""
+    T = 1
+    q = randn_bf16((B, T, H, D), 85)
+    kv_h = randn_bf16((B, N_hca, D), 86)
+    kv_c = randn_bf16((B, N_c, D), 87)
+    raw = randn_bf16((B, L, D), 88)
+    sink = randn_f32((H,), 89)
+    pos = _pos(B, T, [min(128 * N_hca, 4 * N_c, L) - 1 - 7 * i for i in range(B)])
+    nvis = np.array([[min((int(p) + 1) // 4, N_c)] for p in pos.ravel()]).reshape(B, T)
+    idx = synth.random_idx(B, T, k, nvis, seed=90)
+    d = dict(q=q.to(DEV), pos=pos.to(DEV))
+    qt = hattn.query_prep(d["q"], d["pos"], r=r)
+    parts = [hattn.sparse_attn(qt, kv_c.to(DEV), idx.to(DEV), d["pos"], r=r, q_prepped=True,
+                               partials=True),
+             hattn.hca_attn(qt, kv_h.to(DEV), d["pos"], r=r, q_prepped=True, partials=True),
+             hattn.swa_attn(qt, raw.to(DEV), d["pos"], r=r, q_prepped=True, partials=True)]
+    assert all(p.nsplit >= 1 for p in parts)
+    out, lse = hattn.lse_merge_splits(parts, d["pos"], r=r, H=H, sink=sink.to(DEV))
+    branches = [hattn.sparse_attn(qt, kv_c.to(DEV), idx.to(DEV), d["pos"], r=r, q_prepped=True),
+                hattn.hca_attn(qt, kv_h.to(DEV), d["pos"], r=r, q_prepped=True),
+                hattn.swa_attn(qt, raw.to(DEV), d["pos"], r=r, q_prepped=True)]
+    out2, lse2 = hattn.lse_merge([o for o, _ in branches], [l for _, l in branches], d["pos"],
+                                 r=r, sink=sink.to(DEV))
+    hattn.check_status()
+    qb, pn = bits(q), pos.numpy()
+    ro = [orc.attention(orc.KIND_SPARSE, qb, bits(kv_c), pn, idx=idx.numpy(), r=r),
+          orc.attention(orc.KIND_HCA, qb, bits(kv_h), pn, m=128, r=r),
+          orc.attention(orc.KIND_SWA, qb, bits(raw), pn, W=128, r=r)]
+    ref, rl = orc.merge([x[0] for x in ro], [x[1] for x in ro], sink.numpy(), pn, r)
+    check_attn(out, lse, ref, rl, "merge of split partials")
+    check_attn(out2, lse2, ref, rl, "merge of combined branches")
+
+
 # ------------------------------------------------------------------ whole tiny layer
 def test_tiny_layer_end_to_end():
     wl = synth.WORKLOADS["tiny"]

@@ -116,6 +116,26 @@ HATTN_API int hattn_indexer_topk(const void* iq, const float* w, const void* ik_
 HATTN_API size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
                                           int score_out_given);
 
+/* hattn_indexer_topk for callers that cannot allocate device memory: code
+ * that runs where cudaMalloc is not allowed or not wanted, such as an engine
+ * that owns a fixed memory pool, a plugin host that forbids device
+ * allocations, or a stream-ordered path that must not synchronise on the
+ * allocator.  The same selection as hattn_indexer_topk, but the fp32 scores
+ * live in a scratch array compiled into this library (4,194,304 scores,
+ * 16 MiB, held on every device that loads the library until the process
+ * exits), so the call allocates nothing; the caller still passes inputs and
+ * idx_out.  The pages have no counterpart of this call.
+ *   - B * T * N_cap must not exceed 4,194,304 (HATTN_ERR_INVALID_ARG).
+ *   - The first call on a device looks the scratch address up (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one scratch array: calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race.  No
+ *     contents need clearing between calls. */
+HATTN_API int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,
+                                         const int32_t* pos, int B, int T, int HI, int dI,
+                                         int64_t N_cap, int k, int m, int32_t* idx_out,
+                                         hattn_stream_t stream);
+
 /* The two stages of hattn_indexer_topk as separate calls.
  * hattn_indexer_scores writes I[j] for j < n into score_out [B][T][N_cap] fp32
  * (entries j >= n untouched).  hattn_topk_select reads those scores and writes

@@ -476,6 +476,34 @@ int topk_impl(const float* scores, const int32_t* pos, int rows, int64_t N_cap, 
   return ok();
 }
 
+// Score scratch of hattn_indexer_topk_noalloc: a fixed device array that
+// every GPU loading this library holds until the process exits, so that
+// call needs no allocation.  4,194,304 fp32 scores (16 MiB), enough for
+// B * T * N_cap = 8 x 1 x 262,144 (a 1M-token decode batch of 8) twice over.
+constexpr int64_t kNoallocScores = int64_t(1) << 22;
+static __device__ __align__(256) float g_noalloc_scores[kNoallocScores];
+
+// Device address of g_noalloc_scores for each device, looked up once with
+// that device current (in host code the array's name is only a host-side
+// stand-in, not a device address).
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scores(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(HATTN_ERR_CUDA, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scores);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(score scratch)");
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return HATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -512,6 +540,30 @@ int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const i
     scores = static_cast<float*>(workspace);
   }
   int rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream);
+  if (rc) return rc;
+  return topk_impl(scores, pos, B * T, N_cap, k, m, idx_out, stream);
+}
+
+int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,
+                               const int32_t* pos, int B, int T, int HI, int dI, int64_t N_cap,
+                               int k, int m, int32_t* idx_out, hattn_stream_t stream) {
+  REQUIRE_PTR(iq);
+  REQUIRE_PTR(w);
+  REQUIRE_PTR(ik_c);
+  REQUIRE_PTR(pos);
+  REQUIRE_PTR(idx_out);
+  REQUIRE(k >= 1 && k <= 2048, "k=%d must be in [1, 2048]", k);
+  REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
+  REQUIRE(B >= 1 && T >= 1 && N_cap >= 1, "B, T and N_cap must be >= 1");
+  REQUIRE((int64_t)B * T * N_cap <= kNoallocScores,
+          "B * T * N_cap = %lld scores exceed the fixed scratch of %lld (use hattn_indexer_topk "
+          "with a workspace)", (long long)((int64_t)B * T * N_cap), (long long)kNoallocScores);
+  float* scores = nullptr;
+  int rc = noalloc_scores(&scores);
+  if (rc) return rc;
+  // every score the selection reads (entries j < visible count) is written by
+  // the score kernel first, so nothing in the shared scratch needs clearing
+  rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream);
   if (rc) return rc;
   return topk_impl(scores, pos, B * T, N_cap, k, m, idx_out, stream);
 }

@@ -35,6 +35,8 @@ _SIGS = {
     "hattn_indexer_topk": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                   _vp, _vp, _vp, _sz, _vp]),
     "hattn_indexer_topk_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32, _i32]),
+    "hattn_indexer_topk_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
+                                          _i32, _vp, _vp]),
     "hattn_indexer_scores": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
                                     _vp]),
     "hattn_topk_select": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp]),
@@ -189,6 +191,24 @@ def indexer_topk(iq, w, ik_c, pos, *, k, m=4, idx_out=None, score_out=None, work
     _check(lib().hattn_indexer_topk(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI, N_cap,
                                     k, m, _ptr(idx_out), _ptr(score_out), _ptr(workspace),
                                     ws_bytes, _stream(stream)))
+    return idx_out
+
+
+def indexer_topk_noalloc(iq, w, ik_c, pos, *, k, m=4, idx_out=None, stream=None):
+    """indexer_topk with its score scratch in the library's fixed device
+    array (no device allocation by the library; B*T*N_cap <= 4,194,304).
+    Calls that overlap on the GPU share that array and race."""
+    _need(iq, "iq", torch.bfloat16, 4)
+    _need(w, "w", torch.float32, 3)
+    _need(ik_c, "ik_c", torch.bfloat16, 3)
+    _need(pos, "pos", torch.int32, 2)
+    B, T, HI, dI = iq.shape
+    if idx_out is None:
+        idx_out = torch.empty((B, T, k), dtype=torch.int32, device=iq.device)
+    _need(idx_out, "idx_out", torch.int32)
+    _check(lib().hattn_indexer_topk_noalloc(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI,
+                                            dI, ik_c.shape[1], k, m, _ptr(idx_out),
+                                            _stream(stream)))
     return idx_out
 
 

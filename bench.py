@@ -94,8 +94,36 @@ def step_bytes(wl):
 
 
 def indexer_bytes(wl):
+    """Algorithmic bytes of one indexer launch: every visible indexer key
+    read once, the queries and weights, and one fp32 score written per
+    entry."""
     n_csa = wl.L // wl.m_csa
-    return wl.B * (n_csa * wl.dI * 2 + wl.HI * wl.dI * 2 + wl.HI * 4)
+    return wl.B * (n_csa * (wl.dI * 2 + 4) + wl.HI * wl.dI * 2 + wl.HI * 4)
+
+
+# DRAM traffic of indexer_score_kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum) from one ncu capture of an 8 x 65,536-entry launch
+# (138.26 MB), per entry processed; it applies only to the kernel sources it
+# was taken on, checked by hash, else the bench reports traffic as null.
+INDEXER_TRAFFIC = {
+    "bytes_per_entry": 138.264e6 / (8 * 65536),
+    "sources": ["indexer.cu", "common.cuh", "kernels.h"],
+    "sha256": "42b1f38de5468c2c5fd17252330fefd189360ed14e2f02a1eb6006e9687a9b77",
+    "profile": "profiles/indexer_score_kernel_decode_8x65536.md",
+}
+
+
+def indexer_traffic(wl):
+    """Per-launch DRAM bytes scaled from the recorded capture, or None when
+    the indexer sources have changed since it was taken."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in INDEXER_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, "sparse_attention_26_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != INDEXER_TRAFFIC["sha256"]:
+        return None
+    return INDEXER_TRAFFIC["bytes_per_entry"] * wl.B * (wl.L // wl.m_csa)
 
 
 class ClockSampler:
@@ -400,7 +428,10 @@ def run_ours(args, world, rank, local):
     achieved = ib / (idx_ms / 1e3) / 1e9
     sb = step_bytes(wl)
     roofline = {"bound": "hbm", "kernel": "indexer_score_kernel", "achieved": achieved,
-                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": indexer_traffic(wl),
+                "traffic_source": "ncu dram bytes of an 8 x 65,536-entry launch scaled by "
+                                  "entries (" + INDEXER_TRAFFIC["profile"] + ")",
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
                 else "fallback 6.4 TB/s",
                 "algorithmic_bytes_per_launch": ib,

@@ -386,7 +386,7 @@ def run_ours(args, world, rank, local):
     hattn.check_status()
 
     K = args.steps
-    names = ["compress", "qprep", "indexer", "topk", "sparse", "hca", "swa", "merge"]
+    names = layer.event_names(wl.T)
     mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
     step_ev = [mk() for _ in range(K + 1)]
     kev = [{n: (mk(), mk()) for n in names} for _ in range(K)]

@@ -204,6 +204,38 @@ HATTN_API int hattn_swa_attn(const void* q, const float* gamma_q, int q_prepped,
                    int64_t L_cap, int W, int r, float rope_base, float eps, float scale, void* o,
                    float* lse, void* workspace, size_t ws_bytes, hattn_stream_t stream);
 
+/* SWA keys for hattn_hybrid_attn ([DD]: the most recent W tokens, each in the
+ * normalised, roped space of the compressed entries):
+ *   kv_w[b][t][j] = RoPE_u(RMSNorm(kv_raw[b][u]; gamma_kv, eps)),
+ *   u = pos[b][t] - W + 1 + j   (j < W; a zero row where u < 0 or u >= L_cap)
+ * kv_raw [B][L_cap][D] bf16, kv_w [B][T][W][D] bf16 (caller-owned). */
+HATTN_API int hattn_swa_keys(const void* kv_raw, const float* gamma_kv, const int32_t* pos, int B,
+                             int T, int64_t L_cap, int D, int W, int r, float rope_base,
+                             float eps, void* kv_w, hattn_stream_t stream);
+
+/* The three branches as one attention ([DD] CSA + HCA + SWA, merged by
+ * log-sum-exp): for each query the keys are the selected CSA entries
+ * kv_c[b][idx[b][t][i]] (idx >= 0), the visible HCA entries kv_h[b][j],
+ * j < min(floor((pos+1)/m), N_h), and the existing window tokens
+ * kv_w[b][t][j] (from hattn_swa_keys, j >= W-1-pos), all under one softmax.
+ * Because each branch's own normalisation cancels in the sink merge, merging
+ * this result (or its partials) with hattn_lse_merge(_splits), nb = 1, gives
+ * the layer output of the three branch calls merged together.  The output
+ * conventions (o/lse, partials with o == lse == NULL, q_prepped, workspace)
+ * are those of the branch calls; the workspace size and split count come from
+ * the two functions below.  One query per row block: the MMA rows are the H
+ * heads of one query (H <= 128). */
+HATTN_API int hattn_hybrid_attn(const void* q, const float* gamma_q, int q_prepped,
+                                const void* kv_c, const int32_t* idx, int64_t N_c, int k,
+                                const void* kv_h, int64_t N_h, int m, const void* kv_w, int W,
+                                const int32_t* pos, int B, int T, int H, int D, int r,
+                                float rope_base, float eps, float scale, void* o, float* lse,
+                                void* workspace, size_t ws_bytes, hattn_stream_t stream);
+HATTN_API size_t hattn_hybrid_attn_workspace_bytes(int B, int T, int H, int D, int k,
+                                                   int64_t N_h, int W, int q_prepped,
+                                                   int partials);
+HATTN_API int hattn_hybrid_attn_splits(int B, int T, int H, int D, int k, int64_t N_h, int W);
+
 /* Split partials instead of a branch output: with o == NULL and lse == NULL
  * an attention call leaves the softmax of each key split in its workspace,
  * right after the prepared queries (if any):

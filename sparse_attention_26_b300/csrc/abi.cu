@@ -222,11 +222,24 @@ int query_prep_impl(const void* q, const float* gamma_q, const int32_t* pos, int
   return HATTN_OK;
 }
 
+// The fused call's second and third key sources.
+struct FusedSources {
+  const void* kv_h;   // [B][N_h][D] HCA entries
+  int64_t N_h;
+  const void* kv_w;   // [B][T][W][D] SWA keys (hattn_swa_keys)
+};
+
+// Keys the fused call plans for: each segment rounded up to whole tiles.
+int64_t fused_keys(int k, int64_t N_h, int W) {
+  auto up = [](int64_t n) { return (n + 63) / 64 * 64; };
+  return up(k) + up(N_h) + up(W);
+}
+
 int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, const void* kv,
                 const float* gamma_kv, const int32_t* idx, const int32_t* pos, int B, int T, int H,
                 int D, int64_t N_rows, int k, int m, int W, int r, float rope_base, float eps,
                 float scale, void* o, float* lse, void* workspace, size_t ws_bytes,
-                hattn_stream_t stream) {
+                hattn_stream_t stream, const FusedSources* fs = nullptr) {
   REQUIRE_PTR(q);
   REQUIRE_PTR(kv);
   REQUIRE_PTR(pos);
@@ -240,19 +253,28 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   }
   REQUIRE_F32(gamma_q);
   REQUIRE_F32(gamma_kv);
-  if (kind == kSparse) REQUIRE_PTR(idx);
+  if (kind == kSparse || kind == kFused) REQUIRE_PTR(idx);
+  if (kind == kFused) {
+    REQUIRE(fs != nullptr, "fused sources missing");
+    REQUIRE_PTR(fs->kv_h);
+    REQUIRE_PTR(fs->kv_w);
+    REQUIRE(fs->N_h >= 1, "the HCA cache needs at least one row");
+    REQUIRE((int64_t)B * fs->N_h < (1ll << 31), "B * N_h must be < 2^31");
+    REQUIRE((int64_t)B * T * W < (1ll << 31), "B * T * W must be < 2^31");
+  }
   REQUIRE(B >= 1 && T >= 1, "B and T must be >= 1");
   REQUIRE(H >= 1 && H <= 128, "H=%d must be in [1, 128]", H);
   REQUIRE(D >= 64 && D <= 512 && D % 64 == 0, "D=%d must be a multiple of 64 in [64, 512]", D);
   REQUIRE(N_rows >= 1, "the key cache needs at least one row");
   REQUIRE((int64_t)B * N_rows < (1ll << 31), "B * rows of the cache must be < 2^31");
-  if (kind == kSparse) REQUIRE(k >= 1 && k <= 65536, "k=%d out of range", k);
-  if (kind == kHca) REQUIRE(m >= 1, "m must be >= 1");
-  if (kind == kSwa) REQUIRE(W >= 1, "W must be >= 1");
+  if (kind == kSparse || kind == kFused) REQUIRE(k >= 1 && k <= 65536, "k=%d out of range", k);
+  if (kind == kHca || kind == kFused) REQUIRE(m >= 1, "m must be >= 1");
+  if (kind == kSwa || kind == kFused) REQUIRE(W >= 1 && W <= 65536, "W=%d out of range", W);
   REQUIRE(scale > 0.f, "scale must be positive");
   int rc = check_rope(D, r, rope_base, eps);
   if (rc) return rc;
-  const int64_t n_keys = kind == kSparse ? k : (kind == kHca ? N_rows : W);
+  const int64_t n_keys = kind == kFused ? fused_keys(k, fs->N_h, W)
+                                         : (kind == kSparse ? k : (kind == kHca ? N_rows : W));
   AttnPlan p;
   if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p))
     return fail(HATTN_ERR_UNSUPPORTED, "no attention kernel for H=%d D=%d", H, D);
@@ -265,14 +287,24 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   }
   int* status = nullptr;
   if (!device_info(nullptr, &status, nullptr)) return fail(HATTN_ERR_CUDA, "no CUDA device");
-  CUtensorMap tm, tm_q;
+  CUtensorMap tm, tm2, tm_q;
   memset(&tm, 0, sizeof tm);
-  if (kind != kSparse) {
+  memset(&tm2, 0, sizeof tm2);
+  if (kind == kHca || kind == kSwa) {
     // HCA entries / SWA raw tokens: 64 rows x 64 dims per copy
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)N_rows};
     const uint64_t strides[1] = {(uint64_t)D * 2};
     const uint32_t box[2] = {64, 64};
     rc = make_tmap(&tm, kv, 2, dims, strides, box, kind == kHca ? "kv_h" : "kv_raw");
+    if (rc) return rc;
+  } else if (kind == kFused) {
+    const uint64_t strides[1] = {(uint64_t)D * 2};
+    const uint32_t box[2] = {64, 64};
+    const uint64_t dh[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)fs->N_h};
+    rc = make_tmap(&tm, fs->kv_h, 2, dh, strides, box, "kv_h");
+    if (rc) return rc;
+    const uint64_t dw[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)T * (uint64_t)W};
+    rc = make_tmap(&tm2, fs->kv_w, 2, dw, strides, box, "kv_w");
     if (rc) return rc;
   }
   // prepared queries: the caller's, or this call's into the workspace
@@ -312,6 +344,7 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.D = D;
   a.r = r;
   a.N_rows = N_rows;
+  a.N_h = fs ? fs->N_h : 0;
   a.k = k;
   a.m = m;
   a.W = W;
@@ -323,7 +356,7 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.nsplit = p.nsplit;
   a.keys_per_split = p.keys_per_split;
   a.nds = p.nds;
-  cudaError_t e = launch_attention(tm, tm_q, a, p, st);
+  cudaError_t e = launch_attention(tm, tm2, tm_q, a, p, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (p.nsplit > 1 && !partials) {
     CombineArgs c;
@@ -607,6 +640,62 @@ int hattn_hca_attn(const void* q, const float* gamma_q, int q_prepped, const voi
                    size_t ws_bytes, hattn_stream_t stream) {
   return attn_common(kHca, q, gamma_q, q_prepped, kv_h, nullptr, nullptr, pos, B, T, H, D, N_cap, 1, m, 1, r,
                      rope_base, eps, scale, o, lse, workspace, ws_bytes, stream);
+}
+
+int hattn_hybrid_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_c,
+                      const int32_t* idx, int64_t N_c, int k, const void* kv_h, int64_t N_h,
+                      int m, const void* kv_w, int W, const int32_t* pos, int B, int T, int H,
+                      int D, int r, float rope_base, float eps, float scale, void* o,
+                      float* lse, void* workspace, size_t ws_bytes, hattn_stream_t stream) {
+  const FusedSources fs{kv_h, N_h, kv_w};
+  return attn_common(kFused, q, gamma_q, q_prepped, kv_c, nullptr, idx, pos, B, T, H, D, N_c, k,
+                     m, W, r, rope_base, eps, scale, o, lse, workspace, ws_bytes, stream, &fs);
+}
+
+size_t hattn_hybrid_attn_workspace_bytes(int B, int T, int H, int D, int k, int64_t N_h, int W,
+                                         int q_prepped, int partials) {
+  AttnPlan p;
+  if (!plan_attention(kFused, B, T, H, D, fused_keys(k, N_h, W), num_sms_or_default(), &p))
+    return 0;
+  return qprep_bytes(B, T, H, D, q_prepped) +
+         (partials ? partial_bytes(B, T, H, D, p.nsplit) : p.ws_bytes);
+}
+
+int hattn_hybrid_attn_splits(int B, int T, int H, int D, int k, int64_t N_h, int W) {
+  AttnPlan p;
+  if (!plan_attention(kFused, B, T, H, D, fused_keys(k, N_h, W), num_sms_or_default(), &p))
+    return 0;
+  return p.nsplit;
+}
+
+int hattn_swa_keys(const void* kv_raw, const float* gamma_kv, const int32_t* pos, int B, int T,
+                   int64_t L_cap, int D, int W, int r, float rope_base, float eps, void* kv_w,
+                   hattn_stream_t stream) {
+  REQUIRE_PTR(kv_raw);
+  REQUIRE_PTR(pos);
+  REQUIRE_PTR(kv_w);
+  REQUIRE_F32(gamma_kv);
+  REQUIRE(B >= 1 && T >= 1 && L_cap >= 1, "B, T and L_cap must be >= 1");
+  REQUIRE(W >= 1 && W <= 65536, "W=%d out of range", W);
+  REQUIRE(D >= 64 && D <= 512 && D % 64 == 0, "D=%d must be a multiple of 64 in [64, 512]", D);
+  int rc = check_rope(D, r, rope_base, eps);
+  if (rc) return rc;
+  SwaKeysArgs a;
+  a.kv_raw = static_cast<const __nv_bfloat16*>(kv_raw);
+  a.gamma = gamma_kv;
+  a.pos = pos;
+  a.kv_w = static_cast<__nv_bfloat16*>(kv_w);
+  a.B = B;
+  a.T = T;
+  a.D = D;
+  a.r = r;
+  a.W = W;
+  a.L_cap = L_cap;
+  a.eps = eps;
+  make_rope_coef(rope_base, r, &a.rope);
+  cudaError_t e = launch_swa_keys(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "SWA keys launch");
+  return ok();
 }
 
 int hattn_swa_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_raw,

@@ -143,10 +143,52 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Fused kind: one query's keys are three segments of 64-key tiles -- 0: the
+// top-k CSA entries (gathered), 1: the visible HCA entries, 2: the query's W
+// SWA keys (both by TMA).  Split s of nsplit takes tiles
+// [s*n/nsplit, (s+1)*n/nsplit) of each segment, so every split gets its share
+// of the gathered and the streamed tiles.
+struct SegTiles {
+  int first[3], count[3];
+  int64_t nkeys[3];
+  __device__ __forceinline__ void init(int64_t n0, int64_t n1, int64_t n2, int split,
+                                       int nsplit) {
+    nkeys[0] = n0;
+    nkeys[1] = n1;
+    nkeys[2] = n2;
+#pragma unroll
+    for (int g = 0; g < 3; ++g) {
+      const int64_t t = (nkeys[g] + kTile - 1) / kTile;
+      const int64_t lo = t * split / nsplit, hi = t * (split + 1) / nsplit;
+      first[g] = static_cast<int>(lo);
+      count[g] = static_cast<int>(hi - lo);
+    }
+  }
+  __device__ __forceinline__ int total() const { return count[0] + count[1] + count[2]; }
+  // tile i of this split: its segment, first key (within the segment) and
+  // number of keys
+  __device__ __forceinline__ void map(int i, int& seg, int64_t& kt, int& nvalid) const {
+    seg = 0;
+    if (i >= count[0]) {
+      i -= count[0];
+      seg = 1;
+      if (i >= count[1]) {
+        i -= count[1];
+        seg = 2;
+      }
+    }
+    kt = static_cast<int64_t>(first[seg] + i) * kTile;
+    const int64_t rem = nkeys[seg] - kt;
+    nvalid = static_cast<int>(rem < kTile ? rem : kTile);
+  }
+};
+
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
-                const __grid_constant__ AttnArgs a, const int nslot) {
+    attn_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                const __grid_constant__ CUtensorMap tm_kv2,
+                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttnArgs a,
+                const int nslot) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -173,7 +215,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- key range
   int64_t total = 0, u_lo = 0;
-  if (KIND == kSparse) {
+  SegTiles st;
+  if (KIND == kFused) {
+    // one query per row block (G = 1)
+    int64_t nh = vis(a.pos[(int64_t)b * a.T + t0], a.m);
+    if (nh > a.N_h) nh = a.N_h;
+    st.init(a.k, nh, a.W, split, a.nsplit);
+  } else if (KIND == kSparse) {
     total = a.k;
   } else if (KIND == kHca) {
     for (int g = 0; g < gv; ++g) {
@@ -198,8 +246,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t kend = kbeg + a.keys_per_split;
   if (kend > total) kend = total;
   const int nk = kend > kbeg ? static_cast<int>(kend - kbeg) : 0;
-  const int nt = (nk + kTile - 1) / kTile;
+  const int nt = KIND == kFused ? st.total() : (nk + kTile - 1) / kTile;
   const int ocols = n_own * 64;
+  // tile i: segment (the kind's own, or the fused list's), first key and keys
+  auto tile_of = [&](int i, int& seg, int64_t& kt, int& nvalid) {
+    if (KIND == kFused) {
+      st.map(i, seg, kt, nvalid);
+    } else {
+      seg = KIND == kSparse ? 0 : (KIND == kHca ? 1 : 2);
+      kt = kbeg + static_cast<int64_t>(i) * kTile;
+      nvalid = static_cast<int>((kend - kt) < kTile ? (kend - kt) : kTile);
+    }
+  };
 
   if (nt == 0) {
     // empty split: o = 0, lse = -inf
@@ -241,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     if (KIND != kSparse) tma_prefetch_desc(&tm_kv);
+    if (KIND == kFused) tma_prefetch_desc(&tm_kv2);
   }
   if (warp == 4) {
     tmem_alloc(smem_u32(&sm->tmem_base), 512);
@@ -342,6 +401,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       cp_async_wait_all();  // no copy outlives the CTA
+    } else if (KIND == kFused) {
+      // every producer thread takes part in every chunk (the full barriers
+      // count 128 arrivals): gathered chunks as in the sparse branch; for a
+      // streamed chunk thread 0 arms the barrier and issues the TMA copy
+      const int32_t* idx_row = a.idx + ((int64_t)b * a.T + t0) * a.k;
+      bool ok = true;
+      int64_t tma_issued = 0;  // chunks whose copy thread 0 has issued (for the abort drain)
+      for (int i = 0; i < nt && ok && !*abort; ++i) {
+        int seg, nvalid;
+        int64_t kt;
+        tile_of(i, seg, kt, nvalid);
+        const __nv_bfloat16* src[4];
+        int bytes[4];
+        if (seg == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int rI = (pt + 128 * q) >> 3;
+            int32_t j = -1;
+            if (rI < nvalid) j = idx_row[kt + rI];
+            if (j >= a.N_rows) {
+              if ((pt & 7) == 0) record_status(a.status, kStatusBadIndex);
+              j = -1;
+            }
+            bytes[q] = j >= 0 ? 16 : 0;
+            src[q] = a.kv + ((int64_t)b * a.N_rows + (j >= 0 ? j : 0)) * a.D +
+                     ((pt + 128 * q) & 7) * 8;
+          }
+        }
+        const int32_t row0 = seg == 1
+            ? static_cast<int32_t>((int64_t)b * a.N_h + kt)
+            : static_cast<int32_t>(((int64_t)b * a.T + t0) * a.W + kt);
+        for (int p = 0; p < ndc; ++p, advance()) {
+          if (!staging_free(ctr) ||
+              (ctr >= nslot &&
+               !mbar_wait(smem_u32(&sm->empty[slot]), ph ^ 1u, abort, a.status, kWaitLimitNs, 42))) {
+            ok = false;
+            break;
+          }
+          const int dcol = chunk_dc(p) * 64;
+          const uint32_t dst = smem_u32(sRing + slot * 8192);
+          const uint32_t fb = smem_u32(&sm->full[slot]);
+          if (seg == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int pc = pt + 128 * q;
+              cp_async16(dst + swz128(pc >> 3, pc & 7), src[q] + dcol, bytes[q]);
+            }
+            cp_async_mbar_arrive(fb);
+          } else if (pt == 0) {
+            mbar_arrive_expect_tx(fb, 8192);
+            tma_load_2d(dst, seg == 1 ? &tm_kv : &tm_kv2, dcol, row0, fb);
+            tma_issued = ctr + 1;
+          } else {
+            mbar_arrive(fb);
+          }
+        }
+      }
+      cp_async_wait_all();  // no copy outlives the CTA
+      if (!ok && pt == 0) {
+        // TMA copies issued whose completion nobody waited for land before exit
+        const int64_t first = tma_issued > nslot ? tma_issued - nslot : 0;
+        for (int64_t x = first; x < tma_issued; ++x)
+          mbar_wait(smem_u32(&sm->full[x % nslot]), (x / nslot) & 1, nullptr, nullptr,
+                    10000000ull, 43);
+      }
     } else {
       // SWA: keys are RMSNorm'd and RoPE'd raw tokens at their own positions.
       // Row norms come first, from the rows in global memory (two threads per
@@ -469,8 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc_qk = idesc_bf16(128, 64, 0, 0);
     const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sRing);
     for (int i = par; i < nt && ok; i += 2) {
-      const int64_t kt = kbeg + (int64_t)i * kTile;
-      const int nvalid = static_cast<int>((kend - kt) < kTile ? (kend - kt) : kTile);
+      int seg, nvalid;
+      int64_t kt;
+      tile_of(i, seg, kt, nvalid);
       const int sb = i & 1;
       // the S/P buffer is reused once PV of tile i-2 has read its P
       if (i >= 2) {
@@ -490,9 +615,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // gathered rows were written by cp.async (generic proxy); the MMA
         // reads through the async proxy
-        if (KIND == kSparse) fence_proxy_async_smem();
-        if (KIND == kHca && nvalid < kTile) {
-          // an HCA tail tile: zero its invalid key rows
+        if (KIND == kSparse || KIND == kFused) fence_proxy_async_smem();
+        if ((KIND == kHca || (KIND == kFused && seg != 0)) && nvalid < kTile) {
+          // a streamed tail tile: zero its invalid key rows (they may hold
+          // anything, and P = 0 times a NaN would still be NaN)
           uint8_t* dst = sRing + s * 8192;
           for (int pc = nvalid * 8 + lane; pc < kTile * 8; pc += 32)
             *reinterpret_cast<uint4*>(dst + swz128(pc >> 3, pc & 7)) = make_uint4(0, 0, 0, 0);
@@ -541,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const int64_t c0 = (int64_t)i * ndc + n_other;
       const int s0 = static_cast<int>(c0 % nslot);
-      if (KIND == kSparse) {
+      if (KIND == kSparse || KIND == kFused) {
         // this warp's view of the gathered rows, for the async proxy
         for (int e = 0; e < n_own && ok; ++e)
           ok = __all_sync(0xffffffffu,
@@ -618,17 +744,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* idx_row = a.idx + ((int64_t)b * a.T + t0) * a.k;
     float m_used = -INFINITY, l = 0.f;
     for (int i = 0; i < nt && ok; ++i) {
-      const int64_t kt = kbeg + (int64_t)i * kTile;
+      int seg, nv;
+      int64_t kt;
+      tile_of(i, seg, kt, nv);
       uint64_t colmask = 0;  // keys of this tile that exist for every row
-      if (KIND == kSparse) {
+      if (seg == 0) {
         const int64_t k0 = kt + lane, k1 = kt + 32 + lane;
-        const int32_t j0 = k0 < kend ? idx_row[k0] : -1;
-        const int32_t j1 = k1 < kend ? idx_row[k1] : -1;
+        const int32_t j0 = lane < nv ? idx_row[k0] : -1;
+        const int32_t j1 = 32 + lane < nv ? idx_row[k1] : -1;
         const unsigned b0 = __ballot_sync(0xffffffffu, j0 >= 0 && j0 < a.N_rows);
         const unsigned b1 = __ballot_sync(0xffffffffu, j1 >= 0 && j1 < a.N_rows);
         colmask = static_cast<uint64_t>(b0) | (static_cast<uint64_t>(b1) << 32);
       } else {
-        const int nv = static_cast<int>((kend - kt) < kTile ? (kend - kt) : kTile);
         colmask = nv >= 64 ? ~0ull : ((1ull << nv) - 1);
       }
       // the row's own limits as tile columns: valid c in [c_lo, c_hi)
@@ -640,6 +767,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t lo = row_lo - (u_lo + kt), hi = row_hi + 1 - (u_lo + kt);
         c_lo = static_cast<int>(lo < 0 ? 0 : (lo > 64 ? 64 : lo));
         c_hi = row_valid ? static_cast<int>(hi < 0 ? 0 : (hi > 64 ? 64 : hi)) : 0;
+      } else if (KIND == kFused && seg == 2) {
+        // window key j is the raw token tq - W + 1 + j; tokens before 0 do not exist
+        const int64_t lo = (int64_t)a.W - 1 - tq - kt;
+        c_lo = static_cast<int>(lo < 0 ? 0 : (lo > 64 ? 64 : lo));
       }
       const bool full_tile =
           __all_sync(0xffffffffu, colmask == ~0ull && c_lo == 0 && c_hi == 64);
@@ -773,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int num_sms,
                     AttnPlan* p) {
   if (H < 1 || H > 128 || D < 64 || D > 512 || (D % 64) || B < 1 || T < 1) return false;
-  const int G = (kind == kSparse) ? 1 : (128 / H);
+  const int G = (kind == kSparse || kind == kFused) ? 1 : (128 / H);
   const int n_rb = (T + G - 1) / G;
   const int nds = D > 256 ? 2 : 1;
   const int64_t max_keys = kind == kSwa ? (n_keys + G - 1) : n_keys;
@@ -822,32 +953,32 @@ bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int nu
   return true;
 }
 
-cudaError_t launch_attention(const CUtensorMap& tm_kv, const CUtensorMap& tm_q, const AttnArgs& a,
-                             const AttnPlan& p, cudaStream_t stream) {
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& tm_kv, const CUtensorMap& tm_kv2,
+                        const CUtensorMap& tm_q, const AttnArgs& a, const AttnPlan& p,
+                        cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<KIND>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(p.smem_bytes));
+  if (e != cudaSuccess) return e;
   dim3 grid(p.nds * p.nsplit, p.n_rb, a.B);
-  cudaError_t e = cudaSuccess;
+  attn_kernel<KIND><<<grid, kThreads, p.smem_bytes, stream>>>(tm_kv, tm_kv2, tm_q, a, p.nslot);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const CUtensorMap& tm_kv, const CUtensorMap& tm_kv2,
+                             const CUtensorMap& tm_q, const AttnArgs& a, const AttnPlan& p,
+                             cudaStream_t stream) {
   switch (a.kind) {
     case kSparse:
-      e = cudaFuncSetAttribute(attn_kernel<kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(p.smem_bytes));
-      if (e == cudaSuccess)
-        attn_kernel<kSparse><<<grid, kThreads, p.smem_bytes, stream>>>(tm_kv, tm_q, a, p.nslot);
-      break;
+      return launch_kind<kSparse>(tm_kv, tm_kv2, tm_q, a, p, stream);
     case kHca:
-      e = cudaFuncSetAttribute(attn_kernel<kHca>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(p.smem_bytes));
-      if (e == cudaSuccess)
-        attn_kernel<kHca><<<grid, kThreads, p.smem_bytes, stream>>>(tm_kv, tm_q, a, p.nslot);
-      break;
+      return launch_kind<kHca>(tm_kv, tm_kv2, tm_q, a, p, stream);
+    case kSwa:
+      return launch_kind<kSwa>(tm_kv, tm_kv2, tm_q, a, p, stream);
     default:
-      e = cudaFuncSetAttribute(attn_kernel<kSwa>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(p.smem_bytes));
-      if (e == cudaSuccess)
-        attn_kernel<kSwa><<<grid, kThreads, p.smem_bytes, stream>>>(tm_kv, tm_q, a, p.nslot);
-      break;
+      return launch_kind<kFused>(tm_kv, tm_kv2, tm_q, a, p, stream);
   }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
 }  // namespace hattn

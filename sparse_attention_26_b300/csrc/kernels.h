@@ -68,7 +68,9 @@ bool plan_topk(int rows, int64_t N_cap, int num_sms, TopkPlan* p);
 cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, cudaStream_t stream);
 
 // ------------------------------------------------------------ attention
-enum AttnKind { kSparse = 0, kHca = 1, kSwa = 2 };
+// kFused: one query's CSA (top-k), HCA and SWA keys as one key list, so a
+// single softmax (and one set of split partials) covers all three branches.
+enum AttnKind { kSparse = 0, kHca = 1, kSwa = 2, kFused = 3 };
 
 // ------------------------------------------------------------ query prep
 struct QPrepArgs {
@@ -84,7 +86,7 @@ cudaError_t launch_qprep(const QPrepArgs& a, cudaStream_t stream);
 
 struct AttnArgs {
   const __nv_bfloat16* q;       // prepared queries q~ [B][T][H][D]
-  const __nv_bfloat16* kv;      // cache [B][N_cap][D] (sparse/HCA) or raw [B][L_cap][D] (SWA)
+  const __nv_bfloat16* kv;      // cache [B][N_cap][D] (sparse/HCA/fused CSA) or raw [B][L_cap][D] (SWA)
   const float* gamma_kv;        // SWA only
   const int32_t* idx;           // sparse only [B][T][k]
   const int32_t* pos;           // [B][T]
@@ -96,7 +98,8 @@ struct AttnArgs {
   int* status;
   int kind, B, T, H, D, r;
   int64_t N_rows;               // rows per sequence of kv (N_cap or L_cap)
-  int k, m, W;
+  int64_t N_h;                  // fused: HCA entries per sequence (second tensor map)
+  int k, m, W;                  // fused: W keys per query in the SWA key buffer [B][T][W][D]
   float eps, scale;             // eps: SWA key norm
   RopeCoef rope;                // SWA key RoPE
   int G;                        // queries per row block
@@ -111,8 +114,26 @@ struct AttnPlan {
 };
 bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int num_sms,
                     AttnPlan* p);
-cudaError_t launch_attention(const CUtensorMap& tm_kv, const CUtensorMap& tm_q, const AttnArgs& a,
-                             const AttnPlan& p, cudaStream_t stream);
+// tm_kv: HCA entries / SWA raw tokens (fused: HCA entries); tm_kv2: fused only,
+// the SWA key buffer.
+cudaError_t launch_attention(const CUtensorMap& tm_kv, const CUtensorMap& tm_kv2,
+                             const CUtensorMap& tm_q, const AttnArgs& a, const AttnPlan& p,
+                             cudaStream_t stream);
+
+// ------------------------------------------------------------ SWA keys
+// kv_w[b][t][j] = RoPE_u(RMSNorm(kv_raw[b][u])), u = pos[b][t] - W + 1 + j
+// (a zero row where u < 0 or u >= L_cap).
+struct SwaKeysArgs {
+  const __nv_bfloat16* kv_raw;  // [B][L_cap][D]
+  const float* gamma;           // [D] or null
+  const int32_t* pos;           // [B][T]
+  __nv_bfloat16* kv_w;          // [B][T][W][D]
+  int B, T, D, r, W;
+  int64_t L_cap;
+  float eps;
+  RopeCoef rope;
+};
+cudaError_t launch_swa_keys(const SwaKeysArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------ merges
 struct CombineArgs {

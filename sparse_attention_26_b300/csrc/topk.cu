@@ -19,6 +19,8 @@
 // deterministic.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -41,7 +43,8 @@ struct TopkShared {
   uint32_t warp_tot[32];
   int counts[2];       // keys above the threshold, keys equal to it (this CTA)
   int offs[2];         // the same counts summed over the lower-ranked CTAs
-  int ctr;
+  int ctr, ctr_eq;
+  int eq_total;        // keys equal to the threshold in the whole cluster
   uint32_t digit;
   uint32_t above;
 };
@@ -173,6 +176,7 @@ __global__ void topk_kernel(const TopkArgs a) {
     sh->counts[0] = 0;
     sh->counts[1] = 0;
     sh->ctr = 0;
+    sh->ctr_eq = 0;
   }
   __syncthreads();
   int gt = 0, eq = 0;
@@ -184,48 +188,138 @@ __global__ void topk_kernel(const TopkArgs a) {
   if (eq) atomicAdd(&sh->counts[1], eq);
   cluster.sync();
   if (tid < 32) {
-    // counts of the lower-ranked CTAs, summed by one warp
-    int g = 0, e = 0;
-    if (tid < rank) {
+    // counts of the lower-ranked CTAs, and the cluster's tie total, summed by
+    // one warp (C <= 32)
+    int g = 0, e = 0, et = 0;
+    if (tid < C) {
       const int* rc = cluster.map_shared_rank(sh->counts, tid);
-      g = rc[0];
-      e = rc[1];
+      et = rc[1];
+      if (tid < rank) {
+        g = rc[0];
+        e = et;
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       g += __shfl_xor_sync(0xffffffffu, g, o);
       e += __shfl_xor_sync(0xffffffffu, e, o);
+      et += __shfl_xor_sync(0xffffffffu, et, o);
     }
     if (tid == 0) {
       sh->offs[0] = g;
       sh->offs[1] = e;
+      sh->eq_total = et;
     }
   }
   __syncthreads();
   const int off_gt = sh->offs[0];
   const int off_eq = sh->offs[1];
-  // keys above the threshold: any order
-  for (int e = tid; e < len; e += nthr) {
-    if (keys[e] > thr) {
-      const int p = atomicAdd(&sh->ctr, 1);
-      out[off_gt + p] = static_cast<int32_t>(start + e);
+  const int base = a.k - static_cast<int>(need);  // ties go to [base, k)
+  if (sh->eq_total == static_cast<int>(need)) {
+    // every tie is selected (the usual case: one key holds the k-th score),
+    // so no order is needed: keys above and at the threshold are appended
+    for (int e = tid; e < len; e += nthr) {
+      const uint32_t key = keys[e];
+      if (key > thr) {
+        const int p = atomicAdd(&sh->ctr, 1);
+        out[off_gt + p] = static_cast<int32_t>(start + e);
+      } else if (key == thr) {
+        const int p = atomicAdd(&sh->ctr_eq, 1);
+        out[base + off_eq + p] = static_cast<int32_t>(start + e);
+      }
     }
-  }
-  // threshold ties in index order: each thread owns a contiguous run
-  const int per_t = (len + nthr - 1) / nthr;
-  const int e0 = tid * per_t;
-  const int e1 = min(len, e0 + per_t);
-  uint32_t c = 0;
-  for (int e = e0; e < e1; ++e) c += keys[e] == thr;
-  uint32_t rnk = static_cast<uint32_t>(off_eq) + block_exclusive_scan(c, sh, tid, nthr);
-  const int base = a.k - static_cast<int>(need);
-  for (int e = e0; e < e1 && rnk < need; ++e) {
-    if (keys[e] == thr) {
-      out[base + rnk] = static_cast<int32_t>(start + e);
-      ++rnk;
+  } else {
+    // keys above the threshold: any order
+    for (int e = tid; e < len; e += nthr) {
+      if (keys[e] > thr) {
+        const int p = atomicAdd(&sh->ctr, 1);
+        out[off_gt + p] = static_cast<int32_t>(start + e);
+      }
+    }
+    // more ties than places: the ties with the smaller indices win, so each
+    // thread owns a contiguous run and ranks its ties by a block scan; the
+    // count visits the run in a per-lane rotated order (no bank conflicts)
+    const int per_t = (len + nthr - 1) / nthr;
+    const int e0 = tid * per_t;
+    const int n_run = max(0, min(len, e0 + per_t) - e0);
+    const int r0 = n_run > 0 ? (tid & 31) % n_run : 0;
+    uint32_t c = 0;
+    for (int j = 0; j < n_run; ++j) {
+      int jj = j + r0;
+      if (jj >= n_run) jj -= n_run;
+      c += keys[e0 + jj] == thr;
+    }
+    uint32_t rnk = static_cast<uint32_t>(off_eq) + block_exclusive_scan(c, sh, tid, nthr);
+    for (int j = 0; j < n_run && c > 0 && rnk < need; ++j) {
+      if (keys[e0 + j] == thr) {
+        out[base + rnk] = static_cast<int32_t>(start + e0 + j);
+        ++rnk;
+        --c;
+      }
     }
   }
   cluster.sync();  // keep this CTA's shared memory alive for the others' reads
+}
+
+// Clusters of C CTAs (threads, smem per CTA) that the device can hold at
+// once; queried once per (device, shape) and remembered.
+struct OccKey {
+  int dev, C, threads;
+  size_t smem;
+  int n;
+};
+OccKey g_occ[64];
+int g_nocc = 0;
+std::mutex g_occ_mu;
+
+int query_active_clusters(int C, int threads, size_t smem);
+
+int max_active_clusters(int C, int threads, size_t smem) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(g_occ_mu);
+  for (int i = 0; i < g_nocc; ++i)
+    if (g_occ[i].dev == dev && g_occ[i].C == C && g_occ[i].threads == threads &&
+        g_occ[i].smem == smem)
+      return g_occ[i].n;
+  const int n = query_active_clusters(C, threads, smem);
+  if (g_nocc < 64) g_occ[g_nocc++] = OccKey{dev, C, threads, smem, n};
+  return n;
+}
+
+int query_active_clusters(int C, int threads, size_t smem) {
+  if (C > 8) cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, topk_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+void fill_plan(int C, int64_t N_cap, TopkPlan* p) {
+  int slice = static_cast<int>((N_cap + C - 1) / C);
+  if (slice < 1) slice = 1;
+  p->cluster = C;
+  p->slice = slice;
+  p->threads = slice >= 8192 ? 1024 : (slice >= 2048 ? 512 : 256);
+  p->smem_bytes = sizeof(TopkShared) + static_cast<size_t>(slice) * 4;
 }
 
 }  // namespace
@@ -238,43 +332,27 @@ bool plan_topk(int rows, int64_t N_cap, int num_sms, TopkPlan* p) {
   while (C < 16 && (int64_t)rows * C < num_sms && (N_cap + 2 * C - 1) / (2 * C) >= 2048) C *= 2;
   while (C < 16 && (N_cap + C - 1) / C > max_slice) C *= 2;
   if ((N_cap + C - 1) / C > max_slice) return false;
-  if (C > 8) {
-    // 16-CTA clusters are non-portable; fall back to 8 when they cannot be scheduled
-    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  }
-  int slice = static_cast<int>((N_cap + C - 1) / C);
-  if (slice < 1) slice = 1;
-  p->cluster = C;
-  p->slice = slice;
-  p->threads = slice >= 8192 ? 1024 : (slice >= 2048 ? 512 : 256);
-  p->smem_bytes = sizeof(TopkShared) + static_cast<size_t>(slice) * 4;
-  if (C > 8) {
-    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(p->smem_bytes));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(C, 1, 1);
-    cfg.blockDim = dim3(p->threads, 1, 1);
-    cfg.dynamicSmemBytes = p->smem_bytes;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = C;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, topk_kernel, &cfg) != cudaSuccess ||
-        nclusters < 1) {
-      cudaGetLastError();
-      C = 8;
-      slice = static_cast<int>((N_cap + C - 1) / C);
-      if (slice > max_slice) return false;
-      p->cluster = C;
-      p->slice = slice;
-      p->threads = slice >= 8192 ? 1024 : (slice >= 2048 ? 512 : 256);
-      p->smem_bytes = sizeof(TopkShared) + static_cast<size_t>(slice) * 4;
+  // Clusters that do not all fit on the device at once run in waves, and a
+  // second wave repeats every fixed cost (the barriers and scans of each
+  // pass, about as much as 16K keys of work).  Take the cluster size with the
+  // least (waves x (keys per CTA + 16K)), the larger size on ties.
+  int64_t best_cost = -1;
+  TopkPlan best = {};
+  for (int c = C; c >= 1; c >>= 1) {
+    if ((N_cap + c - 1) / c > max_slice) break;
+    TopkPlan q;
+    fill_plan(c, N_cap, &q);
+    const int n = max_active_clusters(c, q.threads, q.smem_bytes);
+    if (n < 1) continue;
+    const int64_t waves = (rows + n - 1) / n;
+    const int64_t cost = waves * (q.slice + 16384);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = q;
     }
   }
+  if (best_cost < 0) return false;
+  *p = best;
   return true;
 }
 

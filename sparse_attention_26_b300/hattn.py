@@ -49,6 +49,14 @@ _SIGS = {
     "hattn_swa_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
                               _i32, _f32, _f32, _f32, _vp, _vp, _vp, _sz, _vp]),
     "hattn_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32]),
+    "hattn_swa_keys": (_i32, [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _f32, _f32, _vp,
+                              _vp]),
+    "hattn_hybrid_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i32,
+                                 _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32, _vp, _vp,
+                                 _vp, _sz, _vp]),
+    "hattn_hybrid_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
+                                                _i32]),
+    "hattn_hybrid_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64, _i32]),
     "hattn_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64]),
     "hattn_lse_merge_splits": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i32),
                                       _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
@@ -366,6 +374,63 @@ def swa_attn(q, kv_raw, pos, *, r, W=128, gamma_q=None, gamma_kv=None, rope_base
                                 B, T, H, D, kv_raw.shape[1], W, r, rope_base, eps, scale, _ptr(o),
                                 _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
     return _result(KIND_SWA, q, W, o, lse, workspace, q_prepped, partials)
+
+
+def swa_keys(kv_raw, pos, *, r, W=128, gamma_kv=None, rope_base=10000.0, eps=1e-6, kv_w=None,
+             stream=None):
+    """The normalised, roped window tokens of every query, kv_w [B, T, W, D]
+    bf16 (row j is token pos - W + 1 + j; zero rows before token 0)."""
+    _need(kv_raw, "kv_raw", torch.bfloat16, 3)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    B, L, D = kv_raw.shape
+    T = pos.shape[1]
+    if kv_w is None:
+        kv_w = torch.empty((B, T, W, D), dtype=torch.bfloat16, device=kv_raw.device)
+    _need(kv_w, "kv_w", torch.bfloat16, 4)
+    _check(lib().hattn_swa_keys(_ptr(kv_raw), _ptr(gamma_kv), _ptr(pos), B, T, L, D, W, r,
+                                rope_base, eps, _ptr(kv_w), _stream(stream)))
+    return kv_w
+
+
+def hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, q_prepped=False, partials=False):
+    return lib().hattn_hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, int(bool(q_prepped)),
+                                                   int(bool(partials)))
+
+
+def hybrid_attn_splits(B, T, H, D, k, N_h, W):
+    return lib().hattn_hybrid_attn_splits(B, T, H, D, k, N_h, W)
+
+
+def hybrid_attn(q, kv_c, idx, kv_h, kv_w, pos, *, r, m=128, gamma_q=None, rope_base=10000.0,
+                eps=1e-6, scale=None, o=None, lse=None, workspace=None, q_prepped=False,
+                partials=False, stream=None):
+    """CSA (selected entries), HCA (visible entries) and SWA (kv_w from
+    swa_keys) keys of each query under one softmax; returns (o fp32, lse
+    fp32) or, with partials=True, a Partials view of the workspace."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv_c, "kv_c", torch.bfloat16, 3)
+    _need(idx, "idx", torch.int32, 3)
+    _need(kv_h, "kv_h", torch.bfloat16, 3)
+    _need(kv_w, "kv_w", torch.bfloat16, 4)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(gamma_q, "gamma_q", torch.float32)
+    B, T, H, D = q.shape
+    k, N_h, W = idx.shape[2], kv_h.shape[1], kv_w.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if not partials:
+        o, lse = _attn_out(q, o, lse)
+    need = hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, q_prepped, partials)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().hattn_hybrid_attn(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_c),
+                                   _ptr(idx), kv_c.shape[1], k, _ptr(kv_h), N_h, m, _ptr(kv_w),
+                                   W, _ptr(pos), B, T, H, D, r, rope_base, eps, scale, _ptr(o),
+                                   _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
+    if not partials:
+        return o, lse
+    return Partials(workspace, q_prepped, B, T, H, D, hybrid_attn_splits(B, T, H, D, k, N_h, W))
 
 
 # ------------------------------------------------------------------ merge

@@ -166,3 +166,30 @@ def test_merge_splits_validation(L):
     assert rc == hattn.INVALID_ARG and "nsplit" in _err(L)
     rc = L.hattn_lse_merge_splits(arr, arr, N, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
     assert rc == hattn.INVALID_ARG
+
+
+def test_fused_attention_validation_and_sizes(L):
+    N = None
+    # hattn_hybrid_attn(q, gamma_q, q_prepped, kv_c, idx, N_c, k, kv_h, N_h, m, kv_w, W, pos,
+    #                   B, T, H, D, r, rope_base, eps, scale, o, lse, ws, ws_bytes, stream)
+    args = [FAKE, N, 1, FAKE, FAKE, 1000, 64, FAKE, 100, 128, FAKE, 128, FAKE,
+            2, 1, 128, 512, 64, 1e4, 1e-6, 0.04, FAKE, FAKE, FAKE, 1 << 30, N]
+    bad = list(args)
+    bad[10] = N  # no SWA key buffer
+    assert L.hattn_hybrid_attn(*bad) == hattn.INVALID_ARG and "kv_w" in _err(L)
+    bad = list(args)
+    bad[8] = 0  # empty HCA cache
+    assert L.hattn_hybrid_attn(*bad) == hattn.INVALID_ARG and "HCA" in _err(L)
+    bad = list(args)
+    bad[4] = N  # no top-k indices
+    assert L.hattn_hybrid_attn(*bad) == hattn.INVALID_ARG and "idx" in _err(L)
+    # the fused call splits its keys like the branches and keeps partials per split
+    n = hattn.hybrid_attn_splits(8, 1, 128, 512, 1024, 8192, 128)
+    assert n > 1
+    assert hattn.hybrid_attn_workspace_bytes(8, 1, 128, 512, 1024, 8192, 128, q_prepped=True,
+                                             partials=True) == 8 * 128 * n * (512 + 1) * 4
+    # hattn_swa_keys(kv_raw, gamma_kv, pos, B, T, L_cap, D, W, r, rope_base, eps, kv_w, stream)
+    assert L.hattn_swa_keys(FAKE, N, FAKE, 1, 1, 100, 512, 0, 64, 1e4, 1e-6, FAKE,
+                            N) == hattn.INVALID_ARG
+    assert L.hattn_swa_keys(FAKE, N, FAKE, 1, 1, 100, 512, 128, 64, 1e4, 1e-6, MISAL,
+                            N) == hattn.MISALIGNED

@@ -351,6 +351,94 @@ def test_merge_of_split_partials(B, H, D, r, N_hca, k, N_c, L):
     check_attn(out2, lse2, ref, rl, "merge of combined branches")
 
 
+# ------------------------------------------------------------------ fused branches
+@pytest.mark.parametrize("B,T,H,D,r,L,W", [
+    (2, 3, 128, 512, 64, 300, 128),
+    (1, 2, 4, 64, 16, 40, 96),
+])
+def test_swa_keys(B, T, H, D, r, L, W):
+    """Each window row is the oracle's normalised, roped raw token (zero rows
+    before token 0)."""
+    raw = randn_bf16((B, L, D), 101)
+    gk = 1.0 + 0.1 * randn_f32((D,), 102)
+    pl = [L - 1, 5, L // 2][:T] * B
+    pos = _pos(B, T, pl[:B * T])
+    kv_w = hattn.swa_keys(raw.to(DEV), pos.to(DEV), r=r, W=W, gamma_kv=gk.to(DEV))
+    hattn.check_status()
+    got = f64(kv_w)
+    for b in range(B):
+        for t in range(T):
+            p = int(pos[b, t])
+            for j in range(W):
+                u = p - W + 1 + j
+                if u < 0:
+                    assert (got[b, t, j] == 0).all()
+                    continue
+                if j % 17 and j != W - 1:
+                    continue  # a sample of the rows
+                ref = orc.rope(orc.rmsnorm(orc.bf16_to_f64(bits(raw[b, u])), gk.numpy()), r, u)
+                assert rel_l2(got[b, t, j], ref) <= KV_REL_L2, (b, t, j)
+
+
+@pytest.mark.parametrize("B,T,H,D,r,N_hca,k,N_c,L,pos_list", [
+    # decode at full head width: every segment split across SMs, a ragged HCA tail
+    (3, 1, 128, 512, 64, 900, 300, 5000, 20480, [20479, 20479 - 7 * 129, 11111]),
+    # queries before the window is full, short HCA prefixes, one with none
+    (2, 2, 128, 512, 64, 40, 64, 100, 400, [100, 127, 130, 399]),
+    # fewer heads than MMA rows (one query per row block)
+    (2, 1, 64, 512, 64, 100, 128, 300, 1300, [1299, 700]),
+])
+def test_hybrid_attn(B, T, H, D, r, N_hca, k, N_c, L, pos_list):
+    """One softmax over the selected CSA entries, the HCA entries and the SWA
+    window, merged with the sink, equals the oracle's merge of the three
+    branches -- through the direct output and through the split partials."""
+    q = randn_bf16((B, T, H, D), 91)
+    kv_h = randn_bf16((B, N_hca, D), 92)
+    kv_c = randn_bf16((B, N_c, D), 93)
+    raw = randn_bf16((B, L, D), 94)
+    sink = randn_f32((H,), 95)
+    pos = _pos(B, T, pos_list)
+    nvis = np.array([min((int(p) + 1) // 4, N_c) for p in pos.ravel()]).reshape(B, T)
+    idx = synth.random_idx(B, T, k, nvis, seed=96)
+    kvh_dev = kv_h.to(DEV)
+    # HCA entries that are not visible to any query may hold anything
+    nh = [min((int(p) + 1) // 128, N_hca) for p in pos.ravel()]
+    for bb in range(B):
+        top = max(nh[bb * T:(bb + 1) * T])
+        kvh_dev[bb, top:] = float("nan")
+    d = dict(q=q.to(DEV), pos=pos.to(DEV))
+    qt = hattn.query_prep(d["q"], d["pos"], r=r)
+    kv_w = hattn.swa_keys(raw.to(DEV), d["pos"], r=r, W=128)
+    o, l = hattn.hybrid_attn(qt, kv_c.to(DEV), idx.to(DEV), kvh_dev, kv_w, d["pos"], r=r,
+                             q_prepped=True)
+    out, lse = hattn.lse_merge([o], [l], d["pos"], r=r, sink=sink.to(DEV))
+    part = hattn.hybrid_attn(qt, kv_c.to(DEV), idx.to(DEV), kvh_dev, kv_w, d["pos"], r=r,
+                             q_prepped=True, partials=True)
+    out2, lse2 = hattn.lse_merge_splits([part], d["pos"], r=r, H=H, sink=sink.to(DEV))
+    hattn.check_status()
+    qb, pn = bits(q), pos.numpy()
+    ro = [orc.attention(orc.KIND_SPARSE, qb, bits(kv_c), pn, idx=idx.numpy(), r=r),
+          orc.attention(orc.KIND_HCA, qb, bits(kv_h), pn, m=128, r=r),
+          orc.attention(orc.KIND_SWA, qb, bits(raw), pn, W=128, r=r)]
+    ref, rl = orc.merge([x[0] for x in ro], [x[1] for x in ro], sink.numpy(), pn, r)
+    check_attn(out, lse, ref, rl, "fused, direct output")
+    check_attn(out2, lse2, ref, rl, "fused, split partials")
+
+
+def test_hybrid_attn_bad_index_is_reported():
+    """An index past the CSA cache is skipped and reported, not read."""
+    B, T, H, D, r = 1, 1, 128, 512, 64
+    q = randn_bf16((B, T, H, D), 97).to(DEV)
+    kv_c = randn_bf16((B, 64, D), 98).to(DEV)
+    kv_h = randn_bf16((B, 8, D), 99).to(DEV)
+    pos = _pos(B, T, [255]).to(DEV)
+    idx = torch.full((B, T, 64), -1, dtype=torch.int32)
+    idx[0, 0, :3] = torch.tensor([1, 64, 5])
+    kv_w = hattn.swa_keys(randn_bf16((B, 256, D), 100).to(DEV), pos, r=r, W=128)
+    hattn.hybrid_attn(q, kv_c, idx.to(DEV), kv_h, kv_w, pos, r=r)
+    assert hattn.check_status_code() == hattn.DEVICE_INDEX
+
+
 # ------------------------------------------------------------------ whole tiny layer
 def test_tiny_layer_end_to_end():
     wl = synth.WORKLOADS["tiny"]

@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--context", type=int, default=0, help="override L (profiling only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dense-sms", type=int, default=0,
+                    help="SMs for the HCA+SWA attention beside the indexer (0: the layer's "
+                         "cost model; profiling only)")
     ap.add_argument("--soak-ms", type=float, default=1500.0,
                     help="replay time under the clock sampler before the timed region")
     return ap.parse_args()
@@ -374,6 +377,7 @@ def run_ours(args, world, rank, local):
     inp = synth.make_inputs(wl, seed=0, device=dev)
     raw = {k: inp[k] for k in ["kv_raw", "ik_raw", "gate_csa", "gate_hca"]}
     layer = HybridLayer(wl, raw, device=dev)
+    layer.override_dense_sms = args.dense_sms
     q, iq, w, pos, sink = inp["q"], inp["iq"], inp["w"], inp["pos"], inp["sink"]
     t_new = wl.L - 1
     torch.cuda.synchronize()
@@ -445,7 +449,7 @@ def run_ours(args, world, rank, local):
     if not args.no_e2e:
         e2e = run_e2e(args, world, layer, inp, wl, t_new, stream, side)
 
-    launches = layer.launches_per_step(wl.T, t_new) * K
+    launches = layer.launches_per_step(wl.T, t_new, side_stream=True) * K
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,

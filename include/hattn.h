@@ -143,6 +143,14 @@ HATTN_API int hattn_indexer_topk_noalloc(const void* iq, const float* w, const v
 HATTN_API int hattn_indexer_scores(const void* iq, const float* w, const void* ik_c,
                                    const int32_t* pos, int B, int T, int HI, int dI,
                                    int64_t N_cap, int m, float* score_out, hattn_stream_t stream);
+/* hattn_indexer_scores on at most n_sms SMs (n_sms = 0: all).  The score
+ * kernel is persistent, one CTA per SM it uses; capping it leaves SMs free
+ * for work on another stream (the attention segments that do not need the
+ * top-k result), which then runs concurrently instead of after it. */
+HATTN_API int hattn_indexer_scores_sms(const void* iq, const float* w, const void* ik_c,
+                                       const int32_t* pos, int B, int T, int HI, int dI,
+                                       int64_t N_cap, int m, int n_sms, float* score_out,
+                                       hattn_stream_t stream);
 HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T,
                                 int64_t N_cap, int k, int m, int32_t* idx_out,
                                 hattn_stream_t stream);
@@ -219,22 +227,32 @@ HATTN_API int hattn_swa_keys(const void* kv_raw, const float* gamma_kv, const in
  * j < min(floor((pos+1)/m), N_h), and the existing window tokens
  * kv_w[b][t][j] (from hattn_swa_keys, j >= W-1-pos), all under one softmax.
  * Because each branch's own normalisation cancels in the sink merge, merging
- * this result (or its partials) with hattn_lse_merge(_splits), nb = 1, gives
- * the layer output of the three branch calls merged together.  The output
- * conventions (o/lse, partials with o == lse == NULL, q_prepped, workspace)
- * are those of the branch calls; the workspace size and split count come from
- * the two functions below.  One query per row block: the MMA rows are the H
- * heads of one query (H <= 128). */
+ * this result (or its partials) with hattn_lse_merge(_splits) gives the
+ * layer output of the three branch calls merged together.
+ *   segments: bit 0 CSA, bit 1 HCA, bit 2 SWA -- the key sets this call
+ *   covers (7 = all); the pointers of the others may be NULL.  Calls over
+ *   disjoint segment sets leave partials that one hattn_lse_merge_splits
+ *   combines, so the part that does not need the top-k result can run
+ *   concurrently with the indexer.
+ *   n_sms: the number of SMs the split plan assumes (0 = all of them); a
+ *   call meant to share the GPU with concurrent work plans for its share.
+ * The output conventions (o/lse, partials with o == lse == NULL, q_prepped,
+ * workspace) are those of the branch calls; the workspace size and split
+ * count come from the two functions below, given the same segments and
+ * n_sms.  One query per row block: the MMA rows are the H heads of one
+ * query (H <= 128). */
 HATTN_API int hattn_hybrid_attn(const void* q, const float* gamma_q, int q_prepped,
                                 const void* kv_c, const int32_t* idx, int64_t N_c, int k,
                                 const void* kv_h, int64_t N_h, int m, const void* kv_w, int W,
                                 const int32_t* pos, int B, int T, int H, int D, int r,
-                                float rope_base, float eps, float scale, void* o, float* lse,
-                                void* workspace, size_t ws_bytes, hattn_stream_t stream);
+                                float rope_base, float eps, float scale, int segments, int n_sms,
+                                void* o, float* lse, void* workspace, size_t ws_bytes,
+                                hattn_stream_t stream);
 HATTN_API size_t hattn_hybrid_attn_workspace_bytes(int B, int T, int H, int D, int k,
-                                                   int64_t N_h, int W, int q_prepped,
-                                                   int partials);
-HATTN_API int hattn_hybrid_attn_splits(int B, int T, int H, int D, int k, int64_t N_h, int W);
+                                                   int64_t N_h, int W, int segments, int n_sms,
+                                                   int q_prepped, int partials);
+HATTN_API int hattn_hybrid_attn_splits(int B, int T, int H, int D, int k, int64_t N_h, int W,
+                                       int segments, int n_sms);
 
 /* Split partials instead of a branch output: with o == NULL and lse == NULL
  * an attention call leaves the softmax of each key split in its workspace,

@@ -227,12 +227,21 @@ struct FusedSources {
   const void* kv_h;   // [B][N_h][D] HCA entries
   int64_t N_h;
   const void* kv_w;   // [B][T][W][D] SWA keys (hattn_swa_keys)
+  int segments;       // bit 0: CSA, bit 1: HCA, bit 2: SWA
+  int n_sms;          // SMs the split plan may assume (0: all)
 };
 
-// Keys the fused call plans for: each segment rounded up to whole tiles.
-int64_t fused_keys(int k, int64_t N_h, int W) {
+// Keys the fused call plans for: each segment it covers rounded up to whole
+// tiles.
+int64_t fused_keys(int k, int64_t N_h, int W, int segments) {
   auto up = [](int64_t n) { return (n + 63) / 64 * 64; };
-  return up(k) + up(N_h) + up(W);
+  return ((segments & 1) ? up(k) : 0) + ((segments & 2) ? up(N_h) : 0) +
+         ((segments & 4) ? up(W) : 0);
+}
+
+int fused_sms(int n_sms) {
+  const int all = num_sms_or_default();
+  return n_sms > 0 && n_sms < all ? n_sms : all;
 }
 
 int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, const void* kv,
@@ -241,7 +250,7 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
                 float scale, void* o, float* lse, void* workspace, size_t ws_bytes,
                 hattn_stream_t stream, const FusedSources* fs = nullptr) {
   REQUIRE_PTR(q);
-  REQUIRE_PTR(kv);
+  if (kind != kFused || (fs && (fs->segments & 1))) REQUIRE_PTR(kv);
   REQUIRE_PTR(pos);
   // o == lse == NULL: leave the split partials in the workspace for
   // hattn_lse_merge_splits instead of combining them
@@ -253,30 +262,40 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   }
   REQUIRE_F32(gamma_q);
   REQUIRE_F32(gamma_kv);
-  if (kind == kSparse || kind == kFused) REQUIRE_PTR(idx);
+  if (kind == kSparse) REQUIRE_PTR(idx);
   if (kind == kFused) {
     REQUIRE(fs != nullptr, "fused sources missing");
-    REQUIRE_PTR(fs->kv_h);
-    REQUIRE_PTR(fs->kv_w);
-    REQUIRE(fs->N_h >= 1, "the HCA cache needs at least one row");
-    REQUIRE((int64_t)B * fs->N_h < (1ll << 31), "B * N_h must be < 2^31");
-    REQUIRE((int64_t)B * T * W < (1ll << 31), "B * T * W must be < 2^31");
+    REQUIRE(fs->segments >= 1 && fs->segments <= 7, "segments=%d must be a mask in [1, 7]",
+            fs->segments);
+    REQUIRE(fs->n_sms >= 0, "n_sms=%d must be >= 0", fs->n_sms);
+    if (fs->segments & 1) REQUIRE_PTR(idx);
+    if (fs->segments & 2) {
+      REQUIRE_PTR(fs->kv_h);
+      REQUIRE(fs->N_h >= 1, "the HCA cache needs at least one row");
+      REQUIRE((int64_t)B * fs->N_h < (1ll << 31), "B * N_h must be < 2^31");
+    }
+    if (fs->segments & 4) {
+      REQUIRE_PTR(fs->kv_w);
+      REQUIRE((int64_t)B * T * W < (1ll << 31), "B * T * W must be < 2^31");
+    }
   }
   REQUIRE(B >= 1 && T >= 1, "B and T must be >= 1");
   REQUIRE(H >= 1 && H <= 128, "H=%d must be in [1, 128]", H);
   REQUIRE(D >= 64 && D <= 512 && D % 64 == 0, "D=%d must be a multiple of 64 in [64, 512]", D);
   REQUIRE(N_rows >= 1, "the key cache needs at least one row");
   REQUIRE((int64_t)B * N_rows < (1ll << 31), "B * rows of the cache must be < 2^31");
-  if (kind == kSparse || kind == kFused) REQUIRE(k >= 1 && k <= 65536, "k=%d out of range", k);
-  if (kind == kHca || kind == kFused) REQUIRE(m >= 1, "m must be >= 1");
-  if (kind == kSwa || kind == kFused) REQUIRE(W >= 1 && W <= 65536, "W=%d out of range", W);
+  const int segs = kind == kFused ? fs->segments : 0;
+  if (kind == kSparse || (segs & 1)) REQUIRE(k >= 1 && k <= 65536, "k=%d out of range", k);
+  if (kind == kHca || (segs & 2)) REQUIRE(m >= 1, "m must be >= 1");
+  if (kind == kSwa || (segs & 4)) REQUIRE(W >= 1 && W <= 65536, "W=%d out of range", W);
   REQUIRE(scale > 0.f, "scale must be positive");
   int rc = check_rope(D, r, rope_base, eps);
   if (rc) return rc;
-  const int64_t n_keys = kind == kFused ? fused_keys(k, fs->N_h, W)
+  const int64_t n_keys = kind == kFused ? fused_keys(k, fs->N_h, W, fs->segments)
                                          : (kind == kSparse ? k : (kind == kHca ? N_rows : W));
   AttnPlan p;
-  if (!plan_attention(kind, B, T, H, D, n_keys, num_sms_or_default(), &p))
+  if (!plan_attention(kind, B, T, H, D, n_keys,
+                      kind == kFused ? fused_sms(fs->n_sms) : num_sms_or_default(), &p))
     return fail(HATTN_ERR_UNSUPPORTED, "no attention kernel for H=%d D=%d", H, D);
   const size_t qbytes = qprep_bytes(B, T, H, D, q_prepped);
   const size_t pbytes = partials ? partial_bytes(B, T, H, D, p.nsplit) : p.ws_bytes;
@@ -290,22 +309,29 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   CUtensorMap tm, tm2, tm_q;
   memset(&tm, 0, sizeof tm);
   memset(&tm2, 0, sizeof tm2);
+  // Streamed keys arrive as groups of gsz 64-dim chunks (one CTA's share of
+  // a row's dims): a 3-D view {64 dims, rows, D/64 chunks} of the row-major
+  // cache, copied as boxes of {64, 64 keys, gsz} (8 KB per chunk, 128-byte
+  // swizzle, chunk after chunk in shared memory).
+  const int gsz = D / 64 / p.nds;
+  auto key_map = [&](CUtensorMap* m, const void* base, uint64_t rows, const char* what) {
+    const uint64_t dims[3] = {64, rows, (uint64_t)D / 64};
+    const uint64_t strides[2] = {(uint64_t)D * 2, 128};
+    const uint32_t box[3] = {64, 64, (uint32_t)gsz};
+    return make_tmap(m, base, 3, dims, strides, box, what);
+  };
   if (kind == kHca || kind == kSwa) {
-    // HCA entries / SWA raw tokens: 64 rows x 64 dims per copy
-    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)N_rows};
-    const uint64_t strides[1] = {(uint64_t)D * 2};
-    const uint32_t box[2] = {64, 64};
-    rc = make_tmap(&tm, kv, 2, dims, strides, box, kind == kHca ? "kv_h" : "kv_raw");
+    rc = key_map(&tm, kv, (uint64_t)B * (uint64_t)N_rows, kind == kHca ? "kv_h" : "kv_raw");
     if (rc) return rc;
   } else if (kind == kFused) {
-    const uint64_t strides[1] = {(uint64_t)D * 2};
-    const uint32_t box[2] = {64, 64};
-    const uint64_t dh[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)fs->N_h};
-    rc = make_tmap(&tm, fs->kv_h, 2, dh, strides, box, "kv_h");
-    if (rc) return rc;
-    const uint64_t dw[2] = {(uint64_t)D, (uint64_t)B * (uint64_t)T * (uint64_t)W};
-    rc = make_tmap(&tm2, fs->kv_w, 2, dw, strides, box, "kv_w");
-    if (rc) return rc;
+    if (fs->segments & 2) {
+      rc = key_map(&tm, fs->kv_h, (uint64_t)B * (uint64_t)fs->N_h, "kv_h");
+      if (rc) return rc;
+    }
+    if (fs->segments & 4) {
+      rc = key_map(&tm2, fs->kv_w, (uint64_t)B * (uint64_t)T * (uint64_t)W, "kv_w");
+      if (rc) return rc;
+    }
   }
   // prepared queries: the caller's, or this call's into the workspace
   const void* qt = q_prepped ? q : workspace;
@@ -345,6 +371,7 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.r = r;
   a.N_rows = N_rows;
   a.N_h = fs ? fs->N_h : 0;
+  a.segments = fs ? fs->segments : 0;
   a.k = k;
   a.m = m;
   a.W = W;
@@ -424,7 +451,7 @@ namespace {
 
 int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
                         int B, int T, int HI, int dI, int64_t N_cap, int m, float* scores,
-                        hattn_stream_t stream) {
+                        hattn_stream_t stream, int n_sms = 0) {
   REQUIRE_PTR(iq);
   REQUIRE_PTR(w);
   REQUIRE_PTR(ik_c);
@@ -435,6 +462,7 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
   REQUIRE(m >= 1, "m must be >= 1");
   REQUIRE((int64_t)B * T * HI < (1ll << 31), "too many query heads");
+  REQUIRE(n_sms >= 0, "n_sms=%d must be >= 0", n_sms);
   IndexerPlan ip;
   if (!plan_indexer(T, HI, dI, &ip))
     return fail(HATTN_ERR_UNSUPPORTED, "no indexer kernel for HI=%d dI=%d", HI, dI);
@@ -474,6 +502,9 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   a.nblk = static_cast<int>((N_cap + 127) / 128);
   a.N_cap = N_cap;
   a.total_slots = (int64_t)B * a.groups_per_seq * a.nblk;
+  // persistent: one CTA per SM it may use (n_sms of them when given, so
+  // that concurrent work keeps the others)
+  if (n_sms > 0 && n_sms < sms) sms = n_sms;
   const int grid = static_cast<int>(a.total_slots < sms ? a.total_slots : sms);
   cudaError_t e = launch_indexer_score(tm_ik, tm_iq, a, ip, grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
@@ -545,6 +576,12 @@ int hattn_indexer_scores(const void* iq, const float* w, const void* ik_c, const
                          int B, int T, int HI, int dI, int64_t N_cap, int m, float* score_out,
                          hattn_stream_t stream) {
   return indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, score_out, stream);
+}
+
+int hattn_indexer_scores_sms(const void* iq, const float* w, const void* ik_c,
+                             const int32_t* pos, int B, int T, int HI, int dI, int64_t N_cap,
+                             int m, int n_sms, float* score_out, hattn_stream_t stream) {
+  return indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms);
 }
 
 int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T, int64_t N_cap, int k,
@@ -645,25 +682,32 @@ int hattn_hca_attn(const void* q, const float* gamma_q, int q_prepped, const voi
 int hattn_hybrid_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_c,
                       const int32_t* idx, int64_t N_c, int k, const void* kv_h, int64_t N_h,
                       int m, const void* kv_w, int W, const int32_t* pos, int B, int T, int H,
-                      int D, int r, float rope_base, float eps, float scale, void* o,
-                      float* lse, void* workspace, size_t ws_bytes, hattn_stream_t stream) {
-  const FusedSources fs{kv_h, N_h, kv_w};
+                      int D, int r, float rope_base, float eps, float scale, int segments,
+                      int n_sms, void* o, float* lse, void* workspace, size_t ws_bytes,
+                      hattn_stream_t stream) {
+  const FusedSources fs{kv_h, N_h, kv_w, segments, n_sms};
   return attn_common(kFused, q, gamma_q, q_prepped, kv_c, nullptr, idx, pos, B, T, H, D, N_c, k,
                      m, W, r, rope_base, eps, scale, o, lse, workspace, ws_bytes, stream, &fs);
 }
 
 size_t hattn_hybrid_attn_workspace_bytes(int B, int T, int H, int D, int k, int64_t N_h, int W,
-                                         int q_prepped, int partials) {
+                                         int segments, int n_sms, int q_prepped,
+                                         int partials) {
   AttnPlan p;
-  if (!plan_attention(kFused, B, T, H, D, fused_keys(k, N_h, W), num_sms_or_default(), &p))
+  if (segments < 1 || segments > 7 || n_sms < 0) return 0;
+  if (!plan_attention(kFused, B, T, H, D, fused_keys(k, N_h, W, segments), fused_sms(n_sms),
+                      &p))
     return 0;
   return qprep_bytes(B, T, H, D, q_prepped) +
          (partials ? partial_bytes(B, T, H, D, p.nsplit) : p.ws_bytes);
 }
 
-int hattn_hybrid_attn_splits(int B, int T, int H, int D, int k, int64_t N_h, int W) {
+int hattn_hybrid_attn_splits(int B, int T, int H, int D, int k, int64_t N_h, int W,
+                             int segments, int n_sms) {
   AttnPlan p;
-  if (!plan_attention(kFused, B, T, H, D, fused_keys(k, N_h, W), num_sms_or_default(), &p))
+  if (segments < 1 || segments > 7 || n_sms < 0) return 0;
+  if (!plan_attention(kFused, B, T, H, D, fused_keys(k, N_h, W, segments), fused_sms(n_sms),
+                      &p))
     return 0;
   return p.nsplit;
 }

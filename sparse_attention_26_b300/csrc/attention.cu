@@ -218,9 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   SegTiles st;
   if (KIND == kFused) {
     // one query per row block (G = 1)
-    int64_t nh = vis(a.pos[(int64_t)b * a.T + t0], a.m);
-    if (nh > a.N_h) nh = a.N_h;
-    st.init(a.k, nh, a.W, split, a.nsplit);
+    int64_t nh = 0;
+    if (a.segments & 2) {
+      nh = vis(a.pos[(int64_t)b * a.T + t0], a.m);
+      if (nh > a.N_h) nh = a.N_h;
+    }
+    st.init((a.segments & 1) ? a.k : 0, (a.segments & 2) ? nh : 0, (a.segments & 4) ? a.W : 0,
+            split, a.nsplit);
   } else if (KIND == kSparse) {
     total = a.k;
   } else if (KIND == kHca) {
@@ -298,8 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm->abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
-    if (KIND != kSparse) tma_prefetch_desc(&tm_kv);
-    if (KIND == kFused) tma_prefetch_desc(&tm_kv2);
+    // (the fused call's maps exist only for the segments it covers)
+    if (KIND == kHca || KIND == kSwa || (KIND == kFused && (a.segments & 2)))
+      tma_prefetch_desc(&tm_kv);
+    if (KIND == kFused && (a.segments & 4)) tma_prefetch_desc(&tm_kv2);
   }
   if (warp == 4) {
     tmem_alloc(smem_u32(&sm->tmem_base), 512);
@@ -314,100 +320,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tO = tmem + 128;    // columns [128, 128 + ocols)
   const uint32_t tQ = tmem + 384;    // nds = 2: the other half of Q, 32 columns per chunk
 
-  // chunk order within a tile: the other half's d chunks first, then ours
-  auto chunk_dc = [&](int p) -> int {
-    if (p < n_other) {
-      const int oth = (dh == 0) ? 1 : 0;
-      return oth * n_own + p;
-    }
-    return dh * n_own + (p - n_other);
+  // The ring holds groups of gsz = n_own consecutive 8 KB chunk slots.  A
+  // tile is the group of the other half's d chunks (nds = 2: keys only, free
+  // once QK has read them), then the group of this CTA's own chunks (keys
+  // and values: PV reads the group as one operand).  A streamed group is one
+  // 3-D TMA copy {64 dims, 64 keys, gsz chunks}.
+  const int gsz = n_own;
+  const int ng = nslot / gsz;   // groups in the ring
+  const int ngt = ndc / gsz;    // groups per tile: 1 or 2
+  // the other half of Q is staged in the last two groups of the ring until
+  // it has been copied into tensor memory
+  const int64_t stage_group = n_other > 0 ? (nslot - 2 * n_other) / gsz : -1;
+  // first d chunk of group q of a tile
+  auto group_dc = [&](int q) -> int {
+    if (q < ngt - 1) return (dh == 0 ? 1 : 0) * n_own;  // the other half
+    return dh * n_own;
   };
 
   if (warp < 4) {
     // ============================================================ producers
     const int pt = threadIdx.x;  // 0..127
-    int64_t ctr = 0;
-    int slot = 0;
-    uint32_t ph = 0;  // ring position (slot, phase) of counter ctr
+    int64_t gc = 0;              // groups requested so far
+    int gs = 0;
+    uint32_t ph = 0;             // ring position (group slot, phase) of gc
     auto advance = [&]() {
-      ++ctr;
-      if (++slot == nslot) { slot = 0; ph ^= 1u; }
+      ++gc;
+      if (++gs == ng) { gs = 0; ph ^= 1u; }
     };
-    // the staging slots of Q are free once Q is in tensor memory
-    auto staging_free = [&](int64_t c) -> bool {
-      if (n_other == 0 || c != stage_slot) return true;
-      return mbar_wait(smem_u32(&sm->q_tmem), 0, abort, a.status, kWaitLimitNs, 33);
+    // the group slot of gc may be refilled: its last reader is done, and the
+    // staging groups of Q have been copied into tensor memory
+    auto group_free = [&](int site) -> bool {
+      if (gc == stage_group &&
+          !mbar_wait(smem_u32(&sm->q_tmem), 0, abort, a.status, kWaitLimitNs, 33))
+        return false;
+      return gc < ng ||
+             mbar_wait(smem_u32(&sm->empty[gs]), ph ^ 1u, abort, a.status, kWaitLimitNs, site);
     };
+    // copies issued whose completion nobody waited for land before exit
+    auto drain = [&](const uint64_t* bars, int64_t issued) {
+      const int64_t first = issued > ng ? issued - ng : 0;
+      for (int64_t x = first; x < issued; ++x)
+        mbar_wait(smem_u32(&bars[x % ng]), (x / ng) & 1, nullptr, nullptr, 10000000ull, 19);
+    };
+    const uint32_t gbytes = static_cast<uint32_t>(gsz) * 8192u;
     if (KIND == kHca) {
       if (pt == 0) {
-        for (int i = 0; i < nt && !*abort; ++i) {
-          for (int p = 0; p < ndc; ++p, advance()) {
-            if (!staging_free(ctr)) break;
-            if (ctr >= nslot &&
-                !mbar_wait(smem_u32(&sm->empty[slot]), ph ^ 1u, abort, a.status, kWaitLimitNs, 18))
-              break;
-            const uint32_t fb = smem_u32(&sm->full[slot]);
-            mbar_arrive_expect_tx(fb, 8192);
-            tma_load_2d(smem_u32(sRing + slot * 8192), &tm_kv, chunk_dc(p) * 64,
-                        static_cast<int32_t>((int64_t)b * a.N_rows + kbeg + (int64_t)i * kTile),
-                        fb);
+        bool ok = true;
+        for (int i = 0; i < nt && ok && !*abort; ++i) {
+          const int32_t row0 =
+              static_cast<int32_t>((int64_t)b * a.N_rows + kbeg + (int64_t)i * kTile);
+          for (int q = 0; q < ngt; ++q, advance()) {
+            if (!(ok = group_free(18))) break;
+            const uint32_t fb = smem_u32(&sm->full[gs]);
+            mbar_arrive_expect_tx(fb, gbytes);
+            tma_load_3d(smem_u32(sRing + gs * gbytes), &tm_kv, 0, row0, group_dc(q), fb);
           }
         }
-        if (*abort) {
-          const int64_t first = ctr > nslot ? ctr - nslot : 0;
-          for (int64_t x = first; x < ctr; ++x)
-            mbar_wait(smem_u32(&sm->full[x % nslot]), (x / nslot) & 1, nullptr, nullptr,
-                      10000000ull, 19);
-        }
+        if (!ok || *abort) drain(sm->full, gc);
       }
-    } else if (KIND == kSparse) {
-      // 512 16-byte pieces per chunk: this thread copies pieces pt + 128 q;
-      // each thread's arrival on the chunk's barrier fires when its copies
-      // have landed, so the producer never waits for its own copies
+    } else if (KIND == kSparse || KIND == kFused) {
+      // Gathered tiles: 512 16-byte pieces per chunk, this thread copies
+      // pieces pt + 128 j of every chunk of the group; its arrival on the
+      // group's barrier fires when its copies have landed, so it never waits
+      // for them itself.  Streamed tiles (fused): thread 0 arms the barrier
+      // and issues the copy, the others just arrive (128 arrivals either way).
       const int32_t* idx_row = a.idx + ((int64_t)b * a.T + t0) * a.k;
       bool ok = true;
-      for (int i = 0; i < nt && ok && !*abort; ++i) {
-        const __nv_bfloat16* src[4];
-        int bytes[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int rI = (pt + 128 * q) >> 3;
-          const int64_t kk = kbeg + (int64_t)i * kTile + rI;
-          int32_t j = -1;
-          if (kk < kend) j = idx_row[kk];
-          if (j >= a.N_rows) {
-            if ((pt & 7) == 0) record_status(a.status, kStatusBadIndex);
-            j = -1;
-          }
-          bytes[q] = j >= 0 ? 16 : 0;
-          src[q] = a.kv + ((int64_t)b * a.N_rows + (j >= 0 ? j : 0)) * a.D +
-                   ((pt + 128 * q) & 7) * 8;
-        }
-        for (int p = 0; p < ndc; ++p, advance()) {
-          if (!staging_free(ctr) ||
-              (ctr >= nslot &&
-               !mbar_wait(smem_u32(&sm->empty[slot]), ph ^ 1u, abort, a.status, kWaitLimitNs, 20))) {
-            ok = false;
-            break;
-          }
-          const int dcol = chunk_dc(p) * 64;
-          const uint32_t dst = smem_u32(sRing + slot * 8192);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int pc = pt + 128 * q;
-            cp_async16(dst + swz128(pc >> 3, pc & 7), src[q] + dcol, bytes[q]);
-          }
-          cp_async_mbar_arrive(smem_u32(&sm->full[slot]));
-        }
-      }
-      cp_async_wait_all();  // no copy outlives the CTA
-    } else if (KIND == kFused) {
-      // every producer thread takes part in every chunk (the full barriers
-      // count 128 arrivals): gathered chunks as in the sparse branch; for a
-      // streamed chunk thread 0 arms the barrier and issues the TMA copy
-      const int32_t* idx_row = a.idx + ((int64_t)b * a.T + t0) * a.k;
-      bool ok = true;
-      int64_t tma_issued = 0;  // chunks whose copy thread 0 has issued (for the abort drain)
+      int64_t tma_issued = 0;  // groups up to the last one thread 0 copied by TMA
       for (int i = 0; i < nt && ok && !*abort; ++i) {
         int seg, nvalid;
         int64_t kt;
@@ -416,64 +395,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bytes[4];
         if (seg == 0) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int rI = (pt + 128 * q) >> 3;
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const int rI = (pt + 128 * j4) >> 3;
             int32_t j = -1;
             if (rI < nvalid) j = idx_row[kt + rI];
             if (j >= a.N_rows) {
               if ((pt & 7) == 0) record_status(a.status, kStatusBadIndex);
               j = -1;
             }
-            bytes[q] = j >= 0 ? 16 : 0;
-            src[q] = a.kv + ((int64_t)b * a.N_rows + (j >= 0 ? j : 0)) * a.D +
-                     ((pt + 128 * q) & 7) * 8;
+            bytes[j4] = j >= 0 ? 16 : 0;
+            src[j4] = a.kv + ((int64_t)b * a.N_rows + (j >= 0 ? j : 0)) * a.D +
+                      ((pt + 128 * j4) & 7) * 8;
           }
         }
-        const int32_t row0 = seg == 1
-            ? static_cast<int32_t>((int64_t)b * a.N_h + kt)
-            : static_cast<int32_t>(((int64_t)b * a.T + t0) * a.W + kt);
-        for (int p = 0; p < ndc; ++p, advance()) {
-          if (!staging_free(ctr) ||
-              (ctr >= nslot &&
-               !mbar_wait(smem_u32(&sm->empty[slot]), ph ^ 1u, abort, a.status, kWaitLimitNs, 42))) {
-            ok = false;
-            break;
-          }
-          const int dcol = chunk_dc(p) * 64;
-          const uint32_t dst = smem_u32(sRing + slot * 8192);
-          const uint32_t fb = smem_u32(&sm->full[slot]);
+        int32_t row0 = 0;
+        if (KIND == kFused && seg != 0)
+          row0 = seg == 1 ? static_cast<int32_t>((int64_t)b * a.N_h + kt)
+                          : static_cast<int32_t>(((int64_t)b * a.T + t0) * a.W + kt);
+        for (int q = 0; q < ngt; ++q, advance()) {
+          if (!(ok = group_free(20))) break;
+          const uint32_t dst = smem_u32(sRing + gs * gbytes);
+          const uint32_t fb = smem_u32(&sm->full[gs]);
           if (seg == 0) {
+            const int dc0 = group_dc(q);
+            for (int e = 0; e < gsz; ++e) {
+              const int dcol = (dc0 + e) * 64;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int pc = pt + 128 * q;
-              cp_async16(dst + swz128(pc >> 3, pc & 7), src[q] + dcol, bytes[q]);
+              for (int j4 = 0; j4 < 4; ++j4) {
+                const int pc = pt + 128 * j4;
+                cp_async16(dst + e * 8192 + swz128(pc >> 3, pc & 7), src[j4] + dcol, bytes[j4]);
+              }
             }
             cp_async_mbar_arrive(fb);
           } else if (pt == 0) {
-            mbar_arrive_expect_tx(fb, 8192);
-            tma_load_2d(dst, seg == 1 ? &tm_kv : &tm_kv2, dcol, row0, fb);
-            tma_issued = ctr + 1;
+            mbar_arrive_expect_tx(fb, gbytes);
+            tma_load_3d(dst, seg == 1 ? &tm_kv : &tm_kv2, 0, row0, group_dc(q), fb);
+            tma_issued = gc + 1;
           } else {
             mbar_arrive(fb);
           }
         }
       }
       cp_async_wait_all();  // no copy outlives the CTA
-      if (!ok && pt == 0) {
-        // TMA copies issued whose completion nobody waited for land before exit
-        const int64_t first = tma_issued > nslot ? tma_issued - nslot : 0;
-        for (int64_t x = first; x < tma_issued; ++x)
-          mbar_wait(smem_u32(&sm->full[x % nslot]), (x / nslot) & 1, nullptr, nullptr,
-                    10000000ull, 43);
-      }
+      if ((!ok || *abort) && pt == 0 && tma_issued > 0) drain(sm->full, tma_issued);
     } else {
       // SWA: keys are RMSNorm'd and RoPE'd raw tokens at their own positions.
       // Row norms come first, from the rows in global memory (two threads per
-      // row, eight 16-byte loads in flight each); then every chunk of the
-      // tile is requested by TMA, and each is normalised in place as it lands.
+      // row, eight 16-byte loads in flight each); then the tile's groups are
+      // requested by TMA, and each is normalised in place as it lands.
       const int nr = pt >> 1, hf = pt & 1;
       const int half_pieces = a.D / 16;  // 16-byte pieces per half row
       bool ok = true;
+      int64_t issued = 0;  // groups thread 0 has requested
       for (int i = 0; i < nt; ++i) {
         const int64_t kt = kbeg + (int64_t)i * kTile;
         const int nvalid = static_cast<int>((kend - kt) < kTile ? (kend - kt) : kTile);
@@ -496,59 +469,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!named_bar_and(3, kProdThreads, ok && !*abort)) break;
         const float* inv_rms = sm->inv_rms[i & 1];
         if (pt == 0) {
-          int s = slot;
+          // request the tile's groups (thread 0 walks ahead of the others'
+          // ring position by up to one tile)
+          int64_t c = gc;
+          int s = gs;
           uint32_t phs = ph;
-          for (int p = 0; p < ndc && ok; ++p) {
-            const int64_t c = ctr + p;
-            ok = staging_free(c) &&
-                 (c < nslot ||
+          for (int q = 0; q < ngt && ok; ++q) {
+            ok = (c != stage_group ||
+                  mbar_wait(smem_u32(&sm->q_tmem), 0, abort, a.status, kWaitLimitNs, 33)) &&
+                 (c < ng ||
                   mbar_wait(smem_u32(&sm->empty[s]), phs ^ 1u, abort, a.status, kWaitLimitNs, 21));
             if (ok) {
               const uint32_t rbar = smem_u32(&sm->raw[s]);
-              mbar_arrive_expect_tx(rbar, 8192);
-              tma_load_2d(smem_u32(sRing + s * 8192), &tm_kv, chunk_dc(p) * 64,
-                          static_cast<int32_t>((int64_t)b * a.N_rows + u_lo + kt), rbar);
+              mbar_arrive_expect_tx(rbar, gbytes);
+              tma_load_3d(smem_u32(sRing + s * gbytes), &tm_kv, 0,
+                          static_cast<int32_t>((int64_t)b * a.N_rows + u_lo + kt), group_dc(q),
+                          rbar);
+              issued = c + 1;
             }
-            if (++s == nslot) { s = 0; phs ^= 1u; }
+            ++c;
+            if (++s == ng) { s = 0; phs ^= 1u; }
           }
         }
-        for (int p = 0; p < ndc; ++p, advance()) {
-          if (ok) ok = mbar_wait(smem_u32(&sm->raw[slot]), ph, abort, a.status, kWaitLimitNs, 26);
+        for (int q = 0; q < ngt; ++q, advance()) {
+          if (ok) ok = mbar_wait(smem_u32(&sm->raw[gs]), ph, abort, a.status, kWaitLimitNs, 26);
           if (!ok) continue;  // nothing more to wait for; the next barrier ends the loop
-          const int dcol = chunk_dc(p) * 64;
-          uint8_t* dst = sRing + slot * 8192;
+          const int dc0 = group_dc(q);
+          for (int e = 0; e < gsz; ++e) {
+            const int dcol = (dc0 + e) * 64;
+            uint8_t* dst = sRing + gs * gbytes + e * 8192;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int pc = pt + 128 * q;
-            const int rI = pc >> 3, piece = pc & 7;
-            uint4* cell = reinterpret_cast<uint4*>(dst + swz128(rI, piece));
-            float y[8];
-            if (rI < nvalid) {
-              unpack8(*cell, y);
-              const float inv = inv_rms[rI];
+            for (int j4 = 0; j4 < 4; ++j4) {
+              const int pc = pt + 128 * j4;
+              const int rI = pc >> 3, piece = pc & 7;
+              uint4* cell = reinterpret_cast<uint4*>(dst + swz128(rI, piece));
+              float y[8];
+              if (rI < nvalid) {
+                unpack8(*cell, y);
+                const float inv = inv_rms[rI];
 #pragma unroll
-              for (int z = 0; z < 8; ++z) {
-                const float gm = a.gamma_kv ? a.gamma_kv[dcol + piece * 8 + z] : 1.f;
-                y[z] = y[z] * inv * gm;
+                for (int z = 0; z < 8; ++z) {
+                  const float gm = a.gamma_kv ? a.gamma_kv[dcol + piece * 8 + z] : 1.f;
+                  y[z] = y[z] * inv * gm;
+                }
+                rope8(y, dcol + piece * 8, a.D, a.r, u_lo + kt + rI, a.rope.c);
+              } else {
+#pragma unroll
+                for (int z = 0; z < 8; ++z) y[z] = 0.f;
               }
-              rope8(y, dcol + piece * 8, a.D, a.r, u_lo + kt + rI, a.rope.c);
-            } else {
-#pragma unroll
-              for (int z = 0; z < 8; ++z) y[z] = 0.f;
+              *cell = pack8(y);
             }
-            *cell = pack8(y);
           }
           fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&sm->full[slot]));
+          mbar_arrive(smem_u32(&sm->full[gs]));
         }
       }
-      if (!ok && pt == 0) {
-        // copies issued whose completion nobody waited for land before exit
-        const int64_t first = ctr > nslot ? ctr - nslot : 0;
-        for (int64_t x = first; x < ctr; ++x)
-          mbar_wait(smem_u32(&sm->raw[x % nslot]), (x / nslot) & 1, nullptr, nullptr,
-                    10000000ull, 27);
-      }
+      if (!ok && pt == 0) drain(sm->raw, issued);
     }
   } else if (warp == 4 || warp == 9) {
     // ============================================================ QK issuers
@@ -604,12 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      // S(i) = Q K(i)^T over all ndc chunks; the other half's chunks are only
-      // keys, so they are released as soon as this product completes
-      for (int p = 0; p < ndc && ok; ++p) {
-        const int64_t c = (int64_t)i * ndc + p;
-        const int s = static_cast<int>(c % nslot);
-        const bool got = mbar_wait(smem_u32(&sm->full[s]), static_cast<uint32_t>((c / nslot) & 1),
+      // S(i) = Q K(i)^T over all ndc chunks, group by group; the other
+      // half's group holds only keys and is released once this product has
+      // read it
+      for (int q = 0; q < ngt && ok; ++q) {
+        const int64_t g = (int64_t)i * ngt + q;
+        const int gsl = static_cast<int>(g % ng);
+        const bool got = mbar_wait(smem_u32(&sm->full[gsl]), static_cast<uint32_t>((g / ng) & 1),
                                    abort, a.status, kWaitLimitNs, 22);
         ok = __all_sync(0xffffffffu, got);  // warp-uniform
         if (!ok) break;
@@ -619,27 +596,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((KIND == kHca || (KIND == kFused && seg != 0)) && nvalid < kTile) {
           // a streamed tail tile: zero its invalid key rows (they may hold
           // anything, and P = 0 times a NaN would still be NaN)
-          uint8_t* dst = sRing + s * 8192;
+          uint8_t* dst = sRing + gsl * gsz * 8192;
           for (int pc = nvalid * 8 + lane; pc < kTile * 8; pc += 32)
-            *reinterpret_cast<uint4*>(dst + swz128(pc >> 3, pc & 7)) = make_uint4(0, 0, 0, 0);
+            for (int e = 0; e < gsz; ++e)
+              *reinterpret_cast<uint4*>(dst + e * 8192 + swz128(pc >> 3, pc & 7)) =
+                  make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) {
           tc_fence_after();
+          for (int e = 0; e < gsz; ++e) {
+            const int p = q * gsz + e;  // chunk of the tile: the other half first
+            const uint32_t slot_a = sRa + static_cast<uint32_t>(gsl * gsz + e) * 8192u;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = smem_desc(sRa + s * 8192 + ks * 32, 16, 1024, kSwizzle128B);
-            const uint32_t acc = (p == 0 && ks == 0) ? 0u : 1u;
-            if (p < n_other) {
-              mma_bf16_ts(tS + sb * 64, tQ + p * 32 + ks * 8, bd, idesc_qk, acc);
-            } else {
-              const uint64_t ad =
-                  smem_desc(sQa + (p - n_other) * 16384 + ks * 32, 16, 1024, kSwizzle128B);
-              mma_bf16_ss(tS + sb * 64, ad, bd, idesc_qk, acc);
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t bd = smem_desc(slot_a + ks * 32, 16, 1024, kSwizzle128B);
+              const uint32_t acc = (p == 0 && ks == 0) ? 0u : 1u;
+              if (p < n_other) {
+                mma_bf16_ts(tS + sb * 64, tQ + p * 32 + ks * 8, bd, idesc_qk, acc);
+              } else {
+                const uint64_t ad =
+                    smem_desc(sQa + (p - n_other) * 16384 + ks * 32, 16, 1024, kSwizzle128B);
+                mma_bf16_ss(tS + sb * 64, ad, bd, idesc_qk, acc);
+              }
             }
           }
-          if (p < n_other) mma_commit(smem_u32(&sm->empty[s]));
+          if (q < ngt - 1) mma_commit(smem_u32(&sm->empty[gsl]));
         }
         __syncwarp();
       }
@@ -665,15 +648,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->p_full), i & 1, abort, a.status,
                                              kWaitLimitNs, 23));
       if (!ok) break;
-      const int64_t c0 = (int64_t)i * ndc + n_other;
-      const int s0 = static_cast<int>(c0 % nslot);
+      const int64_t g = (int64_t)i * ngt + (ngt - 1);  // the tile's own group
+      const int gsl = static_cast<int>(g % ng);
       if (KIND == kSparse || KIND == kFused) {
         // this warp's view of the gathered rows, for the async proxy
-        for (int e = 0; e < n_own && ok; ++e)
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(smem_u32(&sm->full[s0 + e]),
-                                    static_cast<uint32_t>(((c0 + e) / nslot) & 1), abort,
-                                    a.status, kWaitLimitNs, 38));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&sm->full[gsl]), static_cast<uint32_t>((g / ng) & 1),
+                                  abort, a.status, kWaitLimitNs, 38));
         if (!ok) break;
         fence_proxy_async_smem();
         __syncwarp();
@@ -682,10 +663,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = smem_desc(sRa + s0 * 8192 + ks * 2048, 8192, 1024, kSwizzle128B);
+          const uint64_t bd =
+              smem_desc(sRa + static_cast<uint32_t>(gsl * gsz) * 8192u + ks * 2048, 8192, 1024,
+                        kSwizzle128B);
           mma_bf16_ts(tO, tS + (i & 1) * 64 + ks * 8, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
         }
-        for (int e = 0; e < n_own; ++e) mma_commit(smem_u32(&sm->empty[s0 + e]));
+        mma_commit(smem_u32(&sm->empty[gsl]));
         mma_commit(smem_u32(&sm->pv_done));
         mma_commit(smem_u32(&sm->s_free[i & 1]));
       }

@@ -99,6 +99,7 @@ struct AttnArgs {
   int kind, B, T, H, D, r;
   int64_t N_rows;               // rows per sequence of kv (N_cap or L_cap)
   int64_t N_h;                  // fused: HCA entries per sequence (second tensor map)
+  int segments;                 // fused: bit 0 CSA, bit 1 HCA, bit 2 SWA keys
   int k, m, W;                  // fused: W keys per query in the SWA key buffer [B][T][W][D]
   float eps, scale;             // eps: SWA key norm
   RopeCoef rope;                // SWA key RoPE

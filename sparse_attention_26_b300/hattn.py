@@ -52,11 +52,13 @@ _SIGS = {
     "hattn_swa_keys": (_i32, [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _f32, _f32, _vp,
                               _vp]),
     "hattn_hybrid_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i32,
-                                 _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32, _vp, _vp,
-                                 _vp, _sz, _vp]),
+                                 _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32, _i32, _i32,
+                                 _vp, _vp, _vp, _sz, _vp]),
     "hattn_hybrid_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
-                                                _i32]),
-    "hattn_hybrid_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64, _i32]),
+                                                _i32, _i32, _i32]),
+    "hattn_hybrid_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _i32]),
+    "hattn_indexer_scores_sms": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
+                                        _i32, _vp, _vp]),
     "hattn_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64]),
     "hattn_lse_merge_splits": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i32),
                                       _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
@@ -220,9 +222,10 @@ def indexer_topk_noalloc(iq, w, ik_c, pos, *, k, m=4, idx_out=None, stream=None)
     return idx_out
 
 
-def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, stream=None):
+def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, stream=None):
     """Lightning-indexer scores only; returns score_out [B, T, N_cap] fp32
-    (entries beyond each query's visible count are left untouched)."""
+    (entries beyond each query's visible count are left untouched).  n_sms:
+    run the persistent score kernel on at most that many SMs (0 = all)."""
     _need(iq, "iq", torch.bfloat16, 4)
     _need(w, "w", torch.float32, 3)
     _need(ik_c, "ik_c", torch.bfloat16, 3)
@@ -232,8 +235,13 @@ def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, stream=None):
     if score_out is None:
         score_out = torch.empty((B, T, N_cap), dtype=torch.float32, device=iq.device)
     _need(score_out, "score_out", torch.float32)
-    _check(lib().hattn_indexer_scores(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
-                                      N_cap, m, _ptr(score_out), _stream(stream)))
+    if n_sms:
+        _check(lib().hattn_indexer_scores_sms(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI,
+                                              dI, N_cap, m, n_sms, _ptr(score_out),
+                                              _stream(stream)))
+    else:
+        _check(lib().hattn_indexer_scores(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
+                                          N_cap, m, _ptr(score_out), _stream(stream)))
     return score_out
 
 
@@ -393,44 +401,59 @@ def swa_keys(kv_raw, pos, *, r, W=128, gamma_kv=None, rope_base=10000.0, eps=1e-
     return kv_w
 
 
-def hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, q_prepped=False, partials=False):
-    return lib().hattn_hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, int(bool(q_prepped)),
-                                                   int(bool(partials)))
+SEG_CSA, SEG_HCA, SEG_SWA, SEG_ALL = 1, 2, 4, 7
 
 
-def hybrid_attn_splits(B, T, H, D, k, N_h, W):
-    return lib().hattn_hybrid_attn_splits(B, T, H, D, k, N_h, W)
+def hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, q_prepped=False, partials=False,
+                                segments=SEG_ALL, n_sms=0):
+    return lib().hattn_hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, segments, n_sms,
+                                                   int(bool(q_prepped)), int(bool(partials)))
 
 
-def hybrid_attn(q, kv_c, idx, kv_h, kv_w, pos, *, r, m=128, gamma_q=None, rope_base=10000.0,
-                eps=1e-6, scale=None, o=None, lse=None, workspace=None, q_prepped=False,
-                partials=False, stream=None):
+def hybrid_attn_splits(B, T, H, D, k, N_h, W, segments=SEG_ALL, n_sms=0):
+    return lib().hattn_hybrid_attn_splits(B, T, H, D, k, N_h, W, segments, n_sms)
+
+
+def hybrid_attn(q, kv_c, idx, kv_h, kv_w, pos, *, r, m=128, k=None, W=None, gamma_q=None,
+                rope_base=10000.0, eps=1e-6, scale=None, o=None, lse=None, workspace=None,
+                q_prepped=False, partials=False, segments=SEG_ALL, n_sms=0, stream=None):
     """CSA (selected entries), HCA (visible entries) and SWA (kv_w from
     swa_keys) keys of each query under one softmax; returns (o fp32, lse
-    fp32) or, with partials=True, a Partials view of the workspace."""
+    fp32) or, with partials=True, a Partials view of the workspace.
+    segments: the key sets covered (SEG_* mask; tensors of the others may be
+    None); n_sms: the SM share the split plan assumes (0 = all)."""
     _need(q, "q", torch.bfloat16, 4)
-    _need(kv_c, "kv_c", torch.bfloat16, 3)
-    _need(idx, "idx", torch.int32, 3)
-    _need(kv_h, "kv_h", torch.bfloat16, 3)
-    _need(kv_w, "kv_w", torch.bfloat16, 4)
     _need(pos, "pos", torch.int32, 2)
     _opt(gamma_q, "gamma_q", torch.float32)
     B, T, H, D = q.shape
-    k, N_h, W = idx.shape[2], kv_h.shape[1], kv_w.shape[2]
+    if segments & SEG_CSA:
+        _need(kv_c, "kv_c", torch.bfloat16, 3)
+        _need(idx, "idx", torch.int32, 3)
+    if segments & SEG_HCA:
+        _need(kv_h, "kv_h", torch.bfloat16, 3)
+    if segments & SEG_SWA:
+        _need(kv_w, "kv_w", torch.bfloat16, 4)
+    k = idx.shape[2] if idx is not None else (k or 1)
+    N_h = kv_h.shape[1] if kv_h is not None else 1
+    N_c = kv_c.shape[1] if kv_c is not None else 1
+    W = kv_w.shape[2] if kv_w is not None else (W or 1)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     if not partials:
         o, lse = _attn_out(q, o, lse)
-    need = hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, q_prepped, partials)
+    need = hybrid_attn_workspace_bytes(B, T, H, D, k, N_h, W, q_prepped, partials, segments,
+                                       n_sms)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().hattn_hybrid_attn(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_c),
-                                   _ptr(idx), kv_c.shape[1], k, _ptr(kv_h), N_h, m, _ptr(kv_w),
-                                   W, _ptr(pos), B, T, H, D, r, rope_base, eps, scale, _ptr(o),
-                                   _ptr(lse), _ptr(workspace), wsb, _stream(stream)))
+                                   _ptr(idx), N_c, k, _ptr(kv_h), N_h, m, _ptr(kv_w), W,
+                                   _ptr(pos), B, T, H, D, r, rope_base, eps, scale, segments,
+                                   n_sms, _ptr(o), _ptr(lse), _ptr(workspace), wsb,
+                                   _stream(stream)))
     if not partials:
         return o, lse
-    return Partials(workspace, q_prepped, B, T, H, D, hybrid_attn_splits(B, T, H, D, k, N_h, W))
+    return Partials(workspace, q_prepped, B, T, H, D,
+                    hybrid_attn_splits(B, T, H, D, k, N_h, W, segments, n_sms))
 
 
 # ------------------------------------------------------------------ merge

@@ -43,6 +43,7 @@ class HybridLayer:
         self.kv_c = torch.zeros((B, n_c, D), dtype=bf, device=device)
         self.ik_c = torch.zeros((B, n_c, wl.dI), dtype=bf, device=device)
         self.kv_h = torch.zeros((B, n_h, D), dtype=bf, device=device)
+        self.override_dense_sms = 0  # > 0: HCA + SWA attention on that many SMs beside the indexer
         if build_caches:
             self.build_caches()
         self._bufs = {}
@@ -76,9 +77,14 @@ class HybridLayer:
         b["qt"] = torch.empty((B, T, H, D), dtype=bf, device=dev)  # prepared queries
         if self.can_fuse(T):
             b["kv_w"] = torch.empty((B, T, wl.W, D), dtype=bf, device=dev)  # SWA keys
-            ws = hattn.hybrid_attn_workspace_bytes(B, T, H, D, wl.k, self.N_hca, wl.W,
-                                                   q_prepped=True, partials=True)
-            b["ws_fused"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+            for name, segs, n_sms in [("fused", hattn.SEG_ALL, 0),
+                                      ("dense", hattn.SEG_HCA | hattn.SEG_SWA,
+                                       self.override_dense_sms),
+                                      ("sparse", hattn.SEG_CSA, 0)]:
+                ws = hattn.hybrid_attn_workspace_bytes(B, T, H, D, wl.k, self.N_hca, wl.W,
+                                                       q_prepped=True, partials=True,
+                                                       segments=segs, n_sms=n_sms)
+                b["ws_" + name] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         for name, kind, nk in self._branch_kinds():
             b["o_" + name] = torch.empty((B, T, H, D), dtype=torch.float32, device=dev)
             b["l_" + name] = torch.empty((B, T, H), dtype=torch.float32, device=dev)
@@ -88,6 +94,37 @@ class HybridLayer:
             b["ws_" + name] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         self._bufs[T] = b
         return b
+
+    # SMs of this GPU and a cost model of the two concurrent chains (B300,
+    # measured): a streamed 64-key tile of one output half costs ~2.25 us of
+    # one SM, plus ~24 us for the HCA compression, the window keys and the
+    # attention's own prologue/epilogue; the indexer streams at ~5.2 TB/s
+    # when it has the SMs for it (~40 GB/s each: capped at 100 SMs it took
+    # 138 us instead of 100), and top-k takes ~27 us.
+    NUM_SMS = 148
+    TILE_US, DENSE_FIXED_US, TOPK_US = 2.25, 24.0, 27.0
+    IDX_BW, IDX_SM_BW = 5.2e12, 40e9
+
+    def dense_sms(self, T):
+        """A suggestion for override_dense_sms: the SMs to give the HCA + SWA
+        attention while the indexer (on the rest) and top-k run, from the
+        cost model -- the split that makes the two chains end together."""
+        wl, B = self.wl, self.B
+        # the attention's CTAs: nsplit key splits x 2 output halves x B*T queries
+        per_split = 2 * B * T
+        tiles = (self.N_hca + 63) // 64 + (wl.W + 63) // 64  # per query
+        idx_bytes = B * T * (self.N_csa * (wl.dI * 2 + 4))
+        best, best_t = per_split, None
+        nsplit = 1
+        while nsplit * per_split <= self.NUM_SMS - 32:
+            x = nsplit * per_split
+            dense = self.DENSE_FIXED_US + -(-tiles // nsplit) * self.TILE_US
+            idx = idx_bytes / min(self.IDX_BW, (self.NUM_SMS - x) * self.IDX_SM_BW) * 1e6
+            t = max(dense, idx + self.TOPK_US)
+            if best_t is None or t < best_t:
+                best, best_t = x, t
+            nsplit += 1
+        return best
 
     def can_fuse(self, T):
         """The fused attention serves layers with all three branches, one query
@@ -212,6 +249,11 @@ class HybridLayer:
         return b["out"], b["lse"]
 
     def _step_fused(self, q, iq, w, pos, sink, t_new, events, side_stream):
+        """Fused step.  Without a side stream: one attention over all three key
+        sets after top-k.  With one: the HCA + SWA key sets need no top-k, so
+        their attention runs on the side stream on dense_sms() SMs while the
+        indexer runs on the others; the CSA key set follows top-k, and one
+        merge weighs the partials of both."""
         wl, r = self.wl, self.raw
         T = q.shape[1]
         b = self.buffers(T)
@@ -235,54 +277,83 @@ class HybridLayer:
                 hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=j, j_end=j + 1,
                                    m=m, kv_h=self.kv_h)
 
-        def side_work():
-            compress("hca")
-            ev("swa_keys", 0)
-            hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
-            ev("swa_keys", 1)
+        def attn(name, segments, n_sms):
+            ev("attn_" + name, 0)
+            part = hattn.hybrid_attn(b["qt"], self.kv_c, b["idx"], self.kv_h, b["kv_w"], pos,
+                                     r=wl.r, m=wl.m_hca, workspace=b["ws_" + name],
+                                     q_prepped=True, partials=True, segments=segments,
+                                     n_sms=n_sms)
+            ev("attn_" + name, 1)
+            return part
 
         ev("compress", 0)
         compress("csa")
         if side_stream is None:
-            side_work()
+            compress("hca")
         ev("compress", 1)
-        joined = None
-        if side_stream is not None:
-            side_stream.wait_stream(main)
-            with torch.cuda.stream(side_stream):
-                side_work()
-            joined = side_stream
         ev("qprep", 0)
         hattn.query_prep(q, pos, r=wl.r, q_out=b["qt"])
         ev("qprep", 1)
+        # Running the HCA + SWA key sets beside the indexer only pays when the
+        # indexer still reaches full HBM bandwidth on the SMs left to it; on
+        # B300 it needs all of them (capped at 100 SMs it runs ~40% longer),
+        # so the split is opt-in (override_dense_sms) and the default runs the
+        # three key sets as one attention after top-k.
+        n_dense = self.override_dense_sms if side_stream is not None else 0
+        overlap = n_dense > 0
+        if side_stream is not None and overlap:
+            side_stream.wait_stream(main)
+            with torch.cuda.stream(side_stream):
+                compress("hca")
+                ev("swa_keys", 0)
+                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
+                ev("swa_keys", 1)
+                dense = attn("dense", hattn.SEG_HCA | hattn.SEG_SWA, n_dense)
+        elif side_stream is not None:
+            # the HCA compression and the window keys beside the indexer
+            side_stream.wait_stream(main)
+            with torch.cuda.stream(side_stream):
+                compress("hca")
+                ev("swa_keys", 0)
+                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
+                ev("swa_keys", 1)
+        else:
+            ev("swa_keys", 0)
+            hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
+            ev("swa_keys", 1)
         ev("indexer", 0)
-        hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=b["scores"])
+        hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=b["scores"],
+                             n_sms=(self.NUM_SMS - n_dense) if n_dense else 0)
         ev("indexer", 1)
         ev("topk", 0)
         hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
         ev("topk", 1)
-        if joined is not None:
-            main.wait_stream(joined)
-        ev("attn", 0)
-        part = hattn.hybrid_attn(b["qt"], self.kv_c, b["idx"], self.kv_h, b["kv_w"], pos, r=wl.r,
-                                 m=wl.m_hca, workspace=b["ws_fused"], q_prepped=True,
-                                 partials=True)
-        ev("attn", 1)
+        if overlap:
+            parts = [attn("sparse", hattn.SEG_CSA, 0)]
+            main.wait_stream(side_stream)
+            parts.append(dense)
+        else:
+            if side_stream is not None:
+                main.wait_stream(side_stream)
+            parts = [attn("fused", hattn.SEG_ALL, 0)]
         ev("merge", 0)
-        hattn.lse_merge_splits([part], pos, r=wl.r, H=wl.H, sink=sink, out=b["out"],
+        hattn.lse_merge_splits(parts, pos, r=wl.r, H=wl.H, sink=sink, out=b["out"],
                                lse_out=b["lse"])
         ev("merge", 1)
         return b["out"], b["lse"]
 
-    def event_names(self, T, branch_outputs=False, fused=None):
+    def event_names(self, T, branch_outputs=False, fused=None, side_stream=True):
         """The call spans step() records when given events of these names."""
         if fused is None:
             fused = self.can_fuse(T) and not branch_outputs
         if fused:
-            return ["compress", "swa_keys", "qprep", "indexer", "topk", "attn", "merge"]
+            split = side_stream and self.override_dense_sms > 0
+            attn = ["attn_dense", "attn_sparse"] if split else ["attn_fused"]
+            return ["compress", "swa_keys", "qprep", "indexer", "topk"] + attn + ["merge"]
         return ["compress", "qprep", "indexer", "topk", "sparse", "hca", "swa", "merge"]
 
-    def launches_per_step(self, T, t_new=None, branch_outputs=False, fused=None):
+    def launches_per_step(self, T, t_new=None, branch_outputs=False, fused=None,
+                          side_stream=False):
         """Kernels one step launches: the query preparation, each branch's
         attention kernel (plus its combine with split-KV when branch outputs
         are formed), the indexer and top-k of CSA, the merge, and the
@@ -295,7 +366,9 @@ class HybridLayer:
         if fused is None:
             fused = self.can_fuse(T) and not branch_outputs
         if fused:
-            return n + 4  # SWA keys, indexer scores, top-k, fused attention
+            # SWA keys, indexer scores, top-k, and the attention: one call, or
+            # the dense and the sparse key sets when a side stream is used
+            return n + 4 + int(side_stream and self.override_dense_sms > 0)
         for name, kind, nk in self._branch_kinds():
             n += 1 + int(branch_outputs and hattn.attn_splits(kind, B, T, H, D, nk) > 1)
             if name == "csa":

@@ -171,9 +171,10 @@ def test_merge_splits_validation(L):
 def test_fused_attention_validation_and_sizes(L):
     N = None
     # hattn_hybrid_attn(q, gamma_q, q_prepped, kv_c, idx, N_c, k, kv_h, N_h, m, kv_w, W, pos,
-    #                   B, T, H, D, r, rope_base, eps, scale, o, lse, ws, ws_bytes, stream)
+    #                   B, T, H, D, r, rope_base, eps, scale, segments, n_sms, o, lse, ws,
+    #                   ws_bytes, stream)
     args = [FAKE, N, 1, FAKE, FAKE, 1000, 64, FAKE, 100, 128, FAKE, 128, FAKE,
-            2, 1, 128, 512, 64, 1e4, 1e-6, 0.04, FAKE, FAKE, FAKE, 1 << 30, N]
+            2, 1, 128, 512, 64, 1e4, 1e-6, 0.04, 7, 0, FAKE, FAKE, FAKE, 1 << 30, N]
     bad = list(args)
     bad[10] = N  # no SWA key buffer
     assert L.hattn_hybrid_attn(*bad) == hattn.INVALID_ARG and "kv_w" in _err(L)
@@ -183,6 +184,19 @@ def test_fused_attention_validation_and_sizes(L):
     bad = list(args)
     bad[4] = N  # no top-k indices
     assert L.hattn_hybrid_attn(*bad) == hattn.INVALID_ARG and "idx" in _err(L)
+    bad = list(args)
+    bad[21] = 8  # not a segment mask
+    assert L.hattn_hybrid_attn(*bad) == hattn.INVALID_ARG and "segments" in _err(L)
+    # without the CSA segment the top-k indices and the CSA cache are not
+    # needed: validation gets as far as the (too small) workspace, so nothing
+    # is ever launched on these fake pointers
+    ok_args = list(args)
+    ok_args[3], ok_args[4], ok_args[21], ok_args[23], ok_args[24] = N, N, 6, N, N
+    ok_args[26] = 16
+    assert L.hattn_hybrid_attn(*ok_args) == hattn.INVALID_ARG and "workspace" in _err(L)
+    # a smaller SM share plans fewer splits
+    assert (hattn.hybrid_attn_splits(8, 1, 128, 512, 1024, 8192, 128, segments=6, n_sms=48)
+            < hattn.hybrid_attn_splits(8, 1, 128, 512, 1024, 8192, 128, segments=6))
     # the fused call splits its keys like the branches and keeps partials per split
     n = hattn.hybrid_attn_splits(8, 1, 128, 512, 1024, 8192, 128)
     assert n > 1

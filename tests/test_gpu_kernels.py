@@ -415,6 +415,13 @@ def test_hybrid_attn(B, T, H, D, r, N_hca, k, N_c, L, pos_list):
     part = hattn.hybrid_attn(qt, kv_c.to(DEV), idx.to(DEV), kvh_dev, kv_w, d["pos"], r=r,
                              q_prepped=True, partials=True)
     out2, lse2 = hattn.lse_merge_splits([part], d["pos"], r=r, H=H, sink=sink.to(DEV))
+    # the key sets in two calls (as the layer runs them beside the indexer):
+    # HCA + SWA planned for a share of the SMs, then CSA; one merge of both
+    dense = hattn.hybrid_attn(qt, None, None, kvh_dev, kv_w, d["pos"], r=r, k=k, q_prepped=True,
+                              partials=True, segments=hattn.SEG_HCA | hattn.SEG_SWA, n_sms=40)
+    sparse = hattn.hybrid_attn(qt, kv_c.to(DEV), idx.to(DEV), None, None, d["pos"], r=r, W=128,
+                               q_prepped=True, partials=True, segments=hattn.SEG_CSA)
+    out3, lse3 = hattn.lse_merge_splits([dense, sparse], d["pos"], r=r, H=H, sink=sink.to(DEV))
     hattn.check_status()
     qb, pn = bits(q), pos.numpy()
     ro = [orc.attention(orc.KIND_SPARSE, qb, bits(kv_c), pn, idx=idx.numpy(), r=r),
@@ -423,6 +430,7 @@ def test_hybrid_attn(B, T, H, D, r, N_hca, k, N_c, L, pos_list):
     ref, rl = orc.merge([x[0] for x in ro], [x[1] for x in ro], sink.numpy(), pn, r)
     check_attn(out, lse, ref, rl, "fused, direct output")
     check_attn(out2, lse2, ref, rl, "fused, split partials")
+    check_attn(out3, lse3, ref, rl, "fused, key sets in two calls")
 
 
 def test_hybrid_attn_bad_index_is_reported():

@@ -110,8 +110,8 @@ def indexer_bytes(wl):
 # was taken on, checked by hash, else the bench reports traffic as null.
 INDEXER_TRAFFIC = {
     "bytes_per_entry": 138.264e6 / (8 * 65536),
-    "sources": ["indexer.cu", "common.cuh", "kernels.h"],
-    "sha256": "42b1f38de5468c2c5fd17252330fefd189360ed14e2f02a1eb6006e9687a9b77",
+    "sources": ["indexer.cu", "common.cuh"],
+    "sha256": "1a16f370bc82cf9a05017b7e286821c373be1e3659184d5712480b252298fec1",
     "profile": "profiles/indexer_score_kernel_decode_8x65536.md",
 }
 
@@ -468,33 +468,82 @@ def run_ours(args, world, rank, local):
 
 
 def run_e2e(args, world, layer, inp, wl, t_new, stream, side):
+    """The same steps with every step's inputs coming from pinned host memory
+    and its result going back, inside the timed region.  A step's inputs (q,
+    iq, w, pos and the new token's raw KV, indexer key and gate logits) are
+    packed in one pinned buffer and moved by one host-to-device copy; the
+    token rows are then placed in the caches on the device, and out and lse
+    (adjacent in one device buffer) come back by one device-to-host copy.
+    Inputs and results are double-buffered so these copies overlap the
+    compute of the neighbouring steps, as a serving loop would run them."""
     import torch
     K = args.steps
     dev = inp["q"].device
-    host = {k: inp[k].cpu().pin_memory() for k in ["q", "iq", "w", "pos"]}
-    tok = {"kv": inp["kv_raw"][:, t_new].cpu().pin_memory(),
-           "ik": inp["ik_raw"][:, t_new].cpu().pin_memory(),
-           "gc": inp["gate_csa"][:, t_new].cpu().pin_memory(),
-           "gh": inp["gate_hca"][:, t_new].cpu().pin_memory()}
-    dq = {k: torch.empty_like(inp[k]) for k in host}
-    out_h = torch.empty(inp["q"].shape, dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty(inp["q"].shape[:3], dtype=torch.float32).pin_memory()
     raw = layer.raw
+    parts = [("q", inp["q"]), ("iq", inp["iq"]), ("w", inp["w"]), ("pos", inp["pos"]),
+             ("kv", inp["kv_raw"][:, t_new]), ("ik", inp["ik_raw"][:, t_new]),
+             ("gc", inp["gate_csa"][:, t_new]), ("gh", inp["gate_hca"][:, t_new])]
+    offs, total = {}, 0
+    for name, t in parts:
+        nbytes = t.numel() * t.element_size()
+        offs[name] = (total, nbytes, t.dtype, tuple(t.shape))
+        total += (nbytes + 255) // 256 * 256
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for name, t in parts:
+        o, n, _, _ = offs[name]
+        host[o:o + n].copy_(t.contiguous().view(torch.uint8).reshape(-1).cpu())
+    # two device copies of the inputs and of the result, so that the copies
+    # of one step overlap the compute of its neighbours (a copy stream moves
+    # step i+1's inputs in and step i-1's result out while step i runs)
+    dbufs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def view(buf, name):
+        o, n, dt, shape = offs[name]
+        return buf[o:o + n].view(dt).view(shape)
+
+    res = layer.result_buffer(wl.T)  # out and lse, adjacent
+    stage = [torch.empty(res.numel(), dtype=torch.uint8, device=dev) for _ in range(2)]
+    out_h = [torch.empty(res.numel(), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    copy = torch.cuda.Stream(device=dev)
+    mk = lambda: torch.cuda.Event(external=True)  # noqa: E731
+    in_ready = [mk() for _ in range(K)]
+    done = [mk() for _ in range(K)]
+    out_done = [mk() for _ in range(K)]
     ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
         ev[0].record()
-        for _ in range(K):
-            for k in host:
-                dq[k].copy_(host[k], non_blocking=True)
-            raw["kv_raw"][:, t_new].copy_(tok["kv"], non_blocking=True)
-            raw["ik_raw"][:, t_new].copy_(tok["ik"], non_blocking=True)
-            raw["gate_csa"][:, t_new].copy_(tok["gc"], non_blocking=True)
-            raw["gate_hca"][:, t_new].copy_(tok["gh"], non_blocking=True)
-            out, lse = layer.step(dq["q"], dq["iq"], dq["w"], dq["pos"], inp["sink"], t_new=t_new,
-                                  side_stream=side)
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+        copy.wait_stream(stream)
+
+        def fetch(i):  # on the copy stream: step i's inputs into buffer i % 2
+            with torch.cuda.stream(copy):
+                if i >= 2:
+                    copy.wait_event(done[i - 2])  # step i-2 has finished reading that buffer
+                dbufs[i % 2].copy_(host, non_blocking=True)
+                in_ready[i].record(copy)
+
+        fetch(0)
+        if K > 1:
+            fetch(1)
+        for i in range(K):
+            buf, st = dbufs[i % 2], stage[i % 2]
+            stream.wait_event(in_ready[i])
+            for name, cache in [("kv", "kv_raw"), ("ik", "ik_raw"), ("gc", "gate_csa"),
+                                ("gh", "gate_hca")]:
+                raw[cache][:, t_new].copy_(view(buf, name))
+            layer.step(view(buf, "q"), view(buf, "iq"), view(buf, "w"), view(buf, "pos"),
+                       inp["sink"], t_new=t_new, side_stream=side)
+            if i >= 2:
+                stream.wait_event(out_done[i - 2])  # that result copy has left the stage buffer
+            st.copy_(res)
+            done[i].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done[i])
+                out_h[i % 2].copy_(st, non_blocking=True)
+                out_done[i].record(copy)
+            if i + 2 < K:
+                fetch(i + 2)
+        stream.wait_stream(copy)
         ev[1].record()
     torch.cuda.synchronize()
     g.replay()
@@ -505,11 +554,14 @@ def run_e2e(args, world, layer, inp, wl, t_new, stream, side):
     torch.cuda.synchronize()
     barrier(world)
     e2e_value, ms = job_throughput(world, wl.B * wl.T * K, ev[0].elapsed_time(ev[1]))
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + sum(
-        t.numel() * t.element_size() for t in tok.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-    return {"value": e2e_value, "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / K}
+    h2d = sum(n for _, n, _, _ in offs.values())
+    out, lse = layer.buffers(wl.T)["out"], layer.buffers(wl.T)["lse"]
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    return {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / K,
+            "copies_per_step": {"h2d": 1, "d2h": 1, "d2d_token_rows": 4, "d2d_result": 1},
+            "overlap": "double-buffered: step i+1's inputs and step i-1's result move on a "
+                       "copy stream while step i computes"}
 
 
 def main():

@@ -74,6 +74,26 @@ __global__ void __launch_bounds__(kCompressThreads)
     const int64_t j = a.j_begin + item % nj;
     const int64_t u0 = static_cast<int64_t>(a.m) * (j + 1) - a.w;
 
+    // A window that one pass of the token loop covers (CSA: 8 tokens) has
+    // its token rows requested before the gate softmax, so the two global
+    // round trips overlap.
+    const bool one_pass = a.w <= 8 * S;
+    const int c_pre = tid % NC, s_pre = tid / NC;
+    uint4 pre[8];
+    if (one_pass && tid < S * NC) {
+      const __nv_bfloat16* src = c_pre < NCk
+          ? a.kv_raw + (int64_t)b * a.L_cap * a.D + c_pre * 8
+          : a.ik_raw + (int64_t)b * a.L_cap * a.dI + (c_pre - NCk) * 8;
+      const int64_t stride = c_pre < NCk ? a.D : a.dI;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = s_pre + q * S;
+        const int64_t u = u0 + i;
+        pre[q] = (i < a.w && u >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + u * stride))
+                                     : make_uint4(0, 0, 0, 0);
+      }
+    }
+
     // gate softmax over the tokens that exist (warp 0)
     if (tid < 32) {
       float gmax = -INFINITY;
@@ -118,8 +138,11 @@ __global__ void __launch_bounds__(kCompressThreads)
           const int i = i0 + q * S;
           const int64_t u = u0 + i;
           const bool live = i < a.w && u >= 0;
-          v[q] = live ? __ldg(reinterpret_cast<const uint4*>(src + u * stride))
-                      : make_uint4(0, 0, 0, 0);
+          if (one_pass)
+            v[q] = pre[q];  // requested before the softmax (zero where not live)
+          else
+            v[q] = live ? __ldg(reinterpret_cast<const uint4*>(src + u * stride))
+                        : make_uint4(0, 0, 0, 0);
           al[q] = live ? alpha[i] : 0.f;
         }
 #pragma unroll

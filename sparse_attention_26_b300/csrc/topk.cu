@@ -31,6 +31,11 @@ namespace hattn {
 namespace {
 
 constexpr int kBins = 2048;
+// Keys in the first pass's threshold bin, whole cluster, up to which the
+// compact path is taken; keys above that bin number fewer than k <= 2048.
+// Slice positions fit 16 bits (a slice holds at most 49,152 keys).
+constexpr int kMaxCand = 2048;
+constexpr int kMaxAbove = 2048;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);  // -0 and +0 compare equal
@@ -45,6 +50,9 @@ struct TopkShared {
   int offs[2];         // the same counts summed over the lower-ranked CTAs
   int ctr, ctr_eq;
   int eq_total;        // keys equal to the threshold in the whole cluster
+  int n_cand, n_above;
+  uint16_t cand[kMaxCand];        // slice positions of the keys in the bin of the k-th largest
+  uint16_t above_idx[kMaxAbove];  // slice positions of the keys above that bin
   uint32_t digit;
   uint32_t above;
 };
@@ -131,29 +139,31 @@ __global__ void topk_kernel(const TopkArgs a) {
   }
 
   const float* src = a.scores + static_cast<int64_t>(row) * a.N_cap + start;
-  for (int e = tid; e < len; e += nthr) keys[e] = order_key(src[e]);
   for (int i = tid; i < kBins; i += nthr) {
     sh->hist[i] = 0;
     sh->ghist[0][i] = 0;
     sh->ghist[1][i] = 0;
   }
+  __syncthreads();
+  // the keys, and the first pass's histogram of their top 11 bits, in one sweep
+  for (int e = tid; e < len; e += nthr) {
+    const uint32_t key = order_key(src[e]);
+    keys[e] = key;
+    atomicAdd(&sh->hist[key >> 21], 1u);
+  }
   cluster.sync();  // every copy of the cluster histogram is zero before any add
 
   uint32_t prefix = 0;
   uint32_t need = static_cast<uint32_t>(a.k);
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = shifts[pass];
-    const int nb = 1 << widths[pass];
+  // One radix pass over the histogram in sh->hist: add this CTA's nonzero
+  // bins into every CTA's copy of the cluster histogram (buffer pass & 1),
+  // reset the local bins and the other buffer (last scanned by this CTA in
+  // the previous pass; the next adds into it come after the barrier), then
+  // find the digit of the need-th largest key.
+  auto radix_pass = [&](int pass, int width) {
+    const int nb = 1 << width;
     const int buf = pass & 1;
-    for (int e = tid; e < len; e += nthr) {
-      const uint32_t key = keys[e];
-      if (pass == 0 || (key >> (shift + widths[pass])) == prefix)
-        atomicAdd(&sh->hist[(key >> shift) & (nb - 1)], 1u);
-    }
     __syncthreads();
-    // add this CTA's nonzero bins into every CTA's copy; reset the local bins
     for (int bin = tid; bin < nb; bin += nthr) {
       const uint32_t v = sh->hist[bin];
       if (v) {
@@ -161,14 +171,58 @@ __global__ void topk_kernel(const TopkArgs a) {
         sh->hist[bin] = 0;
       }
     }
-    // the other copy was last scanned by this CTA in the previous pass; the
-    // next adds into it come after the cluster barrier below
     if (pass < 2)
       for (int i = tid; i < kBins; i += nthr) sh->ghist[buf ^ 1][i] = 0;
     cluster.sync();
     find_digit(sh->ghist[buf], nb, need, sh, tid, nthr);
-    prefix = (prefix << widths[pass]) | sh->digit;
+    prefix = (prefix << width) | sh->digit;
     need -= sh->above;
+  };
+  radix_pass(0, 11);  // its histogram was built while loading
+  // The keys left to rank are those in the bin of the k-th largest (about
+  // 0.5% of normal scores).  When the whole cluster holds few enough, one
+  // sweep lists them (and the keys above the bin, which are selected), and
+  // the remaining passes, the counts and the writes visit only the lists.
+  // The decision uses the cluster histogram, so every CTA takes the same path.
+  const bool compact = sh->ghist[0][prefix] <= static_cast<uint32_t>(kMaxCand);
+  int n_cand = 0, n_above = 0;
+  if (compact) {
+    if (tid == 0) {
+      sh->n_cand = 0;
+      sh->n_above = 0;
+    }
+    __syncthreads();
+    // few keys qualify, so each takes its place with its own atomic
+    for (int e = tid; e < len; e += nthr) {
+      const uint32_t key = keys[e];
+      const uint32_t d = key >> 21;
+      if (d == prefix) {
+        sh->cand[atomicAdd(&sh->n_cand, 1)] = static_cast<uint16_t>(e);
+        atomicAdd(&sh->hist[(key >> 10) & 2047u], 1u);
+      } else if (d > prefix) {
+        sh->above_idx[atomicAdd(&sh->n_above, 1)] = static_cast<uint16_t>(e);
+      }
+    }
+    __syncthreads();
+    n_cand = sh->n_cand;
+    n_above = sh->n_above;
+    radix_pass(1, 11);
+    for (int c = tid; c < n_cand; c += nthr) {
+      const uint32_t key = keys[sh->cand[c]];
+      if ((key >> 10) == prefix) atomicAdd(&sh->hist[key & 1023u], 1u);
+    }
+    radix_pass(2, 10);
+  } else {
+    for (int e = tid; e < len; e += nthr) {
+      const uint32_t key = keys[e];
+      if ((key >> 21) == prefix) atomicAdd(&sh->hist[(key >> 10) & 2047u], 1u);
+    }
+    radix_pass(1, 11);
+    for (int e = tid; e < len; e += nthr) {
+      const uint32_t key = keys[e];
+      if ((key >> 10) == prefix) atomicAdd(&sh->hist[key & 1023u], 1u);
+    }
+    radix_pass(2, 10);
   }
   const uint32_t thr = prefix;  // the k-th largest key; take `need` of its ties
 
@@ -180,9 +234,18 @@ __global__ void topk_kernel(const TopkArgs a) {
   }
   __syncthreads();
   int gt = 0, eq = 0;
-  for (int e = tid; e < len; e += nthr) {
-    gt += keys[e] > thr;
-    eq += keys[e] == thr;
+  if (compact) {
+    if (tid == 0) gt = n_above;
+    for (int c = tid; c < n_cand; c += nthr) {
+      const uint32_t key = keys[sh->cand[c]];
+      gt += key > thr;
+      eq += key == thr;
+    }
+  } else {
+    for (int e = tid; e < len; e += nthr) {
+      gt += keys[e] > thr;
+      eq += keys[e] == thr;
+    }
   }
   if (gt) atomicAdd(&sh->counts[0], gt);
   if (eq) atomicAdd(&sh->counts[1], eq);
@@ -215,7 +278,26 @@ __global__ void topk_kernel(const TopkArgs a) {
   const int off_gt = sh->offs[0];
   const int off_eq = sh->offs[1];
   const int base = a.k - static_cast<int>(need);  // ties go to [base, k)
-  if (sh->eq_total == static_cast<int>(need)) {
+  const bool all_ties = sh->eq_total == static_cast<int>(need);
+  if (compact) {
+    // keys above the threshold bin, then the candidates above or (when every
+    // tie is selected) at the threshold: any order
+    for (int c = tid; c < n_above; c += nthr) {
+      const int p = atomicAdd(&sh->ctr, 1);
+      out[off_gt + p] = static_cast<int32_t>(start + sh->above_idx[c]);
+    }
+    for (int c = tid; c < n_cand; c += nthr) {
+      const int e = sh->cand[c];
+      const uint32_t key = keys[e];
+      if (key > thr) {
+        const int p = atomicAdd(&sh->ctr, 1);
+        out[off_gt + p] = static_cast<int32_t>(start + e);
+      } else if (key == thr && all_ties) {
+        const int p = atomicAdd(&sh->ctr_eq, 1);
+        out[base + off_eq + p] = static_cast<int32_t>(start + e);
+      }
+    }
+  } else if (all_ties) {
     // every tie is selected (the usual case: one key holds the k-th score),
     // so no order is needed: keys above and at the threshold are appended
     for (int e = tid; e < len; e += nthr) {
@@ -236,6 +318,8 @@ __global__ void topk_kernel(const TopkArgs a) {
         out[off_gt + p] = static_cast<int32_t>(start + e);
       }
     }
+  }
+  if (!all_ties) {
     // more ties than places: the ties with the smaller indices win, so each
     // thread owns a contiguous run and ranks its ties by a block scan; the
     // count visits the run in a per-lane rotated order (no bank conflicts)
@@ -323,6 +407,9 @@ void fill_plan(int C, int64_t N_cap, TopkPlan* p) {
 }
 
 }  // namespace
+
+static_assert(sizeof(TopkShared) + 49152 * 4 <= 227 * 1024,
+              "a 49,152-key slice and the shared state fit one CTA's shared memory");
 
 bool plan_topk(int rows, int64_t N_cap, int num_sms, TopkPlan* p) {
   if (rows <= 0 || N_cap < 0) return false;

@@ -67,12 +67,16 @@ class HybridLayer:
         wl, B, D, dev = self.wl, self.B, self.D, self.dev
         H = wl.H
         bf = torch.bfloat16
+        # out and lse are adjacent in one buffer (one copy returns both)
+        n_out, n_lse = B * T * H * D * 2, B * T * H * 4
+        res = torch.empty(n_out + n_lse, dtype=torch.uint8, device=dev)
         b = dict(
             scores=torch.empty((B, T, self.N_csa if "csa" in wl.branches else 1),
                                dtype=torch.float32, device=dev),
             idx=torch.empty((B, T, wl.k), dtype=torch.int32, device=dev),
-            out=torch.empty((B, T, H, D), dtype=bf, device=dev),
-            lse=torch.empty((B, T, H), dtype=torch.float32, device=dev),
+            out=res[:n_out].view(bf).view(B, T, H, D),
+            lse=res[n_out:].view(torch.float32).view(B, T, H),
+            result=res,
         )
         b["qt"] = torch.empty((B, T, H, D), dtype=bf, device=dev)  # prepared queries
         if self.can_fuse(T):
@@ -125,6 +129,10 @@ class HybridLayer:
                 best, best_t = x, t
             nsplit += 1
         return best
+
+    def result_buffer(self, T):
+        """The one device buffer holding out (bf16) then lse (fp32) of step()."""
+        return self.buffers(T)["result"]
 
     def can_fuse(self, T):
         """The fused attention serves layers with all three branches, one query
@@ -286,14 +294,11 @@ class HybridLayer:
             ev("attn_" + name, 1)
             return part
 
-        ev("compress", 0)
-        compress("csa")
-        if side_stream is None:
-            compress("hca")
-        ev("compress", 1)
-        ev("qprep", 0)
-        hattn.query_prep(q, pos, r=wl.r, q_out=b["qt"])
-        ev("qprep", 1)
+        def qprep():
+            ev("qprep", 0)
+            hattn.query_prep(q, pos, r=wl.r, q_out=b["qt"])
+            ev("qprep", 1)
+
         # Running the HCA + SWA key sets beside the indexer only pays when the
         # indexer still reaches full HBM bandwidth on the SMs left to it; on
         # B300 it needs all of them (capped at 100 SMs it runs ~40% longer),
@@ -301,7 +306,24 @@ class HybridLayer:
         # three key sets as one attention after top-k.
         n_dense = self.override_dense_sms if side_stream is not None else 0
         overlap = n_dense > 0
+        if side_stream is not None and not overlap:
+            # the query preparation, the HCA compression and the window keys
+            # (needed only by the attention) run beside the CSA compression,
+            # the indexer and top-k
+            side_stream.wait_stream(main)
+            with torch.cuda.stream(side_stream):
+                qprep()
+                compress("hca")
+                ev("swa_keys", 0)
+                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
+                ev("swa_keys", 1)
+        ev("compress", 0)
+        compress("csa")
+        if side_stream is None:
+            compress("hca")
+        ev("compress", 1)
         if side_stream is not None and overlap:
+            qprep()
             side_stream.wait_stream(main)
             with torch.cuda.stream(side_stream):
                 compress("hca")
@@ -309,15 +331,8 @@ class HybridLayer:
                 hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
                 ev("swa_keys", 1)
                 dense = attn("dense", hattn.SEG_HCA | hattn.SEG_SWA, n_dense)
-        elif side_stream is not None:
-            # the HCA compression and the window keys beside the indexer
-            side_stream.wait_stream(main)
-            with torch.cuda.stream(side_stream):
-                compress("hca")
-                ev("swa_keys", 0)
-                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
-                ev("swa_keys", 1)
-        else:
+        elif side_stream is None:
+            qprep()
             ev("swa_keys", 0)
             hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
             ev("swa_keys", 1)

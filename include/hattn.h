@@ -311,6 +311,19 @@ HATTN_API int hattn_check_status(hattn_stream_t stream);
  * kernel then records HATTN_ERR_TIMEOUT and returns (no fault, no hang). */
 HATTN_API int hattn_selftest_wait_timeout(uint64_t timeout_ns, hattn_stream_t stream);
 /* Library version string. */
+/* Dependent launches (CUDA programmatic dependent launch).  While enabled on
+ * the calling host thread, the kernels of hattn_indexer_scores(_sms),
+ * hattn_topk_select, the attention calls and the merges are launched as
+ * programmatic dependents of the previous kernel in their stream: they may
+ * start (allocate tensor memory, initialise barriers, prefetch descriptors,
+ * load inputs the predecessor does not write) while that kernel finishes,
+ * and wait for it (griddepcontrol.wait) before reading anything it may
+ * write.  Every kernel of the library also lets its dependents start early.
+ * Use it only where the previous kernel in the stream is the call that
+ * produces the inputs (it relaxes only that one dependency).  Off by
+ * default; returns the previous setting. */
+HATTN_API int hattn_set_dependent_launch(int enable);
+
 HATTN_API const char* hattn_version(void);
 
 #ifdef __cplusplus

@@ -16,6 +16,7 @@ using namespace hattn;
 namespace {
 
 thread_local char g_last_error[512] = "";
+thread_local bool g_dependent_launch = false;
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -403,6 +404,15 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
 }  // namespace
 
 namespace hattn {
+
+bool dependent_launch() { return g_dependent_launch; }
+
+int add_dependent_attr(cudaLaunchAttribute* attrs, int n) {
+  if (!g_dependent_launch) return n;
+  attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[n].val.programmaticStreamSerializationAllowed = 1;
+  return n + 1;
+}
 
 void make_rope_coef(double base, int r, RopeCoef* rc) {
   memset(rc, 0, sizeof *rc);
@@ -856,6 +866,12 @@ int hattn_selftest_wait_timeout(uint64_t timeout_ns, hattn_stream_t stream) {
   cudaError_t e = launch_wait_selftest(timeout_ns, status, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
   return ok();
+}
+
+int hattn_set_dependent_launch(int enable) {
+  const int prev = g_dependent_launch ? 1 : 0;
+  g_dependent_launch = enable != 0;
+  return prev;
 }
 
 const char* hattn_version(void) { return "hattn 0.1 sm_103a"; }

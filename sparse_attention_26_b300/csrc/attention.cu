@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_trigger();  // the merge may begin launching as SMs free up
   const int dh = blockIdx.x % a.nds;
   const int split = blockIdx.x / a.nds;
   const int rb = blockIdx.y;
@@ -264,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (nt == 0) {
+    pdl_wait();
     // empty split: o = 0, lse = -inf
     for (int rI = threadIdx.x; rI < nrows; rI += kThreads) {
       const int g = rI / a.H, h = rI % a.H;
@@ -314,6 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // a dependent launch has overlapped the setup above with its predecessor;
+  // everything below may read what the predecessor wrote
+  pdl_wait();
   const uint32_t tmem = sm->tmem_base;
   volatile int* abort = &sm->abort;
   const uint32_t tS = tmem;          // columns [0, 128): two 64-column S/P buffers
@@ -944,8 +949,16 @@ cudaError_t launch_kind(const CUtensorMap& tm_kv, const CUtensorMap& tm_kv2,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(p.smem_bytes));
   if (e != cudaSuccess) return e;
-  dim3 grid(p.nds * p.nsplit, p.n_rb, a.B);
-  attn_kernel<KIND><<<grid, kThreads, p.smem_bytes, stream>>>(tm_kv, tm_kv2, tm_q, a, p.nslot);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nds * p.nsplit, p.n_rb, a.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  cfg.attrs = at;
+  cfg.numAttrs = add_dependent_attr(at, 0);
+  e = cudaLaunchKernelEx(&cfg, attn_kernel<KIND>, tm_kv, tm_kv2, tm_q, a, p.nslot);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

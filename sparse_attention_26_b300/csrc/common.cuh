@@ -91,6 +91,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// ----------------------------------------------------------------- dependent launch
+// A kernel launched as a programmatic dependent of the previous kernel in its
+// stream may start while that kernel still runs.  pdl_wait() blocks until the
+// predecessor has completed and its writes are visible (a no-op when the
+// kernel was launched normally); pdl_trigger() lets this kernel's own
+// dependent begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

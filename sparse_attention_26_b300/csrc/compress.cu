@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kCompressThreads)
   __shared__ float red[kCompressThreads / 32];
   __shared__ float inv_rms_s;
 
+  pdl_trigger();  // a dependent launch after this kernel may begin
   const int tid = threadIdx.x;
   const int NCk = a.D / 8;                 // KV pieces
   const int NCi = a.ik_raw ? a.dI / 8 : 0; // indexer-key pieces

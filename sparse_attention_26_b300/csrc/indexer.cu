@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_trigger();  // top-k may begin launching as SMs free up
 
   const int64_t s0 = a.total_slots * blockIdx.x / gridDim.x;
   const int64_t s1 = a.total_slots * (blockIdx.x + 1) / gridDim.x;
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       int st = 0;
       uint32_t ph = 0;
       int64_t it = 0, qloads = 0, loaded = -1;
+      bool keys_ready = false;  // the compressed keys of the previous kernel are visible
       for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
         if (!cur.live()) continue;
         if (cur.group != loaded) {
@@ -168,6 +170,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (it >= a.stages &&
             !mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 11))
           break;
+        if (!keys_ready) {
+          pdl_wait();  // a dependent launch waits here for the entries its predecessor writes
+          keys_ready = true;
+        }
         const uint32_t fb = smem_u32(&sm->full[st]);
         mbar_arrive_expect_tx(fb, stage_bytes);
         for (int kc = 0; kc < a.KC; ++kc)
@@ -356,7 +362,16 @@ cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(p.smem_bytes));
   if (e != cudaSuccess) return e;
-  indexer_score_kernel<<<grid, kIdxThreads, p.smem_bytes, stream>>>(tm_ik, tm_iq, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kIdxThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  cfg.attrs = at;
+  cfg.numAttrs = add_dependent_attr(at, 0);
+  e = cudaLaunchKernelEx(&cfg, indexer_score_kernel, tm_ik, tm_iq, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

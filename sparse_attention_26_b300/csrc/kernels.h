@@ -11,6 +11,14 @@
 
 namespace hattn {
 
+// Whether the calling host thread launches the dependent-capable kernels
+// (indexer scores, top-k, attention, merges) as programmatic dependents of
+// the previous kernel in their stream (hattn_set_dependent_launch).
+bool dependent_launch();
+// Appends the programmatic-serialization attribute to attrs[n] when
+// dependent_launch() holds; returns the new attribute count.
+int add_dependent_attr(cudaLaunchAttribute* attrs, int n);
+
 // ------------------------------------------------------------ compressor
 struct CompressArgs {
   const __nv_bfloat16* kv_raw;  // [B][L_cap][D]

@@ -85,6 +85,8 @@ __device__ __forceinline__ float4 row_columns(const Part* parts, int nb, int64_t
 __global__ void __launch_bounds__(kMergeBlock) combine_kernel(const CombineArgs a) {
   __shared__ float coef[kMergeBlock / kRowThreads][kMaxMergeParts];
   __shared__ float lz_s[kMergeBlock / kRowThreads];
+  pdl_trigger();
+  pdl_wait();  // the partials of the attention call are complete
   const int half = threadIdx.x / kRowThreads, t = threadIdx.x % kRowThreads;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kMergeBlock / kRowThreads) + half;
   const bool live = row < a.rows;
@@ -98,6 +100,8 @@ __global__ void __launch_bounds__(kMergeBlock) combine_kernel(const CombineArgs 
 }
 
 __global__ void __launch_bounds__(kMergeBlock) merge_kernel(const __grid_constant__ MergeArgs a) {
+  pdl_trigger();
+  pdl_wait();  // the branch outputs / partials are complete
   __shared__ float coef[kMergeBlock / kRowThreads][kMaxMergeParts];
   __shared__ float lz_s[kMergeBlock / kRowThreads];
   __shared__ float rc[4][kMaxRopePairs];
@@ -160,7 +164,15 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
   const int per = kMergeBlock / kRowThreads;
   const int64_t blocks = (a.rows + per - 1) / per;
-  combine_kernel<<<static_cast<unsigned>(blocks), kMergeBlock, 0, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kMergeBlock, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  cfg.attrs = at;
+  cfg.numAttrs = add_dependent_attr(at, 0);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -169,7 +181,15 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   const int per = kMergeBlock / kRowThreads;
   const int64_t blocks = (rows + per - 1) / per;
-  merge_kernel<<<static_cast<unsigned>(blocks), kMergeBlock, 0, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kMergeBlock, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  cfg.attrs = at;
+  cfg.numAttrs = add_dependent_attr(at, 0);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

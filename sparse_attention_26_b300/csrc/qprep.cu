@@ -95,6 +95,7 @@ __device__ __forceinline__ void load_rope_coef(float (*rc)[kMaxRopePairs], const
 
 __global__ void __launch_bounds__(kQpThreads) qprep_kernel(const __grid_constant__ QPrepArgs a) {
   __shared__ float rc[4][kMaxRopePairs];
+  pdl_trigger();
   load_rope_coef(rc, a.rope, a.r);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rows = static_cast<int64_t>(a.B) * a.T * a.H;
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(kQpThreads) qprep_kernel(const __grid_constant
 __global__ void __launch_bounds__(kQpThreads)
     swa_keys_kernel(const __grid_constant__ SwaKeysArgs a) {
   __shared__ float rc[4][kMaxRopePairs];
+  pdl_trigger();
   load_rope_coef(rc, a.rope, a.r);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rows = static_cast<int64_t>(a.B) * a.T * a.W;

@@ -123,6 +123,8 @@ __global__ void topk_kernel(const TopkArgs a) {
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
 
+  pdl_trigger();
+  pdl_wait();  // the scores (and a dependent launch's predecessor) are complete
   const int32_t t = a.pos[row];
   int64_t n = t < 0 ? 0 : (static_cast<int64_t>(t) + 1) / a.m;
   if (n > a.N_cap) n = a.N_cap;
@@ -452,13 +454,13 @@ cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, cudaStream_t strea
   cfg.blockDim = dim3(p.threads, 1, 1);
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = p.cluster;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = add_dependent_attr(at, 1);
   TopkArgs args = a;
   args.cluster = p.cluster;
   args.slice = p.slice;

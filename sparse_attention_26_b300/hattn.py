@@ -70,6 +70,7 @@ _SIGS = {
     "hattn_check_status": (_i32, [_vp]),
     "hattn_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
     "hattn_version": (ctypes.c_char_p, []),
+    "hattn_set_dependent_launch": (_i32, [_i32]),
 }
 
 _lib = None
@@ -541,3 +542,10 @@ def status_string(code):
 
 def version():
     return lib().hattn_version().decode()
+
+
+def set_dependent_launch(enable):
+    """Launch the indexer, top-k, attention and merge kernels of the calls that
+    follow on this thread as programmatic dependents of the previous kernel in
+    their stream (see hattn_set_dependent_launch); returns the old setting."""
+    return bool(lib().hattn_set_dependent_launch(int(bool(enable))))

@@ -44,6 +44,9 @@ class HybridLayer:
         self.ik_c = torch.zeros((B, n_c, wl.dI), dtype=bf, device=device)
         self.kv_h = torch.zeros((B, n_h, D), dtype=bf, device=device)
         self.override_dense_sms = 0  # > 0: HCA + SWA attention on that many SMs beside the indexer
+        # fused step with a side stream: the indexer, top-k, attention and
+        # merge start as dependent launches of their predecessors
+        self.dependent_launch = True
         if build_caches:
             self.build_caches()
         self._bufs = {}
@@ -322,6 +325,11 @@ class HybridLayer:
         if side_stream is None:
             compress("hca")
         ev("compress", 1)
+        # from here on each main-stream call consumes what the one before it
+        # produced, so its kernel may start as a dependent launch (its setup
+        # overlaps the predecessor's tail; it waits before reading inputs)
+        pdl = side_stream is not None and self.dependent_launch and events is None
+        prev_pdl = hattn.set_dependent_launch(pdl)
         if side_stream is not None and overlap:
             qprep()
             side_stream.wait_stream(main)
@@ -355,6 +363,7 @@ class HybridLayer:
         hattn.lse_merge_splits(parts, pos, r=wl.r, H=wl.H, sink=sink, out=b["out"],
                                lse_out=b["lse"])
         ev("merge", 1)
+        hattn.set_dependent_launch(prev_pdl)
         return b["out"], b["lse"]
 
     def event_names(self, T, branch_outputs=False, fused=None, side_stream=True):

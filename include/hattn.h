@@ -143,14 +143,19 @@ HATTN_API int hattn_indexer_topk_noalloc(const void* iq, const float* w, const v
 HATTN_API int hattn_indexer_scores(const void* iq, const float* w, const void* ik_c,
                                    const int32_t* pos, int B, int T, int HI, int dI,
                                    int64_t N_cap, int m, float* score_out, hattn_stream_t stream);
-/* hattn_indexer_scores on at most n_sms SMs (n_sms = 0: all).  The score
- * kernel is persistent, one CTA per SM it uses; capping it leaves SMs free
- * for work on another stream (the attention segments that do not need the
- * top-k result), which then runs concurrently instead of after it. */
-HATTN_API int hattn_indexer_scores_sms(const void* iq, const float* w, const void* ik_c,
-                                       const int32_t* pos, int B, int T, int HI, int dI,
-                                       int64_t N_cap, int m, int n_sms, float* score_out,
-                                       hattn_stream_t stream);
+/* hattn_indexer_scores with two scheduling options.
+ *   n_sms: run the persistent score kernel on at most that many SMs (0 = all;
+ *   one CTA per SM used), leaving the others to work on another stream.
+ *   fresh_from: with dependent launches enabled (hattn_set_dependent_launch),
+ *   the entries of ik_c at index >= fresh_from are the only ones the
+ *   previous kernel in the stream may write (say, the compressor of the
+ *   newest entry); blocks of entries below it are read without waiting for
+ *   that kernel.  -1: any entry may be written (wait before the first read).
+ *   Ignored without dependent launches. */
+HATTN_API int hattn_indexer_scores_ex(const void* iq, const float* w, const void* ik_c,
+                                      const int32_t* pos, int B, int T, int HI, int dI,
+                                      int64_t N_cap, int m, int n_sms, int64_t fresh_from,
+                                      float* score_out, hattn_stream_t stream);
 HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T,
                                 int64_t N_cap, int k, int m, int32_t* idx_out,
                                 hattn_stream_t stream);

@@ -461,7 +461,7 @@ namespace {
 
 int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
                         int B, int T, int HI, int dI, int64_t N_cap, int m, float* scores,
-                        hattn_stream_t stream, int n_sms = 0) {
+                        hattn_stream_t stream, int n_sms = 0, int64_t fresh_from = -1) {
   REQUIRE_PTR(iq);
   REQUIRE_PTR(w);
   REQUIRE_PTR(ik_c);
@@ -510,6 +510,7 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   a.stages = ip.stages;
   a.groups_per_seq = (T + ip.G - 1) / ip.G;
   a.nblk = static_cast<int>((N_cap + 127) / 128);
+  a.fresh_from = fresh_from;
   a.N_cap = N_cap;
   a.total_slots = (int64_t)B * a.groups_per_seq * a.nblk;
   // persistent: one CTA per SM it may use (n_sms of them when given, so
@@ -588,10 +589,12 @@ int hattn_indexer_scores(const void* iq, const float* w, const void* ik_c, const
   return indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, score_out, stream);
 }
 
-int hattn_indexer_scores_sms(const void* iq, const float* w, const void* ik_c,
-                             const int32_t* pos, int B, int T, int HI, int dI, int64_t N_cap,
-                             int m, int n_sms, float* score_out, hattn_stream_t stream) {
-  return indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms);
+int hattn_indexer_scores_ex(const void* iq, const float* w, const void* ik_c,
+                            const int32_t* pos, int B, int T, int HI, int dI, int64_t N_cap,
+                            int m, int n_sms, int64_t fresh_from, float* score_out,
+                            hattn_stream_t stream) {
+  return indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms,
+                             fresh_from < 0 ? -1 : fresh_from);
 }
 
 int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T, int64_t N_cap, int k,

@@ -170,8 +170,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (it >= a.stages &&
             !mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 11))
           break;
-        if (!keys_ready) {
-          pdl_wait();  // a dependent launch waits here for the entries its predecessor writes
+        if (!keys_ready &&
+            (a.fresh_from < 0 || static_cast<int64_t>(cur.blk + 1) * kBlockRows > a.fresh_from)) {
+          // a dependent launch waits here, before the first block that holds
+          // entries its predecessor may have written (the other blocks stream
+          // while that kernel still runs)
+          pdl_wait();
           keys_ready = true;
         }
         const uint32_t fb = smem_u32(&sm->full[st]);

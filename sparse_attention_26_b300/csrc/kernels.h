@@ -47,6 +47,7 @@ struct IndexerArgs {
   int stages;
   int groups_per_seq;    // ceil(T / G)
   int nblk;              // ceil(N_cap / 128)
+  int64_t fresh_from;    // entries >= this may be written by the previous kernel (-1: any)
   int64_t N_cap;
   int64_t total_slots;   // B * groups_per_seq * nblk
 };

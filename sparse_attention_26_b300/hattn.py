@@ -57,8 +57,8 @@ _SIGS = {
     "hattn_hybrid_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                                 _i32, _i32, _i32]),
     "hattn_hybrid_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _i32]),
-    "hattn_indexer_scores_sms": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
-                                        _i32, _vp, _vp]),
+    "hattn_indexer_scores_ex": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
+                                       _i32, _i64, _vp, _vp]),
     "hattn_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64]),
     "hattn_lse_merge_splits": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i32),
                                       _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
@@ -223,10 +223,13 @@ def indexer_topk_noalloc(iq, w, ik_c, pos, *, k, m=4, idx_out=None, stream=None)
     return idx_out
 
 
-def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, stream=None):
+def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, fresh_from=-1,
+                   stream=None):
     """Lightning-indexer scores only; returns score_out [B, T, N_cap] fp32
     (entries beyond each query's visible count are left untouched).  n_sms:
-    run the persistent score kernel on at most that many SMs (0 = all)."""
+    run the persistent score kernel on at most that many SMs (0 = all);
+    fresh_from: with dependent launches, the first entry the previous kernel
+    may write (-1 = any)."""
     _need(iq, "iq", torch.bfloat16, 4)
     _need(w, "w", torch.float32, 3)
     _need(ik_c, "ik_c", torch.bfloat16, 3)
@@ -236,10 +239,10 @@ def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, stream=Non
     if score_out is None:
         score_out = torch.empty((B, T, N_cap), dtype=torch.float32, device=iq.device)
     _need(score_out, "score_out", torch.float32)
-    if n_sms:
-        _check(lib().hattn_indexer_scores_sms(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI,
-                                              dI, N_cap, m, n_sms, _ptr(score_out),
-                                              _stream(stream)))
+    if n_sms or fresh_from >= 0:
+        _check(lib().hattn_indexer_scores_ex(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI,
+                                             dI, N_cap, m, n_sms, fresh_from, _ptr(score_out),
+                                             _stream(stream)))
     else:
         _check(lib().hattn_indexer_scores(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
                                           N_cap, m, _ptr(score_out), _stream(stream)))

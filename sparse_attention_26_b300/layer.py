@@ -309,17 +309,6 @@ class HybridLayer:
         # three key sets as one attention after top-k.
         n_dense = self.override_dense_sms if side_stream is not None else 0
         overlap = n_dense > 0
-        if side_stream is not None and not overlap:
-            # the query preparation, the HCA compression and the window keys
-            # (needed only by the attention) run beside the CSA compression,
-            # the indexer and top-k
-            side_stream.wait_stream(main)
-            with torch.cuda.stream(side_stream):
-                qprep()
-                compress("hca")
-                ev("swa_keys", 0)
-                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
-                ev("swa_keys", 1)
         ev("compress", 0)
         compress("csa")
         if side_stream is None:
@@ -345,9 +334,26 @@ class HybridLayer:
             hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
             ev("swa_keys", 1)
         ev("indexer", 0)
+        # the only entry the compression above writes is the newest one
+        fresh = (t_new + 1) // wl.m_csa - 1 if t_new is not None else -1
         hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=b["scores"],
-                             n_sms=(self.NUM_SMS - n_dense) if n_dense else 0)
+                             n_sms=(self.NUM_SMS - n_dense) if n_dense else 0,
+                             fresh_from=fresh if (t_new is not None and
+                                                  (t_new + 1) % wl.m_csa == 0) else -1)
         ev("indexer", 1)
+        if side_stream is not None and not overlap:
+            # The query preparation, the HCA compression and the window keys
+            # (needed only by the attention) run beside top-k, which leaves
+            # most SMs free.  Beside the indexer they would hold SMs its
+            # persistent grid needs from the start, and its statically split
+            # work would end later by as much.
+            side_stream.wait_stream(main)
+            with torch.cuda.stream(side_stream):
+                qprep()
+                compress("hca")
+                ev("swa_keys", 0)
+                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
+                ev("swa_keys", 1)
         ev("topk", 0)
         hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
         ev("topk", 1)

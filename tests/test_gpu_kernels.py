@@ -468,3 +468,52 @@ def test_tiny_layer_end_to_end():
     check_attn(o2, l2, ref["o_hca"], ref["lse_hca"], "tiny hca")
     check_attn(out, lse, ref["out"], ref["lse"], "tiny layer")
     assert L == 256
+
+
+# ------------------------------------------------------------------ dependent launches
+def test_dependent_launch_chain_matches_plain_launch():
+    """The indexer -> top-k -> fused attention -> merge chain launched as
+    programmatic dependents gives bit-identical results to plain launches
+    (each kernel waits for its predecessor before reading its outputs)."""
+    B, T, H, D, r, HI, dI, N_c, N_h, L, k = 2, 1, 128, 512, 64, 64, 128, 3000, 90, 12000, 256
+    iq = randn_bf16((B, T, HI, dI), 111).to(DEV)
+    w = randn_f32((B, T, HI), 112).to(DEV)
+    ik = randn_bf16((B, N_c, dI), 113).to(DEV)
+    kv_c = randn_bf16((B, N_c, D), 114).to(DEV)
+    kv_h = randn_bf16((B, N_h, D), 115).to(DEV)
+    raw = randn_bf16((B, L, D), 116).to(DEV)
+    q = randn_bf16((B, T, H, D), 117).to(DEV)
+    sink = randn_f32((H,), 118).to(DEV)
+    pos = _pos(B, T, [11999, 9000]).to(DEV)
+    qt = hattn.query_prep(q, pos, r=r)
+    kv_w = hattn.swa_keys(raw, pos, r=r, W=128)
+    torch.cuda.synchronize()
+
+    def chain():
+        sc = hattn.indexer_scores(iq, w, ik, pos, m=4)
+        idx = hattn.topk_select(sc, pos, k=k, m=4)
+        # the selection comes in no fixed order; sorted, both runs attend to
+        # the entries in the same order (and the attention waits for the sort)
+        idx_s = idx.sort(dim=-1).values
+        part = hattn.hybrid_attn(qt, kv_c, idx_s, kv_h, kv_w, pos, r=r, q_prepped=True,
+                                 partials=True)
+        out, lse = hattn.lse_merge_splits([part], pos, r=r, H=H, sink=sink)
+        return sc, idx_s, out, lse
+
+    plain = [t.clone() for t in chain()]
+    torch.cuda.synchronize()
+    prev = hattn.set_dependent_launch(True)
+    try:
+        dep = [t.clone() for t in chain()]
+    finally:
+        hattn.set_dependent_launch(prev)
+    torch.cuda.synchronize()
+    hattn.check_status()
+    sc0, idx0, out0, lse0 = plain
+    sc1, idx1, out1, lse1 = dep
+    vis = [min((int(p) + 1) // 4, N_c) for p in pos.cpu().ravel()]
+    for bb in range(B):
+        assert torch.equal(sc0[bb, 0, :vis[bb]], sc1[bb, 0, :vis[bb]])
+    assert torch.equal(idx0, idx1)
+    assert torch.equal(out0, out1)
+    assert torch.equal(lse0, lse1)

@@ -107,12 +107,12 @@ def indexer_bytes(wl):
 
 # DRAM traffic of indexer_score_kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum) from one ncu capture of an 8 x 65,536-entry launch
-# (138.26 MB), per entry processed; it applies only to the kernel sources it
+# (138.09 MB), per entry processed; it applies only to the kernel sources it
 # was taken on, checked by hash, else the bench reports traffic as null.
 INDEXER_TRAFFIC = {
-    "bytes_per_entry": 138.264e6 / (8 * 65536),
+    "bytes_per_entry": 138.089e6 / (8 * 65536),
     "sources": ["indexer.cu", "common.cuh"],
-    "sha256": "1a16f370bc82cf9a05017b7e286821c373be1e3659184d5712480b252298fec1",
+    "sha256": "4750d762d6e002352e20659e3f4fd9e43cb406230eda7141f5f59d902f711cae",
     "profile": "profiles/indexer_score_kernel_decode_8x65536.md",
 }
 

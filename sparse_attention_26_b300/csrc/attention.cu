@@ -789,18 +789,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mraw = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
                                fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
       const float mx = mraw * sl2;  // sl2 > 0: the max of the scaled logits
-      // O is rescaled below, and PV(i-1) must have finished writing it
-      if (i > 0) {
-        got = mbar_wait(smem_u32(&sm->pv_done), (i - 1) & 1, abort, a.status, kWaitLimitNs, 32);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-        tc_fence_after();
-      }
       // Lazy rescale: only when the running max grows by more than 2^8.  The
       // tensor-memory loads/stores are warp-collective, so the decision is
-      // taken per warp; lanes that need no rescale multiply by 1.
+      // taken per warp; lanes that need no rescale multiply by 1.  O is
+      // touched only then, after PV(i-1) has finished writing it (PV runs at
+      // most one tile ahead of this wait, so the parity stays unambiguous).
       const bool grow = mx > m_used + 8.f;
       const bool need_rescale = grow && m_used != -INFINITY && i > 0;
       if (__any_sync(0xffffffffu, need_rescale)) {
+        got = mbar_wait(smem_u32(&sm->pv_done), (i - 1) & 1, abort, a.status, kWaitLimitNs, 32);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc_fence_after();
         const float f = need_rescale ? ex2_fast(m_used - mx) : 1.f;
         for (int cc = 0; cc < ocols; cc += 32) {
           float o[32];

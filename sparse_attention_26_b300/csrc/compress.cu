@@ -218,11 +218,129 @@ __global__ void __launch_bounds__(kCompressThreads)
   }
 }
 
+// A few entries with short windows (CSA at decode: one entry per sequence,
+// 8 tokens): 128 threads and ~1 KB of shared memory, so a CTA fits beside a
+// CTA of the persistent indexer on the same SM instead of delaying it.
+// Thread c owns 16-byte piece c of the [KV | indexer-key] row and has every
+// token of the window in flight at once.
+constexpr int kSmallThreads = 128;
+constexpr int kSmallMaxW = 16;
+
+__global__ void __launch_bounds__(kSmallThreads)
+    compress_small_kernel(const __grid_constant__ CompressArgs a) {
+  __shared__ float alpha[kSmallMaxW];
+  __shared__ float rc[4][kMaxRopePairs];
+  __shared__ float red[kSmallThreads / 32];
+  pdl_trigger();  // a dependent launch after this kernel may begin
+  const int tid = threadIdx.x;
+  const int NCk = a.D / 8;
+  const int NC = NCk + (a.ik_raw ? a.dI / 8 : 0);
+  for (int i = tid; i < a.r / 2; i += kSmallThreads) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) rc[c][i] = a.rope.c[c][i];
+  }
+  const int64_t nj = a.j_end - a.j_begin;
+  const int64_t items = nj * a.B;
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const int b = static_cast<int>(item / nj);
+    const int64_t j = a.j_begin + item % nj;
+    const int64_t u0 = static_cast<int64_t>(a.m) * (j + 1) - a.w;
+    // the window's rows of this thread's piece, all requested at once
+    uint4 v[kSmallMaxW];
+    if (tid < NC) {
+      const __nv_bfloat16* src = tid < NCk
+          ? a.kv_raw + (int64_t)b * a.L_cap * a.D + tid * 8
+          : a.ik_raw + (int64_t)b * a.L_cap * a.dI + (tid - NCk) * 8;
+      const int64_t stride = tid < NCk ? a.D : a.dI;
+#pragma unroll
+      for (int q = 0; q < kSmallMaxW; ++q) {
+        const int64_t u = u0 + q;
+        v[q] = (q < a.w && u >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + u * stride))
+                                   : make_uint4(0, 0, 0, 0);
+      }
+    }
+    // gate softmax over the tokens that exist (warp 0, one token per lane)
+    if (tid < 32) {
+      const int64_t u = u0 + tid;
+      const bool live = tid < a.w && u >= 0;
+      const float g = live ? __bfloat162float(a.gate[(int64_t)b * a.L_cap + u]) : -INFINITY;
+      float gmax = g;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+      const float e = live ? __expf(g - gmax) : 0.f;
+      float z = e;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      if (tid < kSmallMaxW) alpha[tid] = e / z;
+    }
+    __syncthreads();
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    float ss = 0.f;
+    if (tid < NC) {
+#pragma unroll
+      for (int q = 0; q < kSmallMaxW; ++q) {
+        const float al = alpha[q];  // zero for tokens that do not exist or lie past w
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[q]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h[e]);
+          acc[2 * e] = fmaf(al, f.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(al, f.y, acc[2 * e + 1]);
+        }
+      }
+      if (tid < NCk)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(acc[e], acc[e], ss);
+    }
+    // RMS over the KV part
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSmallThreads / 32; ++i) tot += red[i];
+    const float inv = rsqrtf(tot / static_cast<float>(a.D) + a.eps);
+    if (tid < NCk) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float g = a.gamma ? a.gamma[tid * 8 + e] : 1.f;
+        y[e] = acc[e] * inv * g;
+      }
+      const int d0 = a.D - a.r;
+      const int64_t p = static_cast<int64_t>(a.m) * (j + 1) - 1;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const int d = tid * 8 + e;
+        if (d >= d0) {
+          float sn, cs;
+          rope_cs(rc, (d - d0) / 2, p, &sn, &cs);
+          const float x0 = y[e], x1 = y[e + 1];
+          y[e] = x0 * cs - x1 * sn;
+          y[e + 1] = x0 * sn + x1 * cs;
+        }
+      }
+      store8(a.kv_out + ((int64_t)b * a.N_cap + j) * a.D + tid * 8, y);
+    } else if (tid < NC) {
+      store8(a.ik_out + ((int64_t)b * a.N_cap + j) * a.dI + (tid - NCk) * 8, acc);
+    }
+    __syncthreads();  // alpha and red are rewritten by the next entry
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_compress(const CompressArgs& a, int num_sms, cudaStream_t stream) {
   const int64_t items = (a.j_end - a.j_begin) * a.B;
   if (items <= 0) return cudaSuccess;
+  const int NC = a.D / 8 + (a.ik_raw ? a.dI / 8 : 0);
+  if (a.w <= kSmallMaxW && NC <= kSmallThreads && items <= 4 * (int64_t)num_sms) {
+    compress_small_kernel<<<static_cast<unsigned>(items), kSmallThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
   const int64_t grid = items < (int64_t)num_sms * 8 ? items : (int64_t)num_sms * 8;
   compress_kernel<<<static_cast<unsigned>(grid), kCompressThreads, 0, stream>>>(a);
   return cudaGetLastError();

@@ -56,6 +56,7 @@ def test_bounded_wait_times_out_and_reports():
     (2, 64, 64, 32, 16, 0, 16),
     (1, 1030, 512, 128, 64, 0, 257),
     (2, 1024, 512, 128, 64, 100, 131),   # incremental range
+    (2, 4096, 64, 32, 16, 0, 1024),      # many entries: the grid-stride kernel, not the small one
 ])
 def test_csa_compress(B, L, D, dI, r, j0, j1):
     kv = randn_bf16((B, L, D), 1)

@@ -24,7 +24,7 @@ namespace hattn {
 
 namespace {
 
-constexpr int kIdxThreads = 192;
+constexpr int kIdxThreads = 224;  // producer, MMA (even slots), 4 epilogue warps, MMA (odd slots)
 constexpr int kBlockRows = 128;
 constexpr int kMaxStages = 8;
 
@@ -35,7 +35,7 @@ struct IdxSmem {
   uint64_t tempty[2];
   uint64_t qfull;
   uint64_t qempty;
-  uint64_t mma_done;
+  uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
   // per epilogue warp (no cross-warp barrier): visible entries per query of
@@ -124,8 +124,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       mbar_init(smem_u32(&sm->tempty[i]), 128);
     }
     mbar_init(smem_u32(&sm->qfull), 1);
-    mbar_init(smem_u32(&sm->qempty), 1);
-    mbar_init(smem_u32(&sm->mma_done), 1);
+    mbar_init(smem_u32(&sm->qempty), 2);  // both MMA issuers leave the query block
+    mbar_init(smem_u32(&sm->mma_done[0]), 1);
+    mbar_init(smem_u32(&sm->mma_done[1]), 1);
     sm->abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_ik);
@@ -194,8 +195,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                     10000000ull, 12);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 6) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues the products of the even live slots (accumulator 0) and
+    // warp 6 those of the odd ones (accumulator 1): a single thread issues a
+    // chained tcgen05.mma only every ~64 ns, close to a slot's share of the
+    // key stream, so two issuers keep the tensor core ahead of it.
+    const int par = warp == 1 ? 0 : 1;
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, a.NQ, 0, 0);
       SlotCursor cur;
@@ -211,31 +217,33 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           loaded = cur.group;
         }
         const int acc = static_cast<int>(it & 1);
-        if (it >= 2 &&
-            !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> 1) + 1) & 1, abort, a.status,
-                       kWaitLimitNs, 14))
-          break;
-        if (!mbar_wait(smem_u32(&sm->full[st]), ph, abort, a.status, kWaitLimitNs, 15)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * a.NQ;
-        for (int kc = 0; kc < a.KC; ++kc) {
-          const uint32_t a_addr = smem_u32(sA + st * stage_bytes + kc * 16384);
-          const uint32_t b_addr = smem_u32(sQ + kc * a.NQ * 128);
+        if (acc == par) {
+          if (it >= 2 &&
+              !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> 1) + 1) & 1, abort, a.status,
+                         kWaitLimitNs, 14))
+            break;
+          if (!mbar_wait(smem_u32(&sm->full[st]), ph, abort, a.status, kWaitLimitNs, 15)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + acc * a.NQ;
+          for (int kc = 0; kc < a.KC; ++kc) {
+            const uint32_t a_addr = smem_u32(sA + st * stage_bytes + kc * 16384);
+            const uint32_t b_addr = smem_u32(sQ + kc * a.NQ * 128);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = smem_desc(a_addr + ks * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(b_addr + ks * 32, 16, 1024, kSwizzle128B);
-            mma_bf16_ss(d_tmem, ad, bd, idesc, (kc | ks) != 0);
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = smem_desc(a_addr + ks * 32, 16, 1024, kSwizzle128B);
+              const uint64_t bd = smem_desc(b_addr + ks * 32, 16, 1024, kSwizzle128B);
+              mma_bf16_ss(d_tmem, ad, bd, idesc, (kc | ks) != 0);
+            }
           }
+          mma_commit(smem_u32(&sm->empty[st]));
+          mma_commit(smem_u32(&sm->tfull[acc]));
         }
-        mma_commit(smem_u32(&sm->empty[st]));
-        mma_commit(smem_u32(&sm->tfull[acc]));
         ++it;
         if (++st == a.stages) { st = 0; ph ^= 1u; }
       }
       // all issued MMAs complete before the accumulators are released
-      mma_commit(smem_u32(&sm->mma_done));
-      mbar_wait(smem_u32(&sm->mma_done), 0, nullptr, a.status, kWaitLimitNs, 16);
+      mma_commit(smem_u32(&sm->mma_done[par]));
+      mbar_wait(smem_u32(&sm->mma_done[par]), 0, nullptr, a.status, kWaitLimitNs, 16);
     }
   } else {
     // ------------------------------------------------------------ epilogue

@@ -37,7 +37,9 @@
  *  - logits s * q~ . k~ with s = 1/sqrt(D); values V = K~ (shared latent);
  *  - RoPE: interleaved pairs (d0+2i, d0+2i+1), d0 = D-r, angle p*base^(-2i/r);
  *  - merge: Z = sum_b exp(lse_b) + exp(sink_h); out = sum_b exp(lse_b) o_b / Z,
- *    then the last r dims are rotated back by the query position.
+ *    then the last r dims are rotated back by the query position;
+ *  - low-precision indexer path (optional): keys and query rows as E4M3 codes
+ *    with one fp32 scale amax/448 per row, dequantised before the score.
  */
 #include <math.h>
 #include <stdint.h>
@@ -234,6 +236,121 @@ int orc_indexer_scores(const uint16_t* iq, const float* w, const uint16_t* ik, c
             }
         }
     }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* FP8 indexer keys  ("DeepSeek-V4" atlas spec sheet, section           */
+/* "Inference efficiency": the indexer QK path is quantised to low      */
+/* precision).  The pages do not fix the format; the reading here is    */
+/* OCP FP8 E4M3 codes with one fp32 scale per 128-dim row.              */
+/* ------------------------------------------------------------------ */
+
+/* E4M3 ("fn" variant): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits;
+ * no infinities, code S.1111.111 is NaN, largest finite 1.75 * 2^8 = 448,
+ * subnormals m * 2^-9 for m = 1..7. */
+double orc_e4m3_to_f64(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 value to an fp32 value (ties to the even code), with values
+ * beyond 448 in magnitude clamped to 448 (saturating). */
+uint8_t orc_f32_to_e4m3(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int e;
+    frexp(a, &e);                 /* a = f * 2^e, f in [0.5, 1) */
+    int q = e - 4;                /* spacing of 4-significant-bit numbers */
+    if (q < -9) q = -9;           /* subnormal spacing */
+    double r = nearbyint(ldexp(a, -q));   /* units of 2^q, half to even */
+    /* r * 2^q is exactly representable; the code is its bit pattern */
+    double v = ldexp(r, q);
+    if (v == 0.0) return sign;
+    int ev;
+    frexp(v, &ev);
+    int E = ev - 1 + 7;           /* biased exponent of v = 1.m * 2^(ev-1) */
+    uint8_t code;
+    if (E <= 0) code = (uint8_t)ldexp(v, 9);                 /* subnormal: m */
+    else code = (uint8_t)((E << 3) | ((int)(ldexp(v, -(ev - 1)) * 8.0) - 8));
+    return (uint8_t)(sign | code);
+}
+
+/* One row of n bf16 values to E4M3 codes and a scale, in fp32 arithmetic:
+ * amax = max |x|; inv = 448 / amax; code_i = e4m3(x_i * inv); the row
+ * decodes as code_i * scale with scale = amax / 448.  A zero row gives
+ * zero codes and scale 0. */
+void orc_quantize_e4m3_row(const uint16_t* x, int n, uint8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf((float)orc_bf16_to_f64(x[i]));
+        if (a > amax) amax = a;
+    }
+    if (!(amax > 0.0f)) {
+        for (int i = 0; i < n; ++i) codes[i] = 0;
+        *scale = 0.0f;
+        return;
+    }
+    float inv = 448.0f / amax;
+    for (int i = 0; i < n; ++i) codes[i] = orc_f32_to_e4m3((float)orc_bf16_to_f64(x[i]) * inv);
+    *scale = amax / 448.0f;
+}
+
+void orc_quantize_e4m3_rows(const uint16_t* x, int64_t rows, int n, uint8_t* codes,
+                            float* scales) {
+    for (int64_t r = 0; r < rows; ++r)
+        orc_quantize_e4m3_row(x + r * n, n, codes + r * n, scales + r);
+}
+
+/*
+ * Indexer scores with FP8 keys: the keys arrive as codes ik8 [B][N_cap][dI]
+ * with scales iks [B][N_cap]; each query row iq[b][t][h] (bf16) is quantised
+ * the same way; both are dequantised to fp64 and the score is the plain
+ * definition sum_h w[t,h] * max(0, q^[t,h] . k^[j]).  NaN past the visible
+ * entries.
+ */
+int orc_indexer_scores_e4m3(const uint16_t* iq, const float* w, const uint8_t* ik8,
+                            const float* iks, const int32_t* pos, int B, int T, int HI, int dI,
+                            int64_t N_cap, int m, double* scores) {
+    if (B <= 0 || T <= 0 || HI <= 0 || dI <= 0 || N_cap < 0 || m <= 0) return ORC_EINVAL;
+    uint8_t* qc = (uint8_t*)malloc((size_t)HI * dI);
+    float* qs = (float*)malloc(sizeof(float) * (size_t)HI);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)HI * dI);
+    double* kd = (double*)malloc(sizeof(double) * (size_t)dI);
+    if (!qc || !qs || !qd || !kd) { free(qc); free(qs); free(qd); free(kd); return ORC_ENOMEM; }
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < T; ++t) {
+            int64_t bt = (int64_t)b * T + t;
+            for (int h = 0; h < HI; ++h) {
+                orc_quantize_e4m3_row(iq + (bt * HI + h) * dI, dI, qc + (size_t)h * dI, qs + h);
+                for (int d = 0; d < dI; ++d)
+                    qd[(size_t)h * dI + d] = orc_e4m3_to_f64(qc[(size_t)h * dI + d]) * (double)qs[h];
+            }
+            int64_t n = orc_visible(pos[bt], m);
+            if (n > N_cap) n = N_cap;
+            double* out = scores + bt * N_cap;
+            for (int64_t j = 0; j < N_cap; ++j) out[j] = NAN;
+            for (int64_t j = 0; j < n; ++j) {
+                const uint8_t* kj = ik8 + ((int64_t)b * N_cap + j) * dI;
+                double sk = (double)iks[(int64_t)b * N_cap + j];
+                for (int d = 0; d < dI; ++d) kd[d] = orc_e4m3_to_f64(kj[d]) * sk;
+                double s = 0.0;
+                for (int h = 0; h < HI; ++h) {
+                    double dot = 0.0;
+                    for (int d = 0; d < dI; ++d) dot += qd[(size_t)h * dI + d] * kd[d];
+                    s += (double)w[bt * HI + h] * (dot > 0.0 ? dot : 0.0);
+                }
+                out[j] = s;
+            }
+        }
+    }
+    free(qc); free(qs); free(qd); free(kd);
     return ORC_OK;
 }
 

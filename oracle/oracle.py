@@ -22,6 +22,7 @@ from . import build as _build
 _lib = None
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -52,6 +53,15 @@ def lib():
         L.orc_indexer_scores.argtypes = [_u16p, _f32p, _u16p, _i32p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                          _f64p]
+        L.orc_e4m3_to_f64.restype = ctypes.c_double
+        L.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.orc_f32_to_e4m3.restype = ctypes.c_uint8
+        L.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
+        L.orc_quantize_e4m3_rows.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, _u8p, _f32p]
+        L.orc_indexer_scores_e4m3.restype = ctypes.c_int
+        L.orc_indexer_scores_e4m3.argtypes = [_u16p, _f32p, _u8p, _f32p, _i32p, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int64, ctypes.c_int, _f64p]
         L.orc_topk.restype = ctypes.c_int
         L.orc_topk.argtypes = [_f64p, _i32p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                ctypes.c_int, _i32p]
@@ -172,6 +182,55 @@ def indexer_scores(iq, w, ik, pos, m):
     rc = lib().orc_indexer_scores(_p(iq, _u16p), _p(w, _f32p), _p(ik, _u16p), _p(pos, _i32p), B, T,
                                   HI, dI, N, m, _p(out, _f64p))
     _check(rc, "indexer_scores")
+    return out
+
+
+# ---------------------------------------------------------------- FP8 indexer keys
+def e4m3_to_f64(codes):
+    """Values of E4M3 codes (uint8 array), fp64."""
+    c = np.asarray(codes, dtype=np.uint8)
+    f = lib().orc_e4m3_to_f64
+    return np.array([f(int(x)) for x in c.ravel()], np.float64).reshape(c.shape)
+
+
+def f32_to_e4m3(x):
+    """Nearest E4M3 codes (ties to even, saturating at 448) of fp32 values."""
+    x = np.asarray(x, dtype=np.float32)
+    f = lib().orc_f32_to_e4m3
+    return np.array([f(float(v)) for v in x.ravel()], np.uint8).reshape(x.shape)
+
+
+def quantize_e4m3(x):
+    """Rows of the last axis of bf16 bits to (codes uint8, scales fp32)."""
+    x = _u16(x)
+    n = x.shape[-1]
+    rows = x.size // n if n else 0
+    codes = np.empty(x.shape, np.uint8)
+    scales = np.empty(x.shape[:-1], np.float32)
+    lib().orc_quantize_e4m3_rows(_p(x, _u16p), rows, n, _p(codes, _u8p), _p(scales, _f32p))
+    return codes, scales
+
+
+def dequantize_e4m3(codes, scales):
+    """codes * scale per row, fp64."""
+    return e4m3_to_f64(codes) * np.asarray(scales, np.float64)[..., None]
+
+
+def indexer_scores_e4m3(iq, w, ik8, iks, pos, m):
+    """fp64 scores [B, T, N_cap] from FP8 keys (codes ik8, row scales iks);
+    the bf16 queries are quantised the same way and both sides dequantised."""
+    iq = _u16(iq)
+    ik8 = np.ascontiguousarray(ik8, dtype=np.uint8)
+    iks = _f32(iks)
+    w = _f32(w)
+    pos = _i32(pos)
+    B, T, HI, dI = iq.shape
+    N = ik8.shape[1]
+    out = np.empty((B, T, N), np.float64)
+    rc = lib().orc_indexer_scores_e4m3(_p(iq, _u16p), _p(w, _f32p), _p(ik8, _u8p),
+                                       _p(iks, _f32p), _p(pos, _i32p), B, T, HI, dI, N, m,
+                                       _p(out, _f64p))
+    _check(rc, "indexer_scores_e4m3")
     return out
 
 

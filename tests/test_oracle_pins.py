@@ -184,6 +184,100 @@ def test_indexer_special_cases(orc):
     np.testing.assert_allclose(s12[ok], (s1 + s2)[ok], rtol=1e-5, atol=1e-5)
 
 
+# --------------------------------------------------------------------- FP8 (E4M3) keys
+def _torch_e4m3(x32):
+    """torch's float8_e4m3fn cast (nearest even, NaN past 464) as uint8 codes."""
+    return torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _e4m3_table():
+    return torch.arange(256, dtype=torch.int32).to(torch.uint8).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_decode_and_rounding_match_torch(orc):
+    """Decoding of every finite code, and nearest-even encoding of the code
+    values, of the midpoints between neighbouring codes (the ties), and of
+    random magnitudes over the whole range, against torch's float8_e4m3fn
+    (an independent implementation), where torch does not overflow."""
+    table = _e4m3_table()
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    np.testing.assert_array_equal(orc.e4m3_to_f64(finite), table[finite])
+    mags = np.unique(np.abs(table[finite]))
+    mids = (mags[1:] + mags[:-1]) / 2
+    rng = np.random.default_rng(21)
+    rnd = rng.standard_normal(20000) * 2.0 ** rng.integers(-14, 10, 20000)
+    x = np.concatenate([table[finite], mids, -mids, rnd])
+    x32 = x.astype(np.float32)
+    x32 = x32[np.abs(x32) <= 464]
+    np.testing.assert_array_equal(orc.f32_to_e4m3(x32), _torch_e4m3(x32))
+
+
+def test_e4m3_hand_cases(orc):
+    cases = [(448.0, 0x7E), (1.0, 0x38), (-1.0, 0xB8), (2.0 ** -9, 0x01), (2.0 ** -6, 0x08),
+             (2.0 ** -10, 0x00),            # half the smallest subnormal: tie to even 0
+             (3 * 2.0 ** -10, 0x02),        # 1.5 subnormal steps: tie to even 2
+             (1.0625, 0x38), (1.1875, 0x3A),  # ties between 1, 1.125 and 1.25
+             (240.0, 0x77), (500.0, 0x7E), (-1e30, 0xFE), (math.inf, 0x7E)]
+    for x, code in cases:
+        assert int(orc.f32_to_e4m3(np.float32(x))) == code, x
+
+
+def test_e4m3_row_quantisation(orc):
+    """Per-row scale amax/448, the largest element on +-448, the codes of
+    x * (448/amax) rounded by torch's cast, and every dequantised value
+    within half an E4M3 step of the input; a zero row has scale 0."""
+    rng = np.random.default_rng(22)
+    xv64 = rng.standard_normal((60, 128)) * 10.0 ** rng.integers(-3, 4, (60, 1))
+    x = b16(xv64)
+    xv = f64(x)
+    codes, scales = orc.quantize_e4m3(x)
+    amax = np.abs(xv).max(-1).astype(np.float32)
+    np.testing.assert_array_equal(scales, amax / np.float32(448))
+    top = np.abs(xv).argmax(-1)
+    assert ((codes[np.arange(60), top] & 0x7F) == 0x7E).all()
+    inv = np.float32(448) / amax
+    np.testing.assert_array_equal(codes, _torch_e4m3(xv.astype(np.float32) * inv[:, None]))
+    deq = orc.dequantize_e4m3(codes, scales)
+    bound = np.maximum(np.abs(xv) * 2.0 ** -4, 2.0 ** -10 * scales[:, None]) * (1 + 1e-6)
+    assert (np.abs(deq - xv) <= bound).all()
+    c0, s0 = orc.quantize_e4m3(np.zeros((1, 128), np.uint16))
+    assert (c0 == 0).all() and s0[0] == 0
+
+
+def test_indexer_e4m3_exact_rows_equal_bf16_scores(orc):
+    """Rows of multiples of 1/2 with largest magnitude 3.5 quantise without
+    loss (scale 2^-7, codes on 64..448), so the FP8 scores equal the bf16
+    scores exactly; scaling a key row by a power of two scales its scores by
+    the same factor (the key scale enters once, ReLU is homogeneous)."""
+    rng = np.random.default_rng(23)
+    B, T, HI, dI, N, m = 2, 3, 4, 128, 9, 4
+
+    def rows(shape):
+        v = rng.integers(-7, 8, shape).astype(np.float64) / 2
+        v[..., 0] = np.where(rng.random(shape[:-1]) < 0.5, 3.5, -3.5)
+        return v
+
+    iq, ik = b16(rows((B, T, HI, dI))), b16(rows((B, N, dI)))
+    w = rng.standard_normal((B, T, HI)).astype(np.float32)
+    pos = np.array([[3, 20, 35], [7, 11, 2]], np.int32)
+    ik8, iks = orc.quantize_e4m3(ik)
+    assert (iks == np.float32(2.0 ** -7)).all()
+    s_bf = orc.indexer_scores(iq, w, ik, pos, m)
+    s_8 = orc.indexer_scores_e4m3(iq, w, ik8, iks, pos, m)
+    np.testing.assert_array_equal(np.isnan(s_8), np.isnan(s_bf))
+    ok = ~np.isnan(s_bf)
+    np.testing.assert_array_equal(s_8[ok], s_bf[ok])
+    iks2 = iks.copy()
+    iks2[1, 2] *= 8
+    s_2 = orc.indexer_scores_e4m3(iq, w, ik8, iks2, pos, m)
+    want = s_8.copy()
+    want[1, :, 2] *= 8
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(s_2[ok], want[ok])
+
+
 # --------------------------------------------------------------------- top-k
 def _pairwise_rule_ok(sc, chosen, n):
     ch = set(chosen)

@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--workload", default="hybrid_decode_1m")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling only)")
     ap.add_argument("--context", type=int, default=0, help="override L (profiling only)")
+    ap.add_argument("--indexer-keys", default="bf16", choices=["bf16", "fp8"],
+                    help="indexer key cache: bf16, or E4M3 codes with a row scale")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dense-sms", type=int, default=0,
@@ -79,30 +81,35 @@ def workload(args):
     return synth.scaled(wl, **kw) if kw else wl
 
 
-def step_bytes(wl):
-    """Algorithmic HBM bytes of one decode step (T=1): indexer keys of every
-    visible entry, the k gathered CSA rows, every visible HCA row, W raw rows,
-    q, iq, w, the output; plus the incremental compression reads/writes."""
-    B, L, D, dI = wl.B, wl.L, wl.D, wl.dI
+def step_bytes(wl, keys="bf16"):
+    """Algorithmic HBM bytes of one decode step with T queries per sequence
+    (the T newest tokens): per sequence, the indexer keys of every visible
+    entry, every visible HCA row and the W+T-1 window rows once (the queries
+    share them); per query, its k gathered CSA rows, q, iq, w and the output;
+    plus the incremental compression reads/writes of the newest entries."""
+    B, L, D, dI, T = wl.B, wl.L, wl.D, wl.dI, wl.T
     n_csa, n_hca = L // wl.m_csa, L // wl.m_hca
     per = 0
     if "csa" in wl.branches:
-        per += n_csa * dI * 2 + min(wl.k, n_csa) * D * 2 + wl.HI * dI * 2 + wl.HI * 4
-        per += wl.w_csa * (D + dI + 1) * 2 + (D + dI) * 2
+        key = dI * 2 if keys == "bf16" else dI + 4
+        per += n_csa * key + T * (min(wl.k, n_csa) * D * 2 + wl.HI * dI * 2 + wl.HI * 4)
+        per += wl.w_csa * (D + dI + 1) * 2 + D * 2 + key
     if "hca" in wl.branches:
         per += n_hca * D * 2 + wl.w_hca * (D + 1) * 2 + D * 2
     if "swa" in wl.branches:
-        per += wl.W * D * 2
-    per += 2 * wl.H * D * 2 + wl.H * 4
+        per += (wl.W + T - 1) * D * 2
+    per += T * (2 * wl.H * D * 2 + wl.H * 4)
     return B * per
 
 
-def indexer_bytes(wl):
+def indexer_bytes(wl, keys="bf16"):
     """Algorithmic bytes of one indexer launch: every visible indexer key
-    read once, the queries and weights, and one fp32 score written per
-    entry."""
+    read once per sequence (its queries share the scan) -- dI bf16 values,
+    or dI E4M3 codes plus an fp32 row scale --, the queries and weights, and
+    one fp32 score written per entry and query."""
     n_csa = wl.L // wl.m_csa
-    return wl.B * (n_csa * (wl.dI * 2 + 4) + wl.HI * wl.dI * 2 + wl.HI * 4)
+    key = wl.dI * 2 if keys == "bf16" else wl.dI + 4
+    return wl.B * (n_csa * (key + 4 * wl.T) + wl.T * (wl.HI * wl.dI * 2 + wl.HI * 4))
 
 
 # DRAM traffic of indexer_score_kernel (dram__bytes_read.sum +
@@ -117,9 +124,11 @@ INDEXER_TRAFFIC = {
 }
 
 
-def indexer_traffic(wl):
+def indexer_traffic(wl, keys="bf16"):
     """Per-launch DRAM bytes scaled from the recorded capture, or None when
     the indexer sources have changed since it was taken."""
+    if keys != "bf16":
+        return None  # the capture is of bf16 keys
     import hashlib
     h = hashlib.sha256()
     for f in INDEXER_TRAFFIC["sources"]:
@@ -127,7 +136,12 @@ def indexer_traffic(wl):
             h.update(fh.read())
     if h.hexdigest() != INDEXER_TRAFFIC["sha256"]:
         return None
+    if wl.T != 1:
+        return None  # the capture is of one query per sequence
     return INDEXER_TRAFFIC["bytes_per_entry"] * wl.B * (wl.L // wl.m_csa)
+
+
+INDEXER_KEYS = {"bf16": "bf16", "fp8": "e4m3 codes + fp32 row scale (queries quantised alike)"}
 
 
 class ClockSampler:
@@ -297,8 +311,9 @@ def cpu_baseline(wl, steps=1):
         oracle_step(wl, s)
     dt = (time.perf_counter() - t0) / steps
     return {"value": 1.0 / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"1 of {wl.B} sequences x 1 decode step of {wl.name} (full 1M-context "
-                      f"sizes: {wl.L // wl.m_csa} indexer entries, top-{wl.k}, "
+            "sample": f"1 query of 1 of {wl.B} sequences, 1 decode step of {wl.name} at "
+                      f"full size ({wl.L}-token context: {wl.L // wl.m_csa} indexer entries, "
+                      f"top-{wl.k}, "
                       f"{wl.L // wl.m_hca} HCA entries, {wl.W} SWA tokens), single-threaded "
                       "fp64 C, seeded synthetic caches",
             "seconds_per_token": dt}
@@ -356,12 +371,12 @@ def run_reference(args, world, rank, budget_s=150.0):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(wl, **extra):
+def config_dict(wl, keys="bf16", **extra):
     d = {"workload": wl.name, "batch": wl.B, "context_tokens": wl.L, "queries_per_seq": wl.T,
          "heads": wl.H, "head_dim": wl.D, "rope_dims": wl.r, "indexer": f"{wl.HI}x{wl.dI}",
          "top_k": wl.k, "csa_entries": wl.L // wl.m_csa, "hca_entries": wl.L // wl.m_hca,
          "swa_window": wl.W, "branches": list(wl.branches),
-         "l2": f"per-step input {step_bytes(wl) / 1e6:.1f} MB > 126 MB L2 (no flush)"}
+         "l2": f"per-step input {step_bytes(wl, keys) / 1e6:.1f} MB > 126 MB L2 (no flush)"}
     d.update(extra)
     return d
 
@@ -377,7 +392,7 @@ def run_ours(args, world, rank, local):
     wl = workload(args)
     inp = synth.make_inputs(wl, seed=0, device=dev)
     raw = {k: inp[k] for k in ["kv_raw", "ik_raw", "gate_csa", "gate_hca"]}
-    layer = HybridLayer(wl, raw, device=dev)
+    layer = HybridLayer(wl, raw, device=dev, indexer_keys=args.indexer_keys)
     layer.override_dense_sms = args.dense_sms
     q, iq, w, pos, sink = inp["q"], inp["iq"], inp["w"], inp["pos"], inp["sink"]
     t_new = wl.L - 1
@@ -441,13 +456,14 @@ def run_ours(args, world, rank, local):
                   for n in names}
 
     hbm, bf16, src = peaks()
-    ib = indexer_bytes(wl)
+    keys = args.indexer_keys
+    ib = indexer_bytes(wl, keys)
     idx_ms = per_kernel["indexer"]
     achieved = ib / (idx_ms / 1e3) / 1e9
-    sb = step_bytes(wl)
+    sb = step_bytes(wl, keys)
     roofline = {"bound": "hbm", "kernel": "indexer_score_kernel", "achieved": achieved,
                 "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": indexer_traffic(wl),
+                "traffic": indexer_traffic(wl, keys),
                 "traffic_source": "ncu dram bytes of an 8 x 65,536-entry launch scaled by "
                                   "entries (" + INDEXER_TRAFFIC["profile"] + ")",
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
@@ -467,9 +483,11 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(wl, parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
-                              step_roofline=step_roof,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if keys == "bf16" else "bf16 (indexer QK: e4m3)", "data": "synthetic",
+        "config": config_dict(wl, keys,
+                              parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
+                              step_roofline=step_roof, indexer_keys=INDEXER_KEYS[keys],
                               per_call_ms=per_kernel),
         "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
     }
@@ -484,9 +502,9 @@ def run_ours(args, world, rank, local):
 def run_e2e(args, world, layer, inp, wl, t_new, stream, side):
     """The same steps with every step's inputs coming from pinned host memory
     and its result going back, inside the timed region.  A step's inputs (q,
-    iq, w, pos and the new token's raw KV, indexer key and gate logits) are
+    iq, w, pos and the new tokens' raw KV, indexer keys and gate logits) are
     packed in one pinned buffer and moved by one host-to-device copy; the
-    token rows are then placed in the caches on the device, and out and lse
+    new tokens' rows are then placed in the caches on the device, and out and lse
     (adjacent in one device buffer) come back by one device-to-host copy.
     Inputs and results are double-buffered so these copies overlap the
     compute of the neighbouring steps, as a serving loop would run them."""
@@ -494,9 +512,10 @@ def run_e2e(args, world, layer, inp, wl, t_new, stream, side):
     K = args.steps
     dev = inp["q"].device
     raw = layer.raw
+    new = slice(t_new - wl.T + 1, t_new + 1)  # the step's new tokens
     parts = [("q", inp["q"]), ("iq", inp["iq"]), ("w", inp["w"]), ("pos", inp["pos"]),
-             ("kv", inp["kv_raw"][:, t_new]), ("ik", inp["ik_raw"][:, t_new]),
-             ("gc", inp["gate_csa"][:, t_new]), ("gh", inp["gate_hca"][:, t_new])]
+             ("kv", inp["kv_raw"][:, new]), ("ik", inp["ik_raw"][:, new]),
+             ("gc", inp["gate_csa"][:, new]), ("gh", inp["gate_hca"][:, new])]
     offs, total = {}, 0
     for name, t in parts:
         nbytes = t.numel() * t.element_size()
@@ -544,7 +563,7 @@ def run_e2e(args, world, layer, inp, wl, t_new, stream, side):
             stream.wait_event(in_ready[i])
             for name, cache in [("kv", "kv_raw"), ("ik", "ik_raw"), ("gc", "gate_csa"),
                                 ("gh", "gate_hca")]:
-                raw[cache][:, t_new].copy_(view(buf, name))
+                raw[cache][:, new].copy_(view(buf, name))
             layer.step(view(buf, "q"), view(buf, "iq"), view(buf, "w"), view(buf, "pos"),
                        inp["sink"], t_new=t_new, side_stream=side)
             if i >= 2:

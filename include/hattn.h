@@ -93,6 +93,32 @@ HATTN_API int hattn_hca_compress(const void* kv_raw, const void* gate, const flo
                        hattn_stream_t stream);
 
 /* -------------------------------------------------------------------------
+ * FP8 indexer keys.  [AT] "Inference efficiency": the indexer's QK path runs
+ * in low precision.  The pages name no format; this library stores E4M3
+ * codes (OCP FP8: bias 7, 3 mantissa bits, largest finite 448, saturating)
+ * with one fp32 scale per row:
+ *   amax = max_i |x_i|, inv = 448 / amax, code_i = e4m3_rne(x_i * inv),
+ *   scale = amax / 448 (each step one correctly rounded fp32 operation);
+ * the row decodes as code_i * scale.  A zero row has zero codes, scale 0.
+ *
+ * hattn_quantize_e4m3: rows x n bf16 -> codes [rows][n] (bytes) and
+ *   scales [rows] fp32; n a multiple of 4.  Used to build an FP8 key cache
+ *   from bf16 keys.
+ * hattn_csa_compress_fp8: hattn_csa_compress that also writes each entry's
+ *   indexer key as E4M3 codes ik8 [B][N_cap][dI] and scale ik_scale
+ *   [B][N_cap] fp32, quantised from the bf16-rounded key (the value ik_c
+ *   holds); ik_c may be NULL (then only the FP8 key is written).
+ * ---------------------------------------------------------------------- */
+HATTN_API int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* codes, float* scales,
+                                  hattn_stream_t stream);
+HATTN_API int hattn_csa_compress_fp8(const void* kv_raw, const void* ik_raw, const void* gate,
+                                     const float* gamma_kv, int B, int64_t L_cap, int D, int dI,
+                                     int m, int w, int r, float rope_base, float eps,
+                                     int64_t j_begin, int64_t j_end, void* kv_c, void* ik_c,
+                                     void* ik8, float* ik_scale, int64_t N_cap,
+                                     hattn_stream_t stream);
+
+/* -------------------------------------------------------------------------
  * Lightning indexer + per-query top-k.  [DD]: CSA keeps the top-1024 (Pro) /
  * top-512 (Flash) compressed entries per query.  [AT] "Design overview": the
  * V3.2 lightning-indexer sparse attention.
@@ -159,6 +185,23 @@ HATTN_API int hattn_indexer_scores_ex(const void* iq, const float* w, const void
 HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T,
                                 int64_t N_cap, int k, int m, int32_t* idx_out,
                                 hattn_stream_t stream);
+
+/* hattn_indexer_scores_ex over FP8 keys: ik8 [B][N_cap][128] E4M3 codes and
+ * ik_scale [B][N_cap] fp32 (see hattn_quantize_e4m3; dI must be 128 and
+ * N_cap a multiple of 4, so that a block's scales are whole 16-byte rows).  Each
+ * bf16 query row iq[b][t][h] is quantised the same way inside the kernel,
+ * and the score is the plain definition over the decoded values,
+ *   I[j] = sum_h w[b][t][h] * max(0, q^[b][t][h] . k^[b][j]),
+ * computed as ik_scale[j] * sum_h (w * q_scale_h) * max(0, q8_h . k8_j) with
+ * the code products on the tensor cores (fp32 accumulation).  Scores go to
+ * score_out as for hattn_indexer_scores; n_sms and fresh_from as for
+ * hattn_indexer_scores_ex.  The key stream is 132 bytes per entry instead of
+ * 256. */
+HATTN_API int hattn_indexer_scores_fp8(const void* iq, const float* w, const void* ik8,
+                                       const float* ik_scale, const int32_t* pos, int B, int T,
+                                       int HI, int dI, int64_t N_cap, int m, int n_sms,
+                                       int64_t fresh_from, float* score_out,
+                                       hattn_stream_t stream);
 
 /* -------------------------------------------------------------------------
  * Query preparation.  [AT] "Design overview": RMSNorm on the queries;

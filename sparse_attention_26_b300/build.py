@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libhattn.so")
 SOURCES = ["abi.cu", "compress.cu", "indexer.cu", "topk.cu", "qprep.cu", "attention.cu",
-           "merge.cu"]
+           "merge.cu", "quant.cu"]
 HEADERS = ["common.cuh", "kernels.h", os.path.join("..", "..", "include", "hattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

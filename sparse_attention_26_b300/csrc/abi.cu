@@ -95,7 +95,9 @@ EncodeTiledFn encode_fn() {
 // bf16 tensor map, 128-byte swizzle.  dims/strides innermost first; strides
 // in bytes for dims 1..rank-1.
 int make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims,
-              const uint64_t* strides, const uint32_t* box, const char* what) {
+              const uint64_t* strides, const uint32_t* box, const char* what,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(HATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t gd[5], gs[4];
@@ -106,8 +108,8 @@ int make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims,
     es[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
-  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bx,
-                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(tm, dtype, rank, const_cast<void*>(base), gd, gs, bx,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(HATTN_ERR_CUDA, "tensor map for %s: CUresult %d", what, (int)r);
   return HATTN_OK;
@@ -138,15 +140,22 @@ int check_rope(int D, int r, float rope_base, float eps) {
 int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
                     const float* gamma_kv, int B, int64_t L_cap, int D, int dI, int m, int w,
                     int r, float rope_base, float eps, int64_t j_begin, int64_t j_end, void* kv_c,
-                    void* ik_c, int64_t N_cap, hattn_stream_t stream) {
+                    void* ik_c, int64_t N_cap, hattn_stream_t stream, void* ik8 = nullptr,
+                    float* ik_scale = nullptr) {
   REQUIRE_PTR(kv_raw);
   REQUIRE_PTR(gate);
   REQUIRE_PTR(kv_c);
   REQUIRE_F32(gamma_kv);
-  REQUIRE((ik_raw == nullptr) == (ik_c == nullptr), "ik_raw and ik_c must both be given or both NULL");
+  REQUIRE((ik8 == nullptr) == (ik_scale == nullptr), "ik8 and ik_scale must both be given or both NULL");
+  REQUIRE((ik_raw == nullptr) == (ik_c == nullptr && ik8 == nullptr),
+          "ik_raw needs an indexer-key output (ik_c or ik8), and an output needs ik_raw");
   if (ik_raw) {
     REQUIRE_PTR(ik_raw);
-    REQUIRE_PTR(ik_c);
+    if (ik_c) REQUIRE_PTR(ik_c);
+    if (ik8) {
+      REQUIRE_PTR(ik8);
+      REQUIRE_PTR(ik_scale);
+    }
     REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
   }
   REQUIRE(B >= 1 && L_cap >= 1 && N_cap >= 1, "B, L_cap and N_cap must be >= 1");
@@ -166,6 +175,8 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
   a.gamma = gamma_kv;
   a.kv_out = static_cast<__nv_bfloat16*>(kv_c);
   a.ik_out = static_cast<__nv_bfloat16*>(ik_c);
+  a.ik8_out = static_cast<uint8_t*>(ik8);
+  a.ik_scale_out = ik_scale;
   a.B = B;
   a.D = D;
   a.dI = ik_raw ? dI : 0;
@@ -440,6 +451,33 @@ int hattn_csa_compress(const void* kv_raw, const void* ik_raw, const void* gate,
                          j_begin, j_end, kv_c, ik_c, N_cap, stream);
 }
 
+int hattn_csa_compress_fp8(const void* kv_raw, const void* ik_raw, const void* gate,
+                           const float* gamma_kv, int B, int64_t L_cap, int D, int dI, int m,
+                           int w, int r, float rope_base, float eps, int64_t j_begin,
+                           int64_t j_end, void* kv_c, void* ik_c, void* ik8, float* ik_scale,
+                           int64_t N_cap, hattn_stream_t stream) {
+  REQUIRE_PTR(ik_raw);
+  REQUIRE_PTR(ik8);
+  REQUIRE_PTR(ik_scale);
+  return compress_common(kv_raw, ik_raw, gate, gamma_kv, B, L_cap, D, dI, m, w, r, rope_base, eps,
+                         j_begin, j_end, kv_c, ik_c, N_cap, stream, ik8, ik_scale);
+}
+
+int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* codes, float* scales,
+                        hattn_stream_t stream) {
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(codes);
+  REQUIRE_PTR(scales);
+  REQUIRE(rows >= 0, "rows must be >= 0");
+  REQUIRE(n >= 4 && n % 4 == 0 && n <= (1 << 20), "n=%d must be a multiple of 4 in [4, 2^20]", n);
+  if (rows == 0) return ok();
+  cudaError_t e = launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(x), rows, n,
+                                       static_cast<uint8_t*>(codes), scales, num_sms_or_default(),
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return ok();
+}
+
 int hattn_hca_compress(const void* kv_raw, const void* gate, const float* gamma_kv, int B,
                        int64_t L_cap, int D, int m, int r, float rope_base, float eps,
                        int64_t j_begin, int64_t j_end, void* kv_h, int64_t N_cap,
@@ -459,9 +497,12 @@ size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
 
 namespace {
 
+// Scores of bf16 indexer keys (ik_c), or of E4M3 keys when k_scale is given
+// (ik_c then holds the codes, [B][N_cap][128] bytes).
 int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
                         int B, int T, int HI, int dI, int64_t N_cap, int m, float* scores,
-                        hattn_stream_t stream, int n_sms = 0, int64_t fresh_from = -1) {
+                        hattn_stream_t stream, int n_sms = 0, int64_t fresh_from = -1,
+                        const float* k_scale = nullptr) {
   REQUIRE_PTR(iq);
   REQUIRE_PTR(w);
   REQUIRE_PTR(ik_c);
@@ -473,19 +514,39 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   REQUIRE(m >= 1, "m must be >= 1");
   REQUIRE((int64_t)B * T * HI < (1ll << 31), "too many query heads");
   REQUIRE(n_sms >= 0, "n_sms=%d must be >= 0", n_sms);
+  const bool f8 = k_scale != nullptr;
+  if (f8) {
+    REQUIRE(dI == 128, "FP8 indexer keys need dI = 128 (one 128-byte row), got %d", dI);
+    REQUIRE(N_cap % 4 == 0, "FP8 indexer keys need N_cap %% 4 == 0 (16-byte scale rows), got %lld",
+            (long long)N_cap);
+  }
   IndexerPlan ip;
-  if (!plan_indexer(T, HI, dI, &ip))
+  if (!plan_indexer(T, HI, dI, f8, &ip))
     return fail(HATTN_ERR_UNSUPPORTED, "no indexer kernel for HI=%d dI=%d", HI, dI);
   int sms = 0;
   int* status = nullptr;
   if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
-  CUtensorMap tm_ik, tm_iq;
-  {
+  CUtensorMap tm_ik, tm_iq, tm_ks;
+  if (f8) {
+    const uint64_t dims[3] = {128, (uint64_t)N_cap, (uint64_t)B};
+    const uint64_t strides[2] = {128, (uint64_t)N_cap * 128};
+    const uint32_t box[3] = {128, 128, 1};
+    int rc = make_tmap(&tm_ik, ik_c, 3, dims, strides, box, "ik8", CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    if (rc) return rc;
+    // the 128 row scales of a key block, beside its codes
+    const uint64_t sdims[2] = {(uint64_t)N_cap, (uint64_t)B};
+    const uint64_t sstrides[1] = {(uint64_t)N_cap * 4};
+    const uint32_t sbox[2] = {128, 1};
+    rc = make_tmap(&tm_ks, k_scale, 2, sdims, sstrides, sbox, "ik_scale",
+                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  } else {
     const uint64_t dims[3] = {(uint64_t)dI, (uint64_t)N_cap, (uint64_t)B};
     const uint64_t strides[2] = {(uint64_t)dI * 2, (uint64_t)N_cap * dI * 2};
     const uint32_t box[3] = {64, 128, 1};
     int rc = make_tmap(&tm_ik, ik_c, 3, dims, strides, box, "ik_c");
     if (rc) return rc;
+    tm_ks = tm_ik;  // unused without FP8 keys
   }
   {
     const uint64_t dims[2] = {(uint64_t)dI, (uint64_t)B * T * HI};
@@ -508,6 +569,7 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   a.NQ = ip.NQ;
   a.KC = ip.KC;
   a.stages = ip.stages;
+  a.nacc = ip.nacc;
   a.groups_per_seq = (T + ip.G - 1) / ip.G;
   a.nblk = static_cast<int>((N_cap + 127) / 128);
   a.fresh_from = fresh_from;
@@ -517,7 +579,8 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   // that concurrent work keeps the others)
   if (n_sms > 0 && n_sms < sms) sms = n_sms;
   const int grid = static_cast<int>(a.total_slots < sms ? a.total_slots : sms);
-  cudaError_t e = launch_indexer_score(tm_ik, tm_iq, a, ip, grid, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      launch_indexer_score(tm_ik, tm_iq, tm_ks, a, ip, f8, grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
   return ok();
 }
@@ -595,6 +658,15 @@ int hattn_indexer_scores_ex(const void* iq, const float* w, const void* ik_c,
                             hattn_stream_t stream) {
   return indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms,
                              fresh_from < 0 ? -1 : fresh_from);
+}
+
+int hattn_indexer_scores_fp8(const void* iq, const float* w, const void* ik8,
+                             const float* ik_scale, const int32_t* pos, int B, int T, int HI,
+                             int dI, int64_t N_cap, int m, int n_sms, int64_t fresh_from,
+                             float* score_out, hattn_stream_t stream) {
+  REQUIRE_PTR(ik_scale);
+  return indexer_scores_impl(iq, w, ik8, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms,
+                             fresh_from < 0 ? -1 : fresh_from, ik_scale);
 }
 
 int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T, int64_t N_cap, int k,

@@ -273,6 +273,18 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], kind::f8f6f4 with the formats the
+// instruction descriptor names (E4M3 here), fp32 accumulate; K = 32 per call.
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when all previously issued tcgen05 async
 // operations of this thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -344,6 +356,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor, kind::f8f6f4 with E4M3 A/B (format code 0), fp32
+// D, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // Byte offset of the 16-byte piece `piece` (0..7) of row `row` inside a
 // 128-byte-swizzled tile whose 8-row atoms are 1024 bytes apart.
 __host__ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t piece) {
@@ -353,6 +373,35 @@ __host__ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t piece
 // ----------------------------------------------------------------- math
 __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// ----------------------------------------------------------------- FP8 (E4M3)
+// Two fp32 values to E4M3 codes, nearest even, saturating at +-448: `lo` in
+// bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Scaling of one E4M3 row: codes of x * inv decode as code * scale, with
+// inv = 448 / amax and scale = amax / 448, each correctly rounded in fp32.
+// A zero row has inv = scale = 0 (all codes 0).
+struct E4m3Row {
+  float inv, scale;
+};
+__device__ __forceinline__ E4m3Row e4m3_row(float amax) {
+  E4m3Row s;
+  s.inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+  s.scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
+  return s;
+}
+
+// Four codes of x[0..3] * inv packed little-endian (zero when inv is 0).
+__device__ __forceinline__ uint32_t e4m3x4(const float* x, float inv) {
+  if (inv == 0.f) return 0u;
+  return e4m3x2(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv)) |
+         (e4m3x2(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv)) << 16);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

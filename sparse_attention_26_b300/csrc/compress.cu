@@ -47,13 +47,34 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&y)[8]) {
   *reinterpret_cast<uint4*>(p) = u;
 }
 
+// Largest magnitude of the bf16-rounded values of one 8-wide piece.
+__device__ __forceinline__ float amax8_bf16(const float (&y)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(bf16_round(y[e])));
+  return m;
+}
+
+// E4M3 codes of the bf16-rounded values of one 8-wide piece (the values the
+// bf16 indexer key holds), scaled by the row's inv.
+__device__ __forceinline__ void store8_e4m3(uint8_t* p, const float (&y)[8], float inv) {
+  float r[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) r[e] = bf16_round(y[e]);
+  uint2 u;
+  u.x = e4m3x4(r, inv);
+  u.y = e4m3x4(r + 4, inv);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
 __global__ void __launch_bounds__(kCompressThreads)
     compress_kernel(const __grid_constant__ CompressArgs a) {
   __shared__ float alpha[kMaxW];
   __shared__ float partial[4096];  // S x (D + dI) floats, S * NC <= 512 -> <= 4096
   __shared__ float rc[4][kMaxRopePairs];
   __shared__ float red[kCompressThreads / 32];
-  __shared__ float inv_rms_s;
+  __shared__ float red_am[kCompressThreads / 32];
+  __shared__ float inv_rms_s, amax_s;
 
   pdl_trigger();  // a dependent launch after this kernel may begin
   const int tid = threadIdx.x;
@@ -165,27 +186,41 @@ __global__ void __launch_bounds__(kCompressThreads)
     }
     __syncthreads();
 
-    // reduce the slices (fixed order), RMS over the KV part
+    // reduce the slices (fixed order), RMS over the KV part, largest
+    // magnitude of the indexer key (for its E4M3 codes)
     float v[8];
-    float ss = 0.f;
+    float ss = 0.f, am = 0.f;
     if (tid < NC) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = 0.f;
       for (int s = 0; s < S; ++s)
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] += partial[s * width + tid * 8 + e];
-      if (tid < NCk)
+      if (tid < NCk) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+      } else if (a.ik8_out) {
+        am = amax8_bf16(v);
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    for (int o = 16; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    }
+    if ((tid & 31) == 0) {
+      red[tid >> 5] = ss;
+      red_am[tid >> 5] = am;
+    }
     __syncthreads();
     if (tid == 0) {
-      float t = 0.f;
-      for (int i = 0; i < kCompressThreads / 32; ++i) t += red[i];
+      float t = 0.f, mx = 0.f;
+      for (int i = 0; i < kCompressThreads / 32; ++i) {
+        t += red[i];
+        mx = fmaxf(mx, red_am[i]);
+      }
       inv_rms_s = rsqrtf(t / static_cast<float>(a.D) + a.eps);
+      amax_s = mx;
     }
     __syncthreads();
 
@@ -212,7 +247,13 @@ __global__ void __launch_bounds__(kCompressThreads)
       }
       store8(a.kv_out + ((int64_t)b * a.N_cap + j) * a.D + tid * 8, y);
     } else if (tid < NC) {
-      store8(a.ik_out + ((int64_t)b * a.N_cap + j) * a.dI + (tid - NCk) * 8, v);
+      const int64_t row = (int64_t)b * a.N_cap + j;
+      if (a.ik_out) store8(a.ik_out + row * a.dI + (tid - NCk) * 8, v);
+      if (a.ik8_out) {
+        const E4m3Row q = e4m3_row(amax_s);
+        store8_e4m3(a.ik8_out + row * a.dI + (tid - NCk) * 8, v, q.inv);
+        if (tid == NCk) a.ik_scale_out[row] = q.scale;
+      }
     }
     __syncthreads();
   }
@@ -231,6 +272,7 @@ __global__ void __launch_bounds__(kSmallThreads)
   __shared__ float alpha[kSmallMaxW];
   __shared__ float rc[4][kMaxRopePairs];
   __shared__ float red[kSmallThreads / 32];
+  __shared__ float red_am[kSmallThreads / 32];
   pdl_trigger();  // a dependent launch after this kernel may begin
   const int tid = threadIdx.x;
   const int NCk = a.D / 8;
@@ -277,7 +319,7 @@ __global__ void __launch_bounds__(kSmallThreads)
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    float ss = 0.f;
+    float ss = 0.f, am = 0.f;
     if (tid < NC) {
 #pragma unroll
       for (int q = 0; q < kSmallMaxW; ++q) {
@@ -290,18 +332,30 @@ __global__ void __launch_bounds__(kSmallThreads)
           acc[2 * e + 1] = fmaf(al, f.y, acc[2 * e + 1]);
         }
       }
-      if (tid < NCk)
+      if (tid < NCk) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) ss = fmaf(acc[e], acc[e], ss);
+      } else if (a.ik8_out) {
+        am = amax8_bf16(acc);
+      }
     }
-    // RMS over the KV part
+    // RMS over the KV part, largest magnitude of the indexer key
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    for (int o = 16; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    }
+    if ((tid & 31) == 0) {
+      red[tid >> 5] = ss;
+      red_am[tid >> 5] = am;
+    }
     __syncthreads();
-    float tot = 0.f;
+    float tot = 0.f, amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < kSmallThreads / 32; ++i) tot += red[i];
+    for (int i = 0; i < kSmallThreads / 32; ++i) {
+      tot += red[i];
+      amax = fmaxf(amax, red_am[i]);
+    }
     const float inv = rsqrtf(tot / static_cast<float>(a.D) + a.eps);
     if (tid < NCk) {
       float y[8];
@@ -325,7 +379,13 @@ __global__ void __launch_bounds__(kSmallThreads)
       }
       store8(a.kv_out + ((int64_t)b * a.N_cap + j) * a.D + tid * 8, y);
     } else if (tid < NC) {
-      store8(a.ik_out + ((int64_t)b * a.N_cap + j) * a.dI + (tid - NCk) * 8, acc);
+      const int64_t row = (int64_t)b * a.N_cap + j;
+      if (a.ik_out) store8(a.ik_out + row * a.dI + (tid - NCk) * 8, acc);
+      if (a.ik8_out) {
+        const E4m3Row q = e4m3_row(amax);
+        store8_e4m3(a.ik8_out + row * a.dI + (tid - NCk) * 8, acc, q.inv);
+        if (tid == NCk) a.ik_scale_out[row] = q.scale;
+      }
     }
     __syncthreads();  // alpha and red are rewritten by the next entry
   }

@@ -13,10 +13,21 @@
 // Work = (query group, 128-entry block) slots, flattened and split evenly
 // over a grid of one CTA per SM.  Roles: warp 0 issues TMA loads of key
 // blocks (128B-swizzled, a ring of `stages` buffers) and of the group's
-// queries; warp 1 issues the MMAs (M=128, N=NQ, K=16 steps) into one of two
-// tensor-memory accumulators; warps 2-5 drain an accumulator (tcgen05.ld),
-// reduce it and write fp32 scores with coalesced stores.  HBM traffic is the
-// key blocks once plus the scores.
+// queries; warps 1 and 2 issue the MMAs (M=128, N=NQ) of alternate slots
+// into a ring of `nacc` tensor-memory accumulators; kEpiGroups groups of
+// four warps drain alternate accumulators (tcgen05.ld), reduce them and
+// write fp32 scores with coalesced stores.  HBM traffic is the key blocks
+// once plus the scores.
+//
+// FP8 keys ("DeepSeek-V4" atlas spec sheet, "Inference efficiency": the
+// indexer QK path runs in low precision): each key is 128 E4M3 codes (one
+// 128-byte swizzle row) with an fp32 row scale s_j.  The epilogue warps
+// quantise the group's bf16 query rows the same way in shared memory
+// (codes plus a scale s_h per row), the MMAs run kind::f8f6f4 (K = 32 per
+// call, 4 calls per block), and since both scales are positive,
+//     I(t, j) = s_j * sum_h (w[t,h] * s_h) * max(0, q8_h . k8_j),
+// so the scales cost one multiply per column weight and one per score.
+// A key costs 128 + 4 bytes instead of 256.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,24 +35,35 @@ namespace hattn {
 
 namespace {
 
-constexpr int kIdxThreads = 224;  // producer, MMA (even slots), 4 epilogue warps, MMA (odd slots)
+// warps: 0 producer, 1 and 2 MMA issuers (even / odd slots), then
+// kEpiGroups x 4 epilogue warps (any 4 consecutive warps cover the four
+// 32-lane quarters of tensor memory)
+constexpr int kEpiGroups = 2;
+constexpr int kEpiWarps = 4 * kEpiGroups;
+constexpr int kFirstEpiWarp = 3;
+constexpr int kIdxThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kBlockRows = 128;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
+constexpr int kMaxStagesBf16 = 8;
+constexpr int kMaxAcc = 4;  // accumulators in flight (TMEM columns permitting)
 
 struct IdxSmem {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t sempty[kMaxStages];  // FP8: the epilogue has read the stage's key scales
+  uint64_t tfull[kMaxAcc];
+  uint64_t tempty[kMaxAcc];
   uint64_t qfull;
   uint64_t qempty;
+  uint64_t q8full;  // FP8 keys: the group's query codes and scales are in place
   uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
   // per epilogue warp (no cross-warp barrier): visible entries per query of
   // the current group, and the head weight of every accumulator column
-  int nt[4][256];
-  alignas(16) float wcol[4][256];
+  int nt[kEpiWarps][256];
+  alignas(16) float wcol[kEpiWarps][256];
+  float qscale[256];  // FP8 keys: scale of each query row
 };
 
 __device__ __forceinline__ int64_t visible_entries(int32_t t, int m, int64_t cap) {
@@ -94,18 +116,49 @@ struct SlotCursor {
   }
 };
 
+// Quantises the group's bf16 query rows (sQ, 128B-swizzled 64-dim chunks)
+// to E4M3 codes in sQ8 (one 128-byte swizzled row each) and their scales;
+// epilogue warp e takes rows e, e + kEpiWarps, ...  Lane l holds dims
+// 4l .. 4l+3 of a row.
+__device__ __forceinline__ void quantize_query_rows(const uint8_t* sQ, uint8_t* sQ8,
+                                                    float* qscale, int NQ, int ew, int lane) {
+  const int d = 4 * lane;
+  const uint32_t src_off = static_cast<uint32_t>(d >> 6) * NQ * 128u;
+  const uint32_t piece = (d & 63) >> 3, within = (d & 7) * 2;
+  for (int r = ew; r < NQ; r += kEpiWarps) {
+    const uint2 u = *reinterpret_cast<const uint2*>(sQ + src_off + swz128(r, piece) + within);
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    const float v[4] = {f0.x, f0.y, f1.x, f1.y};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const E4m3Row q = e4m3_row(amax);
+    *reinterpret_cast<uint32_t*>(sQ8 + swz128(r, lane >> 2) + 4 * (lane & 3)) = e4m3x4(v, q.inv);
+    if (lane == 0) qscale[r] = q.scale;
+  }
+}
+
+template <bool F8>
 __global__ void __launch_bounds__(kIdxThreads, 1)
     indexer_score_kernel(const __grid_constant__ CUtensorMap tm_ik,
-                         const __grid_constant__ CUtensorMap tm_iq, const IndexerArgs a) {
+                         const __grid_constant__ CUtensorMap tm_iq,
+                         const __grid_constant__ CUtensorMap tm_ks, const IndexerArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128B-swizzled operand buffers
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  // [E4M3 query rows (FP8 keys)] [bf16 query rows] [key stages]
+  // [key scales of each stage (FP8 keys)] [IdxSmem]
+  const uint32_t q8_bytes = F8 ? static_cast<uint32_t>(a.NQ) * 128u : 0u;
   const uint32_t q_bytes = static_cast<uint32_t>(a.KC) * a.NQ * 128u;
-  const uint32_t stage_bytes = static_cast<uint32_t>(a.KC) * 16384u;
-  uint8_t* sQ = base;
-  uint8_t* sA = base + q_bytes;
-  IdxSmem* sm = reinterpret_cast<IdxSmem*>(sA + a.stages * stage_bytes);
+  const uint32_t stage_bytes = F8 ? 16384u : static_cast<uint32_t>(a.KC) * 16384u;
+  uint8_t* sQ8 = base;
+  uint8_t* sQ = base + q8_bytes;
+  uint8_t* sA = sQ + q_bytes;
+  float* sScale = reinterpret_cast<float*>(sA + a.stages * stage_bytes);
+  IdxSmem* sm = reinterpret_cast<IdxSmem*>(sA + a.stages * stage_bytes +
+                                           (F8 ? a.stages * kBlockRows * 4 : 0));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -118,21 +171,26 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     for (int i = 0; i < a.stages; ++i) {
       mbar_init(smem_u32(&sm->full[i]), 1);
       mbar_init(smem_u32(&sm->empty[i]), 1);
+      mbar_init(smem_u32(&sm->sempty[i]), 4);  // the four warps of the slot's epilogue group
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < a.nacc; ++i) {
       mbar_init(smem_u32(&sm->tfull[i]), 1);
-      mbar_init(smem_u32(&sm->tempty[i]), 128);
+      mbar_init(smem_u32(&sm->tempty[i]), 128);  // the four warps of one epilogue group
     }
     mbar_init(smem_u32(&sm->qfull), 1);
     mbar_init(smem_u32(&sm->qempty), 2);  // both MMA issuers leave the query block
+    mbar_init(smem_u32(&sm->q8full), kEpiWarps);  // each epilogue warp quantised its rows
     mbar_init(smem_u32(&sm->mma_done[0]), 1);
     mbar_init(smem_u32(&sm->mma_done[1]), 1);
     sm->abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_ik);
     tma_prefetch_desc(&tm_iq);
+    if (F8) tma_prefetch_desc(&tm_ks);
   }
-  const uint32_t tmem_cols = (2 * a.NQ <= 32) ? 32 : (2 * a.NQ <= 64 ? 64 : (2 * a.NQ <= 128 ? 128 : (2 * a.NQ <= 256 ? 256 : 512)));
+  const int acc_cols = a.nacc * a.NQ;
+  const uint32_t tmem_cols = acc_cols <= 32 ? 32 : (acc_cols <= 64 ? 64 : (acc_cols <= 128 ? 128 : (acc_cols <= 256 ? 256 : 512)));
+  const int acc_mask = a.nacc - 1, acc_shift = a.nacc == 2 ? 1 : (a.nacc == 4 ? 2 : 3);
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm->tmem_base), tmem_cols);
     tmem_relinquish();
@@ -167,9 +225,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           ++qloads;
           loaded = cur.group;
         }
-        // stage st was last filled `stages` uses ago, in phase ph ^ 1
+        // stage st was last filled `stages` uses ago, in phase ph ^ 1; with
+        // FP8 keys its scales are also read by the epilogue, which lags the MMAs
         if (it >= a.stages &&
             !mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 11))
+          break;
+        if (F8 && it >= a.stages &&
+            !mbar_wait(smem_u32(&sm->sempty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 20))
           break;
         if (!keys_ready &&
             (a.fresh_from < 0 || static_cast<int64_t>(cur.blk + 1) * kBlockRows > a.fresh_from)) {
@@ -180,10 +242,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           keys_ready = true;
         }
         const uint32_t fb = smem_u32(&sm->full[st]);
-        mbar_arrive_expect_tx(fb, stage_bytes);
-        for (int kc = 0; kc < a.KC; ++kc)
-          tma_load_3d(smem_u32(sA + st * stage_bytes + kc * 16384), &tm_ik, kc * 64,
-                      cur.blk * kBlockRows, cur.b, fb);
+        mbar_arrive_expect_tx(fb, stage_bytes + (F8 ? kBlockRows * 4 : 0));
+        if (F8) {
+          tma_load_3d(smem_u32(sA + st * stage_bytes), &tm_ik, 0, cur.blk * kBlockRows, cur.b, fb);
+          tma_load_2d(smem_u32(sScale + st * kBlockRows), &tm_ks, cur.blk * kBlockRows, cur.b, fb);
+        } else
+          for (int kc = 0; kc < a.KC; ++kc)
+            tma_load_3d(smem_u32(sA + st * stage_bytes + kc * 16384), &tm_ik, kc * 64,
+                        cur.blk * kBlockRows, cur.b, fb);
         ++it;
         if (++st == a.stages) { st = 0; ph ^= 1u; }
       }
@@ -195,15 +261,18 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                     10000000ull, 12);
       }
     }
-  } else if (warp == 1 || warp == 6) {
+  } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
-    // Warp 1 issues the products of the even live slots (accumulator 0) and
-    // warp 6 those of the odd ones (accumulator 1): a single thread issues a
-    // chained tcgen05.mma only every ~64 ns, close to a slot's share of the
-    // key stream, so two issuers keep the tensor core ahead of it.
+    // Warp 1 issues the products of the even live slots and warp 2 those of
+    // the odd ones: a single thread issues a chained tcgen05.mma only every
+    // ~64 ns, close to a slot's share of the key stream, so two issuers keep
+    // the tensor core ahead of it.  Slot `it` accumulates into accumulator
+    // it % nacc, its (it / nacc)-th use.
     const int par = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, a.NQ, 0, 0);
+      const uint32_t idesc = F8 ? idesc_e4m3(128, a.NQ) : idesc_bf16(128, a.NQ, 0, 0);
+      // the operand rows the products read: E4M3 codes, or the bf16 rows
+      const uint64_t qbar = smem_u32(F8 ? &sm->q8full : &sm->qfull);
       SlotCursor cur;
       int st = 0;
       uint32_t ph = 0;
@@ -212,27 +281,41 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (!cur.live()) continue;
         if (cur.group != loaded) {
           if (qn > 0) mma_commit(smem_u32(&sm->qempty));  // previous group's reads of sQ done
-          if (!mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 13)) break;
+          if (!mbar_wait(static_cast<uint32_t>(qbar), qn & 1, abort, a.status, kWaitLimitNs, 13))
+            break;
           ++qn;
           loaded = cur.group;
         }
-        const int acc = static_cast<int>(it & 1);
-        if (acc == par) {
-          if (it >= 2 &&
-              !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> 1) + 1) & 1, abort, a.status,
-                         kWaitLimitNs, 14))
+        const int acc = static_cast<int>(it & acc_mask);
+        if (static_cast<int>(it & 1) == par) {
+          // the accumulator's previous use has been drained by the epilogue
+          if (it >= a.nacc &&
+              !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> acc_shift) + 1) & 1, abort,
+                         a.status, kWaitLimitNs, 14))
             break;
           if (!mbar_wait(smem_u32(&sm->full[st]), ph, abort, a.status, kWaitLimitNs, 15)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + acc * a.NQ;
-          for (int kc = 0; kc < a.KC; ++kc) {
-            const uint32_t a_addr = smem_u32(sA + st * stage_bytes + kc * 16384);
-            const uint32_t b_addr = smem_u32(sQ + kc * a.NQ * 128);
+          if (F8) {
+            // one 128-byte row per key and per query: 4 steps of K = 32
+            const uint32_t a_addr = smem_u32(sA + st * stage_bytes);
+            const uint32_t b_addr = smem_u32(sQ8);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t ad = smem_desc(a_addr + ks * 32, 16, 1024, kSwizzle128B);
               const uint64_t bd = smem_desc(b_addr + ks * 32, 16, 1024, kSwizzle128B);
-              mma_bf16_ss(d_tmem, ad, bd, idesc, (kc | ks) != 0);
+              mma_f8_ss(d_tmem, ad, bd, idesc, ks != 0);
+            }
+          } else {
+            for (int kc = 0; kc < a.KC; ++kc) {
+              const uint32_t a_addr = smem_u32(sA + st * stage_bytes + kc * 16384);
+              const uint32_t b_addr = smem_u32(sQ + kc * a.NQ * 128);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ad = smem_desc(a_addr + ks * 32, 16, 1024, kSwizzle128B);
+                const uint64_t bd = smem_desc(b_addr + ks * 32, 16, 1024, kSwizzle128B);
+                mma_bf16_ss(d_tmem, ad, bd, idesc, (kc | ks) != 0);
+              }
             }
           }
           mma_commit(smem_u32(&sm->empty[st]));
@@ -247,23 +330,44 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Group eg drains the slots it with it % kEpiGroups == eg; its warp for
+    // tensor-memory lanes quad*32 .. quad*32+31 handles those 32 entries.
+    const int ew = warp - kFirstEpiWarp;
+    const int eg = ew >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    float* wcol = sm->wcol[quad];
-    int* ntv = sm->nt[quad];
+    float* wcol = sm->wcol[ew];
+    int* ntv = sm->nt[ew];
     // heads a multiple of 32: every 32-column accumulator chunk belongs to
     // one query, so a query's score is a straight sum over its chunks
     const bool whole = (a.HI & 31) == 0;
     const int cpq = a.HI >> 5;
     SlotCursor cur;
-    int64_t it = 0, wgroup = -1;
+    int64_t it = 0, wgroup = -1, qn = 0;
+    int st = 0;  // the slot's key stage (FP8: its scales are read from there)
+    uint32_t ph = 0;
     for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
       if (!cur.live()) continue;
       if (cur.group != wgroup) {
+        if (F8) {
+          // the group's bf16 query rows have landed: quantise this warp's
+          // share, publish it to the MMA issuers, then wait for the others'
+          // row scales
+          bool got = mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 18);
+          if (!__all_sync(0xffffffffu, got)) break;
+          quantize_query_rows(sQ, sQ8, sm->qscale, a.NQ, ew, lane);
+          fence_proxy_async_smem();  // visible to the tensor core's reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->q8full));
+          got = mbar_wait(smem_u32(&sm->q8full), qn & 1, abort, a.status, kWaitLimitNs, 19);
+          if (!__all_sync(0xffffffffu, got)) break;
+          ++qn;
+        }
         __syncwarp();
         for (int c = lane; c < a.NQ; c += 32) {
           const int g = c / a.HI, h = c % a.HI;
-          wcol[c] = (g < cur.gv) ? a.w[((int64_t)cur.b * a.T + cur.t0 + g) * a.HI + h] : 0.f;
+          const float wv = (g < cur.gv) ? a.w[((int64_t)cur.b * a.T + cur.t0 + g) * a.HI + h] : 0.f;
+          wcol[c] = F8 ? wv * sm->qscale[c] : wv;
         }
         for (int g = lane; g < a.G; g += 32)
           ntv[g] = g < cur.gv ? static_cast<int>(visible_entries(
@@ -272,17 +376,36 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         __syncwarp();
         wgroup = cur.group;
       }
-      const int acc = static_cast<int>(it & 1);
-      const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), (it >> 1) & 1, abort, a.status,
-                                 kWaitLimitNs, 17);
+      const int sst = st;
+      const uint32_t sph = ph;
+      if (++st == a.stages) { st = 0; ph ^= 1u; }
+      if (static_cast<int>(it % kEpiGroups) != eg) {
+        ++it;
+        continue;  // the other epilogue group's slot
+      }
+      const int acc = static_cast<int>(it & acc_mask);
+      const int64_t j = static_cast<int64_t>(cur.blk) * kBlockRows + row;
+      const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), (it >> acc_shift) & 1, abort,
+                                 a.status, kWaitLimitNs, 17);
       if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: tcgen05.ld follows
       tc_fence_after();
-      const int64_t j = static_cast<int64_t>(cur.blk) * kBlockRows + row;
+      float ks = 1.f;
+      if (F8) {
+        // the stage's copy completed before its MMAs ran; this wait returns
+        // at once and makes the scales the copy wrote visible here
+        const bool sg = mbar_wait(smem_u32(&sm->full[sst]), sph, abort, a.status, kWaitLimitNs, 21);
+        if (!__all_sync(0xffffffffu, sg)) break;
+        ks = sScale[sst * kBlockRows + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->sempty[sst]));
+      }
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * a.NQ;
       float* srow = a.scores + ((int64_t)cur.b * a.T + cur.t0) * a.N_cap + j;
       if (whole) {
         for (int g = 0; g < cur.gv; ++g) {
-          float sum = 0.f;
+          // four independent partial sums (one per column of a float4), so
+          // the FMAs do not wait on one another
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
           for (int c = 0; c < cpq; c += 2) {
             const int col = (g * cpq + c) * 32;
             float x0[32], x1[32];
@@ -293,24 +416,25 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 wv = w0[i];
-              sum = fmaf(wv.x, fmaxf(x0[4 * i], 0.f), sum);
-              sum = fmaf(wv.y, fmaxf(x0[4 * i + 1], 0.f), sum);
-              sum = fmaf(wv.z, fmaxf(x0[4 * i + 2], 0.f), sum);
-              sum = fmaf(wv.w, fmaxf(x0[4 * i + 3], 0.f), sum);
+              s4[0] = fmaf(wv.x, fmaxf(x0[4 * i], 0.f), s4[0]);
+              s4[1] = fmaf(wv.y, fmaxf(x0[4 * i + 1], 0.f), s4[1]);
+              s4[2] = fmaf(wv.z, fmaxf(x0[4 * i + 2], 0.f), s4[2]);
+              s4[3] = fmaf(wv.w, fmaxf(x0[4 * i + 3], 0.f), s4[3]);
             }
             if (c + 1 < cpq) {
               const float4* w1 = reinterpret_cast<const float4*>(wcol + col + 32);
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const float4 wv = w1[i];
-                sum = fmaf(wv.x, fmaxf(x1[4 * i], 0.f), sum);
-                sum = fmaf(wv.y, fmaxf(x1[4 * i + 1], 0.f), sum);
-                sum = fmaf(wv.z, fmaxf(x1[4 * i + 2], 0.f), sum);
-                sum = fmaf(wv.w, fmaxf(x1[4 * i + 3], 0.f), sum);
+                s4[0] = fmaf(wv.x, fmaxf(x1[4 * i], 0.f), s4[0]);
+                s4[1] = fmaf(wv.y, fmaxf(x1[4 * i + 1], 0.f), s4[1]);
+                s4[2] = fmaf(wv.z, fmaxf(x1[4 * i + 2], 0.f), s4[2]);
+                s4[3] = fmaf(wv.w, fmaxf(x1[4 * i + 3], 0.f), s4[3]);
               }
             }
           }
-          if (j < ntv[g]) srow[(int64_t)g * a.N_cap] = sum;
+          const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          if (j < ntv[g]) srow[(int64_t)g * a.N_cap] = F8 ? sum * ks : sum;
         }
       } else {
         float sum = 0.f;
@@ -323,7 +447,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           for (int i = 0; i < 32; ++i) {
             sum = fmaf(wcol[cc + i], fmaxf(x[i], 0.f), sum);
             if (++h == a.HI) {
-              if (g < cur.gv && j < ntv[g]) srow[(int64_t)g * a.N_cap] = sum;
+              if (g < cur.gv && j < ntv[g]) srow[(int64_t)g * a.N_cap] = F8 ? sum * ks : sum;
               sum = 0.f;
               h = 0;
               ++g;
@@ -345,8 +469,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
 }  // namespace
 
-bool plan_indexer(int T, int HI, int dI, IndexerPlan* p) {
+bool plan_indexer(int T, int HI, int dI, bool f8, IndexerPlan* p) {
   if (HI <= 0 || HI > 256 || dI <= 0 || dI > 128) return false;
+  if (f8 && dI != 128) return false;
   int G = 256 / HI;
   if (G > T) G = T;
   if (G < 1) G = 1;
@@ -355,23 +480,36 @@ bool plan_indexer(int T, int HI, int dI, IndexerPlan* p) {
   p->G = G;
   p->NQ = NQ;
   p->KC = (dI + 63) / 64;
-  const size_t q_bytes = (size_t)p->KC * NQ * 128;
-  const size_t stage_bytes = (size_t)p->KC * 16384;
+  const size_t q_bytes = (size_t)p->KC * NQ * 128 + (f8 ? (size_t)NQ * 128 : 0);
+  // FP8: 16 KB of codes plus the block's 128 fp32 scales per stage
+  const size_t stage_bytes = f8 ? 16384 + kBlockRows * 4 : (size_t)p->KC * 16384;
   const size_t budget = 227 * 1024 - 1024 - sizeof(IdxSmem) - q_bytes;
   int stages = static_cast<int>(budget / stage_bytes);
-  if (stages > kMaxStages) stages = kMaxStages;
+  const int cap = f8 ? kMaxStages : kMaxStagesBf16;
+  if (stages > cap) stages = cap;
+  // An even ring: slot s uses stage s % stages and is issued by MMA warp
+  // s % 2, so every stage (like every accumulator) belongs to one issuer and
+  // one epilogue group, and each waits on a barrier's phases in order.  With
+  // an odd ring a stage alternates between the issuers, and an issuer that
+  // runs a lap ahead of the other would wait on the parity of a phase whose
+  // predecessor is still pending -- a parity wait that passes at once.
+  stages &= ~1;
   if (stages < 2) return false;
   p->stages = stages;
-  p->tmem_cols = 2 * NQ;
+  // as many accumulators as tensor memory holds, up to kMaxAcc (a power of 2)
+  int nacc = 2;
+  while (nacc * 2 <= kMaxAcc && nacc * 2 * NQ <= 512) nacc *= 2;
+  p->nacc = nacc;
+  p->tmem_cols = nacc * NQ;
   p->smem_bytes = 1024 + q_bytes + stages * stage_bytes + sizeof(IdxSmem);
   return true;
 }
 
 cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm_iq,
-                                 const IndexerArgs& a, const IndexerPlan& p, int grid,
-                                 cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(indexer_score_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 const CUtensorMap& tm_ks, const IndexerArgs& a,
+                                 const IndexerPlan& p, bool f8, int grid, cudaStream_t stream) {
+  auto kernel = f8 ? indexer_score_kernel<true> : indexer_score_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(p.smem_bytes));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -382,7 +520,7 @@ cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm
   cudaLaunchAttribute at[1];
   cfg.attrs = at;
   cfg.numAttrs = add_dependent_attr(at, 0);
-  e = cudaLaunchKernelEx(&cfg, indexer_score_kernel, tm_ik, tm_iq, a);
+  e = cudaLaunchKernelEx(&cfg, kernel, tm_ik, tm_iq, tm_ks, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -27,6 +27,8 @@ struct CompressArgs {
   const float* gamma;           // [D] or null
   __nv_bfloat16* kv_out;        // [B][N_cap][D]
   __nv_bfloat16* ik_out;        // [B][N_cap][dI] or null
+  uint8_t* ik8_out;             // [B][N_cap][dI] E4M3 codes of the indexer key, or null
+  float* ik_scale_out;          // [B][N_cap] their row scales (with ik8_out)
   int B, D, dI, m, w, r;
   int64_t L_cap, N_cap, j_begin, j_end;
   float eps;
@@ -43,8 +45,9 @@ struct IndexerArgs {
   int B, T, HI, dI, m;
   int G;                 // queries per group (B operand rows = G*HI, padded to NQ)
   int NQ;                // MMA N
-  int KC;                // 64-wide K chunks
+  int KC;                // 64-wide K chunks of the bf16 operands
   int stages;
+  int nacc;              // tensor-memory accumulators in flight (2, 4 or 8)
   int groups_per_seq;    // ceil(T / G)
   int nblk;              // ceil(N_cap / 128)
   int64_t fresh_from;    // entries >= this may be written by the previous kernel (-1: any)
@@ -52,13 +55,21 @@ struct IndexerArgs {
   int64_t total_slots;   // B * groups_per_seq * nblk
 };
 struct IndexerPlan {
-  int G, NQ, KC, stages, tmem_cols;
+  int G, NQ, KC, stages, nacc, tmem_cols;
   size_t smem_bytes;
 };
-bool plan_indexer(int T, int HI, int dI, IndexerPlan* p);
+// f8: E4M3 keys (dI = 128, one 128-byte row each) and queries quantised in
+// the kernel; else bf16 keys and queries.
+bool plan_indexer(int T, int HI, int dI, bool f8, IndexerPlan* p);
+// tm_ks: the FP8 keys' row scales [B][N_cap] fp32, boxes of 128 (FP8 only).
 cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm_iq,
-                                 const IndexerArgs& a, const IndexerPlan& p, int grid,
-                                 cudaStream_t stream);
+                                 const CUtensorMap& tm_ks, const IndexerArgs& a,
+                                 const IndexerPlan& p, bool f8, int grid, cudaStream_t stream);
+
+// ------------------------------------------------------------ E4M3 rows
+// rows x n bf16 -> E4M3 codes [rows][n] and row scales [rows]; n % 4 == 0.
+cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
+                                 float* scales, int num_sms, cudaStream_t stream);
 
 // ------------------------------------------------------------ top-k select
 struct TopkArgs {

@@ -32,6 +32,12 @@ _SIGS = {
                                   _f32, _f32, _i64, _i64, _vp, _vp, _i64, _vp]),
     "hattn_hca_compress": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _f32, _f32, _i64,
                                   _i64, _vp, _i64, _vp]),
+    "hattn_csa_compress_fp8": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
+                                      _i32, _f32, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _i64,
+                                      _vp]),
+    "hattn_quantize_e4m3": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp]),
+    "hattn_indexer_scores_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
+                                        _i32, _i32, _i64, _vp, _vp]),
     "hattn_indexer_topk": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                   _vp, _vp, _vp, _sz, _vp]),
     "hattn_indexer_topk_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32, _i32]),
@@ -157,6 +163,57 @@ def csa_compress(kv_raw, ik_raw, gate, *, r, j_begin=0, j_end=None, m=4, w=8, kv
     return kv_c, ik_c
 
 
+def csa_compress_fp8(kv_raw, ik_raw, gate, *, r, j_begin=0, j_end=None, m=4, w=8, kv_c=None,
+                     ik8=None, ik_scale=None, ik_c=None, N_cap=None, gamma_kv=None,
+                     rope_base=10000.0, eps=1e-6, stream=None):
+    """csa_compress that writes each entry's indexer key as E4M3 codes with a
+    row scale (and, when ik_c is given, also as bf16); returns
+    (kv_c, ik8 uint8 [B, N_cap, dI], ik_scale fp32 [B, N_cap])."""
+    _need(kv_raw, "kv_raw", torch.bfloat16, 3)
+    _need(ik_raw, "ik_raw", torch.bfloat16, 3)
+    _need(gate, "gate", torch.bfloat16, 2)
+    B, L, D = kv_raw.shape
+    dI = ik_raw.shape[2]
+    if N_cap is None:
+        N_cap = kv_c.shape[1] if kv_c is not None else L // m
+    if j_end is None:
+        j_end = min(N_cap, L // m)
+    dev = kv_raw.device
+    if kv_c is None:
+        kv_c = torch.zeros((B, N_cap, D), dtype=torch.bfloat16, device=dev)
+    if ik8 is None:
+        ik8 = torch.zeros((B, N_cap, dI), dtype=torch.uint8, device=dev)
+    if ik_scale is None:
+        ik_scale = torch.zeros((B, N_cap), dtype=torch.float32, device=dev)
+    _need(kv_c, "kv_c", torch.bfloat16, 3)
+    _need(ik8, "ik8", torch.uint8, 3)
+    _need(ik_scale, "ik_scale", torch.float32, 2)
+    _opt(ik_c, "ik_c", torch.bfloat16)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    _check(lib().hattn_csa_compress_fp8(_ptr(kv_raw), _ptr(ik_raw), _ptr(gate), _ptr(gamma_kv), B,
+                                        L, D, dI, m, w, r, rope_base, eps, j_begin, j_end,
+                                        _ptr(kv_c), _ptr(ik_c), _ptr(ik8), _ptr(ik_scale), N_cap,
+                                        _stream(stream)))
+    return kv_c, ik8, ik_scale
+
+
+def quantize_e4m3(x, *, codes=None, scales=None, stream=None):
+    """Rows of the last axis of a bf16 tensor to E4M3 codes (uint8, same
+    shape) and fp32 row scales (shape without the last axis)."""
+    _need(x, "x", torch.bfloat16)
+    n = x.shape[-1]
+    rows = x.numel() // n if n else 0
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _need(codes, "codes", torch.uint8)
+    _need(scales, "scales", torch.float32)
+    _check(lib().hattn_quantize_e4m3(_ptr(x), rows, n, _ptr(codes), _ptr(scales),
+                                     _stream(stream)))
+    return codes, scales
+
+
 def hca_compress(kv_raw, gate, *, r, j_begin=0, j_end=None, m=128, kv_h=None, N_cap=None,
                  gamma_kv=None, rope_base=10000.0, eps=1e-6, stream=None):
     """C(m, m) of KV for entries [j_begin, j_end); returns kv_h."""
@@ -246,6 +303,27 @@ def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, fresh_from
     else:
         _check(lib().hattn_indexer_scores(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
                                           N_cap, m, _ptr(score_out), _stream(stream)))
+    return score_out
+
+
+def indexer_scores_fp8(iq, w, ik8, ik_scale, pos, *, m=4, score_out=None, n_sms=0,
+                       fresh_from=-1, stream=None):
+    """indexer_scores over E4M3 keys (ik8 uint8 [B, N_cap, 128] with row
+    scales ik_scale fp32 [B, N_cap]); the bf16 queries are quantised the
+    same way in the kernel."""
+    _need(iq, "iq", torch.bfloat16, 4)
+    _need(w, "w", torch.float32, 3)
+    _need(ik8, "ik8", torch.uint8, 3)
+    _need(ik_scale, "ik_scale", torch.float32, 2)
+    _need(pos, "pos", torch.int32, 2)
+    B, T, HI, dI = iq.shape
+    N_cap = ik8.shape[1]
+    if score_out is None:
+        score_out = torch.empty((B, T, N_cap), dtype=torch.float32, device=iq.device)
+    _need(score_out, "score_out", torch.float32)
+    _check(lib().hattn_indexer_scores_fp8(_ptr(iq), _ptr(w), _ptr(ik8), _ptr(ik_scale), _ptr(pos),
+                                          B, T, HI, dI, N_cap, m, n_sms, fresh_from,
+                                          _ptr(score_out), _stream(stream)))
     return score_out
 
 

@@ -28,10 +28,16 @@ from . import hattn
 
 
 class HybridLayer:
-    def __init__(self, wl, raw: dict, device="cuda", build_caches=True):
+    def __init__(self, wl, raw: dict, device="cuda", build_caches=True, indexer_keys="bf16"):
+        """indexer_keys: "bf16", or "fp8" to keep the indexer keys as E4M3
+        codes with a row scale (ik8, ik_scale) and score them on the FP8
+        tensor-core path."""
+        if indexer_keys not in ("bf16", "fp8"):
+            raise ValueError(f"indexer_keys must be 'bf16' or 'fp8', got {indexer_keys!r}")
         self.wl = wl
         self.dev = device
         self.raw = raw  # kv_raw, ik_raw, gate_csa, gate_hca on device
+        self.fp8 = indexer_keys == "fp8"
         B, L, D = raw["kv_raw"].shape
         self.B, self.L, self.D = B, L, D
         self.N_csa = L // wl.m_csa
@@ -41,7 +47,10 @@ class HybridLayer:
         n_c = self.N_csa if "csa" in wl.branches else 1
         n_h = self.N_hca if "hca" in wl.branches else 1
         self.kv_c = torch.zeros((B, n_c, D), dtype=bf, device=device)
-        self.ik_c = torch.zeros((B, n_c, wl.dI), dtype=bf, device=device)
+        self.ik_c = torch.zeros((B, 1 if self.fp8 else n_c, wl.dI), dtype=bf, device=device)
+        if self.fp8:
+            self.ik8 = torch.zeros((B, n_c, wl.dI), dtype=torch.uint8, device=device)
+            self.ik_scale = torch.zeros((B, n_c), dtype=torch.float32, device=device)
         self.kv_h = torch.zeros((B, n_h, D), dtype=bf, device=device)
         self.override_dense_sms = 0  # > 0: HCA + SWA attention on that many SMs beside the indexer
         # fused step with a side stream: the indexer, top-k, attention and
@@ -56,9 +65,7 @@ class HybridLayer:
         wl, r = self.wl, self.raw
         L = self.L if n_tokens is None else n_tokens
         if "csa" in wl.branches:
-            hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=0,
-                               j_end=L // wl.m_csa, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c,
-                               ik_c=self.ik_c)
+            self._csa_compress(0, L // wl.m_csa)
         if "hca" in wl.branches and L // wl.m_hca > 0:
             hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=0, j_end=L // wl.m_hca,
                                m=wl.m_hca, kv_h=self.kv_h)
@@ -152,12 +159,54 @@ class HybridLayer:
                                             ("swa", hattn.KIND_SWA, wl.W)]
                 if n in wl.branches]
 
+    def new_entries(self, kind, t_new, n_new=1):
+        """[j0, j1): the entries of the CSA or HCA cache that the n_new tokens
+        at positions t_new-n_new+1 .. t_new complete (entry j is complete once
+        the token at m*(j+1)-1 is cached)."""
+        if t_new is None:
+            return 0, 0
+        m = self.wl.m_csa if kind == "csa" else self.wl.m_hca
+        return (t_new - n_new + 1) // m, (t_new + 1) // m
+
+    def _csa_compress(self, j0, j1):
+        wl, r = self.wl, self.raw
+        if self.fp8:
+            hattn.csa_compress_fp8(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j0,
+                                   j_end=j1, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c,
+                                   ik8=self.ik8, ik_scale=self.ik_scale)
+        else:
+            hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j0,
+                               j_end=j1, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c, ik_c=self.ik_c)
+
+    def _indexer(self, iq, w, pos, scores, n_sms=0, fresh_from=-1):
+        wl = self.wl
+        if self.fp8:
+            hattn.indexer_scores_fp8(iq, w, self.ik8, self.ik_scale, pos, m=wl.m_csa,
+                                     score_out=scores, n_sms=n_sms, fresh_from=fresh_from)
+        else:
+            hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=scores,
+                                 n_sms=n_sms, fresh_from=fresh_from)
+
+    def _compress_new(self, kind, t_new, n_new):
+        """Compress the entries that the step's new tokens complete."""
+        wl, r = self.wl, self.raw
+        j0, j1 = self.new_entries(kind, t_new, n_new)
+        if j1 <= j0:
+            return
+        if kind == "csa":
+            self._csa_compress(j0, j1)
+        else:
+            hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=j0, j_end=j1,
+                               m=wl.m_hca, kv_h=self.kv_h)
+
     def step(self, q, iq, w, pos, sink, t_new=None, events=None, side_stream=None,
              branch_outputs=False, fused=None):
         """One pass of the hot path for queries q [B,T,H,D] at positions pos.
 
-        t_new: position of the newest token (compresses the entries it
-        completes); None skips the incremental compression.  events: optional
+        t_new: position of the newest token; the T newest tokens (positions
+        t_new-T+1 .. t_new, one per query) are new this step, and the entries
+        they complete are compressed first.  None skips the incremental
+        compression.  events: optional
         dict name -> (start, end) torch.cuda.Event pairs recorded around the
         calls.  side_stream: a second CUDA stream; when given, the HCA and
         SWA branches run on it, concurrently with the indexer, top-k and CSA
@@ -181,18 +230,8 @@ class HybridLayer:
                 events[name][i].record(torch.cuda.current_stream())
 
         def compress(kind):
-            if t_new is None or kind not in wl.branches:
-                return
-            m, w_ = (wl.m_csa, wl.w_csa) if kind == "csa" else (wl.m_hca, wl.m_hca)
-            if (t_new + 1) % m:
-                return
-            j = (t_new + 1) // m - 1
-            if kind == "csa":
-                hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j,
-                                   j_end=j + 1, m=m, w=w_, kv_c=self.kv_c, ik_c=self.ik_c)
-            else:
-                hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=j, j_end=j + 1,
-                                   m=m, kv_h=self.kv_h)
+            if kind in wl.branches:
+                self._compress_new(kind, t_new, T)
 
         ev("compress", 0)
         compress("csa")
@@ -233,7 +272,7 @@ class HybridLayer:
             joined = side_stream
         if "csa" in wl.branches:
             ev("indexer", 0)
-            hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=b["scores"])
+            self._indexer(iq, w, pos, b["scores"])
             ev("indexer", 1)
             ev("topk", 0)
             hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
@@ -275,18 +314,7 @@ class HybridLayer:
                 events[name][i].record(torch.cuda.current_stream())
 
         def compress(kind):
-            if t_new is None:
-                return
-            m = wl.m_csa if kind == "csa" else wl.m_hca
-            if (t_new + 1) % m:
-                return
-            j = (t_new + 1) // m - 1
-            if kind == "csa":
-                hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j,
-                                   j_end=j + 1, m=m, w=wl.w_csa, kv_c=self.kv_c, ik_c=self.ik_c)
-            else:
-                hattn.hca_compress(r["kv_raw"], r["gate_hca"], r=wl.r, j_begin=j, j_end=j + 1,
-                                   m=m, kv_h=self.kv_h)
+            self._compress_new(kind, t_new, T)
 
         def attn(name, segments, n_sms):
             ev("attn_" + name, 0)
@@ -334,12 +362,10 @@ class HybridLayer:
             hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
             ev("swa_keys", 1)
         ev("indexer", 0)
-        # the only entry the compression above writes is the newest one
-        fresh = (t_new + 1) // wl.m_csa - 1 if t_new is not None else -1
-        hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=b["scores"],
-                             n_sms=(self.NUM_SMS - n_dense) if n_dense else 0,
-                             fresh_from=fresh if (t_new is not None and
-                                                  (t_new + 1) % wl.m_csa == 0) else -1)
+        # the entries the compression above writes are the newest ones
+        j0, j1 = self.new_entries("csa", t_new, T)
+        self._indexer(iq, w, pos, b["scores"], n_sms=(self.NUM_SMS - n_dense) if n_dense else 0,
+                      fresh_from=j0 if j1 > j0 else -1)
         ev("indexer", 1)
         if side_stream is not None and not overlap:
             # The query preparation, the HCA compression and the window keys
@@ -390,9 +416,9 @@ class HybridLayer:
         compressions the new token needs."""
         wl, B, D, H = self.wl, self.B, self.D, self.wl.H
         n = 2  # query preparation, merge
-        if t_new is not None:
-            n += int("csa" in wl.branches and (t_new + 1) % wl.m_csa == 0)
-            n += int("hca" in wl.branches and (t_new + 1) % wl.m_hca == 0)
+        for kind in ("csa", "hca"):
+            j0, j1 = self.new_entries(kind, t_new, T)
+            n += int(kind in wl.branches and j1 > j0)
         if fused is None:
             fused = self.can_fuse(T) and not branch_outputs
         if fused:

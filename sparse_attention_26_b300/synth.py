@@ -56,7 +56,7 @@ class Workload:
                     k=self.k, W=self.W, r=self.r, base=self.base, eps=self.eps)
 
 
-# The five workloads (sizes from the layer shapes of V4-Flash / V4-Pro).
+# The workloads (sizes from the layer shapes of V4-Flash / V4-Pro).
 WORKLOADS = {
     "tiny": Workload("tiny", B=1, L=256, T=256, H=4, D=64, r=16, HI=2, dI=32, k=16,
                      d_model=256),
@@ -70,6 +70,10 @@ WORKLOADS = {
                             dI=128, k=1024, branches=("hca",)),
     "hybrid_decode_1m": Workload("hybrid_decode_1m", B=8, L=1 << 20, T=1, H=128, D=512, r=64,
                                  HI=64, dI=128, k=1024),
+    # speculative decode with one multi-token-prediction draft: the accepted
+    # token and the draft, two queries per sequence over the same caches
+    "hybrid_decode_1m_mtp2": Workload("hybrid_decode_1m_mtp2", B=8, L=1 << 20, T=2, H=128,
+                                      D=512, r=64, HI=64, dI=128, k=1024),
 }
 
 

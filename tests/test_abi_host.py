@@ -97,6 +97,39 @@ def test_indexer_validation(L):
     assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 1) == 0
 
 
+def test_fp8_key_validation(L):
+    N = None
+    s = None
+    # FP8 indexer keys are one 128-byte row: dI = 64 is rejected before any launch
+    rc = L.hattn_indexer_scores_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 100, 4, 0, -1,
+                                    FAKE, s)
+    assert rc == hattn.INVALID_ARG and "dI = 128" in _err(L)
+    rc = L.hattn_indexer_scores_fp8(FAKE, FAKE, FAKE, N, FAKE, 1, 1, 64, 128, 100, 4, 0, -1,
+                                    FAKE, s)
+    assert rc == hattn.INVALID_ARG and "ik_scale" in _err(L)
+    # the scales travel in 16-byte rows: N_cap a multiple of 4
+    rc = L.hattn_indexer_scores_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 128, 102, 4, 0, -1,
+                                    FAKE, s)
+    assert rc == hattn.INVALID_ARG and "N_cap % 4" in _err(L)
+    rc = L.hattn_indexer_scores_fp8(FAKE, FAKE, FAKE, MISAL, FAKE, 1, 1, 64, 128, 100, 4, 0, -1,
+                                    FAKE, s)
+    assert rc == hattn.MISALIGNED
+    # the compressor's FP8 key needs both the codes and the scales
+    rc = L.hattn_csa_compress_fp8(FAKE, FAKE, FAKE, N, 1, 64, 64, 32, 4, 8, 16, 1e4, 1e-6, 0, 4,
+                                  FAKE, N, FAKE, N, 16, s)
+    assert rc == hattn.INVALID_ARG and "ik_scale" in _err(L)
+    rc = L.hattn_csa_compress_fp8(FAKE, N, FAKE, N, 1, 64, 64, 32, 4, 8, 16, 1e4, 1e-6, 0, 4,
+                                  FAKE, N, FAKE, FAKE, 16, s)
+    assert rc == hattn.INVALID_ARG and "ik_raw" in _err(L)
+    # an empty range succeeds without a device
+    rc = L.hattn_csa_compress_fp8(FAKE, FAKE, FAKE, N, 1, 64, 64, 32, 4, 8, 16, 1e4, 1e-6, 2, 2,
+                                  FAKE, N, FAKE, FAKE, 16, s)
+    assert rc == hattn.OK
+    rc = L.hattn_quantize_e4m3(FAKE, 10, 6, FAKE, FAKE, s)
+    assert rc == hattn.INVALID_ARG and "n=6" in _err(L)
+    assert L.hattn_quantize_e4m3(FAKE, 0, 128, FAKE, FAKE, s) == hattn.OK
+
+
 def test_attention_validation(L):
     N = None
     rc = L.hattn_sparse_attn(FAKE, N, 0, FAKE, N, FAKE, 1, 1, 128, 512, 100, 16, 64, 1e4, 1e-6,

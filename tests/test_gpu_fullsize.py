@@ -48,14 +48,14 @@ def _host_rows(t, b, rows):
     return out
 
 
-def _run(wl, t_new=None, side=False):
+def _run(wl, t_new=None, side=False, indexer_keys="bf16"):
     """The layer step twice on the same inputs: first forming each branch's
     output (kept for the stage checks), then as the benchmark runs it (split
     partials merged in one pass, HCA and SWA on a second stream when `side`).
     Returns the inputs, the layer and both (out, lse) results."""
     inp = synth.make_inputs(wl, 0, device=DEV)
     raw = {k: inp[k] for k in ["kv_raw", "ik_raw", "gate_csa", "gate_hca"]}
-    layer = HybridLayer(wl, raw, device=DEV)
+    layer = HybridLayer(wl, raw, device=DEV, indexer_keys=indexer_keys)
     args = (inp["q"], inp["iq"], inp["w"], inp["pos"], inp["sink"])
     out_b, lse_b = layer.step(*args, t_new=t_new, branch_outputs=True)
     out_b, lse_b = out_b.clone(), lse_b.clone()
@@ -77,7 +77,16 @@ def _check_compress(wl, inp, layer, b, entries, kind):
     for j in entries:
         rk, ri, _ = orc.compress(kv, gate, m, w, wl.r, j, j + 1, ik_raw=ik)
         assert rel_l2(got_kv[b, j], rk[0, 0]) <= KV_REL_L2, f"{kind} entry {j}"
-        if kind == "csa":
+        if kind == "csa" and layer.fp8:
+            # the E4M3 key decodes to within half a step of the fp64 key
+            # (plus the bf16 rounding it is quantised from)
+            sc = float(layer.ik_scale[b, j])
+            deq = orc.dequantize_e4m3(layer.ik8[b, j].cpu().numpy(), np.float64(sc))
+            ref = ri[0, 0]
+            bound = (np.maximum(np.abs(ref) * 2.0 ** -4, 2.0 ** -10 * sc)
+                     + np.abs(ref) * 2.0 ** -8) * 1.01 + 1e-6
+            assert (np.abs(deq - ref) <= bound).all(), f"FP8 indexer key {j}"
+        elif kind == "csa":
             assert rel_l2(layer.ik_c[b, j], ri[0, 0]) <= KV_REL_L2, f"indexer key {j}"
 
 
@@ -93,9 +102,13 @@ def _check_sequence(wl, inp, layer, res_b, res, b, ts):
     sink = inp["sink"].cpu().numpy()
     o_list, l_list = [], []
     if "csa" in wl.branches:
-        ik_c = _bits(layer.ik_c[b:b + 1])
-        ref_sc = orc.indexer_scores(_bits(inp["iq"][b:b + 1, tsel]),
-                                    inp["w"][b:b + 1, tsel].cpu().numpy(), ik_c, pos, wl.m_csa)
+        iq = _bits(inp["iq"][b:b + 1, tsel])
+        w = inp["w"][b:b + 1, tsel].cpu().numpy()
+        if layer.fp8:
+            ref_sc = orc.indexer_scores_e4m3(iq, w, layer.ik8[b:b + 1].cpu().numpy(),
+                                             layer.ik_scale[b:b + 1].cpu().numpy(), pos, wl.m_csa)
+        else:
+            ref_sc = orc.indexer_scores(iq, w, _bits(layer.ik_c[b:b + 1]), pos, wl.m_csa)
         got_sc = f64(bufs["scores"][b:b + 1, tsel])
         vis = ~np.isnan(ref_sc)
         err = np.abs(got_sc[vis] - ref_sc[vis])
@@ -136,6 +149,30 @@ def test_hybrid_decode_1m():
     _check_compress(wl, inp, layer, 5, [0, 1, 77777, n - 1], "csa")
     _check_compress(wl, inp, layer, 2, [0, 4095, wl.L // wl.m_hca - 1], "hca")
     _check_sequence(wl, inp, layer, res_b, res, 5, [0])
+    assert torch.isfinite(res[0].float()).all()
+
+
+def test_hybrid_decode_1m_mtp2():
+    """Two queries per sequence (the accepted token at 1,048,574 and one
+    multi-token-prediction draft at 1,048,575) over the 1M caches, the
+    benchmark's step; the entry both new tokens complete is compressed once."""
+    wl = synth.WORKLOADS["hybrid_decode_1m_mtp2"]
+    inp, layer, res_b, res = _run(wl, t_new=wl.L - 1, side=True)
+    _check_compress(wl, inp, layer, 6, [wl.L // wl.m_csa - 1], "csa")
+    _check_compress(wl, inp, layer, 6, [wl.L // wl.m_hca - 1], "hca")
+    _check_sequence(wl, inp, layer, res_b, res, 6, [0, 1])
+    assert torch.isfinite(res[0].float()).all()
+
+
+def test_hybrid_decode_1m_fp8_keys():
+    """The 1M decode step with the indexer keys held as E4M3 codes and row
+    scales: the compressor's FP8 keys, the FP8 indexer scores (against the
+    oracle's dequantised definition), top-k, and the attention and merge."""
+    wl = synth.WORKLOADS["hybrid_decode_1m"]
+    inp, layer, res_b, res = _run(wl, t_new=wl.L - 1, side=True, indexer_keys="fp8")
+    n = wl.L // wl.m_csa
+    _check_compress(wl, inp, layer, 3, [0, 1, 123457, n - 1], "csa")
+    _check_sequence(wl, inp, layer, res_b, res, 3, [0])
     assert torch.isfinite(res[0].float()).all()
 
 

@@ -128,6 +128,137 @@ def test_indexer_tiny_shape():
     _indexer_case(1, 256, 2, 32, 64, 16, [list(range(256))], 30)
 
 
+# ------------------------------------------------------------------ FP8 indexer keys
+def _u8(t):
+    return t.cpu().numpy().astype(np.uint8)
+
+
+@pytest.mark.parametrize("rows,n", [(1000, 128), (37, 64), (5, 4)])
+def test_quantize_e4m3_bit_exact(rows, n):
+    """Codes and row scales equal the oracle's bit for bit: row magnitudes
+    from 1e-4 to 1e4 (subnormal codes included), one all-zero row, rows
+    whose largest element is negative."""
+    g = torch.Generator().manual_seed(50)
+    mag = 10.0 ** torch.randint(-4, 5, (rows, 1), generator=g).float()
+    x = (torch.randn((rows, n), generator=g) * mag).to(torch.bfloat16)
+    x[0] = 0
+    if rows > 3:
+        x[3, 1] = -4 * x[3].float().abs().max()
+    codes, scales = hattn.quantize_e4m3(x.to(DEV))
+    hattn.check_status()
+    rc, rs = orc.quantize_e4m3(bits(x))
+    np.testing.assert_array_equal(_u8(codes), rc)
+    np.testing.assert_array_equal(scales.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("B,L,D,dI,r,j0,j1", [
+    (2, 1024, 512, 128, 64, 255, 256),   # one new entry per sequence: the small kernel
+    (2, 4096, 512, 128, 64, 0, 1024),    # cache build: the grid-stride kernel
+])
+def test_csa_compress_fp8(B, L, D, dI, r, j0, j1):
+    """The FP8 indexer key the compressor writes is the oracle's quantisation
+    of the bf16 key it writes beside it, and decodes to within half an E4M3
+    step of the oracle's fp64 key; the KV entries are those of the bf16
+    call."""
+    kv = randn_bf16((B, L, D), 51)
+    ik = randn_bf16((B, L, dI), 52)
+    gate = randn_bf16((B, L), 53)
+    N_cap = L // 4
+    d = dict(kv=kv.to(DEV), ik=ik.to(DEV), gate=gate.to(DEV))
+    kv_c, ik_c = hattn.csa_compress(d["kv"], d["ik"], d["gate"], r=r, j_begin=j0, j_end=j1)
+    kv_c8 = torch.zeros_like(kv_c)
+    ik_c8 = torch.zeros_like(ik_c)
+    _, ik8, iks = hattn.csa_compress_fp8(d["kv"], d["ik"], d["gate"], r=r, j_begin=j0, j_end=j1,
+                                         kv_c=kv_c8, ik_c=ik_c8)
+    # the FP8 key alone (no bf16 key output)
+    _, ik8b, iksb = hattn.csa_compress_fp8(d["kv"], d["ik"], d["gate"], r=r, j_begin=j0,
+                                           j_end=j1)
+    hattn.check_status()
+    assert torch.equal(kv_c8, kv_c) and torch.equal(ik_c8, ik_c)
+    assert torch.equal(ik8b, ik8) and torch.equal(iksb, iks)
+    rc, rs = orc.quantize_e4m3(bits(ik_c[:, j0:j1].cpu()))
+    np.testing.assert_array_equal(_u8(ik8[:, j0:j1]), rc)
+    np.testing.assert_array_equal(iks[:, j0:j1].cpu().numpy(), rs)
+    _, ref_ik, _ = orc.compress(bits(kv), bits(gate), 4, 8, r, j0, j1, ik_raw=bits(ik))
+    deq = orc.dequantize_e4m3(_u8(ik8[:, j0:j1]), iks[:, j0:j1].cpu().numpy())
+    sc = iks[:, j0:j1].cpu().numpy().astype(np.float64)[..., None]
+    # half an E4M3 step of the bf16 key plus the bf16 rounding of the key
+    bound = (np.maximum(np.abs(ref_ik) * 2.0 ** -4, 2.0 ** -10 * sc) + np.abs(ref_ik) * 2.0 ** -8
+             ) * 1.01 + 1e-6
+    assert (np.abs(deq - ref_ik) <= bound).all()
+    assert (ik8[:, :j0] == 0).all() and (ik8[:, j1:] == 0).all()
+
+
+def _indexer_fp8_case(B, T, HI, N_cap, k, pos, seed, m=4):
+    dI = 128
+    iq = randn_bf16((B, T, HI, dI), seed)
+    w = randn_f32((B, T, HI), seed + 1)
+    ik = randn_bf16((B, N_cap, dI), seed + 2)
+    ik8, iks = orc.quantize_e4m3(bits(ik))
+    pos_t = torch.tensor(pos, dtype=torch.int32).reshape(B, T)
+    scores = torch.full((B, T, N_cap), float("nan"), device=DEV)
+    hattn.indexer_scores_fp8(iq.to(DEV), w.to(DEV), torch.from_numpy(ik8).to(DEV),
+                             torch.from_numpy(iks).to(DEV), pos_t.to(DEV), m=m,
+                             score_out=scores)
+    idx = hattn.topk_select(scores, pos_t.to(DEV), k=k, m=m)
+    hattn.check_status()
+    ref = orc.indexer_scores_e4m3(bits(iq), w.numpy(), ik8, iks, pos_t.numpy(), m)
+    vis = ~np.isnan(ref)
+    got = f64(scores)
+    assert np.isnan(got[~vis]).all()  # entries past the visible count untouched
+    err = np.abs(got[vis] - ref[vis])
+    tol = 2e-3 * (np.abs(ref[vis]) + np.sqrt(HI * dI) * 0.05)
+    assert (err <= tol).all(), f"score error {err.max():.3e}"
+    check_topk(idx.cpu().numpy(), ref, pos_t.numpy(), m, k)
+
+
+def test_indexer_fp8_decode_ragged():
+    # visible counts 0, 10 (< k), 150 (two 128-blocks), 600 (ragged tail)
+    _indexer_fp8_case(4, 1, 64, 600, 16, [2, 41, 603, 2399], 60)
+
+
+def test_indexer_fp8_multi_query():
+    # two queries per sequence (the multi-token-prediction decode), and T=7
+    # with 64 heads: 4 queries per group and a ragged group
+    _indexer_fp8_case(3, 2, 64, 1000, 64, [3998, 3999, 1500, 1501, 17, 18], 61)
+    T = 7
+    _indexer_fp8_case(2, T, 64, 520, 32, [[4 * j + 3 + 40 * t for t in range(T)]
+                                          for j in range(2)], 62)
+
+
+def test_indexer_fp8_exact_scores_and_ties():
+    """Keys and queries of multiples of 1/2 with largest magnitude 3.5
+    quantise without loss (scale 2^-7), and with weights 1 and 1/2 every
+    product, head sum and scale is exact in fp32: the scores equal the
+    oracle's bit for bit and the selected sets agree, ties included."""
+    B, T, HI, dI, N_cap, k = 2, 1, 64, 128, 20000, 1024
+    g = torch.Generator().manual_seed(63)
+
+    def rows(shape):
+        v = torch.randint(-7, 8, shape, generator=g).float() / 2
+        v[..., 5] = 3.5
+        return v.to(torch.bfloat16)
+
+    iq, ik = rows((B, T, HI, dI)), rows((B, N_cap, dI))
+    w = torch.where(torch.arange(HI) % 2 == 0, 1.0, 0.5).repeat(B, T, 1).float()
+    pos = torch.tensor([[4 * N_cap - 1], [4 * 7777 + 2]], dtype=torch.int32)
+    ik8, iks = hattn.quantize_e4m3(ik.to(DEV))
+    scores = torch.zeros((B, T, N_cap), device=DEV)
+    hattn.indexer_scores_fp8(iq.to(DEV), w.to(DEV), ik8, iks, pos.to(DEV), score_out=scores)
+    idx = hattn.topk_select(scores, pos.to(DEV), k=k)
+    hattn.check_status()
+    assert (iks == 2.0 ** -7).all()
+    ref = orc.indexer_scores_e4m3(bits(iq), w.numpy(), _u8(ik8), iks.cpu().numpy(), pos.numpy(),
+                                  4)
+    vis = ~np.isnan(ref)
+    np.testing.assert_array_equal(f64(scores)[vis], ref[vis])
+    ref_idx = orc.topk(ref, pos.numpy(), 4, k)
+    got = idx.cpu().numpy()
+    for b in range(B):
+        assert sorted(got[b, 0][got[b, 0] >= 0].tolist()) == sorted(
+            ref_idx[b, 0][ref_idx[b, 0] >= 0].tolist())
+
+
 @pytest.mark.parametrize("N_cap,k", [(40000, 1024), (262144, 1024), (3000, 512)])
 def test_topk_exact_with_ties(N_cap, k):
     """Integer-valued scores are exact in fp32 on both sides, so the selected

@@ -69,17 +69,48 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, letting the hardware suspend the thread for up to
+// `hint_ns` until the phase completes instead of returning at once: waiting
+// warps then leave the issue slots to the warps that have work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSuspendHintNs = 1000;
+
+// The waiting loop of mbar_wait, out of line: every wait site then inlines
+// only its first test, which keeps the warp-specialised loops small enough
+// for the instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort, int* status,
+                                                   uint64_t limit_ns, int site);
+
 // Bounded wait for the phase with the given parity.  Gives up after
-// `limit_ns` (or at once when *abort is set by another thread of the CTA),
-// records kStatusTimeout, sets *abort and returns false.
+// `limit_ns` (or within ~64 us when *abort is set by another thread of the
+// CTA), records kStatusTimeout, sets *abort and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           int* status, uint64_t limit_ns = kWaitLimitNs,
                                           int site = 1) {
   if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, status, limit_ns, site);
+}
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort, int* status,
+                                                   uint64_t limit_ns, int site) {
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if (spins >= 8) __nanosleep(32);  // a long wait: leave the issue slots to others
     if ((++spins & 63u) == 0) {
       if (abort && *abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -402,6 +433,20 @@ __device__ __forceinline__ uint32_t e4m3x4(const float* x, float inv) {
   if (inv == 0.f) return 0u;
   return e4m3x2(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv)) |
          (e4m3x2(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv)) << 16);
+}
+
+// d = a * b + c on two fp32 lanes at once (each lane one IEEE fma).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

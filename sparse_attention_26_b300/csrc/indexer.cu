@@ -403,9 +403,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       float* srow = a.scores + ((int64_t)cur.b * a.T + cur.t0) * a.N_cap + j;
       if (whole) {
         for (int g = 0; g < cur.gv; ++g) {
-          // four independent partial sums (one per column of a float4), so
-          // the FMAs do not wait on one another
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          // four independent partial sums (one per column of a float4), as
+          // two packed pairs, so the FMAs do not wait on one another
+          float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
           for (int c = 0; c < cpq; c += 2) {
             const int col = (g * cpq + c) * 32;
             float x0[32], x1[32];
@@ -416,24 +416,24 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 wv = w0[i];
-              s4[0] = fmaf(wv.x, fmaxf(x0[4 * i], 0.f), s4[0]);
-              s4[1] = fmaf(wv.y, fmaxf(x0[4 * i + 1], 0.f), s4[1]);
-              s4[2] = fmaf(wv.z, fmaxf(x0[4 * i + 2], 0.f), s4[2]);
-              s4[3] = fmaf(wv.w, fmaxf(x0[4 * i + 3], 0.f), s4[3]);
+              s01 = ffma2(make_float2(wv.x, wv.y),
+                          make_float2(fmaxf(x0[4 * i], 0.f), fmaxf(x0[4 * i + 1], 0.f)), s01);
+              s23 = ffma2(make_float2(wv.z, wv.w),
+                          make_float2(fmaxf(x0[4 * i + 2], 0.f), fmaxf(x0[4 * i + 3], 0.f)), s23);
             }
             if (c + 1 < cpq) {
               const float4* w1 = reinterpret_cast<const float4*>(wcol + col + 32);
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const float4 wv = w1[i];
-                s4[0] = fmaf(wv.x, fmaxf(x1[4 * i], 0.f), s4[0]);
-                s4[1] = fmaf(wv.y, fmaxf(x1[4 * i + 1], 0.f), s4[1]);
-                s4[2] = fmaf(wv.z, fmaxf(x1[4 * i + 2], 0.f), s4[2]);
-                s4[3] = fmaf(wv.w, fmaxf(x1[4 * i + 3], 0.f), s4[3]);
+                s01 = ffma2(make_float2(wv.x, wv.y),
+                            make_float2(fmaxf(x1[4 * i], 0.f), fmaxf(x1[4 * i + 1], 0.f)), s01);
+                s23 = ffma2(make_float2(wv.z, wv.w),
+                            make_float2(fmaxf(x1[4 * i + 2], 0.f), fmaxf(x1[4 * i + 3], 0.f)), s23);
               }
             }
           }
-          const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          const float sum = (s01.x + s01.y) + (s23.x + s23.y);
           if (j < ntv[g]) srow[(int64_t)g * a.N_cap] = F8 ? sum * ks : sum;
         }
       } else {

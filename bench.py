@@ -114,12 +114,13 @@ def indexer_bytes(wl, keys="bf16"):
 
 # DRAM traffic of indexer_score_kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum) from one ncu capture of an 8 x 65,536-entry launch
-# (138.09 MB), per entry processed; it applies only to the kernel sources it
-# was taken on, checked by hash, else the bench reports traffic as null.
+# per key format (bf16 keys: 138.12 MB; E4M3 keys: 70.29 MB), per entry
+# processed; it applies only to the kernel sources it was taken on, checked
+# by hash, and to one query per sequence, else the bench reports null.
 INDEXER_TRAFFIC = {
-    "bytes_per_entry": 138.089e6 / (8 * 65536),
+    "bytes_per_entry": {"bf16": 138.117e6 / (8 * 65536), "fp8": 70.290e6 / (8 * 65536)},
     "sources": ["indexer.cu", "common.cuh"],
-    "sha256": "4750d762d6e002352e20659e3f4fd9e43cb406230eda7141f5f59d902f711cae",
+    "sha256": "ad7eac0e568a5b75a33423e009018756959790c99a987369e91df780a32f29dc",
     "profile": "profiles/indexer_score_kernel_decode_8x65536.md",
 }
 
@@ -127,8 +128,6 @@ INDEXER_TRAFFIC = {
 def indexer_traffic(wl, keys="bf16"):
     """Per-launch DRAM bytes scaled from the recorded capture, or None when
     the indexer sources have changed since it was taken."""
-    if keys != "bf16":
-        return None  # the capture is of bf16 keys
     import hashlib
     h = hashlib.sha256()
     for f in INDEXER_TRAFFIC["sources"]:
@@ -138,7 +137,7 @@ def indexer_traffic(wl, keys="bf16"):
         return None
     if wl.T != 1:
         return None  # the capture is of one query per sequence
-    return INDEXER_TRAFFIC["bytes_per_entry"] * wl.B * (wl.L // wl.m_csa)
+    return INDEXER_TRAFFIC["bytes_per_entry"][keys] * wl.B * (wl.L // wl.m_csa)
 
 
 INDEXER_KEYS = {"bf16": "bf16", "fp8": "e4m3 codes + fp32 row scale (queries quantised alike)"}

@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--context", type=int, default=0, help="override L (profiling only)")
     ap.add_argument("--indexer-keys", default="bf16", choices=["bf16", "fp8"],
                     help="indexer key cache: bf16, or E4M3 codes with a row scale")
+    ap.add_argument("--stack", type=int, default=0,
+                    help="time the decode step of N attention layers in the pages' pattern "
+                         "(2 SWA, then CSA and HCA alternating; 61 for V4-Pro) instead of one "
+                         "hybrid layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dense-sms", type=int, default=0,
@@ -498,6 +502,124 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def stack_bytes(wl, kinds):
+    """Algorithmic HBM bytes of one decode step of the layer stack: per
+    layer and sequence, its query in and output out, the new token's rows
+    into the ring, the W window rows; a CSA layer adds every indexer key, the
+    k gathered entries and the compression of the newest entry, an HCA layer
+    every visible HCA entry and the compression of the newest entry."""
+    B, L, D, dI, W = wl.B, wl.L, wl.D, wl.dI, wl.W
+    n_csa, n_hca = L // wl.m_csa, L // wl.m_hca
+    per = 0
+    for kind in kinds:
+        per += 2 * wl.H * D * 2 + wl.H * 4 + W * D * 2 + (D + 1) * 2
+        if kind == "csa":
+            per += n_csa * dI * 2 + min(wl.k, n_csa) * D * 2 + wl.HI * dI * 2 + wl.HI * 4
+            per += dI * 2 + wl.w_csa * (D + dI + 1) * 2 + (D + dI) * 2
+        elif kind == "hca":
+            per += n_hca * D * 2 + wl.w_hca * (D + 1) * 2 + D * 2
+    return B * per
+
+
+def run_stack(args, world, rank, local):
+    """The decode step of args.stack attention layers at the 1M shapes: every
+    layer appends the new token to its 256-row ring, compresses the entries
+    it completes (t = L-1 completes a CSA and an HCA entry) and runs its
+    fused attention and merge.  The compressed caches stand for a built 1M
+    context and are drawn directly (seeded N(0,1) bf16): the work of a step
+    does not depend on their values."""
+    import torch
+    from sparse_attention_26_b300 import hattn
+    from sparse_attention_26_b300.stack import DecodeStack, layer_pattern
+
+    hattn.lib()
+    dev = torch.device("cuda", local)
+    wl = workload(args)
+    kinds = layer_pattern(args.stack)
+    stack = DecodeStack(kinds, B=wl.B, H=wl.H, D=wl.D, r=wl.r, HI=wl.HI, dI=wl.dI, k=wl.k,
+                        L_max=wl.L, W=wl.W, device=dev)
+    for l in range(len(kinds)):
+        stack.fill_random(l, 1000 + l)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+
+    def rnd(shape, dtype=torch.bfloat16):
+        return torch.randn(shape, generator=g, device=dev).to(dtype)
+
+    n = len(kinds)
+    q = [rnd((wl.B, 1, wl.H, wl.D)) for _ in range(n)]
+    iq = [rnd((wl.B, 1, wl.HI, wl.dI)) for _ in range(n)]
+    w = [rnd((wl.B, 1, wl.HI), torch.float32) for _ in range(n)]
+    sinks = [rnd((wl.H,), torch.float32) for _ in range(n)]
+    new_kv = rnd((n, wl.B, wl.D))
+    new_ik = rnd((n, wl.B, wl.dI))
+    new_g = rnd((n, wl.B))
+    t = wl.L - 1
+    pos = torch.full((wl.B, 1), t, dtype=torch.int32, device=dev)
+
+    def step():
+        for l in range(n):
+            stack.append(l, t, new_kv[l], new_ik[l], new_g[l])
+        stack.step(t, q, iq, w, sinks, pos)
+
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    hattn.check_status()
+    K = args.steps
+    stream = torch.cuda.Stream(device=dev)
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream, capture_error_mode="relaxed"):
+        ev[0].record()
+        for _ in range(K):
+            step()
+        ev[1].record()
+    torch.cuda.synchronize()
+    gr.replay()
+    torch.cuda.synchronize()
+    hattn.check_status()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.perf_counter() + args.soak_ms / 1e3
+    while time.perf_counter() < t_end:
+        gr.replay()
+        torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    gr.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    hattn.check_status()
+    value, total_ms = job_throughput(world, wl.B * K, ev[0].elapsed_time(ev[1]))
+    ms_step = total_ms / K
+    hbm, _, src = peaks()
+    sb = stack_bytes(wl, kinds)
+    achieved = sb / (ms_step / 1e3) / 1e9
+    counts = {kd: kinds.count(kd) for kd in ("swa", "csa", "hca")}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(wl, workload=f"attention_stack_{len(kinds)}_layers_1m",
+                              l2=f"per-step input {sb / 1e9:.1f} GB > 126 MB L2 (no flush)",
+                              layers=counts, ring_tokens=stack.ring,
+                              caches="compressed caches drawn directly (seeded N(0,1) bf16) "
+                                     "for a built 1M context",
+                              parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "roofline": {"bound": "hbm", "kernel": "whole step (all layers)", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_step": sb},
+        "clocks": clocks, "gpu_launches": stack.launches_per_step(t) * K,
+        "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, world, layer, inp, wl, t_new, stream, side):
     """The same steps with every step's inputs coming from pinned host memory
     and its result going back, inside the timed region.  A step's inputs (q,
@@ -601,6 +723,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.stack:
+        run_stack(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

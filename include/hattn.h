@@ -92,6 +92,29 @@ HATTN_API int hattn_hca_compress(const void* kv_raw, const void* gate, const flo
                        int64_t j_begin, int64_t j_end, void* kv_h, int64_t N_cap,
                        hattn_stream_t stream);
 
+/* Ring-buffer raw caches.  A decode loop needs only the newest raw tokens:
+ * the compressors read the window of the entry the newest token completes
+ * (8 tokens for CSA, 128 for HCA) and the window keys the last W tokens.  In
+ * these forms the raw buffers kv_ring [B][ring][D], ik_ring [B][ring][dI] and
+ * gate_ring [B][ring] hold token u in row u mod ring (ring a power of two),
+ * so a 256-row ring replaces a 1M-row cache.  Positions (pos, entry indices)
+ * stay absolute.  The caller keeps every token a call reads in the ring:
+ * for the compressors the m*(j_end-j_begin)+w-m tokens ending at
+ * m*j_end-1, for the window keys the W+T-1 tokens ending at each
+ * sequence's newest query position.  Otherwise as hattn_csa_compress,
+ * hattn_hca_compress and hattn_swa_keys. */
+HATTN_API int hattn_csa_compress_ring(const void* kv_ring, const void* ik_ring,
+                                      const void* gate_ring, const float* gamma_kv, int B,
+                                      int64_t ring, int D, int dI, int m, int w, int r,
+                                      float rope_base, float eps, int64_t j_begin, int64_t j_end,
+                                      void* kv_c, void* ik_c, int64_t N_cap,
+                                      hattn_stream_t stream);
+HATTN_API int hattn_hca_compress_ring(const void* kv_ring, const void* gate_ring,
+                                      const float* gamma_kv, int B, int64_t ring, int D, int m,
+                                      int r, float rope_base, float eps, int64_t j_begin,
+                                      int64_t j_end, void* kv_h, int64_t N_cap,
+                                      hattn_stream_t stream);
+
 /* -------------------------------------------------------------------------
  * FP8 indexer keys.  [AT] "Inference efficiency": the indexer's QK path runs
  * in low precision.  The pages name no format; this library stores E4M3
@@ -268,6 +291,11 @@ HATTN_API int hattn_swa_attn(const void* q, const float* gamma_q, int q_prepped,
 HATTN_API int hattn_swa_keys(const void* kv_raw, const float* gamma_kv, const int32_t* pos, int B,
                              int T, int64_t L_cap, int D, int W, int r, float rope_base,
                              float eps, void* kv_w, hattn_stream_t stream);
+/* hattn_swa_keys over a ring-buffer raw cache kv_ring [B][ring][D] (token u
+ * in row u mod ring; ring a power of two, at least W + T - 1). */
+HATTN_API int hattn_swa_keys_ring(const void* kv_ring, const float* gamma_kv, const int32_t* pos,
+                                  int B, int T, int64_t ring, int D, int W, int r,
+                                  float rope_base, float eps, void* kv_w, hattn_stream_t stream);
 
 /* The three branches as one attention ([DD] CSA + HCA + SWA, merged by
  * log-sum-exp): for each query the keys are the selected CSA entries

@@ -141,7 +141,7 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
                     const float* gamma_kv, int B, int64_t L_cap, int D, int dI, int m, int w,
                     int r, float rope_base, float eps, int64_t j_begin, int64_t j_end, void* kv_c,
                     void* ik_c, int64_t N_cap, hattn_stream_t stream, void* ik8 = nullptr,
-                    float* ik_scale = nullptr) {
+                    float* ik_scale = nullptr, int64_t ring = 0) {
   REQUIRE_PTR(kv_raw);
   REQUIRE_PTR(gate);
   REQUIRE_PTR(kv_c);
@@ -165,8 +165,18 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
   if (rc) return rc;
   REQUIRE(j_begin >= 0 && j_end >= j_begin && j_end <= N_cap, "entry range [%lld, %lld) outside [0, N_cap=%lld)",
           (long long)j_begin, (long long)j_end, (long long)N_cap);
-  REQUIRE((int64_t)m * j_end <= L_cap, "entry %lld needs tokens beyond L_cap=%lld", (long long)(j_end - 1),
-          (long long)L_cap);
+  if (ring > 0) {
+    // the raw buffers hold the last `ring` tokens: the window of every entry
+    // compressed in this call must still be in it
+    REQUIRE((ring & (ring - 1)) == 0 && ring == L_cap, "ring=%lld must be a power of two equal to L_cap",
+            (long long)ring);
+    REQUIRE((int64_t)m * (j_end - j_begin) + w - m <= ring,
+            "entries [%lld, %lld) span more tokens than the ring of %lld holds", (long long)j_begin,
+            (long long)j_end, (long long)ring);
+  } else {
+    REQUIRE((int64_t)m * j_end <= L_cap, "entry %lld needs tokens beyond L_cap=%lld", (long long)(j_end - 1),
+            (long long)L_cap);
+  }
   if (j_end == j_begin) return ok();
   CompressArgs a;
   a.kv_raw = static_cast<const __nv_bfloat16*>(kv_raw);
@@ -187,6 +197,7 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
   a.N_cap = N_cap;
   a.j_begin = j_begin;
   a.j_end = j_end;
+  a.ring = ring;
   a.eps = eps;
   make_rope_coef(rope_base, r, &a.rope);
   cudaError_t e = launch_compress(a, num_sms_or_default(), static_cast<cudaStream_t>(stream));
@@ -461,6 +472,25 @@ int hattn_csa_compress_fp8(const void* kv_raw, const void* ik_raw, const void* g
   REQUIRE_PTR(ik_scale);
   return compress_common(kv_raw, ik_raw, gate, gamma_kv, B, L_cap, D, dI, m, w, r, rope_base, eps,
                          j_begin, j_end, kv_c, ik_c, N_cap, stream, ik8, ik_scale);
+}
+
+int hattn_csa_compress_ring(const void* kv_ring, const void* ik_ring, const void* gate_ring,
+                            const float* gamma_kv, int B, int64_t ring, int D, int dI, int m,
+                            int w, int r, float rope_base, float eps, int64_t j_begin,
+                            int64_t j_end, void* kv_c, void* ik_c, int64_t N_cap,
+                            hattn_stream_t stream) {
+  REQUIRE(ring >= 1, "ring=%lld must be >= 1", (long long)ring);
+  return compress_common(kv_ring, ik_ring, gate_ring, gamma_kv, B, ring, D, dI, m, w, r, rope_base,
+                         eps, j_begin, j_end, kv_c, ik_c, N_cap, stream, nullptr, nullptr, ring);
+}
+
+int hattn_hca_compress_ring(const void* kv_ring, const void* gate_ring, const float* gamma_kv,
+                            int B, int64_t ring, int D, int m, int r, float rope_base, float eps,
+                            int64_t j_begin, int64_t j_end, void* kv_h, int64_t N_cap,
+                            hattn_stream_t stream) {
+  REQUIRE(ring >= 1, "ring=%lld must be >= 1", (long long)ring);
+  return compress_common(kv_ring, nullptr, gate_ring, gamma_kv, B, ring, D, 0, m, m, r, rope_base,
+                         eps, j_begin, j_end, kv_h, nullptr, N_cap, stream, nullptr, nullptr, ring);
 }
 
 int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* codes, float* scales,
@@ -797,9 +827,9 @@ int hattn_hybrid_attn_splits(int B, int T, int H, int D, int k, int64_t N_h, int
   return p.nsplit;
 }
 
-int hattn_swa_keys(const void* kv_raw, const float* gamma_kv, const int32_t* pos, int B, int T,
-                   int64_t L_cap, int D, int W, int r, float rope_base, float eps, void* kv_w,
-                   hattn_stream_t stream) {
+static int swa_keys_common(const void* kv_raw, const float* gamma_kv, const int32_t* pos, int B, int T,
+                    int64_t L_cap, int D, int W, int r, float rope_base, float eps, void* kv_w,
+                    hattn_stream_t stream, int64_t ring) {
   REQUIRE_PTR(kv_raw);
   REQUIRE_PTR(pos);
   REQUIRE_PTR(kv_w);
@@ -820,11 +850,30 @@ int hattn_swa_keys(const void* kv_raw, const float* gamma_kv, const int32_t* pos
   a.r = r;
   a.W = W;
   a.L_cap = L_cap;
+  a.ring = ring;
   a.eps = eps;
   make_rope_coef(rope_base, r, &a.rope);
   cudaError_t e = launch_swa_keys(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "SWA keys launch");
   return ok();
+}
+
+int hattn_swa_keys(const void* kv_raw, const float* gamma_kv, const int32_t* pos, int B, int T,
+                   int64_t L_cap, int D, int W, int r, float rope_base, float eps, void* kv_w,
+                   hattn_stream_t stream) {
+  return swa_keys_common(kv_raw, gamma_kv, pos, B, T, L_cap, D, W, r, rope_base, eps, kv_w, stream,
+                         0);
+}
+
+int hattn_swa_keys_ring(const void* kv_ring, const float* gamma_kv, const int32_t* pos, int B,
+                        int T, int64_t ring, int D, int W, int r, float rope_base, float eps,
+                        void* kv_w, hattn_stream_t stream) {
+  // the T queries of a sequence together need the W + T - 1 newest tokens
+  REQUIRE(ring >= 1 && (ring & (ring - 1)) == 0, "ring=%lld must be a power of two", (long long)ring);
+  REQUIRE(ring >= (int64_t)W + T - 1, "ring=%lld holds fewer than W + T - 1 = %d tokens", (long long)ring,
+          W + T - 1);
+  return swa_keys_common(kv_ring, gamma_kv, pos, B, T, ring, D, W, r, rope_base, eps, kv_w, stream,
+                         ring);
 }
 
 int hattn_swa_attn(const void* q, const float* gamma_q, int q_prepped, const void* kv_raw,

@@ -47,6 +47,12 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&y)[8]) {
   *reinterpret_cast<uint4*>(p) = u;
 }
 
+// Row of token u in the raw buffers: u itself, or u mod ring when they are a
+// ring of the last `ring` tokens (a power of two).
+__device__ __forceinline__ int64_t token_row(const CompressArgs& a, int64_t u) {
+  return a.ring > 0 ? (u & (a.ring - 1)) : u;
+}
+
 // Largest magnitude of the bf16-rounded values of one 8-wide piece.
 __device__ __forceinline__ float amax8_bf16(const float (&y)[8]) {
   float m = 0.f;
@@ -111,7 +117,7 @@ __global__ void __launch_bounds__(kCompressThreads)
       for (int q = 0; q < 8; ++q) {
         const int i = s_pre + q * S;
         const int64_t u = u0 + i;
-        pre[q] = (i < a.w && u >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + u * stride))
+        pre[q] = (i < a.w && u >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + token_row(a, u) * stride))
                                      : make_uint4(0, 0, 0, 0);
       }
     }
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(kCompressThreads)
       float gmax = -INFINITY;
       for (int s = tid; s < a.w; s += 32) {
         int64_t u = u0 + s;
-        if (u >= 0) gmax = fmaxf(gmax, __bfloat162float(a.gate[(int64_t)b * a.L_cap + u]));
+        if (u >= 0) gmax = fmaxf(gmax, __bfloat162float(a.gate[(int64_t)b * a.L_cap + token_row(a, u)]));
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
@@ -129,7 +135,7 @@ __global__ void __launch_bounds__(kCompressThreads)
       for (int s = tid; s < a.w; s += 32) {
         int64_t u = u0 + s;
         float e = 0.f;
-        if (u >= 0) e = __expf(__bfloat162float(a.gate[(int64_t)b * a.L_cap + u]) - gmax);
+        if (u >= 0) e = __expf(__bfloat162float(a.gate[(int64_t)b * a.L_cap + token_row(a, u)]) - gmax);
         alpha[s] = e;
         z += e;
       }
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(kCompressThreads)
           if (one_pass)
             v[q] = pre[q];  // requested before the softmax (zero where not live)
           else
-            v[q] = live ? __ldg(reinterpret_cast<const uint4*>(src + u * stride))
+            v[q] = live ? __ldg(reinterpret_cast<const uint4*>(src + token_row(a, u) * stride))
                         : make_uint4(0, 0, 0, 0);
           al[q] = live ? alpha[i] : 0.f;
         }
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(kSmallThreads)
 #pragma unroll
       for (int q = 0; q < kSmallMaxW; ++q) {
         const int64_t u = u0 + q;
-        v[q] = (q < a.w && u >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + u * stride))
+        v[q] = (q < a.w && u >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + token_row(a, u) * stride))
                                    : make_uint4(0, 0, 0, 0);
       }
     }
@@ -305,7 +311,7 @@ __global__ void __launch_bounds__(kSmallThreads)
     if (tid < 32) {
       const int64_t u = u0 + tid;
       const bool live = tid < a.w && u >= 0;
-      const float g = live ? __bfloat162float(a.gate[(int64_t)b * a.L_cap + u]) : -INFINITY;
+      const float g = live ? __bfloat162float(a.gate[(int64_t)b * a.L_cap + token_row(a, u)]) : -INFINITY;
       float gmax = g;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));

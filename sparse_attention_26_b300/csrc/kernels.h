@@ -31,6 +31,7 @@ struct CompressArgs {
   float* ik_scale_out;          // [B][N_cap] their row scales (with ik8_out)
   int B, D, dI, m, w, r;
   int64_t L_cap, N_cap, j_begin, j_end;
+  int64_t ring;                 // 0: token u in row u; else row u mod ring (L_cap == ring)
   float eps;
   RopeCoef rope;
 };
@@ -151,6 +152,7 @@ struct SwaKeysArgs {
   __nv_bfloat16* kv_w;          // [B][T][W][D]
   int B, T, D, r, W;
   int64_t L_cap;
+  int64_t ring;                 // 0: token u in row u; else row u mod ring (L_cap == ring)
   float eps;
   RopeCoef rope;
 };

@@ -123,8 +123,10 @@ __global__ void __launch_bounds__(kQpThreads)
   const int j = static_cast<int>(row - bt * a.W);
   const int64_t b = bt / a.T;
   const int64_t u = static_cast<int64_t>(a.pos[bt]) - a.W + 1 + j;
-  const bool exists = u >= 0 && u < a.L_cap;
-  norm_rope_row(exists ? a.kv_raw + (b * a.L_cap + u) * a.D : nullptr, a.kv_w + row * a.D, a.D,
+  // in a ring of the last `ring` tokens (a power of two), token u is row u mod ring
+  const bool exists = u >= 0 && (a.ring > 0 || u < a.L_cap);
+  const int64_t ru = a.ring > 0 ? (u & (a.ring - 1)) : u;
+  norm_rope_row(exists ? a.kv_raw + (b * a.L_cap + ru) * a.D : nullptr, a.kv_w + row * a.D, a.D,
                 a.r, u, a.gamma, a.eps, rc, lane);
 }
 

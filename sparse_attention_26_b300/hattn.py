@@ -36,6 +36,12 @@ _SIGS = {
                                       _i32, _f32, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _i64,
                                       _vp]),
     "hattn_quantize_e4m3": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp]),
+    "hattn_csa_compress_ring": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
+                                       _i32, _f32, _f32, _i64, _i64, _vp, _vp, _i64, _vp]),
+    "hattn_hca_compress_ring": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _f32, _f32,
+                                       _i64, _i64, _vp, _i64, _vp]),
+    "hattn_swa_keys_ring": (_i32, [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _f32, _f32,
+                                   _vp, _vp]),
     "hattn_indexer_scores_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
                                         _i32, _i32, _i64, _vp, _vp]),
     "hattn_indexer_topk": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
@@ -195,6 +201,54 @@ def csa_compress_fp8(kv_raw, ik_raw, gate, *, r, j_begin=0, j_end=None, m=4, w=8
                                         _ptr(kv_c), _ptr(ik_c), _ptr(ik8), _ptr(ik_scale), N_cap,
                                         _stream(stream)))
     return kv_c, ik8, ik_scale
+
+
+def csa_compress_ring(kv_ring, ik_ring, gate_ring, *, r, j_begin, j_end, kv_c, ik_c, m=4, w=8,
+                      gamma_kv=None, rope_base=10000.0, eps=1e-6, stream=None):
+    """csa_compress over ring-buffer raw caches ([B, ring, ...], token u in
+    row u % ring) into kv_c / ik_c rows [j_begin, j_end)."""
+    _need(kv_ring, "kv_ring", torch.bfloat16, 3)
+    _need(ik_ring, "ik_ring", torch.bfloat16, 3)
+    _need(gate_ring, "gate_ring", torch.bfloat16, 2)
+    _need(kv_c, "kv_c", torch.bfloat16, 3)
+    _need(ik_c, "ik_c", torch.bfloat16, 3)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    B, ring, D = kv_ring.shape
+    _check(lib().hattn_csa_compress_ring(_ptr(kv_ring), _ptr(ik_ring), _ptr(gate_ring),
+                                         _ptr(gamma_kv), B, ring, D, ik_ring.shape[2], m, w, r,
+                                         rope_base, eps, j_begin, j_end, _ptr(kv_c), _ptr(ik_c),
+                                         kv_c.shape[1], _stream(stream)))
+    return kv_c, ik_c
+
+
+def hca_compress_ring(kv_ring, gate_ring, *, r, j_begin, j_end, kv_h, m=128, gamma_kv=None,
+                      rope_base=10000.0, eps=1e-6, stream=None):
+    """hca_compress over ring-buffer raw caches into kv_h rows [j_begin, j_end)."""
+    _need(kv_ring, "kv_ring", torch.bfloat16, 3)
+    _need(gate_ring, "gate_ring", torch.bfloat16, 2)
+    _need(kv_h, "kv_h", torch.bfloat16, 3)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    B, ring, D = kv_ring.shape
+    _check(lib().hattn_hca_compress_ring(_ptr(kv_ring), _ptr(gate_ring), _ptr(gamma_kv), B, ring,
+                                         D, m, r, rope_base, eps, j_begin, j_end, _ptr(kv_h),
+                                         kv_h.shape[1], _stream(stream)))
+    return kv_h
+
+
+def swa_keys_ring(kv_ring, pos, *, r, W=128, gamma_kv=None, rope_base=10000.0, eps=1e-6,
+                  kv_w=None, stream=None):
+    """swa_keys over a ring-buffer raw cache [B, ring, D] (token u in row u % ring)."""
+    _need(kv_ring, "kv_ring", torch.bfloat16, 3)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    B, ring, D = kv_ring.shape
+    T = pos.shape[1]
+    if kv_w is None:
+        kv_w = torch.empty((B, T, W, D), dtype=torch.bfloat16, device=kv_ring.device)
+    _need(kv_w, "kv_w", torch.bfloat16, 4)
+    _check(lib().hattn_swa_keys_ring(_ptr(kv_ring), _ptr(gamma_kv), _ptr(pos), B, T, ring, D, W, r,
+                                     rope_base, eps, _ptr(kv_w), _stream(stream)))
+    return kv_w
 
 
 def quantize_e4m3(x, *, codes=None, scales=None, stream=None):

@@ -5,7 +5,7 @@ Each test runs one pass of the layer exactly as the benchmark launches it
 queries stage by stage against the fp64 oracle.  To keep the oracle to
 seconds, each downstream stage is fed the GPU's own upstream tensors (its
 compressed caches and its top-k indices), and the compressor is checked on
-sampled entries; near-tie swaps in top-k are judged by the tolerance rule,
+sampled entries; near-tie swaps in top-k are decided by the tolerance rule,
 not by the attention comparison.
 """
 import numpy as np

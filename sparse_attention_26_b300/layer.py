@@ -90,8 +90,9 @@ class HybridLayer:
         )
         b["qt"] = torch.empty((B, T, H, D), dtype=bf, device=dev)  # prepared queries
         if self.can_fuse(T):
-            b["kv_w"] = torch.empty((B, T, wl.W, D), dtype=bf, device=dev)  # SWA keys
-            for name, segs, n_sms in [("fused", hattn.SEG_ALL, 0),
+            if "swa" in wl.branches:
+                b["kv_w"] = torch.empty((B, T, wl.W, D), dtype=bf, device=dev)  # SWA keys
+            for name, segs, n_sms in [("fused", self.segments(), 0),
                                       ("dense", hattn.SEG_HCA | hattn.SEG_SWA,
                                        self.override_dense_sms),
                                       ("sparse", hattn.SEG_CSA, 0)]:
@@ -144,13 +145,22 @@ class HybridLayer:
         """The one device buffer holding out (bf16) then lse (fp32) of step()."""
         return self.buffers(T)["result"]
 
+    def segments(self):
+        """The fused attention's segment mask for this layer's branches."""
+        m = {"csa": hattn.SEG_CSA, "hca": hattn.SEG_HCA, "swa": hattn.SEG_SWA}
+        seg = 0
+        for name in self.wl.branches:
+            seg |= m[name]
+        return seg
+
     def can_fuse(self, T):
-        """The fused attention serves layers with all three branches, one query
-        per row block (H = 128, or single-token decode) and a window buffer
-        of at most 256 MB."""
+        """The fused attention serves one query per row block (H = 128, or
+        single-token decode) with a window buffer of at most 256 MB: decode
+        steps of any branch subset, and all three branches at any T."""
         wl = self.wl
-        return (set(wl.branches) == {"csa", "hca", "swa"} and (wl.H == 128 or T == 1)
-                and self.B * T * wl.W * self.D * 2 <= (256 << 20))
+        fits = "swa" not in wl.branches or self.B * T * wl.W * self.D * 2 <= (256 << 20)
+        all_three = set(wl.branches) == {"csa", "hca", "swa"}
+        return (wl.H == 128 or T == 1) and fits and (all_three or T <= 2)
 
     def _branch_kinds(self):
         wl = self.wl
@@ -191,7 +201,7 @@ class HybridLayer:
         """Compress the entries that the step's new tokens complete."""
         wl, r = self.wl, self.raw
         j0, j1 = self.new_entries(kind, t_new, n_new)
-        if j1 <= j0:
+        if j1 <= j0 or kind not in wl.branches:
             return
         if kind == "csa":
             self._csa_compress(j0, j1)
@@ -316,14 +326,24 @@ class HybridLayer:
         def compress(kind):
             self._compress_new(kind, t_new, T)
 
+        has = set(wl.branches)
+
         def attn(name, segments, n_sms):
             ev("attn_" + name, 0)
-            part = hattn.hybrid_attn(b["qt"], self.kv_c, b["idx"], self.kv_h, b["kv_w"], pos,
-                                     r=wl.r, m=wl.m_hca, workspace=b["ws_" + name],
-                                     q_prepped=True, partials=True, segments=segments,
-                                     n_sms=n_sms)
+            part = hattn.hybrid_attn(b["qt"], self.kv_c if "csa" in has else None,
+                                     b["idx"] if "csa" in has else None,
+                                     self.kv_h if "hca" in has else None, b.get("kv_w"), pos,
+                                     r=wl.r, m=wl.m_hca, k=wl.k, W=wl.W,
+                                     workspace=b["ws_" + name], q_prepped=True, partials=True,
+                                     segments=segments, n_sms=n_sms)
             ev("attn_" + name, 1)
             return part
+
+        def swa_keys():
+            if "swa" in has:
+                ev("swa_keys", 0)
+                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
+                ev("swa_keys", 1)
 
         def qprep():
             ev("qprep", 0)
@@ -335,8 +355,15 @@ class HybridLayer:
         # B300 it needs all of them (capped at 100 SMs it runs ~40% longer),
         # so the split is opt-in (override_dense_sms) and the default runs the
         # three key sets as one attention after top-k.
-        n_dense = self.override_dense_sms if side_stream is not None else 0
+        all_three = has == {"csa", "hca", "swa"}
+        n_dense = self.override_dense_sms if (side_stream is not None and all_three) else 0
         overlap = n_dense > 0
+        # dependent launches when the caller runs the step as the benchmark
+        # does (with a side stream, without per-call events)
+        pdl = side_stream is not None and self.dependent_launch and events is None
+        if "csa" not in has:
+            # no indexer to run beside: the layer's calls follow one another
+            side_stream = None
         ev("compress", 0)
         compress("csa")
         if side_stream is None:
@@ -345,28 +372,25 @@ class HybridLayer:
         # from here on each main-stream call consumes what the one before it
         # produced, so its kernel may start as a dependent launch (its setup
         # overlaps the predecessor's tail; it waits before reading inputs)
-        pdl = side_stream is not None and self.dependent_launch and events is None
         prev_pdl = hattn.set_dependent_launch(pdl)
         if side_stream is not None and overlap:
             qprep()
             side_stream.wait_stream(main)
             with torch.cuda.stream(side_stream):
                 compress("hca")
-                ev("swa_keys", 0)
-                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
-                ev("swa_keys", 1)
+                swa_keys()
                 dense = attn("dense", hattn.SEG_HCA | hattn.SEG_SWA, n_dense)
         elif side_stream is None:
             qprep()
-            ev("swa_keys", 0)
-            hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
-            ev("swa_keys", 1)
-        ev("indexer", 0)
-        # the entries the compression above writes are the newest ones
-        j0, j1 = self.new_entries("csa", t_new, T)
-        self._indexer(iq, w, pos, b["scores"], n_sms=(self.NUM_SMS - n_dense) if n_dense else 0,
-                      fresh_from=j0 if j1 > j0 else -1)
-        ev("indexer", 1)
+            swa_keys()
+        if "csa" in has:
+            ev("indexer", 0)
+            # the entries the compression above writes are the newest ones
+            j0, j1 = self.new_entries("csa", t_new, T)
+            self._indexer(iq, w, pos, b["scores"],
+                          n_sms=(self.NUM_SMS - n_dense) if n_dense else 0,
+                          fresh_from=j0 if j1 > j0 else -1)
+            ev("indexer", 1)
         if side_stream is not None and not overlap:
             # The query preparation, the HCA compression and the window keys
             # (needed only by the attention) run beside top-k, which leaves
@@ -377,12 +401,11 @@ class HybridLayer:
             with torch.cuda.stream(side_stream):
                 qprep()
                 compress("hca")
-                ev("swa_keys", 0)
-                hattn.swa_keys(r["kv_raw"], pos, r=wl.r, W=wl.W, kv_w=b["kv_w"])
-                ev("swa_keys", 1)
-        ev("topk", 0)
-        hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
-        ev("topk", 1)
+                swa_keys()
+        if "csa" in has:
+            ev("topk", 0)
+            hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
+            ev("topk", 1)
         if overlap:
             parts = [attn("sparse", hattn.SEG_CSA, 0)]
             main.wait_stream(side_stream)
@@ -390,7 +413,7 @@ class HybridLayer:
         else:
             if side_stream is not None:
                 main.wait_stream(side_stream)
-            parts = [attn("fused", hattn.SEG_ALL, 0)]
+            parts = [attn("fused", self.segments(), 0)]
         ev("merge", 0)
         hattn.lse_merge_splits(parts, pos, r=wl.r, H=wl.H, sink=sink, out=b["out"],
                                lse_out=b["lse"])
@@ -403,10 +426,17 @@ class HybridLayer:
         if fused is None:
             fused = self.can_fuse(T) and not branch_outputs
         if fused:
-            split = side_stream and self.override_dense_sms > 0
+            has = set(self.wl.branches)
+            split = side_stream and self.override_dense_sms > 0 and has == {"csa", "hca", "swa"}
             attn = ["attn_dense", "attn_sparse"] if split else ["attn_fused"]
-            return ["compress", "swa_keys", "qprep", "indexer", "topk"] + attn + ["merge"]
-        return ["compress", "qprep", "indexer", "topk", "sparse", "hca", "swa", "merge"]
+            names = ["compress"] + (["swa_keys"] if "swa" in has else []) + ["qprep"]
+            names += ["indexer", "topk"] if "csa" in has else []
+            return names + attn + ["merge"]
+        names = ["compress", "qprep"]
+        if "csa" in self.wl.branches:
+            names += ["indexer", "topk", "sparse"]
+        names += [n for n in ("hca", "swa") if n in self.wl.branches]
+        return names + ["merge"]
 
     def launches_per_step(self, T, t_new=None, branch_outputs=False, fused=None,
                           side_stream=False):
@@ -424,7 +454,9 @@ class HybridLayer:
         if fused:
             # SWA keys, indexer scores, top-k, and the attention: one call, or
             # the dense and the sparse key sets when a side stream is used
-            return n + 4 + int(side_stream and self.override_dense_sms > 0)
+            has = set(wl.branches)
+            split = side_stream and self.override_dense_sms > 0 and has == {"csa", "hca", "swa"}
+            return (n + int("swa" in has) + 2 * int("csa" in has) + 1 + int(split))
         for name, kind, nk in self._branch_kinds():
             n += 1 + int(branch_outputs and hattn.attn_splits(kind, B, T, H, D, nk) > 1)
             if name == "csa":

@@ -199,6 +199,78 @@ int orc_compress(const uint16_t* kv_raw, const uint16_t* ik_raw, const uint16_t*
     return ORC_OK;
 }
 
+/*
+ * C(m, w) of projected hidden states ("Why DeepSeek V4 Stands Apart",
+ * section "Core Architectural Innovations": the compressor that turns the
+ * per-token KV into compressed entries, here fed from the hidden states).
+ * Each token's KV and indexer-key row is the projection x_u . W of its
+ * hidden state, in fp64 without rounding: W [dm][D + dI] bf16 holds the KV
+ * columns, then the indexer-key columns.  The entries then follow
+ * orc_compress: gate-softmax pooling of the window's projected rows, RMSNorm
+ * and RoPE of the KV part.  x [B][L_cap][dm] bf16.
+ */
+int orc_compress_hidden(const uint16_t* x, const uint16_t* W, const uint16_t* gate,
+                        const float* gamma, int B, int64_t L_cap, int dm, int D, int dI, int m,
+                        int w, int r, double base, double eps, int64_t j_begin, int64_t j_end,
+                        double* kv_out, double* ik_out) {
+    if (B <= 0 || L_cap <= 0 || dm <= 0 || D <= 0 || dI < 0 || m <= 0 || w <= 0 || r < 0 ||
+        r > D || (r % 2) || j_begin < 0 || j_end < j_begin)
+        return ORC_EINVAL;
+    if ((int64_t)m * j_end > L_cap) return ORC_EINVAL;
+    const int P = D + dI;
+    int64_t nj = j_end - j_begin;
+    double* alpha = (double*)malloc(sizeof(double) * (size_t)w);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)P);
+    double* proj = (double*)malloc(sizeof(double) * (size_t)P);
+    double* Wd = (double*)malloc(sizeof(double) * (size_t)dm * P);
+    if (!alpha || !acc || !proj || !Wd) {
+        free(alpha); free(acc); free(proj); free(Wd);
+        return ORC_ENOMEM;
+    }
+    for (int64_t i = 0; i < (int64_t)dm * P; ++i) Wd[i] = orc_bf16_to_f64(W[i]);
+    for (int b = 0; b < B; ++b) {
+        for (int64_t j = j_begin; j < j_end; ++j) {
+            int64_t u0 = (int64_t)m * (j + 1) - w;
+            double gmax = -INFINITY;
+            for (int s = 0; s < w; ++s) {
+                int64_t u = u0 + s;
+                if (u < 0) continue;
+                double g = orc_bf16_to_f64(gate[(int64_t)b * L_cap + u]);
+                if (g > gmax) gmax = g;
+            }
+            double z = 0.0;
+            for (int s = 0; s < w; ++s) {
+                int64_t u = u0 + s;
+                if (u < 0) { alpha[s] = 0.0; continue; }
+                alpha[s] = exp(orc_bf16_to_f64(gate[(int64_t)b * L_cap + u]) - gmax);
+                z += alpha[s];
+            }
+            for (int s = 0; s < w; ++s) alpha[s] /= z;
+            for (int c = 0; c < P; ++c) acc[c] = 0.0;
+            for (int s = 0; s < w; ++s) {
+                int64_t u = u0 + s;
+                if (u < 0) continue;
+                /* the token's projected row */
+                const uint16_t* xr = x + ((int64_t)b * L_cap + u) * dm;
+                for (int c = 0; c < P; ++c) proj[c] = 0.0;
+                for (int i = 0; i < dm; ++i) {
+                    double xi = orc_bf16_to_f64(xr[i]);
+                    const double* wr = Wd + (int64_t)i * P;
+                    for (int c = 0; c < P; ++c) proj[c] += xi * wr[c];
+                }
+                for (int c = 0; c < P; ++c) acc[c] += alpha[s] * proj[c];
+            }
+            orc_rmsnorm(acc, D, gamma, eps);
+            orc_rope(acc, D, r, base, (int64_t)m * (j + 1) - 1, +1);
+            int64_t o = (int64_t)b * nj + (j - j_begin);
+            memcpy(kv_out + o * D, acc, sizeof(double) * (size_t)D);
+            if (ik_out && dI > 0) memcpy(ik_out + o * dI, acc + D, sizeof(double) * (size_t)dI);
+        }
+    }
+    free(alpha); free(acc); free(proj); free(Wd);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* Lightning indexer score and top-k  ([DD] "Core Architectural         */
 /* Innovations": top-1024 / top-512 entries per query; [AT] "Design     */

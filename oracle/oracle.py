@@ -47,6 +47,12 @@ def lib():
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_double, ctypes.c_double,
                                    ctypes.c_int64, ctypes.c_int64, _f64p, _f64p, _f64p]
+        L.orc_compress_hidden.restype = ctypes.c_int
+        L.orc_compress_hidden.argtypes = [_u16p, _u16p, _u16p, _f32p, ctypes.c_int, ctypes.c_int64,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                          ctypes.c_double, ctypes.c_int64, ctypes.c_int64, _f64p,
+                                          _f64p]
         L.orc_visible.restype = ctypes.c_int64
         L.orc_visible.argtypes = [ctypes.c_int64, ctypes.c_int]
         L.orc_indexer_scores.restype = ctypes.c_int
@@ -168,6 +174,27 @@ def compress(kv_raw, gate, m, w, r, j_begin, j_end, ik_raw=None, gamma=None, bas
                             _p(ik, _f64p), _p(alpha, _f64p))
     _check(rc, "compress")
     return kv, ik, alpha
+
+
+def compress_hidden(x, W, gate, m, w, r, j_begin, j_end, D, gamma=None, base=10000.0, eps=1e-6):
+    """C(m, w) of the projected hidden states x [B, L, dm] (bf16 bits) with
+    W [dm, D + dI] (bf16 bits: KV columns, then indexer-key columns): every
+    token projected in fp64, then pooled, normed and roped.  Returns fp64
+    (kv [B, nj, D], ik [B, nj, dI] or None)."""
+    x = _u16(x)
+    W = _u16(W)
+    gate = _u16(gate)
+    B, L, dm = x.shape
+    dI = W.shape[1] - D
+    nj = j_end - j_begin
+    kv = np.zeros((B, nj, D), np.float64)
+    ik = np.zeros((B, nj, dI), np.float64) if dI else None
+    g = _f32(gamma)
+    rc = lib().orc_compress_hidden(_p(x, _u16p), _p(W, _u16p), _p(gate, _u16p), _p(g, _f32p), B, L,
+                                   dm, D, dI, m, w, r, base, eps, j_begin, j_end, _p(kv, _f64p),
+                                   _p(ik, _f64p))
+    _check(rc, "compress_hidden")
+    return kv, ik
 
 
 def indexer_scores(iq, w, ik, pos, m):

@@ -184,6 +184,40 @@ def test_indexer_special_cases(orc):
     np.testing.assert_allclose(s12[ok], (s1 + s2)[ok], rtol=1e-5, atol=1e-5)
 
 
+# --------------------------------------------------------------------- compressor from hidden states
+def test_compress_hidden_with_identity_projection_is_compress(orc):
+    """W = [I 0; 0 I] makes each projected row the hidden state itself, so the
+    result equals the compressor over those rows exactly."""
+    rng = np.random.default_rng(31)
+    B, L, D, dI, r = 2, 40, 16, 8, 4
+    x = b16(rng.standard_normal((B, L, D + dI)))
+    gate = b16(rng.standard_normal((B, L)))
+    W = b16(np.eye(D + dI))
+    kv, ik = orc.compress_hidden(x, W, gate, 4, 8, r, 0, L // 4, D)
+    rk, ri, _ = orc.compress(np.ascontiguousarray(x[..., :D]), gate, 4, 8, r, 0, L // 4,
+                             ik_raw=np.ascontiguousarray(x[..., D:]))
+    np.testing.assert_array_equal(kv, rk)
+    np.testing.assert_array_equal(ik, ri)
+
+
+def test_compress_hidden_single_token_window_is_norm_of_projection(orc):
+    """With m = w = 1 the entry of token u is RMSNorm(x_u . W_kv), roped at
+    u, and its indexer key x_u . W_ik: compared with torch's fp64 matmul and
+    rms_norm and the (separately pinned) RoPE."""
+    rng = np.random.default_rng(32)
+    B, L, dm, D, dI, r = 1, 6, 24, 16, 8, 4
+    x = b16(rng.standard_normal((B, L, dm)))
+    W = b16(rng.standard_normal((dm, D + dI)) / np.sqrt(dm))
+    gate = b16(rng.standard_normal((B, L)))
+    kv, ik = orc.compress_hidden(x, W, gate, 1, 1, r, 0, L, D)
+    y = torch.from_numpy(f64(x)) @ torch.from_numpy(f64(W))
+    ref_kv = torch.nn.functional.rms_norm(y[..., :D], (D,), eps=1e-6).numpy()
+    for u in range(L):
+        np.testing.assert_allclose(kv[0, u], orc.rope(ref_kv[0, u], r, u), rtol=1e-12,
+                                   atol=1e-12)
+    np.testing.assert_allclose(ik, y[..., D:].numpy(), rtol=1e-12, atol=1e-12)
+
+
 # --------------------------------------------------------------------- FP8 (E4M3) keys
 def _torch_e4m3(x32):
     """torch's float8_e4m3fn cast (nearest even, NaN past 464) as uint8 codes."""

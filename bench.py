@@ -27,6 +27,7 @@ reference this layer has) on one sequence of the same workload per step.
 """
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -55,6 +56,9 @@ def parse():
                     help="time the decode step of N attention layers in the pages' pattern "
                          "(2 SWA, then CSA and HCA alternating; 61 for V4-Pro) instead of one "
                          "hybrid layer")
+    ap.add_argument("--cache-build", action="store_true",
+                    help="time building the CSA and HCA caches of one 1M-token sequence "
+                         "straight from V4-Pro hidden states (d_model 7168)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dense-sms", type=int, default=0,
@@ -697,6 +701,82 @@ def run_stack(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_cache_build(args, world, rank, local):
+    """The cache build of one sequence from hidden states: the CSA entries
+    (with indexer keys) and the HCA entries of L tokens, each by
+    hattn_compress_hidden (pool the window's hidden states, project once per
+    entry, norm and rope).  Hidden states and weights are seeded N(0,1) bf16
+    (weights scaled by 1/sqrt(d_model))."""
+    import torch
+    from sparse_attention_26_b300 import hattn
+
+    hattn.lib()
+    dev = torch.device("cuda", local)
+    L = args.context or (1 << 20)
+    dm, D, dI, r = 7168, 512, 128, 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    x = torch.empty((1, L, dm), dtype=torch.bfloat16, device=dev)
+    for c in range(0, L, 16384):
+        x[:, c:c + 16384].copy_(torch.randn((1, min(16384, L - c), dm), generator=g, device=dev))
+    W_c = (torch.randn((dm, D + dI), generator=g, device=dev) / math.sqrt(dm)).to(torch.bfloat16)
+    W_h = (torch.randn((dm, D), generator=g, device=dev) / math.sqrt(dm)).to(torch.bfloat16)
+    g_c = torch.randn((1, L), generator=g, device=dev).to(torch.bfloat16)
+    g_h = torch.randn((1, L), generator=g, device=dev).to(torch.bfloat16)
+    kv_c = torch.empty((1, L // 4, D), dtype=torch.bfloat16, device=dev)
+    ik_c = torch.empty((1, L // 4, dI), dtype=torch.bfloat16, device=dev)
+    kv_h = torch.empty((1, L // 128, D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(hattn.lib().hattn_compress_hidden_workspace_bytes(1, 0, L // 4, dm, D, dI),
+                         hattn.lib().hattn_compress_hidden_workspace_bytes(1, 0, L // 128, dm, D, 0)),
+                     dtype=torch.uint8, device=dev)
+
+    def build():
+        hattn.compress_hidden(x, W_c, g_c, D=D, r=r, m=4, w=8, kv_out=kv_c, ik_out=ik_c,
+                              workspace=ws)
+        hattn.compress_hidden(x, W_h, g_h, D=D, r=r, m=128, w=128, kv_out=kv_h, workspace=ws)
+
+    for _ in range(args.warmup):
+        build()
+    torch.cuda.synchronize()
+    hattn.check_status()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev[0].record()
+    for _ in range(args.steps):
+        build()
+    ev[1].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    hattn.check_status()
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    hbm, _, src = peaks()
+    x_bytes = L * dm * 2
+    n_c, n_h = L // 4, L // 128
+    # both passes read the hidden states once (the CSA windows overlap by
+    # half: their second read is of rows just read), write their entries
+    alg_bytes = 2 * x_bytes + n_c * (D + dI) * 2 + n_h * D * 2 + 2 * L * 2
+    # the projections: pooled rows (two bf16 parts each) times W
+    flops = 2 * 2.0 * dm * (n_c * (D + dI) + n_h * D)
+    achieved = alg_bytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "cache build tokens/s from hidden states (1 B300)", "value": L / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "cache_build_1m_from_hidden", "context_tokens": L, "d_model": dm,
+                   "head_dim": D, "indexer_dim": dI, "csa_entries": n_c, "hca_entries": n_h},
+        "roofline": {"bound": "hbm", "kernel": "whole build (pool, project, norm)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes": alg_bytes, "projection_flops": flops,
+                     "projection_tflops": flops / (ms / 1e3) / 1e12},
+        "clocks": clocks, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, world, layer, inp, wl, t_new, stream, side):
     """The same steps with every step's inputs coming from pinned host memory
     and its result going back, inside the timed region.  A step's inputs (q,
@@ -802,6 +882,8 @@ def main():
         run_reference(args, world, rank)
     elif args.stack:
         run_stack(args, world, rank, local)
+    elif args.cache_build:
+        run_cache_build(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

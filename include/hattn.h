@@ -92,6 +92,30 @@ HATTN_API int hattn_hca_compress(const void* kv_raw, const void* gate, const flo
                        int64_t j_begin, int64_t j_end, void* kv_h, int64_t N_cap,
                        hattn_stream_t stream);
 
+/* Compressed entries straight from hidden states (cache build).  Each
+ * token's KV and indexer-key row is the projection x_u . W of its hidden
+ * state (W [dm][D + dI] bf16: the D KV columns, then the dI indexer-key
+ * columns), and entry j is C(m, w) of those rows as in hattn_csa_compress:
+ * gate-softmax pooling, RMSNorm and RoPE of the KV part.  Pooling is linear,
+ * so the library pools the hidden states first and projects once per entry,
+ * (sum_u a_u x_u) . W, which is the same entry up to rounding: the hidden
+ * states are read once per window, no per-token KV row is written, and the
+ * projection runs on one row per entry.  The pooled row is kept to ~16
+ * significant bits (two bf16 parts) and projected by cuBLASLt with fp32
+ * accumulation.
+ *   x [B][L_cap][dm] bf16 (dm a multiple of 8), gate [B][L_cap] bf16;
+ *   entries [j_begin, j_end) go to kv_out [B][N_cap][D] and, when dI > 0,
+ *   ik_out [B][N_cap][dI] (NULL when dI == 0: HCA is m = w = 128, dI = 0);
+ *   workspace of hattn_compress_hidden_workspace_bytes() bytes. */
+HATTN_API size_t hattn_compress_hidden_workspace_bytes(int B, int64_t j_begin, int64_t j_end,
+                                                       int dm, int D, int dI);
+HATTN_API int hattn_compress_hidden(const void* x, const void* W, const void* gate,
+                                    const float* gamma_kv, int B, int64_t L_cap, int dm, int D,
+                                    int dI, int m, int w, int r, float rope_base, float eps,
+                                    int64_t j_begin, int64_t j_end, void* kv_out, void* ik_out,
+                                    int64_t N_cap, void* workspace, size_t ws_bytes,
+                                    hattn_stream_t stream);
+
 /* Ring-buffer raw caches.  A decode loop needs only the newest raw tokens:
  * the compressors read the window of the entry the newest token completes
  * (8 tokens for CSA, 128 for HCA) and the window keys the last W tokens.  In

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libhattn.so")
 SOURCES = ["abi.cu", "compress.cu", "indexer.cu", "topk.cu", "qprep.cu", "attention.cu",
-           "merge.cu", "quant.cu"]
+           "merge.cu", "quant.cu", "hidden.cu"]
 HEADERS = ["common.cuh", "kernels.h", os.path.join("..", "..", "include", "hattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -69,7 +69,7 @@ def build(force=False, verbose=False):
                 print(out)
     if force or jobs or _stale(LIB, objs):
         run([nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", LIB] + objs +
-            ["-Xlinker", "-rpath=" + _cuda_lib_dir(nvcc)])
+            ["-lcublasLt", "-Xlinker", "-rpath=" + _cuda_lib_dir(nvcc)])
     return LIB
 
 

@@ -493,6 +493,68 @@ int hattn_hca_compress_ring(const void* kv_ring, const void* gate_ring, const fl
                          eps, j_begin, j_end, kv_h, nullptr, N_cap, stream, nullptr, nullptr, ring);
 }
 
+size_t hattn_compress_hidden_workspace_bytes(int B, int64_t j_begin, int64_t j_end, int dm, int D,
+                                             int dI) {
+  if (B < 1 || j_end <= j_begin || dm < 1 || D < 1 || dI < 0) return 0;
+  return hidden_workspace_bytes((int64_t)B * (j_end - j_begin), dm, D + dI);
+}
+
+int hattn_compress_hidden(const void* x, const void* W, const void* gate, const float* gamma_kv,
+                          int B, int64_t L_cap, int dm, int D, int dI, int m, int w, int r,
+                          float rope_base, float eps, int64_t j_begin, int64_t j_end, void* kv_out,
+                          void* ik_out, int64_t N_cap, void* workspace, size_t ws_bytes,
+                          hattn_stream_t stream) {
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(W);
+  REQUIRE_PTR(gate);
+  REQUIRE_PTR(kv_out);
+  REQUIRE_F32(gamma_kv);
+  REQUIRE((ik_out == nullptr) == (dI == 0), "ik_out must be given exactly when dI > 0");
+  if (ik_out) REQUIRE_PTR(ik_out);
+  REQUIRE(B >= 1 && L_cap >= 1 && N_cap >= 1, "B, L_cap and N_cap must be >= 1");
+  REQUIRE(dm >= 8 && dm % 8 == 0, "dm=%d must be a positive multiple of 8", dm);
+  REQUIRE(D >= 64 && D <= 512 && D % 64 == 0, "D=%d must be a multiple of 64 in [64, 512]", D);
+  REQUIRE(dI == 0 || (dI >= 8 && dI <= 128 && dI % 8 == 0),
+          "dI=%d must be 0 or a multiple of 8 in [8, 128]", dI);
+  REQUIRE(m >= 1 && w >= m && w % m == 0 && w <= 512,
+          "need 1 <= m <= w <= 512, w %% m == 0 (m=%d w=%d)", m, w);
+  int rc = check_rope(D, r, rope_base, eps);
+  if (rc) return rc;
+  REQUIRE(j_begin >= 0 && j_end >= j_begin && j_end <= N_cap,
+          "entry range [%lld, %lld) outside [0, N_cap=%lld)", (long long)j_begin,
+          (long long)j_end, (long long)N_cap);
+  REQUIRE((int64_t)m * j_end <= L_cap, "entry %lld needs tokens beyond L_cap=%lld",
+          (long long)(j_end - 1), (long long)L_cap);
+  if (j_end == j_begin) return ok();
+  const size_t need = hattn_compress_hidden_workspace_bytes(B, j_begin, j_end, dm, D, dI);
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  HiddenArgs a;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.W = static_cast<const __nv_bfloat16*>(W);
+  a.gate = static_cast<const __nv_bfloat16*>(gate);
+  a.gamma = gamma_kv;
+  a.kv_out = static_cast<__nv_bfloat16*>(kv_out);
+  a.ik_out = static_cast<__nv_bfloat16*>(ik_out);
+  a.B = B;
+  a.dm = dm;
+  a.D = D;
+  a.dI = dI;
+  a.m = m;
+  a.w = w;
+  a.r = r;
+  a.L_cap = L_cap;
+  a.N_cap = N_cap;
+  a.j_begin = j_begin;
+  a.j_end = j_end;
+  a.eps = eps;
+  make_rope_coef(rope_base, r, &a.rope);
+  cudaError_t e = launch_compress_hidden(a, workspace, num_sms_or_default(),
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "compress from hidden states");
+  return ok();
+}
+
 int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* codes, float* scales,
                         hattn_stream_t stream) {
   REQUIRE_PTR(x);

@@ -471,6 +471,17 @@ struct RopeCoef {
 // dropped exactly, and the fraction of a turn left, accurate to about 1e-7
 // turns at any position, goes to sincospif.  The _rn intrinsics keep the
 // compiler from contracting the products into other operations.
+// The RoPE angle coefficients of RopeCoef into shared memory (every thread
+// of the block calls it; it ends with a block barrier).
+__device__ __forceinline__ void load_rope_coef(float (*rc)[kMaxRopePairs], const RopeCoef& c,
+                                               int r) {
+  for (int i = threadIdx.x; i < r / 2; i += blockDim.x) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rc[k][i] = c.c[k][i];
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ void rope_cs(const float (*rc)[kMaxRopePairs], int i, int64_t p,
                                         float* sn, float* cs) {
   const uint32_t ap = static_cast<uint32_t>(p < 0 ? -p : p);

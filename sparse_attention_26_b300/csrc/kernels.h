@@ -67,6 +67,26 @@ cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm
                                  const CUtensorMap& tm_ks, const IndexerArgs& a,
                                  const IndexerPlan& p, bool f8, int grid, cudaStream_t stream);
 
+// ------------------------------------------------------------ entries from hidden states
+struct HiddenArgs {
+  const __nv_bfloat16* x;       // [B][L_cap][dm] hidden states
+  const __nv_bfloat16* W;       // [dm][D + dI]: KV columns, then indexer-key columns
+  const __nv_bfloat16* gate;    // [B][L_cap]
+  const float* gamma;           // [D] or null
+  __nv_bfloat16* kv_out;        // [B][N_cap][D]
+  __nv_bfloat16* ik_out;        // [B][N_cap][dI] or null (dI == 0)
+  int B, dm, D, dI, m, w, r;
+  int64_t L_cap, N_cap, j_begin, j_end;
+  float eps;
+  RopeCoef rope;
+};
+constexpr int64_t kHiddenChunk = 16384;          // entries pooled and projected per pass
+constexpr size_t kHiddenLtWorkspace = 32u << 20;  // the GEMM's scratch
+size_t hidden_chunk_entries(int64_t total);
+size_t hidden_workspace_bytes(int64_t total, int dm, int P);
+cudaError_t launch_compress_hidden(const HiddenArgs& a, void* ws, int num_sms,
+                                   cudaStream_t stream);
+
 // ------------------------------------------------------------ E4M3 rows
 // rows x n bf16 -> E4M3 codes [rows][n] and row scales [rows]; n % 4 == 0.
 cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,

@@ -84,15 +84,6 @@ __device__ __forceinline__ void norm_rope_row(const __nv_bfloat16* src, __nv_bfl
   }
 }
 
-__device__ __forceinline__ void load_rope_coef(float (*rc)[kMaxRopePairs], const RopeCoef& c,
-                                               int r) {
-  for (int i = threadIdx.x; i < r / 2; i += blockDim.x) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) rc[k][i] = c.c[k][i];
-  }
-  __syncthreads();
-}
-
 __global__ void __launch_bounds__(kQpThreads) qprep_kernel(const __grid_constant__ QPrepArgs a) {
   __shared__ float rc[4][kMaxRopePairs];
   pdl_trigger();

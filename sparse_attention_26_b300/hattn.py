@@ -36,6 +36,10 @@ _SIGS = {
                                       _i32, _f32, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _i64,
                                       _vp]),
     "hattn_quantize_e4m3": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp]),
+    "hattn_compress_hidden_workspace_bytes": (_sz, [_i32, _i64, _i64, _i32, _i32, _i32]),
+    "hattn_compress_hidden": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
+                                     _i32, _i32, _f32, _f32, _i64, _i64, _vp, _vp, _i64, _vp,
+                                     _sz, _vp]),
     "hattn_csa_compress_ring": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
                                        _i32, _f32, _f32, _i64, _i64, _vp, _vp, _i64, _vp]),
     "hattn_hca_compress_ring": (_i32, [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _f32, _f32,
@@ -249,6 +253,40 @@ def swa_keys_ring(kv_ring, pos, *, r, W=128, gamma_kv=None, rope_base=10000.0, e
     _check(lib().hattn_swa_keys_ring(_ptr(kv_ring), _ptr(gamma_kv), _ptr(pos), B, T, ring, D, W, r,
                                      rope_base, eps, _ptr(kv_w), _stream(stream)))
     return kv_w
+
+
+def compress_hidden(x, W, gate, *, D, r, m=4, w=8, j_begin=0, j_end=None, kv_out=None,
+                    ik_out=None, N_cap=None, gamma_kv=None, rope_base=10000.0, eps=1e-6,
+                    workspace=None, stream=None):
+    """C(m, w) entries [j_begin, j_end) of the projected hidden states x
+    [B, L, dm] with W [dm, D + dI] (KV columns, then indexer-key columns);
+    returns (kv_out [B, N_cap, D], ik_out [B, N_cap, dI] or None)."""
+    _need(x, "x", torch.bfloat16, 3)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(gate, "gate", torch.bfloat16, 2)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    B, L, dm = x.shape
+    dI = W.shape[1] - D
+    if N_cap is None:
+        N_cap = kv_out.shape[1] if kv_out is not None else L // m
+    if j_end is None:
+        j_end = min(N_cap, L // m)
+    dev = x.device
+    if kv_out is None:
+        kv_out = torch.zeros((B, N_cap, D), dtype=torch.bfloat16, device=dev)
+    if ik_out is None and dI > 0:
+        ik_out = torch.zeros((B, N_cap, dI), dtype=torch.bfloat16, device=dev)
+    _need(kv_out, "kv_out", torch.bfloat16, 3)
+    _opt(ik_out, "ik_out", torch.bfloat16)
+    need = lib().hattn_compress_hidden_workspace_bytes(B, j_begin, j_end, dm, D, dI)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wsb = workspace.numel() if workspace is not None else 0
+    _check(lib().hattn_compress_hidden(_ptr(x), _ptr(W), _ptr(gate), _ptr(gamma_kv), B, L, dm, D,
+                                       dI, m, w, r, rope_base, eps, j_begin, j_end, _ptr(kv_out),
+                                       _ptr(ik_out), N_cap, _ptr(workspace), wsb,
+                                       _stream(stream)))
+    return kv_out, ik_out
 
 
 def quantize_e4m3(x, *, codes=None, scales=None, stream=None):

@@ -77,6 +77,45 @@ def test_csa_compress(B, L, D, dI, r, j0, j1):
     assert torch.isnan(kv_c[:, :j0].float()).all() and torch.isnan(kv_c[:, j1:].float()).all()
 
 
+@pytest.mark.parametrize("B,L,dm,D,dI,m,w,r,j0,j1", [
+    (2, 1024, 512, 512, 128, 4, 8, 64, 0, 256),      # a CSA cache build
+    (1, 1030, 1024, 512, 128, 4, 8, 64, 200, 257),   # an entry range, ragged length
+    (2, 1024, 512, 512, 0, 128, 128, 64, 0, 8),      # HCA: no indexer key
+])
+def test_compress_hidden(B, L, dm, D, dI, m, w, r, j0, j1):
+    """Entries from hidden states (pooled, then projected once) against the
+    oracle, which projects every token in fp64 and then compresses."""
+    x = randn_bf16((B, L, dm), 70)
+    W = (randn_f32((dm, D + dI), 71) / math.sqrt(dm)).to(torch.bfloat16)
+    gate = randn_bf16((B, L), 72)
+    N_cap = L // m
+    kv = torch.full((B, N_cap, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ik = torch.full((B, N_cap, dI), float("nan"), dtype=torch.bfloat16, device=DEV) if dI else None
+    hattn.compress_hidden(x.to(DEV), W.to(DEV), gate.to(DEV), D=D, r=r, m=m, w=w, j_begin=j0,
+                          j_end=j1, kv_out=kv, ik_out=ik)
+    hattn.check_status()
+    ref_kv, ref_ik = orc.compress_hidden(bits(x), bits(W), bits(gate), m, w, r, j0, j1, D)
+    assert rel_l2(kv[:, j0:j1], ref_kv) <= KV_REL_L2
+    if dI:
+        assert rel_l2(ik[:, j0:j1], ref_ik) <= KV_REL_L2
+    assert torch.isnan(kv[:, :j0].float()).all() and torch.isnan(kv[:, j1:].float()).all()
+
+
+def test_compress_hidden_across_chunks():
+    """17,500 entries: two passes of pooling and projection; sampled entries
+    on both sides of the chunk boundary and at the ends."""
+    B, L, dm, D, dI, r = 1, 70000, 256, 512, 128, 64
+    x = randn_bf16((B, L, dm), 73)
+    W = (randn_f32((dm, D + dI), 74) / math.sqrt(dm)).to(torch.bfloat16)
+    gate = randn_bf16((B, L), 75)
+    kv, ik = hattn.compress_hidden(x.to(DEV), W.to(DEV), gate.to(DEV), D=D, r=r)
+    hattn.check_status()
+    for j0, j1 in [(0, 3), (16382, 16386), (L // 4 - 2, L // 4)]:
+        ref_kv, ref_ik = orc.compress_hidden(bits(x), bits(W), bits(gate), 4, 8, r, j0, j1, D)
+        assert rel_l2(kv[:, j0:j1], ref_kv) <= KV_REL_L2, (j0, j1)
+        assert rel_l2(ik[:, j0:j1], ref_ik) <= KV_REL_L2, (j0, j1)
+
+
 @pytest.mark.parametrize("B,L,D,r", [(2, 1024, 512, 64), (1, 300, 64, 16)])
 def test_hca_compress(B, L, D, r):
     kv = randn_bf16((B, L, D), 5)

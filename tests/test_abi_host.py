@@ -130,6 +130,37 @@ def test_fp8_key_validation(L):
     assert L.hattn_quantize_e4m3(FAKE, 0, 128, FAKE, FAKE, s) == hattn.OK
 
 
+def test_ring_and_hidden_validation(L):
+    N = None
+    s = None
+    # a ring must be a power of two equal to L_cap, and hold the entries' windows
+    rc = L.hattn_csa_compress_ring(FAKE, FAKE, FAKE, N, 1, 200, 512, 128, 4, 8, 64, 1e4, 1e-6,
+                                   0, 10, FAKE, FAKE, 100, s)
+    assert rc == hattn.INVALID_ARG and "power of two" in _err(L)
+    rc = L.hattn_csa_compress_ring(FAKE, FAKE, FAKE, N, 1, 256, 512, 128, 4, 8, 64, 1e4, 1e-6,
+                                   0, 100, FAKE, FAKE, 100, s)
+    assert rc == hattn.INVALID_ARG and "span more tokens" in _err(L)
+    rc = L.hattn_hca_compress_ring(FAKE, FAKE, N, 1, 256, 512, 128, 64, 1e4, 1e-6, 5, 8, FAKE,
+                                   10, s)  # three 128-token entries
+    assert rc == hattn.INVALID_ARG and "span more tokens" in _err(L)
+    rc = L.hattn_swa_keys_ring(FAKE, N, FAKE, 1, 2, 128, 512, 128, 64, 1e4, 1e-6, FAKE, s)
+    assert rc == hattn.INVALID_ARG and "W + T - 1" in _err(L)
+    # entries from hidden states: d_model a multiple of 8, the indexer-key
+    # output exactly when dI > 0, a large enough workspace
+    rc = L.hattn_compress_hidden(FAKE, FAKE, FAKE, N, 1, 1024, 100, 512, 128, 4, 8, 64, 1e4, 1e-6,
+                                 0, 256, FAKE, FAKE, 256, FAKE, 1 << 30, s)
+    assert rc == hattn.INVALID_ARG and "dm=100" in _err(L)
+    rc = L.hattn_compress_hidden(FAKE, FAKE, FAKE, N, 1, 1024, 512, 512, 128, 4, 8, 64, 1e4, 1e-6,
+                                 0, 256, FAKE, N, 256, FAKE, 1 << 30, s)
+    assert rc == hattn.INVALID_ARG and "ik_out" in _err(L)
+    need = L.hattn_compress_hidden_workspace_bytes(1, 0, 256, 512, 512, 128)
+    assert need > 256 * 512 * 4
+    rc = L.hattn_compress_hidden(FAKE, FAKE, FAKE, N, 1, 1024, 512, 512, 128, 4, 8, 64, 1e4, 1e-6,
+                                 0, 256, FAKE, FAKE, 256, FAKE, need - 1, s)
+    assert rc == hattn.INVALID_ARG and "workspace" in _err(L)
+    assert L.hattn_compress_hidden_workspace_bytes(1, 5, 5, 512, 512, 128) == 0
+
+
 def test_attention_validation(L):
     N = None
     rc = L.hattn_sparse_attn(FAKE, N, 0, FAKE, N, FAKE, 1, 1, 128, 512, 100, 16, 64, 1e4, 1e-6,

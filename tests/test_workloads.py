@@ -51,3 +51,43 @@ def test_random_idx_distinct():
             vals = row[row >= 0]
             assert len(set(vals.tolist())) == len(vals)
     assert (idx[1, 0] == -1).all() and (idx[0, 0, 5:] == -1).all()
+
+
+def test_layer_pattern_of_the_pages():
+    """Two sliding-window layers, then CSA and HCA alternating: V4-Pro's 61
+    layers are 2 + 30 + 29, V4-Flash's 43 are 2 + 21 + 20."""
+    from sparse_attention_26_b300.stack import CSA, HCA, SWA, layer_pattern
+    pro = layer_pattern(61)
+    assert pro[:2] == [SWA, SWA] and pro[2:6] == [CSA, HCA, CSA, HCA]
+    assert (pro.count(SWA), pro.count(CSA), pro.count(HCA)) == (2, 30, 29)
+    flash = layer_pattern(43)
+    assert (flash.count(SWA), flash.count(CSA), flash.count(HCA)) == (2, 21, 20)
+    assert layer_pattern(1) == [SWA]
+
+
+def test_new_entries_of_a_step():
+    """The entries a step's new tokens complete: entry j is complete once the
+    token at m(j+1)-1 is cached."""
+    from sparse_attention_26_b300.layer import HybridLayer
+
+    class Shapes(HybridLayer):
+        def __init__(self, wl):
+            self.wl = wl
+
+    layer = Shapes(synth.WORKLOADS["hybrid_decode_1m"])
+    assert layer.new_entries("csa", 7, 1) == (1, 2)      # token 7 completes entry 1
+    assert layer.new_entries("csa", 8, 1) == (2, 2)      # token 8 completes nothing
+    assert layer.new_entries("csa", 11, 8) == (1, 3)     # tokens 4..11: entries 1 and 2
+    assert layer.new_entries("hca", 255, 2) == (1, 2)    # tokens 254, 255: HCA entry 1
+    assert layer.new_entries("hca", 257, 2) == (2, 2)      # tokens 256, 257: none
+    L = 1 << 20
+    assert layer.new_entries("csa", L - 1, 2) == (L // 4 - 1, L // 4)
+    assert layer.new_entries("csa", None, 1) == (0, 0)
+    # brute force against the definition
+    for m in (4, 128):
+        kind = "csa" if m == 4 else "hca"
+        for t in range(0, 600, 7):
+            for n in (1, 2, 5):
+                done = [j for j in range(t // m + 2) if t - n + 1 <= m * (j + 1) - 1 <= t]
+                j0, j1 = layer.new_entries(kind, t, n)
+                assert list(range(j0, j1)) == done, (kind, t, n)

@@ -176,7 +176,8 @@ class HybridLayer:
         if t_new is None:
             return 0, 0
         m = self.wl.m_csa if kind == "csa" else self.wl.m_hca
-        return (t_new - n_new + 1) // m, (t_new + 1) // m
+        j1 = (t_new + 1) // m
+        return min(max(0, (t_new - n_new + 1) // m), j1), j1
 
     def _csa_compress(self, j0, j1):
         wl, r = self.wl, self.raw

@@ -360,15 +360,17 @@ def oracle_sample_setup(wl, seed=0):
     return s
 
 
-def oracle_step(wl, s):
-    """The decode step of one sequence through the oracle's stages."""
+def oracle_step(wl, s, compress=True):
+    """The decode step of one sequence through the oracle's stages (the query
+    at s["pos"], by default L-1, and the entries its token completes)."""
     import oracle as orc
-    L, t = wl.L, wl.L - 1
+    L, t = wl.L, int(s["pos"][0, 0])
     o_list, l_list = [], []
     if "csa" in wl.branches:
         j = (t + 1) // wl.m_csa - 1
-        orc.compress(s["kv_raw"], s["gate_csa"], wl.m_csa, wl.w_csa, wl.r, j, j + 1,
-                     ik_raw=s["ik_raw"])
+        if compress and (t + 1) % wl.m_csa == 0:
+            orc.compress(s["kv_raw"], s["gate_csa"], wl.m_csa, wl.w_csa, wl.r, j, j + 1,
+                         ik_raw=s["ik_raw"])
         sc = orc.indexer_scores(s["iq"], s["w"], s["ik_c"], s["pos"], wl.m_csa)
         idx = orc.topk(sc, s["pos"], wl.m_csa, wl.k)
         o, l = orc.attention(orc.KIND_SPARSE, s["q"], s["kv_c"], s["pos"], idx=idx, r=wl.r)
@@ -376,7 +378,8 @@ def oracle_step(wl, s):
         l_list.append(l)
     if "hca" in wl.branches:
         j = (t + 1) // wl.m_hca - 1
-        orc.compress(s["kv_raw"], s["gate_hca"], wl.m_hca, wl.w_hca, wl.r, j, j + 1)
+        if compress and (t + 1) % wl.m_hca == 0:
+            orc.compress(s["kv_raw"], s["gate_hca"], wl.m_hca, wl.w_hca, wl.r, j, j + 1)
         o, l = orc.attention(orc.KIND_HCA, s["q"], s["kv_h"], s["pos"], m=wl.m_hca, r=wl.r)
         o_list.append(o)
         l_list.append(l)
@@ -388,7 +391,48 @@ def oracle_step(wl, s):
     return L
 
 
+def cpu_baseline_prefill(wl, n_sample=None):
+    """The oracle on one prefill pass of one sequence: the compression of
+    every entry the pass's T tokens complete, timed in full, plus the
+    per-query work timed on n_sample evenly spaced queries and extrapolated
+    linearly to all T (the per-query cost grows with the causal prefix, so
+    the sample spans it)."""
+    import numpy as np
+
+    import oracle as orc
+    from sparse_attention_26_b300.layer import HybridLayer
+
+    if n_sample is None:
+        n_sample = 8 if "hca" in wl.branches and wl.L > (1 << 17) else 64
+    s = oracle_sample_setup(wl)
+    shapes = HybridLayer.__new__(HybridLayer)
+    shapes.wl = wl
+    t0 = time.perf_counter()
+    for kind, m, w, ik in (("csa", wl.m_csa, wl.w_csa, s["ik_raw"]), ("hca", wl.m_hca, wl.w_hca,
+                                                                     None)):
+        if kind in wl.branches:
+            j0, j1 = shapes.new_entries(kind, wl.L - 1, wl.T)
+            if j1 > j0:
+                orc.compress(s["kv_raw"], s["gate_" + kind], m, w, wl.r, j0, j1, ik_raw=ik)
+    t_comp = time.perf_counter() - t0
+    ts = np.unique(np.linspace(wl.L - wl.T, wl.L - 1, n_sample).round().astype(np.int64))
+    t0 = time.perf_counter()
+    for t in ts:
+        s["pos"] = np.array([[t]], np.int32)
+        oracle_step(wl, s, compress=False)
+    per_query = (time.perf_counter() - t0) / len(ts)
+    per_pass = t_comp + per_query * wl.T
+    return {"value": wl.T / per_pass, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"extrapolated: one sequence's prefill pass of {wl.name} = the compression "
+                      f"of its new entries (timed in full, {t_comp:.2f} s) + {wl.T} queries x "
+                      f"{per_query:.3f} s per query (mean of {len(ts)} evenly spaced queries), "
+                      "single-threaded fp64 C, seeded synthetic caches",
+            "seconds_per_pass": per_pass}
+
+
 def cpu_baseline(wl, steps=1):
+    if wl.T > 2:
+        return cpu_baseline_prefill(wl)
     s = oracle_sample_setup(wl)
     t0 = time.perf_counter()
     for _ in range(steps):

@@ -72,15 +72,24 @@ __global__ void __launch_bounds__(kPoolThreads)
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[k] = 0.f;
       const __nv_bfloat16* src = a.x + ((int64_t)b * a.L_cap + u0) * a.dm + c;
-      for (int s = s_lo; s < a.w; ++s) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)s * a.dm));
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-        const float al = alpha[s];
+      // eight token rows requested at once, then accumulated in order
+      for (int s0 = s_lo; s0 < a.w; s0 += 8) {
+        uint4 v[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __bfloat1622float2(h[k]);
-          acc[2 * k] = fmaf(al, f.x, acc[2 * k]);
-          acc[2 * k + 1] = fmaf(al, f.y, acc[2 * k + 1]);
+        for (int q = 0; q < 8; ++q) {
+          const uint4* row = reinterpret_cast<const uint4*>(src + (int64_t)(s0 + q) * a.dm);
+          v[q] = s0 + q < a.w ? __ldg(row) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float al = s0 + q < a.w ? alpha[s0 + q] : 0.f;
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[q]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(h[k]);
+            acc[2 * k] = fmaf(al, f.x, acc[2 * k]);
+            acc[2 * k + 1] = fmaf(al, f.y, acc[2 * k + 1]);
+          }
         }
       }
       float hi[8], lo[8];

@@ -39,7 +39,9 @@
  *  - merge: Z = sum_b exp(lse_b) + exp(sink_h); out = sum_b exp(lse_b) o_b / Z,
  *    then the last r dims are rotated back by the query position;
  *  - low-precision indexer path (optional): keys and query rows as E4M3 codes
- *    with one fp32 scale amax/448 per row, dequantised before the score.
+ *    with one fp32 scale amax/448 per row, dequantised before the score;
+ *  - MXFP4 indexer rows (optional): E2M1 codes in blocks of 32 along the
+ *    head dim, each block with an E8M0 scale 2^(floor(log2 amax) - 2).
  */
 #include <math.h>
 #include <stdint.h>
@@ -412,6 +414,143 @@ int orc_indexer_scores_e4m3(const uint16_t* iq, const float* w, const uint8_t* i
                 const uint8_t* kj = ik8 + ((int64_t)b * N_cap + j) * dI;
                 double sk = (double)iks[(int64_t)b * N_cap + j];
                 for (int d = 0; d < dI; ++d) kd[d] = orc_e4m3_to_f64(kj[d]) * sk;
+                double s = 0.0;
+                for (int h = 0; h < HI; ++h) {
+                    double dot = 0.0;
+                    for (int d = 0; d < dI; ++d) dot += qd[(size_t)h * dI + d] * kd[d];
+                    s += (double)w[bt * HI + h] * (dot > 0.0 ? dot : 0.0);
+                }
+                out[j] = s;
+            }
+        }
+    }
+    free(qc); free(qs); free(qd); free(kd);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* MXFP4 indexer rows                                                  */
+/* ------------------------------------------------------------------ */
+
+/* "DeepSeek-V4" atlas spec sheet, section "Inference efficiency": the indexer
+ * QK path is trained for FP4 (MXFP4); "Why DeepSeek V4 Stands Apart",
+ * section "Core Architectural Innovations" (FP4 quantization-aware
+ * training): the FP4 elements are E2M1.  MXFP4 is the OCP
+ * Microscaling format: E2M1 elements, 32 consecutive elements sharing one
+ * power-of-two scale stored as E8M0.
+ *
+ * E2M1: 1 sign, 2 exponent bits (bias 1), 1 mantissa bit, no Inf or NaN;
+ * exponent field 0 is subnormal (m * 0.5), so the magnitudes are
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double orc_e2m1_to_f64(uint8_t c) {
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* Nearest E2M1 code to y (ties to the even code), magnitudes beyond 6
+ * clamped to 6; a result of zero is encoded +0 whatever the sign of y. */
+uint8_t orc_f64_to_e2m1(double y) {
+    double a = fabs(y);
+    uint8_t code;
+    if (a >= 6.0) {
+        code = 7;
+    } else {
+        int e;
+        frexp(a, &e);              /* a = f * 2^e, f in [0.5, 1) */
+        int q = e - 2;             /* spacing of 2-significant-bit numbers */
+        if (q < -1) q = -1;        /* subnormal spacing 0.5 */
+        double v = ldexp(nearbyint(ldexp(a, -q)), q);   /* half to even */
+        if (v == 0.0) return 0;
+        if (v == 0.5) {
+            code = 1;
+        } else {
+            int ev;
+            frexp(v, &ev);         /* v = 1.m * 2^(ev-1), biased exponent ev */
+            code = (uint8_t)((ev << 1) | (int)((ldexp(v, -(ev - 1)) - 1.0) * 2.0));
+        }
+    }
+    return (uint8_t)((signbit(y) ? 8 : 0) | code);
+}
+
+/* E8M0 scale code c stands for 2^(c - 127); c = 255 is NaN. */
+double orc_e8m0_to_f64(uint8_t c) { return c == 255 ? NAN : ldexp(1.0, (int)c - 127); }
+
+/* The block's scale exponent: floor(log2(amax)) minus the largest E2M1
+ * exponent (2), so amax / X lies in [4, 8); clamped to E8M0's range
+ * [-127, 127].  An all-zero block takes the smallest scale. */
+static int orc_mx_scale_exp(double amax) {
+    if (!(amax > 0.0)) return -127;
+    int e;
+    frexp(amax, &e);               /* floor(log2(amax)) = e - 1 */
+    int s = e - 1 - 2;
+    return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+/* One row of n bf16 values (n a multiple of 32) to MXFP4: codes [n/2] bytes
+ * with element 2i in the low nibble and 2i+1 in the high nibble of byte i,
+ * and scales [n/32] E8M0 codes, block b covering elements [32b, 32b+32). */
+void orc_quantize_mxfp4_row(const uint16_t* x, int n, uint8_t* codes, uint8_t* scales) {
+    for (int b = 0; b < n / 32; ++b) {
+        double amax = 0.0;
+        for (int i = 32 * b; i < 32 * b + 32; ++i) {
+            double a = fabs(orc_bf16_to_f64(x[i]));
+            if (a > amax) amax = a;
+        }
+        int se = orc_mx_scale_exp(amax);
+        scales[b] = (uint8_t)(se + 127);
+        for (int i = 32 * b; i < 32 * b + 32; i += 2) {
+            uint8_t lo = orc_f64_to_e2m1(ldexp(orc_bf16_to_f64(x[i]), -se));
+            uint8_t hi = orc_f64_to_e2m1(ldexp(orc_bf16_to_f64(x[i + 1]), -se));
+            codes[i / 2] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+void orc_quantize_mxfp4_rows(const uint16_t* x, int64_t rows, int n, uint8_t* codes,
+                             uint8_t* scales) {
+    for (int64_t r = 0; r < rows; ++r)
+        orc_quantize_mxfp4_row(x + r * n, n, codes + r * (n / 2), scales + r * (n / 32));
+}
+
+/* Element d of an MXFP4 row. */
+static double orc_mxfp4_value(const uint8_t* codes, const uint8_t* scales, int d) {
+    uint8_t c = (uint8_t)((codes[d / 2] >> (4 * (d & 1))) & 15);
+    return orc_e2m1_to_f64(c) * orc_e8m0_to_f64(scales[d / 32]);
+}
+
+/*
+ * Indexer scores with MXFP4 keys: codes ik4 [B][N_cap][dI/2] and E8M0 scales
+ * iks [B][N_cap][dI/32]; each bf16 query row iq[b][t][h] is quantised the
+ * same way; both are dequantised to fp64 and the score is the plain
+ * definition sum_h w[t,h] * max(0, q^[t,h] . k^[j]).  NaN past the visible
+ * entries.  dI must be a multiple of 32.
+ */
+int orc_indexer_scores_mxfp4(const uint16_t* iq, const float* w, const uint8_t* ik4,
+                             const uint8_t* iks, const int32_t* pos, int B, int T, int HI, int dI,
+                             int64_t N_cap, int m, double* scores) {
+    if (B <= 0 || T <= 0 || HI <= 0 || dI <= 0 || dI % 32 || N_cap < 0 || m <= 0)
+        return ORC_EINVAL;
+    uint8_t* qc = (uint8_t*)malloc((size_t)dI / 2);
+    uint8_t* qs = (uint8_t*)malloc((size_t)dI / 32);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)HI * dI);
+    double* kd = (double*)malloc(sizeof(double) * (size_t)dI);
+    if (!qc || !qs || !qd || !kd) { free(qc); free(qs); free(qd); free(kd); return ORC_ENOMEM; }
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < T; ++t) {
+            int64_t bt = (int64_t)b * T + t;
+            for (int h = 0; h < HI; ++h) {
+                orc_quantize_mxfp4_row(iq + (bt * HI + h) * dI, dI, qc, qs);
+                for (int d = 0; d < dI; ++d) qd[(size_t)h * dI + d] = orc_mxfp4_value(qc, qs, d);
+            }
+            int64_t n = orc_visible(pos[bt], m);
+            if (n > N_cap) n = N_cap;
+            double* out = scores + bt * N_cap;
+            for (int64_t j = 0; j < N_cap; ++j) out[j] = NAN;
+            for (int64_t j = 0; j < n; ++j) {
+                const uint8_t* kc = ik4 + ((int64_t)b * N_cap + j) * (dI / 2);
+                const uint8_t* ks = iks + ((int64_t)b * N_cap + j) * (dI / 32);
+                for (int d = 0; d < dI; ++d) kd[d] = orc_mxfp4_value(kc, ks, d);
                 double s = 0.0;
                 for (int h = 0; h < HI; ++h) {
                     double dot = 0.0;

@@ -68,6 +68,17 @@ def lib():
         L.orc_indexer_scores_e4m3.argtypes = [_u16p, _f32p, _u8p, _f32p, _i32p, ctypes.c_int,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int64, ctypes.c_int, _f64p]
+        L.orc_e2m1_to_f64.restype = ctypes.c_double
+        L.orc_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        L.orc_f64_to_e2m1.restype = ctypes.c_uint8
+        L.orc_f64_to_e2m1.argtypes = [ctypes.c_double]
+        L.orc_e8m0_to_f64.restype = ctypes.c_double
+        L.orc_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        L.orc_quantize_mxfp4_rows.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, _u8p, _u8p]
+        L.orc_indexer_scores_mxfp4.restype = ctypes.c_int
+        L.orc_indexer_scores_mxfp4.argtypes = [_u16p, _f32p, _u8p, _u8p, _i32p, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int64, ctypes.c_int, _f64p]
         L.orc_topk.restype = ctypes.c_int
         L.orc_topk.argtypes = [_f64p, _i32p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                ctypes.c_int, _i32p]
@@ -258,6 +269,69 @@ def indexer_scores_e4m3(iq, w, ik8, iks, pos, m):
                                        _p(iks, _f32p), _p(pos, _i32p), B, T, HI, dI, N, m,
                                        _p(out, _f64p))
     _check(rc, "indexer_scores_e4m3")
+    return out
+
+
+# ---------------------------------------------------------------- MXFP4 indexer rows
+def e2m1_to_f64(codes):
+    """Values of E2M1 codes (the low 4 bits of each uint8), fp64."""
+    c = np.asarray(codes, dtype=np.uint8)
+    f = lib().orc_e2m1_to_f64
+    return np.array([f(int(x)) for x in c.ravel()], np.float64).reshape(c.shape)
+
+
+def f64_to_e2m1(y):
+    """Nearest E2M1 codes (ties to even, saturating at 6, zero as +0)."""
+    y = np.asarray(y, dtype=np.float64)
+    f = lib().orc_f64_to_e2m1
+    return np.array([f(float(v)) for v in y.ravel()], np.uint8).reshape(y.shape)
+
+
+def e8m0_to_f64(codes):
+    """Values 2^(c-127) of E8M0 scale codes (255 is NaN), fp64."""
+    c = np.asarray(codes, dtype=np.uint8)
+    f = lib().orc_e8m0_to_f64
+    return np.array([f(int(x)) for x in c.ravel()], np.float64).reshape(c.shape)
+
+
+def quantize_mxfp4(x):
+    """Rows of the last axis (n bf16 bits, n a multiple of 32) to MXFP4:
+    (codes uint8 [.., n/2], element 2i in the low nibble; scales uint8
+    E8M0 [.., n/32])."""
+    x = _u16(x)
+    n = x.shape[-1]
+    rows = x.size // n if n else 0
+    codes = np.empty(x.shape[:-1] + (n // 2,), np.uint8)
+    scales = np.empty(x.shape[:-1] + (n // 32,), np.uint8)
+    lib().orc_quantize_mxfp4_rows(_p(x, _u16p), rows, n, _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def dequantize_mxfp4(codes, scales):
+    """fp64 values [.., n] of MXFP4 rows."""
+    codes = np.asarray(codes, np.uint8)
+    nib = np.stack([codes & 15, codes >> 4], axis=-1).reshape(codes.shape[:-1] + (-1,))
+    n = nib.shape[-1]
+    sc = np.repeat(e8m0_to_f64(scales), 32, axis=-1)[..., :n]
+    return e2m1_to_f64(nib) * sc
+
+
+def indexer_scores_mxfp4(iq, w, ik4, iks, pos, m):
+    """fp64 scores [B, T, N_cap] from MXFP4 keys (codes ik4 [B, N_cap, dI/2],
+    E8M0 scales iks [B, N_cap, dI/32]); the bf16 queries are quantised the
+    same way and both sides dequantised."""
+    iq = _u16(iq)
+    ik4 = np.ascontiguousarray(ik4, dtype=np.uint8)
+    iks = np.ascontiguousarray(iks, dtype=np.uint8)
+    w = _f32(w)
+    pos = _i32(pos)
+    B, T, HI, dI = iq.shape
+    N = ik4.shape[1]
+    out = np.empty((B, T, N), np.float64)
+    rc = lib().orc_indexer_scores_mxfp4(_p(iq, _u16p), _p(w, _f32p), _p(ik4, _u8p),
+                                        _p(iks, _u8p), _p(pos, _i32p), B, T, HI, dI, N, m,
+                                        _p(out, _f64p))
+    _check(rc, "indexer_scores_mxfp4")
     return out
 
 

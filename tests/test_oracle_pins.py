@@ -312,6 +312,146 @@ def test_indexer_e4m3_exact_rows_equal_bf16_scores(orc):
     np.testing.assert_array_equal(s_2[ok], want[ok])
 
 
+# --------------------------------------------------------------------- MXFP4 (E2M1) rows
+# The E2M1 element magnitudes of codes 0..7 as the OCP Microscaling Formats
+# specification v1.0 tabulates them (FP4 E2M1: max normal 6, min normal 1,
+# max subnormal 0.5); code bit 3 is the sign.
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_brute(y):
+    """Nearest table value by exhaustive search: the smallest |y - v| over
+    the 8 magnitudes, ties to the even code, sign from y, +0 for zero."""
+    out = np.empty(np.shape(y), np.uint8)
+    for idx, v in np.ndenumerate(np.asarray(y, np.float64)):
+        a = min(abs(v), 6.0)
+        err = [abs(a - t) for t in E2M1_MAGNITUDES]
+        best = min(err)
+        cands = [c for c in range(8) if err[c] == best]
+        c = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+        out[idx] = c | (8 if (v < 0 and c) else 0)
+    return out
+
+
+def test_e2m1_decode_table(orc):
+    codes = np.arange(16, dtype=np.uint8)
+    want = np.array(E2M1_MAGNITUDES + [-v for v in E2M1_MAGNITUDES])
+    np.testing.assert_array_equal(orc.e2m1_to_f64(codes), want)
+
+
+def test_e2m1_rounding_brute_force(orc):
+    """Every table value, every midpoint between neighbours (the ties), values
+    just either side of them, saturation beyond 6, and random values, against
+    the exhaustive nearest-value search."""
+    mags = np.array(E2M1_MAGNITUDES)
+    mids = (mags[1:] + mags[:-1]) / 2
+    near = np.concatenate([mids * (1 + 2.0 ** -20), mids * (1 - 2.0 ** -20)])
+    rng = np.random.default_rng(24)
+    y = np.concatenate([mags, mids, near, [6.5, 7.0, 7.999, 1e3, 1e-30, 0.0],
+                        rng.uniform(-8, 8, 3000), rng.standard_normal(500) * 1e-2])
+    y = np.concatenate([y, -y])
+    np.testing.assert_array_equal(orc.f64_to_e2m1(y), _e2m1_brute(y))
+    # the ties by hand: 0.25 -> 0, 0.75 -> 1, 1.25 -> 1, 1.75 -> 2, 2.5 -> 2,
+    # 3.5 -> 4, 5 -> 4 (each to the code with an even low bit)
+    np.testing.assert_array_equal(orc.f64_to_e2m1(mids), [0, 2, 2, 4, 4, 6, 6])
+    assert int(orc.f64_to_e2m1(-0.1)) == 0 and int(orc.f64_to_e2m1(-0.3)) == 9
+
+
+def test_e8m0_decode_matches_torch(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = orc.e8m0_to_f64(codes)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want))
+    np.testing.assert_array_equal(got[:255], want[:255])
+
+
+def test_mxfp4_row_quantisation(orc):
+    """Per 32-element block: the scale exponent is floor(log2 amax) - 2 (read
+    here from the fp32 exponent field), so amax / X lies in [4, 8); the codes
+    are the brute-force nearest values of x / X; nibble order is element 2i
+    low; every dequantised value lies within a quarter of (|x| + X) of x;
+    an all-zero block takes scale code 0 and zero codes."""
+    rng = np.random.default_rng(25)
+    rows, n = 24, 128
+    xv64 = rng.standard_normal((rows, n)) * 10.0 ** rng.integers(-6, 7, (rows, n // 32)).repeat(
+        32, axis=1)
+    xv64[2, 32:64] = 0.0
+    x = b16(xv64)
+    xv = f64(x)
+    codes, scales = orc.quantize_mxfp4(x)
+    assert codes.shape == (rows, n // 2) and scales.shape == (rows, n // 32)
+    blocks = xv.reshape(rows, n // 32, 32)
+    amax = np.abs(blocks).max(-1)
+    expo = ((amax.astype(np.float32).view(np.uint32) >> 23) & 0xFF).astype(np.int64) - 127
+    want_scale = np.where(amax > 0, expo - 2 + 127, 0)
+    np.testing.assert_array_equal(scales, want_scale)
+    X = 2.0 ** (scales.astype(np.float64) - 127)
+    live = amax > 0
+    ratio = amax[live] / X[live]
+    assert ((ratio >= 4) & (ratio < 8)).all()
+    y = blocks / X[..., None]
+    want_codes = _e2m1_brute(y).reshape(rows, n)
+    np.testing.assert_array_equal(codes & 15, want_codes[:, 0::2])
+    np.testing.assert_array_equal(codes >> 4, want_codes[:, 1::2])
+    deq = orc.dequantize_mxfp4(codes, scales)
+    Xe = np.repeat(X, 32, axis=1)
+    assert (np.abs(deq - xv) <= (np.abs(xv) + Xe) / 4).all()
+    assert scales[2, 1] == 0 and (codes[2, 16:32] == 0).all()
+
+
+def _mx_exact_rows(rng, shape):
+    """Rows whose blocks are table values times a per-block power of two,
+    with one element of each block at +-4 or +-6 times it: MXFP4 holds them
+    exactly (amax / X is 4 or 6)."""
+    n = shape[-1]
+    nb = n // 32
+    v = rng.choice(E2M1_MAGNITUDES, size=shape) * rng.choice([-1.0, 1.0], size=shape)
+    lead = rng.choice([4.0, 6.0], size=shape[:-1] + (nb,)) * rng.choice([-1.0, 1.0],
+                                                                        size=shape[:-1] + (nb,))
+    v = v.reshape(shape[:-1] + (nb, 32))
+    v[..., 0] = lead
+    v *= 2.0 ** rng.integers(-6, 4, size=shape[:-1] + (nb, 1))
+    return v.reshape(shape)
+
+
+def test_indexer_mxfp4_exact_rows_equal_bf16_scores(orc):
+    """Rows that MXFP4 holds exactly (block scales differing within a row, so
+    a block scale applied to the wrong elements, or swapped nibbles, changes
+    the values) give MXFP4 scores equal to the bf16 scores; raising one key
+    row's four block scales by 3 multiplies its scores by 8."""
+    rng = np.random.default_rng(26)
+    B, T, HI, dI, N, m = 2, 3, 4, 128, 9, 4
+    iq = b16(_mx_exact_rows(rng, (B, T, HI, dI)))
+    ik = b16(_mx_exact_rows(rng, (B, N, dI)))
+    w = rng.standard_normal((B, T, HI)).astype(np.float32)
+    pos = np.array([[3, 20, 35], [7, 11, 2]], np.int32)
+    ik4, iks = orc.quantize_mxfp4(ik)
+    np.testing.assert_array_equal(orc.dequantize_mxfp4(ik4, iks), f64(ik))
+    s_bf = orc.indexer_scores(iq, w, ik, pos, m)
+    s_4 = orc.indexer_scores_mxfp4(iq, w, ik4, iks, pos, m)
+    np.testing.assert_array_equal(np.isnan(s_4), np.isnan(s_bf))
+    ok = ~np.isnan(s_bf)
+    np.testing.assert_array_equal(s_4[ok], s_bf[ok])
+    iks2 = iks.copy()
+    iks2[1, 2] += 3
+    s_2 = orc.indexer_scores_mxfp4(iq, w, ik4, iks2, pos, m)
+    want = s_4.copy()
+    want[1, :, 2] *= 8
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(s_2[ok], want[ok])
+    # a query MXFP4 does not hold: it is scored as its quantised value (which
+    # bf16 holds exactly: two significant bits times a power of two)
+    iq_r = b16(rng.standard_normal((B, T, HI, dI)))
+    qc, qs = orc.quantize_mxfp4(iq_r)
+    iq_d = b16(orc.dequantize_mxfp4(qc, qs))
+    np.testing.assert_array_equal(f64(iq_d), orc.dequantize_mxfp4(qc, qs))
+    assert not np.array_equal(iq_d, iq_r)
+    s_r = orc.indexer_scores_mxfp4(iq_r, w, ik4, iks, pos, m)
+    s_d = orc.indexer_scores(iq_d, w, ik, pos, m)
+    ok = ~np.isnan(s_d)
+    np.testing.assert_array_equal(s_r[ok], s_d[ok])
+
+
 # --------------------------------------------------------------------- top-k
 def _pairwise_rule_ok(sc, chosen, n):
     ch = set(chosen)

@@ -150,7 +150,7 @@ HATTN_API int hattn_hca_compress_ring(const void* kv_ring, const void* gate_ring
  *
  * hattn_quantize_e4m3: rows x n bf16 -> codes [rows][n] (bytes) and
  *   scales [rows] fp32; n a multiple of 4.  Used to build an FP8 key cache
- *   from bf16 keys.
+ *   from bf16 keys.  With rows = 0 the pointers are not checked.
  * hattn_csa_compress_fp8: hattn_csa_compress that also writes each entry's
  *   indexer key as E4M3 codes ik8 [B][N_cap][dI] and scale ik_scale
  *   [B][N_cap] fp32, quantised from the bf16-rounded key (the value ik_c
@@ -158,6 +158,31 @@ HATTN_API int hattn_hca_compress_ring(const void* kv_ring, const void* gate_ring
  * ---------------------------------------------------------------------- */
 HATTN_API int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* codes, float* scales,
                                   hattn_stream_t stream);
+
+/* -------------------------------------------------------------------------
+ * MXFP4 indexer rows.  [AT] "Inference efficiency" names the indexer QK
+ * path's format: FP4 (MXFP4); [DD] "Core Architectural Innovations" (FP4
+ * quantization-aware training) names the FP4 element type, E2M1.  MXFP4 is
+ * the OCP Microscaling format: blocks of 32 consecutive elements share one
+ * power-of-two scale, stored as an E8M0 code c (value 2^(c-127)).
+ *   amax_b = max |x_i| over block b, X_b = 2^(floor(log2 amax_b) - 2)
+ *     (exponent clamped to [-127, 125]; an all-zero block takes c = 0),
+ *   code_i = e2m1_rne_satfinite(x_i / X_b)   (magnitudes 0, 0.5, 1, 1.5,
+ *     2, 3, 4, 6; ties to the even code; beyond 6 clamps to 6; a zero
+ *     result is stored as +0),
+ * and element i decodes as e2m1(code_i) * X_b.  Inputs must be finite.
+ *
+ * hattn_quantize_mxfp4: rows x n bf16 (n a multiple of 32) -> codes
+ *   [rows][n/2] bytes, element 2i in the low nibble and 2i+1 in the high
+ *   nibble of byte i, and scales [rows][n/32] E8M0 bytes.  For a 128-dim
+ *   indexer row: 64 code bytes and 4 scale bytes (68 B, against 256 B of
+ *   bf16).  All three pointers device memory, 16-byte aligned, caller-owned
+ *   (any value when rows = 0: nothing is touched); the call is asynchronous
+ *   on `stream`.
+ * ---------------------------------------------------------------------- */
+HATTN_API int hattn_quantize_mxfp4(const void* x, int64_t rows, int n, void* codes, void* scales,
+                                   hattn_stream_t stream);
+
 HATTN_API int hattn_csa_compress_fp8(const void* kv_raw, const void* ik_raw, const void* gate,
                                      const float* gamma_kv, int B, int64_t L_cap, int D, int dI,
                                      int m, int w, int r, float rope_base, float eps,

@@ -557,15 +557,32 @@ int hattn_compress_hidden(const void* x, const void* W, const void* gate, const 
 
 int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* codes, float* scales,
                         hattn_stream_t stream) {
+  REQUIRE(rows >= 0, "rows must be >= 0");
+  REQUIRE(n >= 4 && n % 4 == 0 && n <= (1 << 20), "n=%d must be a multiple of 4 in [4, 2^20]", n);
+  if (rows == 0) return ok();  // nothing to read or write: any pointers
   REQUIRE_PTR(x);
   REQUIRE_PTR(codes);
   REQUIRE_PTR(scales);
-  REQUIRE(rows >= 0, "rows must be >= 0");
-  REQUIRE(n >= 4 && n % 4 == 0 && n <= (1 << 20), "n=%d must be a multiple of 4 in [4, 2^20]", n);
-  if (rows == 0) return ok();
   cudaError_t e = launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(x), rows, n,
                                        static_cast<uint8_t*>(codes), scales, num_sms_or_default(),
                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return ok();
+}
+
+int hattn_quantize_mxfp4(const void* x, int64_t rows, int n, void* codes, void* scales,
+                         hattn_stream_t stream) {
+  REQUIRE(rows >= 0, "rows must be >= 0");
+  REQUIRE(n >= 32 && n % 32 == 0 && n <= (1 << 20), "n=%d must be a multiple of 32 in [32, 2^20]",
+          n);
+  if (rows == 0) return ok();  // nothing to read or write: any pointers
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(codes);
+  REQUIRE_PTR(scales);
+  cudaError_t e = launch_quantize_mxfp4(static_cast<const __nv_bfloat16*>(x), rows, n,
+                                        static_cast<uint8_t*>(codes),
+                                        static_cast<uint8_t*>(scales), num_sms_or_default(),
+                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return ok();
 }

@@ -92,6 +92,12 @@ cudaError_t launch_compress_hidden(const HiddenArgs& a, void* ws, int num_sms,
 cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
                                  float* scales, int num_sms, cudaStream_t stream);
 
+// ------------------------------------------------------------ MXFP4 rows
+// rows x n bf16 -> E2M1 codes [rows][n/2] (element 2i in the low nibble of
+// byte i) and E8M0 block scales [rows][n/32]; n % 32 == 0.
+cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
+                                  uint8_t* scales, int num_sms, cudaStream_t stream);
+
 // ------------------------------------------------------------ top-k select
 struct TopkArgs {
   const float* scores;   // [rows][N_cap]

@@ -1,14 +1,16 @@
-// quant.cu -- E4M3 rows of the low-precision indexer path.
+// quant.cu -- E4M3 and MXFP4 rows of the low-precision indexer path.
 //
 // "DeepSeek-V4" atlas spec sheet, section "Inference efficiency": the
 // indexer's QK path runs in low precision.  Here the keys are stored as FP8
 // E4M3 codes with one fp32 scale per row: code_i = e4m3(x_i * 448 / amax),
-// decoded as code_i * amax / 448.  This kernel quantises whole bf16 rows
+// decoded as code_i * amax / 448.  The E4M3 kernel quantises whole bf16 rows
 // (cache builds); the compressor quantises each new entry as it writes it and
 // the indexer quantises its query rows in shared memory, all through the
-// same row scaling (e4m3_row).
+// same row scaling (e4m3_row).  The pages' own format, MXFP4, has a kernel
+// for whole rows below (keys and queries in that format for the scoring
+// kernel to read).
 //
-// One warp per row; lane l covers elements 4l, 4l+1, 4l+2, 4l+3 of each
+// E4M3: one warp per row; lane l covers elements 4l, 4l+1, 4l+2, 4l+3 of each
 // 128-element span, so a row is read twice from L1/L2-resident lines (once
 // for the largest magnitude, once for the codes) and written once.
 #include "common.cuh"
@@ -49,7 +51,78 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
+// MXFP4 rows (OCP Microscaling: E2M1 elements, one E8M0 scale per 32
+// consecutive elements).  The block scale is X = 2^(floor(log2 amax) - 2),
+// the largest E2M1 exponent being 2, so amax / X lies in [4, 8); its
+// exponent is read off amax's fp32 exponent field and clamped to [-127, 125]
+// (the lower end also covers zero and subnormal blocks).  x / X is exact in
+// fp32, and the hardware conversion rounds it to the nearest E2M1 value
+// (ties to even) saturating at +-6.  Element 2i goes to the low nibble of
+// byte i; a zero result is stored as +0.
+//
+// One warp per row, lane l on elements 4l..4l+3 of each 128-element span, so
+// lanes 8g..8g+7 hold block g of the span and reduce its amax among
+// themselves.  n is a multiple of 32, so a span's blocks are whole.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_mxfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int n,
+                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kQuantThreads / 32);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
+       row < rows; row += warps) {
+    const __nv_bfloat16* xr = x + row * n;
+    uint8_t* cr = codes + row * (n / 2);
+    uint8_t* sr = scales + row * (n / 32);
+    for (int base = 0; base < n; base += 128) {
+      const int i = base + lane * 4;
+      const bool in = i < n;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (in) {
+        const uint2 u = *reinterpret_cast<const uint2*>(xr + i);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+      }
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      int se = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 2;
+      se = se < -127 ? -127 : se;
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);  // 2^-se
+      if (in) {
+        uint32_t w = e2m1x2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv)) |
+                     (e2m1x2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv)) << 8);
+        const uint32_t mag = w & 0x7777u;
+        w = mag | (w & ((mag + 0x7777u) & 0x8888u));  // drop the sign of zero nibbles
+        *reinterpret_cast<uint16_t*>(cr + i / 2) = static_cast<uint16_t>(w);
+        if ((lane & 7) == 0) sr[i / 32] = static_cast<uint8_t>(se + 127);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
+                                  uint8_t* scales, int num_sms, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const int64_t per_cta = kQuantThreads / 32;
+  const int64_t want = (rows + per_cta - 1) / per_cta;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  quantize_mxfp4_kernel<<<grid, kQuantThreads, 0, stream>>>(x, rows, n, codes, scales);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
                                  float* scales, int num_sms, cudaStream_t stream) {

@@ -36,6 +36,7 @@ _SIGS = {
                                       _i32, _f32, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _i64,
                                       _vp]),
     "hattn_quantize_e4m3": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp]),
+    "hattn_quantize_mxfp4": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp]),
     "hattn_compress_hidden_workspace_bytes": (_sz, [_i32, _i64, _i64, _i32, _i32, _i32]),
     "hattn_compress_hidden": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
                                      _i32, _i32, _f32, _f32, _i64, _i64, _vp, _vp, _i64, _vp,
@@ -303,6 +304,26 @@ def quantize_e4m3(x, *, codes=None, scales=None, stream=None):
     _need(scales, "scales", torch.float32)
     _check(lib().hattn_quantize_e4m3(_ptr(x), rows, n, _ptr(codes), _ptr(scales),
                                      _stream(stream)))
+    return codes, scales
+
+
+def quantize_mxfp4(x, *, codes=None, scales=None, stream=None):
+    """Rows of the last axis of a bf16 tensor (a multiple of 32 long) to
+    MXFP4: E2M1 codes (uint8 [.., n/2], element 2i in the low nibble) and
+    E8M0 block scales (uint8 [.., n/32])."""
+    _need(x, "x", torch.bfloat16)
+    n = x.shape[-1]
+    rows = x.numel() // n if n else 0
+    if codes is None:
+        codes = torch.empty(x.shape[:-1] + (n // 2,), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1] + (n // 32,), dtype=torch.uint8, device=x.device)
+    _need(codes, "codes", torch.uint8)
+    _need(scales, "scales", torch.uint8)
+    if codes.numel() * 2 != x.numel() or scales.numel() * 32 != x.numel():
+        raise ValueError("codes must hold n/2 bytes and scales n/32 bytes per row")
+    _check(lib().hattn_quantize_mxfp4(_ptr(x), rows, n, _ptr(codes), _ptr(scales),
+                                      _stream(stream)))
     return codes, scales
 
 

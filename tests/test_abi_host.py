@@ -130,6 +130,25 @@ def test_fp8_key_validation(L):
     assert L.hattn_quantize_e4m3(FAKE, 0, 128, FAKE, FAKE, s) == hattn.OK
 
 
+def test_mxfp4_validation(L):
+    N = None
+    s = None
+    # MXFP4 rows are whole 32-element blocks
+    for n in (16, 48, 0):
+        rc = L.hattn_quantize_mxfp4(FAKE, 10, n, FAKE, FAKE, s)
+        assert rc == hattn.INVALID_ARG and f"n={n}" in _err(L)
+    rc = L.hattn_quantize_mxfp4(FAKE, -1, 128, FAKE, FAKE, s)
+    assert rc == hattn.INVALID_ARG and "rows" in _err(L)
+    rc = L.hattn_quantize_mxfp4(FAKE, 10, 128, FAKE, N, s)
+    assert rc == hattn.INVALID_ARG and "scales" in _err(L)
+    rc = L.hattn_quantize_mxfp4(FAKE, 10, 128, MISAL, FAKE, s)
+    assert rc == hattn.MISALIGNED and "codes" in _err(L)
+    assert L.hattn_quantize_mxfp4(FAKE, 0, 128, FAKE, FAKE, s) == hattn.OK
+    # no rows: nothing is read or written, so null pointers (an empty tensor's) pass
+    assert L.hattn_quantize_mxfp4(N, 0, 128, N, N, s) == hattn.OK
+    assert L.hattn_quantize_e4m3(N, 0, 128, N, N, s) == hattn.OK
+
+
 def test_ring_and_hidden_validation(L):
     N = None
     s = None

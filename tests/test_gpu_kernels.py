@@ -190,6 +190,35 @@ def test_quantize_e4m3_bit_exact(rows, n):
     np.testing.assert_array_equal(scales.cpu().numpy(), rs)
 
 
+@pytest.mark.parametrize("rows,n", [(1000, 128), (37, 96), (5, 32), (3, 512)])
+def test_quantize_mxfp4_bit_exact(rows, n):
+    """E2M1 codes and E8M0 block scales equal the oracle's bit for bit.
+    Block magnitudes span 1e-30..1e30 and include subnormal blocks (scale
+    exponent clamped at -127); one block is all zeros, another holds -0 and
+    small negatives (stored as +0), another puts every element on a tie
+    between two E2M1 values, another saturates (amax / X = 7).  n = 96 leaves
+    a partial 128-element span; rows = 0 launches nothing."""
+    g = torch.Generator().manual_seed(54)
+    nb = n // 32
+    mag = 10.0 ** torch.randint(-30, 31, (rows, nb, 1), generator=g).float()
+    x = torch.randn((rows, nb, 32), generator=g) * mag
+    x[0, 0] = torch.randn(32, generator=g) * 1e-39            # subnormal block
+    ties = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -2.5, -5.0] * 3 + [6.0, 1.0])
+    x[1 % rows, nb - 1] = ties * 2.0 ** -3
+    if rows > 2:
+        x[2, 0] = 0.0
+        x[2, nb - 1] = torch.tensor([-0.0, -1e-3, 7.0, -7.0] * 8) * 2.0 ** 10   # -0, saturation
+    x = x.reshape(rows, n).to(torch.bfloat16)
+    codes, scales = hattn.quantize_mxfp4(x.to(DEV))
+    hattn.check_status()
+    rc, rs = orc.quantize_mxfp4(bits(x))
+    np.testing.assert_array_equal(_u8(scales), rs)
+    np.testing.assert_array_equal(_u8(codes), rc)
+    e_codes, e_scales = hattn.quantize_mxfp4(torch.empty((0, n), dtype=torch.bfloat16,
+                                                         device=DEV))
+    assert e_codes.shape == (0, n // 2) and e_scales.shape == (0, n // 32)
+
+
 @pytest.mark.parametrize("B,L,D,dI,r,j0,j1", [
     (2, 1024, 512, 128, 64, 255, 256),   # one new entry per sequence: the small kernel
     (2, 4096, 512, 128, 64, 0, 1024),    # cache build: the grid-stride kernel

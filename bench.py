@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--cache-build", action="store_true",
                     help="time building the CSA and HCA caches of one 1M-token sequence "
                          "straight from V4-Pro hidden states (d_model 7168)")
+    ap.add_argument("--quantize-keys", default="", choices=["", "fp8", "mxfp4"],
+                    help="time quantising the bf16 indexer key cache of the 1M-token decode "
+                         "workload (8 x 262,144 rows of 128) to E4M3 rows or MXFP4 blocks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dense-sms", type=int, default=0,
@@ -744,6 +747,82 @@ def run_cache_build(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_quantize_keys(args, world, rank, local):
+    """Quantising a bf16 indexer key cache in place of building it in the
+    low-precision format: B x L/4 rows of 128 (8 x 262,144 for the 1M-token
+    decode workload, 537 MB, larger than L2), to E4M3 codes with a row scale
+    (hattn_quantize_e4m3) or to MXFP4 codes with E8M0 block scales
+    (hattn_quantize_mxfp4).  Keys are seeded N(0,1) bf16."""
+    import torch
+    from sparse_attention_26_b300 import hattn
+
+    hattn.lib()
+    dev = torch.device("cuda", local)
+    B = args.batch or 8
+    N = (args.context or (1 << 20)) // 4
+    dI = 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(12)
+    ik = torch.randn((B, N, dI), generator=g, device=dev).to(torch.bfloat16)
+    if args.quantize_keys == "mxfp4":
+        codes = torch.empty((B, N, dI // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty((B, N, dI // 32), dtype=torch.uint8, device=dev)
+        out_bytes = dI // 2 + dI // 32
+
+        def run():
+            hattn.quantize_mxfp4(ik, codes=codes, scales=scales)
+    else:
+        codes = torch.empty((B, N, dI), dtype=torch.uint8, device=dev)
+        scales = torch.empty((B, N), dtype=torch.float32, device=dev)
+        out_bytes = dI + 4
+
+        def run():
+            hattn.quantize_e4m3(ik, codes=codes, scales=scales)
+
+    for _ in range(max(args.warmup, 3)):
+        run()
+    torch.cuda.synchronize()
+    hattn.check_status()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.perf_counter() + args.soak_ms / 1e3  # clocks under the same load
+    while time.perf_counter() < t_end:
+        run()
+        torch.cuda.synchronize()
+    ev[0].record()
+    for _ in range(args.steps):
+        run()
+    ev[1].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    clocks["window"] = "soak launches of the same kernel immediately before and during the timed region"
+    hattn.check_status()
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    hbm, _, src = peaks()
+    rows = B * N
+    alg_bytes = rows * (dI * 2 + out_bytes)
+    achieved = alg_bytes / (ms / 1e3) / 1e9
+    kernel = ("quantize_mxfp4_kernel<128>" if args.quantize_keys == "mxfp4"
+              else "quantize_e4m3_rows128_kernel")
+    line = {
+        "metric": "indexer key rows quantised per second (1 B300)", "value": rows / (ms / 1e3),
+        "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8" if args.quantize_keys == "mxfp4" else "u8+f32", "data": "synthetic",
+        "config": {"workload": f"quantize_indexer_keys_{args.quantize_keys}", "batch": B,
+                   "rows_per_sequence": N, "indexer_dim": dI, "l2": "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes": alg_bytes,
+                     "bytes_per_row": dI * 2 + out_bytes},
+        "clocks": clocks, "e2e": None, "gpu_launches": args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, world, layer, inp, wl, t_new, stream, side):
     """The same steps with every step's inputs coming from pinned host memory
     and its result going back, inside the timed region.  A step's inputs (q,
@@ -851,6 +930,8 @@ def main():
         run_stack(args, world, rank, local)
     elif args.cache_build:
         run_cache_build(args, world, rank, local)
+    elif args.quantize_keys:
+        run_quantize_keys(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -60,9 +60,13 @@ __global__ void __launch_bounds__(kQuantThreads)
 // (ties to even) saturating at +-6.  Element 2i goes to the low nibble of
 // byte i; a zero result is stored as +0.
 //
-// One warp per row, lane l on elements 4l..4l+3 of each 128-element span, so
-// lanes 8g..8g+7 hold block g of the span and reduce its amax among
-// themselves.  n is a multiple of 32, so a span's blocks are whole.
+// A warp takes kMxRows rows at a time and issues all their loads before it
+// reduces any of them, so an SM keeps enough bytes in flight to cover HBM
+// latency; lane l holds elements 4l..4l+3 of each 128-element span, so lanes
+// 8g..8g+7 hold block g of the span and reduce its amax among themselves.
+// n is a multiple of 32, so a span's blocks are whole.
+constexpr int kMxRows = 8;
+
 __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   uint32_t r;
   asm("{\n\t.reg .b8 t;\n\t"
@@ -73,39 +77,86 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   return r;
 }
 
+// kN > 0: rows of exactly kN elements (row offsets become immediates); kN = 0:
+// any n, a multiple of 32.
+template <int kN>
 __global__ void __launch_bounds__(kQuantThreads)
-    quantize_mxfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int n,
+    quantize_mxfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int n_arg,
                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int n = kN > 0 ? kN : n_arg;
   const int lane = threadIdx.x & 31;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kQuantThreads / 32);
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
-       row < rows; row += warps) {
-    const __nv_bfloat16* xr = x + row * n;
-    uint8_t* cr = codes + row * (n / 2);
-    uint8_t* sr = scales + row * (n / 32);
+  const int64_t warp = static_cast<int64_t>(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (kQuantThreads / 32) * kMxRows;
+  for (int64_t row0 = warp * kMxRows; row0 < rows; row0 += stride) {
+    // rows of this group that exist (warp-uniform); row k sits k * n
+    // elements past the group's first
+    const int nk = rows - row0 < kMxRows ? static_cast<int>(rows - row0) : kMxRows;
+    const __nv_bfloat16* xg = x + row0 * n;
+    uint8_t* cg = codes + row0 * (n / 2);
+    uint8_t* sg = scales + row0 * (n / 32);
     for (int base = 0; base < n; base += 128) {
       const int i = base + lane * 4;
       const bool in = i < n;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (in) {
-        const uint2 u = *reinterpret_cast<const uint2*>(xr + i);
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-        v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+      uint2 u[kMxRows];
+#pragma unroll
+      for (int k = 0; k < kMxRows; ++k) {
+        u[k] = make_uint2(0u, 0u);
+        if (in && k < nk) u[k] = *reinterpret_cast<const uint2*>(xg + k * n + i);
       }
+#pragma unroll
+      for (int k = 0; k < kMxRows; ++k) {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[k].x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[k].y));
+        float amax = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        int se = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 2;
+        se = se < -127 ? -127 : se;
+        const float inv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);  // 2^-se
+        if (in && k < nk) {
+          uint32_t w = e2m1x2(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv)) |
+                       (e2m1x2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)) << 8);
+          const uint32_t mag = w & 0x7777u;
+          w = mag | (w & ((mag + 0x7777u) & 0x8888u));  // drop the sign of zero nibbles
+          *reinterpret_cast<uint16_t*>(cg + k * (n / 2) + i / 2) = static_cast<uint16_t>(w);
+          if ((lane & 7) == 0) sg[k * (n / 32) + i / 32] = static_cast<uint8_t>(se + 127);
+        }
+      }
+    }
+  }
+}
+
+// E4M3 rows of exactly 128 (indexer keys): one warp-wide span per row, and a
+// warp takes kMxRows rows at a time with all their loads issued first, as
+// the MXFP4 kernel does.
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_e4m3_rows128_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+                                 uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = static_cast<int64_t>(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (kQuantThreads / 32) * kMxRows;
+  for (int64_t row0 = warp * kMxRows; row0 < rows; row0 += stride) {
+    const int nk = rows - row0 < kMxRows ? static_cast<int>(rows - row0) : kMxRows;
+    const __nv_bfloat16* xg = x + row0 * 128 + lane * 4;
+    uint8_t* cg = codes + row0 * 128 + lane * 4;
+    uint2 u[kMxRows];
+#pragma unroll
+    for (int k = 0; k < kMxRows; ++k) {
+      u[k] = make_uint2(0u, 0u);
+      if (k < nk) u[k] = *reinterpret_cast<const uint2*>(xg + k * 128);
+    }
+#pragma unroll
+    for (int k = 0; k < kMxRows; ++k) {
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[k].x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[k].y));
+      const float v[4] = {f0.x, f0.y, f1.x, f1.y};
       float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      int se = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 2;
-      se = se < -127 ? -127 : se;
-      const float inv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);  // 2^-se
-      if (in) {
-        uint32_t w = e2m1x2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv)) |
-                     (e2m1x2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv)) << 8);
-        const uint32_t mag = w & 0x7777u;
-        w = mag | (w & ((mag + 0x7777u) & 0x8888u));  // drop the sign of zero nibbles
-        *reinterpret_cast<uint16_t*>(cr + i / 2) = static_cast<uint16_t>(w);
-        if ((lane & 7) == 0) sr[i / 32] = static_cast<uint8_t>(se + 127);
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const E4m3Row sc = e4m3_row(amax);
+      if (k < nk) {
+        *reinterpret_cast<uint32_t*>(cg + k * 128) = e4m3x4(v, sc.inv);
+        if (lane == 0) scales[row0 + k] = sc.scale;
       }
     }
   }
@@ -116,17 +167,34 @@ __global__ void __launch_bounds__(kQuantThreads)
 cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
                                   uint8_t* scales, int num_sms, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  const int64_t per_cta = kQuantThreads / 32;
+  // one wave of resident CTAs, each striding over groups of rows
+  auto kernel = n == 128 ? quantize_mxfp4_kernel<128> : quantize_mxfp4_kernel<0>;
+  int resident = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, kQuantThreads, 0);
+  if (e != cudaSuccess) return e;
+  const int64_t per_cta = (kQuantThreads / 32) * kMxRows;
   const int64_t want = (rows + per_cta - 1) / per_cta;
-  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * (resident > 0 ? resident : 1);
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  quantize_mxfp4_kernel<<<grid, kQuantThreads, 0, stream>>>(x, rows, n, codes, scales);
+  kernel<<<grid, kQuantThreads, 0, stream>>>(x, rows, n, codes, scales);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
                                  float* scales, int num_sms, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  if (n == 128) {  // one wave of resident CTAs, each striding over groups of rows
+    int resident = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &resident, quantize_e4m3_rows128_kernel, kQuantThreads, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t per_cta = (kQuantThreads / 32) * kMxRows;
+    const int64_t want = (rows + per_cta - 1) / per_cta;
+    const int64_t cap = static_cast<int64_t>(num_sms) * (resident > 0 ? resident : 1);
+    const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+    quantize_e4m3_rows128_kernel<<<grid, kQuantThreads, 0, stream>>>(x, rows, codes, scales);
+    return cudaGetLastError();
+  }
   const int64_t per_cta = kQuantThreads / 32;
   const int64_t want = (rows + per_cta - 1) / per_cta;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;

@@ -172,11 +172,12 @@ def _u8(t):
     return t.cpu().numpy().astype(np.uint8)
 
 
-@pytest.mark.parametrize("rows,n", [(1000, 128), (37, 64), (5, 4)])
+@pytest.mark.parametrize("rows,n", [(1003, 128), (37, 64), (5, 4)])
 def test_quantize_e4m3_bit_exact(rows, n):
     """Codes and row scales equal the oracle's bit for bit: row magnitudes
     from 1e-4 to 1e4 (subnormal codes included), one all-zero row, rows
-    whose largest element is negative."""
+    whose largest element is negative; 1003 rows of 128 leave a partial
+    group of eight for the 128-wide kernel."""
     g = torch.Generator().manual_seed(50)
     mag = 10.0 ** torch.randint(-4, 5, (rows, 1), generator=g).float()
     x = (torch.randn((rows, n), generator=g) * mag).to(torch.bfloat16)
@@ -190,14 +191,15 @@ def test_quantize_e4m3_bit_exact(rows, n):
     np.testing.assert_array_equal(scales.cpu().numpy(), rs)
 
 
-@pytest.mark.parametrize("rows,n", [(1000, 128), (37, 96), (5, 32), (3, 512)])
+@pytest.mark.parametrize("rows,n", [(1003, 128), (37, 96), (5, 32), (3, 512)])
 def test_quantize_mxfp4_bit_exact(rows, n):
     """E2M1 codes and E8M0 block scales equal the oracle's bit for bit.
     Block magnitudes span 1e-30..1e30 and include subnormal blocks (scale
     exponent clamped at -127); one block is all zeros, another holds -0 and
     small negatives (stored as +0), another puts every element on a tie
     between two E2M1 values, another saturates (amax / X = 7).  n = 96 leaves
-    a partial 128-element span; rows = 0 launches nothing."""
+    a partial 128-element span, 1003 rows a partial group of eight (the
+    128-wide kernel); rows = 0 launches nothing."""
     g = torch.Generator().manual_seed(54)
     nb = n // 32
     mag = 10.0 ** torch.randint(-30, 31, (rows, nb, 1), generator=g).float()

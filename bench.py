@@ -136,6 +136,83 @@ INDEXER_TRAFFIC = {
 }
 
 
+def step_flops(wl):
+    """Algorithmic flops of one pass over the T queries at positions
+    [L-T, L) (causal-exact): 2*HI*dI per (query, visible entry) for the
+    indexer, 4*H*D per (query, key) for each attention branch (QK^T and PV
+    share the key rows); per sequence, times B."""
+    import numpy as np
+    t = np.arange(wl.L - wl.T, wl.L, dtype=np.int64)
+    vis_c = np.minimum((t + 1) // wl.m_csa, wl.L // wl.m_csa)
+    fl = {}
+    if "csa" in wl.branches:
+        fl["indexer"] = float(2 * wl.HI * wl.dI * vis_c.sum())
+        fl["sparse"] = float(4 * wl.H * wl.D * np.minimum(vis_c, wl.k).sum())
+    if "hca" in wl.branches:
+        fl["hca"] = float(4 * wl.H * wl.D * ((t + 1) // wl.m_hca).sum())
+    if "swa" in wl.branches:
+        fl["swa"] = float(4 * wl.H * wl.D * np.minimum(t + 1, wl.W).sum())
+    return {k: v * wl.B for k, v in fl.items()}
+
+
+def measured_bf16_sustained():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return 1400.0
+
+
+def kernel_roofline(wl, keys, per_kernel, hbm, src):
+    """The roofline object of the dominant kernel.  Decode with CSA: the
+    indexer against HBM (its keys are the dominant bytes).  Decode without
+    CSA: the HCA attention at the ridge, with both fractions.  Prefill: the
+    slowest call of the pass against the bf16 tensor peak (the sustained
+    figure: it runs inside a long step)."""
+    peak_src = (f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                else "fallback 6.4 TB/s")
+    if wl.T <= 2 and "csa" in wl.branches:
+        ib = indexer_bytes(wl, keys)
+        idx_ms = per_kernel["indexer"]
+        achieved = ib / (idx_ms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "indexer_score_kernel", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": indexer_traffic(wl, keys),
+                "traffic_source": "ncu dram bytes of an 8 x 65,536-entry launch scaled by "
+                                  "entries (" + INDEXER_TRAFFIC["profile"] + ")",
+                "peak_source": peak_src, "algorithmic_bytes_per_launch": ib,
+                "avg_launch_ms": idx_ms}
+    fl = step_flops(wl)
+    tf = measured_bf16_sustained()
+    if wl.T <= 2:
+        # HCA decode: every visible entry once per sequence, the queries and outputs
+        n_h = wl.L // wl.m_hca
+        by = wl.B * (n_h * wl.D * 2 + wl.T * (2 * wl.H * wl.D * 2 + wl.H * 4))
+        name = "hca" if "hca" in per_kernel else "attn_fused"
+        ms = per_kernel[name]
+        a_gbs = by / (ms / 1e3) / 1e9
+        a_tf = fl["hca"] / (ms / 1e3) / 1e12
+        kern = "attn_kernel<kHca>" if name == "hca" else "attn_kernel<kFused> (HCA segment)"
+        return {"bound": "hbm", "kernel": kern, "achieved": a_gbs, "peak": hbm,
+                "unit": "GB/s", "frac": a_gbs / hbm, "traffic": None, "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": by, "avg_launch_ms": ms,
+                "tensor": {"achieved": a_tf, "peak": tf, "unit": "TFLOP/s", "frac": a_tf / tf,
+                           "flops_per_launch": fl["hca"]},
+                "note": "at the ridge: both the HBM and the tensor fraction are given"}
+    calls = {n: per_kernel[n] for n in fl if n in per_kernel}
+    name = max(calls, key=calls.get)
+    ms = calls[name]
+    achieved = fl[name] / (ms / 1e3) / 1e12
+    kern = {"indexer": "indexer_score_kernel", "sparse": "attn_kernel<kSparse>",
+            "hca": "attn_kernel<kHca>", "swa": "attn_kernel<kSwa>"}[name]
+    return {"bound": "tensor", "kernel": kern, "achieved": achieved, "peak": tf,
+            "unit": "TFLOP/s", "frac": achieved / tf, "traffic": None,
+            "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops_sustained)",
+            "flops_per_launch": fl[name], "avg_launch_ms": ms,
+            "by_call": {n: {"ms": per_kernel[n], "tflops": fl[n] / (per_kernel[n] / 1e3) / 1e12}
+                        for n in calls}}
+
+
 def indexer_traffic(wl, keys="bf16"):
     """Per-launch DRAM bytes scaled from the recorded capture, or None when
     the indexer sources have changed since it was taken."""

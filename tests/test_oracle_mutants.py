@@ -3,9 +3,11 @@
 Each case copies oracle.c, plants one mistake in one function (a dropped
 term, a wrong sign, index, position or order, a missing normalisation),
 builds the copy into its own library under _build/, and runs the pin tests
-(tests/test_oracle_pins.py) against it in a child process.  The case passes
-when the pins fail: exit status 1, a failed assertion rather than a crash.
-The oracle source itself is never modified.  Every planted mistake keeps
+(tests/test_oracle_pins.py) against it in a child process.  Mistakes in the
+layer composition (oracle.py) go into a copy of the package, imported ahead
+of the pins.  A case passes when the pins fail: exit status 1, a failed
+assertion rather than a crash.  Unchanged copies taken the same routes pass.
+The oracle's own files are never modified, and every planted mistake keeps
 every memory access in bounds.
 """
 import os
@@ -115,6 +117,31 @@ MISTAKES = [
 ]
 
 
+# Mistakes in the layer composition (oracle.py): how the branches are fed,
+# kept and merged.
+PY_MISTAKES = [
+    ("merge leaves out the sink",
+     'out, lse = merge(o_list, l_list, inp.get("sink"), pos, r, base)',
+     'out, lse = merge(o_list, l_list, None, pos, r, base)'),
+    ("merge rotates back by the next position",
+     'out, lse = merge(o_list, l_list, inp.get("sink"), pos, r, base)',
+     'out, lse = merge(o_list, l_list, inp.get("sink"), pos + 1, r, base)'),
+    ("the HCA branch is not merged",
+     "        o_list.append(o)\n        l_list.append(l)\n        if keep:\n"
+     "            res.update(kv_h=kv_h",
+     "        if keep:\n            res.update(kv_h=kv_h"),
+    ("the CSA cache is built one entry short",
+     "n = min(L // m, visible(tmax, m)) if L >= m else 0",
+     "n = min(L // m, visible(tmax, m)) - 1 if L >= m else 0"),
+    ("the indexer scores with the wrong stride",
+     'scores = indexer_scores(inp["iq"], inp["w"], ik_c, pos, m)',
+     'scores = indexer_scores(inp["iq"], inp["w"], ik_c, pos, m + 1)'),
+    ("the SWA window is halved",
+     'attention(KIND_SWA, inp["q"], kv_raw, pos, W=cfg["W"]',
+     'attention(KIND_SWA, inp["q"], kv_raw, pos, W=cfg["W"] // 2'),
+]
+
+
 def _function(text, first_line):
     a = text.index(first_line)
     return a, text.index("\n}\n", a) + 3
@@ -149,4 +176,48 @@ def test_pins_fail_on_planted_mistake(name, fn, old, new):
     tag = "m%02d" % [m[0] for m in MISTAKES].index(name)
     r = _pins_against(src[:a] + body.replace(old, new) + src[b:], tag)
     assert r.returncode == 1, (r.returncode, r.stdout[-2000:])
+    assert "failed" in r.stdout.splitlines()[-1]
+
+
+
+def _package_copy(tag, oracle_py):
+    """A copy of the oracle package under _build/ with the given oracle.py."""
+    import shutil
+    pkg = os.path.join(OUT, tag, "oracle")
+    os.makedirs(pkg, exist_ok=True)
+    for f in ("__init__.py", "build.py"):
+        shutil.copy(os.path.join(ROOT, "oracle", f), os.path.join(pkg, f))
+    with open(os.path.join(pkg, "oracle.py"), "w") as f:
+        f.write(oracle_py)
+    return pkg
+
+
+def _pins_with_package(pkg):
+    """Run the pins in a child that imports the package copy first (the
+    unchanged C library underneath)."""
+    driver = ("import sys; sys.path.insert(0, %r); import oracle; "
+              "assert oracle.__file__.startswith(%r); import pytest; "
+              "sys.exit(pytest.main(['-x', '-q', '-p', 'no:cacheprovider', %r]))"
+              % (os.path.dirname(pkg), pkg, os.path.join(ROOT, "tests", "test_oracle_pins.py")))
+    return subprocess.run([sys.executable, "-c", driver], cwd=ROOT, capture_output=True,
+                          text=True, env=dict(os.environ, ORACLE_LIB=obuild.build()),
+                          timeout=600)
+
+
+def test_unchanged_package_copy_passes_the_pins():
+    """The control of the composition cases."""
+    src = open(os.path.join(ROOT, "oracle", "oracle.py")).read()
+    r = _pins_with_package(_package_copy("pycontrol", src))
+    assert r.returncode == 0, (r.stdout[-2000:], r.stderr[-2000:])
+
+
+@pytest.mark.parametrize("name,old,new", PY_MISTAKES, ids=[m[0] for m in PY_MISTAKES])
+def test_pins_fail_on_planted_composition_mistake(name, old, new):
+    """A copy of the oracle package with one mistake in oracle.py is imported
+    ahead of the pins."""
+    src = open(os.path.join(ROOT, "oracle", "oracle.py")).read()
+    assert src.count(old) == 1
+    tag = "py%02d" % [m[0] for m in PY_MISTAKES].index(name)
+    r = _pins_with_package(_package_copy(tag, src.replace(old, new)))
+    assert r.returncode == 1, (r.returncode, r.stdout[-2000:], r.stderr[-2000:])
     assert "failed" in r.stdout.splitlines()[-1]

@@ -642,6 +642,70 @@ def test_merge_inverse_rope_and_empty_branch(orc):
     np.testing.assert_allclose(lse2, lse, rtol=1e-14)
 
 
+def test_layer_composition_reduces_to_causal_attention(orc):
+    """The whole layer (compress, bf16 storage, indexer, top-k, branches,
+    sink merge, inverse RoPE) with C(1,1) for both compressors, k and W at
+    least L and no sink: every branch is standard causal attention over the
+    normalised, roped tokens (torch SDPA, is_causal), rotated back by the
+    query position.  Two identical branches merge to the same output with
+    lse + ln 2; a finite sink s scales the output by 1 / (1 + e^(s - lse))."""
+    from sparse_attention_26_b300 import synth
+    wl = synth.scaled(synth.WORKLOADS["tiny"], L=40, T=40, H=2, D=32, r=8, HI=2, dI=16, k=64)
+    inp = synth.to_numpy(synth.make_inputs(wl, 3))
+    inp.pop("sink")
+    cfg = dict(wl.cfg(), m_csa=1, w_csa=1, m_hca=1, w_hca=1, k=64, W=64, r=8)
+    L, H, D, r = 40, 2, 32, 8
+    raw = f64(inp["kv_raw"])[0]
+    keys64 = np.stack([orc.rope(orc.rmsnorm(raw[u], None, 1e-6), r, u) for u in range(L)])
+    keys16 = f64(orc.f64_to_bf16(keys64))
+    qq = np.stack([[_prep_q(orc, f64(inp["q"])[0, t, h], r, t) for t in range(L)]
+                   for h in range(H)])
+
+    def reference(keys):
+        kt = torch.from_numpy(keys)[None, None].expand(1, H, L, D)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(qq)[None], kt, kt, is_causal=True)[0].numpy()   # [H, L, D]
+        lg = torch.from_numpy(qq) @ torch.from_numpy(keys).T / math.sqrt(D)
+        lg = lg.masked_fill(torch.triu(torch.ones(L, L, dtype=torch.bool), 1), -math.inf)
+        lse = torch.logsumexp(lg, -1).numpy()                                # [H, L]
+        out = np.stack([[orc.rope(o[h, t], r, t, sign=-1) for h in range(H)] for t in range(L)])
+        return out, lse.T
+
+    ref16, lse16 = reference(keys16)
+    ref64, lse64 = reference(keys64)
+    for branches, ref, lse_ref in [(("csa",), ref16, lse16), (("hca",), ref16, lse16),
+                                   (("swa",), ref64, lse64)]:
+        res = orc.layer(inp, cfg, branches=branches)
+        np.testing.assert_allclose(res["out"][0], ref, rtol=1e-10, atol=1e-10)
+        np.testing.assert_allclose(res["lse"][0], lse_ref, rtol=1e-10, atol=1e-10)
+    both = orc.layer(inp, cfg, branches=("csa", "hca"))
+    np.testing.assert_allclose(both["out"][0], ref16, rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(both["lse"][0], lse16 + math.log(2), rtol=1e-10, atol=1e-10)
+    sink = np.array([0.5, -1.5], np.float32)
+    sunk = orc.layer(dict(inp, sink=sink), cfg, branches=("swa",))
+    factor = 1 / (1 + np.exp(sink.astype(np.float64)[None, :] - lse64))    # [L, H]
+    np.testing.assert_allclose(sunk["out"][0], ref64 * factor[..., None], rtol=1e-10,
+                               atol=1e-10)
+    np.testing.assert_allclose(sunk["lse"][0], np.logaddexp(lse64, sink[None, :]), rtol=1e-10,
+                               atol=1e-10)
+    # k = 4 < visible: the CSA branch attends to the 4 best-scored entries.
+    # C(1,1) leaves an indexer key as its token, so the scores are those of
+    # the raw keys; numpy's sort picks the 4 (score descending, index
+    # ascending) and torch SDPA attends to them.
+    k = 4
+    sel = orc.layer(inp, dict(cfg, k=k), branches=("csa",))
+    sc = orc.indexer_scores(inp["iq"], inp["w"], inp["ik_raw"], inp["pos"], 1)[0]
+    for t in range(L):
+        n = t + 1
+        pick = np.lexsort((np.arange(n), -sc[t, :n]))[:k]
+        kt = torch.from_numpy(keys16[pick])[None]
+        for h in range(H):
+            o = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(qq[h, t])[None, None], kt, kt)[0, 0].numpy()
+            np.testing.assert_allclose(sel["out"][0, t, h], orc.rope(o, r, t, sign=-1),
+                                       rtol=1e-10, atol=1e-10)
+
+
 def test_tiny_layer_runs(orc):
     from sparse_attention_26_b300 import synth
     wl = synth.WORKLOADS["tiny"]

@@ -40,6 +40,33 @@ def test_library_exports_every_declared_symbol(L):
         assert s in hattn._SIGS, f"{s} has no binding signature"
 
 
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature in the binding has the header's parameter count,
+    and each parameter the header's kind (pointer, int, int64, float, size_t,
+    uint64), so no call passes arguments the library reads differently."""
+    txt = open(os.path.join(ROOT, "include", "hattn.h")).read()
+    decls = re.findall(r"HATTN_API\s+([^;]*?)\b(hattn_\w+)\s*\(([^)]*)\)\s*;", txt, re.S)
+    assert len(decls) == len(header_symbols())
+    ptr_array = ctypes.POINTER(ctypes.c_void_p)
+    scalar = {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "float": ctypes.c_float,
+              "size_t": ctypes.c_size_t, "uint64_t": ctypes.c_uint64}
+    ret_kind = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "const char*": ctypes.c_char_p}
+    for ret, name, params in decls:
+        restype, argtypes = hattn._SIGS[name]
+        assert restype is ret_kind[" ".join(ret.split())], name
+        ps = [" ".join(p.split()) for p in params.split(",")]
+        ps = [p for p in ps if p and p != "void"]
+        assert len(ps) == len(argtypes), f"{name}: header {len(ps)} args, binding {len(argtypes)}"
+        for i, (p, a) in enumerate(zip(ps, argtypes)):
+            ctype = re.sub(r"\s*\b\w+$", "", p)
+            if ctype.endswith("* const*"):
+                assert a is ptr_array, (name, i, p)
+            elif ctype.endswith("*") or ctype == "hattn_stream_t":
+                assert a is ctypes.c_void_p or issubclass(a, ctypes._Pointer), (name, i, p)
+            else:
+                assert a is scalar[ctype], (name, i, p, a)
+
+
 def test_status_strings(L):
     assert hattn.status_string(0) == "ok"
     assert "misaligned" in hattn.status_string(2)

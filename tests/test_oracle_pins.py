@@ -706,6 +706,33 @@ def test_layer_composition_reduces_to_causal_attention(orc):
                                        rtol=1e-10, atol=1e-10)
 
 
+def test_degenerate_cases(orc):
+    """Nothing to attend: an HCA query before the first entry is complete
+    (t < m - 1) and a CSA query whose indices are all padding both give
+    o = 0 and lse = -inf; top-k over no visible entry is all padding; a
+    merge of empty branches gives 0 and lse = -inf without a sink, and 0 with
+    lse = s with a sink s (the sink takes all the weight)."""
+    rng = np.random.default_rng(31)
+    B, T, H, D, r = 1, 2, 2, 32, 8
+    q = b16(rng.standard_normal((B, T, H, D)))
+    cache = b16(rng.standard_normal((B, 4, D)))
+    pos = np.array([[0, 126]], np.int32)
+    o, l = orc.attention(orc.KIND_HCA, q, cache, pos, m=128, r=r)
+    assert (o == 0).all() and np.isneginf(l).all()
+    idx = np.full((B, T, 8), -1, np.int32)
+    o2, l2 = orc.attention(orc.KIND_SPARSE, q, cache, pos, idx=idx, r=r)
+    assert (o2 == 0).all() and np.isneginf(l2).all()
+    sc = np.full((2, 16), np.nan)
+    top = orc.topk(sc, np.array([2, 0], np.int32), 4, 5)
+    assert (top == -1).all()
+    out, lse = orc.merge([o, o2], [l, l2], None, pos, r)
+    assert (out == 0).all() and np.isneginf(lse).all()
+    sink = np.array([0.25, -2.0], np.float32)
+    out, lse = orc.merge([o, o2], [l, l2], sink, pos, r)
+    assert (out == 0).all()
+    np.testing.assert_array_equal(lse[0], np.tile(sink.astype(np.float64), (T, 1)))
+
+
 def test_tiny_layer_runs(orc):
     from sparse_attention_26_b300 import synth
     wl = synth.WORKLOADS["tiny"]

@@ -317,3 +317,18 @@ def test_fused_attention_validation_and_sizes(L):
                             N) == hattn.INVALID_ARG
     assert L.hattn_swa_keys(FAKE, N, FAKE, 1, 1, 100, 512, 128, 64, 1e4, 1e-6, MISAL,
                             N) == hattn.MISALIGNED
+
+
+def test_no_fallback_without_the_library_or_a_gpu(monkeypatch):
+    """The binding has no CPU or PyTorch path: with the library missing it
+    raises, and CPU tensors are refused before any call."""
+    import torch
+    x = torch.zeros((4, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        hattn.quantize_mxfp4(x)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        hattn.quantize_e4m3(x)
+    monkeypatch.setattr(hattn, "_lib", None)
+    monkeypatch.setattr(hattn, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libhattn.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        hattn.lib()

@@ -3,6 +3,7 @@ import json
 import os
 
 import numpy as np
+import pytest
 import torch
 
 from sparse_attention_26_b300 import synth
@@ -129,3 +130,29 @@ def test_stack_launch_count_at_1m():
                      k=wl.k, L_max=wl.L, device="meta")
     assert st.launches_per_step(wl.L - 1) == 2 * 4 + 30 * 7 + 29 * 5 == 363
     assert st.launches_per_step(wl.L - 2) == 2 * 4 + 30 * 6 + 29 * 4
+
+
+def test_which_steps_take_the_fused_attention():
+    """Decode steps of any branch subset and all-three-branch steps take the
+    fused attention; a prefill of one or two branches (many queries per
+    sequence) runs the branch calls. The segment mask names the branches."""
+    from sparse_attention_26_b300 import hattn
+    want = {"hybrid_decode_1m": True, "hybrid_decode_1m_mtp2": True, "pro_csa_decode": True,
+            "hca_decode": True, "hca_prefill": False, "flash_csa_prefill": False}
+    seg = {"csa": hattn.SEG_CSA, "hca": hattn.SEG_HCA, "swa": hattn.SEG_SWA}
+    for name, fused in want.items():
+        wl, layer = _meta_layer(name)
+        assert layer.can_fuse(wl.T) == fused, name
+        assert layer.segments() == sum(seg[b] for b in wl.branches), name
+        names = layer.event_names(wl.T)
+        assert ("attn_fused" in names) == fused, (name, names)
+        assert ("indexer" in names) == ("csa" in wl.branches), (name, names)
+
+
+def test_stack_ring_must_hold_every_window():
+    from sparse_attention_26_b300.stack import DecodeStack, layer_pattern
+    kw = dict(B=1, H=128, D=512, r=64, HI=64, dI=128, k=1024, L_max=4096, device="meta")
+    for ring in (192, 64):   # not a power of two; smaller than the HCA window
+        with pytest.raises(ValueError, match="ring"):
+            DecodeStack(layer_pattern(4), ring=ring, **kw)
+    assert DecodeStack(layer_pattern(4), ring=128, **kw).ring == 128

@@ -1,4 +1,7 @@
-"""The synthetic workloads carry the structural constants printed on the pages."""
+"""The synthetic workloads carry the structural constants printed on the
+pages, and the layer and stack plan their steps (entries completed, launch
+counts, fused or branch attention) as the recorded runs did: host logic,
+checked on meta tensors without a device."""
 import json
 import os
 

@@ -130,3 +130,14 @@ def test_roofline_prefill_takes_the_slowest_call():
 def test_traffic_profile_is_committed():
     path = os.path.join(bench.ROOT, bench.INDEXER_TRAFFIC["profile"])
     assert os.path.isfile(path)
+
+
+def test_default_run_keeps_the_timing_contract(monkeypatch):
+    """With no flags: one GPU, at least 3 warm-up steps, a short timed run,
+    the 1M decode workload, the oracle baseline and the end-to-end leg on."""
+    monkeypatch.setattr("sys.argv", ["bench.py"])
+    a = bench.parse()
+    assert a.gpus == 1 and a.warmup >= 3 and 1 <= a.steps <= 100
+    assert a.impl == "ours" and a.workload == "hybrid_decode_1m"
+    assert not a.no_cpu_baseline and not a.no_e2e and a.indexer_keys == "bf16"
+    assert not a.stack and not a.cache_build and not a.quantize_keys

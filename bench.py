@@ -426,11 +426,26 @@ def cpu_baseline_prefill(wl, n_sample=None):
     per_query = (time.perf_counter() - t0) / len(ts)
     per_pass = t_comp + per_query * wl.T
     return {"value": wl.T / per_pass, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "host": host_cpu(),
             "sample": f"extrapolated: one sequence's prefill pass of {wl.name} = the compression "
                       f"of its new entries (timed in full, {t_comp:.2f} s) + {wl.T} queries x "
                       f"{per_query:.3f} s per query (mean of {len(ts)} evenly spaced queries), "
                       "single-threaded fp64 C, seeded synthetic caches",
             "seconds_per_pass": per_pass}
+
+
+def host_cpu():
+    """The host the oracle baseline ran on: CPU model and logical cores."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"cpu_model": model, "nproc": os.cpu_count()}
 
 
 def cpu_baseline(wl, steps=1):
@@ -442,6 +457,7 @@ def cpu_baseline(wl, steps=1):
         oracle_step(wl, s)
     dt = (time.perf_counter() - t0) / steps
     return {"value": 1.0 / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "host": host_cpu(),
             "sample": f"1 query of 1 of {wl.B} sequences, 1 decode step of {wl.name} at "
                       f"full size ({wl.L}-token context: {wl.L // wl.m_csa} indexer entries, "
                       f"top-{wl.k}, "
@@ -495,7 +511,7 @@ def run_reference(args, world, rank, budget_s=150.0):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(wl, sample=sample),
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_cpu()},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -141,3 +141,14 @@ def test_default_run_keeps_the_timing_contract(monkeypatch):
     assert a.impl == "ours" and a.workload == "hybrid_decode_1m"
     assert not a.no_cpu_baseline and not a.no_e2e and a.indexer_keys == "bf16"
     assert not a.stack and not a.cache_build and not a.quantize_keys
+
+
+def test_cpu_baseline_runs_on_the_host():
+    """The oracle legs of the bench at reduced sizes, on CPU: a decode step
+    and a sampled prefill pass, each a single-threaded oracle time with the
+    host's CPU model and core count."""
+    dec = bench.cpu_baseline(synth.scaled(W["hybrid_decode_1m"], L=8192))
+    assert dec["kind"] == "oracle" and dec["cores"] == 1 and dec["value"] > 0
+    assert dec["host"]["nproc"] >= 1 and dec["host"]["cpu_model"]
+    pre = bench.cpu_baseline(synth.scaled(W["flash_csa_prefill"], L=512, T=512))
+    assert pre["value"] > 0 and pre["sample"].startswith("extrapolated")

@@ -75,3 +75,28 @@ def test_reference_arm_prints_on_rank_zero_only():
     with redirect_stdout(buf):
         bench.run_reference(A(), 2, 1)
     assert buf.getvalue() == ""
+
+
+def test_reference_arm_line_on_rank_zero():
+    """Rank 0 times the oracle on a bounded sample and prints one JSON line
+    with the reference arm's keys: impl, the bench's metric and unit, a
+    cpu_baseline describing this run, and an e2e object with no host copies."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        steps, warmup, gpus, workload, batch, context = 1, 0, 1, "hybrid_decode_1m", 0, 1 << 16
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(A(), 1, 0, budget_s=2.0)
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] == 1 and d["cpu_baseline"]["host"]["nproc"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["steps"] == 1 and d["dtype"] == "f64"

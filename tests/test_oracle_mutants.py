@@ -142,6 +142,14 @@ PY_MISTAKES = [
 ]
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _clean_up_builds():
+    """The planted builds live only while this module runs."""
+    import shutil
+    yield
+    shutil.rmtree(OUT, ignore_errors=True)
+
+
 def _function(text, first_line):
     a = text.index(first_line)
     return a, text.index("\n}\n", a) + 3

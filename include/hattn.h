@@ -52,6 +52,20 @@ extern "C" {
 
 typedef void* hattn_stream_t; /* cudaStream_t */
 
+/* Launch flags of the calls that take `flags` (a per-call argument; the
+ * library keeps no launch mode between calls).
+ *
+ * HATTN_LAUNCH_DEPENDENT: launch the call's kernels as programmatic
+ * dependents (CUDA programmatic dependent launch) of the previous kernel in
+ * `stream`.  They may start -- allocate tensor memory, initialise barriers,
+ * prefetch descriptors -- while that kernel finishes, and wait for it
+ * (griddepcontrol.wait) before reading anything it may write.  Set it only
+ * where the previous kernel in the stream is the one producing the call's
+ * inputs: it relaxes only that one dependency.  Each call's comment says
+ * which of its inputs it may read before that wait.  Every kernel of the
+ * library lets its own dependents start early. */
+#define HATTN_LAUNCH_DEPENDENT 1
+
 enum {
   HATTN_OK = 0,
   HATTN_ERR_INVALID_ARG = 1, /* null pointer, size out of range, inconsistent sizes */
@@ -204,8 +218,10 @@ HATTN_API int hattn_csa_compress_fp8(const void* kv_raw, const void* ik_raw, con
  *   idx_out [B][T][k] int32, score_out [B][T][N_cap] fp32 or NULL (when given,
  *   receives I for j < n; entries j >= n are left untouched).
  *   workspace: device buffer of at least hattn_indexer_topk_workspace_bytes()
- *   bytes (may be NULL when that is 0); contents need no initialisation.
- *   Limits: 1 <= k <= 2048, HI * min(T, 256 / HI) <= 256, N_cap <= 786432.
+ *   bytes (may be NULL when that is 0): the scores (unless score_out is
+ *   given), then the selection's scratch (hattn_topk_workspace_bytes);
+ *   contents need no initialisation.
+ *   Limits: 1 <= k <= 2048, HI * min(T, 256 / HI) <= 256, N_cap < 2^31.
  * ---------------------------------------------------------------------- */
 HATTN_API int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
                        int B, int T, int HI, int dI, int64_t N_cap, int k, int m,
@@ -219,16 +235,18 @@ HATTN_API size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap,
  * that owns a fixed memory pool, a plugin host that forbids device
  * allocations, or a stream-ordered path that must not synchronise on the
  * allocator.  The same selection as hattn_indexer_topk, but the fp32 scores
- * live in a scratch array compiled into this library (4,194,304 scores,
- * 16 MiB, held on every device that loads the library until the process
- * exits), so the call allocates nothing; the caller still passes inputs and
- * idx_out.  The pages have no counterpart of this call.
+ * and the selection's scratch live in an array compiled into this library
+ * (34 MiB: 4,194,304 scores, then up to 18 MiB of selection scratch, held
+ * on every device that loads the library until the process exits), so the
+ * call allocates nothing; the caller still passes inputs and idx_out.  The
+ * pages have no counterpart of this call.
  *   - B * T * N_cap must not exceed 4,194,304 (HATTN_ERR_INVALID_ARG).
  *   - The first call on a device looks the scratch address up (cudaGetSymbolAddress)
  *     with that device current; make that first call before any stream capture.
  *   - Every call on a device shares the one scratch array: calls whose work
  *     overlaps on the GPU (other streams, other host threads) race.  No
- *     contents need clearing between calls. */
+ *     contents need clearing between calls: every score the selection reads
+ *     is written first, and the selection clears its own counters. */
 HATTN_API int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,
                                          const int32_t* pos, int B, int T, int HI, int dI,
                                          int64_t N_cap, int k, int m, int32_t* idx_out,
@@ -241,22 +259,33 @@ HATTN_API int hattn_indexer_topk_noalloc(const void* iq, const float* w, const v
 HATTN_API int hattn_indexer_scores(const void* iq, const float* w, const void* ik_c,
                                    const int32_t* pos, int B, int T, int HI, int dI,
                                    int64_t N_cap, int m, float* score_out, hattn_stream_t stream);
-/* hattn_indexer_scores with two scheduling options.
+/* hattn_indexer_scores with scheduling options.
  *   n_sms: run the persistent score kernel on at most that many SMs (0 = all;
  *   one CTA per SM used), leaving the others to work on another stream.
- *   fresh_from: with dependent launches enabled (hattn_set_dependent_launch),
- *   the entries of ik_c at index >= fresh_from are the only ones the
- *   previous kernel in the stream may write (say, the compressor of the
- *   newest entry); blocks of entries below it are read without waiting for
- *   that kernel.  -1: any entry may be written (wait before the first read).
- *   Ignored without dependent launches. */
+ *   flags: HATTN_LAUNCH_DEPENDENT or 0.  A dependent launch reads iq, w and
+ *   pos before its wait, so those must not be written by the previous
+ *   kernel in the stream; of ik_c it reads before the wait only the blocks
+ *   of entries below fresh_from.
+ *   fresh_from: with HATTN_LAUNCH_DEPENDENT, the entries of ik_c at index >=
+ *   fresh_from are the only ones the previous kernel in the stream may write
+ *   (say, the compressor of the newest entry); blocks of entries below it
+ *   are read without waiting for that kernel.  -1: any entry may be written
+ *   (wait before the first key read).  Ignored without the flag. */
 HATTN_API int hattn_indexer_scores_ex(const void* iq, const float* w, const void* ik_c,
                                       const int32_t* pos, int B, int T, int HI, int dI,
                                       int64_t N_cap, int m, int n_sms, int64_t fresh_from,
-                                      float* score_out, hattn_stream_t stream);
+                                      float* score_out, int flags, hattn_stream_t stream);
+/* hattn_topk_select: scores [B][T][N_cap] fp32 (entries j < n as written by
+ * the score calls) -> idx_out [B][T][k] int32.  Few long rows (say 8 rows of
+ * 262,144) are spread over many CTAs, which needs a caller-owned scratch of
+ * hattn_topk_workspace_bytes(B, T, N_cap, k) bytes (0 when the rows fit one
+ * CTA each; workspace may then be NULL).  The scratch needs no
+ * initialisation; calls sharing one scratch must not overlap on the GPU.
+ * flags: HATTN_LAUNCH_DEPENDENT or 0 (every input is read after the wait). */
+HATTN_API size_t hattn_topk_workspace_bytes(int B, int T, int64_t N_cap, int k);
 HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T,
-                                int64_t N_cap, int k, int m, int32_t* idx_out,
-                                hattn_stream_t stream);
+                                int64_t N_cap, int k, int m, int32_t* idx_out, void* workspace,
+                                size_t ws_bytes, int flags, hattn_stream_t stream);
 
 /* hattn_indexer_scores_ex over FP8 keys: ik8 [B][N_cap][128] E4M3 codes and
  * ik_scale [B][N_cap] fp32 (see hattn_quantize_e4m3; dI must be 128 and
@@ -266,13 +295,13 @@ HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, 
  *   I[j] = sum_h w[b][t][h] * max(0, q^[b][t][h] . k^[b][j]),
  * computed as ik_scale[j] * sum_h (w * q_scale_h) * max(0, q8_h . k8_j) with
  * the code products on the tensor cores (fp32 accumulation).  Scores go to
- * score_out as for hattn_indexer_scores; n_sms and fresh_from as for
- * hattn_indexer_scores_ex.  The key stream is 132 bytes per entry instead of
- * 256. */
+ * score_out as for hattn_indexer_scores; n_sms, fresh_from and flags as for
+ * hattn_indexer_scores_ex (a dependent launch reads ik_scale like ik8).  The
+ * key stream is 132 bytes per entry instead of 256. */
 HATTN_API int hattn_indexer_scores_fp8(const void* iq, const float* w, const void* ik8,
                                        const float* ik_scale, const int32_t* pos, int B, int T,
                                        int HI, int dI, int64_t N_cap, int m, int n_sms,
-                                       int64_t fresh_from, float* score_out,
+                                       int64_t fresh_from, float* score_out, int flags,
                                        hattn_stream_t stream);
 
 /* -------------------------------------------------------------------------
@@ -365,14 +394,15 @@ HATTN_API int hattn_swa_keys_ring(const void* kv_ring, const float* gamma_kv, co
  * workspace) are those of the branch calls; the workspace size and split
  * count come from the two functions below, given the same segments and
  * n_sms.  One query per row block: the MMA rows are the H heads of one
- * query (H <= 128). */
+ * query (H <= 128).  flags: HATTN_LAUNCH_DEPENDENT or 0 (a dependent launch
+ * reads pos before its wait, everything else after it). */
 HATTN_API int hattn_hybrid_attn(const void* q, const float* gamma_q, int q_prepped,
                                 const void* kv_c, const int32_t* idx, int64_t N_c, int k,
                                 const void* kv_h, int64_t N_h, int m, const void* kv_w, int W,
                                 const int32_t* pos, int B, int T, int H, int D, int r,
                                 float rope_base, float eps, float scale, int segments, int n_sms,
                                 void* o, float* lse, void* workspace, size_t ws_bytes,
-                                hattn_stream_t stream);
+                                int flags, hattn_stream_t stream);
 HATTN_API size_t hattn_hybrid_attn_workspace_bytes(int B, int T, int H, int D, int k,
                                                    int64_t N_h, int W, int segments, int n_sms,
                                                    int q_prepped, int partials);
@@ -414,12 +444,13 @@ HATTN_API int hattn_lse_merge(const void* const* o_list, const float* const* lse
  * part_lse_list[i] fp32 [B*T*H][nsplit[i]] (as left by an attention call with
  * o == lse == NULL).  The result equals combining each branch's splits and
  * then merging (a branch's own normalisation cancels).  At most 128 partials
- * per row in total. */
+ * per row in total.  flags: HATTN_LAUNCH_DEPENDENT or 0 (every input is read
+ * after the wait). */
 HATTN_API int hattn_lse_merge_splits(const void* const* part_o_list,
                                      const float* const* part_lse_list, const int* nsplit, int nb,
                                      const float* sink, const int32_t* pos, int B, int T, int H,
                                      int D, int r, float rope_base, void* out, float* lse_out,
-                                     hattn_stream_t stream);
+                                     int flags, hattn_stream_t stream);
 
 /* -------------------------------------------------------------------------
  * Status and diagnostics.
@@ -436,19 +467,6 @@ HATTN_API int hattn_check_status(hattn_stream_t stream);
  * kernel then records HATTN_ERR_TIMEOUT and returns (no fault, no hang). */
 HATTN_API int hattn_selftest_wait_timeout(uint64_t timeout_ns, hattn_stream_t stream);
 /* Library version string. */
-/* Dependent launches (CUDA programmatic dependent launch).  While enabled on
- * the calling host thread, the kernels of hattn_indexer_scores(_sms),
- * hattn_topk_select, the attention calls and the merges are launched as
- * programmatic dependents of the previous kernel in their stream: they may
- * start (allocate tensor memory, initialise barriers, prefetch descriptors,
- * load inputs the predecessor does not write) while that kernel finishes,
- * and wait for it (griddepcontrol.wait) before reading anything it may
- * write.  Every kernel of the library also lets its dependents start early.
- * Use it only where the previous kernel in the stream is the call that
- * produces the inputs (it relaxes only that one dependency).  Off by
- * default; returns the previous setting. */
-HATTN_API int hattn_set_dependent_launch(int enable);
-
 HATTN_API const char* hattn_version(void);
 
 #ifdef __cplusplus

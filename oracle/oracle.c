@@ -25,7 +25,7 @@
  *        64 dims with inverse RoPE on outputs, RMSNorm on q and compressed KV,
  *        designed attention sinks; section "Inference efficiency": shared-KV MQA.
  *
- * Readings adopted where the pages are silent (listed in the design notes):
+ * Readings adopted where the pages are silent:
  *  - entry j of C(m,w) pools tokens u in [m(j+1)-w, m(j+1)-1], u >= 0, with
  *    weights softmax(gate_u) over the existing tokens (CSA: m=4, w=8, i.e. the
  *    8 tokens [4j-4, 4j+4));

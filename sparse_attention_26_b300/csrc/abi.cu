@@ -16,7 +16,6 @@ using namespace hattn;
 namespace {
 
 thread_local char g_last_error[512] = "";
-thread_local bool g_dependent_launch = false;
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -128,6 +127,11 @@ int make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims,
   do {                                                                         \
     if ((p) && !aligned4(p)) return fail(HATTN_ERR_MISALIGNED, "%s is not 4-byte aligned", #p); \
   } while (0)
+
+int check_flags(int flags) {
+  REQUIRE((flags & ~HATTN_LAUNCH_DEPENDENT) == 0, "flags=%d: unknown bits", flags);
+  return HATTN_OK;
+}
 
 int check_rope(int D, int r, float rope_base, float eps) {
   REQUIRE(r >= 0 && r % 2 == 0 && r <= D && r <= 2 * kMaxRopePairs,
@@ -271,7 +275,9 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
                 const float* gamma_kv, const int32_t* idx, const int32_t* pos, int B, int T, int H,
                 int D, int64_t N_rows, int k, int m, int W, int r, float rope_base, float eps,
                 float scale, void* o, float* lse, void* workspace, size_t ws_bytes,
-                hattn_stream_t stream, const FusedSources* fs = nullptr) {
+                hattn_stream_t stream, const FusedSources* fs = nullptr, int flags = 0) {
+  if (int rcf = check_flags(flags)) return rcf;
+  const bool dependent = (flags & HATTN_LAUNCH_DEPENDENT) != 0;
   REQUIRE_PTR(q);
   if (kind != kFused || (fs && (fs->segments & 1))) REQUIRE_PTR(kv);
   REQUIRE_PTR(pos);
@@ -406,6 +412,8 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.nsplit = p.nsplit;
   a.keys_per_split = p.keys_per_split;
   a.nds = p.nds;
+  // the attention kernel is a dependent of the query preparation it follows
+  a.dependent = (dependent || !q_prepped) ? 1 : 0;
   cudaError_t e = launch_attention(tm, tm2, tm_q, a, p, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (p.nsplit > 1 && !partials) {
@@ -417,6 +425,7 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
     c.rows = rows;
     c.nsplit = p.nsplit;
     c.D = D;
+    c.dependent = 1;  // follows the attention kernel it combines
     e = launch_combine(c, st);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
@@ -427,10 +436,8 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
 
 namespace hattn {
 
-bool dependent_launch() { return g_dependent_launch; }
-
-int add_dependent_attr(cudaLaunchAttribute* attrs, int n) {
-  if (!g_dependent_launch) return n;
+int add_dependent_attr(cudaLaunchAttribute* attrs, int n, bool dependent) {
+  if (!dependent) return n;
   attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[n].val.programmaticStreamSerializationAllowed = 1;
   return n + 1;
@@ -595,13 +602,6 @@ int hattn_hca_compress(const void* kv_raw, const void* gate, const float* gamma_
                          j_begin, j_end, kv_h, nullptr, N_cap, stream);
 }
 
-size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
-                                          int score_out_given) {
-  (void)k;
-  if (B < 1 || T < 1 || N_cap < 1 || score_out_given) return 0;
-  return (size_t)B * T * N_cap * sizeof(float);
-}
-
 }  // extern "C"
 
 namespace {
@@ -611,7 +611,8 @@ namespace {
 int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
                         int B, int T, int HI, int dI, int64_t N_cap, int m, float* scores,
                         hattn_stream_t stream, int n_sms = 0, int64_t fresh_from = -1,
-                        const float* k_scale = nullptr) {
+                        const float* k_scale = nullptr, int flags = 0) {
+  if (int rcf = check_flags(flags)) return rcf;
   REQUIRE_PTR(iq);
   REQUIRE_PTR(w);
   REQUIRE_PTR(ik_c);
@@ -682,6 +683,7 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   a.groups_per_seq = (T + ip.G - 1) / ip.G;
   a.nblk = static_cast<int>((N_cap + 127) / 128);
   a.fresh_from = fresh_from;
+  a.dependent = (flags & HATTN_LAUNCH_DEPENDENT) ? 1 : 0;
   a.N_cap = N_cap;
   a.total_slots = (int64_t)B * a.groups_per_seq * a.nblk;
   // persistent: one CTA per SM it may use (n_sms of them when given, so
@@ -694,48 +696,68 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   return ok();
 }
 
-int topk_impl(const float* scores, const int32_t* pos, int rows, int64_t N_cap, int k, int m,
-              int32_t* idx_out, hattn_stream_t stream) {
+int topk_impl(const float* scores, const int32_t* pos, int64_t rows, int64_t N_cap, int k, int m,
+              int32_t* idx_out, void* workspace, size_t ws_bytes, int flags,
+              hattn_stream_t stream) {
+  if (int rcf = check_flags(flags)) return rcf;
   REQUIRE_PTR(scores);
   REQUIRE_PTR(pos);
   REQUIRE_PTR(idx_out);
-  REQUIRE(rows >= 1 && rows < 65536 * 32768ll && N_cap >= 1, "rows and N_cap must be >= 1");
+  REQUIRE(rows >= 1 && N_cap >= 1, "rows and N_cap must be >= 1");
+  REQUIRE(N_cap < (1ll << 31), "N_cap=%lld must be < 2^31", (long long)N_cap);
+  REQUIRE(rows <= 65535ll * 65535ll, "rows=%lld: at most 65535^2 query rows", (long long)rows);
   REQUIRE(k >= 1 && k <= 2048, "k=%d must be in [1, 2048]", k);
   REQUIRE(m >= 1, "m must be >= 1");
-  int sms = 0;
-  if (!device_info(nullptr, nullptr, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  // the plan (and so the scratch it needs) is checked before any device call
   TopkPlan tp;
-  if (!plan_topk(rows, N_cap, sms, &tp))
+  if (!plan_topk(rows, N_cap, k, num_sms_or_default(), &tp))
     return fail(HATTN_ERR_UNSUPPORTED, "top-k over N_cap=%lld entries is not supported",
                 (long long)N_cap);
-  TopkArgs t;
+  TopkArgs t = {};
+  if (tp.ws_bytes > 0) {
+    REQUIRE_PTR(workspace);
+    REQUIRE(ws_bytes >= tp.ws_bytes, "top-k workspace of %zu bytes, need %zu", ws_bytes,
+            tp.ws_bytes);
+    topk_scratch_carve(tp, rows, workspace, &t);
+  }
   t.scores = scores;
   t.pos = pos;
   t.idx = idx_out;
   t.rows = rows;
   t.k = k;
   t.m = m;
-  t.cluster = tp.cluster;
   t.N_cap = N_cap;
-  t.slice = tp.slice;
-  cudaError_t e = launch_topk(t, tp, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_topk(t, tp, (flags & HATTN_LAUNCH_DEPENDENT) != 0,
+                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
   return ok();
 }
 
-// Score scratch of hattn_indexer_topk_noalloc: a fixed device array that
-// every GPU loading this library holds until the process exits, so that
-// call needs no allocation.  4,194,304 fp32 scores (16 MiB), enough for
-// B * T * N_cap = 8 x 1 x 262,144 (a 1M-token decode batch of 8) twice over.
-constexpr int64_t kNoallocScores = int64_t(1) << 22;
-static __device__ __align__(256) float g_noalloc_scores[kNoallocScores];
+// Scratch bytes of the selection (0 when it runs in shared memory alone).
+size_t topk_ws_bytes(int64_t rows, int64_t N_cap, int k) {
+  TopkPlan tp;
+  if (rows < 1 || N_cap < 1 || k < 1 || !plan_topk(rows, N_cap, k, num_sms_or_default(), &tp))
+    return 0;
+  return tp.ws_bytes;
+}
 
-// Device address of g_noalloc_scores for each device, looked up once with
+// Scratch of hattn_indexer_topk_noalloc: a fixed device array that every GPU
+// loading this library holds until the process exits, so that call needs no
+// allocation.  It holds the fp32 scores, then the selection's scratch:
+// 4,194,304 scores (16 MiB, enough for B * T * N_cap = 8 x 1 x 262,144, a
+// 1M-token decode batch of 8, twice over) and at most as many candidate
+// indices plus histograms and counters (18 MiB).
+constexpr int64_t kNoallocScores = int64_t(1) << 22;
+constexpr size_t kNoallocTopkBytes = (size_t(1) << 22) * 4 + (size_t(2) << 20);
+constexpr size_t kNoallocBytes = kNoallocScores * 4 + kNoallocTopkBytes;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocBytes];
+
+// Device address of g_noalloc_scratch for each device, looked up once with
 // that device current (in host code the array's name is only a host-side
 // stand-in, not a device address).
-float* g_noalloc_ptr[kMaxDevices] = {};
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};
 
-int noalloc_scores(float** out) {
+int noalloc_scratch(uint8_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -743,13 +765,15 @@ int noalloc_scores(float** out) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scores);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(score scratch)");
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
   }
   *out = g_noalloc_ptr[dev];
   return HATTN_OK;
 }
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 
 }  // namespace
 
@@ -763,25 +787,39 @@ int hattn_indexer_scores(const void* iq, const float* w, const void* ik_c, const
 
 int hattn_indexer_scores_ex(const void* iq, const float* w, const void* ik_c,
                             const int32_t* pos, int B, int T, int HI, int dI, int64_t N_cap,
-                            int m, int n_sms, int64_t fresh_from, float* score_out,
+                            int m, int n_sms, int64_t fresh_from, float* score_out, int flags,
                             hattn_stream_t stream) {
   return indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms,
-                             fresh_from < 0 ? -1 : fresh_from);
+                             fresh_from < 0 ? -1 : fresh_from, nullptr, flags);
 }
 
 int hattn_indexer_scores_fp8(const void* iq, const float* w, const void* ik8,
                              const float* ik_scale, const int32_t* pos, int B, int T, int HI,
                              int dI, int64_t N_cap, int m, int n_sms, int64_t fresh_from,
-                             float* score_out, hattn_stream_t stream) {
+                             float* score_out, int flags, hattn_stream_t stream) {
   REQUIRE_PTR(ik_scale);
   return indexer_scores_impl(iq, w, ik8, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms,
-                             fresh_from < 0 ? -1 : fresh_from, ik_scale);
+                             fresh_from < 0 ? -1 : fresh_from, ik_scale, flags);
+}
+
+size_t hattn_topk_workspace_bytes(int B, int T, int64_t N_cap, int k) {
+  if (B < 1 || T < 1) return 0;
+  return topk_ws_bytes((int64_t)B * T, N_cap, k);
 }
 
 int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T, int64_t N_cap, int k,
-                      int m, int32_t* idx_out, hattn_stream_t stream) {
+                      int m, int32_t* idx_out, void* workspace, size_t ws_bytes, int flags,
+                      hattn_stream_t stream) {
   REQUIRE(B >= 1 && T >= 1, "B and T must be >= 1");
-  return topk_impl(scores, pos, B * T, N_cap, k, m, idx_out, stream);
+  return topk_impl(scores, pos, (int64_t)B * T, N_cap, k, m, idx_out, workspace, ws_bytes, flags,
+                   stream);
+}
+
+size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
+                                          int score_out_given) {
+  if (B < 1 || T < 1 || N_cap < 1) return 0;
+  const size_t scores = score_out_given ? 0 : round256((size_t)B * T * N_cap * sizeof(float));
+  return scores + topk_ws_bytes((int64_t)B * T, N_cap, k);
 }
 
 int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
@@ -795,17 +833,23 @@ int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const i
   REQUIRE(k >= 1 && k <= 2048, "k=%d must be in [1, 2048]", k);
   REQUIRE_PTR(idx_out);
   REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
-  float* scores = score_out;
-  if (!scores) {
-    REQUIRE(B >= 1 && T >= 1 && N_cap >= 1, "B, T and N_cap must be >= 1");
-    const size_t need = hattn_indexer_topk_workspace_bytes(B, T, N_cap, k, 0);
+  REQUIRE(B >= 1 && T >= 1 && N_cap >= 1, "B, T and N_cap must be >= 1");
+  const size_t need = hattn_indexer_topk_workspace_bytes(B, T, N_cap, k, score_out != nullptr);
+  if (need > 0) {
     REQUIRE_PTR(workspace);
     REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  }
+  float* scores = score_out;
+  uint8_t* rest = static_cast<uint8_t*>(workspace);
+  if (!scores) {
     scores = static_cast<float*>(workspace);
+    rest += round256((size_t)B * T * N_cap * sizeof(float));
   }
   int rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream);
   if (rc) return rc;
-  return topk_impl(scores, pos, B * T, N_cap, k, m, idx_out, stream);
+  const size_t left = need > (size_t)(rest - static_cast<uint8_t*>(workspace))
+                          ? need - (size_t)(rest - static_cast<uint8_t*>(workspace)) : 0;
+  return topk_impl(scores, pos, (int64_t)B * T, N_cap, k, m, idx_out, rest, left, 0, stream);
 }
 
 int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,
@@ -822,14 +866,21 @@ int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,
   REQUIRE((int64_t)B * T * N_cap <= kNoallocScores,
           "B * T * N_cap = %lld scores exceed the fixed scratch of %lld (use hattn_indexer_topk "
           "with a workspace)", (long long)((int64_t)B * T * N_cap), (long long)kNoallocScores);
-  float* scores = nullptr;
-  int rc = noalloc_scores(&scores);
+  const size_t sel = topk_ws_bytes((int64_t)B * T, N_cap, k);
+  REQUIRE(sel <= kNoallocTopkBytes,
+          "the selection needs %zu bytes of scratch, the fixed scratch holds %zu (use "
+          "hattn_indexer_topk with a workspace)", sel, kNoallocTopkBytes);
+  uint8_t* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
   if (rc) return rc;
-  // every score the selection reads (entries j < visible count) is written by
-  // the score kernel first, so nothing in the shared scratch needs clearing
+  float* scores = reinterpret_cast<float*>(scratch);
+  // every score the selection reads (entries j < visible count) is written
+  // by the score kernel first, and the selection clears its own counters, so
+  // nothing in the shared scratch needs clearing between calls
   rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream);
   if (rc) return rc;
-  return topk_impl(scores, pos, B * T, N_cap, k, m, idx_out, stream);
+  return topk_impl(scores, pos, (int64_t)B * T, N_cap, k, m, idx_out,
+                   scratch + kNoallocScores * 4, kNoallocTopkBytes, 0, stream);
 }
 
 size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys,
@@ -878,10 +929,11 @@ int hattn_hybrid_attn(const void* q, const float* gamma_q, int q_prepped, const 
                       int m, const void* kv_w, int W, const int32_t* pos, int B, int T, int H,
                       int D, int r, float rope_base, float eps, float scale, int segments,
                       int n_sms, void* o, float* lse, void* workspace, size_t ws_bytes,
-                      hattn_stream_t stream) {
+                      int flags, hattn_stream_t stream) {
   const FusedSources fs{kv_h, N_h, kv_w, segments, n_sms};
   return attn_common(kFused, q, gamma_q, q_prepped, kv_c, nullptr, idx, pos, B, T, H, D, N_c, k,
-                     m, W, r, rope_base, eps, scale, o, lse, workspace, ws_bytes, stream, &fs);
+                     m, W, r, rope_base, eps, scale, o, lse, workspace, ws_bytes, stream, &fs,
+                     flags);
 }
 
 size_t hattn_hybrid_attn_workspace_bytes(int B, int T, int H, int D, int k, int64_t N_h, int W,
@@ -969,7 +1021,9 @@ namespace {
 
 int merge_impl(const void* const* o_list, const float* const* lse_list, const int* nsplit, int nb,
                const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
-               float rope_base, void* out, float* lse_out, hattn_stream_t stream) {
+               float rope_base, void* out, float* lse_out, hattn_stream_t stream,
+               int flags = 0) {
+  if (int rcf = check_flags(flags)) return rcf;
   REQUIRE(o_list && lse_list, "o_list and lse_list must not be NULL");
   REQUIRE(nb >= 1 && nb <= 4, "nb=%d must be in [1, 4]", nb);
   MergeArgs a;
@@ -986,6 +1040,8 @@ int merge_impl(const void* const* o_list, const float* const* lse_list, const in
     a.nsplit[i] = ns;
   }
   REQUIRE(parts <= kMaxMergeParts, "%d partials per row, at most %d", parts, kMaxMergeParts);
+  a.cum[0] = 0;
+  for (int i = 0; i < 4; ++i) a.cum[i + 1] = a.cum[i] + (i < nb ? a.nsplit[i] : 0);
   REQUIRE_PTR(pos);
   REQUIRE_PTR(out);
   REQUIRE_F32(sink);
@@ -1005,6 +1061,7 @@ int merge_impl(const void* const* o_list, const float* const* lse_list, const in
   a.H = H;
   a.D = D;
   a.r = r;
+  a.dependent = (flags & HATTN_LAUNCH_DEPENDENT) ? 1 : 0;
   make_rope_coef(rope_base, r, &a.rope);
   cudaError_t e = launch_merge(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
@@ -1025,10 +1082,10 @@ int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int
 int hattn_lse_merge_splits(const void* const* part_o_list, const float* const* part_lse_list,
                            const int* nsplit, int nb, const float* sink, const int32_t* pos, int B,
                            int T, int H, int D, int r, float rope_base, void* out, float* lse_out,
-                           hattn_stream_t stream) {
+                           int flags, hattn_stream_t stream) {
   if (!nsplit) return fail(HATTN_ERR_INVALID_ARG, "nsplit must not be NULL");
   return merge_impl(part_o_list, part_lse_list, nsplit, nb, sink, pos, B, T, H, D, r, rope_base,
-                    out, lse_out, stream);
+                    out, lse_out, stream, flags);
 }
 
 const char* hattn_status_string(int code) {
@@ -1071,12 +1128,6 @@ int hattn_selftest_wait_timeout(uint64_t timeout_ns, hattn_stream_t stream) {
   return ok();
 }
 
-int hattn_set_dependent_launch(int enable) {
-  const int prev = g_dependent_launch ? 1 : 0;
-  g_dependent_launch = enable != 0;
-  return prev;
-}
-
-const char* hattn_version(void) { return "hattn 0.1 sm_103a"; }
+const char* hattn_version(void) { return "hattn 0.2 sm_103a"; }
 
 }  // extern "C"

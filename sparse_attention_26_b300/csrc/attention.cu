@@ -955,7 +955,7 @@ cudaError_t launch_kind(const CUtensorMap& tm_kv, const CUtensorMap& tm_kv2,
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   cfg.attrs = at;
-  cfg.numAttrs = add_dependent_attr(at, 0);
+  cfg.numAttrs = add_dependent_attr(at, 0, a.dependent != 0);
   e = cudaLaunchKernelEx(&cfg, attn_kernel<KIND>, tm_kv, tm_kv2, tm_q, a, p.nslot);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -519,7 +519,7 @@ cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   cfg.attrs = at;
-  cfg.numAttrs = add_dependent_attr(at, 0);
+  cfg.numAttrs = add_dependent_attr(at, 0, a.dependent != 0);
   e = cudaLaunchKernelEx(&cfg, kernel, tm_ik, tm_iq, tm_ks, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

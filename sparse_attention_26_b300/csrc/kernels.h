@@ -11,13 +11,12 @@
 
 namespace hattn {
 
-// Whether the calling host thread launches the dependent-capable kernels
-// (indexer scores, top-k, attention, merges) as programmatic dependents of
-// the previous kernel in their stream (hattn_set_dependent_launch).
-bool dependent_launch();
 // Appends the programmatic-serialization attribute to attrs[n] when
-// dependent_launch() holds; returns the new attribute count.
-int add_dependent_attr(cudaLaunchAttribute* attrs, int n);
+// `dependent` (the call's HATTN_LAUNCH_DEPENDENT flag) is set: the kernel
+// may then start while the previous kernel in its stream still runs, and
+// waits (griddepcontrol.wait) before reading what that kernel writes.
+// Returns the new attribute count.
+int add_dependent_attr(cudaLaunchAttribute* attrs, int n, bool dependent);
 
 // ------------------------------------------------------------ compressor
 struct CompressArgs {
@@ -54,6 +53,7 @@ struct IndexerArgs {
   int64_t fresh_from;    // entries >= this may be written by the previous kernel (-1: any)
   int64_t N_cap;
   int64_t total_slots;   // B * groups_per_seq * nblk
+  int dependent;         // launched as a programmatic dependent
 };
 struct IndexerPlan {
   int G, NQ, KC, stages, nacc, tmem_cols;
@@ -103,16 +103,29 @@ struct TopkArgs {
   const float* scores;   // [rows][N_cap]
   const int32_t* pos;    // [rows]
   int32_t* idx;          // [rows][k]
-  int rows, k, m, cluster;
+  // slice path scratch (caller-owned; nothing needs clearing)
+  uint16_t* hist;        // [rows][S][2048] per-slice histograms of the top key digit
+  int32_t* ctr;          // [rows][4]: selected so far, candidates, tickets
+  int32_t* cand;         // [rows][N_cap] candidate entry indices
+  int64_t rows;
+  int k, m;
+  int S;                 // CTAs per row (slice path)
+  int vec4;              // rows are 16-byte aligned and slices start at multiples of 4
   int64_t N_cap;
-  int slice;             // entries per CTA of a cluster
+  int64_t slice;         // entries per CTA (slice path)
 };
 struct TopkPlan {
-  int cluster, slice, threads;
-  size_t smem_bytes;
+  bool slice_path;
+  int S, threads;
+  int64_t slice;
+  size_t smem_bytes, ws_bytes;
 };
-bool plan_topk(int rows, int64_t N_cap, int num_sms, TopkPlan* p);
-cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, cudaStream_t stream);
+bool plan_topk(int64_t rows, int64_t N_cap, int k, int num_sms, TopkPlan* p);
+size_t topk_scratch_bytes(const TopkPlan& p, int64_t rows, int64_t N_cap);
+// Points a->hist, a->ctr and a->cand into a scratch of topk_scratch_bytes().
+void topk_scratch_carve(const TopkPlan& p, int64_t rows, void* ws, TopkArgs* a);
+cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, bool dependent,
+                        cudaStream_t stream);
 
 // ------------------------------------------------------------ attention
 // kFused: one query's CSA (top-k), HCA and SWA keys as one key list, so a
@@ -155,6 +168,7 @@ struct AttnArgs {
   int nsplit;                   // key splits
   int keys_per_split;           // multiple of 64
   int nds;                      // D splits (1 or 2)
+  int dependent;                // launched as a programmatic dependent
 };
 struct AttnPlan {
   int G, n_rb, nsplit, keys_per_split, nds, nslot;
@@ -192,6 +206,7 @@ struct CombineArgs {
   float* lse;
   int64_t rows;   // B*T*H
   int nsplit, D;
+  int dependent;  // launched as a programmatic dependent
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
@@ -203,12 +218,14 @@ struct MergeArgs {
   const float* o[4];            // fp32 partials of each branch
   const float* lse[4];
   int nsplit[4];
+  int cum[5];                   // cum[i] = partials of branches before i (cum[nb] = total)
   int nb;
   const float* sink;    // [H] or null
   const int32_t* pos;   // [B][T]
   __nv_bfloat16* out;
   float* lse_out;       // or null
   int B, T, H, D, r;
+  int dependent;        // launched as a programmatic dependent
   RopeCoef rope;
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);

@@ -147,6 +147,78 @@ __global__ void __launch_bounds__(kMergeBlock) merge_kernel(const __grid_constan
   if (t == 0 && a.lse_out) a.lse_out[row] = lz_s[half];
 }
 
+// The same merge when the row has at most kFastParts partials and a row's
+// float4 columns divide the block: every thread issues the loads of all the
+// row's partials for its four columns at once (one round of memory latency),
+// then weighs them itself from the row's log-sum-exps (read by every thread
+// of the row from the same addresses) -- no shared memory, no block barrier.
+constexpr int kFastParts = 16;
+__global__ void __launch_bounds__(kMergeBlock)
+    merge_fast_kernel(const __grid_constant__ MergeArgs a, const int tpr) {
+  pdl_trigger();
+  pdl_wait();  // the branch outputs / partials are complete
+  const int rpb = kMergeBlock / tpr;
+  const int t = threadIdx.x % tpr;
+  const int64_t rows = static_cast<int64_t>(a.B) * a.T * a.H;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * rpb + threadIdx.x / tpr;
+  if (row >= rows) return;
+  const int total = a.cum[a.nb];
+  float4 v[kFastParts];
+  float l[kFastParts];
+#pragma unroll
+  for (int k = 0; k < kFastParts; ++k) {
+    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    l[k] = -INFINITY;
+    if (k < total) {
+      const int i = (k >= a.cum[1]) + (k >= a.cum[2]) + (k >= a.cum[3]);
+      const int ns = a.nsplit[i];
+      const int64_t part = row * ns + (k - a.cum[i]);
+      v[k] = __ldcg(reinterpret_cast<const float4*>(a.o[i] + part * a.D) + t);
+      l[k] = __ldcg(a.lse[i] + part);
+    }
+  }
+  const int h = static_cast<int>(row % a.H);
+  const bool has_sink = a.sink != nullptr;
+  const float sink = has_sink ? __ldg(a.sink + h) : -INFINITY;
+  float mx = sink;
+#pragma unroll
+  for (int k = 0; k < kFastParts; ++k) mx = fmaxf(mx, l[k]);
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+  float lz = -INFINITY;
+  if (mx != -INFINITY) {
+    float z = has_sink ? __expf(sink - mx) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kFastParts; ++k) {
+      const float e = __expf(l[k] - mx);  // an empty split: exp(-inf) = 0
+      z += e;
+      y[0] = fmaf(e, v[k].x, y[0]);
+      y[1] = fmaf(e, v[k].y, y[1]);
+      y[2] = fmaf(e, v[k].z, y[2]);
+      y[3] = fmaf(e, v[k].w, y[3]);
+    }
+    const float inv = 1.f / z;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] *= inv;
+    lz = mx + __logf(z);
+  }
+  const int64_t pos = a.pos[row / a.H];
+  const int d0 = a.D - a.r;
+#pragma unroll
+  for (int e = 0; e < 4; e += 2) {
+    const int d = 4 * t + e;
+    if (d >= d0) {
+      float sn, cs;
+      rope_cs(a.rope.c, (d - d0) >> 1, -pos, &sn, &cs);
+      const float x0 = y[e], x1 = y[e + 1];
+      y[e] = x0 * cs - x1 * sn;
+      y[e + 1] = x0 * sn + x1 * cs;
+    }
+  }
+  *reinterpret_cast<uint2*>(a.out + row * a.D + 4 * t) =
+      make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+  if (t == 0 && a.lse_out) a.lse_out[row] = lz;
+}
+
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
 // gives up after `timeout_ns` and records the timeout in the status word.
 __global__ void wait_selftest_kernel(uint64_t timeout_ns, int* status) {
@@ -170,7 +242,7 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   cfg.attrs = at;
-  cfg.numAttrs = add_dependent_attr(at, 0);
+  cfg.numAttrs = add_dependent_attr(at, 0, a.dependent != 0);
   cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -179,16 +251,22 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.B) * a.T * a.H;
   if (rows <= 0) return cudaSuccess;
-  const int per = kMergeBlock / kRowThreads;
+  // fast path: few partials per row, and a row's float4 columns divide the block
+  const int tpr = a.D / 4;
+  const bool fast = a.cum[a.nb] <= kFastParts && a.D % 4 == 0 && tpr <= kMergeBlock &&
+                    kMergeBlock % tpr == 0;
+  const int per = fast ? kMergeBlock / tpr : kMergeBlock / kRowThreads;
   const int64_t blocks = (rows + per - 1) / per;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
   cfg.blockDim = dim3(kMergeBlock, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   cfg.attrs = at;
-  cfg.numAttrs = add_dependent_attr(at, 0);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel, a);
+  cfg.numAttrs = add_dependent_attr(at, 0, a.dependent != 0);
+  cudaError_t e = fast ? cudaLaunchKernelEx(&cfg, merge_fast_kernel, a, tpr)
+                       : cudaLaunchKernelEx(&cfg, merge_kernel, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

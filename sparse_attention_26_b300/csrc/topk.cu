@@ -5,61 +5,61 @@
 // query.  Selection rule: the min(k, n) largest scores among the n visible
 // entries, ties to the smaller entry index; the output order is unspecified.
 //
-// One thread-block cluster of C CTAs handles one query row: CTA `rank` holds
-// entries [rank*slice, (rank+1)*slice) as order-preserving uint32 keys in
-// shared memory (one read of the fp32 scores).  Three radix passes (11, 11,
-// 10 bits, most significant first) find the k-th largest key: every CTA
-// builds a shared-memory histogram of the digit among the keys that still
-// match the prefix and adds its nonzero bins into every CTA's copy of the
-// cluster histogram with remote shared-memory atomics (double-buffered, so
-// one cluster barrier per pass); every CTA then finds the digit with a
-// block-wide suffix scan.  The final pass writes every key above the
-// threshold, then the threshold ties in global index order until k are
-// written.  No global atomics, no inter-kernel passes; the result is
-// deterministic.
-#include <cooperative_groups.h>
-
-#include <mutex>
-
+// Scores are ranked as order-preserving uint32 keys, most significant digit
+// first (11, 11 and 10 bits).  Two paths:
+//
+//   row path (rows that fit one CTA's shared memory, or many rows): one CTA
+//   per row holds the row's keys in shared memory, builds the top digit's
+//   histogram while loading, lists the keys of the threshold bin, and ranks
+//   only that list in the later passes.
+//
+//   slice path (few long rows, e.g. decode at 1M context: 8 rows of 262,144):
+//   S CTAs per row, two kernels and no inter-CTA waiting.
+//     topk_hist_kernel: each CTA histograms the top digit of its slice into
+//       its own 2,048 16-bit bins of the scratch (no atomics, nothing to
+//       clear), and CTA 0 of the row clears the row's counters.
+//     topk_pick_kernel: each CTA sums the row's S histograms, finds the bin
+//       of the k-th largest key, and sweeps its slice again: keys above that
+//       bin are selected at once (appended to the output), keys in it are
+//       appended to the row's candidate list.  The last CTA of the row to
+//       finish (a ticket counter) ranks the candidates -- the remaining two
+//       digits, then, only if more ties sit at the threshold than places
+//       are left, the tie indices from the smallest -- and writes the rest.
+//   The scratch is caller-owned (hattn_topk_workspace_bytes).
 #include "common.cuh"
 #include "kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace hattn {
 
 namespace {
 
 constexpr int kBins = 2048;
-// Keys in the first pass's threshold bin, whole cluster, up to which the
-// compact path is taken; keys above that bin number fewer than k <= 2048.
-// Slice positions fit 16 bits (a slice holds at most 49,152 keys).
+// Row path: keys of the first pass's threshold bin up to which the compact
+// path is taken; keys above that bin number fewer than k <= 2048.  Slice
+// positions fit 16 bits (a row holds at most 49,152 keys).
 constexpr int kMaxCand = 2048;
 constexpr int kMaxAbove = 2048;
+constexpr int kRowMaxKeys = 49152;
+constexpr int kPickThreads = 512;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);  // -0 and +0 compare equal
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-struct TopkShared {
-  uint32_t hist[kBins];
-  uint32_t ghist[2][kBins];
+__device__ __forceinline__ int64_t visible_count(int32_t t, int m, int64_t cap) {
+  int64_t n = t < 0 ? 0 : (static_cast<int64_t>(t) + 1) / m;
+  return n < cap ? n : cap;
+}
+
+struct ScanShared {
   uint32_t warp_tot[32];
-  int counts[2];       // keys above the threshold, keys equal to it (this CTA)
-  int offs[2];         // the same counts summed over the lower-ranked CTAs
-  int ctr, ctr_eq;
-  int eq_total;        // keys equal to the threshold in the whole cluster
-  int n_cand, n_above;
-  uint16_t cand[kMaxCand];        // slice positions of the keys in the bin of the k-th largest
-  uint16_t above_idx[kMaxAbove];  // slice positions of the keys above that bin
   uint32_t digit;
   uint32_t above;
 };
 
-// Inclusive scan over the threads of the block, in thread order; uses
-// sh->warp_tot.  Returns this thread's exclusive prefix.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, TopkShared* sh, int tid,
+// Exclusive prefix of v over the threads of the block, in thread order.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, ScanShared* sh, int tid,
                                                          int nthr) {
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t inc = v;
@@ -87,19 +87,24 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, TopkShared*
   return r;
 }
 
-// The bin holding the need-th largest key: bins are visited from the top;
-// sh->digit = that bin, sh->above = the keys in the bins above it.
-__device__ __forceinline__ void find_digit(const uint32_t* gh, int nb, uint32_t need,
-                                           TopkShared* sh, int tid, int nthr) {
-  const int bpt = nb / nthr;            // bins per thread (nb >= nthr)
-  const int hi = nb - bpt * tid;        // this thread's bins: [hi - bpt, hi)
+// The bin holding the need-th largest key (1 <= need <= total): bins are
+// visited from the top; sh->digit = that bin, sh->above = keys in the bins
+// above it.  nb >= nthr, both powers of two.
+__device__ __forceinline__ void find_digit_desc(const uint32_t* h, int nb, uint32_t need,
+                                                ScanShared* sh, int tid, int nthr) {
+  if (tid == 0) {  // ordered before the finder's write by the scan's barriers
+    sh->digit = 0;
+    sh->above = 0;
+  }
+  const int bpt = nb / nthr;
+  const int hi = nb - bpt * tid;  // this thread's bins: [hi - bpt, hi)
   uint32_t tot = 0;
-  for (int i = 0; i < bpt; ++i) tot += gh[hi - 1 - i];
+  for (int i = 0; i < bpt; ++i) tot += h[hi - 1 - i];
   const uint32_t before = block_exclusive_scan(tot, sh, tid, nthr);
   if (before < need && before + tot >= need) {
     uint32_t run = before;
     for (int i = 0; i < bpt; ++i) {
-      const uint32_t c = gh[hi - 1 - i];
+      const uint32_t c = h[hi - 1 - i];
       if (run + c >= need) {
         sh->digit = static_cast<uint32_t>(hi - 1 - i);
         sh->above = run;
@@ -111,41 +116,78 @@ __device__ __forceinline__ void find_digit(const uint32_t* gh, int nb, uint32_t 
   __syncthreads();
 }
 
-__global__ void topk_kernel(const TopkArgs a) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  TopkShared* sh = reinterpret_cast<TopkShared*>(smem_raw);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkShared));
+// The bin holding the need-th smallest value: bins visited from the bottom;
+// sh->digit = that bin, sh->above = values in the bins below it.
+__device__ __forceinline__ void find_digit_asc(const uint32_t* h, int nb, uint32_t need,
+                                               ScanShared* sh, int tid, int nthr) {
+  if (tid == 0) {
+    sh->digit = 0;
+    sh->above = 0;
+  }
+  const int bpt = nb / nthr;
+  const int lo = bpt * tid;
+  uint32_t tot = 0;
+  for (int i = 0; i < bpt; ++i) tot += h[lo + i];
+  const uint32_t before = block_exclusive_scan(tot, sh, tid, nthr);
+  if (before < need && before + tot >= need) {
+    uint32_t run = before;
+    for (int i = 0; i < bpt; ++i) {
+      const uint32_t c = h[lo + i];
+      if (run + c >= need) {
+        sh->digit = static_cast<uint32_t>(lo + i);
+        sh->above = run;
+        break;
+      }
+      run += c;
+    }
+  }
+  __syncthreads();
+}
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = a.cluster;
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int row = blockIdx.y;
-  const int tid = threadIdx.x;
-  const int nthr = blockDim.x;
+// Appends `take` (per thread) to a global counter with one atomic per warp;
+// returns this thread's slot (valid where take).
+__device__ __forceinline__ int warp_append(int* ctr, bool take) {
+  const unsigned mask = __ballot_sync(0xffffffffu, take);
+  if (!mask) return -1;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(mask) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(ctr, __popc(mask));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(mask & ((1u << lane) - 1u));
+}
+
+// ============================================================ row path
+struct RowShared {
+  ScanShared scan;
+  uint32_t hist[kBins];
+  int counts[2];
+  int ctr, ctr_eq;
+  int n_cand, n_above;
+  uint16_t cand[kMaxCand];
+  uint16_t above_idx[kMaxAbove];
+};
+
+__global__ void __launch_bounds__(1024) topk_row_kernel(const TopkArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  RowShared* sh = reinterpret_cast<RowShared*>(smem_raw);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(RowShared));
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int64_t row = static_cast<int64_t>(blockIdx.y) + static_cast<int64_t>(gridDim.y) * blockIdx.z;
 
   pdl_trigger();
   pdl_wait();  // the scores (and a dependent launch's predecessor) are complete
-  const int32_t t = a.pos[row];
-  int64_t n = t < 0 ? 0 : (static_cast<int64_t>(t) + 1) / a.m;
-  if (n > a.N_cap) n = a.N_cap;
-  const int64_t start = static_cast<int64_t>(rank) * a.slice;
-  int len = 0;
-  if (n > start) len = static_cast<int>((n - start) < a.slice ? (n - start) : a.slice);
-  int32_t* out = a.idx + static_cast<int64_t>(row) * a.k;
+  if (row >= a.rows) return;
+  const int len = static_cast<int>(visible_count(a.pos[row], a.m, a.N_cap));
+  int32_t* out = a.idx + row * a.k;
 
-  if (n <= a.k) {  // every visible entry is selected (same branch for the whole cluster)
-    for (int e = tid; e < len; e += nthr) out[start + e] = static_cast<int32_t>(start + e);
-    if (rank == 0)
-      for (int64_t p = n + tid; p < a.k; p += nthr) out[p] = -1;
+  if (len <= a.k) {  // every visible entry is selected
+    for (int e = tid; e < a.k; e += nthr) out[e] = e < len ? e : -1;
     return;
   }
 
-  const float* src = a.scores + static_cast<int64_t>(row) * a.N_cap + start;
-  for (int i = tid; i < kBins; i += nthr) {
-    sh->hist[i] = 0;
-    sh->ghist[0][i] = 0;
-    sh->ghist[1][i] = 0;
-  }
+  const float* src = a.scores + row * a.N_cap;
+  for (int i = tid; i < kBins; i += nthr) sh->hist[i] = 0;
   __syncthreads();
   // the keys, and the first pass's histogram of their top 11 bits, in one sweep
   for (int e = tid; e < len; e += nthr) {
@@ -153,172 +195,101 @@ __global__ void topk_kernel(const TopkArgs a) {
     keys[e] = key;
     atomicAdd(&sh->hist[key >> 21], 1u);
   }
-  cluster.sync();  // every copy of the cluster histogram is zero before any add
+  __syncthreads();
 
   uint32_t prefix = 0;
   uint32_t need = static_cast<uint32_t>(a.k);
-  // One radix pass over the histogram in sh->hist: add this CTA's nonzero
-  // bins into every CTA's copy of the cluster histogram (buffer pass & 1),
-  // reset the local bins and the other buffer (last scanned by this CTA in
-  // the previous pass; the next adds into it come after the barrier), then
-  // find the digit of the need-th largest key.
-  auto radix_pass = [&](int pass, int width) {
+  // one radix pass: the digit of the need-th largest key among those left;
+  // returns the keys in that digit's bin, and clears the histogram
+  auto radix_pass = [&](int width) -> uint32_t {
     const int nb = 1 << width;
-    const int buf = pass & 1;
+    find_digit_desc(sh->hist, nb, need, &sh->scan, tid, nthr);
+    const uint32_t in_bin = sh->hist[sh->scan.digit];
+    prefix = (prefix << width) | sh->scan.digit;
+    need -= sh->scan.above;
+    __syncthreads();  // every thread has read the bin
+    for (int i = tid; i < kBins; i += nthr) sh->hist[i] = 0;
     __syncthreads();
-    for (int bin = tid; bin < nb; bin += nthr) {
-      const uint32_t v = sh->hist[bin];
-      if (v) {
-        for (int q = 0; q < C; ++q) atomicAdd(cluster.map_shared_rank(&sh->ghist[buf][bin], q), v);
-        sh->hist[bin] = 0;
-      }
-    }
-    if (pass < 2)
-      for (int i = tid; i < kBins; i += nthr) sh->ghist[buf ^ 1][i] = 0;
-    cluster.sync();
-    find_digit(sh->ghist[buf], nb, need, sh, tid, nthr);
-    prefix = (prefix << width) | sh->digit;
-    need -= sh->above;
+    return in_bin;
   };
-  radix_pass(0, 11);  // its histogram was built while loading
   // The keys left to rank are those in the bin of the k-th largest (about
-  // 0.5% of normal scores).  When the whole cluster holds few enough, one
-  // sweep lists them (and the keys above the bin, which are selected), and
-  // the remaining passes, the counts and the writes visit only the lists.
-  // The decision uses the cluster histogram, so every CTA takes the same path.
-  const bool compact = sh->ghist[0][prefix] <= static_cast<uint32_t>(kMaxCand);
+  // 0.5% of normal scores).  When few enough, one sweep lists them (and the
+  // keys above the bin, which are selected), and the remaining passes, the
+  // counts and the writes visit only the lists.
+  const bool compact = radix_pass(11) <= static_cast<uint32_t>(kMaxCand);
+  const uint32_t d0 = prefix;
+  if (tid == 0) {
+    sh->n_cand = 0;
+    sh->n_above = 0;
+  }
+  __syncthreads();
   int n_cand = 0, n_above = 0;
   if (compact) {
-    if (tid == 0) {
-      sh->n_cand = 0;
-      sh->n_above = 0;
-    }
-    __syncthreads();
-    // few keys qualify, so each takes its place with its own atomic
     for (int e = tid; e < len; e += nthr) {
       const uint32_t key = keys[e];
       const uint32_t d = key >> 21;
-      if (d == prefix) {
+      if (d == d0) {
         sh->cand[atomicAdd(&sh->n_cand, 1)] = static_cast<uint16_t>(e);
         atomicAdd(&sh->hist[(key >> 10) & 2047u], 1u);
-      } else if (d > prefix) {
+      } else if (d > d0) {
         sh->above_idx[atomicAdd(&sh->n_above, 1)] = static_cast<uint16_t>(e);
       }
     }
     __syncthreads();
     n_cand = sh->n_cand;
     n_above = sh->n_above;
-    radix_pass(1, 11);
+    radix_pass(11);
     for (int c = tid; c < n_cand; c += nthr) {
       const uint32_t key = keys[sh->cand[c]];
       if ((key >> 10) == prefix) atomicAdd(&sh->hist[key & 1023u], 1u);
     }
-    radix_pass(2, 10);
+    __syncthreads();
+    radix_pass(10);
   } else {
     for (int e = tid; e < len; e += nthr) {
       const uint32_t key = keys[e];
       if ((key >> 21) == prefix) atomicAdd(&sh->hist[(key >> 10) & 2047u], 1u);
     }
-    radix_pass(1, 11);
+    __syncthreads();
+    radix_pass(11);
     for (int e = tid; e < len; e += nthr) {
       const uint32_t key = keys[e];
       if ((key >> 10) == prefix) atomicAdd(&sh->hist[key & 1023u], 1u);
     }
-    radix_pass(2, 10);
+    __syncthreads();
+    radix_pass(10);
   }
   const uint32_t thr = prefix;  // the k-th largest key; take `need` of its ties
 
   if (tid == 0) {
-    sh->counts[0] = 0;
     sh->counts[1] = 0;
     sh->ctr = 0;
     sh->ctr_eq = 0;
   }
   __syncthreads();
-  int gt = 0, eq = 0;
+  int eq = 0;
   if (compact) {
-    if (tid == 0) gt = n_above;
-    for (int c = tid; c < n_cand; c += nthr) {
-      const uint32_t key = keys[sh->cand[c]];
-      gt += key > thr;
-      eq += key == thr;
-    }
+    for (int c = tid; c < n_cand; c += nthr) eq += keys[sh->cand[c]] == thr;
   } else {
-    for (int e = tid; e < len; e += nthr) {
-      gt += keys[e] > thr;
-      eq += keys[e] == thr;
-    }
+    for (int e = tid; e < len; e += nthr) eq += keys[e] == thr;
   }
-  if (gt) atomicAdd(&sh->counts[0], gt);
   if (eq) atomicAdd(&sh->counts[1], eq);
-  cluster.sync();
-  if (tid < 32) {
-    // counts of the lower-ranked CTAs, and the cluster's tie total, summed by
-    // one warp (C <= 32)
-    int g = 0, e = 0, et = 0;
-    if (tid < C) {
-      const int* rc = cluster.map_shared_rank(sh->counts, tid);
-      et = rc[1];
-      if (tid < rank) {
-        g = rc[0];
-        e = et;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      g += __shfl_xor_sync(0xffffffffu, g, o);
-      e += __shfl_xor_sync(0xffffffffu, e, o);
-      et += __shfl_xor_sync(0xffffffffu, et, o);
-    }
-    if (tid == 0) {
-      sh->offs[0] = g;
-      sh->offs[1] = e;
-      sh->eq_total = et;
-    }
-  }
   __syncthreads();
-  const int off_gt = sh->offs[0];
-  const int off_eq = sh->offs[1];
   const int base = a.k - static_cast<int>(need);  // ties go to [base, k)
-  const bool all_ties = sh->eq_total == static_cast<int>(need);
+  const bool all_ties = sh->counts[1] == static_cast<int>(need);
   if (compact) {
-    // keys above the threshold bin, then the candidates above or (when every
-    // tie is selected) at the threshold: any order
-    for (int c = tid; c < n_above; c += nthr) {
-      const int p = atomicAdd(&sh->ctr, 1);
-      out[off_gt + p] = static_cast<int32_t>(start + sh->above_idx[c]);
-    }
+    for (int c = tid; c < n_above; c += nthr) out[atomicAdd(&sh->ctr, 1)] = sh->above_idx[c];
     for (int c = tid; c < n_cand; c += nthr) {
       const int e = sh->cand[c];
       const uint32_t key = keys[e];
-      if (key > thr) {
-        const int p = atomicAdd(&sh->ctr, 1);
-        out[off_gt + p] = static_cast<int32_t>(start + e);
-      } else if (key == thr && all_ties) {
-        const int p = atomicAdd(&sh->ctr_eq, 1);
-        out[base + off_eq + p] = static_cast<int32_t>(start + e);
-      }
-    }
-  } else if (all_ties) {
-    // every tie is selected (the usual case: one key holds the k-th score),
-    // so no order is needed: keys above and at the threshold are appended
-    for (int e = tid; e < len; e += nthr) {
-      const uint32_t key = keys[e];
-      if (key > thr) {
-        const int p = atomicAdd(&sh->ctr, 1);
-        out[off_gt + p] = static_cast<int32_t>(start + e);
-      } else if (key == thr) {
-        const int p = atomicAdd(&sh->ctr_eq, 1);
-        out[base + off_eq + p] = static_cast<int32_t>(start + e);
-      }
+      if (key > thr) out[atomicAdd(&sh->ctr, 1)] = e;
+      else if (key == thr && all_ties) out[base + atomicAdd(&sh->ctr_eq, 1)] = e;
     }
   } else {
-    // keys above the threshold: any order
     for (int e = tid; e < len; e += nthr) {
-      if (keys[e] > thr) {
-        const int p = atomicAdd(&sh->ctr, 1);
-        out[off_gt + p] = static_cast<int32_t>(start + e);
-      }
+      const uint32_t key = keys[e];
+      if (key > thr) out[atomicAdd(&sh->ctr, 1)] = e;
+      else if (key == thr && all_ties) out[base + atomicAdd(&sh->ctr_eq, 1)] = e;
     }
   }
   if (!all_ties) {
@@ -335,136 +306,300 @@ __global__ void topk_kernel(const TopkArgs a) {
       if (jj >= n_run) jj -= n_run;
       c += keys[e0 + jj] == thr;
     }
-    uint32_t rnk = static_cast<uint32_t>(off_eq) + block_exclusive_scan(c, sh, tid, nthr);
+    uint32_t rnk = block_exclusive_scan(c, &sh->scan, tid, nthr);
     for (int j = 0; j < n_run && c > 0 && rnk < need; ++j) {
       if (keys[e0 + j] == thr) {
-        out[base + rnk] = static_cast<int32_t>(start + e0 + j);
+        out[base + rnk] = e0 + j;
         ++rnk;
         --c;
       }
     }
   }
-  cluster.sync();  // keep this CTA's shared memory alive for the others' reads
 }
 
-// Clusters of C CTAs (threads, smem per CTA) that the device can hold at
-// once; queried once per (device, shape) and remembered.
-struct OccKey {
-  int dev, C, threads;
-  size_t smem;
-  int n;
+// ============================================================ slice path
+struct SliceShared {
+  ScanShared scan;
+  uint32_t hist[kBins];
+  int last;
+  int n_gt, n_eq;
 };
-OccKey g_occ[64];
-int g_nocc = 0;
-std::mutex g_occ_mu;
 
-int query_active_clusters(int C, int threads, size_t smem);
-
-int max_active_clusters(int C, int threads, size_t smem) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> lk(g_occ_mu);
-  for (int i = 0; i < g_nocc; ++i)
-    if (g_occ[i].dev == dev && g_occ[i].C == C && g_occ[i].threads == threads &&
-        g_occ[i].smem == smem)
-      return g_occ[i].n;
-  const int n = query_active_clusters(C, threads, smem);
-  if (g_nocc < 64) g_occ[g_nocc++] = OccKey{dev, C, threads, smem, n};
-  return n;
+// Histogram of the top 11 key bits of this CTA's slice, into its own bins.
+__global__ void __launch_bounds__(kPickThreads) topk_hist_kernel(const TopkArgs a) {
+  __shared__ uint32_t hist[kBins];
+  const int tid = threadIdx.x;
+  const int s = blockIdx.x;
+  const int64_t row = static_cast<int64_t>(blockIdx.y) + static_cast<int64_t>(gridDim.y) * blockIdx.z;
+  pdl_trigger();
+  pdl_wait();  // the scores are complete
+  if (row >= a.rows) return;
+  if (s == 0 && tid < 4) a.ctr[row * 4 + tid] = 0;  // read by topk_pick_kernel
+  const int64_t n = visible_count(a.pos[row], a.m, a.N_cap);
+  if (n <= a.k) return;  // every visible entry is selected (the pick kernel writes them)
+  for (int i = tid; i < kBins; i += kPickThreads) hist[i] = 0;
+  __syncthreads();
+  const int64_t lo = static_cast<int64_t>(s) * a.slice;
+  const int64_t hi = lo + a.slice < n ? lo + a.slice : n;
+  const float* src = a.scores + row * a.N_cap;
+  if (hi <= lo) {
+    // nothing visible in this slice
+  } else if (a.vec4) {
+    // slices start at multiples of 4 and rows are 16-byte aligned
+    const int64_t q_hi = hi >> 2;
+    for (int64_t q = (lo >> 2) + tid; q < q_hi; q += kPickThreads) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(src) + q);
+      atomicAdd(&hist[order_key(v.x) >> 21], 1u);
+      atomicAdd(&hist[order_key(v.y) >> 21], 1u);
+      atomicAdd(&hist[order_key(v.z) >> 21], 1u);
+      atomicAdd(&hist[order_key(v.w) >> 21], 1u);
+    }
+    for (int64_t e = (q_hi << 2) + tid; e < hi; e += kPickThreads)
+      atomicAdd(&hist[order_key(src[e]) >> 21], 1u);
+  } else {
+    for (int64_t e = lo + tid; e < hi; e += kPickThreads)
+      atomicAdd(&hist[order_key(src[e]) >> 21], 1u);
+  }
+  __syncthreads();
+  uint16_t* dst = a.hist + (row * a.S + s) * kBins;
+  for (int i = tid; i < kBins; i += kPickThreads) dst[i] = static_cast<uint16_t>(hist[i]);
 }
 
-int query_active_clusters(int C, int threads, size_t smem) {
-  if (C > 8) cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
+__global__ void __launch_bounds__(kPickThreads) topk_pick_kernel(const TopkArgs a) {
+  __shared__ SliceShared sh;
+  const int tid = threadIdx.x;
+  const int s = blockIdx.x;
+  const int64_t row = static_cast<int64_t>(blockIdx.y) + static_cast<int64_t>(gridDim.y) * blockIdx.z;
+  pdl_trigger();
+  pdl_wait();  // the histograms (and the scores before them) are complete
+  if (row >= a.rows) return;
+  const int64_t n = visible_count(a.pos[row], a.m, a.N_cap);
+  int32_t* out = a.idx + row * a.k;
+  const int64_t lo = static_cast<int64_t>(s) * a.slice;
+  const int64_t hi = lo + a.slice < n ? lo + a.slice : n;
+  if (n <= a.k) {
+    // every visible entry is selected; CTA 0 pads
+    for (int64_t e = lo + tid; e < hi; e += kPickThreads) out[e] = static_cast<int32_t>(e);
+    if (s == 0)
+      for (int64_t e = n + tid; e < a.k; e += kPickThreads) out[e] = -1;
+    return;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, 1, 1);
-  cfg.blockDim = dim3(threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = C;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, topk_kernel, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
+  // the row's histogram: the sum of its S slices' bins
+  const uint16_t* rh = a.hist + row * a.S * kBins;
+  for (int i = tid; i < kBins; i += kPickThreads) {
+    uint32_t c = 0;
+    for (int q = 0; q < a.S; ++q) c += rh[q * kBins + i];
+    sh.hist[i] = c;
   }
-  return n;
-}
-
-void fill_plan(int C, int64_t N_cap, TopkPlan* p) {
-  int slice = static_cast<int>((N_cap + C - 1) / C);
-  if (slice < 1) slice = 1;
-  p->cluster = C;
-  p->slice = slice;
-  p->threads = slice >= 8192 ? 1024 : (slice >= 2048 ? 512 : 256);
-  p->smem_bytes = sizeof(TopkShared) + static_cast<size_t>(slice) * 4;
+  __syncthreads();
+  find_digit_desc(sh.hist, kBins, static_cast<uint32_t>(a.k), &sh.scan, tid, kPickThreads);
+  const uint32_t d0 = sh.scan.digit;
+  const uint32_t n_above = sh.scan.above;  // keys in bins above d0: all selected
+  int* ctr = a.ctr + row * 4;              // [0] above appended, [1] candidates, [2] tickets
+  int32_t* cand = a.cand + row * a.N_cap;
+  const float* src = a.scores + row * a.N_cap;
+  // sweep the slice: above the bin -> output, in the bin -> candidates
+  for (int64_t e0 = lo; e0 < hi; e0 += kPickThreads) {
+    const int64_t e = e0 + tid;
+    uint32_t d = 0;
+    if (e < hi) d = order_key(src[e]) >> 21;
+    const bool up = e < hi && d > d0;
+    const bool in = e < hi && d == d0;
+    const int p_up = warp_append(&ctr[0], up);
+    const int p_in = warp_append(&ctr[1], in);
+    if (up && p_up < a.k) out[p_up] = static_cast<int32_t>(e);
+    if (in && p_in < a.N_cap) cand[p_in] = static_cast<int32_t>(e);
+  }
+  // the last CTA of the row to get here ranks the candidates
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh.last = atomicAdd(&ctr[2], 1) == a.S - 1;
+  __syncthreads();
+  if (!sh.last) return;
+  __threadfence();
+  const int C = min(__ldcg(&ctr[1]), static_cast<int>(a.N_cap));
+  uint32_t need = static_cast<uint32_t>(a.k) - n_above;  // 1 <= need <= C
+  const int room = static_cast<int>(need);               // places left in the output
+  int32_t* rest = out + n_above;
+  if (static_cast<int>(need) >= C) {
+    for (int c = tid; c < C; c += kPickThreads) rest[c] = __ldcg(cand + c);
+    return;
+  }
+  // the two remaining digits of the need-th largest candidate key
+  uint32_t prefix = d0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int width = pass == 0 ? 11 : 10;
+    const int shift = pass == 0 ? 10 : 0;
+    const int nb = 1 << width;
+    for (int i = tid; i < kBins; i += kPickThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int c = tid; c < C; c += kPickThreads) {
+      const uint32_t key = order_key(src[__ldcg(cand + c)]);
+      if ((key >> (shift + width)) == prefix) atomicAdd(&sh.hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    find_digit_desc(sh.hist, nb, need, &sh.scan, tid, kPickThreads);
+    prefix = (prefix << width) | sh.scan.digit;
+    need -= sh.scan.above;
+  }
+  const uint32_t thr = prefix;  // the k-th largest key; `need` of its ties are taken
+  // candidates above the threshold, and the count of ties at it (the loops
+  // run the same trip count in every thread: warp_append is warp-collective)
+  if (tid == 0) {
+    sh.n_gt = 0;
+    sh.n_eq = 0;
+  }
+  __syncthreads();
+  int eq = 0;
+  for (int c0 = 0; c0 < C; c0 += kPickThreads) {
+    const int c = c0 + tid;
+    int32_t j = 0;
+    uint32_t key = 0;
+    if (c < C) {
+      j = __ldcg(cand + c);
+      key = order_key(src[j]);
+    }
+    const bool gt = c < C && key > thr;
+    const int p = warp_append(&sh.n_gt, gt);  // shared-memory counter
+    if (gt && p < room) rest[p] = j;
+    eq += c < C && key == thr;
+  }
+  if (eq) atomicAdd(&sh.n_eq, eq);
+  __syncthreads();
+  const int n_gt = sh.n_gt;
+  const uint32_t n_eq = static_cast<uint32_t>(sh.n_eq);
+  int32_t* ties_out = rest + n_gt;
+  // ties at the threshold: the need smallest entry indices among them (every
+  // tie when they are exactly the places left).  Radix select on the index
+  // value, smallest first, finds the need-th smallest tie index ti.
+  uint32_t ti = 0xffffffffu;
+  if (n_eq != need) {
+    uint32_t ip = 0, left = need;
+    for (int pass = 0; pass < 3; ++pass) {
+      const int width = pass == 2 ? 10 : 11;
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const int nb = 1 << width;
+      for (int i = tid; i < kBins; i += kPickThreads) sh.hist[i] = 0;
+      __syncthreads();
+      for (int c = tid; c < C; c += kPickThreads) {
+        const uint32_t j = static_cast<uint32_t>(__ldcg(cand + c));
+        if (order_key(src[j]) != thr) continue;
+        if (pass > 0 && (j >> (shift + width)) != ip) continue;
+        atomicAdd(&sh.hist[(j >> shift) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      find_digit_asc(sh.hist, nb, left, &sh.scan, tid, kPickThreads);
+      ip = (ip << width) | sh.scan.digit;
+      left -= sh.scan.above;
+    }
+    ti = ip;  // indices are distinct: the ties with index <= ti are exactly `need`
+  }
+  if (tid == 0) sh.n_gt = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < C; c0 += kPickThreads) {
+    const int c = c0 + tid;
+    int32_t j = 0;
+    bool take = false;
+    if (c < C) {
+      j = __ldcg(cand + c);
+      take = order_key(src[j]) == thr && static_cast<uint32_t>(j) <= ti;
+    }
+    const int p = warp_append(&sh.n_gt, take);
+    if (take && n_gt + p < room) ties_out[p] = j;
+  }
 }
 
 }  // namespace
 
-static_assert(sizeof(TopkShared) + 49152 * 4 <= 227 * 1024,
-              "a 49,152-key slice and the shared state fit one CTA's shared memory");
+static_assert(sizeof(RowShared) + kRowMaxKeys * 4 <= 227 * 1024,
+              "a 49,152-key row and the shared state fit one CTA's shared memory");
 
-bool plan_topk(int rows, int64_t N_cap, int num_sms, TopkPlan* p) {
-  if (rows <= 0 || N_cap < 0) return false;
-  const int64_t max_slice = 49152;  // keys per CTA held in shared memory
-  int C = 1;
-  // spread small batches over more SMs, keep slices large enough to be worth it
-  while (C < 16 && (int64_t)rows * C < num_sms && (N_cap + 2 * C - 1) / (2 * C) >= 2048) C *= 2;
-  while (C < 16 && (N_cap + C - 1) / C > max_slice) C *= 2;
-  if ((N_cap + C - 1) / C > max_slice) return false;
-  // Clusters that do not all fit on the device at once run in waves, and a
-  // second wave repeats every fixed cost (the barriers and scans of each
-  // pass, about as much as 16K keys of work).  Take the cluster size with the
-  // least (waves x (keys per CTA + 16K)), the larger size on ties.
-  int64_t best_cost = -1;
-  TopkPlan best = {};
-  for (int c = C; c >= 1; c >>= 1) {
-    if ((N_cap + c - 1) / c > max_slice) break;
-    TopkPlan q;
-    fill_plan(c, N_cap, &q);
-    const int n = max_active_clusters(c, q.threads, q.smem_bytes);
-    if (n < 1) continue;
-    const int64_t waves = (rows + n - 1) / n;
-    const int64_t cost = waves * (q.slice + 16384);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = q;
-    }
+bool plan_topk(int64_t rows, int64_t N_cap, int k, int num_sms, TopkPlan* p) {
+  if (rows <= 0 || N_cap < 1 || k < 1) return false;
+  *p = TopkPlan{};
+  // Few long rows spread over many CTAs (slice path); otherwise one CTA per
+  // row with the keys in shared memory (row path).
+  const bool row_fits = N_cap <= kRowMaxKeys;
+  const bool few_rows = rows * 2 < num_sms;
+  if (row_fits && (!few_rows || N_cap <= 8192)) {
+    p->slice_path = false;
+    p->S = 1;
+    p->threads = N_cap >= 8192 ? 1024 : (N_cap >= 2048 ? 512 : 256);
+    p->smem_bytes = sizeof(RowShared) + static_cast<size_t>(N_cap) * 4;
+  } else {
+    p->slice_path = true;
+    // about one CTA per SM over all rows; a slice is a multiple of 64
+    // entries and holds at most 65,535 (the bins are 16-bit)
+    int64_t S = num_sms / rows;
+    if (S < 1) S = 1;
+    int64_t slice = ((N_cap + S - 1) / S + 63) / 64 * 64;
+    if (slice > 65472) slice = 65472;
+    S = (N_cap + slice - 1) / slice;
+    if (S > 65535) return false;
+    p->S = static_cast<int>(S);
+    p->slice = slice;
+    p->threads = kPickThreads;
+    p->smem_bytes = 0;
   }
-  if (best_cost < 0) return false;
-  *p = best;
+  p->ws_bytes = topk_scratch_bytes(*p, rows, N_cap);
   return true;
 }
 
-cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(p.smem_bytes));
-  if (e != cudaSuccess) return e;
+size_t topk_scratch_bytes(const TopkPlan& p, int64_t rows, int64_t N_cap) {
+  if (!p.slice_path) return 0;
+  const size_t hist = static_cast<size_t>(rows) * p.S * kBins * sizeof(uint16_t);
+  const size_t ctr = static_cast<size_t>(rows) * 4 * sizeof(int32_t);
+  const size_t cand = static_cast<size_t>(rows) * N_cap * sizeof(int32_t);
+  return (hist + 255) / 256 * 256 + (ctr + 255) / 256 * 256 + cand;
+}
+
+void topk_scratch_carve(const TopkPlan& p, int64_t rows, void* ws, TopkArgs* a) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  const size_t hist = static_cast<size_t>(rows) * p.S * kBins * sizeof(uint16_t);
+  const size_t ctr = static_cast<size_t>(rows) * 4 * sizeof(int32_t);
+  a->hist = reinterpret_cast<uint16_t*>(b);
+  b += (hist + 255) / 256 * 256;
+  a->ctr = reinterpret_cast<int32_t*>(b);
+  b += (ctr + 255) / 256 * 256;
+  a->cand = reinterpret_cast<int32_t*>(b);
+}
+
+cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, bool dependent,
+                        cudaStream_t stream) {
+  // rows fold over grid y and z (y <= 65535)
+  const int64_t gy = a.rows < 65535 ? a.rows : 65535;
+  const int64_t gz = (a.rows + gy - 1) / gy;
+  if (gz > 65535) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.cluster, a.rows, 1);
   cfg.blockDim = dim3(p.threads, 1, 1);
-  cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = p.cluster;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute at[1];
   cfg.attrs = at;
-  cfg.numAttrs = add_dependent_attr(at, 1);
+  cfg.numAttrs = add_dependent_attr(at, 0, dependent);
   TopkArgs args = a;
-  args.cluster = p.cluster;
+  args.S = p.S;
   args.slice = p.slice;
-  e = cudaLaunchKernelEx(&cfg, topk_kernel, args);
+  args.vec4 = (a.N_cap % 4 == 0) && (reinterpret_cast<uintptr_t>(a.scores) % 16 == 0) &&
+              (p.slice % 4 == 0);
+  cudaError_t e;
+  if (!p.slice_path) {
+    e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(p.smem_bytes));
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(1, static_cast<unsigned>(gy), static_cast<unsigned>(gz));
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    e = cudaLaunchKernelEx(&cfg, topk_row_kernel, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+  cfg.gridDim = dim3(p.S, static_cast<unsigned>(gy), static_cast<unsigned>(gz));
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, topk_hist_kernel, args);
+  if (e != cudaSuccess) return e;
+  // the pick kernel reads what the histogram kernel wrote: always a
+  // dependent of it (it waits before its first read)
+  cfg.numAttrs = add_dependent_attr(at, 0, true);
+  e = cudaLaunchKernelEx(&cfg, topk_pick_kernel, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -48,7 +48,7 @@ _SIGS = {
     "hattn_swa_keys_ring": (_i32, [_vp, _vp, _vp, _i32, _i32, _i64, _i32, _i32, _i32, _f32, _f32,
                                    _vp, _vp]),
     "hattn_indexer_scores_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
-                                        _i32, _i32, _i64, _vp, _vp]),
+                                        _i32, _i32, _i64, _vp, _i32, _vp]),
     "hattn_indexer_topk": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                   _vp, _vp, _vp, _sz, _vp]),
     "hattn_indexer_topk_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32, _i32]),
@@ -56,7 +56,9 @@ _SIGS = {
                                           _i32, _vp, _vp]),
     "hattn_indexer_scores": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
                                     _vp]),
-    "hattn_topk_select": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp]),
+    "hattn_topk_select": (_i32, [_vp, _vp, _i32, _i32, _i64, _i32, _i32, _vp, _vp, _sz, _i32,
+                                 _vp]),
+    "hattn_topk_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32]),
     "hattn_query_prep": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _vp,
                                 _vp]),
     "hattn_sparse_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
@@ -70,16 +72,16 @@ _SIGS = {
                               _vp]),
     "hattn_hybrid_attn": (_i32, [_vp, _vp, _i32, _vp, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i32,
                                  _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32, _i32, _i32,
-                                 _vp, _vp, _vp, _sz, _vp]),
+                                 _vp, _vp, _vp, _sz, _i32, _vp]),
     "hattn_hybrid_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                                 _i32, _i32, _i32]),
     "hattn_hybrid_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _i32]),
     "hattn_indexer_scores_ex": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
-                                       _i32, _i64, _vp, _vp]),
+                                       _i32, _i64, _vp, _i32, _vp]),
     "hattn_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64]),
     "hattn_lse_merge_splits": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i32),
                                       _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp,
-                                      _vp]),
+                                      _i32, _vp]),
     "hattn_lse_merge": (_i32, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32, _vp, _vp, _i32,
                                _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp]),
     "hattn_status_string": (ctypes.c_char_p, [_i32]),
@@ -87,8 +89,9 @@ _SIGS = {
     "hattn_check_status": (_i32, [_vp]),
     "hattn_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
     "hattn_version": (ctypes.c_char_p, []),
-    "hattn_set_dependent_launch": (_i32, [_i32]),
 }
+
+LAUNCH_DEPENDENT = 1  # HATTN_LAUNCH_DEPENDENT
 
 _lib = None
 
@@ -145,6 +148,32 @@ def _need(t, name, dtype, ndim=None):
 
 def _opt(t, name, dtype):
     return None if t is None else _need(t, name, dtype)
+
+
+def _shape(t, name, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _flags(dependent):
+    return LAUNCH_DEPENDENT if dependent else 0
+
+
+def _indexer_inputs(iq, w, ik, pos, ik_name="ik_c", ik_dtype=torch.bfloat16):
+    """Checks the indexer inputs against each other; returns B, T, HI, dI, N_cap."""
+    _need(iq, "iq", torch.bfloat16, 4)
+    _need(w, "w", torch.float32, 3)
+    _need(ik, ik_name, ik_dtype, 3)
+    _need(pos, "pos", torch.int32, 2)
+    B, T, HI, dI = iq.shape
+    _shape(w, "w", (B, T, HI))
+    _shape(pos, "pos", (B, T))
+    if ik.shape[0] != B:
+        raise ValueError(f"{ik_name} holds {ik.shape[0]} sequences, iq {B}")
+    if ik_dtype == torch.bfloat16 and ik.shape[2] != dI:
+        raise ValueError(f"{ik_name} rows have {ik.shape[2]} dims, iq {dI}")
+    return B, T, HI, dI, ik.shape[1]
 
 
 # ------------------------------------------------------------------ compression
@@ -352,19 +381,31 @@ def indexer_topk_workspace_bytes(B, T, N_cap, k, score_out_given=False):
     return int(lib().hattn_indexer_topk_workspace_bytes(B, T, N_cap, k, int(bool(score_out_given))))
 
 
+def topk_workspace_bytes(B, T, N_cap, k):
+    return int(lib().hattn_topk_workspace_bytes(B, T, N_cap, k))
+
+
+def topk_launches(B, T, N_cap, k):
+    """Kernels one top-k selection launches: two when its rows are spread
+    over many CTAs (the calls that need a scratch), else one."""
+    return 2 if topk_workspace_bytes(B, T, N_cap, k) > 0 else 1
+
+
+def _idx_out(idx_out, B, T, k, device):
+    if idx_out is None:
+        idx_out = torch.empty((B, T, k), dtype=torch.int32, device=device)
+    _need(idx_out, "idx_out", torch.int32, 3)
+    return _shape(idx_out, "idx_out", (B, T, k))
+
+
 def indexer_topk(iq, w, ik_c, pos, *, k, m=4, idx_out=None, score_out=None, workspace=None,
                  stream=None):
     """Lightning-indexer scores + per-query top-k; returns idx [B, T, k] int32."""
-    _need(iq, "iq", torch.bfloat16, 4)
-    _need(w, "w", torch.float32, 3)
-    _need(ik_c, "ik_c", torch.bfloat16, 3)
-    _need(pos, "pos", torch.int32, 2)
-    B, T, HI, dI = iq.shape
-    N_cap = ik_c.shape[1]
-    if idx_out is None:
-        idx_out = torch.empty((B, T, k), dtype=torch.int32, device=iq.device)
-    _need(idx_out, "idx_out", torch.int32)
-    _opt(score_out, "score_out", torch.float32)
+    B, T, HI, dI, N_cap = _indexer_inputs(iq, w, ik_c, pos)
+    idx_out = _idx_out(idx_out, B, T, k, iq.device)
+    if score_out is not None:
+        _need(score_out, "score_out", torch.float32, 3)
+        _shape(score_out, "score_out", (B, T, N_cap))
     need = indexer_topk_workspace_bytes(B, T, N_cap, k, score_out is not None)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=iq.device)
@@ -376,43 +417,34 @@ def indexer_topk(iq, w, ik_c, pos, *, k, m=4, idx_out=None, score_out=None, work
 
 
 def indexer_topk_noalloc(iq, w, ik_c, pos, *, k, m=4, idx_out=None, stream=None):
-    """indexer_topk with its score scratch in the library's fixed device
-    array (no device allocation by the library; B*T*N_cap <= 4,194,304).
-    Calls that overlap on the GPU share that array and race."""
-    _need(iq, "iq", torch.bfloat16, 4)
-    _need(w, "w", torch.float32, 3)
-    _need(ik_c, "ik_c", torch.bfloat16, 3)
-    _need(pos, "pos", torch.int32, 2)
-    B, T, HI, dI = iq.shape
-    if idx_out is None:
-        idx_out = torch.empty((B, T, k), dtype=torch.int32, device=iq.device)
-    _need(idx_out, "idx_out", torch.int32)
+    """indexer_topk with its score and selection scratch in the library's
+    fixed device array (no device allocation by the library;
+    B*T*N_cap <= 4,194,304).  Calls that overlap on the GPU share that array
+    and race."""
+    B, T, HI, dI, N_cap = _indexer_inputs(iq, w, ik_c, pos)
+    idx_out = _idx_out(idx_out, B, T, k, iq.device)
     _check(lib().hattn_indexer_topk_noalloc(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI,
-                                            dI, ik_c.shape[1], k, m, _ptr(idx_out),
-                                            _stream(stream)))
+                                            dI, N_cap, k, m, _ptr(idx_out), _stream(stream)))
     return idx_out
 
 
 def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, fresh_from=-1,
-                   stream=None):
+                   dependent=False, stream=None):
     """Lightning-indexer scores only; returns score_out [B, T, N_cap] fp32
     (entries beyond each query's visible count are left untouched).  n_sms:
     run the persistent score kernel on at most that many SMs (0 = all);
-    fresh_from: with dependent launches, the first entry the previous kernel
-    may write (-1 = any)."""
-    _need(iq, "iq", torch.bfloat16, 4)
-    _need(w, "w", torch.float32, 3)
-    _need(ik_c, "ik_c", torch.bfloat16, 3)
-    _need(pos, "pos", torch.int32, 2)
-    B, T, HI, dI = iq.shape
-    N_cap = ik_c.shape[1]
+    dependent: launch as a programmatic dependent of the previous kernel in
+    the stream (HATTN_LAUNCH_DEPENDENT), with fresh_from the first entry that
+    kernel may write (-1 = any)."""
+    B, T, HI, dI, N_cap = _indexer_inputs(iq, w, ik_c, pos)
     if score_out is None:
         score_out = torch.empty((B, T, N_cap), dtype=torch.float32, device=iq.device)
-    _need(score_out, "score_out", torch.float32)
-    if n_sms or fresh_from >= 0:
+    _need(score_out, "score_out", torch.float32, 3)
+    _shape(score_out, "score_out", (B, T, N_cap))
+    if n_sms or fresh_from >= 0 or dependent:
         _check(lib().hattn_indexer_scores_ex(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI,
                                              dI, N_cap, m, n_sms, fresh_from, _ptr(score_out),
-                                             _stream(stream)))
+                                             _flags(dependent), _stream(stream)))
     else:
         _check(lib().hattn_indexer_scores(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
                                           N_cap, m, _ptr(score_out), _stream(stream)))
@@ -420,36 +452,39 @@ def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, fresh_from
 
 
 def indexer_scores_fp8(iq, w, ik8, ik_scale, pos, *, m=4, score_out=None, n_sms=0,
-                       fresh_from=-1, stream=None):
+                       fresh_from=-1, dependent=False, stream=None):
     """indexer_scores over E4M3 keys (ik8 uint8 [B, N_cap, 128] with row
     scales ik_scale fp32 [B, N_cap]); the bf16 queries are quantised the
     same way in the kernel."""
-    _need(iq, "iq", torch.bfloat16, 4)
-    _need(w, "w", torch.float32, 3)
-    _need(ik8, "ik8", torch.uint8, 3)
+    B, T, HI, dI, N_cap = _indexer_inputs(iq, w, ik8, pos, "ik8", torch.uint8)
     _need(ik_scale, "ik_scale", torch.float32, 2)
-    _need(pos, "pos", torch.int32, 2)
-    B, T, HI, dI = iq.shape
-    N_cap = ik8.shape[1]
+    _shape(ik_scale, "ik_scale", (B, N_cap))
     if score_out is None:
         score_out = torch.empty((B, T, N_cap), dtype=torch.float32, device=iq.device)
-    _need(score_out, "score_out", torch.float32)
+    _need(score_out, "score_out", torch.float32, 3)
+    _shape(score_out, "score_out", (B, T, N_cap))
     _check(lib().hattn_indexer_scores_fp8(_ptr(iq), _ptr(w), _ptr(ik8), _ptr(ik_scale), _ptr(pos),
                                           B, T, HI, dI, N_cap, m, n_sms, fresh_from,
-                                          _ptr(score_out), _stream(stream)))
+                                          _ptr(score_out), _flags(dependent), _stream(stream)))
     return score_out
 
 
-def topk_select(scores, pos, *, k, m=4, idx_out=None, stream=None):
-    """Per-query top-k over precomputed scores; returns idx [B, T, k] int32."""
+def topk_select(scores, pos, *, k, m=4, idx_out=None, workspace=None, dependent=False,
+                stream=None):
+    """Per-query top-k over precomputed scores; returns idx [B, T, k] int32.
+    workspace: the selection's scratch (topk_workspace_bytes; allocated here
+    when needed and not given)."""
     _need(scores, "scores", torch.float32, 3)
     _need(pos, "pos", torch.int32, 2)
     B, T, N_cap = scores.shape
-    if idx_out is None:
-        idx_out = torch.empty((B, T, k), dtype=torch.int32, device=scores.device)
-    _need(idx_out, "idx_out", torch.int32)
+    _shape(pos, "pos", (B, T))
+    idx_out = _idx_out(idx_out, B, T, k, scores.device)
+    need = topk_workspace_bytes(B, T, N_cap, k)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().hattn_topk_select(_ptr(scores), _ptr(pos), B, T, N_cap, k, m, _ptr(idx_out),
-                                   _stream(stream)))
+                                   _ptr(workspace), wsb, _flags(dependent), _stream(stream)))
     return idx_out
 
 
@@ -611,12 +646,14 @@ def hybrid_attn_splits(B, T, H, D, k, N_h, W, segments=SEG_ALL, n_sms=0):
 
 def hybrid_attn(q, kv_c, idx, kv_h, kv_w, pos, *, r, m=128, k=None, W=None, gamma_q=None,
                 rope_base=10000.0, eps=1e-6, scale=None, o=None, lse=None, workspace=None,
-                q_prepped=False, partials=False, segments=SEG_ALL, n_sms=0, stream=None):
+                q_prepped=False, partials=False, segments=SEG_ALL, n_sms=0, dependent=False,
+                stream=None):
     """CSA (selected entries), HCA (visible entries) and SWA (kv_w from
     swa_keys) keys of each query under one softmax; returns (o fp32, lse
     fp32) or, with partials=True, a Partials view of the workspace.
     segments: the key sets covered (SEG_* mask; tensors of the others may be
-    None); n_sms: the SM share the split plan assumes (0 = all)."""
+    None); n_sms: the SM share the split plan assumes (0 = all); dependent:
+    launch as a programmatic dependent of the previous kernel in the stream."""
     _need(q, "q", torch.bfloat16, 4)
     _need(pos, "pos", torch.int32, 2)
     _opt(gamma_q, "gamma_q", torch.float32)
@@ -644,7 +681,7 @@ def hybrid_attn(q, kv_c, idx, kv_h, kv_w, pos, *, r, m=128, k=None, W=None, gamm
                                    _ptr(idx), N_c, k, _ptr(kv_h), N_h, m, _ptr(kv_w), W,
                                    _ptr(pos), B, T, H, D, r, rope_base, eps, scale, segments,
                                    n_sms, _ptr(o), _ptr(lse), _ptr(workspace), wsb,
-                                   _stream(stream)))
+                                   _flags(dependent), _stream(stream)))
     if not partials:
         return o, lse
     return Partials(workspace, q_prepped, B, T, H, D,
@@ -678,7 +715,7 @@ def lse_merge(o_list, lse_list, pos, *, r, sink=None, rope_base=10000.0, out=Non
 
 
 def lse_merge_splits(parts, pos, *, r, H, sink=None, rope_base=10000.0, out=None, lse_out=None,
-                     stream=None):
+                     dependent=False, stream=None):
     """Sink-augmented merge over the split partials of 1..4 branches (a list
     of Partials) + inverse RoPE; returns (out bf16 [B, T, H, D], lse)."""
     nb = len(parts)
@@ -699,7 +736,8 @@ def lse_merge_splits(parts, pos, *, r, H, sink=None, rope_base=10000.0, out=None
     lp = (_vp * nb)(*[p.lse.data_ptr() for p in parts])
     ns = (_i32 * nb)(*[p.nsplit for p in parts])
     _check(lib().hattn_lse_merge_splits(op, lp, ns, nb, _ptr(sink), _ptr(pos), B, T, H, D, r,
-                                        rope_base, _ptr(out), _ptr(lse_out), _stream(stream)))
+                                        rope_base, _ptr(out), _ptr(lse_out), _flags(dependent),
+                                        _stream(stream)))
     return out, lse_out
 
 
@@ -736,10 +774,3 @@ def status_string(code):
 
 def version():
     return lib().hattn_version().decode()
-
-
-def set_dependent_launch(enable):
-    """Launch the indexer, top-k, attention and merge kernels of the calls that
-    follow on this thread as programmatic dependents of the previous kernel in
-    their stream (see hattn_set_dependent_launch); returns the old setting."""
-    return bool(lib().hattn_set_dependent_launch(int(bool(enable))))

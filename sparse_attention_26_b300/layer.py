@@ -80,10 +80,12 @@ class HybridLayer:
         # out and lse are adjacent in one buffer (one copy returns both)
         n_out, n_lse = B * T * H * D * 2, B * T * H * 4
         res = torch.empty(n_out + n_lse, dtype=torch.uint8, device=dev)
+        n_sc = self.N_csa if "csa" in wl.branches else 1
         b = dict(
-            scores=torch.empty((B, T, self.N_csa if "csa" in wl.branches else 1),
-                               dtype=torch.float32, device=dev),
+            scores=torch.empty((B, T, n_sc), dtype=torch.float32, device=dev),
             idx=torch.empty((B, T, wl.k), dtype=torch.int32, device=dev),
+            ws_topk=torch.empty(max(hattn.topk_workspace_bytes(B, T, n_sc, wl.k), 16),
+                                dtype=torch.uint8, device=dev),
             out=res[:n_out].view(bf).view(B, T, H, D),
             lse=res[n_out:].view(torch.float32).view(B, T, H),
             result=res,
@@ -189,14 +191,15 @@ class HybridLayer:
             hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j0,
                                j_end=j1, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c, ik_c=self.ik_c)
 
-    def _indexer(self, iq, w, pos, scores, n_sms=0, fresh_from=-1):
+    def _indexer(self, iq, w, pos, scores, n_sms=0, fresh_from=-1, dependent=False):
         wl = self.wl
         if self.fp8:
             hattn.indexer_scores_fp8(iq, w, self.ik8, self.ik_scale, pos, m=wl.m_csa,
-                                     score_out=scores, n_sms=n_sms, fresh_from=fresh_from)
+                                     score_out=scores, n_sms=n_sms, fresh_from=fresh_from,
+                                     dependent=dependent)
         else:
             hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=scores,
-                                 n_sms=n_sms, fresh_from=fresh_from)
+                                 n_sms=n_sms, fresh_from=fresh_from, dependent=dependent)
 
     def _compress_new(self, kind, t_new, n_new):
         """Compress the entries that the step's new tokens complete."""
@@ -286,7 +289,8 @@ class HybridLayer:
             self._indexer(iq, w, pos, b["scores"])
             ev("indexer", 1)
             ev("topk", 0)
-            hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
+            hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"],
+                              workspace=b["ws_topk"])
             ev("topk", 1)
             ev("sparse", 0)
             parts["csa"] = hattn.sparse_attn(qt, self.kv_c, b["idx"], pos, r=wl.r,
@@ -329,14 +333,14 @@ class HybridLayer:
 
         has = set(wl.branches)
 
-        def attn(name, segments, n_sms):
+        def attn(name, segments, n_sms, dependent=False):
             ev("attn_" + name, 0)
             part = hattn.hybrid_attn(b["qt"], self.kv_c if "csa" in has else None,
                                      b["idx"] if "csa" in has else None,
                                      self.kv_h if "hca" in has else None, b.get("kv_w"), pos,
                                      r=wl.r, m=wl.m_hca, k=wl.k, W=wl.W,
                                      workspace=b["ws_" + name], q_prepped=True, partials=True,
-                                     segments=segments, n_sms=n_sms)
+                                     segments=segments, n_sms=n_sms, dependent=dependent)
             ev("attn_" + name, 1)
             return part
 
@@ -373,7 +377,6 @@ class HybridLayer:
         # from here on each main-stream call consumes what the one before it
         # produced, so its kernel may start as a dependent launch (its setup
         # overlaps the predecessor's tail; it waits before reading inputs)
-        prev_pdl = hattn.set_dependent_launch(pdl)
         if side_stream is not None and overlap:
             qprep()
             side_stream.wait_stream(main)
@@ -390,7 +393,7 @@ class HybridLayer:
             j0, j1 = self.new_entries("csa", t_new, T)
             self._indexer(iq, w, pos, b["scores"],
                           n_sms=(self.NUM_SMS - n_dense) if n_dense else 0,
-                          fresh_from=j0 if j1 > j0 else -1)
+                          fresh_from=j0 if j1 > j0 else -1, dependent=pdl)
             ev("indexer", 1)
         if side_stream is not None and not overlap:
             # The query preparation, the HCA compression and the window keys
@@ -405,21 +408,21 @@ class HybridLayer:
                 swa_keys()
         if "csa" in has:
             ev("topk", 0)
-            hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"])
+            hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"],
+                              workspace=b["ws_topk"], dependent=pdl)
             ev("topk", 1)
         if overlap:
-            parts = [attn("sparse", hattn.SEG_CSA, 0)]
+            parts = [attn("sparse", hattn.SEG_CSA, 0, dependent=pdl)]
             main.wait_stream(side_stream)
             parts.append(dense)
         else:
             if side_stream is not None:
                 main.wait_stream(side_stream)
-            parts = [attn("fused", self.segments(), 0)]
+            parts = [attn("fused", self.segments(), 0, dependent=pdl)]
         ev("merge", 0)
         hattn.lse_merge_splits(parts, pos, r=wl.r, H=wl.H, sink=sink, out=b["out"],
-                               lse_out=b["lse"])
+                               lse_out=b["lse"], dependent=pdl)
         ev("merge", 1)
-        hattn.set_dependent_launch(prev_pdl)
         return b["out"], b["lse"]
 
     def event_names(self, T, branch_outputs=False, fused=None, side_stream=True):
@@ -457,9 +460,10 @@ class HybridLayer:
             # the dense and the sparse key sets when a side stream is used
             has = set(wl.branches)
             split = side_stream and self.override_dense_sms > 0 and has == {"csa", "hca", "swa"}
-            return (n + int("swa" in has) + 2 * int("csa" in has) + 1 + int(split))
+            topk = hattn.topk_launches(B, T, self.N_csa, wl.k) if "csa" in has else 0
+            return n + int("swa" in has) + int("csa" in has) + topk + 1 + int(split)
         for name, kind, nk in self._branch_kinds():
             n += 1 + int(branch_outputs and hattn.attn_splits(kind, B, T, H, D, nk) > 1)
             if name == "csa":
-                n += 2  # indexer scores + top-k select
+                n += 1 + hattn.topk_launches(B, T, self.N_csa, wl.k)  # indexer + top-k
         return n

@@ -74,6 +74,9 @@ class DecodeStack:
         self.kv_w = torch.empty((B, T, W, D), dtype=bf, device=device)
         self.scores = torch.empty((B, T, self.N_csa), dtype=torch.float32, device=device)
         self.idx = torch.empty((B, T, k), dtype=torch.int32, device=device)
+        ws = hattn.topk_workspace_bytes(B, T, self.N_csa, k)
+        self.ws_topk = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        self.topk_launches = hattn.topk_launches(B, T, self.N_csa, k)
         self.out = torch.empty((len(self.kinds), B, T, H, D), dtype=bf, device=device)
         self.lse = torch.empty((len(self.kinds), B, T, H), dtype=torch.float32, device=device)
         self.ws = {}
@@ -141,15 +144,12 @@ class DecodeStack:
         already appended): q [L][B][1][H][D], iq [L][B][1][HI][dI],
         w [L][B][1][HI], sinks [L][H], pos [B][1] (all t).  Outputs land in
         self.out[l], self.lse[l]."""
-        prev = hattn.set_dependent_launch(self.dependent_launch)
-        try:
-            for l, st in enumerate(self.layers):
-                self._layer(l, st, t, q[l], iq[l], w[l], sinks[l], pos)
-        finally:
-            hattn.set_dependent_launch(prev)
+        for l, st in enumerate(self.layers):
+            self._layer(l, st, t, q[l], iq[l], w[l], sinks[l], pos)
 
     def _layer(self, l, st, t, q, iq, w, sink, pos):
         r, kind = self.r, st["kind"]
+        dep = self.dependent_launch
         # Launch order keeps every dependent launch after a kernel it may
         # overlap: compress (plain) -> indexer, top-k (dependent) -> query
         # prep, window keys (plain) -> attention, merge (dependent).
@@ -161,8 +161,9 @@ class DecodeStack:
                                         m=self.m_csa, w=self.w_csa, eps=self.eps)
             fresh = (t + 1) // self.m_csa - 1 if (t + 1) % self.m_csa == 0 else -1
             hattn.indexer_scores(iq, w, st["ik_c"], pos, m=self.m_csa, score_out=self.scores,
-                                 fresh_from=fresh)
-            hattn.topk_select(self.scores, pos, k=self.k, m=self.m_csa, idx_out=self.idx)
+                                 fresh_from=fresh, dependent=dep)
+            hattn.topk_select(self.scores, pos, k=self.k, m=self.m_csa, idx_out=self.idx,
+                              workspace=self.ws_topk, dependent=dep)
         elif kind == HCA and (t + 1) % self.m_hca == 0:
             j = (t + 1) // self.m_hca - 1
             hattn.hca_compress_ring(st["kv_ring"], st["gate_ring"], r=r, j_begin=j, j_end=j + 1,
@@ -172,9 +173,9 @@ class DecodeStack:
         part = hattn.hybrid_attn(self.qt, st.get("kv_c"), self.idx if kind == CSA else None,
                                  st.get("kv_h"), self.kv_w, pos, r=r, m=self.m_hca, k=self.k,
                                  W=self.W, eps=self.eps, workspace=self.ws[kind], q_prepped=True,
-                                 partials=True, segments=self.segments(kind))
+                                 partials=True, segments=self.segments(kind), dependent=dep)
         hattn.lse_merge_splits([part], pos, r=r, H=self.H, sink=sink, out=self.out[l],
-                               lse_out=self.lse[l])
+                               lse_out=self.lse[l], dependent=dep)
 
     def launches_per_step(self, t):
         """Kernels one step at position t launches."""
@@ -182,7 +183,7 @@ class DecodeStack:
         for st in self.layers:
             n += 4  # query prep, window keys, attention, merge
             if st["kind"] == CSA:
-                n += 2 + int((t + 1) % self.m_csa == 0)
+                n += 1 + self.topk_launches + int((t + 1) % self.m_csa == 0)
             elif st["kind"] == HCA:
                 n += int((t + 1) % self.m_hca == 0)
         return n

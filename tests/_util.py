@@ -35,21 +35,31 @@ def bf16_half_ulp(x):
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
-def check_attn(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+def check_attn(o_gpu, lse_gpu, o_ref, lse_ref, what="", stored_bf16=None):
     """Spec tolerance: max-abs 1e-2 and rel-L2 5e-3 on the attention output
-    (bf16 in, fp32 accumulate).  The layer output is stored in bf16, so a
-    result that is correct in fp32 may still land one rounding step away
-    from the oracle: every element may also differ by the half bf16 ulp that
-    storing it costs (0.0078 at magnitudes 2..4)."""
+    (bf16 in, fp32 accumulate).
+
+    fp32 outputs (the branch outputs o of the attention calls) face that
+    tolerance directly.  A bf16-stored output (the merged layer output, the
+    prepared queries) may land one rounding step away from the oracle even
+    when its fp32 value was correct, so for it the max-abs check applies to
+    the error beyond the half bf16 ulp that storing it costs (0.0078 at
+    magnitudes 2..4); its rel-L2 check is unchanged.  stored_bf16=None takes
+    the storage format from o_gpu's dtype."""
+    if stored_bf16 is None:
+        stored_bf16 = isinstance(o_gpu, torch.Tensor) and o_gpu.dtype == torch.bfloat16
     o_gpu, o_ref = f64(o_gpu), f64(o_ref)
     assert np.isfinite(o_gpu).all(), f"{what}: non-finite output"
     if o_ref.size:
-        excess = np.abs(o_gpu - o_ref) - bf16_half_ulp(o_ref)
-        err = float(excess.max())
+        dev = np.abs(o_gpu - o_ref)
+        if stored_bf16:
+            dev = dev - bf16_half_ulp(o_ref)
+        err = float(dev.max())
     else:
         err = 0.0
     rl = rel_l2(o_gpu, o_ref)
-    assert err <= ATTN_MAX_ABS, f"{what}: max-abs beyond bf16 rounding {err:.3e} > {ATTN_MAX_ABS}"
+    kind = "beyond bf16 rounding " if stored_bf16 else ""
+    assert err <= ATTN_MAX_ABS, f"{what}: max-abs {kind}{err:.3e} > {ATTN_MAX_ABS}"
     assert rl <= ATTN_REL_L2, f"{what}: rel-L2 {rl:.3e} > {ATTN_REL_L2}"
     if lse_gpu is not None:
         lg, lr = f64(lse_gpu), f64(lse_ref)

@@ -120,8 +120,52 @@ def test_indexer_validation(L):
     assert rc == hattn.INVALID_ARG
     rc = L.hattn_indexer_topk(FAKE, FAKE, FAKE, N, 1, 1, 64, 128, 100, 16, 4, FAKE, N, N, 0, N)
     assert rc == hattn.INVALID_ARG and "pos" in _err(L)
-    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 0) == 8 * 262144 * 4
-    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 1) == 0
+    # the scores, then the selection's scratch; rows that fit one CTA need none
+    sel = L.hattn_topk_workspace_bytes(8, 1, 262144, 1024)
+    assert sel >= 8 * 262144 * 4  # at least one candidate slot per entry
+    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 0) == 8 * 262144 * 4 + sel
+    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 1) == sel
+    assert L.hattn_topk_workspace_bytes(8192, 1, 2048, 512) == 0
+    assert L.hattn_indexer_topk_workspace_bytes(1, 8192, 2048, 512, 0) == 8192 * 2048 * 4
+
+
+def test_topk_validation(L):
+    """Arguments of the selection are checked before any launch: unknown
+    flag bits, a missing or short scratch where the plan needs one, k."""
+    N = None
+    s = None
+    sel = L.hattn_topk_workspace_bytes(8, 1, 262144, 1024)
+    # hattn_topk_select(scores, pos, B, T, N_cap, k, m, idx_out, ws, ws_bytes, flags, stream)
+    rc = L.hattn_topk_select(FAKE, FAKE, 8, 1, 262144, 1024, 4, FAKE, FAKE, sel, 2, s)
+    assert rc == hattn.INVALID_ARG and "flags" in _err(L)
+    rc = L.hattn_topk_select(FAKE, FAKE, 8, 1, 262144, 1024, 4, FAKE, N, 0, 0, s)
+    assert rc == hattn.INVALID_ARG and "workspace" in _err(L)
+    rc = L.hattn_topk_select(FAKE, FAKE, 8, 1, 262144, 1024, 4, FAKE, FAKE, sel - 1, 0, s)
+    assert rc == hattn.INVALID_ARG and "workspace" in _err(L)
+    rc = L.hattn_topk_select(FAKE, FAKE, 8, 1, 262144, 4096, 4, FAKE, FAKE, sel, 0, s)
+    assert rc == hattn.INVALID_ARG and "k=4096" in _err(L)
+    rc = L.hattn_topk_select(FAKE, FAKE, 8, 1, 1 << 31, 1024, 4, FAKE, FAKE, sel, 0, s)
+    assert rc == hattn.INVALID_ARG and "N_cap" in _err(L)
+
+
+def test_launch_flags_are_per_call(L):
+    """No launch mode is kept between calls: the dependent-launch choice is
+    a flag of each call that may launch that way, and unknown bits are
+    refused."""
+    import re
+    assert not hasattr(L, "hattn_set_dependent_launch")
+    with open(HEADER) as f:
+        hdr = f.read()
+    assert re.search(r"#define\s+HATTN_LAUNCH_DEPENDENT\s+1\b", hdr)
+    for name in ["hattn_indexer_scores_ex", "hattn_indexer_scores_fp8", "hattn_topk_select",
+                 "hattn_hybrid_attn", "hattn_lse_merge_splits"]:
+        decl = re.search(name + r"\(([^;]*)\);", hdr).group(1)
+        params = [x.strip() for x in decl.split(",")]
+        assert params[-2] == "int flags" and params[-1].startswith("hattn_stream_t"), name
+    N = None
+    rc = L.hattn_indexer_scores_ex(FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 128, 100, 4, 0, -1, FAKE, 4,
+                                   N)
+    assert rc == hattn.INVALID_ARG and "flags" in _err(L)
 
 
 def test_fp8_key_validation(L):
@@ -129,17 +173,17 @@ def test_fp8_key_validation(L):
     s = None
     # FP8 indexer keys are one 128-byte row: dI = 64 is rejected before any launch
     rc = L.hattn_indexer_scores_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 100, 4, 0, -1,
-                                    FAKE, s)
+                                    FAKE, 0, s)
     assert rc == hattn.INVALID_ARG and "dI = 128" in _err(L)
     rc = L.hattn_indexer_scores_fp8(FAKE, FAKE, FAKE, N, FAKE, 1, 1, 64, 128, 100, 4, 0, -1,
-                                    FAKE, s)
+                                    FAKE, 0, s)
     assert rc == hattn.INVALID_ARG and "ik_scale" in _err(L)
     # the scales travel in 16-byte rows: N_cap a multiple of 4
     rc = L.hattn_indexer_scores_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 128, 102, 4, 0, -1,
-                                    FAKE, s)
+                                    FAKE, 0, s)
     assert rc == hattn.INVALID_ARG and "N_cap % 4" in _err(L)
     rc = L.hattn_indexer_scores_fp8(FAKE, FAKE, FAKE, MISAL, FAKE, 1, 1, 64, 128, 100, 4, 0, -1,
-                                    FAKE, s)
+                                    FAKE, 0, s)
     assert rc == hattn.MISALIGNED
     # the compressor's FP8 key needs both the codes and the scales
     rc = L.hattn_csa_compress_fp8(FAKE, FAKE, FAKE, N, 1, 64, 64, 32, 4, 8, 16, 1e4, 1e-6, 0, 4,
@@ -269,12 +313,12 @@ def test_merge_splits_validation(L):
     N = None
     arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
     ns = (ctypes.c_int * 2)(100, 40)
-    rc = L.hattn_lse_merge_splits(arr, arr, ns, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
+    rc = L.hattn_lse_merge_splits(arr, arr, ns, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, 0, N)
     assert rc == hattn.INVALID_ARG and "partials" in _err(L)
     ns = (ctypes.c_int * 2)(3, 0)
-    rc = L.hattn_lse_merge_splits(arr, arr, ns, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
+    rc = L.hattn_lse_merge_splits(arr, arr, ns, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, 0, N)
     assert rc == hattn.INVALID_ARG and "nsplit" in _err(L)
-    rc = L.hattn_lse_merge_splits(arr, arr, N, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, N)
+    rc = L.hattn_lse_merge_splits(arr, arr, N, 2, N, FAKE, 1, 1, 1, 64, 0, 1e4, FAKE, N, 0, N)
     assert rc == hattn.INVALID_ARG
 
 
@@ -282,9 +326,9 @@ def test_fused_attention_validation_and_sizes(L):
     N = None
     # hattn_hybrid_attn(q, gamma_q, q_prepped, kv_c, idx, N_c, k, kv_h, N_h, m, kv_w, W, pos,
     #                   B, T, H, D, r, rope_base, eps, scale, segments, n_sms, o, lse, ws,
-    #                   ws_bytes, stream)
+    #                   ws_bytes, flags, stream)
     args = [FAKE, N, 1, FAKE, FAKE, 1000, 64, FAKE, 100, 128, FAKE, 128, FAKE,
-            2, 1, 128, 512, 64, 1e4, 1e-6, 0.04, 7, 0, FAKE, FAKE, FAKE, 1 << 30, N]
+            2, 1, 128, 512, 64, 1e4, 1e-6, 0.04, 7, 0, FAKE, FAKE, FAKE, 1 << 30, 0, N]
     bad = list(args)
     bad[10] = N  # no SWA key buffer
     assert L.hattn_hybrid_attn(*bad) == hattn.INVALID_ARG and "kv_w" in _err(L)

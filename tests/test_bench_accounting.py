@@ -17,16 +17,20 @@ W = synth.WORKLOADS
 
 def test_indexer_bytes_decode_1m():
     """One indexer launch at 1M context, batch 8: per (sequence, entry) a
-    256 B bf16 key (or 128 B of E4M3 codes plus a 4 B scale) and a 4 B
-    score; per sequence the 64 x 128 bf16 query rows and 64 fp32 weights."""
+    256 B bf16 key (or 128 B of E4M3 codes plus a 4 B scale); per sequence
+    the 64 x 128 bf16 query rows and 64 fp32 weights.  The 4 B score written
+    per (query, entry) is implementation overhead, counted apart."""
     wl = W["hybrid_decode_1m"]
     entries = 8 * 262144
     queries = 8 * (64 * 128 * 2 + 64 * 4)
-    assert bench.indexer_bytes(wl, "bf16") == entries * (256 + 4) + queries == 545_392_640
-    assert bench.indexer_bytes(wl, "fp8") == entries * (128 + 4 + 4) + queries == 285_345_792
-    # two queries per sequence: one key scan, a score per query
+    assert queries == 133_120
+    assert bench.indexer_bytes(wl, "bf16") == entries * 256 + queries == 536_870_912 + 133_120
+    assert bench.indexer_bytes(wl, "fp8") == entries * (128 + 4) + queries == 276_957_184
+    assert bench.indexer_overhead_bytes(wl) == entries * 4
+    # two queries per sequence: one key scan, the query rows twice, a score per query
     wl2 = W["hybrid_decode_1m_mtp2"]
-    assert bench.indexer_bytes(wl2, "bf16") == entries * (256 + 8) + 2 * queries
+    assert bench.indexer_bytes(wl2, "bf16") == entries * 256 + 2 * queries
+    assert bench.indexer_overhead_bytes(wl2) == entries * 8
 
 
 def test_step_bytes_decode_1m():
@@ -95,8 +99,10 @@ def test_roofline_decode_indexer():
         assert rf["unit"] == "GB/s" and rf["peak"] == 6482.7
         assert rf["achieved"] == pytest.approx(ib / 1e-4 / 1e9)
         assert rf["frac"] == pytest.approx(rf["achieved"] / 6482.7)
-        if rf["traffic"] is not None:  # scaled from the recorded capture
-            assert 0.95 < rf["traffic"] / ib < 1.05
+        assert rf["overhead_bytes_per_launch"] == bench.indexer_overhead_bytes(wl)
+        if rf["traffic"] is not None:  # scaled from the recorded capture (scores included)
+            tot = ib + rf["overhead_bytes_per_launch"]
+            assert 0.95 < rf["traffic"] / tot < 1.05
     # the capture is of one query per sequence: none for two
     rf2 = bench.kernel_roofline(W["hybrid_decode_1m_mtp2"], "bf16", {"indexer": 0.1}, 6482.7,
                                 "measured")
@@ -110,7 +116,8 @@ def test_roofline_hca_decode_reports_both_fractions():
     assert rf["bound"] == "hbm" and rf["algorithmic_bytes_per_launch"] == by
     assert rf["achieved"] == pytest.approx(by / 0.085e-3 / 1e9)
     t = rf["tensor"]
-    assert t["unit"] == "TFLOP/s" and t["peak"] == bench.measured_bf16_sustained()
+    # a decode step lasts microseconds: the burst peak
+    assert t["unit"] == "TFLOP/s" and t["peak"] == bench.measured_bf16_burst()[0]
     assert t["flops_per_launch"] == 16 * 4 * 128 * 512 * 8192
 
 
@@ -121,10 +128,33 @@ def test_roofline_prefill_takes_the_slowest_call():
     fl = bench.step_flops(wl)
     assert rf["bound"] == "tensor" and rf["kernel"] == "attn_kernel<kSparse>"
     assert rf["achieved"] == pytest.approx(fl["sparse"] / 3.0e-3 / 1e12)
-    assert rf["peak"] == bench.measured_bf16_sustained()
+    # a prefill pass lasts milliseconds: the burst peak, not the seconds-long sustained one
+    assert rf["peak"] == bench.measured_bf16_burst()[0]
     assert set(rf["by_call"]) == {"indexer", "sparse", "swa"}
     rh = bench.kernel_roofline(W["hca_prefill"], "bf16", {"hca": 14.7}, 6482.7, "measured")
     assert rh["kernel"] == "attn_kernel<kHca>"
+
+
+def test_l2_note_is_true_per_workload():
+    """Decode: the step's algorithmic input exceeds L2.  Prefill: the
+    streamed queries exceed L2 while the compressed caches are L2-resident
+    by design, and the note says so rather than calling the input larger."""
+    assert "> 126 MB L2 (no flush)" in bench.l2_note(W["hybrid_decode_1m"])
+    for name, cache_mb in (("flash_csa_prefill", 2.6), ("hca_prefill", 8.4)):
+        note = bench.l2_note(W[name])
+        assert "L2-resident" in note and f"({cache_mb:.1f} MB)" in note, note
+
+
+def test_timed_replays_split_the_steps():
+    """The K timed steps run as R separately timed replays of one graph of
+    K / R steps (R up to 10), so the line carries a median and a spread."""
+    assert bench.timed_replays(50) == (10, 5)
+    assert bench.timed_replays(20) == (10, 2)
+    assert bench.timed_replays(7) == (7, 1)
+    assert bench.timed_replays(1) == (1, 1)
+    for k in range(1, 101):
+        r, g = bench.timed_replays(k)
+        assert r * g == k and 1 <= r <= 10
 
 
 def test_traffic_profile_is_committed():

@@ -354,6 +354,49 @@ def test_topk_exact_with_ties(N_cap, k):
         assert (got[b, 0] == -1).sum() == (ref_idx[b, 0] == -1).sum()
 
 
+def _topk_ref_check(scores, pos, k, m, idx):
+    """The oracle's selection over the same fp32 scores: identical sets."""
+    ref_idx = orc.topk(scores.cpu().numpy().astype(np.float64), pos.cpu().numpy(), m, k)
+    got = idx.cpu().numpy()
+    for r in range(got.shape[0] * got.shape[1]):
+        g, rf = got.reshape(-1, k)[r], ref_idx.reshape(-1, k)[r]
+        assert sorted(g[g >= 0].tolist()) == sorted(rf[rf >= 0].tolist()), r
+        n_pad = int((rf == -1).sum())
+        assert (g == -1).sum() == n_pad, r
+        assert (g[len(g) - n_pad:] == -1).all(), r
+
+
+@pytest.mark.parametrize("B,N_cap,k", [(4, 100000, 1024), (3, 40000, 2048), (300, 3000, 512)])
+def test_topk_select_edge_cases(B, N_cap, k):
+    """Both selection paths (few long rows spread over many CTAs; many rows
+    one CTA each) on scores built to hit their corners, against the oracle's
+    selection over the same fp32 values: a row of one repeated value (every
+    entry ties, the smallest indices win), a row with fewer visible entries
+    than k (all of them, then -1), ties straddling the threshold, signed
+    zeros, and a row of distinct random values."""
+    g = torch.Generator().manual_seed(31)
+    sc = torch.randn((B, 1, N_cap), generator=g)
+    sc[0, 0] = 1.5                                   # all tie
+    if B > 1:
+        sc[1, 0, : 2 * k] = torch.randint(0, 3, (2 * k,), generator=g).float()  # few values
+        sc[1, 0, 2 * k:] = -1.0
+    if B > 2:
+        v = torch.randn((N_cap,), generator=g)
+        top = v.topk(k).values[-1]
+        v[v.abs() < 0.01] = -0.0                     # signed zeros
+        v[: 3 * k: 3] = top                          # ties at the threshold
+        sc[2, 0] = v
+    pos = torch.full((B, 1), 4 * N_cap - 1, dtype=torch.int32)
+    if B > 3:
+        pos[3, 0] = 4 * (k // 2) + 2                 # k // 2 visible entries
+    d_sc, d_pos = sc.to(DEV), pos.to(DEV)
+    idx = hattn.topk_select(d_sc, d_pos, k=k, m=4)
+    idx2 = hattn.topk_select(d_sc, d_pos, k=k, m=4, dependent=True)  # twice: reused scratch
+    hattn.check_status()
+    _topk_ref_check(sc, pos, k, 4, idx)
+    assert torch.equal(idx.sort(dim=-1).values, idx2.sort(dim=-1).values)
+
+
 def test_topk_without_score_output_uses_workspace():
     B, T, HI, dI, N = 1, 1, 64, 128, 2048
     iq = randn_bf16((B, T, HI, dI), 40).to(DEV)
@@ -691,24 +734,20 @@ def test_dependent_launch_chain_matches_plain_launch():
     kv_w = hattn.swa_keys(raw, pos, r=r, W=128)
     torch.cuda.synchronize()
 
-    def chain():
-        sc = hattn.indexer_scores(iq, w, ik, pos, m=4)
-        idx = hattn.topk_select(sc, pos, k=k, m=4)
+    def chain(dep):
+        sc = hattn.indexer_scores(iq, w, ik, pos, m=4, dependent=dep)
+        idx = hattn.topk_select(sc, pos, k=k, m=4, dependent=dep)
         # the selection comes in no fixed order; sorted, both runs attend to
         # the entries in the same order (and the attention waits for the sort)
         idx_s = idx.sort(dim=-1).values
         part = hattn.hybrid_attn(qt, kv_c, idx_s, kv_h, kv_w, pos, r=r, q_prepped=True,
-                                 partials=True)
-        out, lse = hattn.lse_merge_splits([part], pos, r=r, H=H, sink=sink)
+                                 partials=True, dependent=dep)
+        out, lse = hattn.lse_merge_splits([part], pos, r=r, H=H, sink=sink, dependent=dep)
         return sc, idx_s, out, lse
 
-    plain = [t.clone() for t in chain()]
+    plain = [t.clone() for t in chain(False)]
     torch.cuda.synchronize()
-    prev = hattn.set_dependent_launch(True)
-    try:
-        dep = [t.clone() for t in chain()]
-    finally:
-        hattn.set_dependent_launch(prev)
+    dep = [t.clone() for t in chain(True)]
     torch.cuda.synchronize()
     hattn.check_status()
     sc0, idx0, out0, lse0 = plain

@@ -1,9 +1,9 @@
 """hattn_indexer_topk_noalloc: the indexer top-k for callers that cannot
 allocate device memory (an engine with its own fixed pool, a plugin host that
-forbids device allocations).  Its score scratch is an array compiled into the
-library, so the call must give the same selection as hattn_indexer_topk with
-a caller-provided workspace, call after call, and refuse requests larger than
-that array.
+forbids device allocations).  Its score and selection scratch is an array
+compiled into the library, so the call must give the same selection as
+hattn_indexer_topk with a caller-provided workspace, call after call, and
+refuse requests larger than that array.
 
 This file is collected last, so a run that stops at the first failure has
 already run every other test; it passes alone and after the other tests."""
@@ -60,3 +60,22 @@ def test_noalloc_matches_workspace_call_twice(L):
         ref = np.sort(ref.cpu().numpy(), axis=-1)
         np.testing.assert_array_equal(got, ref)
         assert (got >= 0).all()
+
+
+@pytest.mark.gpu
+def test_noalloc_back_to_back_and_on_every_device(L):
+    """Calls queued back to back on one stream, with no synchronisation in
+    between, each see only their own scores: the second call's scores land
+    in the shared scratch after the first call's selection has read it
+    (stream order).  Where more than one GPU is visible, the same holds with
+    each device current (each device has its own copy of the scratch)."""
+    for dev in range(torch.cuda.device_count()):
+        with torch.cuda.device(dev):
+            runs = [_inputs(8, 1, 64, 128, 65536, 10 + i) for i in range(2)]
+            runs = [tuple(t.to(f"cuda:{dev}") for t in r) for r in runs]
+            got = [hattn.indexer_topk_noalloc(*r, k=1024) for r in runs]
+            ref = [hattn.indexer_topk(*r, k=1024) for r in runs]
+            hattn.check_status()
+            for g_, r_ in zip(got, ref):
+                np.testing.assert_array_equal(np.sort(g_.cpu().numpy(), axis=-1),
+                                              np.sort(r_.cpu().numpy(), axis=-1))

@@ -104,6 +104,15 @@ __device__ __forceinline__ uint4 pack8(const float (&y)[8]) {
   return u;
 }
 
+__device__ __forceinline__ uint4 pack8_f16(const float (&y)[8]) {
+  uint4 u;
+  u.x = pack_f16x2(y[0], y[1]);
+  u.y = pack_f16x2(y[2], y[3]);
+  u.z = pack_f16x2(y[4], y[5]);
+  u.w = pack_f16x2(y[6], y[7]);
+  return u;
+}
+
 __device__ __forceinline__ float sumsq8(const uint4& u) {
   float x[8];
   unpack8(u, x);
@@ -205,6 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The SWA branch normalises and ropes its keys in this kernel, so their
+  // products run in fp16 (11 significant bits): Q is converted once, the
+  // normalised keys and P are rounded to fp16 rather than bf16.  Every other
+  // kind reads bf16 caches and runs in bf16.
+  constexpr bool kF16 = KIND == kSwa;
   pdl_trigger();  // the merge may begin launching as SMs free up
   const int dh = blockIdx.x % a.nds;
   const int split = blockIdx.x / a.nds;
@@ -522,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int z = 0; z < 8; ++z) y[z] = 0.f;
               }
-              *cell = pack8(y);
+              *cell = kF16 ? pack8_f16(y) : pack8(y);
             }
           }
           fence_proxy_async_smem();
@@ -560,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (ok && n_other > 0)
+      if (ok && (n_other > 0 || kF16))
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_tmem), 0, abort, a.status,
                                                kWaitLimitNs, 34));
       if (lane == 0) mbar_arrive(smem_u32(&sm->q_ready));  // also on failure: abort is set
@@ -571,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = ok && !*abort;
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    const uint32_t idesc_qk = idesc_bf16(128, 64, 0, 0);
+    const uint32_t idesc_qk = kF16 ? idesc_f16(128, 64, 0, 0) : idesc_bf16(128, 64, 0, 0);
     const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sRing);
     for (int i = par; i < nt && ok; i += 2) {
       int seg, nvalid;
@@ -646,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O += P(i) V(i): P from tensor memory (S/P buffer i & 1), V = the n_own
     // chunks of tile i, consecutive ring slots (the ring holds a whole number
     // of such groups), read as one MN-major operand of N = ocols
-    const uint32_t idesc_pv = idesc_bf16(128, ocols, 0, 1);
+    const uint32_t idesc_pv = kF16 ? idesc_f16(128, ocols, 0, 1) : idesc_bf16(128, ocols, 0, 1);
     const uint32_t sRa = smem_u32(sRing);
     bool ok = true;
     for (int i = 0; i < nt && ok; ++i) {
@@ -695,11 +709,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t tq = row_valid ? a.pos[(int64_t)b * a.T + t0 + g] : 0;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     bool ok = true;
-    if (n_other > 0) {
+    if (n_other > 0 || kF16) {
       // the other half of this row's q~ into tensor memory (zeros for rows
-      // that are not this block's)
+      // that are not this block's); with fp16 products, this row of the own
+      // half is converted in shared memory too (the QK issuer zeroes the
+      // rows past the block's, these threads convert the others)
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_full), 0, abort, a.status,
                                              kWaitLimitNs, 35));
+      if (kF16 && row_valid && ok) {
+        for (int e = 0; e < n_own; ++e)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint4* cell = reinterpret_cast<uint4*>(sQ + e * 16384 + swz128(rI, q));
+            *cell = bf16x8_to_f16x8(*cell);
+          }
+        fence_proxy_async_smem();  // the tensor core reads these rows
+      }
       for (int e = 0; e < n_other; ++e) {
         float w[32];
 #pragma unroll
@@ -707,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 u = make_uint4(0, 0, 0, 0);
           if (row_valid && ok)
             u = *reinterpret_cast<const uint4*>(sQstage + e * 16384 + swz128(rI, q));
+          if (kF16) u = bf16x8_to_f16x8(u);
           w[4 * q] = __uint_as_float(u.x);
           w[4 * q + 1] = __uint_as_float(u.y);
           w[4 * q + 2] = __uint_as_float(u.z);
@@ -714,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tQ + lane_base + e * 32, w);
       }
-      tmem_wait_st();
+      if (n_other > 0) tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm->q_tmem));
     }
@@ -825,9 +851,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 64; c += 2) {
         const float p0 = ex2_fast(fmaf(s[c], sl2, moff));
         const float p1 = ex2_fast(fmaf(s[c + 1], sl2, moff));
-        const uint32_t u = pack_bf16x2(p0, p1);
-        l4[(c >> 1) & 3] += __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
-        pk[c >> 1] = __uint_as_float(u);
+        if (kF16) {
+          const uint32_t u = pack_f16x2(p0, p1);
+          const float2 f = unpack_f16x2(u);
+          l4[(c >> 1) & 3] += f.x + f.y;
+          pk[c >> 1] = __uint_as_float(u);
+        } else {
+          const uint32_t u = pack_bf16x2(p0, p1);
+          l4[(c >> 1) & 3] += __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
+          pk[c >> 1] = __uint_as_float(u);
+        }
       }
       l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
       tmem_st32(tS + lane_base + sb * 64, pk);

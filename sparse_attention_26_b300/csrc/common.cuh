@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -387,6 +388,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor, kind::f16 with fp16 A/B and fp32 D (formats 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(a_mn) << 15)       // A major
+         | (static_cast<uint32_t>(b_mn) << 16)       // B major
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // Instruction descriptor, kind::f8f6f4 with E4M3 A/B (format code 0), fp32
 // D, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
@@ -452,6 +462,34 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two fp32 values to fp16, nearest even, saturating at +-65504: `lo` in
+// bits 0-15, `hi` in bits 16-31.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two packed fp16 values (as pack_f16x2 lays them out) back to fp32.
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
+  __half2 h = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(h);
+}
+
+// Eight bf16 values (16 bytes) to eight fp16 values, in place of each pair;
+// exact for magnitudes in fp16's normal range, saturating beyond it.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  uint4 r;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    o[i] = pack_f16x2(f.x, f.y);
+  }
+  return r;
 }
 
 // RoPE coefficients of one call, computed on the host in fp64: for pair i,

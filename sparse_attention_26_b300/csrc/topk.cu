@@ -318,11 +318,19 @@ __global__ void __launch_bounds__(1024) topk_row_kernel(const TopkArgs a) {
 }
 
 // ============================================================ slice path
+constexpr int kListCap = 2048;   // per-CTA shared-memory lists of the pick sweep
+constexpr int kLoadBatch = 8;    // float4 loads a thread issues before using them
+constexpr int kCandSmem = 8192;  // candidates the last CTA ranks in shared memory
+
 struct SliceShared {
   ScanShared scan;
   uint32_t hist[kBins];
+  int n_up, n_in;        // fills of the two lists
+  int base_up, base_in;  // their ranges in the row's output and candidate list
   int last;
   int n_gt, n_eq;
+  int32_t up[kListCap];  // entries above the threshold bin (selected)
+  int32_t in[kListCap];  // entries in the threshold bin (candidates)
 };
 
 // Histogram of the top 11 key bits of this CTA's slice, into its own bins.
@@ -345,28 +353,128 @@ __global__ void __launch_bounds__(kPickThreads) topk_hist_kernel(const TopkArgs 
   if (hi <= lo) {
     // nothing visible in this slice
   } else if (a.vec4) {
-    // slices start at multiples of 4 and rows are 16-byte aligned
+    // slices start at multiples of 4 and rows are 16-byte aligned; each
+    // thread issues up to kLoadBatch float4 loads before using any of them
     const int64_t q_hi = hi >> 2;
-    for (int64_t q = (lo >> 2) + tid; q < q_hi; q += kPickThreads) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(src) + q);
-      atomicAdd(&hist[order_key(v.x) >> 21], 1u);
-      atomicAdd(&hist[order_key(v.y) >> 21], 1u);
-      atomicAdd(&hist[order_key(v.z) >> 21], 1u);
-      atomicAdd(&hist[order_key(v.w) >> 21], 1u);
+    for (int64_t q0 = (lo >> 2) + tid; q0 < q_hi; q0 += kLoadBatch * kPickThreads) {
+      float4 v[kLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int64_t q = q0 + static_cast<int64_t>(u) * kPickThreads;
+        v[u] = q < q_hi ? __ldcg(reinterpret_cast<const float4*>(src) + q)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        if (q0 + static_cast<int64_t>(u) * kPickThreads >= q_hi) break;
+        atomicAdd(&hist[order_key(v[u].x) >> 21], 1u);
+        atomicAdd(&hist[order_key(v[u].y) >> 21], 1u);
+        atomicAdd(&hist[order_key(v[u].z) >> 21], 1u);
+        atomicAdd(&hist[order_key(v[u].w) >> 21], 1u);
+      }
     }
     for (int64_t e = (q_hi << 2) + tid; e < hi; e += kPickThreads)
-      atomicAdd(&hist[order_key(src[e]) >> 21], 1u);
+      atomicAdd(&hist[order_key(__ldcg(src + e)) >> 21], 1u);
   } else {
     for (int64_t e = lo + tid; e < hi; e += kPickThreads)
-      atomicAdd(&hist[order_key(src[e]) >> 21], 1u);
+      atomicAdd(&hist[order_key(__ldcg(src + e)) >> 21], 1u);
   }
   __syncthreads();
   uint16_t* dst = a.hist + (row * a.S + s) * kBins;
   for (int i = tid; i < kBins; i += kPickThreads) dst[i] = static_cast<uint16_t>(hist[i]);
 }
 
+// The ranking of the row's candidates by its last CTA: `need` more entries
+// are taken from the C candidates (all in the threshold bin d0), written to
+// rest[0 .. need).  idx_of(c) / key_of(c) give candidate c's entry index and
+// order-preserving key.
+template <class IdxOf, class KeyOf>
+__device__ __forceinline__ void rank_candidates(int C, uint32_t need, uint32_t d0, int32_t* rest,
+                                                SliceShared& sh, IdxOf idx_of, KeyOf key_of) {
+  const int tid = threadIdx.x;
+  const int room = static_cast<int>(need);
+  // the two remaining digits of the need-th largest candidate key
+  uint32_t prefix = d0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int width = pass == 0 ? 11 : 10;
+    const int shift = pass == 0 ? 10 : 0;
+    const int nb = 1 << width;
+    for (int i = tid; i < kBins; i += kPickThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int c = tid; c < C; c += kPickThreads) {
+      const uint32_t key = key_of(c);
+      if ((key >> (shift + width)) == prefix) atomicAdd(&sh.hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    find_digit_desc(sh.hist, nb, need, &sh.scan, tid, kPickThreads);
+    prefix = (prefix << width) | sh.scan.digit;
+    need -= sh.scan.above;
+  }
+  const uint32_t thr = prefix;  // the k-th largest key; `need` of its ties are taken
+  // candidates above the threshold, and the count of ties at it (the loop
+  // runs the same trip count in every thread: warp_append is warp-collective)
+  if (tid == 0) {
+    sh.n_gt = 0;
+    sh.n_eq = 0;
+  }
+  __syncthreads();
+  int eq = 0;
+  for (int c0 = 0; c0 < C; c0 += kPickThreads) {
+    const int c = c0 + tid;
+    const uint32_t key = c < C ? key_of(c) : 0u;
+    const bool gt = c < C && key > thr;
+    const int p = warp_append(&sh.n_gt, gt);  // shared-memory counter
+    if (gt && p < room) rest[p] = idx_of(c);
+    eq += c < C && key == thr;
+  }
+  if (eq) atomicAdd(&sh.n_eq, eq);
+  __syncthreads();
+  const int n_gt = sh.n_gt;
+  const uint32_t n_eq = static_cast<uint32_t>(sh.n_eq);
+  // ties at the threshold: the need smallest entry indices among them (every
+  // tie when they are exactly the places left).  Radix select on the index
+  // value, smallest first, finds the need-th smallest tie index ti.
+  uint32_t ti = 0xffffffffu;
+  if (n_eq != need) {
+    uint32_t ip = 0, left = need;
+    for (int pass = 0; pass < 3; ++pass) {
+      const int width = pass == 2 ? 10 : 11;
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const int nb = 1 << width;
+      for (int i = tid; i < kBins; i += kPickThreads) sh.hist[i] = 0;
+      __syncthreads();
+      for (int c = tid; c < C; c += kPickThreads) {
+        if (key_of(c) != thr) continue;
+        const uint32_t j = static_cast<uint32_t>(idx_of(c));
+        if (pass > 0 && (j >> (shift + width)) != ip) continue;
+        atomicAdd(&sh.hist[(j >> shift) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      find_digit_asc(sh.hist, nb, left, &sh.scan, tid, kPickThreads);
+      ip = (ip << width) | sh.scan.digit;
+      left -= sh.scan.above;
+    }
+    ti = ip;  // indices are distinct: the ties with index <= ti are exactly `need`
+  }
+  if (tid == 0) sh.n_gt = 0;
+  __syncthreads();
+  int32_t* ties_out = rest + n_gt;
+  for (int c0 = 0; c0 < C; c0 += kPickThreads) {
+    const int c = c0 + tid;
+    bool take = false;
+    int32_t j = 0;
+    if (c < C && key_of(c) == thr) {
+      j = idx_of(c);
+      take = static_cast<uint32_t>(j) <= ti;
+    }
+    const int p = warp_append(&sh.n_gt, take);
+    if (take && n_gt + p < room) ties_out[p] = j;
+  }
+}
+
 __global__ void __launch_bounds__(kPickThreads) topk_pick_kernel(const TopkArgs a) {
   __shared__ SliceShared sh;
+  extern __shared__ __align__(16) uint8_t pick_dyn[];  // the last CTA's candidates
   const int tid = threadIdx.x;
   const int s = blockIdx.x;
   const int64_t row = static_cast<int64_t>(blockIdx.y) + static_cast<int64_t>(gridDim.y) * blockIdx.z;
@@ -385,11 +493,23 @@ __global__ void __launch_bounds__(kPickThreads) topk_pick_kernel(const TopkArgs 
     return;
   }
   // the row's histogram: the sum of its S slices' bins
+  // (each thread sums its bins over the slices with up to 16 loads in
+  // flight at once: the loads do not wait on one another)
   const uint16_t* rh = a.hist + row * a.S * kBins;
   for (int i = tid; i < kBins; i += kPickThreads) {
     uint32_t c = 0;
-    for (int q = 0; q < a.S; ++q) c += rh[q * kBins + i];
+    for (int q0 = 0; q0 < a.S; q0 += 16) {
+      uint16_t h[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) h[u] = q0 + u < a.S ? __ldcg(rh + (q0 + u) * kBins + i) : 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) c += h[u];
+    }
     sh.hist[i] = c;
+  }
+  if (tid == 0) {
+    sh.n_up = 0;
+    sh.n_in = 0;
   }
   __syncthreads();
   find_digit_desc(sh.hist, kBins, static_cast<uint32_t>(a.k), &sh.scan, tid, kPickThreads);
@@ -398,18 +518,67 @@ __global__ void __launch_bounds__(kPickThreads) topk_pick_kernel(const TopkArgs 
   int* ctr = a.ctr + row * 4;              // [0] above appended, [1] candidates, [2] tickets
   int32_t* cand = a.cand + row * a.N_cap;
   const float* src = a.scores + row * a.N_cap;
-  // sweep the slice: above the bin -> output, in the bin -> candidates
-  for (int64_t e0 = lo; e0 < hi; e0 += kPickThreads) {
-    const int64_t e = e0 + tid;
-    uint32_t d = 0;
-    if (e < hi) d = order_key(src[e]) >> 21;
-    const bool up = e < hi && d > d0;
-    const bool in = e < hi && d == d0;
-    const int p_up = warp_append(&ctr[0], up);
-    const int p_in = warp_append(&ctr[1], in);
-    if (up && p_up < a.k) out[p_up] = static_cast<int32_t>(e);
-    if (in && p_in < a.N_cap) cand[p_in] = static_cast<int32_t>(e);
+  // Sweep the slice: above the bin -> the output, in the bin -> the
+  // candidates.  Both go to shared-memory lists first (a slice holds few of
+  // either), then one global reservation per list; entries beyond a list's
+  // capacity (a slice of near-equal scores) are appended one by one.
+  auto place = [&](int64_t e, float v) {
+    const uint32_t d = order_key(v) >> 21;
+    if (d > d0) {
+      const int p = atomicAdd(&sh.n_up, 1);
+      if (p < kListCap) {
+        sh.up[p] = static_cast<int32_t>(e);
+      } else {
+        const int q = atomicAdd(&ctr[0], 1);
+        if (q < a.k) out[q] = static_cast<int32_t>(e);
+      }
+    } else if (d == d0) {
+      const int p = atomicAdd(&sh.n_in, 1);
+      if (p < kListCap) {
+        sh.in[p] = static_cast<int32_t>(e);
+      } else {
+        const int q = atomicAdd(&ctr[1], 1);
+        if (q < a.N_cap) cand[q] = static_cast<int32_t>(e);
+      }
+    }
+  };
+  if (hi <= lo) {
+    // nothing visible in this slice
+  } else if (a.vec4) {
+    const int64_t q_hi = hi >> 2;
+    for (int64_t q0 = (lo >> 2) + tid; q0 < q_hi; q0 += kLoadBatch * kPickThreads) {
+      float4 v[kLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int64_t q = q0 + static_cast<int64_t>(u) * kPickThreads;
+        v[u] = q < q_hi ? __ldcg(reinterpret_cast<const float4*>(src) + q)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int64_t q = q0 + static_cast<int64_t>(u) * kPickThreads;
+        if (q >= q_hi) break;
+        place(4 * q, v[u].x);
+        place(4 * q + 1, v[u].y);
+        place(4 * q + 2, v[u].z);
+        place(4 * q + 3, v[u].w);
+      }
+    }
+    for (int64_t e = (q_hi << 2) + tid; e < hi; e += kPickThreads) place(e, __ldcg(src + e));
+  } else {
+    for (int64_t e = lo + tid; e < hi; e += kPickThreads) place(e, __ldcg(src + e));
   }
+  __syncthreads();
+  const int nu = min(sh.n_up, kListCap), ni = min(sh.n_in, kListCap);
+  if (tid == 0) {
+    sh.base_up = nu ? atomicAdd(&ctr[0], nu) : 0;
+    sh.base_in = ni ? atomicAdd(&ctr[1], ni) : 0;
+  }
+  __syncthreads();
+  for (int i = tid; i < nu; i += kPickThreads)
+    if (sh.base_up + i < a.k) out[sh.base_up + i] = sh.up[i];
+  for (int i = tid; i < ni; i += kPickThreads)
+    if (sh.base_in + i < a.N_cap) cand[sh.base_in + i] = sh.in[i];
   // the last CTA of the row to get here ranks the candidates
   __threadfence();
   __syncthreads();
@@ -418,94 +587,41 @@ __global__ void __launch_bounds__(kPickThreads) topk_pick_kernel(const TopkArgs 
   if (!sh.last) return;
   __threadfence();
   const int C = min(__ldcg(&ctr[1]), static_cast<int>(a.N_cap));
-  uint32_t need = static_cast<uint32_t>(a.k) - n_above;  // 1 <= need <= C
-  const int room = static_cast<int>(need);               // places left in the output
+  const uint32_t need = static_cast<uint32_t>(a.k) - n_above;  // 1 <= need <= C
   int32_t* rest = out + n_above;
   if (static_cast<int>(need) >= C) {
     for (int c = tid; c < C; c += kPickThreads) rest[c] = __ldcg(cand + c);
     return;
   }
-  // the two remaining digits of the need-th largest candidate key
-  uint32_t prefix = d0;
-  for (int pass = 0; pass < 2; ++pass) {
-    const int width = pass == 0 ? 11 : 10;
-    const int shift = pass == 0 ? 10 : 0;
-    const int nb = 1 << width;
-    for (int i = tid; i < kBins; i += kPickThreads) sh.hist[i] = 0;
-    __syncthreads();
-    for (int c = tid; c < C; c += kPickThreads) {
-      const uint32_t key = order_key(src[__ldcg(cand + c)]);
-      if ((key >> (shift + width)) == prefix) atomicAdd(&sh.hist[(key >> shift) & (nb - 1)], 1u);
-    }
-    __syncthreads();
-    find_digit_desc(sh.hist, nb, need, &sh.scan, tid, kPickThreads);
-    prefix = (prefix << width) | sh.scan.digit;
-    need -= sh.scan.above;
-  }
-  const uint32_t thr = prefix;  // the k-th largest key; `need` of its ties are taken
-  // candidates above the threshold, and the count of ties at it (the loops
-  // run the same trip count in every thread: warp_append is warp-collective)
-  if (tid == 0) {
-    sh.n_gt = 0;
-    sh.n_eq = 0;
-  }
-  __syncthreads();
-  int eq = 0;
-  for (int c0 = 0; c0 < C; c0 += kPickThreads) {
-    const int c = c0 + tid;
-    int32_t j = 0;
-    uint32_t key = 0;
-    if (c < C) {
-      j = __ldcg(cand + c);
-      key = order_key(src[j]);
-    }
-    const bool gt = c < C && key > thr;
-    const int p = warp_append(&sh.n_gt, gt);  // shared-memory counter
-    if (gt && p < room) rest[p] = j;
-    eq += c < C && key == thr;
-  }
-  if (eq) atomicAdd(&sh.n_eq, eq);
-  __syncthreads();
-  const int n_gt = sh.n_gt;
-  const uint32_t n_eq = static_cast<uint32_t>(sh.n_eq);
-  int32_t* ties_out = rest + n_gt;
-  // ties at the threshold: the need smallest entry indices among them (every
-  // tie when they are exactly the places left).  Radix select on the index
-  // value, smallest first, finds the need-th smallest tie index ti.
-  uint32_t ti = 0xffffffffu;
-  if (n_eq != need) {
-    uint32_t ip = 0, left = need;
-    for (int pass = 0; pass < 3; ++pass) {
-      const int width = pass == 2 ? 10 : 11;
-      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-      const int nb = 1 << width;
-      for (int i = tid; i < kBins; i += kPickThreads) sh.hist[i] = 0;
-      __syncthreads();
-      for (int c = tid; c < C; c += kPickThreads) {
-        const uint32_t j = static_cast<uint32_t>(__ldcg(cand + c));
-        if (order_key(src[j]) != thr) continue;
-        if (pass > 0 && (j >> (shift + width)) != ip) continue;
-        atomicAdd(&sh.hist[(j >> shift) & (nb - 1)], 1u);
+  if (C <= kCandSmem) {
+    // the candidates and their keys into shared memory, in one gather
+    int32_t* cj = reinterpret_cast<int32_t*>(pick_dyn);
+    uint32_t* ck = reinterpret_cast<uint32_t*>(pick_dyn + kCandSmem * 4);
+    for (int c0 = tid; c0 < C; c0 += kLoadBatch * kPickThreads) {
+      int32_t j[kLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int c = c0 + u * kPickThreads;
+        j[u] = c < C ? __ldcg(cand + c) : 0;
       }
-      __syncthreads();
-      find_digit_asc(sh.hist, nb, left, &sh.scan, tid, kPickThreads);
-      ip = (ip << width) | sh.scan.digit;
-      left -= sh.scan.above;
+      float v[kLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) v[u] = __ldcg(src + j[u]);
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int c = c0 + u * kPickThreads;
+        if (c < C) {
+          cj[c] = j[u];
+          ck[c] = order_key(v[u]);
+        }
+      }
     }
-    ti = ip;  // indices are distinct: the ties with index <= ti are exactly `need`
-  }
-  if (tid == 0) sh.n_gt = 0;
-  __syncthreads();
-  for (int c0 = 0; c0 < C; c0 += kPickThreads) {
-    const int c = c0 + tid;
-    int32_t j = 0;
-    bool take = false;
-    if (c < C) {
-      j = __ldcg(cand + c);
-      take = order_key(src[j]) == thr && static_cast<uint32_t>(j) <= ti;
-    }
-    const int p = warp_append(&sh.n_gt, take);
-    if (take && n_gt + p < room) ties_out[p] = j;
+    __syncthreads();
+    rank_candidates(C, need, d0, rest, sh, [&](int c) { return cj[c]; },
+                    [&](int c) { return ck[c]; });
+  } else {
+    rank_candidates(C, need, d0, rest, sh, [&](int c) { return __ldcg(cand + c); },
+                    [&](int c) { return order_key(__ldcg(src + __ldcg(cand + c))); });
   }
 }
 
@@ -599,6 +715,10 @@ cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, bool dependent,
   // the pick kernel reads what the histogram kernel wrote: always a
   // dependent of it (it waits before its first read)
   cfg.numAttrs = add_dependent_attr(at, 0, true);
+  cfg.dynamicSmemBytes = kCandSmem * 8;
+  e = cudaFuncSetAttribute(topk_pick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kCandSmem * 8);
+  if (e != cudaSuccess) return e;
   e = cudaLaunchKernelEx(&cfg, topk_pick_kernel, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

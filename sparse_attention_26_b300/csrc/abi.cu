@@ -412,6 +412,7 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.nsplit = p.nsplit;
   a.keys_per_split = p.keys_per_split;
   a.nds = p.nds;
+  a.n_tq = p.n_tq;
   // the attention kernel is a dependent of the query preparation it follows
   a.dependent = (dependent || !q_prepped) ? 1 : 0;
   cudaError_t e = launch_attention(tm, tm2, tm_q, a, p, st);

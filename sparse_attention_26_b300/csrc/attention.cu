@@ -39,6 +39,7 @@ namespace {
 
 constexpr int kThreads = 352;
 constexpr int kTile = 64;
+constexpr int kNSB = 3;  // S/P buffers in tensor memory (64 columns each)
 constexpr int kMaxSlots = 20;
 constexpr int kProdThreads = 128;
 
@@ -46,10 +47,9 @@ struct AttnShared {
   uint64_t full[kMaxSlots];
   uint64_t raw[kMaxSlots];  // SWA: the TMA copy of a raw chunk has landed
   uint64_t empty[kMaxSlots];
-  uint64_t s_full[2];
-  uint64_t s_free[2];       // PV of the tile that last used this S/P buffer is done
+  uint64_t s_full[kNSB];
+  uint64_t s_free[kNSB];    // PV of the tile that last used this S/P buffer is done
   uint64_t p_full;
-  uint64_t pv_done;
   uint64_t o_full;
   uint64_t q_full;
   uint64_t q_tmem;          // the other half of Q is in tensor memory
@@ -140,18 +140,6 @@ __device__ __forceinline__ void rope8(float (&y)[8], int d_first, int D, int r, 
   }
 }
 
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A (M=128 rows x K=16 bf16) is
-// read from 8 tensor-memory columns, two bf16 per 32-bit column.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Fused kind: one query's keys are three segments of 64-key tiles -- 0: the
 // top-k CSA entries (gathered), 1: the visible HCA entries, 2: the query's W
 // SWA keys (both by TMA).  Split s of nsplit takes tiles
@@ -204,12 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ndc = a.D / 64;                // 64-wide d chunks of a row
   const int n_own = ndc / a.nds;           // chunks of this CTA's output columns
   const int n_other = ndc - n_own;
-  uint8_t* sQ = base;                      // n_own x [128 rows x 128 B]
-  uint8_t* sRing = sQ + n_own * 16384;     // nslot x [64 keys x 128 B]
+  const int n_tq = a.n_tq;                 // chunks of the other half held in tensor memory
+  const int n_sq = n_own + n_other - n_tq; // chunks of Q held in shared memory
+  uint8_t* sQ = base;                      // n_sq x [128 rows x 128 B]: own chunks, then
+                                           // the other half's shared-memory chunks
+  uint8_t* sRing = sQ + n_sq * 16384;      // nslot x [64 keys x 128 B]
   AttnShared* sm = reinterpret_cast<AttnShared*>(sRing + nslot * 8192);
-  // the other half of Q is staged in the last ring slots until it has been
-  // copied into tensor memory
-  const int stage_slot = nslot - 2 * n_other;
+  // the other half's tensor-memory chunks of Q are staged in the last ring
+  // slots until they have been copied into tensor memory
+  const int stage_slot = nslot - 2 * n_tq;
   uint8_t* sQstage = sRing + stage_slot * 8192;
 
   const int warp = threadIdx.x >> 5;
@@ -304,13 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm->raw[i]), 1);
       mbar_init(smem_u32(&sm->empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNSB; ++i) {
       mbar_init(smem_u32(&sm->s_full[i]), 1);
       mbar_init(smem_u32(&sm->s_free[i]), 1);
-      mbar_init(smem_u32(&sm->drain[i]), 1);
     }
+    mbar_init(smem_u32(&sm->drain[0]), 1);
+    mbar_init(smem_u32(&sm->drain[1]), 1);
     mbar_init(smem_u32(&sm->p_full), 128);
-    mbar_init(smem_u32(&sm->pv_done), 1);
     mbar_init(smem_u32(&sm->o_full), 1);
     mbar_init(smem_u32(&sm->q_full), 1);
     mbar_init(smem_u32(&sm->q_tmem), 128);
@@ -335,9 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   const uint32_t tmem = sm->tmem_base;
   volatile int* abort = &sm->abort;
-  const uint32_t tS = tmem;          // columns [0, 128): two 64-column S/P buffers
-  const uint32_t tO = tmem + 128;    // columns [128, 128 + ocols)
-  const uint32_t tQ = tmem + 384;    // nds = 2: the other half of Q, 32 columns per chunk
+  const uint32_t tS = tmem;                  // columns [0, 64 kNSB): the S/P buffers
+  const uint32_t tO = tmem + 64 * kNSB;      // ocols columns
+  const uint32_t tQ = tO + ocols;            // n_tq chunks of the other half of Q, 32 columns each
 
   // The ring holds groups of gsz = n_own consecutive 8 KB chunk slots.  A
   // tile is the group of the other half's d chunks (nds = 2: keys only, free
@@ -347,9 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int gsz = n_own;
   const int ng = nslot / gsz;   // groups in the ring
   const int ngt = ndc / gsz;    // groups per tile: 1 or 2
-  // the other half of Q is staged in the last two groups of the ring until
-  // it has been copied into tensor memory
-  const int64_t stage_group = n_other > 0 ? (nslot - 2 * n_other) / gsz : -1;
+  // the tensor-memory chunks of Q are staged in the last groups of the ring
+  // until they have been copied into tensor memory
+  const int64_t stage_group = n_tq > 0 ? (nslot - 2 * n_tq) / gsz : -1;
   // first d chunk of group q of a tile
   auto group_dc = [&](int q) -> int {
     if (q < ngt - 1) return (dh == 0 ? 1 : 0) * n_own;  // the other half
@@ -557,8 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t qrow0 = static_cast<int32_t>(((int64_t)b * a.T + t0) * a.H);
         for (int dc = 0; dc < ndc; ++dc) {
           const int e = dc - dh * n_own;  // own chunk index, or outside [0, n_own)
+          const int oc = dc - (dh == 0 ? n_own : 0);  // else: chunk of the other half
           uint8_t* dst = (e >= 0 && e < n_own) ? sQ + e * 16384
-                                               : sQstage + (dc - (dh == 0 ? n_own : 0)) * 16384;
+                         : (oc < n_tq ? sQstage + oc * 16384 : sQ + (n_own + oc - n_tq) * 16384);
           tma_load_2d(smem_u32(dst), &tm_q, dc * 64, qrow0, qb);
         }
       }
@@ -567,14 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the query rows of other queries (or past the tensor) in the box are
       // zeroed, so they contribute nothing to S
       if (ok && nrows < 128) {
-        for (int e = 0; e < n_own; ++e)
+        for (int e = 0; e < n_sq; ++e)
           for (int pc = nrows * 8 + lane; pc < 128 * 8; pc += 32)
             *reinterpret_cast<uint4*>(sQ + e * 16384 + swz128(pc >> 3, pc & 7)) =
                 make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (ok && (n_other > 0 || kF16))
+      if (ok && (n_tq > 0 || kF16))
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_tmem), 0, abort, a.status,
                                                kWaitLimitNs, 34));
       if (lane == 0) mbar_arrive(smem_u32(&sm->q_ready));  // also on failure: abort is set
@@ -591,10 +583,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int seg, nvalid;
       int64_t kt;
       tile_of(i, seg, kt, nvalid);
-      const int sb = i & 1;
-      // the S/P buffer is reused once PV of tile i-2 has read its P
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->s_free[sb]), ((i >> 1) - 1) & 1,
+      const int sb = i % kNSB;
+      // the S/P buffer is reused once PV of tile i - kNSB has read its P.
+      // (Buffers alternate between the two issuers, but each wait is still
+      // exact: this issuer's previous tile, i - 2, waited for PV(i - 2 - kNSB),
+      // so the phase before the one waited for here has completed.)
+      if (i >= kNSB) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->s_free[sb]), ((i / kNSB) - 1) & 1,
                                                abort, a.status, kWaitLimitNs, 37));
         if (!ok) break;
         tc_fence_after();
@@ -632,11 +627,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t bd = smem_desc(slot_a + ks * 32, 16, 1024, kSwizzle128B);
               const uint32_t acc = (p == 0 && ks == 0) ? 0u : 1u;
-              if (p < n_other) {
+              if (p < n_tq) {
                 mma_bf16_ts(tS + sb * 64, tQ + p * 32 + ks * 8, bd, idesc_qk, acc);
               } else {
+                // the other half's shared-memory chunks follow the own ones
+                const int qc = p < n_other ? n_own + p - n_tq : p - n_other;
                 const uint64_t ad =
-                    smem_desc(sQa + (p - n_other) * 16384 + ks * 32, 16, 1024, kSwizzle128B);
+                    smem_desc(sQa + qc * 16384 + ks * 32, 16, 1024, kSwizzle128B);
                 mma_bf16_ss(tS + sb * 64, ad, bd, idesc_qk, acc);
               }
             }
@@ -685,11 +682,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd =
               smem_desc(sRa + static_cast<uint32_t>(gsl * gsz) * 8192u + ks * 2048, 8192, 1024,
                         kSwizzle128B);
-          mma_bf16_ts(tO, tS + (i & 1) * 64 + ks * 8, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+          mma_bf16_ts(tO, tS + (i % kNSB) * 64 + ks * 8, bd, idesc_pv,
+                      (i > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm->empty[gsl]));
-        mma_commit(smem_u32(&sm->pv_done));
-        mma_commit(smem_u32(&sm->s_free[i & 1]));
+        mma_commit(smem_u32(&sm->s_free[i % kNSB]));
       }
       __syncwarp();
     }
@@ -709,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t tq = row_valid ? a.pos[(int64_t)b * a.T + t0 + g] : 0;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     bool ok = true;
-    if (n_other > 0 || kF16) {
+    if (n_tq > 0 || kF16) {
       // the other half of this row's q~ into tensor memory (zeros for rows
       // that are not this block's); with fp16 products, this row of the own
       // half is converted in shared memory too (the QK issuer zeroes the
@@ -717,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_full), 0, abort, a.status,
                                              kWaitLimitNs, 35));
       if (kF16 && row_valid && ok) {
-        for (int e = 0; e < n_own; ++e)
+        for (int e = 0; e < n_sq; ++e)
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             uint4* cell = reinterpret_cast<uint4*>(sQ + e * 16384 + swz128(rI, q));
@@ -725,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         fence_proxy_async_smem();  // the tensor core reads these rows
       }
-      for (int e = 0; e < n_other; ++e) {
+      for (int e = 0; e < n_tq; ++e) {
         float w[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -740,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tQ + lane_base + e * 32, w);
       }
-      if (n_other > 0) tmem_wait_st();
+      if (n_tq > 0) tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm->q_tmem));
     }
@@ -788,8 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool full_tile =
           __all_sync(0xffffffffu, colmask == ~0ull && c_lo == 0 && c_hi == 64);
-      const int sb = i & 1;
-      bool got = mbar_wait(smem_u32(&sm->s_full[sb]), (i >> 1) & 1, abort, a.status,
+      const int sb = i % kNSB;
+      bool got = mbar_wait(smem_u32(&sm->s_full[sb]), (i / kNSB) & 1, abort, a.status,
                            kWaitLimitNs, 25);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }  // warp-uniform exit
       tc_fence_after();
@@ -818,12 +815,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Lazy rescale: only when the running max grows by more than 2^8.  The
       // tensor-memory loads/stores are warp-collective, so the decision is
       // taken per warp; lanes that need no rescale multiply by 1.  O is
-      // touched only then, after PV(i-1) has finished writing it (PV runs at
-      // most one tile ahead of this wait, so the parity stays unambiguous).
+      // touched only then, after PV(i-1) has finished writing it.
       const bool grow = mx > m_used + 8.f;
       const bool need_rescale = grow && m_used != -INFINITY && i > 0;
       if (__any_sync(0xffffffffu, need_rescale)) {
-        got = mbar_wait(smem_u32(&sm->pv_done), (i - 1) & 1, abort, a.status, kWaitLimitNs, 32);
+        // PV(i-1) has completed once it frees its S buffer; the phase before
+        // (PV(i-1-kNSB)) completed before QK(i-1) was issued, and PV(i)
+        // needs this thread's P, so the parity names PV(i-1) alone
+        got = mbar_wait(smem_u32(&sm->s_free[(i - 1) % kNSB]), ((i - 1) / kNSB) & 1, abort,
+                        a.status, kWaitLimitNs, 32);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
         const float f = need_rescale ? ex2_fast(m_used - mx) : 1.f;
@@ -946,14 +946,20 @@ bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int nu
   if (ndc % nds) return false;  // the halves of the output are whole chunks
   const int n_own = ndc / nds;
   const int n_other = ndc - n_own;
-  // tensor memory: S 128 + O (own columns) + the other half of Q (32 per chunk)
-  if (128 + n_own * 64 + n_other * 32 > 512) return false;
+  // tensor memory: the S/P buffers, O (own columns), then as many chunks of
+  // the other half of Q as fit (32 columns each); the rest of Q stays in
+  // shared memory
+  const int tq_fit = (512 - kNSB * 64 - n_own * 64) / 32;
+  if (tq_fit < 0) return false;
+  const int n_tq = n_other < tq_fit ? n_other : tq_fit;
+  const int n_sq = ndc - n_tq;
   p->G = G;
   p->n_rb = n_rb;
   p->nds = nds;
+  p->n_tq = n_tq;
   p->nsplit = static_cast<int>(nsplit);
   p->keys_per_split = static_cast<int>(tps * kTile);
-  const size_t fixed = 1024 + (size_t)n_own * 16384 + sizeof(AttnShared);
+  const size_t fixed = 1024 + (size_t)n_sq * 16384 + sizeof(AttnShared);
   int nslot = static_cast<int>((227 * 1024 - fixed) / 8192);
   if (nslot > kMaxSlots) nslot = kMaxSlots;
   // the own chunks of a tile are consecutive slots: a tile's own group
@@ -961,11 +967,11 @@ bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int nu
   nslot -= nslot % n_own;
   // QK of the next tile (all ndc chunks) is issued before PV of the current
   // one (our n_own chunks): both must fit the ring at once, and the staging
-  // of the other half of Q (two slots per chunk) fits at its end
-  if (nslot < ndc + n_own || nslot < 2 * n_other) return false;
+  // of the tensor-memory chunks of Q (two slots per chunk) fits at its end
+  if (nslot < ndc + n_own || nslot < 2 * n_tq) return false;
   // epilogue staging of 128 rows x (own columns + 4) fp32 over the Q area
   // and the ring, both free once every MMA has completed
-  if ((size_t)128 * (n_own * 64 + 4) * 4 > (size_t)n_own * 16384 + (size_t)nslot * 8192)
+  if ((size_t)128 * (n_own * 64 + 4) * 4 > (size_t)n_sq * 16384 + (size_t)nslot * 8192)
     return false;
   p->nslot = nslot;
   p->smem_bytes = fixed + (size_t)nslot * 8192;

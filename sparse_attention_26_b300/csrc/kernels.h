@@ -168,10 +168,11 @@ struct AttnArgs {
   int nsplit;                   // key splits
   int keys_per_split;           // multiple of 64
   int nds;                      // D splits (1 or 2)
+  int n_tq;                     // chunks of the other D half of Q kept in tensor memory
   int dependent;                // launched as a programmatic dependent
 };
 struct AttnPlan {
-  int G, n_rb, nsplit, keys_per_split, nds, nslot;
+  int G, n_rb, nsplit, keys_per_split, nds, n_tq, nslot;
   size_t smem_bytes, ws_bytes;
 };
 bool plan_attention(int kind, int B, int T, int H, int D, int64_t n_keys, int num_sms,

@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(1024) topk_row_kernel(const TopkArgs a) {
 // ============================================================ slice path
 constexpr int kListCap = 2048;   // per-CTA shared-memory lists of the pick sweep
 constexpr int kLoadBatch = 8;    // float4 loads a thread issues before using them
+constexpr int kSumBatch = 24;    // slices whose histogram loads a thread issues at once
 constexpr int kCandSmem = 8192;  // candidates the last CTA ranks in shared memory
 
 struct SliceShared {
@@ -492,20 +493,35 @@ __global__ void __launch_bounds__(kPickThreads) topk_pick_kernel(const TopkArgs 
       for (int64_t e = n + tid; e < a.k; e += kPickThreads) out[e] = -1;
     return;
   }
-  // the row's histogram: the sum of its S slices' bins
-  // (each thread sums its bins over the slices with up to 16 loads in
-  // flight at once: the loads do not wait on one another)
-  const uint16_t* rh = a.hist + row * a.S * kBins;
-  for (int i = tid; i < kBins; i += kPickThreads) {
-    uint32_t c = 0;
-    for (int q0 = 0; q0 < a.S; q0 += 16) {
-      uint16_t h[16];
+  // the row's histogram: the sum of its S slices' bins.  Thread t sums bin
+  // pairs t and t + 512 (one 32-bit load holds two 16-bit bins) with up to
+  // kSumBatch slices' loads in flight at once, so a row of up to kSumBatch
+  // slices costs one round of memory latency.
+  static_assert(kBins == 4 * kPickThreads, "two bin pairs per thread");
+  {
+    const uint32_t* rh = reinterpret_cast<const uint32_t*>(a.hist + row * a.S * kBins);
+    uint32_t c[4] = {0u, 0u, 0u, 0u};
+    for (int q0 = 0; q0 < a.S; q0 += kSumBatch) {
+      uint32_t v0[kSumBatch], v1[kSumBatch];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) h[u] = q0 + u < a.S ? __ldcg(rh + (q0 + u) * kBins + i) : 0;
+      for (int u = 0; u < kSumBatch; ++u) {
+        const bool in = q0 + u < a.S;
+        const uint32_t* p = rh + (q0 + u) * (kBins / 2) + tid;
+        v0[u] = in ? __ldcg(p) : 0u;
+        v1[u] = in ? __ldcg(p + kPickThreads) : 0u;
+      }
 #pragma unroll
-      for (int u = 0; u < 16; ++u) c += h[u];
+      for (int u = 0; u < kSumBatch; ++u) {
+        c[0] += v0[u] & 0xffffu;
+        c[1] += v0[u] >> 16;
+        c[2] += v1[u] & 0xffffu;
+        c[3] += v1[u] >> 16;
+      }
     }
-    sh.hist[i] = c;
+    sh.hist[2 * tid] = c[0];
+    sh.hist[2 * tid + 1] = c[1];
+    sh.hist[2 * (tid + kPickThreads)] = c[2];
+    sh.hist[2 * (tid + kPickThreads) + 1] = c[3];
   }
   if (tid == 0) {
     sh.n_up = 0;

@@ -63,8 +63,15 @@ typedef void* hattn_stream_t; /* cudaStream_t */
  * where the previous kernel in the stream is the one producing the call's
  * inputs: it relaxes only that one dependency.  Each call's comment says
  * which of its inputs it may read before that wait.  Every kernel of the
- * library lets its own dependents start early. */
+ * library lets its own dependents start early.
+ *
+ * HATTN_EVENT_EXTERNAL: a call that records an event of the caller's
+ * (hattn_indexer_topk_ex's split_event) records it with
+ * cudaEventRecordExternal, so that under stream capture it becomes an event
+ * record node a graph replay can be timed by.  Without it a captured record
+ * only marks a point other streams can wait for. */
 #define HATTN_LAUNCH_DEPENDENT 1
+#define HATTN_EVENT_EXTERNAL 2
 
 enum {
   HATTN_OK = 0,
@@ -219,8 +226,14 @@ HATTN_API int hattn_csa_compress_fp8(const void* kv_raw, const void* ik_raw, con
  *   receives I for j < n; entries j >= n are left untouched).
  *   workspace: device buffer of at least hattn_indexer_topk_workspace_bytes()
  *   bytes (may be NULL when that is 0): the scores (unless score_out is
- *   given), then the selection's scratch (hattn_topk_workspace_bytes);
- *   contents need no initialisation.
+ *   given), the score kernel's per-CTA histograms (when the selection runs
+ *   in clusters, see hattn_topk_select), then the selection's scratch;
+ *   contents need no initialisation.  Calls sharing one workspace must not
+ *   overlap on the GPU.
+ *   With one query per indexer group (T == 1 or HI > 128) and few long rows,
+ *   the score kernel also counts the top 11 bits of each score's
+ *   order-preserving key per row as it writes the scores, so the selection
+ *   starts from the row's histogram instead of a pass over the scores.
  *   Limits: 1 <= k <= 2048, HI * min(T, 256 / HI) <= 256, N_cap < 2^31.
  * ---------------------------------------------------------------------- */
 HATTN_API int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
@@ -229,6 +242,25 @@ HATTN_API int hattn_indexer_topk(const void* iq, const float* w, const void* ik_
                        hattn_stream_t stream);
 HATTN_API size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
                                           int score_out_given);
+/* hattn_indexer_topk with the options of hattn_indexer_scores_ex and FP8 keys:
+ *   ik_scale: NULL for bf16 keys ik_c [B][N_cap][dI]; else ik_c holds E4M3
+ *   codes [B][N_cap][128] with these row scales [B][N_cap] fp32 (see
+ *   hattn_indexer_scores_fp8 for the limits and the arithmetic).
+ *   n_sms, fresh_from, flags: as hattn_indexer_scores_ex, for the score
+ *   kernel; the selection kernel is always launched as a programmatic
+ *   dependent of it and reads nothing before its wait.
+ *   workspace: hattn_indexer_topk_workspace_bytes() bytes, as above.
+ *   split_event: a cudaEvent_t (cast to void*) recorded on `stream` between
+ *   the score and the selection kernel, or NULL: other streams may wait for
+ *   the scores alone on it, and with HATTN_EVENT_EXTERNAL in flags it times
+ *   the two kernels apart (an external record keeps the selection from
+ *   starting early). */
+HATTN_API int hattn_indexer_topk_ex(const void* iq, const float* w, const void* ik_c,
+                                    const float* ik_scale, const int32_t* pos, int B, int T,
+                                    int HI, int dI, int64_t N_cap, int k, int m, int n_sms,
+                                    int64_t fresh_from, int32_t* idx_out, float* score_out,
+                                    void* workspace, size_t ws_bytes, int flags,
+                                    void* split_event, hattn_stream_t stream);
 
 /* hattn_indexer_topk for callers that cannot allocate device memory: code
  * that runs where cudaMalloc is not allowed or not wanted, such as an engine
@@ -236,7 +268,7 @@ HATTN_API size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap,
  * allocations, or a stream-ordered path that must not synchronise on the
  * allocator.  The same selection as hattn_indexer_topk, but the fp32 scores
  * and the selection's scratch live in an array compiled into this library
- * (34 MiB: 4,194,304 scores, then up to 18 MiB of selection scratch, held
+ * (34 MiB: 4,194,304 scores, then up to 18 MiB of histograms and selection scratch, held
  * on every device that loads the library until the process exits), so the
  * call allocates nothing; the caller still passes inputs and idx_out.  The
  * pages have no counterpart of this call.
@@ -245,8 +277,8 @@ HATTN_API size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap,
  *     with that device current; make that first call before any stream capture.
  *   - Every call on a device shares the one scratch array: calls whose work
  *     overlaps on the GPU (other streams, other host threads) race.  No
- *     contents need clearing between calls: every score the selection reads
- *     is written first, and the selection clears its own counters. */
+ *     contents need clearing between calls: every score, histogram and
+ *     counter the selection reads is written earlier in the same call. */
 HATTN_API int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,
                                          const int32_t* pos, int B, int T, int HI, int dI,
                                          int64_t N_cap, int k, int m, int32_t* idx_out,
@@ -277,10 +309,13 @@ HATTN_API int hattn_indexer_scores_ex(const void* iq, const float* w, const void
                                       float* score_out, int flags, hattn_stream_t stream);
 /* hattn_topk_select: scores [B][T][N_cap] fp32 (entries j < n as written by
  * the score calls) -> idx_out [B][T][k] int32.  Few long rows (say 8 rows of
- * 262,144) are spread over many CTAs, which needs a caller-owned scratch of
- * hattn_topk_workspace_bytes(B, T, N_cap, k) bytes (0 when the rows fit one
- * CTA each; workspace may then be NULL).  The scratch needs no
- * initialisation; calls sharing one scratch must not overlap on the GPU.
+ * 262,144) are each spread over a thread-block cluster of 8 or 16 CTAs,
+ * which needs a caller-owned scratch of hattn_topk_workspace_bytes(B, T,
+ * N_cap, k) bytes (B * T * N_cap int32: the candidates of a row whose
+ * threshold bin holds more than 12,288 entries, say a row of near-equal
+ * scores); it is 0 when the rows fit one CTA each, and workspace may then be
+ * NULL.  The scratch needs no initialisation; calls sharing one scratch must
+ * not overlap on the GPU.
  * flags: HATTN_LAUNCH_DEPENDENT or 0 (every input is read after the wait). */
 HATTN_API size_t hattn_topk_workspace_bytes(int B, int T, int64_t N_cap, int k);
 HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T,

@@ -129,7 +129,8 @@ int make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims,
   } while (0)
 
 int check_flags(int flags) {
-  REQUIRE((flags & ~HATTN_LAUNCH_DEPENDENT) == 0, "flags=%d: unknown bits", flags);
+  REQUIRE((flags & ~(HATTN_LAUNCH_DEPENDENT | HATTN_EVENT_EXTERNAL)) == 0,
+          "flags=%d: unknown bits", flags);
   return HATTN_OK;
 }
 
@@ -609,10 +610,13 @@ namespace {
 
 // Scores of bf16 indexer keys (ik_c), or of E4M3 keys when k_scale is given
 // (ik_c then holds the codes, [B][N_cap][128] bytes).
+// hist_part: the folded first selection pass (IndexerArgs::hist_part; the
+// caller has checked fold_plan), else nullptr.  grid_out: the CTAs launched.
 int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
                         int B, int T, int HI, int dI, int64_t N_cap, int m, float* scores,
                         hattn_stream_t stream, int n_sms = 0, int64_t fresh_from = -1,
-                        const float* k_scale = nullptr, int flags = 0) {
+                        const float* k_scale = nullptr, int flags = 0,
+                        uint16_t* hist_part = nullptr, int64_t* grid_out = nullptr) {
   if (int rcf = check_flags(flags)) return rcf;
   REQUIRE_PTR(iq);
   REQUIRE_PTR(w);
@@ -632,7 +636,7 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
             (long long)N_cap);
   }
   IndexerPlan ip;
-  if (!plan_indexer(T, HI, dI, f8, &ip))
+  if (!plan_indexer(T, HI, dI, f8, hist_part != nullptr, &ip))
     return fail(HATTN_ERR_UNSUPPORTED, "no indexer kernel for HI=%d dI=%d", HI, dI);
   int sms = 0;
   int* status = nullptr;
@@ -691,15 +695,20 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   // that concurrent work keeps the others)
   if (n_sms > 0 && n_sms < sms) sms = n_sms;
   const int grid = static_cast<int>(a.total_slots < sms ? a.total_slots : sms);
+  a.hist_part = hist_part;
+  if (grid_out) *grid_out = grid;
   cudaError_t e =
       launch_indexer_score(tm_ik, tm_iq, tm_ks, a, ip, f8, grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
   return ok();
 }
 
+// part_*: the folded first pass (TopkArgs::hist_part and the indexer's slot
+// split), or part == nullptr.
 int topk_impl(const float* scores, const int32_t* pos, int64_t rows, int64_t N_cap, int k, int m,
               int32_t* idx_out, void* workspace, size_t ws_bytes, int flags,
-              hattn_stream_t stream) {
+              hattn_stream_t stream, const uint16_t* part = nullptr, int64_t part_total = 0,
+              int64_t part_grid = 0, int64_t part_nblk = 0) {
   if (int rcf = check_flags(flags)) return rcf;
   REQUIRE_PTR(scores);
   REQUIRE_PTR(pos);
@@ -728,6 +737,16 @@ int topk_impl(const float* scores, const int32_t* pos, int64_t rows, int64_t N_c
   t.k = k;
   t.m = m;
   t.N_cap = N_cap;
+  if (tp.slice_path) {
+    int sms = 0;
+    if (!device_info(nullptr, &t.status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  }
+  if (tp.slice_path && part) {
+    t.hist_part = part;
+    t.part_total = part_total;
+    t.part_grid = part_grid;
+    t.part_nblk = part_nblk;
+  }
   cudaError_t e = launch_topk(t, tp, (flags & HATTN_LAUNCH_DEPENDENT) != 0,
                               static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
@@ -746,8 +765,8 @@ size_t topk_ws_bytes(int64_t rows, int64_t N_cap, int k) {
 // loading this library holds until the process exits, so that call needs no
 // allocation.  It holds the fp32 scores, then the selection's scratch:
 // 4,194,304 scores (16 MiB, enough for B * T * N_cap = 8 x 1 x 262,144, a
-// 1M-token decode batch of 8, twice over) and at most as many candidate
-// indices plus histograms and counters (18 MiB).
+// 1M-token decode batch of 8, twice over), then the indexer's partial
+// histograms (up to 2 MiB) and at most as many candidate indices (16 MiB).
 constexpr int64_t kNoallocScores = int64_t(1) << 22;
 constexpr size_t kNoallocTopkBytes = (size_t(1) << 22) * 4 + (size_t(2) << 20);
 constexpr size_t kNoallocBytes = kNoallocScores * 4 + kNoallocTopkBytes;
@@ -775,6 +794,89 @@ int noalloc_scratch(uint8_t** out) {
 }
 
 size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Bytes of the indexer's partial histograms for the folded first pass.
+size_t part_bytes(int64_t grid) { return round256((size_t)grid * 2 * kSelBins * sizeof(uint16_t)); }
+
+// Whether the indexer can count the selection's first pass as it writes the
+// scores (one query per indexer group, each CTA's slots within two rows and
+// at most 65,535 entries, and the cluster path of the selection), for an
+// indexer grid of `grid` CTAs.
+bool fold_plan(int T, int HI, int dI, bool f8, int64_t rows, int64_t N_cap, int k, int64_t grid) {
+  IndexerPlan ip;
+  if (!plan_indexer(T, HI, dI, f8, true, &ip)) return false;
+  TopkPlan tp;
+  if (!plan_topk(rows, N_cap, k, num_sms_or_default(), &tp) || !tp.slice_path) return false;
+  const int64_t nblk = (N_cap + 127) / 128;
+  const int64_t total = rows * nblk;  // one query per group: a group is a row
+  if (grid < 1 || grid > total) return false;
+  const int64_t spc = (total + grid - 1) / grid;
+  return spc <= nblk && spc * 128 <= 65535;
+}
+
+// The indexer's grid for a call (as indexer_scores_impl launches it).
+int64_t indexer_grid(int64_t rows_times_nblk_groups, int n_sms, int sms) {
+  if (n_sms > 0 && n_sms < sms) sms = n_sms;
+  return rows_times_nblk_groups < sms ? rows_times_nblk_groups : sms;
+}
+
+// Scores, then selection (folded when fold_plan allows).  workspace layout:
+// [scores, unless score_out] [partial histograms, on the cluster path]
+// [selection scratch].
+int indexer_topk_impl(const void* iq, const float* w, const void* ik_c, const float* ik_scale,
+                      const int32_t* pos, int B, int T, int HI, int dI, int64_t N_cap, int k,
+                      int m, int n_sms, int64_t fresh_from, int32_t* idx_out, float* score_out,
+                      uint8_t* workspace, size_t ws_bytes, int flags, void* split_event,
+                      hattn_stream_t stream) {
+  const int64_t rows = (int64_t)B * T;
+  float* scores = score_out;
+  uint8_t* rest = workspace;
+  if (!scores) {
+    scores = reinterpret_cast<float*>(workspace);
+    rest += round256((size_t)rows * N_cap * sizeof(float));
+  }
+  TopkPlan tp;
+  const bool cluster = plan_topk(rows, N_cap, k, num_sms_or_default(), &tp) && tp.slice_path;
+  uint16_t* part = nullptr;
+  int64_t grid = 0;
+  if (cluster) {
+    int sms = 0;
+    int* status = nullptr;
+    if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+    grid = indexer_grid(rows * ((N_cap + 127) / 128), n_sms, sms);
+    if (fold_plan(T, HI, dI, ik_scale != nullptr, rows, N_cap, k, grid) &&
+        part_bytes(grid) <= part_bytes(num_sms_or_default()))
+      part = reinterpret_cast<uint16_t*>(rest);
+    rest += part_bytes(num_sms_or_default());
+  }
+  const size_t used = (size_t)(rest - workspace);
+  const size_t left = ws_bytes > used ? ws_bytes - used : 0;
+  int64_t launched = 0;
+  int rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream, n_sms,
+                               fresh_from, ik_scale, flags, part, &launched);
+  if (rc) return rc;
+  if (split_event) {
+    // external: an event record node when the stream is being captured
+    cudaError_t e = cudaEventRecordWithFlags(
+        static_cast<cudaEvent_t>(split_event), static_cast<cudaStream_t>(stream),
+        (flags & HATTN_EVENT_EXTERNAL) ? cudaEventRecordExternal : cudaEventRecordDefault);
+    if (e != cudaSuccess) return cuda_fail(e, "split event record");
+  }
+  // the selection waits for the scores before its first read: always a
+  // dependent launch of the score kernel
+  return topk_impl(scores, pos, rows, N_cap, k, m, idx_out, rest, left, HATTN_LAUNCH_DEPENDENT,
+                   stream, part, rows * ((N_cap + 127) / 128), launched, (N_cap + 127) / 128);
+}
+
+size_t indexer_topk_ws(int B, int T, int64_t N_cap, int k, bool score_out_given) {
+  if (B < 1 || T < 1 || N_cap < 1) return 0;
+  const int64_t rows = (int64_t)B * T;
+  const size_t scores = score_out_given ? 0 : round256((size_t)rows * N_cap * sizeof(float));
+  TopkPlan tp;
+  const bool cluster = k >= 1 && plan_topk(rows, N_cap, k, num_sms_or_default(), &tp) &&
+                       tp.slice_path;
+  return scores + (cluster ? part_bytes(num_sms_or_default()) : 0) + topk_ws_bytes(rows, N_cap, k);
+}
 
 }  // namespace
 
@@ -818,15 +920,23 @@ int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T, int
 
 size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap, int k,
                                           int score_out_given) {
-  if (B < 1 || T < 1 || N_cap < 1) return 0;
-  const size_t scores = score_out_given ? 0 : round256((size_t)B * T * N_cap * sizeof(float));
-  return scores + topk_ws_bytes((int64_t)B * T, N_cap, k);
+  return indexer_topk_ws(B, T, N_cap, k, score_out_given != 0);
 }
 
 int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
                        int B, int T, int HI, int dI, int64_t N_cap, int k, int m,
                        int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
                        hattn_stream_t stream) {
+  return hattn_indexer_topk_ex(iq, w, ik_c, nullptr, pos, B, T, HI, dI, N_cap, k, m, 0, -1,
+                               idx_out, score_out, workspace, ws_bytes, 0, nullptr, stream);
+}
+
+int hattn_indexer_topk_ex(const void* iq, const float* w, const void* ik_c, const float* ik_scale,
+                          const int32_t* pos, int B, int T, int HI, int dI, int64_t N_cap, int k,
+                          int m, int n_sms, int64_t fresh_from, int32_t* idx_out,
+                          float* score_out, void* workspace, size_t ws_bytes, int flags,
+                          void* split_event, hattn_stream_t stream) {
+  if (int rcf = check_flags(flags)) return rcf;
   REQUIRE_PTR(iq);
   REQUIRE_PTR(w);
   REQUIRE_PTR(ik_c);
@@ -835,22 +945,16 @@ int hattn_indexer_topk(const void* iq, const float* w, const void* ik_c, const i
   REQUIRE_PTR(idx_out);
   REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
   REQUIRE(B >= 1 && T >= 1 && N_cap >= 1, "B, T and N_cap must be >= 1");
-  const size_t need = hattn_indexer_topk_workspace_bytes(B, T, N_cap, k, score_out != nullptr);
+  REQUIRE(n_sms >= 0, "n_sms=%d must be >= 0", n_sms);
+  const size_t need = indexer_topk_ws(B, T, N_cap, k, score_out != nullptr);
   if (need > 0) {
     REQUIRE_PTR(workspace);
     REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
   }
-  float* scores = score_out;
-  uint8_t* rest = static_cast<uint8_t*>(workspace);
-  if (!scores) {
-    scores = static_cast<float*>(workspace);
-    rest += round256((size_t)B * T * N_cap * sizeof(float));
-  }
-  int rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream);
-  if (rc) return rc;
-  const size_t left = need > (size_t)(rest - static_cast<uint8_t*>(workspace))
-                          ? need - (size_t)(rest - static_cast<uint8_t*>(workspace)) : 0;
-  return topk_impl(scores, pos, (int64_t)B * T, N_cap, k, m, idx_out, rest, left, 0, stream);
+  return indexer_topk_impl(iq, w, ik_c, ik_scale, pos, B, T, HI, dI, N_cap, k, m, n_sms,
+                           fresh_from < 0 ? -1 : fresh_from, idx_out, score_out,
+                           static_cast<uint8_t*>(workspace), ws_bytes, flags, split_event,
+                           stream);
 }
 
 int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,
@@ -867,21 +971,20 @@ int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,
   REQUIRE((int64_t)B * T * N_cap <= kNoallocScores,
           "B * T * N_cap = %lld scores exceed the fixed scratch of %lld (use hattn_indexer_topk "
           "with a workspace)", (long long)((int64_t)B * T * N_cap), (long long)kNoallocScores);
-  const size_t sel = topk_ws_bytes((int64_t)B * T, N_cap, k);
+  const size_t sel = indexer_topk_ws(B, T, N_cap, k, true);
   REQUIRE(sel <= kNoallocTopkBytes,
           "the selection needs %zu bytes of scratch, the fixed scratch holds %zu (use "
           "hattn_indexer_topk with a workspace)", sel, kNoallocTopkBytes);
   uint8_t* scratch = nullptr;
   int rc = noalloc_scratch(&scratch);
   if (rc) return rc;
-  float* scores = reinterpret_cast<float*>(scratch);
   // every score the selection reads (entries j < visible count) is written
-  // by the score kernel first, and the selection clears its own counters, so
-  // nothing in the shared scratch needs clearing between calls
-  rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream);
-  if (rc) return rc;
-  return topk_impl(scores, pos, (int64_t)B * T, N_cap, k, m, idx_out,
-                   scratch + kNoallocScores * 4, kNoallocTopkBytes, 0, stream);
+  // by the score kernel first, and every histogram and counter it reads is
+  // written in the same call, so nothing in the shared scratch needs
+  // clearing between calls
+  return indexer_topk_impl(iq, w, ik_c, nullptr, pos, B, T, HI, dI, N_cap, k, m, 0, -1, idx_out,
+                           reinterpret_cast<float*>(scratch), scratch + kNoallocScores * 4,
+                           kNoallocTopkBytes, 0, nullptr, stream);
 }
 
 size_t hattn_attn_workspace_bytes(int kind, int B, int T, int H, int D, int64_t n_keys,

@@ -46,6 +46,7 @@ constexpr int kBlockRows = 128;
 constexpr int kMaxStages = 12;
 constexpr int kMaxStagesBf16 = 8;
 constexpr int kMaxAcc = 4;  // accumulators in flight (TMEM columns permitting)
+constexpr int kHistWords = kSelBins / 2;  // a row's 16-bit bins, two per word
 
 struct IdxSmem {
   uint64_t full[kMaxStages];
@@ -59,12 +60,37 @@ struct IdxSmem {
   uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
-  // per epilogue warp (no cross-warp barrier): visible entries per query of
-  // the current group, and the head weight of every accumulator column
-  int nt[kEpiWarps][256];
-  alignas(16) float wcol[kEpiWarps][256];
-  float qscale[256];  // FP8 keys: scale of each query row
 };
+
+// The rest of the epilogue's shared state follows IdxSmem, sized by the
+// plan: per epilogue warp (no cross-warp barrier) the head weight of every
+// accumulator column and the visible entries of each query of the current
+// group; the query row scales (FP8 keys); and, when the call folds the
+// selection's first pass in, two 2,048-bin histograms of 16-bit counts
+// (packed in pairs) for the first and second row of this CTA's slots.
+struct EpiLayout {
+  uint32_t wcol, qscale, nt, hist, bytes;
+};
+__host__ __device__ __forceinline__ EpiLayout epi_layout(int NQ, int G, bool hist) {
+  EpiLayout l;
+  uint32_t o = 0;
+  l.wcol = o;
+  o += kEpiWarps * NQ * 4;
+  l.qscale = o;
+  o += (NQ * 4 + 15) / 16 * 16;
+  l.nt = o;
+  o += (kEpiWarps * G * 4 + 15) / 16 * 16;
+  l.hist = o;
+  o += hist ? 2 * kHistWords * 4 : 0;
+  l.bytes = o;
+  return l;
+}
+
+// order-preserving key of a score (the selection ranks these)
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);  // -0 and +0 compare equal
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 __device__ __forceinline__ int64_t visible_entries(int32_t t, int m, int64_t cap) {
   int64_t n = t < 0 ? 0 : (static_cast<int64_t>(t) + 1) / m;
@@ -159,6 +185,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   float* sScale = reinterpret_cast<float*>(sA + a.stages * stage_bytes);
   IdxSmem* sm = reinterpret_cast<IdxSmem*>(sA + a.stages * stage_bytes +
                                            (F8 ? a.stages * kBlockRows * 4 : 0));
+  const EpiLayout el = epi_layout(a.NQ, a.G, a.hist_part != nullptr);
+  uint8_t* epi = reinterpret_cast<uint8_t*>(sm) + (sizeof(IdxSmem) + 15) / 16 * 16;
+  float* qscale = reinterpret_cast<float*>(epi + el.qscale);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(epi + el.hist);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -211,6 +241,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       uint32_t ph = 0;
       int64_t it = 0, qloads = 0, loaded = -1;
       bool keys_ready = false;  // the compressed keys of the previous kernel are visible
+      const uint64_t once = l2_policy_evict_first();
       for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
         if (!cur.live()) continue;
         if (cur.group != loaded) {
@@ -243,13 +274,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         }
         const uint32_t fb = smem_u32(&sm->full[st]);
         mbar_arrive_expect_tx(fb, stage_bytes + (F8 ? kBlockRows * 4 : 0));
+        // the keys are read once: first out of L2 (the scores written
+        // meanwhile, and whatever the attention reads again, stay)
         if (F8) {
-          tma_load_3d(smem_u32(sA + st * stage_bytes), &tm_ik, 0, cur.blk * kBlockRows, cur.b, fb);
-          tma_load_2d(smem_u32(sScale + st * kBlockRows), &tm_ks, cur.blk * kBlockRows, cur.b, fb);
+          tma_load_3d_hint(smem_u32(sA + st * stage_bytes), &tm_ik, 0, cur.blk * kBlockRows,
+                           cur.b, fb, once);
+          tma_load_2d_hint(smem_u32(sScale + st * kBlockRows), &tm_ks, cur.blk * kBlockRows,
+                           cur.b, fb, once);
         } else
           for (int kc = 0; kc < a.KC; ++kc)
-            tma_load_3d(smem_u32(sA + st * stage_bytes + kc * 16384), &tm_ik, kc * 64,
-                        cur.blk * kBlockRows, cur.b, fb);
+            tma_load_3d_hint(smem_u32(sA + st * stage_bytes + kc * 16384), &tm_ik, kc * 64,
+                             cur.blk * kBlockRows, cur.b, fb, once);
         ++it;
         if (++st == a.stages) { st = 0; ph ^= 1u; }
       }
@@ -336,8 +371,20 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     const int eg = ew >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    float* wcol = sm->wcol[ew];
-    int* ntv = sm->nt[ew];
+    float* wcol = reinterpret_cast<float*>(epi + el.wcol) + ew * a.NQ;
+    int* ntv = reinterpret_cast<int*>(epi + el.nt) + ew * a.G;
+    // Folded first selection pass (one query per group): the top 11 bits of
+    // each visible score's key are counted per row, for the first and the
+    // second row this CTA's slots touch (its slots span at most two rows).
+    const bool fold = a.hist_part != nullptr;
+    const int64_t row0 = s0 / a.nblk;
+    // the scores are read again by the selection right after this kernel
+    const uint64_t keep = l2_policy_evict_last();
+    if (fold) {
+      for (int i = threadIdx.x - kFirstEpiWarp * 32; i < 2 * kHistWords; i += kEpiWarps * 32)
+        hist[i] = 0u;
+      named_bar_sync(1, kEpiWarps * 32);
+    }
     // heads a multiple of 32: every 32-column accumulator chunk belongs to
     // one query, so a query's score is a straight sum over its chunks
     const bool whole = (a.HI & 31) == 0;
@@ -355,7 +402,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           // row scales
           bool got = mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 18);
           if (!__all_sync(0xffffffffu, got)) break;
-          quantize_query_rows(sQ, sQ8, sm->qscale, a.NQ, ew, lane);
+          quantize_query_rows(sQ, sQ8, qscale, a.NQ, ew, lane);
           fence_proxy_async_smem();  // visible to the tensor core's reads
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm->q8full));
@@ -367,7 +414,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         for (int c = lane; c < a.NQ; c += 32) {
           const int g = c / a.HI, h = c % a.HI;
           const float wv = (g < cur.gv) ? a.w[((int64_t)cur.b * a.T + cur.t0 + g) * a.HI + h] : 0.f;
-          wcol[c] = F8 ? wv * sm->qscale[c] : wv;
+          wcol[c] = F8 ? wv * qscale[c] : wv;
         }
         for (int g = lane; g < a.G; g += 32)
           ntv[g] = g < cur.gv ? static_cast<int>(visible_entries(
@@ -434,7 +481,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             }
           }
           const float sum = (s01.x + s01.y) + (s23.x + s23.y);
-          if (j < ntv[g]) srow[(int64_t)g * a.N_cap] = F8 ? sum * ks : sum;
+          if (j < ntv[g]) {
+            const float sc = F8 ? sum * ks : sum;
+            st_global_hint(srow + (int64_t)g * a.N_cap, sc, keep);
+            if (fold) {
+              const uint32_t bin = score_key(sc) >> 21;
+              atomicAdd(&hist[(cur.group == row0 ? 0 : kHistWords) + (bin >> 1)],
+                        1u << ((bin & 1u) * 16u));
+            }
+          }
         }
       } else {
         float sum = 0.f;
@@ -447,7 +502,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           for (int i = 0; i < 32; ++i) {
             sum = fmaf(wcol[cc + i], fmaxf(x[i], 0.f), sum);
             if (++h == a.HI) {
-              if (g < cur.gv && j < ntv[g]) srow[(int64_t)g * a.N_cap] = F8 ? sum * ks : sum;
+              if (g < cur.gv && j < ntv[g]) {
+                const float sc = F8 ? sum * ks : sum;
+                st_global_hint(srow + (int64_t)g * a.N_cap, sc, keep);
+                if (fold) {
+                  const uint32_t bin = score_key(sc) >> 21;
+                  atomicAdd(&hist[(cur.group == row0 ? 0 : kHistWords) + (bin >> 1)],
+                            1u << ((bin & 1u) * 16u));
+                }
+              }
               sum = 0.f;
               h = 0;
               ++g;
@@ -459,6 +522,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       mbar_arrive(smem_u32(&sm->tempty[acc]));
       ++it;
     }
+    if (fold) {
+      // this CTA's partial histograms, part[cta][0] for its first row and
+      // part[cta][1] for the second (when its slots reach one)
+      named_bar_sync(1, kEpiWarps * 32);
+      const int64_t row1 = (s1 - 1) / a.nblk;
+      const int nv = (row1 != row0 ? 2 : 1) * kHistWords / 4;
+      uint4* dst = reinterpret_cast<uint4*>(a.hist_part + static_cast<int64_t>(blockIdx.x) * 2 * kSelBins);
+      const uint4* src = reinterpret_cast<const uint4*>(hist);
+      for (int i = threadIdx.x - kFirstEpiWarp * 32; i < nv; i += kEpiWarps * 32) dst[i] = src[i];
+    }
   }
 
   tc_fence_before();
@@ -469,7 +542,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
 }  // namespace
 
-bool plan_indexer(int T, int HI, int dI, bool f8, IndexerPlan* p) {
+bool plan_indexer(int T, int HI, int dI, bool f8, bool fold, IndexerPlan* p) {
   if (HI <= 0 || HI > 256 || dI <= 0 || dI > 128) return false;
   if (f8 && dI != 128) return false;
   int G = 256 / HI;
@@ -483,7 +556,9 @@ bool plan_indexer(int T, int HI, int dI, bool f8, IndexerPlan* p) {
   const size_t q_bytes = (size_t)p->KC * NQ * 128 + (f8 ? (size_t)NQ * 128 : 0);
   // FP8: 16 KB of codes plus the block's 128 fp32 scales per stage
   const size_t stage_bytes = f8 ? 16384 + kBlockRows * 4 : (size_t)p->KC * 16384;
-  const size_t budget = 227 * 1024 - 1024 - sizeof(IdxSmem) - q_bytes;
+  if (fold && G != 1) return false;  // the folded pass counts one query per group
+  const size_t fixed = (sizeof(IdxSmem) + 15) / 16 * 16 + epi_layout(NQ, G, fold).bytes;
+  const size_t budget = 227 * 1024 - 1024 - fixed - q_bytes;
   int stages = static_cast<int>(budget / stage_bytes);
   const int cap = f8 ? kMaxStages : kMaxStagesBf16;
   if (stages > cap) stages = cap;
@@ -501,7 +576,7 @@ bool plan_indexer(int T, int HI, int dI, bool f8, IndexerPlan* p) {
   while (nacc * 2 <= kMaxAcc && nacc * 2 * NQ <= 512) nacc *= 2;
   p->nacc = nacc;
   p->tmem_cols = nacc * NQ;
-  p->smem_bytes = 1024 + q_bytes + stages * stage_bytes + sizeof(IdxSmem);
+  p->smem_bytes = 1024 + q_bytes + stages * stage_bytes + fixed;
   return true;
 }
 

@@ -37,6 +37,10 @@ struct CompressArgs {
 cudaError_t launch_compress(const CompressArgs& a, int num_sms, cudaStream_t stream);
 
 // ------------------------------------------------------------ indexer score
+// Bins of the selection's first radix pass: the top 11 bits of a score's
+// order-preserving key.
+constexpr int kSelBins = 2048;
+
 struct IndexerArgs {
   const float* w;        // [B][T][HI]
   const int32_t* pos;    // [B][T]
@@ -54,6 +58,12 @@ struct IndexerArgs {
   int64_t N_cap;
   int64_t total_slots;   // B * groups_per_seq * nblk
   int dependent;         // launched as a programmatic dependent
+  // Folded first pass of the selection (one query per group, each CTA's
+  // slots within two rows): CTA c writes the 2,048-bin histogram of the top
+  // 11 key bits of its visible scores, 16-bit counts, to
+  // hist_part[c][0][.] for the row of its first slot and hist_part[c][1][.]
+  // for the row of its last slot when that differs.  nullptr: no histograms.
+  uint16_t* hist_part;
 };
 struct IndexerPlan {
   int G, NQ, KC, stages, nacc, tmem_cols;
@@ -61,7 +71,7 @@ struct IndexerPlan {
 };
 // f8: E4M3 keys (dI = 128, one 128-byte row each) and queries quantised in
 // the kernel; else bf16 keys and queries.
-bool plan_indexer(int T, int HI, int dI, bool f8, IndexerPlan* p);
+bool plan_indexer(int T, int HI, int dI, bool f8, bool fold, IndexerPlan* p);
 // tm_ks: the FP8 keys' row scales [B][N_cap] fp32, boxes of 128 (FP8 only).
 cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm_iq,
                                  const CUtensorMap& tm_ks, const IndexerArgs& a,
@@ -103,16 +113,21 @@ struct TopkArgs {
   const float* scores;   // [rows][N_cap]
   const int32_t* pos;    // [rows]
   int32_t* idx;          // [rows][k]
-  // slice path scratch (caller-owned; nothing needs clearing)
-  uint16_t* hist;        // [rows][S][2048] per-slice histograms of the top key digit
-  int32_t* ctr;          // [rows][4]: selected so far, candidates, tickets
-  int32_t* cand;         // [rows][N_cap] candidate entry indices
+  // cluster path: the folded first pass (the indexer's partial histograms,
+  // IndexerArgs::hist_part, one query per row) or nullptr (the kernel
+  // histograms the scores itself), and the indexer's slot split it follows
+  const uint16_t* hist_part;
+  int64_t part_total;    // indexer slots
+  int64_t part_grid;     // indexer CTAs
+  int64_t part_nblk;     // indexer slots per row
+  int32_t* cand;         // [rows][N_cap] candidates past the leader's shared memory (scratch)
+  int* status;           // device status word (a wait that gave up)
   int64_t rows;
   int k, m;
-  int S;                 // CTAs per row (slice path)
+  int S;                 // CTAs per row: the cluster size (cluster path)
   int vec4;              // rows are 16-byte aligned and slices start at multiples of 4
   int64_t N_cap;
-  int64_t slice;         // entries per CTA (slice path)
+  int64_t slice;         // entries per CTA (cluster path)
 };
 struct TopkPlan {
   bool slice_path;
@@ -122,7 +137,7 @@ struct TopkPlan {
 };
 bool plan_topk(int64_t rows, int64_t N_cap, int k, int num_sms, TopkPlan* p);
 size_t topk_scratch_bytes(const TopkPlan& p, int64_t rows, int64_t N_cap);
-// Points a->hist, a->ctr and a->cand into a scratch of topk_scratch_bytes().
+// Points a->cand into a scratch of topk_scratch_bytes().
 void topk_scratch_carve(const TopkPlan& p, int64_t rows, void* ws, TopkArgs* a);
 cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, bool dependent,
                         cudaStream_t stream);

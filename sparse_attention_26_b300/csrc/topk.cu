@@ -13,19 +13,18 @@
 //   histogram while loading, lists the keys of the threshold bin, and ranks
 //   only that list in the later passes.
 //
-//   slice path (few long rows, e.g. decode at 1M context: 8 rows of 262,144):
-//   S CTAs per row, two kernels and no inter-CTA waiting.
-//     topk_hist_kernel: each CTA histograms the top digit of its slice into
-//       its own 2,048 16-bit bins of the scratch (no atomics, nothing to
-//       clear), and CTA 0 of the row clears the row's counters.
-//     topk_pick_kernel: each CTA sums the row's S histograms, finds the bin
-//       of the k-th largest key, and sweeps its slice again: keys above that
-//       bin are selected at once (appended to the output), keys in it are
-//       appended to the row's candidate list.  The last CTA of the row to
-//       finish (a ticket counter) ranks the candidates -- the remaining two
-//       digits, then, only if more ties sit at the threshold than places
-//       are left, the tie indices from the smallest -- and writes the rest.
-//   The scratch is caller-owned (hattn_topk_workspace_bytes).
+//   cluster path (few long rows, e.g. decode at 1M context: 8 rows of
+//   262,144): a cluster of 8 or 16 CTAs per row, one kernel.  The row's
+//   top-digit histogram comes from the indexer (which counts its scores as
+//   it writes them: the sum of its CTAs' partials) or, without it, from the
+//   cluster's own slices summed in the leader CTA's shared memory.  Every
+//   CTA finds the bin of the k-th largest key and sweeps its slice: keys
+//   above that bin are selected at once, keys in it (the candidates) go to
+//   the leader's shared memory with their second-digit counts.  After one
+//   cluster barrier the leader ranks the candidates -- the third digit, then,
+//   only if more ties sit at the threshold than places are left, the tie
+//   indices from the smallest -- and writes the rest.
+//   The only scratch is for candidates past the leader's shared memory.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -33,14 +32,13 @@ namespace hattn {
 
 namespace {
 
-constexpr int kBins = 2048;
+constexpr int kBins = kSelBins;
 // Row path: keys of the first pass's threshold bin up to which the compact
 // path is taken; keys above that bin number fewer than k <= 2048.  Slice
 // positions fit 16 bits (a row holds at most 49,152 keys).
 constexpr int kMaxCand = 2048;
 constexpr int kMaxAbove = 2048;
 constexpr int kRowMaxKeys = 49152;
-constexpr int kPickThreads = 512;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);  // -0 and +0 compare equal
@@ -90,7 +88,7 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, ScanShared*
 // The bin holding the need-th largest key (1 <= need <= total): bins are
 // visited from the top; sh->digit = that bin, sh->above = keys in the bins
 // above it.  nb >= nthr, both powers of two.
-__device__ __forceinline__ void find_digit_desc(const uint32_t* h, int nb, uint32_t need,
+__device__ __noinline__ void find_digit_desc(const uint32_t* h, int nb, uint32_t need,
                                                 ScanShared* sh, int tid, int nthr) {
   if (tid == 0) {  // ordered before the finder's write by the scan's barriers
     sh->digit = 0;
@@ -118,7 +116,7 @@ __device__ __forceinline__ void find_digit_desc(const uint32_t* h, int nb, uint3
 
 // The bin holding the need-th smallest value: bins visited from the bottom;
 // sh->digit = that bin, sh->above = values in the bins below it.
-__device__ __forceinline__ void find_digit_asc(const uint32_t* h, int nb, uint32_t need,
+__device__ __noinline__ void find_digit_asc(const uint32_t* h, int nb, uint32_t need,
                                                ScanShared* sh, int tid, int nthr) {
   if (tid == 0) {
     sh->digit = 0;
@@ -317,101 +315,72 @@ __global__ void __launch_bounds__(1024) topk_row_kernel(const TopkArgs a) {
   }
 }
 
-// ============================================================ slice path
-constexpr int kListCap = 2048;   // per-CTA shared-memory lists of the pick sweep
-constexpr int kLoadBatch = 8;    // float4 loads a thread issues before using them
-constexpr int kSumBatch = 24;    // slices whose histogram loads a thread issues at once
-constexpr int kCandSmem = 8192;  // candidates the last CTA ranks in shared memory
+// ============================================================ cluster path
+constexpr int kClusterSize = 8;          // CTAs per row (the portable cluster size)
+constexpr int kClusterThreads = 1024;
+constexpr int kSumBatch = 24;            // partial histograms whose loads a thread issues at once
+constexpr int kSliceChunk = 8192;        // entries per bulk copy of the slice (32 KB)
+constexpr int kSliceChunks = 4;
+constexpr int kMaxSlice = kSliceChunk * kSliceChunks;  // entries a CTA stages in shared memory
+constexpr int kUpCap = 2048;             // a CTA's list of entries above the threshold bin
+constexpr int kLocalCand = 2048;         // a CTA's list of candidates (entries in that bin)
+constexpr int kCandCap = 4096;           // candidates the leader holds in shared memory
+static_assert(kBins == 2 * kClusterThreads, "one bin pair per thread");
 
-struct SliceShared {
+struct ClusterShared {
+  // (16-byte aligned arrays: hist and rowhist move as 16-byte vectors)
+  alignas(16) uint32_t hist[kBins];     // the row's top-digit histogram; the leader's third-digit counts
+  alignas(16) uint32_t rowhist[kBins];  // leader, no folded pass: the slices' top-digit histograms summed
+  alignas(16) uint32_t hist2[kBins];    // leader: the row's candidates' second-digit histogram
+  alignas(16) uint32_t lhist2[kBins];   // this CTA's candidates' second-digit histogram
+  alignas(16) int32_t up[kUpCap];
+  alignas(16) uint32_t lkey[kLocalCand];
+  alignas(16) int32_t lidx[kLocalCand];  // the leader reuses it for its bin list
+  uint64_t chunk_full[kSliceChunks];     // the slice's bulk copies have landed
   ScanShared scan;
-  uint32_t hist[kBins];
-  int n_up, n_in;        // fills of the two lists
-  int base_up, base_in;  // their ranges in the row's output and candidate list
-  int last;
-  int n_gt, n_eq;
-  int32_t up[kListCap];  // entries above the threshold bin (selected)
-  int32_t in[kListCap];  // entries in the threshold bin (candidates)
+  int n_up, n_cand;         // leader: the row's list fills
+  int l_up, l_cand;         // this CTA's list fills
+  int base_up, base_cand;   // this CTA's ranges in the row's lists
+  int n_gt, n_eq, n_bin;
 };
+static_assert(sizeof(ClusterShared) % 16 == 0, "the candidate arrays follow, 16-byte aligned");
+// dynamic shared memory: the staged slice, ClusterShared, then the leader's
+// candidate keys and entry indices (kCandCap each)
+constexpr size_t kSliceBytes = static_cast<size_t>(kMaxSlice) * 4;
+constexpr size_t kClusterSmem = kSliceBytes + sizeof(ClusterShared) + static_cast<size_t>(kCandCap) * 8;
+static_assert(kClusterSmem <= 227 * 1024, "one CTA's shared memory");
 
-// Histogram of the top 11 key bits of this CTA's slice, into its own bins.
-__global__ void __launch_bounds__(kPickThreads) topk_hist_kernel(const TopkArgs a) {
-  __shared__ uint32_t hist[kBins];
-  const int tid = threadIdx.x;
-  const int s = blockIdx.x;
-  const int64_t row = static_cast<int64_t>(blockIdx.y) + static_cast<int64_t>(gridDim.y) * blockIdx.z;
-  pdl_trigger();
-  pdl_wait();  // the scores are complete
-  if (row >= a.rows) return;
-  if (s == 0 && tid < 4) a.ctr[row * 4 + tid] = 0;  // read by topk_pick_kernel
-  const int64_t n = visible_count(a.pos[row], a.m, a.N_cap);
-  if (n <= a.k) return;  // every visible entry is selected (the pick kernel writes them)
-  for (int i = tid; i < kBins; i += kPickThreads) hist[i] = 0;
-  __syncthreads();
-  const int64_t lo = static_cast<int64_t>(s) * a.slice;
-  const int64_t hi = lo + a.slice < n ? lo + a.slice : n;
-  const float* src = a.scores + row * a.N_cap;
-  if (hi <= lo) {
-    // nothing visible in this slice
-  } else if (a.vec4) {
-    // slices start at multiples of 4 and rows are 16-byte aligned; each
-    // thread issues up to kLoadBatch float4 loads before using any of them
-    const int64_t q_hi = hi >> 2;
-    for (int64_t q0 = (lo >> 2) + tid; q0 < q_hi; q0 += kLoadBatch * kPickThreads) {
-      float4 v[kLoadBatch];
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u) {
-        const int64_t q = q0 + static_cast<int64_t>(u) * kPickThreads;
-        v[u] = q < q_hi ? __ldcg(reinterpret_cast<const float4*>(src) + q)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u) {
-        if (q0 + static_cast<int64_t>(u) * kPickThreads >= q_hi) break;
-        atomicAdd(&hist[order_key(v[u].x) >> 21], 1u);
-        atomicAdd(&hist[order_key(v[u].y) >> 21], 1u);
-        atomicAdd(&hist[order_key(v[u].z) >> 21], 1u);
-        atomicAdd(&hist[order_key(v[u].w) >> 21], 1u);
-      }
-    }
-    for (int64_t e = (q_hi << 2) + tid; e < hi; e += kPickThreads)
-      atomicAdd(&hist[order_key(__ldcg(src + e)) >> 21], 1u);
-  } else {
-    for (int64_t e = lo + tid; e < hi; e += kPickThreads)
-      atomicAdd(&hist[order_key(__ldcg(src + e)) >> 21], 1u);
-  }
-  __syncthreads();
-  uint16_t* dst = a.hist + (row * a.S + s) * kBins;
-  for (int i = tid; i < kBins; i += kPickThreads) dst[i] = static_cast<uint16_t>(hist[i]);
+// The indexer CTA whose slots contain slot x (its slots are
+// [total * c / grid, total * (c + 1) / grid)).
+__device__ __forceinline__ int64_t part_owner(int64_t x, int64_t total, int64_t grid) {
+  return ((x + 1) * grid + total - 1) / total - 1;
 }
 
-// The ranking of the row's candidates by its last CTA: `need` more entries
-// are taken from the C candidates (all in the threshold bin d0), written to
-// rest[0 .. need).  idx_of(c) / key_of(c) give candidate c's entry index and
-// order-preserving key.
+// Candidates c and `need` places left (need < C), all in the top-digit bin
+// d0; h2 holds the candidates' second-digit histogram.  Writes `need`
+// entries to rest[]: those above the need-th largest key, then its ties
+// with the smallest entry indices.  (The general ranking; the leader takes
+// it when the second digit's bin holds more candidates than one warp ranks.)
 template <class IdxOf, class KeyOf>
-__device__ __forceinline__ void rank_candidates(int C, uint32_t need, uint32_t d0, int32_t* rest,
-                                                SliceShared& sh, IdxOf idx_of, KeyOf key_of) {
+__device__ __noinline__ void rank_candidates(int C, uint32_t need, uint32_t d0, const uint32_t* h2,
+                                             int32_t* rest, ClusterShared& sh, IdxOf idx_of,
+                                             KeyOf key_of) {
   const int tid = threadIdx.x;
   const int room = static_cast<int>(need);
-  // the two remaining digits of the need-th largest candidate key
-  uint32_t prefix = d0;
-  for (int pass = 0; pass < 2; ++pass) {
-    const int width = pass == 0 ? 11 : 10;
-    const int shift = pass == 0 ? 10 : 0;
-    const int nb = 1 << width;
-    for (int i = tid; i < kBins; i += kPickThreads) sh.hist[i] = 0;
-    __syncthreads();
-    for (int c = tid; c < C; c += kPickThreads) {
-      const uint32_t key = key_of(c);
-      if ((key >> (shift + width)) == prefix) atomicAdd(&sh.hist[(key >> shift) & (nb - 1)], 1u);
-    }
-    __syncthreads();
-    find_digit_desc(sh.hist, nb, need, &sh.scan, tid, kPickThreads);
-    prefix = (prefix << width) | sh.scan.digit;
-    need -= sh.scan.above;
+  // second digit from the gathered histogram, third by one pass
+  find_digit_desc(h2, kBins, need, &sh.scan, tid, kClusterThreads);
+  uint32_t prefix = (d0 << 11) | sh.scan.digit;
+  need -= sh.scan.above;
+  for (int i = tid; i < kBins; i += kClusterThreads) sh.hist[i] = 0;
+  __syncthreads();
+  for (int c = tid; c < C; c += kClusterThreads) {
+    const uint32_t key = key_of(c);
+    if ((key >> 10) == prefix) atomicAdd(&sh.hist[key & 1023u], 1u);
   }
-  const uint32_t thr = prefix;  // the k-th largest key; `need` of its ties are taken
+  __syncthreads();
+  find_digit_desc(sh.hist, 1024, need, &sh.scan, tid, kClusterThreads);
+  const uint32_t thr = (prefix << 10) | sh.scan.digit;  // the k-th largest key
+  need -= sh.scan.above;                                // its ties still to take
   // candidates above the threshold, and the count of ties at it (the loop
   // runs the same trip count in every thread: warp_append is warp-collective)
   if (tid == 0) {
@@ -420,7 +389,7 @@ __device__ __forceinline__ void rank_candidates(int C, uint32_t need, uint32_t d
   }
   __syncthreads();
   int eq = 0;
-  for (int c0 = 0; c0 < C; c0 += kPickThreads) {
+  for (int c0 = 0; c0 < C; c0 += kClusterThreads) {
     const int c = c0 + tid;
     const uint32_t key = c < C ? key_of(c) : 0u;
     const bool gt = c < C && key > thr;
@@ -442,16 +411,16 @@ __device__ __forceinline__ void rank_candidates(int C, uint32_t need, uint32_t d
       const int width = pass == 2 ? 10 : 11;
       const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
       const int nb = 1 << width;
-      for (int i = tid; i < kBins; i += kPickThreads) sh.hist[i] = 0;
+      for (int i = tid; i < kBins; i += kClusterThreads) sh.hist[i] = 0;
       __syncthreads();
-      for (int c = tid; c < C; c += kPickThreads) {
+      for (int c = tid; c < C; c += kClusterThreads) {
         if (key_of(c) != thr) continue;
         const uint32_t j = static_cast<uint32_t>(idx_of(c));
         if (pass > 0 && (j >> (shift + width)) != ip) continue;
         atomicAdd(&sh.hist[(j >> shift) & (nb - 1)], 1u);
       }
       __syncthreads();
-      find_digit_asc(sh.hist, nb, left, &sh.scan, tid, kPickThreads);
+      find_digit_asc(sh.hist, nb, left, &sh.scan, tid, kClusterThreads);
       ip = (ip << width) | sh.scan.digit;
       left -= sh.scan.above;
     }
@@ -460,7 +429,7 @@ __device__ __forceinline__ void rank_candidates(int C, uint32_t need, uint32_t d
   if (tid == 0) sh.n_gt = 0;
   __syncthreads();
   int32_t* ties_out = rest + n_gt;
-  for (int c0 = 0; c0 < C; c0 += kPickThreads) {
+  for (int c0 = 0; c0 < C; c0 += kClusterThreads) {
     const int c = c0 + tid;
     bool take = false;
     int32_t j = 0;
@@ -473,171 +442,319 @@ __device__ __forceinline__ void rank_candidates(int C, uint32_t need, uint32_t d
   }
 }
 
-__global__ void __launch_bounds__(kPickThreads) topk_pick_kernel(const TopkArgs a) {
-  __shared__ SliceShared sh;
-  extern __shared__ __align__(16) uint8_t pick_dyn[];  // the last CTA's candidates
+// Where the sweep sends an entry at or above the threshold bin d0 (a few
+// per thousand): above it to this CTA's list of selected entries, in it to
+// its candidate list and second-digit counts; past a list's capacity (a
+// slice of near-equal scores) to the row's lists in the leader CTA one by
+// one.  Not inlined: the sweep's unrolled loop stays small, and one copy of
+// this code serves every call (a short kernel runs most code only once, so
+// its size is instruction-fetch time).
+struct SweepCtx {
+  ClusterShared* sh;
+  int32_t* out;     // the row's k output places
+  int32_t* cand_g;  // the row's overflow candidates
+  uint32_t r_up, r_cand, r_ckey, r_cidx, r_hist2;  // leader addresses
+  int k;
+  int64_t N_cap;
+};
+__device__ __noinline__ void sweep_take(const SweepCtx& x, int64_t e, uint32_t key, uint32_t d0) {
+  ClusterShared& sh = *x.sh;
+  if ((key >> 21) > d0) {
+    const int p = atomicAdd(&sh.l_up, 1);
+    if (p < kUpCap) {
+      sh.up[p] = static_cast<int32_t>(e);
+    } else {
+      const uint32_t q = atom_add_cluster(x.r_up, 1u);
+      if (q < static_cast<uint32_t>(x.k)) x.out[q] = static_cast<int32_t>(e);
+    }
+    return;
+  }
+  const int p = atomicAdd(&sh.l_cand, 1);
+  if (p < kLocalCand) {
+    sh.lkey[p] = key;
+    sh.lidx[p] = static_cast<int32_t>(e);
+    atomicAdd(&sh.lhist2[(key >> 10) & 2047u], 1u);
+    return;
+  }
+  const uint32_t q = atom_add_cluster(x.r_cand, 1u);
+  if (q < static_cast<uint32_t>(kCandCap)) {
+    st_cluster_u32(x.r_ckey + 4u * q, key);
+    st_cluster_u32(x.r_cidx + 4u * q, static_cast<uint32_t>(e));
+  } else if (static_cast<int64_t>(q) - kCandCap < x.N_cap) {
+    x.cand_g[q - kCandCap] = static_cast<int32_t>(e);
+  }
+  red_add_cluster(x.r_hist2 + 4u * ((key >> 10) & 2047u), 1u);
+}
+
+// One cluster of kClusterSize CTAs per row; CTA r of the cluster sweeps
+// entries [r * slice, (r + 1) * slice) of the row.
+__global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const TopkArgs a) {
+  extern __shared__ __align__(16) uint8_t csm[];
+  float* sslice = reinterpret_cast<float*>(csm);
+  ClusterShared& sh = *reinterpret_cast<ClusterShared*>(csm + kSliceBytes);
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(csm + kSliceBytes + sizeof(ClusterShared));
+  int32_t* cidx = reinterpret_cast<int32_t*>(csm + kSliceBytes + sizeof(ClusterShared) + kCandCap * 4);
   const int tid = threadIdx.x;
-  const int s = blockIdx.x;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
   const int64_t row = static_cast<int64_t>(blockIdx.y) + static_cast<int64_t>(gridDim.y) * blockIdx.z;
+  const int64_t lo = static_cast<int64_t>(rank) * a.slice;
+  // this CTA's part of the row staged in shared memory by bulk copies
+  // (rows 16-byte aligned, N_cap a multiple of 4): entries [lo, lo + staged)
+  const int64_t room = a.N_cap - lo;
+  const int staged = !a.vec4 || row >= a.rows || room <= 0
+                         ? 0
+                         : static_cast<int>(min(min(a.slice, static_cast<int64_t>(kMaxSlice)), room));
+  if (tid == 0) {
+    for (int c = 0; c < kSliceChunks; ++c) mbar_init(smem_u32(&sh.chunk_full[c]), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
   pdl_trigger();
-  pdl_wait();  // the histograms (and the scores before them) are complete
-  if (row >= a.rows) return;
+  pdl_wait();  // the scores (and the folded histograms) are complete
+  const float* src = a.scores + row * a.N_cap;
+  if (tid == 0) {
+    for (int c = 0; c < kSliceChunks; ++c) {
+      const int c0 = c * kSliceChunk;
+      if (c0 >= staged) break;
+      const uint32_t bytes = static_cast<uint32_t>(min(kSliceChunk, staged - c0)) * 4u;
+      const uint32_t bar = smem_u32(&sh.chunk_full[c]);
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_copy_g2s(smem_u32(sslice + c0), src + lo + c0, bytes, bar);
+    }
+  }
+  // every condition that ends a CTA early holds for its whole cluster (one row)
+  bool ok = true;
+  auto drain = [&]() {
+    // the slice's copies land before the CTA's shared memory is released
+    for (int c = 0; c * kSliceChunk < staged; ++c)
+      mbar_wait(smem_u32(&sh.chunk_full[c]), 0, nullptr, a.status, kWaitLimitNs, 41);
+  };
+  if (row >= a.rows) return;  // (nothing staged)
   const int64_t n = visible_count(a.pos[row], a.m, a.N_cap);
   int32_t* out = a.idx + row * a.k;
-  const int64_t lo = static_cast<int64_t>(s) * a.slice;
   const int64_t hi = lo + a.slice < n ? lo + a.slice : n;
   if (n <= a.k) {
-    // every visible entry is selected; CTA 0 pads
-    for (int64_t e = lo + tid; e < hi; e += kPickThreads) out[e] = static_cast<int32_t>(e);
-    if (s == 0)
-      for (int64_t e = n + tid; e < a.k; e += kPickThreads) out[e] = -1;
+    // every visible entry is selected; the leader pads
+    for (int64_t e = lo + tid; e < hi; e += kClusterThreads) out[e] = static_cast<int32_t>(e);
+    if (leader)
+      for (int64_t e = n + tid; e < a.k; e += kClusterThreads) out[e] = -1;
+    drain();
     return;
   }
-  // the row's histogram: the sum of its S slices' bins.  Thread t sums bin
-  // pairs t and t + 512 (one 32-bit load holds two 16-bit bins) with up to
-  // kSumBatch slices' loads in flight at once, so a row of up to kSumBatch
-  // slices costs one round of memory latency.
-  static_assert(kBins == 4 * kPickThreads, "two bin pairs per thread");
-  {
-    const uint32_t* rh = reinterpret_cast<const uint32_t*>(a.hist + row * a.S * kBins);
-    uint32_t c[4] = {0u, 0u, 0u, 0u};
-    for (int q0 = 0; q0 < a.S; q0 += kSumBatch) {
-      uint32_t v0[kSumBatch], v1[kSumBatch];
-#pragma unroll
-      for (int u = 0; u < kSumBatch; ++u) {
-        const bool in = q0 + u < a.S;
-        const uint32_t* p = rh + (q0 + u) * (kBins / 2) + tid;
-        v0[u] = in ? __ldcg(p) : 0u;
-        v1[u] = in ? __ldcg(p + kPickThreads) : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kSumBatch; ++u) {
-        c[0] += v0[u] & 0xffffu;
-        c[1] += v0[u] >> 16;
-        c[2] += v1[u] & 0xffffu;
-        c[3] += v1[u] >> 16;
-      }
+  const bool folded = a.hist_part != nullptr;
+  for (int i = tid; i < kBins; i += kClusterThreads) {
+    sh.lhist2[i] = 0;
+    if (leader) {
+      sh.hist2[i] = 0;
+      sh.rowhist[i] = 0;
     }
-    sh.hist[2 * tid] = c[0];
-    sh.hist[2 * tid + 1] = c[1];
-    sh.hist[2 * (tid + kPickThreads)] = c[2];
-    sh.hist[2 * (tid + kPickThreads) + 1] = c[3];
+    if (!folded) sh.hist[i] = 0;
   }
   if (tid == 0) {
+    sh.l_up = 0;
+    sh.l_cand = 0;
     sh.n_up = 0;
-    sh.n_in = 0;
+    sh.n_cand = 0;
   }
   __syncthreads();
-  find_digit_desc(sh.hist, kBins, static_cast<uint32_t>(a.k), &sh.scan, tid, kPickThreads);
+  cluster_arrive();  // (A) the leader's counters and histograms are cleared
+  // the staged entries this CTA sweeps: [lo, lo + n_st), the rest of its
+  // slice [lo + n_st, hi) from global memory
+  const int n_st = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(staged), hi - lo)));
+  auto chunk_wait = [&](int c) {
+    ok = mbar_wait(smem_u32(&sh.chunk_full[c]), 0, nullptr, a.status, kWaitLimitNs, 41) && ok;
+  };
+  if (folded) {
+    // the row's histogram: the sum of the indexer CTAs' partials for it.
+    // Thread t sums the bin pair t (one 32-bit word holds two 16-bit bins),
+    // kSumBatch partials' loads in flight at once.  (Partial j = 1 of an
+    // indexer CTA is its second row: only the first CTA of the row can hold
+    // the row there, when its slots begin in the row before.)
+    const int64_t first = row * a.part_nblk;
+    const int64_t c_lo = part_owner(first, a.part_total, a.part_grid);
+    const int64_t c_hi = part_owner(first + a.part_nblk - 1, a.part_total, a.part_grid);
+    const int np = static_cast<int>(c_hi - c_lo + 1);
+    const bool lo_second = a.part_total * c_lo / a.part_grid < first;
+    const uint32_t* base = reinterpret_cast<const uint32_t*>(a.hist_part + c_lo * 2 * kBins) + tid;
+    uint32_t c2[2] = {0u, 0u};
+    for (int q0 = 0; q0 < np; q0 += kSumBatch) {
+      uint32_t v[kSumBatch];
+#pragma unroll
+      for (int u = 0; u < kSumBatch; ++u) {
+        const int q = q0 + u;
+        // partial (c_lo + q, j) starts (2 q + j) * kBins / 2 words from base
+        v[u] = q < np ? __ldcg(base + (2 * q + (q == 0 && lo_second ? 1 : 0)) * (kBins / 2)) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kSumBatch; ++u) {
+        c2[0] += v[u] & 0xffffu;
+        c2[1] += v[u] >> 16;
+      }
+    }
+    sh.hist[2 * tid] = c2[0];
+    sh.hist[2 * tid + 1] = c2[1];
+    cluster_wait();  // (A)
+  } else {
+    // this slice's histogram, added into the leader's, which every CTA reads
+    // back once all slices are in
+    for (int c = 0; c * kSliceChunk < n_st; ++c) {
+      chunk_wait(c);
+      const int e1 = min(n_st, (c + 1) * kSliceChunk);
+      for (int e = c * kSliceChunk + tid; e < e1; e += kClusterThreads)
+        atomicAdd(&sh.hist[order_key(sslice[e]) >> 21], 1u);
+    }
+    for (int64_t e = lo + n_st + tid; e < hi; e += kClusterThreads)
+      atomicAdd(&sh.hist[order_key(__ldcg(src + e)) >> 21], 1u);
+    __syncthreads();
+    cluster_wait();  // (A)
+    for (int i = tid; i < kBins; i += kClusterThreads)
+      if (sh.hist[i]) red_add_cluster(mapa_shared(smem_u32(&sh.rowhist[i]), 0), sh.hist[i]);
+    cluster_arrive();
+    cluster_wait();  // (B) every slice is in the leader's histogram
+    const uint32_t rh = mapa_shared(smem_u32(sh.rowhist), 0);
+    for (int i = tid; i < kBins / 4; i += kClusterThreads)
+      reinterpret_cast<uint4*>(sh.hist)[i] = ld_cluster_v4(rh + 16u * i);
+  }
+  __syncthreads();
+  find_digit_desc(sh.hist, kBins, static_cast<uint32_t>(a.k), &sh.scan, tid, kClusterThreads);
   const uint32_t d0 = sh.scan.digit;
   const uint32_t n_above = sh.scan.above;  // keys in bins above d0: all selected
-  int* ctr = a.ctr + row * 4;              // [0] above appended, [1] candidates, [2] tickets
-  int32_t* cand = a.cand + row * a.N_cap;
-  const float* src = a.scores + row * a.N_cap;
-  // Sweep the slice: above the bin -> the output, in the bin -> the
-  // candidates.  Both go to shared-memory lists first (a slice holds few of
-  // either), then one global reservation per list; entries beyond a list's
-  // capacity (a slice of near-equal scores) are appended one by one.
-  auto place = [&](int64_t e, float v) {
-    const uint32_t d = order_key(v) >> 21;
-    if (d > d0) {
-      const int p = atomicAdd(&sh.n_up, 1);
-      if (p < kListCap) {
-        sh.up[p] = static_cast<int32_t>(e);
-      } else {
-        const int q = atomicAdd(&ctr[0], 1);
-        if (q < a.k) out[q] = static_cast<int32_t>(e);
-      }
-    } else if (d == d0) {
-      const int p = atomicAdd(&sh.n_in, 1);
-      if (p < kListCap) {
-        sh.in[p] = static_cast<int32_t>(e);
-      } else {
-        const int q = atomicAdd(&ctr[1], 1);
-        if (q < a.N_cap) cand[q] = static_cast<int32_t>(e);
+  int32_t* cand_g = a.cand + row * a.N_cap;  // candidates past the leader's capacity
+  SweepCtx x;
+  x.sh = &sh;
+  x.out = out;
+  x.cand_g = cand_g;
+  x.r_up = mapa_shared(smem_u32(&sh.n_up), 0);
+  x.r_cand = mapa_shared(smem_u32(&sh.n_cand), 0);
+  x.r_ckey = mapa_shared(smem_u32(ckey), 0);
+  x.r_cidx = mapa_shared(smem_u32(cidx), 0);
+  x.r_hist2 = mapa_shared(smem_u32(sh.hist2), 0);
+  x.k = a.k;
+  x.N_cap = a.N_cap;
+  // Sweep the slice: an entry at or above the threshold bin goes to
+  // sweep_take; the rest (all but a few per thousand) cost a compare.
+  for (int c = 0; c * kSliceChunk < n_st; ++c) {
+    if (!folded) {
+      // (waited for in the histogram pass)
+    } else {
+      chunk_wait(c);
+    }
+    const int e1 = min(n_st, (c + 1) * kSliceChunk);
+    const float4* s4 = reinterpret_cast<const float4*>(sslice);
+    for (int q = (c * kSliceChunk >> 2) + tid; 4 * q < e1; q += kClusterThreads) {
+      const float4 v = s4[q];
+      const uint32_t k0 = order_key(v.x), k1 = order_key(v.y);
+      const uint32_t k2 = order_key(v.z), k3 = order_key(v.w);
+      if (max(max(k0, k1), max(k2, k3)) >> 21 >= d0) {
+        const int64_t e = lo + 4 * q;
+        // (entries past the visible count are not swept)
+        if ((k0 >> 21) >= d0 && 4 * q < e1) sweep_take(x, e, k0, d0);
+        if ((k1 >> 21) >= d0 && 4 * q + 1 < e1) sweep_take(x, e + 1, k1, d0);
+        if ((k2 >> 21) >= d0 && 4 * q + 2 < e1) sweep_take(x, e + 2, k2, d0);
+        if ((k3 >> 21) >= d0 && 4 * q + 3 < e1) sweep_take(x, e + 3, k3, d0);
       }
     }
-  };
-  if (hi <= lo) {
-    // nothing visible in this slice
-  } else if (a.vec4) {
-    const int64_t q_hi = hi >> 2;
-    for (int64_t q0 = (lo >> 2) + tid; q0 < q_hi; q0 += kLoadBatch * kPickThreads) {
-      float4 v[kLoadBatch];
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u) {
-        const int64_t q = q0 + static_cast<int64_t>(u) * kPickThreads;
-        v[u] = q < q_hi ? __ldcg(reinterpret_cast<const float4*>(src) + q)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u) {
-        const int64_t q = q0 + static_cast<int64_t>(u) * kPickThreads;
-        if (q >= q_hi) break;
-        place(4 * q, v[u].x);
-        place(4 * q + 1, v[u].y);
-        place(4 * q + 2, v[u].z);
-        place(4 * q + 3, v[u].w);
-      }
-    }
-    for (int64_t e = (q_hi << 2) + tid; e < hi; e += kPickThreads) place(e, __ldcg(src + e));
-  } else {
-    for (int64_t e = lo + tid; e < hi; e += kPickThreads) place(e, __ldcg(src + e));
   }
+  for (int64_t e = lo + n_st + tid; e < hi; e += kClusterThreads) {
+    const uint32_t key = order_key(__ldcg(src + e));
+    if ((key >> 21) >= d0) sweep_take(x, e, key, d0);
+  }
+  // the staged chunks past the visible entries were never waited for
+  for (int c = 0; c * kSliceChunk < staged; ++c)
+    if (c * kSliceChunk >= n_st) chunk_wait(c);
   __syncthreads();
-  const int nu = min(sh.n_up, kListCap), ni = min(sh.n_in, kListCap);
+  // one reservation per list in the row's lists, then the copies
+  const int nu = min(sh.l_up, kUpCap), nc = min(sh.l_cand, kLocalCand);
   if (tid == 0) {
-    sh.base_up = nu ? atomicAdd(&ctr[0], nu) : 0;
-    sh.base_in = ni ? atomicAdd(&ctr[1], ni) : 0;
+    sh.base_up = nu ? static_cast<int>(atom_add_cluster(x.r_up, static_cast<uint32_t>(nu))) : 0;
+    sh.base_cand = nc ? static_cast<int>(atom_add_cluster(x.r_cand, static_cast<uint32_t>(nc))) : 0;
   }
   __syncthreads();
-  for (int i = tid; i < nu; i += kPickThreads)
+  for (int i = tid; i < nu; i += kClusterThreads)
     if (sh.base_up + i < a.k) out[sh.base_up + i] = sh.up[i];
-  for (int i = tid; i < ni; i += kPickThreads)
-    if (sh.base_in + i < a.N_cap) cand[sh.base_in + i] = sh.in[i];
-  // the last CTA of the row to get here ranks the candidates
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh.last = atomicAdd(&ctr[2], 1) == a.S - 1;
-  __syncthreads();
-  if (!sh.last) return;
-  __threadfence();
-  const int C = min(__ldcg(&ctr[1]), static_cast<int>(a.N_cap));
+  for (int i = tid; i < nc; i += kClusterThreads) {
+    const uint32_t q = static_cast<uint32_t>(sh.base_cand + i);
+    if (q < static_cast<uint32_t>(kCandCap)) {
+      st_cluster_u32(x.r_ckey + 4u * q, sh.lkey[i]);
+      st_cluster_u32(x.r_cidx + 4u * q, static_cast<uint32_t>(sh.lidx[i]));
+    } else if (static_cast<int64_t>(q) - kCandCap < a.N_cap) {
+      cand_g[q - kCandCap] = sh.lidx[i];
+    }
+  }
+  for (int i = tid; i < kBins; i += kClusterThreads)
+    if (sh.lhist2[i]) red_add_cluster(x.r_hist2 + 4u * i, sh.lhist2[i]);
+  // (C) the row's candidates are with the leader (and in the overflow
+  // list); the other CTAs are done and their shared memory is not read
+  cluster_arrive();
+  cluster_wait();
+  if (!leader || !ok) return;
+  const int C = min(sh.n_cand, static_cast<int>(min(a.N_cap, static_cast<int64_t>(INT32_MAX))));
   const uint32_t need = static_cast<uint32_t>(a.k) - n_above;  // 1 <= need <= C
   int32_t* rest = out + n_above;
+  auto idx_of = [&](int c) -> int32_t {
+    return c < kCandCap ? cidx[c] : __ldcg(cand_g + (c - kCandCap));
+  };
+  auto key_of = [&](int c) -> uint32_t {
+    return c < kCandCap ? ckey[c] : order_key(__ldcg(src + __ldcg(cand_g + (c - kCandCap))));
+  };
   if (static_cast<int>(need) >= C) {
-    for (int c = tid; c < C; c += kPickThreads) rest[c] = __ldcg(cand + c);
+    for (int c = tid; c < C; c += kClusterThreads) rest[c] = idx_of(c);
     return;
   }
-  if (C <= kCandSmem) {
-    // the candidates and their keys into shared memory, in one gather
-    int32_t* cj = reinterpret_cast<int32_t*>(pick_dyn);
-    uint32_t* ck = reinterpret_cast<uint32_t*>(pick_dyn + kCandSmem * 4);
-    for (int c0 = tid; c0 < C; c0 += kLoadBatch * kPickThreads) {
-      int32_t j[kLoadBatch];
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u) {
-        const int c = c0 + u * kPickThreads;
-        j[u] = c < C ? __ldcg(cand + c) : 0;
+  // The second digit's bin from the gathered histogram, then one pass: the
+  // candidates above that bin are selected, those in it listed.  The list
+  // is a few entries for spread-out scores; one warp ranks up to 32 of them
+  // (key descending, then entry index ascending), else the general ranking
+  // runs.
+  find_digit_desc(sh.hist2, kBins, need, &sh.scan, tid, kClusterThreads);
+  const uint32_t p1 = (d0 << 11) | sh.scan.digit;
+  const uint32_t above1 = sh.scan.above;
+  const uint32_t need1 = need - above1;  // >= 1
+  if (tid == 0) {
+    sh.n_gt = 0;
+    sh.n_bin = 0;
+  }
+  __syncthreads();
+  for (int c0 = 0; c0 < C; c0 += kClusterThreads) {
+    const int c = c0 + tid;
+    const uint32_t p = c < C ? key_of(c) >> 10 : 0u;
+    const bool gt = c < C && p > p1;
+    const bool in = c < C && p == p1;
+    const int g = warp_append(&sh.n_gt, gt);
+    if (gt && g < static_cast<int>(above1)) rest[g] = idx_of(c);
+    const int b = warp_append(&sh.n_bin, in);
+    if (in && b < kLocalCand) sh.lidx[b] = c;
+  }
+  __syncthreads();
+  const int nb = sh.n_bin;
+  if (nb <= 32) {
+    if (tid < 32) {
+      // bitonic sort of the bin's (key, index) pairs over one warp, best first
+      const int lane = tid;
+      uint32_t key = 0u;
+      int32_t j = INT32_MAX;
+      if (lane < nb) {
+        key = key_of(sh.lidx[lane]);
+        j = idx_of(sh.lidx[lane]);
       }
-      float v[kLoadBatch];
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u) v[u] = __ldcg(src + j[u]);
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u) {
-        const int c = c0 + u * kPickThreads;
-        if (c < C) {
-          cj[c] = j[u];
-          ck[c] = order_key(v[u]);
+      for (int kk = 2; kk <= 32; kk <<= 1) {
+        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+          const uint32_t ok2 = __shfl_xor_sync(0xffffffffu, key, jj);
+          const int32_t oj = __shfl_xor_sync(0xffffffffu, j, jj);
+          const bool mine_first = key > ok2 || (key == ok2 && j < oj);
+          const bool lower = (lane & jj) == 0;
+          const bool best_first = (lane & kk) == 0;
+          if ((lower == best_first) != mine_first) {
+            key = ok2;
+            j = oj;
+          }
         }
       }
+      if (lane < static_cast<int>(need1)) rest[above1 + lane] = j;
     }
-    __syncthreads();
-    rank_candidates(C, need, d0, rest, sh, [&](int c) { return cj[c]; },
-                    [&](int c) { return ck[c]; });
   } else {
-    rank_candidates(C, need, d0, rest, sh, [&](int c) { return __ldcg(cand + c); },
-                    [&](int c) { return order_key(__ldcg(src + __ldcg(cand + c))); });
+    rank_candidates(C, need, d0, sh.hist2, rest, sh, idx_of, key_of);
   }
 }
 
@@ -649,8 +766,8 @@ static_assert(sizeof(RowShared) + kRowMaxKeys * 4 <= 227 * 1024,
 bool plan_topk(int64_t rows, int64_t N_cap, int k, int num_sms, TopkPlan* p) {
   if (rows <= 0 || N_cap < 1 || k < 1) return false;
   *p = TopkPlan{};
-  // Few long rows spread over many CTAs (slice path); otherwise one CTA per
-  // row with the keys in shared memory (row path).
+  // Few long rows spread over a cluster of CTAs each (cluster path);
+  // otherwise one CTA per row with the keys in shared memory (row path).
   const bool row_fits = N_cap <= kRowMaxKeys;
   const bool few_rows = rows * 2 < num_sms;
   if (row_fits && (!few_rows || N_cap <= 8192)) {
@@ -660,18 +777,12 @@ bool plan_topk(int64_t rows, int64_t N_cap, int k, int num_sms, TopkPlan* p) {
     p->smem_bytes = sizeof(RowShared) + static_cast<size_t>(N_cap) * 4;
   } else {
     p->slice_path = true;
-    // about one CTA per SM over all rows; a slice is a multiple of 64
-    // entries and holds at most 65,535 (the bins are 16-bit)
-    int64_t S = num_sms / rows;
-    if (S < 1) S = 1;
-    int64_t slice = ((N_cap + S - 1) / S + 63) / 64 * 64;
-    if (slice > 65472) slice = 65472;
-    S = (N_cap + slice - 1) / slice;
-    if (S > 65535) return false;
-    p->S = static_cast<int>(S);
-    p->slice = slice;
-    p->threads = kPickThreads;
-    p->smem_bytes = 0;
+    // 8 CTAs per row (the portable cluster size: any GPC holds one, so the
+    // rows' clusters start together); a slice is a multiple of 64 entries
+    p->S = kClusterSize;
+    p->slice = ((N_cap + p->S - 1) / p->S + 63) / 64 * 64;
+    p->threads = kClusterThreads;
+    p->smem_bytes = kClusterSmem;
   }
   p->ws_bytes = topk_scratch_bytes(*p, rows, N_cap);
   return true;
@@ -679,21 +790,14 @@ bool plan_topk(int64_t rows, int64_t N_cap, int k, int num_sms, TopkPlan* p) {
 
 size_t topk_scratch_bytes(const TopkPlan& p, int64_t rows, int64_t N_cap) {
   if (!p.slice_path) return 0;
-  const size_t hist = static_cast<size_t>(rows) * p.S * kBins * sizeof(uint16_t);
-  const size_t ctr = static_cast<size_t>(rows) * 4 * sizeof(int32_t);
-  const size_t cand = static_cast<size_t>(rows) * N_cap * sizeof(int32_t);
-  return (hist + 255) / 256 * 256 + (ctr + 255) / 256 * 256 + cand;
+  // the candidates past the leader's shared memory (a row of near-equal scores)
+  return static_cast<size_t>(rows) * N_cap * sizeof(int32_t);
 }
 
 void topk_scratch_carve(const TopkPlan& p, int64_t rows, void* ws, TopkArgs* a) {
-  uint8_t* b = static_cast<uint8_t*>(ws);
-  const size_t hist = static_cast<size_t>(rows) * p.S * kBins * sizeof(uint16_t);
-  const size_t ctr = static_cast<size_t>(rows) * 4 * sizeof(int32_t);
-  a->hist = reinterpret_cast<uint16_t*>(b);
-  b += (hist + 255) / 256 * 256;
-  a->ctr = reinterpret_cast<int32_t*>(b);
-  b += (ctr + 255) / 256 * 256;
-  a->cand = reinterpret_cast<int32_t*>(b);
+  (void)p;
+  (void)rows;
+  a->cand = static_cast<int32_t*>(ws);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, bool dependent,
@@ -705,16 +809,14 @@ cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, bool dependent,
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(p.threads, 1, 1);
   cfg.stream = stream;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   cfg.attrs = at;
-  cfg.numAttrs = add_dependent_attr(at, 0, dependent);
   TopkArgs args = a;
-  args.S = p.S;
-  args.slice = p.slice;
-  args.vec4 = (a.N_cap % 4 == 0) && (reinterpret_cast<uintptr_t>(a.scores) % 16 == 0) &&
-              (p.slice % 4 == 0);
   cudaError_t e;
   if (!p.slice_path) {
+    args.S = 1;
+    args.vec4 = 0;
+    cfg.numAttrs = add_dependent_attr(at, 0, dependent);
     e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(p.smem_bytes));
     if (e != cudaSuccess) return e;
@@ -724,18 +826,21 @@ cudaError_t launch_topk(const TopkArgs& a, const TopkPlan& p, bool dependent,
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
+  args.S = p.S;
+  args.slice = p.slice;
+  args.vec4 = (a.N_cap % 4 == 0) && (reinterpret_cast<uintptr_t>(a.scores) % 16 == 0) &&
+              (p.slice % 4 == 0);
+  e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kClusterSmem));
+  if (e != cudaSuccess) return e;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = static_cast<unsigned>(p.S);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.numAttrs = add_dependent_attr(at, 1, dependent);
   cfg.gridDim = dim3(p.S, static_cast<unsigned>(gy), static_cast<unsigned>(gz));
-  cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, topk_hist_kernel, args);
-  if (e != cudaSuccess) return e;
-  // the pick kernel reads what the histogram kernel wrote: always a
-  // dependent of it (it waits before its first read)
-  cfg.numAttrs = add_dependent_attr(at, 0, true);
-  cfg.dynamicSmemBytes = kCandSmem * 8;
-  e = cudaFuncSetAttribute(topk_pick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kCandSmem * 8);
-  if (e != cudaSuccess) return e;
-  e = cudaLaunchKernelEx(&cfg, topk_pick_kernel, args);
+  cfg.dynamicSmemBytes = kClusterSmem;
+  e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -52,6 +52,8 @@ _SIGS = {
     "hattn_indexer_topk": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                   _vp, _vp, _vp, _sz, _vp]),
     "hattn_indexer_topk_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32, _i32]),
+    "hattn_indexer_topk_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
+                                     _i32, _i32, _i64, _vp, _vp, _vp, _sz, _i32, _vp, _vp]),
     "hattn_indexer_topk_noalloc": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
                                           _i32, _vp, _vp]),
     "hattn_indexer_scores": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _vp,
@@ -92,6 +94,7 @@ _SIGS = {
 }
 
 LAUNCH_DEPENDENT = 1  # HATTN_LAUNCH_DEPENDENT
+EVENT_EXTERNAL = 2  # HATTN_EVENT_EXTERNAL
 
 _lib = None
 
@@ -130,6 +133,17 @@ def _ptr(t):
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _event(ev):
+    """The cudaEvent_t of a torch.cuda.Event that has been recorded once (its
+    CUDA event exists), or None."""
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        raise ValueError("split_event must have been recorded once (its CUDA event is created "
+                         "on the first record)")
+    return ctypes.c_void_p(ev.cuda_event)
 
 
 def _need(t, name, dtype, ndim=None):
@@ -386,9 +400,8 @@ def topk_workspace_bytes(B, T, N_cap, k):
 
 
 def topk_launches(B, T, N_cap, k):
-    """Kernels one top-k selection launches: two when its rows are spread
-    over many CTAs (the calls that need a scratch), else one."""
-    return 2 if topk_workspace_bytes(B, T, N_cap, k) > 0 else 1
+    """Kernels one top-k selection launches (one, on either path)."""
+    return 1
 
 
 def _idx_out(idx_out, B, T, k, device):
@@ -399,9 +412,22 @@ def _idx_out(idx_out, B, T, k, device):
 
 
 def indexer_topk(iq, w, ik_c, pos, *, k, m=4, idx_out=None, score_out=None, workspace=None,
-                 stream=None):
-    """Lightning-indexer scores + per-query top-k; returns idx [B, T, k] int32."""
-    B, T, HI, dI, N_cap = _indexer_inputs(iq, w, ik_c, pos)
+                 ik_scale=None, n_sms=0, fresh_from=-1, dependent=False, split_event=None,
+                 split_external=False, stream=None):
+    """Lightning-indexer scores + per-query top-k; returns idx [B, T, k] int32.
+    ik_scale: given, ik_c holds E4M3 codes uint8 [B, N_cap, 128] with these
+    row scales fp32 [B, N_cap].  n_sms, fresh_from, dependent: as
+    indexer_scores, for the score kernel.  split_event: a torch.cuda.Event
+    (recorded once before) that the call records between the score and the
+    selection kernel: other streams may wait on it for the scores alone, and
+    with split_external (an external event) it times the two kernels
+    apart."""
+    if ik_scale is None:
+        B, T, HI, dI, N_cap = _indexer_inputs(iq, w, ik_c, pos)
+    else:
+        B, T, HI, dI, N_cap = _indexer_inputs(iq, w, ik_c, pos, "ik8", torch.uint8)
+        _need(ik_scale, "ik_scale", torch.float32, 2)
+        _shape(ik_scale, "ik_scale", (B, N_cap))
     idx_out = _idx_out(idx_out, B, T, k, iq.device)
     if score_out is not None:
         _need(score_out, "score_out", torch.float32, 3)
@@ -410,9 +436,18 @@ def indexer_topk(iq, w, ik_c, pos, *, k, m=4, idx_out=None, score_out=None, work
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=iq.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib().hattn_indexer_topk(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI, N_cap,
-                                    k, m, _ptr(idx_out), _ptr(score_out), _ptr(workspace),
-                                    ws_bytes, _stream(stream)))
+    if ik_scale is None and split_event is None and not (n_sms or fresh_from >= 0 or dependent):
+        _check(lib().hattn_indexer_topk(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
+                                        N_cap, k, m, _ptr(idx_out), _ptr(score_out),
+                                        _ptr(workspace), ws_bytes, _stream(stream)))
+    else:
+        _check(lib().hattn_indexer_topk_ex(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(ik_scale),
+                                           _ptr(pos), B, T, HI, dI, N_cap, k, m, n_sms,
+                                           fresh_from, _ptr(idx_out), _ptr(score_out),
+                                           _ptr(workspace), ws_bytes,
+                                           _flags(dependent) | (EVENT_EXTERNAL if split_external
+                                                                else 0),
+                                           _event(split_event), _stream(stream)))
     return idx_out
 
 

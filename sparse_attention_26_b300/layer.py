@@ -56,6 +56,7 @@ class HybridLayer:
         # fused step with a side stream: the indexer, top-k, attention and
         # merge start as dependent launches of their predecessors
         self.dependent_launch = True
+        self._split_event = None  # marks the end of the score kernel in each step
         if build_caches:
             self.build_caches()
         self._bufs = {}
@@ -84,8 +85,8 @@ class HybridLayer:
         b = dict(
             scores=torch.empty((B, T, n_sc), dtype=torch.float32, device=dev),
             idx=torch.empty((B, T, wl.k), dtype=torch.int32, device=dev),
-            ws_topk=torch.empty(max(hattn.topk_workspace_bytes(B, T, n_sc, wl.k), 16),
-                                dtype=torch.uint8, device=dev),
+            ws_topk=torch.empty(max(hattn.indexer_topk_workspace_bytes(B, T, n_sc, wl.k, True),
+                                    16), dtype=torch.uint8, device=dev),
             out=res[:n_out].view(bf).view(B, T, H, D),
             lse=res[n_out:].view(torch.float32).view(B, T, H),
             result=res,
@@ -191,15 +192,34 @@ class HybridLayer:
             hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j0,
                                j_end=j1, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c, ik_c=self.ik_c)
 
-    def _indexer(self, iq, w, pos, scores, n_sms=0, fresh_from=-1, dependent=False):
+    def _indexer_topk(self, iq, w, pos, b, events=None, n_sms=0, fresh_from=-1, dependent=False):
+        """Indexer scores and top-k as one call (the score kernel counts the
+        selection's first pass as it writes the scores).  Returns an event
+        recorded between the two kernels, for other streams to wait on the
+        scores alone.  With events, "indexer" spans the score kernel and
+        "topk" the selection."""
         wl = self.wl
-        if self.fp8:
-            hattn.indexer_scores_fp8(iq, w, self.ik8, self.ik_scale, pos, m=wl.m_csa,
-                                     score_out=scores, n_sms=n_sms, fresh_from=fresh_from,
-                                     dependent=dependent)
+        cur = torch.cuda.current_stream()
+        timed = events is not None and "indexer" in events
+        if timed:
+            events["indexer"][0].record(cur)
+            split = events["indexer"][1]
+            split.record(cur)  # creates its CUDA event; recorded again between the kernels
+            events["topk"] = (split, events["topk"][1])
         else:
-            hattn.indexer_scores(iq, w, self.ik_c, pos, m=wl.m_csa, score_out=scores,
-                                 n_sms=n_sms, fresh_from=fresh_from, dependent=dependent)
+            if self._split_event is None:
+                self._split_event = torch.cuda.Event()
+                self._split_event.record(cur)  # creates its CUDA event
+            split = self._split_event
+        keys = self.ik8 if self.fp8 else self.ik_c
+        hattn.indexer_topk(iq, w, keys, pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"],
+                           score_out=b["scores"], workspace=b["ws_topk"],
+                           ik_scale=self.ik_scale if self.fp8 else None, n_sms=n_sms,
+                           fresh_from=fresh_from, dependent=dependent, split_event=split,
+                           split_external=timed)
+        if timed:
+            events["topk"][1].record(cur)
+        return split
 
     def _compress_new(self, kind, t_new, n_new):
         """Compress the entries that the step's new tokens complete."""
@@ -285,13 +305,7 @@ class HybridLayer:
                 dense_branches()
             joined = side_stream
         if "csa" in wl.branches:
-            ev("indexer", 0)
-            self._indexer(iq, w, pos, b["scores"])
-            ev("indexer", 1)
-            ev("topk", 0)
-            hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"],
-                              workspace=b["ws_topk"])
-            ev("topk", 1)
+            self._indexer_topk(iq, w, pos, b, events)
             ev("sparse", 0)
             parts["csa"] = hattn.sparse_attn(qt, self.kv_c, b["idx"], pos, r=wl.r,
                                              workspace=b["ws_csa"], q_prepped=True,
@@ -387,30 +401,28 @@ class HybridLayer:
         elif side_stream is None:
             qprep()
             swa_keys()
+        scores_done = None
         if "csa" in has:
-            ev("indexer", 0)
             # the entries the compression above writes are the newest ones
             j0, j1 = self.new_entries("csa", t_new, T)
-            self._indexer(iq, w, pos, b["scores"],
-                          n_sms=(self.NUM_SMS - n_dense) if n_dense else 0,
-                          fresh_from=j0 if j1 > j0 else -1, dependent=pdl)
-            ev("indexer", 1)
+            scores_done = self._indexer_topk(iq, w, pos, b, events,
+                                             n_sms=(self.NUM_SMS - n_dense) if n_dense else 0,
+                                             fresh_from=j0 if j1 > j0 else -1, dependent=pdl)
         if side_stream is not None and not overlap:
             # The query preparation, the HCA compression and the window keys
             # (needed only by the attention) run beside top-k, which leaves
-            # most SMs free.  Beside the indexer they would hold SMs its
+            # SMs free.  Beside the indexer they would hold SMs its
             # persistent grid needs from the start, and its statically split
-            # work would end later by as much.
-            side_stream.wait_stream(main)
+            # work would end later by as much.  (With per-call events they
+            # follow the whole call.)
+            if scores_done is not None and (events is None or "indexer" not in events):
+                side_stream.wait_event(scores_done)
+            else:
+                side_stream.wait_stream(main)
             with torch.cuda.stream(side_stream):
                 qprep()
                 compress("hca")
                 swa_keys()
-        if "csa" in has:
-            ev("topk", 0)
-            hattn.topk_select(b["scores"], pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"],
-                              workspace=b["ws_topk"], dependent=pdl)
-            ev("topk", 1)
         if overlap:
             parts = [attn("sparse", hattn.SEG_CSA, 0, dependent=pdl)]
             main.wait_stream(side_stream)

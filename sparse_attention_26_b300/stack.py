@@ -74,7 +74,7 @@ class DecodeStack:
         self.kv_w = torch.empty((B, T, W, D), dtype=bf, device=device)
         self.scores = torch.empty((B, T, self.N_csa), dtype=torch.float32, device=device)
         self.idx = torch.empty((B, T, k), dtype=torch.int32, device=device)
-        ws = hattn.topk_workspace_bytes(B, T, self.N_csa, k)
+        ws = hattn.indexer_topk_workspace_bytes(B, T, self.N_csa, k, True)
         self.ws_topk = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         self.topk_launches = hattn.topk_launches(B, T, self.N_csa, k)
         self.out = torch.empty((len(self.kinds), B, T, H, D), dtype=bf, device=device)
@@ -160,10 +160,9 @@ class DecodeStack:
                                         j_begin=j, j_end=j + 1, kv_c=st["kv_c"], ik_c=st["ik_c"],
                                         m=self.m_csa, w=self.w_csa, eps=self.eps)
             fresh = (t + 1) // self.m_csa - 1 if (t + 1) % self.m_csa == 0 else -1
-            hattn.indexer_scores(iq, w, st["ik_c"], pos, m=self.m_csa, score_out=self.scores,
-                                 fresh_from=fresh, dependent=dep)
-            hattn.topk_select(self.scores, pos, k=self.k, m=self.m_csa, idx_out=self.idx,
-                              workspace=self.ws_topk, dependent=dep)
+            hattn.indexer_topk(iq, w, st["ik_c"], pos, k=self.k, m=self.m_csa, idx_out=self.idx,
+                               score_out=self.scores, workspace=self.ws_topk, fresh_from=fresh,
+                               dependent=dep)
         elif kind == HCA and (t + 1) % self.m_hca == 0:
             j = (t + 1) // self.m_hca - 1
             hattn.hca_compress_ring(st["kv_ring"], st["gate_ring"], r=r, j_begin=j, j_end=j + 1,

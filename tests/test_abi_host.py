@@ -120,11 +120,24 @@ def test_indexer_validation(L):
     assert rc == hattn.INVALID_ARG
     rc = L.hattn_indexer_topk(FAKE, FAKE, FAKE, N, 1, 1, 64, 128, 100, 16, 4, FAKE, N, N, 0, N)
     assert rc == hattn.INVALID_ARG and "pos" in _err(L)
-    # the scores, then the selection's scratch; rows that fit one CTA need none
+    # the scores, the score kernel's partial histograms (two rows of 2,048
+    # 16-bit bins per CTA, one CTA per SM: 148 without a device), then the
+    # selection's scratch; rows that fit one CTA need neither of the last two
     sel = L.hattn_topk_workspace_bytes(8, 1, 262144, 1024)
-    assert sel >= 8 * 262144 * 4  # at least one candidate slot per entry
-    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 0) == 8 * 262144 * 4 + sel
-    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 1) == sel
+    assert sel == 8 * 262144 * 4  # one candidate slot per entry
+    hist = 148 * 2 * 2048 * 2
+    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 0) == 8 * 262144 * 4 + hist + sel
+    assert L.hattn_indexer_topk_workspace_bytes(8, 1, 262144, 1024, 1) == hist + sel
+    # the extended call checks its own arguments before any launch
+    rc = L.hattn_indexer_topk_ex(FAKE, FAKE, FAKE, N, FAKE, 8, 1, 64, 128, 262144, 1024, 4, 0, -1,
+                                 FAKE, N, FAKE, hist + sel, 8, N, N)
+    assert rc == hattn.INVALID_ARG and "flags" in _err(L)
+    rc = L.hattn_indexer_topk_ex(FAKE, FAKE, FAKE, N, FAKE, 8, 1, 64, 128, 262144, 1024, 4, -1, -1,
+                                 FAKE, N, FAKE, hist + sel, 0, N, N)
+    assert rc == hattn.INVALID_ARG and "n_sms" in _err(L)
+    rc = L.hattn_indexer_topk_ex(FAKE, FAKE, FAKE, N, FAKE, 8, 1, 64, 128, 262144, 1024, 4, 0, -1,
+                                 FAKE, FAKE, FAKE, hist + sel - 1, 0, N, N)
+    assert rc == hattn.INVALID_ARG and "workspace" in _err(L)
     assert L.hattn_topk_workspace_bytes(8192, 1, 2048, 512) == 0
     assert L.hattn_indexer_topk_workspace_bytes(1, 8192, 2048, 512, 0) == 8192 * 2048 * 4
 
@@ -136,7 +149,7 @@ def test_topk_validation(L):
     s = None
     sel = L.hattn_topk_workspace_bytes(8, 1, 262144, 1024)
     # hattn_topk_select(scores, pos, B, T, N_cap, k, m, idx_out, ws, ws_bytes, flags, stream)
-    rc = L.hattn_topk_select(FAKE, FAKE, 8, 1, 262144, 1024, 4, FAKE, FAKE, sel, 2, s)
+    rc = L.hattn_topk_select(FAKE, FAKE, 8, 1, 262144, 1024, 4, FAKE, FAKE, sel, 4, s)
     assert rc == hattn.INVALID_ARG and "flags" in _err(L)
     rc = L.hattn_topk_select(FAKE, FAKE, 8, 1, 262144, 1024, 4, FAKE, N, 0, 0, s)
     assert rc == hattn.INVALID_ARG and "workspace" in _err(L)

@@ -108,32 +108,32 @@ def _meta_layer(name):
 
 def test_launch_counts_match_the_recorded_launch_lists():
     """The kernels one decode step launches, as the bench counts them for
-    gpu_launches, equal the ncu launch lists of the same steps (99 launches
+    gpu_launches, equal the ncu launch lists of the same steps (88 launches
     over 11 steps in profiles/launches_hybrid_decode_1m.md and
     profiles/launches_hybrid_decode_1m_mtp2.md): two compressions, window
-    keys, query prep, indexer, the two top-k kernels (eight rows of 262,144
-    scores spread over many CTAs), the fused attention and the merge."""
+    keys, query prep, the indexer, the top-k kernel (a cluster of CTAs per
+    row of 262,144 scores), the fused attention and the merge."""
     for name, T in (("hybrid_decode_1m", 1), ("hybrid_decode_1m_mtp2", 2)):
         wl, layer = _meta_layer(name)
         n = layer.launches_per_step(T, wl.L - 1, side_stream=True)
-        assert n == 99 // 11 == 9, (name, n)
+        assert n == 88 // 11 == 8, (name, n)
         assert len(layer.event_names(T)) == 7  # one span covers both compressions
     # a step whose token completes no entry skips both compressions
     wl, layer = _meta_layer("hybrid_decode_1m")
-    assert layer.launches_per_step(1, wl.L - 2, side_stream=True) == 7
+    assert layer.launches_per_step(1, wl.L - 2, side_stream=True) == 6
 
 
 def test_stack_launch_count_at_1m():
-    """The 61-layer decode step at t = 2^20 - 1 launches 393 kernels: every
+    """The 61-layer decode step at t = 2^20 - 1 launches 363 kernels: every
     layer query prep, window keys, attention and merge; a CSA layer adds the
-    indexer, the two top-k kernels and its new entry's compression, an HCA
-    layer its new entry's compression (t + 1 is a multiple of 4 and of 128)."""
+    indexer, the top-k kernel and its new entry's compression, an HCA layer
+    its new entry's compression (t + 1 is a multiple of 4 and of 128)."""
     from sparse_attention_26_b300.stack import DecodeStack, layer_pattern
     wl = synth.WORKLOADS["hybrid_decode_1m"]
     st = DecodeStack(layer_pattern(61), B=wl.B, H=wl.H, D=wl.D, r=wl.r, HI=wl.HI, dI=wl.dI,
                      k=wl.k, L_max=wl.L, device="meta")
-    assert st.launches_per_step(wl.L - 1) == 2 * 4 + 30 * 8 + 29 * 5 == 393
-    assert st.launches_per_step(wl.L - 2) == 2 * 4 + 30 * 7 + 29 * 4
+    assert st.launches_per_step(wl.L - 1) == 2 * 4 + 30 * 7 + 29 * 5 == 363
+    assert st.launches_per_step(wl.L - 2) == 2 * 4 + 30 * 6 + 29 * 4
 
 
 def test_which_steps_take_the_fused_attention():

@@ -248,7 +248,7 @@ HATTN_API size_t hattn_indexer_topk_workspace_bytes(int B, int T, int64_t N_cap,
  *   hattn_indexer_scores_fp8 for the limits and the arithmetic).
  *   n_sms, fresh_from, flags: as hattn_indexer_scores_ex, for the score
  *   kernel; the selection kernel is always launched as a programmatic
- *   dependent of it and reads nothing before its wait.
+ *   dependent of it and reads only pos before its wait.
  *   workspace: hattn_indexer_topk_workspace_bytes() bytes, as above.
  *   split_event: a cudaEvent_t (cast to void*) recorded on `stream` between
  *   the score and the selection kernel, or NULL: other streams may wait for
@@ -316,7 +316,9 @@ HATTN_API int hattn_indexer_scores_ex(const void* iq, const float* w, const void
  * scores); it is 0 when the rows fit one CTA each, and workspace may then be
  * NULL.  The scratch needs no initialisation; calls sharing one scratch must
  * not overlap on the GPU.
- * flags: HATTN_LAUNCH_DEPENDENT or 0 (every input is read after the wait). */
+ * flags: HATTN_LAUNCH_DEPENDENT or 0 (with the flag, the cluster path reads
+ * pos before the wait, so the previous kernel must not write pos; the
+ * scores are read after it). */
 HATTN_API size_t hattn_topk_workspace_bytes(int B, int T, int64_t N_cap, int k);
 HATTN_API int hattn_topk_select(const float* scores, const int32_t* pos, int B, int T,
                                 int64_t N_cap, int k, int m, int32_t* idx_out, void* workspace,

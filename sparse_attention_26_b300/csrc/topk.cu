@@ -85,6 +85,100 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, ScanShared*
   return r;
 }
 
+// Exclusive prefixes of two per-thread counts over the threads of the block,
+// in thread order, and their totals (*tot_a, *tot_b).  One pass: the pair
+// travels as one 64-bit value.
+__device__ __forceinline__ void block_exclusive_scan2(uint32_t a, uint32_t b, uint32_t* pa,
+                                                      uint32_t* pb, uint32_t* tot_a,
+                                                      uint32_t* tot_b, uint64_t* warp_tot,
+                                                      int tid, int nthr) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint64_t v = (static_cast<uint64_t>(a) << 32) | b;
+  uint64_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t x = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += x;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nthr >> 5;
+    const uint64_t w = lane < nw ? warp_tot[lane] : 0;
+    uint64_t t = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t x = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += x;
+    }
+    if (lane < nw) warp_tot[lane] = t - w;
+    if (lane == nw - 1) warp_tot[32] = t;
+  }
+  __syncthreads();
+  const uint64_t r = warp_tot[warp] + inc - v;
+  *pa = static_cast<uint32_t>(r >> 32);
+  *pb = static_cast<uint32_t>(r);
+  *tot_a = static_cast<uint32_t>(warp_tot[32] >> 32);
+  *tot_b = static_cast<uint32_t>(warp_tot[32]);
+  __syncthreads();  // warp_tot is reused by the next scan
+}
+
+// find_digit_desc by one warp (nb = 1024 or 2048 bins, nb / 32 per lane,
+// lane 0 the top ones), which leaves the other warps free and takes one
+// block barrier instead of four.  Every thread of the block calls it.
+__device__ __noinline__ void find_digit_desc_warp(const uint32_t* h, int nb, uint32_t need,
+                                                  ScanShared* sh, int tid) {
+  if (tid < 32) {
+    const int lane = tid;
+    const int per = nb >> 5;
+    const int hi = nb - per * lane;  // this lane's bins: [hi - per, hi)
+    uint32_t tot = 0;
+    const uint4* h4 = reinterpret_cast<const uint4*>(h + hi - per);
+    for (int i = 0; i < per / 4; ++i) {
+      const uint4 v = h4[i];
+      tot += v.x + v.y + v.z + v.w;
+    }
+    uint32_t inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += x;
+    }
+    const uint32_t before = inc - tot;
+    const unsigned who = __ballot_sync(0xffffffffu, before < need && inc >= need);
+    if (who == 0) {
+      if (lane == 0) {  // (need beyond the total: no bin)
+        sh->digit = 0;
+        sh->above = 0;
+      }
+    } else {
+      // the found lane's per bins, per / 32 to a lane (top first), scanned
+      // again across the warp
+      const int f = __ffs(who) - 1;
+      const uint32_t base_before = __shfl_sync(0xffffffffu, before, f);
+      const int fhi = nb - per * f;
+      const int sub = per >> 5;  // 1 or 2
+      const int my_hi = fhi - sub * lane;
+      uint32_t t2 = h[my_hi - 1];
+      if (sub == 2) t2 += h[my_hi - 2];
+      uint32_t inc2 = t2;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, inc2, o);
+        if (lane >= o) inc2 += x;
+      }
+      const uint32_t b2 = base_before + inc2 - t2;
+      if (b2 < need && b2 + t2 >= need) {
+        const uint32_t c0 = h[my_hi - 1];
+        const bool first = b2 + c0 >= need || sub == 1;
+        sh->digit = static_cast<uint32_t>(first ? my_hi - 1 : my_hi - 2);
+        sh->above = first ? b2 : b2 + c0;
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // The bin holding the need-th largest key (1 <= need <= total): bins are
 // visited from the top; sh->digit = that bin, sh->above = keys in the bins
 // above it.  nb >= nthr, both powers of two.
@@ -322,9 +416,8 @@ constexpr int kSumBatch = 24;            // partial histograms whose loads a thr
 constexpr int kSliceChunk = 8192;        // entries per bulk copy of the slice (32 KB)
 constexpr int kSliceChunks = 4;
 constexpr int kMaxSlice = kSliceChunk * kSliceChunks;  // entries a CTA stages in shared memory
-constexpr int kUpCap = 2048;             // a CTA's list of entries above the threshold bin
-constexpr int kLocalCand = 2048;         // a CTA's list of candidates (entries in that bin)
-constexpr int kCandCap = 4096;           // candidates the leader holds in shared memory
+constexpr int kCandCap = 6144;           // candidates the leader holds in shared memory
+constexpr int kBinCap = 2048;            // the leader's list of one second-digit bin
 static_assert(kBins == 2 * kClusterThreads, "one bin pair per thread");
 
 struct ClusterShared {
@@ -333,13 +426,11 @@ struct ClusterShared {
   alignas(16) uint32_t rowhist[kBins];  // leader, no folded pass: the slices' top-digit histograms summed
   alignas(16) uint32_t hist2[kBins];    // leader: the row's candidates' second-digit histogram
   alignas(16) uint32_t lhist2[kBins];   // this CTA's candidates' second-digit histogram
-  alignas(16) int32_t up[kUpCap];
-  alignas(16) uint32_t lkey[kLocalCand];
-  alignas(16) int32_t lidx[kLocalCand];  // the leader reuses it for its bin list
+  alignas(16) int32_t binlist[kBinCap];  // leader: the candidates in one second-digit bin
   uint64_t chunk_full[kSliceChunks];     // the slice's bulk copies have landed
+  uint64_t wtot[33];                     // block_exclusive_scan2's warp totals
   ScanShared scan;
   int n_up, n_cand;         // leader: the row's list fills
-  int l_up, l_cand;         // this CTA's list fills
   int base_up, base_cand;   // this CTA's ranges in the row's lists
   int n_gt, n_eq, n_bin;
 };
@@ -368,7 +459,7 @@ __device__ __noinline__ void rank_candidates(int C, uint32_t need, uint32_t d0, 
   const int tid = threadIdx.x;
   const int room = static_cast<int>(need);
   // second digit from the gathered histogram, third by one pass
-  find_digit_desc(h2, kBins, need, &sh.scan, tid, kClusterThreads);
+  find_digit_desc_warp(h2, kBins, need, &sh.scan, tid);
   uint32_t prefix = (d0 << 11) | sh.scan.digit;
   need -= sh.scan.above;
   for (int i = tid; i < kBins; i += kClusterThreads) sh.hist[i] = 0;
@@ -378,7 +469,7 @@ __device__ __noinline__ void rank_candidates(int C, uint32_t need, uint32_t d0, 
     if ((key >> 10) == prefix) atomicAdd(&sh.hist[key & 1023u], 1u);
   }
   __syncthreads();
-  find_digit_desc(sh.hist, 1024, need, &sh.scan, tid, kClusterThreads);
+  find_digit_desc_warp(sh.hist, 1024, need, &sh.scan, tid);
   const uint32_t thr = (prefix << 10) | sh.scan.digit;  // the k-th largest key
   need -= sh.scan.above;                                // its ties still to take
   // candidates above the threshold, and the count of ties at it (the loop
@@ -442,50 +533,6 @@ __device__ __noinline__ void rank_candidates(int C, uint32_t need, uint32_t d0, 
   }
 }
 
-// Where the sweep sends an entry at or above the threshold bin d0 (a few
-// per thousand): above it to this CTA's list of selected entries, in it to
-// its candidate list and second-digit counts; past a list's capacity (a
-// slice of near-equal scores) to the row's lists in the leader CTA one by
-// one.  Not inlined: the sweep's unrolled loop stays small, and one copy of
-// this code serves every call (a short kernel runs most code only once, so
-// its size is instruction-fetch time).
-struct SweepCtx {
-  ClusterShared* sh;
-  int32_t* out;     // the row's k output places
-  int32_t* cand_g;  // the row's overflow candidates
-  uint32_t r_up, r_cand, r_ckey, r_cidx, r_hist2;  // leader addresses
-  int k;
-  int64_t N_cap;
-};
-__device__ __noinline__ void sweep_take(const SweepCtx& x, int64_t e, uint32_t key, uint32_t d0) {
-  ClusterShared& sh = *x.sh;
-  if ((key >> 21) > d0) {
-    const int p = atomicAdd(&sh.l_up, 1);
-    if (p < kUpCap) {
-      sh.up[p] = static_cast<int32_t>(e);
-    } else {
-      const uint32_t q = atom_add_cluster(x.r_up, 1u);
-      if (q < static_cast<uint32_t>(x.k)) x.out[q] = static_cast<int32_t>(e);
-    }
-    return;
-  }
-  const int p = atomicAdd(&sh.l_cand, 1);
-  if (p < kLocalCand) {
-    sh.lkey[p] = key;
-    sh.lidx[p] = static_cast<int32_t>(e);
-    atomicAdd(&sh.lhist2[(key >> 10) & 2047u], 1u);
-    return;
-  }
-  const uint32_t q = atom_add_cluster(x.r_cand, 1u);
-  if (q < static_cast<uint32_t>(kCandCap)) {
-    st_cluster_u32(x.r_ckey + 4u * q, key);
-    st_cluster_u32(x.r_cidx + 4u * q, static_cast<uint32_t>(e));
-  } else if (static_cast<int64_t>(q) - kCandCap < x.N_cap) {
-    x.cand_g[q - kCandCap] = static_cast<int32_t>(e);
-  }
-  red_add_cluster(x.r_hist2 + 4u * ((key >> 10) & 2047u), 1u);
-}
-
 // One cluster of kClusterSize CTAs per row; CTA r of the cluster sweeps
 // entries [r * slice, (r + 1) * slice) of the row.
 __global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const TopkArgs a) {
@@ -509,6 +556,9 @@ __global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const 
     for (int c = 0; c < kSliceChunks; ++c) mbar_init(smem_u32(&sh.chunk_full[c]), 1);
     fence_barrier_init();
   }
+  // the visible count: pos is an input of the step, read before the wait
+  // (as the score kernel does)
+  const int64_t n = row < a.rows ? visible_count(a.pos[row], a.m, a.N_cap) : 0;
   __syncthreads();
   pdl_trigger();
   pdl_wait();  // the scores (and the folded histograms) are complete
@@ -531,7 +581,6 @@ __global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const 
       mbar_wait(smem_u32(&sh.chunk_full[c]), 0, nullptr, a.status, kWaitLimitNs, 41);
   };
   if (row >= a.rows) return;  // (nothing staged)
-  const int64_t n = visible_count(a.pos[row], a.m, a.N_cap);
   int32_t* out = a.idx + row * a.k;
   const int64_t hi = lo + a.slice < n ? lo + a.slice : n;
   if (n <= a.k) {
@@ -552,8 +601,6 @@ __global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const 
     if (!folded) sh.hist[i] = 0;
   }
   if (tid == 0) {
-    sh.l_up = 0;
-    sh.l_cand = 0;
     sh.n_up = 0;
     sh.n_cand = 0;
   }
@@ -617,73 +664,87 @@ __global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const 
       reinterpret_cast<uint4*>(sh.hist)[i] = ld_cluster_v4(rh + 16u * i);
   }
   __syncthreads();
-  find_digit_desc(sh.hist, kBins, static_cast<uint32_t>(a.k), &sh.scan, tid, kClusterThreads);
+  find_digit_desc_warp(sh.hist, kBins, static_cast<uint32_t>(a.k), &sh.scan, tid);
   const uint32_t d0 = sh.scan.digit;
   const uint32_t n_above = sh.scan.above;  // keys in bins above d0: all selected
   int32_t* cand_g = a.cand + row * a.N_cap;  // candidates past the leader's capacity
-  SweepCtx x;
-  x.sh = &sh;
-  x.out = out;
-  x.cand_g = cand_g;
-  x.r_up = mapa_shared(smem_u32(&sh.n_up), 0);
-  x.r_cand = mapa_shared(smem_u32(&sh.n_cand), 0);
-  x.r_ckey = mapa_shared(smem_u32(ckey), 0);
-  x.r_cidx = mapa_shared(smem_u32(cidx), 0);
-  x.r_hist2 = mapa_shared(smem_u32(sh.hist2), 0);
-  x.k = a.k;
-  x.N_cap = a.N_cap;
-  // Sweep the slice: an entry at or above the threshold bin goes to
-  // sweep_take; the rest (all but a few per thousand) cost a compare.
-  for (int c = 0; c * kSliceChunk < n_st; ++c) {
-    if (!folded) {
-      // (waited for in the histogram pass)
-    } else {
-      chunk_wait(c);
-    }
-    const int e1 = min(n_st, (c + 1) * kSliceChunk);
-    const float4* s4 = reinterpret_cast<const float4*>(sslice);
-    for (int q = (c * kSliceChunk >> 2) + tid; 4 * q < e1; q += kClusterThreads) {
-      const float4 v = s4[q];
-      const uint32_t k0 = order_key(v.x), k1 = order_key(v.y);
-      const uint32_t k2 = order_key(v.z), k3 = order_key(v.w);
-      if (max(max(k0, k1), max(k2, k3)) >> 21 >= d0) {
+  const uint32_t r_up = mapa_shared(smem_u32(&sh.n_up), 0);
+  const uint32_t r_cand = mapa_shared(smem_u32(&sh.n_cand), 0);
+  const uint32_t r_ckey = mapa_shared(smem_u32(ckey), 0);
+  const uint32_t r_cidx = mapa_shared(smem_u32(cidx), 0);
+  const uint32_t r_hist2 = mapa_shared(smem_u32(sh.hist2), 0);
+  // Sweep the slice twice, each thread over the same entries: count the
+  // entries above the threshold bin (selected) and in it (candidates), scan
+  // the counts over the block and reserve the CTA's ranges in the row's
+  // lists at the leader, then write each entry to its place.  No atomics on
+  // a shared counter, and the common entry costs a compare.
+  // The smallest score of bin d0, as a float (order_key is monotone): a
+  // score x is at or above the bin iff !(x < T), one float compare instead
+  // of a key (integer operations run at half the float rate).  NaN scores
+  // fail every compare and take the exact key test, as do all scores when
+  // the bin holds infinities or NaN keys (d0 outside [4, 2044]).
+  float T = -INFINITY;
+  if (d0 >= 4 && d0 <= 2044) {
+    const uint32_t kl = d0 << 21;
+    T = __uint_as_float((kl & 0x80000000u) ? (kl & 0x7fffffffu) : ~kl);
+  }
+  const float4* s4 = reinterpret_cast<const float4*>(sslice);
+  auto visit = [&](auto&& fn) {
+    for (int c = 0; c * kSliceChunk < n_st; ++c) {
+      const int e1 = min(n_st, (c + 1) * kSliceChunk);
+      for (int q = (c * kSliceChunk >> 2) + tid; 4 * q < e1; q += kClusterThreads) {
+        const float4 v = s4[q];
+        if (v.x < T && v.y < T && v.z < T && v.w < T) continue;
+        const uint32_t k0 = order_key(v.x), k1 = order_key(v.y);
+        const uint32_t k2 = order_key(v.z), k3 = order_key(v.w);
         const int64_t e = lo + 4 * q;
-        // (entries past the visible count are not swept)
-        if ((k0 >> 21) >= d0 && 4 * q < e1) sweep_take(x, e, k0, d0);
-        if ((k1 >> 21) >= d0 && 4 * q + 1 < e1) sweep_take(x, e + 1, k1, d0);
-        if ((k2 >> 21) >= d0 && 4 * q + 2 < e1) sweep_take(x, e + 2, k2, d0);
-        if ((k3 >> 21) >= d0 && 4 * q + 3 < e1) sweep_take(x, e + 3, k3, d0);
+        // (entries past the visible count are not visited)
+        if (4 * q < e1) fn(e, k0);
+        if (4 * q + 1 < e1) fn(e + 1, k1);
+        if (4 * q + 2 < e1) fn(e + 2, k2);
+        if (4 * q + 3 < e1) fn(e + 3, k3);
       }
     }
+    for (int64_t e = lo + n_st + tid; e < hi; e += kClusterThreads) fn(e, order_key(__ldcg(src + e)));
+  };
+  if (folded)
+    for (int c = 0; c * kSliceChunk < n_st; ++c) chunk_wait(c);
+  uint32_t cu = 0, cc = 0;
+  visit([&](int64_t, uint32_t key) {
+    cu += (key >> 21) > d0;
+    cc += (key >> 21) == d0;
+  });
+  uint32_t ou, oc, tu, tc;
+  block_exclusive_scan2(cu, cc, &ou, &oc, &tu, &tc, sh.wtot, tid, kClusterThreads);
+  if (tid == 0) {
+    sh.base_up = tu ? static_cast<int>(atom_add_cluster(r_up, tu)) : 0;
+    sh.base_cand = tc ? static_cast<int>(atom_add_cluster(r_cand, tc)) : 0;
   }
-  for (int64_t e = lo + n_st + tid; e < hi; e += kClusterThreads) {
-    const uint32_t key = order_key(__ldcg(src + e));
-    if ((key >> 21) >= d0) sweep_take(x, e, key, d0);
-  }
+  __syncthreads();
+  uint32_t pu = static_cast<uint32_t>(sh.base_up) + ou;
+  uint32_t pc = static_cast<uint32_t>(sh.base_cand) + oc;
+  visit([&](int64_t e, uint32_t key) {
+    const uint32_t d = key >> 21;
+    if (d > d0) {
+      if (pu < static_cast<uint32_t>(a.k)) out[pu] = static_cast<int32_t>(e);
+      ++pu;
+    } else if (d == d0) {
+      if (pc < static_cast<uint32_t>(kCandCap)) {
+        st_cluster_u32(r_ckey + 4u * pc, key);
+        st_cluster_u32(r_cidx + 4u * pc, static_cast<uint32_t>(e));
+      } else if (static_cast<int64_t>(pc) - kCandCap < a.N_cap) {
+        cand_g[pc - kCandCap] = static_cast<int32_t>(e);
+      }
+      ++pc;
+      atomicAdd(&sh.lhist2[(key >> 10) & 2047u], 1u);
+    }
+  });
   // the staged chunks past the visible entries were never waited for
   for (int c = 0; c * kSliceChunk < staged; ++c)
     if (c * kSliceChunk >= n_st) chunk_wait(c);
   __syncthreads();
-  // one reservation per list in the row's lists, then the copies
-  const int nu = min(sh.l_up, kUpCap), nc = min(sh.l_cand, kLocalCand);
-  if (tid == 0) {
-    sh.base_up = nu ? static_cast<int>(atom_add_cluster(x.r_up, static_cast<uint32_t>(nu))) : 0;
-    sh.base_cand = nc ? static_cast<int>(atom_add_cluster(x.r_cand, static_cast<uint32_t>(nc))) : 0;
-  }
-  __syncthreads();
-  for (int i = tid; i < nu; i += kClusterThreads)
-    if (sh.base_up + i < a.k) out[sh.base_up + i] = sh.up[i];
-  for (int i = tid; i < nc; i += kClusterThreads) {
-    const uint32_t q = static_cast<uint32_t>(sh.base_cand + i);
-    if (q < static_cast<uint32_t>(kCandCap)) {
-      st_cluster_u32(x.r_ckey + 4u * q, sh.lkey[i]);
-      st_cluster_u32(x.r_cidx + 4u * q, static_cast<uint32_t>(sh.lidx[i]));
-    } else if (static_cast<int64_t>(q) - kCandCap < a.N_cap) {
-      cand_g[q - kCandCap] = sh.lidx[i];
-    }
-  }
   for (int i = tid; i < kBins; i += kClusterThreads)
-    if (sh.lhist2[i]) red_add_cluster(x.r_hist2 + 4u * i, sh.lhist2[i]);
+    if (sh.lhist2[i]) red_add_cluster(r_hist2 + 4u * i, sh.lhist2[i]);
   // (C) the row's candidates are with the leader (and in the overflow
   // list); the other CTAs are done and their shared memory is not read
   cluster_arrive();
@@ -707,7 +768,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const 
   // is a few entries for spread-out scores; one warp ranks up to 32 of them
   // (key descending, then entry index ascending), else the general ranking
   // runs.
-  find_digit_desc(sh.hist2, kBins, need, &sh.scan, tid, kClusterThreads);
+  find_digit_desc_warp(sh.hist2, kBins, need, &sh.scan, tid);
   const uint32_t p1 = (d0 << 11) | sh.scan.digit;
   const uint32_t above1 = sh.scan.above;
   const uint32_t need1 = need - above1;  // >= 1
@@ -724,7 +785,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const 
     const int g = warp_append(&sh.n_gt, gt);
     if (gt && g < static_cast<int>(above1)) rest[g] = idx_of(c);
     const int b = warp_append(&sh.n_bin, in);
-    if (in && b < kLocalCand) sh.lidx[b] = c;
+    if (in && b < kBinCap) sh.binlist[b] = c;
   }
   __syncthreads();
   const int nb = sh.n_bin;
@@ -735,8 +796,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1) topk_cluster_kernel(const 
       uint32_t key = 0u;
       int32_t j = INT32_MAX;
       if (lane < nb) {
-        key = key_of(sh.lidx[lane]);
-        j = idx_of(sh.lidx[lane]);
+        key = key_of(sh.binlist[lane]);
+        j = idx_of(sh.binlist[lane]);
       }
       for (int kk = 2; kk <= 32; kk <<= 1) {
         for (int jj = kk >> 1; jj > 0; jj >>= 1) {

@@ -108,15 +108,15 @@ def _meta_layer(name):
 
 def test_launch_counts_match_the_recorded_launch_lists():
     """The kernels one decode step launches, as the bench counts them for
-    gpu_launches, equal the ncu launch lists of the same steps (88 launches
-    over 11 steps in profiles/launches_hybrid_decode_1m.md and
+    gpu_launches, equal the ncu launch lists of the same steps (80 launches
+    over 10 steps in profiles/launches_hybrid_decode_1m.md and
     profiles/launches_hybrid_decode_1m_mtp2.md): two compressions, window
     keys, query prep, the indexer, the top-k kernel (a cluster of CTAs per
     row of 262,144 scores), the fused attention and the merge."""
     for name, T in (("hybrid_decode_1m", 1), ("hybrid_decode_1m_mtp2", 2)):
         wl, layer = _meta_layer(name)
         n = layer.launches_per_step(T, wl.L - 1, side_stream=True)
-        assert n == 88 // 11 == 8, (name, n)
+        assert n == 80 // 10 == 8, (name, n)
         assert len(layer.event_names(T)) == 7  # one span covers both compressions
     # a step whose token completes no entry skips both compressions
     wl, layer = _meta_layer("hybrid_decode_1m")

@@ -556,6 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->q_full), 0, abort, a.status,
                                              kWaitLimitNs, 29));
+      // on an abort the query copies issued above land before the CTA exits
+      if (!ok && lane == 0)
+        mbar_wait(smem_u32(&sm->q_full), 0, nullptr, nullptr, 10000000ull, 42);
       // the query rows of other queries (or past the tensor) in the box are
       // zeroed, so they contribute nothing to S
       if (ok && nrows < 128) {

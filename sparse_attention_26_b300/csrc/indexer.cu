@@ -289,7 +289,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (++st == a.stages) { st = 0; ph ^= 1u; }
       }
       if (*abort) {
-        // let the copies already issued land before the CTA exits
+        // let the copies already issued land before the CTA exits: the last
+        // query block (its predecessor's phase completed before it was
+        // issued: the issuers had released it), then the key stages
+        if (qloads > 0)
+          mbar_wait(smem_u32(&sm->qfull), (qloads - 1) & 1, nullptr, nullptr, 10000000ull, 13);
         const int64_t first = it > a.stages ? it - a.stages : 0;
         for (int64_t x = first; x < it; ++x)
           mbar_wait(smem_u32(&sm->full[x % a.stages]), (x / a.stages) & 1, nullptr, nullptr,

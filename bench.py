@@ -219,12 +219,18 @@ def kernel_roofline(wl, keys, per_kernel, hbm, src):
                 "note": "at the ridge: both the HBM and the tensor fraction are given"}
     # a prefill pass lasts milliseconds, not seconds: the burst peak applies
     tf, tf_src = measured_bf16_burst()
+    # the fused attention covers every attention branch in one launch
+    fl = dict(fl)
+    if "attn_fused" in per_kernel:
+        fl["attn_fused"] = sum(v for n, v in fl.items() if n in ("sparse", "hca", "swa"))
     calls = {n: per_kernel[n] for n in fl if n in per_kernel}
     name = max(calls, key=calls.get)
     ms = calls[name]
     achieved = fl[name] / (ms / 1e3) / 1e12
     kern = {"indexer": "indexer_score_kernel", "sparse": "attn_kernel<kSparse>",
-            "hca": "attn_kernel<kHca>", "swa": "attn_kernel<kSwa>"}[name]
+            "hca": "attn_kernel<kHca>", "swa": "attn_kernel<kSwa>",
+            "attn_fused": "attn_kernel<kFused> (or the branch kind of a single key set; the "
+                          "layer output written in the kernel)"}[name]
     return {"bound": "tensor", "kernel": kern, "achieved": achieved, "peak": tf,
             "unit": "TFLOP/s", "frac": achieved / tf, "traffic": None,
             "peak_source": tf_src,

@@ -440,6 +440,32 @@ HATTN_API int hattn_hybrid_attn(const void* q, const float* gamma_q, int q_prepp
                                 float rope_base, float eps, float scale, int segments, int n_sms,
                                 void* o, float* lse, void* workspace, size_t ws_bytes,
                                 int flags, hattn_stream_t stream);
+/* hattn_hybrid_attn straight to the layer output: the sink merge and the
+ * inverse RoPE ([AT] "Spec sheet / Core block": attention sinks, inverse RoPE
+ * on the outputs) applied to the call's single softmax,
+ *   Z = sum_j e^(l_j) + e^(sink[h]),  y = sum_j e^(l_j) v_j / Z,
+ *   out = y with its last r dims rotated back by the query position,
+ *   lse_out = log Z,
+ * which equals hattn_hybrid_attn's partials merged by hattn_lse_merge_splits
+ * when the call covers every key set of the layer.  When each query's keys
+ * take one split (prefill: many row blocks) the attention kernel writes out
+ * and lse_out itself, with no partials; otherwise it leaves partials in the
+ * workspace and a merge kernel follows (launched as its dependent).
+ *   sink [H] fp32 or NULL; out [B][T][H][D] bf16; lse_out [B][T][H] fp32 or
+ *   NULL.  The other arguments, the limits and flags are hattn_hybrid_attn's;
+ *   workspace: hattn_hybrid_attn_out_workspace_bytes() bytes (0 when the
+ *   queries come prepared and the keys take one split). */
+HATTN_API int hattn_hybrid_attn_out(const void* q, const float* gamma_q, int q_prepped,
+                                    const void* kv_c, const int32_t* idx, int64_t N_c, int k,
+                                    const void* kv_h, int64_t N_h, int m, const void* kv_w,
+                                    int W, const int32_t* pos, int B, int T, int H, int D, int r,
+                                    float rope_base, float eps, float scale, int segments,
+                                    int n_sms, const float* sink, void* out, float* lse_out,
+                                    void* workspace, size_t ws_bytes, int flags,
+                                    hattn_stream_t stream);
+HATTN_API size_t hattn_hybrid_attn_out_workspace_bytes(int B, int T, int H, int D, int k,
+                                                       int64_t N_h, int W, int segments,
+                                                       int n_sms, int q_prepped);
 HATTN_API size_t hattn_hybrid_attn_workspace_bytes(int B, int T, int H, int D, int k,
                                                    int64_t N_h, int W, int segments, int n_sms,
                                                    int q_prepped, int partials);

@@ -251,6 +251,18 @@ int query_prep_impl(const void* q, const float* gamma_q, const int32_t* pos, int
 }
 
 // The fused call's second and third key sources.
+// The layer output of a fused call: the sink merge and the inverse RoPE
+// applied to its single softmax (hattn_hybrid_attn_out).
+struct FinalOut {
+  void* out;          // [B][T][H][D] bf16
+  float* lse_out;     // [B][T][H] or null
+  const float* sink;  // [H] or null
+};
+
+int merge_impl(const void* const* o_list, const float* const* lse_list, const int* nsplit, int nb,
+               const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
+               float rope_base, void* out, float* lse_out, hattn_stream_t stream, int flags);
+
 struct FusedSources {
   const void* kv_h;   // [B][N_h][D] HCA entries
   int64_t N_h;
@@ -276,14 +288,21 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
                 const float* gamma_kv, const int32_t* idx, const int32_t* pos, int B, int T, int H,
                 int D, int64_t N_rows, int k, int m, int W, int r, float rope_base, float eps,
                 float scale, void* o, float* lse, void* workspace, size_t ws_bytes,
-                hattn_stream_t stream, const FusedSources* fs = nullptr, int flags = 0) {
+                hattn_stream_t stream, const FusedSources* fs = nullptr, int flags = 0,
+                const FinalOut* fo = nullptr) {
   if (int rcf = check_flags(flags)) return rcf;
   const bool dependent = (flags & HATTN_LAUNCH_DEPENDENT) != 0;
   REQUIRE_PTR(q);
   if (kind != kFused || (fs && (fs->segments & 1))) REQUIRE_PTR(kv);
   REQUIRE_PTR(pos);
+  if (fo) {
+    REQUIRE_PTR(fo->out);
+    REQUIRE_F32(fo->lse_out);
+    REQUIRE_F32(fo->sink);
+  }
   // o == lse == NULL: leave the split partials in the workspace for
-  // hattn_lse_merge_splits instead of combining them
+  // hattn_lse_merge_splits instead of combining them (or, with a final
+  // output, for this call's own merge when the keys take several splits)
   const bool partials = o == nullptr && lse == nullptr;
   if (!partials) {
     REQUIRE_PTR(o);
@@ -328,7 +347,10 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
                       kind == kFused ? fused_sms(fs->n_sms) : num_sms_or_default(), &p))
     return fail(HATTN_ERR_UNSUPPORTED, "no attention kernel for H=%d D=%d", H, D);
   const size_t qbytes = qprep_bytes(B, T, H, D, q_prepped);
-  const size_t pbytes = partials ? partial_bytes(B, T, H, D, p.nsplit) : p.ws_bytes;
+  // a final output in one split needs no partials
+  const bool final_direct = fo && p.nsplit == 1;
+  const size_t pbytes = final_direct ? 0
+                        : (partials ? partial_bytes(B, T, H, D, p.nsplit) : p.ws_bytes);
   const size_t need = qbytes + pbytes;
   if (need > 0) {
     REQUIRE_PTR(workspace);
@@ -388,10 +410,13 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.lse = lse;
   float* ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + qbytes);
   const int64_t rows = (int64_t)B * T * H;
-  const bool split_out = partials || p.nsplit > 1;
+  const bool split_out = !final_direct && (partials || p.nsplit > 1);
   a.part_o = split_out ? ws : nullptr;
   a.part_lse = split_out ? ws + rows * p.nsplit * D : nullptr;
-  a.partials = partials ? 1 : 0;
+  a.partials = partials && !final_direct ? 1 : 0;
+  a.out = final_direct ? static_cast<__nv_bfloat16*>(fo->out) : nullptr;
+  a.lse_out = final_direct ? fo->lse_out : nullptr;
+  a.sink = final_direct ? fo->sink : nullptr;
   a.status = status;
   a.kind = kind;
   a.B = B;
@@ -418,6 +443,14 @@ int attn_common(int kind, const void* q, const float* gamma_q, int q_prepped, co
   a.dependent = (dependent || !q_prepped) ? 1 : 0;
   cudaError_t e = launch_attention(tm, tm2, tm_q, a, p, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (fo && !final_direct) {
+    // several key splits: the merge of this call's partials with the sink
+    const void* ol[1] = {a.part_o};
+    const float* ll[1] = {a.part_lse};
+    const int ns[1] = {p.nsplit};
+    return merge_impl(ol, ll, ns, 1, fo->sink, pos, B, T, H, D, r, rope_base, fo->out,
+                      fo->lse_out, stream, HATTN_LAUNCH_DEPENDENT);
+  }
   if (p.nsplit > 1 && !partials) {
     CombineArgs c;
     c.part_o = a.part_o;
@@ -1040,6 +1073,45 @@ int hattn_hybrid_attn(const void* q, const float* gamma_q, int q_prepped, const 
                      flags);
 }
 
+int hattn_hybrid_attn_out(const void* q, const float* gamma_q, int q_prepped, const void* kv_c,
+                          const int32_t* idx, int64_t N_c, int k, const void* kv_h, int64_t N_h,
+                          int m, const void* kv_w, int W, const int32_t* pos, int B, int T, int H,
+                          int D, int r, float rope_base, float eps, float scale, int segments,
+                          int n_sms, const float* sink, void* out, float* lse_out,
+                          void* workspace, size_t ws_bytes, int flags, hattn_stream_t stream) {
+  const FusedSources fs{kv_h, N_h, kv_w, segments, n_sms};
+  const FinalOut fo{out, lse_out, sink};
+  // one key set alone runs its own branch kernel (the same keys, without
+  // the fused call's segment bookkeeping; the HCA kind also stacks several
+  // queries' heads when H < 128)
+  if (segments == 2 && n_sms == 0)
+    return attn_common(kHca, q, gamma_q, q_prepped, kv_h, nullptr, nullptr, pos, B, T, H, D, N_h,
+                       1, m, 1, r, rope_base, eps, scale, nullptr, nullptr, workspace, ws_bytes,
+                       stream, nullptr, flags, &fo);
+  if (segments == 1 && n_sms == 0)
+    return attn_common(kSparse, q, gamma_q, q_prepped, kv_c, nullptr, idx, pos, B, T, H, D, N_c,
+                       k, 1, 1, r, rope_base, eps, scale, nullptr, nullptr, workspace, ws_bytes,
+                       stream, nullptr, flags, &fo);
+  return attn_common(kFused, q, gamma_q, q_prepped, kv_c, nullptr, idx, pos, B, T, H, D, N_c, k,
+                     m, W, r, rope_base, eps, scale, nullptr, nullptr, workspace, ws_bytes,
+                     stream, &fs, flags, &fo);
+}
+
+size_t hattn_hybrid_attn_out_workspace_bytes(int B, int T, int H, int D, int k, int64_t N_h,
+                                             int W, int segments, int n_sms, int q_prepped) {
+  AttnPlan p;
+  if (segments < 1 || segments > 7 || n_sms < 0) return 0;
+  // (the kind hattn_hybrid_attn_out runs for this segment set)
+  const bool hca = segments == 2 && n_sms == 0, csa = segments == 1 && n_sms == 0;
+  const int kind = hca ? kHca : (csa ? kSparse : kFused);
+  const int64_t nk = hca ? N_h : (csa ? k : fused_keys(k, N_h, W, segments));
+  if (!plan_attention(kind, B, T, H, D, nk, kind == kFused ? fused_sms(n_sms) : num_sms_or_default(),
+                      &p))
+    return 0;
+  return qprep_bytes(B, T, H, D, q_prepped) +
+         (p.nsplit > 1 ? partial_bytes(B, T, H, D, p.nsplit) : 0);
+}
+
 size_t hattn_hybrid_attn_workspace_bytes(int B, int T, int H, int D, int k, int64_t N_h, int W,
                                          int segments, int n_sms, int q_prepped,
                                          int partials) {
@@ -1125,8 +1197,7 @@ namespace {
 
 int merge_impl(const void* const* o_list, const float* const* lse_list, const int* nsplit, int nb,
                const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
-               float rope_base, void* out, float* lse_out, hattn_stream_t stream,
-               int flags = 0) {
+               float rope_base, void* out, float* lse_out, hattn_stream_t stream, int flags) {
   if (int rcf = check_flags(flags)) return rcf;
   REQUIRE(o_list && lse_list, "o_list and lse_list must not be NULL");
   REQUIRE(nb >= 1 && nb <= 4, "nb=%d must be in [1, 4]", nb);
@@ -1180,7 +1251,7 @@ int hattn_lse_merge(const void* const* o_list, const float* const* lse_list, int
                     const float* sink, const int32_t* pos, int B, int T, int H, int D, int r,
                     float rope_base, void* out, float* lse_out, hattn_stream_t stream) {
   return merge_impl(o_list, lse_list, nullptr, nb, sink, pos, B, T, H, D, r, rope_base, out,
-                    lse_out, stream);
+                    lse_out, stream, 0);
 }
 
 int hattn_lse_merge_splits(const void* const* part_o_list, const float* const* part_lse_list,

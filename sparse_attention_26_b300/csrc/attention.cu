@@ -271,11 +271,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (nt == 0) {
     pdl_wait();
-    // empty split: o = 0, lse = -inf
+    // empty split: o = 0, lse = -inf (a finalised output: 0, and the
+    // sink alone in lse_out)
     for (int rI = threadIdx.x; rI < nrows; rI += kThreads) {
       const int g = rI / a.H, h = rI % a.H;
       const int64_t row = ((int64_t)b * a.T + t0 + g) * a.H + h;
-      if (a.nsplit == 1 && !a.partials) {
+      if (a.out) {
+        for (int c = 0; c < ocols; ++c) a.out[row * a.D + dh * ocols + c] = __float2bfloat16(0.f);
+        if (dh == 0 && a.lse_out) a.lse_out[row] = a.sink ? a.sink[h] : -INFINITY;
+      } else if (a.nsplit == 1 && !a.partials) {
         for (int c = 0; c < ocols; ++c) a.o[row * a.D + dh * ocols + c] = 0.f;
         if (dh == 0) a.lse[row] = -INFINITY;
       } else {
@@ -879,8 +883,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     done = __all_sync(0xffffffffu, done);
     if (done) {
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const float lse = l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      // Finalised output (a.out): the sink-augmented merge of this single
+      // split, Z = sum_j e^l_j + e^sink, y = sum_j e^l_j v_j / Z, taken in
+      // base 2 around the larger of the two terms; else the split's own
+      // normalisation and log-sum-exp.
+      const bool fin = a.out != nullptr;
+      float inv_l, lse;
+      if (fin) {
+        const float s2 = a.sink ? __ldg(a.sink + h) * 1.4426950408889634f : -INFINITY;
+        const float lb = l > 0.f ? m_used + log2f(l) : -INFINITY;  // log2 sum_j 2^(l_j log2 e)
+        const float mx = fmaxf(lb, s2);
+        if (mx == -INFINITY) {
+          inv_l = 0.f;
+          lse = -INFINITY;
+        } else {
+          const float lz = mx + log2f(exp2f(lb - mx) + exp2f(s2 - mx));
+          inv_l = l > 0.f ? exp2f(m_used - lz) : 0.f;  // 2^m / Z: o is the unnormalised sum
+          lse = lz * 0.6931471805599453f;
+        }
+      } else {
+        inv_l = l > 0.f ? 1.f / l : 0.f;
+        lse = l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      }
       // this warp's 32 rows, fp32, row stride ocols + 4 floats (bank spread)
       float* stage = reinterpret_cast<float*>(sQ) + quad * 32 * (ocols + 4);
       for (int cc = 0; cc < ocols; cc += 32) {
@@ -893,11 +917,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(dstrow + e) =
               make_float4(o[e] * inv_l, o[e + 1] * inv_l, o[e + 2] * inv_l, o[e + 3] * inv_l);
       }
+      if (fin && row_valid) {
+        // the last r dims rotated back by the query position, then the row
+        // as bf16 over the start of its own staging row (each 4-byte pair
+        // is read before the 2 bytes written at or below it)
+        float* srow = stage + lane * (ocols + 4);
+        const int d0 = a.D - a.r;
+        for (int c = 0; c < ocols; c += 2) {
+          const int d = dh * ocols + c;
+          float x0 = srow[c], x1 = srow[c + 1];
+          if (d >= d0) {
+            float sn, cs;
+            rope_cs(a.rope.c, (d - d0) >> 1, -static_cast<int64_t>(tq), &sn, &cs);
+            const float y0 = x0 * cs - x1 * sn;
+            x1 = x0 * sn + x1 * cs;
+            x0 = y0;
+          }
+          reinterpret_cast<uint32_t*>(srow)[c >> 1] = pack_bf16x2(x0, x1);
+        }
+      }
       // the staged row of this thread goes out as one bulk copy by the copy
       // engine (all 128 rows stream in parallel)
       const bool direct = a.nsplit == 1 && !a.partials;
       fence_proxy_async_smem();
-      if (row_valid) {
+      if (fin && row_valid) {
+        const int64_t row = ((int64_t)b * a.T + t0 + g) * a.H + h;
+        bulk_copy_s2g(a.out + row * a.D + dh * ocols, smem_u32(stage + lane * (ocols + 4)),
+                      static_cast<uint32_t>(ocols) * 2u);
+        bulk_commit();
+        if (dh == 0 && a.lse_out) a.lse_out[row] = lse;
+        bulk_wait_read();
+      } else if (row_valid) {
         const int64_t row = ((int64_t)b * a.T + t0 + g) * a.H + h;
         float* dst = direct ? a.o + row * a.D + dh * ocols
                             : a.part_o + (row * a.nsplit + split) * a.D + dh * ocols;

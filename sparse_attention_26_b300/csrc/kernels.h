@@ -170,6 +170,13 @@ struct AttnArgs {
   float* part_o;                // [B*T*H][nsplit][D] partials (nsplit > 1 or partials)
   float* part_lse;              // [B*T*H][nsplit]
   int partials;                 // 1: always write partials, even for one split
+  // Finalised output (one split, no partials): the sink-augmented merge and
+  // the inverse RoPE of this call's single softmax, out [B][T][H][D] bf16
+  // and lse_out [B][T][H] (or null); sink [H] or null.  out == null: o/lse
+  // or partials as above.
+  __nv_bfloat16* out;
+  float* lse_out;
+  const float* sink;
   int* status;
   int kind, B, T, H, D, r;
   int64_t N_rows;               // rows per sequence of kv (N_cap or L_cap)

@@ -77,6 +77,11 @@ _SIGS = {
                                  _vp, _vp, _vp, _sz, _i32, _vp]),
     "hattn_hybrid_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                                 _i32, _i32, _i32]),
+    "hattn_hybrid_attn_out": (_i32, [_vp, _vp, _i32, _vp, _vp, _i64, _i32, _vp, _i64, _i32, _vp,
+                                     _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32,
+                                     _i32, _i32, _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
+    "hattn_hybrid_attn_out_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32,
+                                                    _i32, _i32, _i32]),
     "hattn_hybrid_attn_splits": (_i32, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32, _i32]),
     "hattn_indexer_scores_ex": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32,
                                        _i32, _i64, _vp, _i32, _vp]),
@@ -721,6 +726,59 @@ def hybrid_attn(q, kv_c, idx, kv_h, kv_w, pos, *, r, m=128, k=None, W=None, gamm
         return o, lse
     return Partials(workspace, q_prepped, B, T, H, D,
                     hybrid_attn_splits(B, T, H, D, k, N_h, W, segments, n_sms))
+
+
+def hybrid_attn_out_workspace_bytes(B, T, H, D, k, N_h, W, q_prepped=False, segments=SEG_ALL,
+                                    n_sms=0):
+    return lib().hattn_hybrid_attn_out_workspace_bytes(B, T, H, D, k, N_h, W, segments, n_sms,
+                                                       int(bool(q_prepped)))
+
+
+def hybrid_attn_out(q, kv_c, idx, kv_h, kv_w, pos, *, r, m=128, k=None, W=None, gamma_q=None,
+                    rope_base=10000.0, eps=1e-6, scale=None, sink=None, out=None, lse_out=None,
+                    workspace=None, q_prepped=False, segments=SEG_ALL, n_sms=0,
+                    dependent=False, stream=None):
+    """hybrid_attn straight to the layer output: the sink merge and the
+    inverse RoPE of the call's one softmax (in the attention kernel when
+    every query's keys take one split, else by a merge that follows).
+    Returns (out bf16 [B, T, H, D], lse fp32 [B, T, H])."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(pos, "pos", torch.int32, 2)
+    _opt(gamma_q, "gamma_q", torch.float32)
+    B, T, H, D = q.shape
+    if segments & SEG_CSA:
+        _need(kv_c, "kv_c", torch.bfloat16, 3)
+        _need(idx, "idx", torch.int32, 3)
+    if segments & SEG_HCA:
+        _need(kv_h, "kv_h", torch.bfloat16, 3)
+    if segments & SEG_SWA:
+        _need(kv_w, "kv_w", torch.bfloat16, 4)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, 1)
+        _shape(sink, "sink", (H,))
+    k = idx.shape[2] if idx is not None else (k or 1)
+    N_h = kv_h.shape[1] if kv_h is not None else 1
+    N_c = kv_c.shape[1] if kv_c is not None else 1
+    W = kv_w.shape[2] if kv_w is not None else (W or 1)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if out is None:
+        out = torch.empty((B, T, H, D), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, 4)
+    _shape(out, "out", (B, T, H, D))
+    if lse_out is None:
+        lse_out = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+    _need(lse_out, "lse_out", torch.float32, 3)
+    _shape(lse_out, "lse_out", (B, T, H))
+    need = hybrid_attn_out_workspace_bytes(B, T, H, D, k, N_h, W, q_prepped, segments, n_sms)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().hattn_hybrid_attn_out(_ptr(q), _ptr(gamma_q), int(bool(q_prepped)), _ptr(kv_c),
+                                       _ptr(idx), N_c, k, _ptr(kv_h), N_h, m, _ptr(kv_w), W,
+                                       _ptr(pos), B, T, H, D, r, rope_base, eps, scale, segments,
+                                       n_sms, _ptr(sink), _ptr(out), _ptr(lse_out),
+                                       _ptr(workspace), wsb, _flags(dependent), _stream(stream)))
+    return out, lse_out
 
 
 # ------------------------------------------------------------------ merge

@@ -57,6 +57,7 @@ class HybridLayer:
         # merge start as dependent launches of their predecessors
         self.dependent_launch = True
         self._split_event = None  # marks the end of the score kernel in each step
+        self._final = {}  # T -> the fused call writes the layer output itself
         if build_caches:
             self.build_caches()
         self._bufs = {}
@@ -157,13 +158,24 @@ class HybridLayer:
         return seg
 
     def can_fuse(self, T):
-        """The fused attention serves one query per row block (H = 128, or
-        single-token decode) with a window buffer of at most 256 MB: decode
-        steps of any branch subset, and all three branches at any T."""
+        """The fused attention serves one query per row block: it takes every
+        step where that costs no MMA rows over the branch calls (H = 128,
+        single-token decode, or a CSA layer, whose sparse branch runs one
+        query per row block anyway), with a window buffer of at most 2 GB.
+        In prefill that also removes the merge: one split per query, so the
+        attention writes the layer output itself."""
         wl = self.wl
-        fits = "swa" not in wl.branches or self.B * T * wl.W * self.D * 2 <= (256 << 20)
-        all_three = set(wl.branches) == {"csa", "hca", "swa"}
-        return (wl.H == 128 or T == 1) and fits and (all_three or T <= 2)
+        fits = "swa" not in wl.branches or self.B * T * wl.W * self.D * 2 <= (2 << 30)
+        return (wl.H == 128 or T == 1 or "csa" in wl.branches) and fits
+
+    def fused_final(self, T):
+        """Whether the fused call finalises the output itself (each query's
+        keys in one split, so no merge follows)."""
+        if T not in self._final:
+            wl = self.wl
+            self._final[T] = hattn.hybrid_attn_splits(self.B, T, wl.H, self.D, wl.k, self.N_hca,
+                                                      wl.W, segments=self.segments()) == 1
+        return self._final[T]
 
     def _branch_kinds(self):
         wl = self.wl
@@ -430,6 +442,18 @@ class HybridLayer:
         else:
             if side_stream is not None:
                 main.wait_stream(side_stream)
+            if self.fused_final(T):
+                # one split per query: the attention applies the sink merge
+                # and the inverse RoPE itself
+                ev("attn_fused", 0)
+                hattn.hybrid_attn_out(b["qt"], self.kv_c if "csa" in has else None,
+                                      b["idx"] if "csa" in has else None,
+                                      self.kv_h if "hca" in has else None, b.get("kv_w"), pos,
+                                      r=wl.r, m=wl.m_hca, k=wl.k, W=wl.W, sink=sink,
+                                      out=b["out"], lse_out=b["lse"], workspace=b["ws_fused"],
+                                      q_prepped=True, segments=self.segments(), dependent=pdl)
+                ev("attn_fused", 1)
+                return b["out"], b["lse"]
             parts = [attn("fused", self.segments(), 0, dependent=pdl)]
         ev("merge", 0)
         hattn.lse_merge_splits(parts, pos, r=wl.r, H=wl.H, sink=sink, out=b["out"],
@@ -447,7 +471,8 @@ class HybridLayer:
             attn = ["attn_dense", "attn_sparse"] if split else ["attn_fused"]
             names = ["compress"] + (["swa_keys"] if "swa" in has else []) + ["qprep"]
             names += ["indexer", "topk"] if "csa" in has else []
-            return names + attn + ["merge"]
+            merge = [] if (not split and self.fused_final(T)) else ["merge"]
+            return names + attn + merge
         names = ["compress", "qprep"]
         if "csa" in self.wl.branches:
             names += ["indexer", "topk", "sparse"]
@@ -473,7 +498,9 @@ class HybridLayer:
             has = set(wl.branches)
             split = side_stream and self.override_dense_sms > 0 and has == {"csa", "hca", "swa"}
             topk = hattn.topk_launches(B, T, self.N_csa, wl.k) if "csa" in has else 0
-            return n + int("swa" in has) + int("csa" in has) + topk + 1 + int(split)
+            # (no merge when the attention writes the layer output itself)
+            final = not split and self.fused_final(T)
+            return n - int(final) + int("swa" in has) + int("csa" in has) + topk + 1 + int(split)
         for name, kind, nk in self._branch_kinds():
             n += 1 + int(branch_outputs and hattn.attn_splits(kind, B, T, H, D, nk) > 1)
             if name == "csa":

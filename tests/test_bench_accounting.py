@@ -133,6 +133,12 @@ def test_roofline_prefill_takes_the_slowest_call():
     assert set(rf["by_call"]) == {"indexer", "sparse", "swa"}
     rh = bench.kernel_roofline(W["hca_prefill"], "bf16", {"hca": 14.7}, 6482.7, "measured")
     assert rh["kernel"] == "attn_kernel<kHca>"
+    # the fused call: one launch carries the flops of every attention branch
+    rf = bench.kernel_roofline(wl, "bf16", {"indexer": 0.4, "attn_fused": 4.0}, 6482.7,
+                               "measured")
+    assert rf["kernel"].startswith("attn_kernel<kFused>")
+    assert rf["flops_per_launch"] == pytest.approx(fl["sparse"] + fl["swa"])
+    assert rf["achieved"] == pytest.approx((fl["sparse"] + fl["swa"]) / 4.0e-3 / 1e12)
 
 
 def test_l2_note_is_true_per_workload():

@@ -632,11 +632,17 @@ def test_swa_keys(B, T, H, D, r, L, W):
     (2, 2, 128, 512, 64, 40, 64, 100, 400, [100, 127, 130, 399]),
     # fewer heads than MMA rows (one query per row block)
     (2, 1, 64, 512, 64, 100, 128, 300, 1300, [1299, 700]),
+    # prefill-like: 96 queries, one key split each (the attention writes the
+    # layer output itself), ragged windows and HCA prefixes
+    (1, 96, 64, 512, 64, 40, 64, 1300, 5200, [5199 - 53 * i for i in range(96)]),
+    (1, 80, 128, 512, 64, 30, 32, 1000, 4000, [3999 - 47 * i for i in range(80)]),
 ])
 def test_hybrid_attn(B, T, H, D, r, N_hca, k, N_c, L, pos_list):
     """One softmax over the selected CSA entries, the HCA entries and the SWA
     window, merged with the sink, equals the oracle's merge of the three
-    branches -- through the direct output and through the split partials."""
+    branches -- through the direct output, through the split partials, and
+    straight to the layer output (hybrid_attn_out: written by the attention
+    kernel when each query's keys take one split, else by a merge)."""
     q = randn_bf16((B, T, H, D), 91)
     kv_h = randn_bf16((B, N_hca, D), 92)
     kv_c = randn_bf16((B, N_c, D), 93)
@@ -667,6 +673,17 @@ def test_hybrid_attn(B, T, H, D, r, N_hca, k, N_c, L, pos_list):
     sparse = hattn.hybrid_attn(qt, kv_c.to(DEV), idx.to(DEV), None, None, d["pos"], r=r, W=128,
                                q_prepped=True, partials=True, segments=hattn.SEG_CSA)
     out3, lse3 = hattn.lse_merge_splits([dense, sparse], d["pos"], r=r, H=H, sink=sink.to(DEV))
+    out4, lse4 = hattn.hybrid_attn_out(qt, kv_c.to(DEV), idx.to(DEV), kvh_dev, kv_w, d["pos"],
+                                       r=r, sink=sink.to(DEV), q_prepped=True)
+    out5, lse5 = hattn.hybrid_attn_out(d["q"], kv_c.to(DEV), idx.to(DEV), kvh_dev, kv_w,
+                                       d["pos"], r=r, dependent=True)
+    # one key set alone (the branch kernels, finalised the same way)
+    out6, lse6 = hattn.hybrid_attn_out(qt, None, None, kvh_dev, None, d["pos"], r=r, k=k, W=128,
+                                       sink=sink.to(DEV), q_prepped=True,
+                                       segments=hattn.SEG_HCA)
+    out7, lse7 = hattn.hybrid_attn_out(qt, kv_c.to(DEV), idx.to(DEV), None, None, d["pos"], r=r,
+                                       W=128, sink=sink.to(DEV), q_prepped=True,
+                                       segments=hattn.SEG_CSA)
     hattn.check_status()
     qb, pn = bits(q), pos.numpy()
     ro = [orc.attention(orc.KIND_SPARSE, qb, bits(kv_c), pn, idx=idx.numpy(), r=r),
@@ -676,6 +693,13 @@ def test_hybrid_attn(B, T, H, D, r, N_hca, k, N_c, L, pos_list):
     check_attn(out, lse, ref, rl, "fused, direct output")
     check_attn(out2, lse2, ref, rl, "fused, split partials")
     check_attn(out3, lse3, ref, rl, "fused, key sets in two calls")
+    check_attn(out4, lse4, ref, rl, "fused, layer output")
+    ref5, rl5 = orc.merge([x[0] for x in ro], [x[1] for x in ro], None, pn, r)
+    check_attn(out5, lse5, ref5, rl5, "fused, layer output without a sink, raw queries")
+    ref6, rl6 = orc.merge([ro[1][0]], [ro[1][1]], sink.numpy(), pn, r)
+    check_attn(out6, lse6, ref6, rl6, "HCA alone, layer output")
+    ref7, rl7 = orc.merge([ro[0][0]], [ro[0][1]], sink.numpy(), pn, r)
+    check_attn(out7, lse7, ref7, rl7, "CSA alone, layer output")
 
 
 def test_hybrid_attn_bad_index_is_reported():

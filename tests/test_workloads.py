@@ -137,19 +137,26 @@ def test_stack_launch_count_at_1m():
 
 
 def test_which_steps_take_the_fused_attention():
-    """Decode steps of any branch subset and all-three-branch steps take the
-    fused attention; a prefill of one or two branches (many queries per
-    sequence) runs the branch calls. The segment mask names the branches."""
+    """Every configured workload takes the fused attention: decode steps of
+    any branch subset, the H = 128 HCA prefill, and the CSA prefill (its
+    sparse branch runs one query per row block anyway; the 1 GB window
+    buffer fits the 2 GB bound).  The prefills' queries each take one key
+    split, so the attention writes the layer output and no merge follows;
+    the decode steps split each query's keys and merge.  The segment mask
+    names the branches."""
     from sparse_attention_26_b300 import hattn
-    want = {"hybrid_decode_1m": True, "hybrid_decode_1m_mtp2": True, "pro_csa_decode": True,
-            "hca_decode": True, "hca_prefill": False, "flash_csa_prefill": False}
+    want = {"hybrid_decode_1m": (True, False), "hybrid_decode_1m_mtp2": (True, False),
+            "pro_csa_decode": (True, False), "hca_decode": (True, False),
+            "hca_prefill": (True, True), "flash_csa_prefill": (True, True)}
     seg = {"csa": hattn.SEG_CSA, "hca": hattn.SEG_HCA, "swa": hattn.SEG_SWA}
-    for name, fused in want.items():
+    for name, (fused, final) in want.items():
         wl, layer = _meta_layer(name)
         assert layer.can_fuse(wl.T) == fused, name
+        assert layer.fused_final(wl.T) == final, name
         assert layer.segments() == sum(seg[b] for b in wl.branches), name
         names = layer.event_names(wl.T)
         assert ("attn_fused" in names) == fused, (name, names)
+        assert ("merge" in names) == (not final), (name, names)
         assert ("indexer" in names) == ("csa" in wl.branches), (name, names)
 
 

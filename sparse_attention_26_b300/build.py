@@ -69,7 +69,7 @@ def build(force=False, verbose=False):
                 print(out)
     if force or jobs or _stale(LIB, objs):
         run([nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", LIB] + objs +
-            ["-lcublasLt", "-Xlinker", "-rpath=" + _cuda_lib_dir(nvcc)])
+            ["-Xlinker", "-rpath=" + _cuda_lib_dir(nvcc)])
     return LIB
 
 

@@ -591,7 +591,32 @@ int hattn_compress_hidden(const void* x, const void* W, const void* gate, const 
   a.j_end = j_end;
   a.eps = eps;
   make_rope_coef(rope_base, r, &a.rope);
-  cudaError_t e = launch_compress_hidden(a, workspace, num_sms_or_default(),
+  int sms = 0;
+  int* status = nullptr;
+  if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  // the projection's operands: the pooled parts of a chunk (rows past the
+  // chunk's entries read zeros or the previous chunk's rows, and their
+  // outputs are not written) and W, all in 128-byte swizzled boxes
+  const size_t ce = hidden_chunk_entries((int64_t)B * (j_end - j_begin));
+  CUtensorMap tm_ah, tm_al, tm_w;
+  {
+    const uint64_t dims[2] = {(uint64_t)dm, (uint64_t)ce};
+    const uint64_t strides[1] = {(uint64_t)dm * 2};
+    const uint32_t box[2] = {64, 128};
+    rc = make_tmap(&tm_ah, workspace, 2, dims, strides, box, "pooled hi");
+    if (rc) return rc;
+    rc = make_tmap(&tm_al, static_cast<uint8_t*>(workspace) + hidden_part_bytes(ce, dm), 2, dims,
+                   strides, box, "pooled lo");
+    if (rc) return rc;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)(D + dI), (uint64_t)dm};
+    const uint64_t strides[1] = {(uint64_t)(D + dI) * 2};
+    const uint32_t box[2] = {64, 64};
+    rc = make_tmap(&tm_w, W, 2, dims, strides, box, "W");
+    if (rc) return rc;
+  }
+  cudaError_t e = launch_compress_hidden(a, workspace, sms, tm_ah, tm_al, tm_w, status,
                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "compress from hidden states");
   return ok();

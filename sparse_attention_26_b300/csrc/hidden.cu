@@ -10,15 +10,14 @@
 // to, never writes per-token KV rows, and runs the projection on one row per
 // entry: a quarter of the tokens for CSA, 1/128 for HCA.
 //
-// Three steps per chunk of entries:
+// Two kernels per chunk of entries:
 //   1. pool_hidden_kernel: the gate softmax of each window and the pooled row
 //      x_bar in fp32, stored as a pair of bf16 rows hi + lo (hi = bf16(x_bar),
 //      lo = bf16(x_bar - hi)) that together keep ~16 significant bits;
-//   2. two bf16 GEMMs (cuBLASLt, fp32 accumulation and output):
-//      Y = hi . W + lo . W;
-//   3. entry_norm_rope_kernel: RMSNorm of Y's KV columns, RoPE at the
-//      entry's last token, bf16 KV entry; the indexer-key columns in bf16.
-#include <cublasLt.h>
+//   2. project_entries_kernel: Y = hi . W + lo . W on the tensor cores
+//      (tcgen05, fp32 accumulation in tensor memory), then in its epilogue the
+//      RMSNorm of Y's KV columns, RoPE at the entry's last token and the bf16
+//      KV entry, or the indexer-key columns in bf16.  Y never leaves the SM.
 
 #include "common.cuh"
 #include "kernels.h"
@@ -114,126 +113,267 @@ __global__ void __launch_bounds__(kPoolThreads)
   }
 }
 
-// One warp per entry: RMSNorm + RoPE of the KV columns, the indexer key.
-__global__ void __launch_bounds__(256)
-    entry_norm_rope_kernel(const __grid_constant__ HiddenArgs a, int64_t e0, int64_t ne,
-                           const float* __restrict__ Y) {
-  __shared__ float rc[4][kMaxRopePairs];
-  load_rope_coef(rc, a.rope, a.r);
-  const int lane = threadIdx.x & 31;
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (e >= ne) return;
-  const int64_t nj = a.j_end - a.j_begin;
-  const int64_t flat = e0 + e;
-  const int b = static_cast<int>(flat / nj);
-  const int64_t j = a.j_begin + flat % nj;
-  const int P = a.D + a.dI;
-  const float* y = Y + e * P;
-  float ss = 0.f;
-  for (int d = lane; d < a.D; d += 32) ss = fmaf(y[d], y[d], ss);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
-  const int64_t p = static_cast<int64_t>(a.m) * (j + 1) - 1;
-  const int d0 = a.D - a.r;
-  __nv_bfloat16* kv = a.kv_out + ((int64_t)b * a.N_cap + j) * a.D;
-  // lanes take consecutive pairs so that each rotation stays in one lane
-  for (int d = 2 * lane; d < a.D; d += 64) {
-    float x0 = y[d] * inv * (a.gamma ? a.gamma[d] : 1.f);
-    float x1 = y[d + 1] * inv * (a.gamma ? a.gamma[d + 1] : 1.f);
-    if (d >= d0) {
-      float sn, cs;
-      rope_cs(rc, (d - d0) / 2, p, &sn, &cs);
-      const float t0 = x0 * cs - x1 * sn;
-      x1 = x0 * sn + x1 * cs;
-      x0 = t0;
+// ---------------------------------------------------------------- projection
+// Y = hi . W + lo . W for a tile of 128 pooled entries, on the tensor cores,
+// with the entry epilogue fused: one CTA per (128-entry tile, column group),
+// column group 0 the D KV columns (RMSNorm, RoPE at the entry's last token,
+// bf16 KV entry), group 1 the dI indexer-key columns (bf16).  K = dm runs in
+// blocks of 64: per block the A tiles hi and lo (128 rows x 128 B each, TMA,
+// 128-byte swizzle, K-major) and the W rows (64 x N, TMA boxes of 64 columns,
+// MN-major), and per 16-wide K step one tcgen05.mma per A tile and 256-column
+// piece of N, all into one fp32 accumulator in tensor memory.
+// Warps: 0 loads, 1 issues the MMAs, 2..5 run the epilogue (one row each).
+constexpr int kProjThreads = 192;
+constexpr int kProjMaxStages = 4;
+
+struct ProjSmem {
+  uint64_t full[kProjMaxStages];
+  uint64_t empty[kProjMaxStages];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct ProjPlan {
+  int n;       // accumulator columns of the tile (a multiple of 64)
+  int stages;
+  uint32_t stage_bytes, tmem_cols;
+  size_t smem_bytes;
+};
+
+__host__ __device__ inline ProjPlan proj_plan(int n) {
+  ProjPlan p;
+  p.n = n;
+  p.stage_bytes = 2u * 16384u + static_cast<uint32_t>(n) * 128u;
+  const size_t room = 227 * 1024 - 1024 - (sizeof(ProjSmem) + 15) / 16 * 16;
+  p.stages = static_cast<int>(room / p.stage_bytes);
+  if (p.stages > kProjMaxStages) p.stages = kProjMaxStages;
+  p.tmem_cols = n <= 64 ? 64 : (n <= 128 ? 128 : (n <= 256 ? 256 : 512));
+  p.smem_bytes = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (sizeof(ProjSmem) + 15) / 16 * 16;
+  return p;
+}
+
+__global__ void __launch_bounds__(kProjThreads, 1)
+    project_entries_kernel(const __grid_constant__ CUtensorMap tm_ah,
+                           const __grid_constant__ CUtensorMap tm_al,
+                           const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ HiddenArgs a, int64_t e0, int64_t ne,
+                           int n_kv, int n_ik, int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const bool kv_tile = blockIdx.y == 0;
+  const int n = kv_tile ? n_kv : n_ik;  // accumulator columns
+  const ProjPlan pl = proj_plan(n);
+  ProjSmem* sm = reinterpret_cast<ProjSmem*>(base + pl.stages * pl.stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * 128;  // first entry of the tile (chunk-relative)
+  const int col0 = kv_tile ? 0 : a.D;                          // first W column of the group
+  const int nkb = (a.dm + 63) / 64;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < pl.stages; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
     }
-    *reinterpret_cast<uint32_t*>(kv + d) = pack_bf16x2(x0, x1);
+    mbar_init(smem_u32(&sm->done), 1);
+    sm->abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_ah);
+    tma_prefetch_desc(&tm_al);
+    tma_prefetch_desc(&tm_w);
   }
-  if (a.ik_out) {
-    __nv_bfloat16* ik = a.ik_out + ((int64_t)b * a.N_cap + j) * a.dI;
-    for (int d = 2 * lane; d < a.dI; d += 64)
-      *reinterpret_cast<uint32_t*>(ik + d) = pack_bf16x2(y[a.D + d], y[a.D + d + 1]);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm->tmem_base), pl.tmem_cols);
+    tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int* abort = &sm->abort;
+  if (warp == 0) {
+    // ------------------------------------------------------------ loads
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int kb = 0; kb < nkb && !*abort; ++kb) {
+        const int st = kb % pl.stages;
+        const uint32_t ph = static_cast<uint32_t>(kb / pl.stages) & 1u;
+        // the stage's previous use (block kb - stages) has been read by its MMAs
+        if (kb >= pl.stages &&
+            !mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, status, kWaitLimitNs, 50))
+          break;
+        uint8_t* sb = base + st * pl.stage_bytes;
+        const uint32_t fb = smem_u32(&sm->full[st]);
+        mbar_arrive_expect_tx(fb, pl.stage_bytes);
+        tma_load_2d(smem_u32(sb), &tm_ah, kb * 64, static_cast<int32_t>(m0), fb);
+        tma_load_2d(smem_u32(sb + 16384), &tm_al, kb * 64, static_cast<int32_t>(m0), fb);
+        for (int c = 0; c < n / 64; ++c)
+          tma_load_2d(smem_u32(sb + 32768 + c * 8192), &tm_w, col0 + c * 64, kb * 64, fb);
+        ++issued;
+      }
+      if (*abort) {
+        // the copies already issued land before the CTA exits
+        for (int64_t x = issued > pl.stages ? issued - pl.stages : 0; x < issued; ++x)
+          mbar_wait(smem_u32(&sm->full[x % pl.stages]), static_cast<uint32_t>(x / pl.stages) & 1u,
+                    nullptr, nullptr, 10000000ull, 51);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMAs
+    if (lane == 0) {
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int st = kb % pl.stages;
+        ok = mbar_wait(smem_u32(&sm->full[st]), static_cast<uint32_t>(kb / pl.stages) & 1u, abort,
+                       status, kWaitLimitNs, 52);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(base + st * pl.stage_bytes);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ah = smem_desc(sa + ks * 32, 16, 1024, kSwizzle128B);
+          const uint64_t al = smem_desc(sa + 16384 + ks * 32, 16, 1024, kSwizzle128B);
+          for (int c0 = 0; c0 < n; c0 += 256) {
+            const int nn = n - c0 < 256 ? n - c0 : 256;
+            const uint32_t idesc = idesc_bf16(128, nn, 0, 1);
+            // W rows of this K step, columns c0 .. c0 + nn: MN-major, one
+            // 64-column chunk (64 K rows x 128 B) after another
+            const uint64_t bd =
+                smem_desc(sa + 32768 + (c0 / 64) * 8192 + ks * 2048, 8192, 1024, kSwizzle128B);
+            mma_bf16_ss(tmem + c0, ah, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + c0, al, bd, idesc, 1u);
+          }
+        }
+        mma_commit(smem_u32(&sm->empty[st]));
+      }
+      // every MMA issued above completes before `done` (also on an abort)
+      mma_commit(smem_u32(&sm->done));
+      if (!ok) mbar_wait(smem_u32(&sm->done), 0, nullptr, nullptr, 10000000ull, 53);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // tensor-memory lane = tile row
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    bool ok = mbar_wait(smem_u32(&sm->done), 0, abort, status, kWaitLimitNs, 54);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const int64_t e = m0 + row;  // chunk-relative entry
+      const bool valid = e < ne;
+      const int ncols = kv_tile ? a.D : a.dI;
+      // the stage buffers are free once every MMA has completed: each row
+      // is staged as bf16 there, then leaves by one bulk copy
+      const int rstride = ncols * 2 + 16;
+      uint8_t* srow = base + row * rstride;
+      float inv = 1.f;
+      if (kv_tile) {
+        float ss = 0.f;
+        for (int c = 0; c < a.D; c += 32) {
+          float y[32];
+          tmem_ld32(tmem + lane_base + c, y);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ss = fmaf(y[i], y[i], ss);
+        }
+        inv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
+      }
+      const int64_t nj = a.j_end - a.j_begin;
+      const int64_t flat = e0 + (valid ? e : 0);
+      const int bb = static_cast<int>(flat / nj);
+      const int64_t j = a.j_begin + flat % nj;
+      const int64_t p = static_cast<int64_t>(a.m) * (j + 1) - 1;  // the entry's last token
+      const int d0 = a.D - a.r;
+      for (int c = 0; c < ncols; c += 32) {
+        float y[32];
+        tmem_ld32(tmem + lane_base + c, y);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float x0 = y[i], x1 = y[i + 1];
+          if (kv_tile) {
+            const int d = c + i;
+            x0 *= inv * (a.gamma ? a.gamma[d] : 1.f);
+            x1 *= inv * (a.gamma ? a.gamma[d + 1] : 1.f);
+            if (d >= d0) {
+              float sn, cs;
+              rope_cs(a.rope.c, (d - d0) >> 1, p, &sn, &cs);
+              const float t0 = x0 * cs - x1 * sn;
+              x1 = x0 * sn + x1 * cs;
+              x0 = t0;
+            }
+          }
+          pk[i >> 1] = pack_bf16x2(x0, x1);
+        }
+        // (ncols is a multiple of 8: whole 16-byte pieces)
+        const int nq = (ncols - c) < 32 ? (ncols - c) / 8 : 4;
+        for (int q = 0; q < nq; ++q)
+          reinterpret_cast<uint4*>(srow + c * 2)[q] =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      if (valid) {
+        __nv_bfloat16* dst = kv_tile ? a.kv_out + ((int64_t)bb * a.N_cap + j) * a.D
+                                     : a.ik_out + ((int64_t)bb * a.N_cap + j) * a.dI;
+        bulk_copy_s2g(dst, smem_u32(srow), static_cast<uint32_t>(ncols) * 2u);
+        bulk_commit();
+        bulk_wait_read();
+      }
+    } else {
+      // no MMA may still write the accumulator when it is released
+      mbar_wait(smem_u32(&sm->done), 0, nullptr, nullptr, 10000000ull, 55);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, pl.tmem_cols);
 }
-
-// One cuBLASLt handle per host thread (created on first use).
-thread_local cublasLtHandle_t t_lt = nullptr;
-
-// Y [ne][P] fp32 (row-major) = X [ne][dm] bf16 . W [dm][P] bf16, added to Y
-// when accumulate is set.  In cuBLASLt's column-major terms this is
-// Y^T (P x ne) = W^T (P x dm) . X^T (dm x ne), no transposes.
-cudaError_t project(const __nv_bfloat16* X, const __nv_bfloat16* W, float* Y, int64_t ne, int dm,
-                    int P, bool accumulate, void* lt_ws, size_t lt_ws_bytes, cudaStream_t stream) {
-  if (!t_lt && cublasLtCreate(&t_lt) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-  cublasLtMatmulDesc_t op = nullptr;
-  cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-  cublasLtMatmulPreference_t pref = nullptr;
-  cudaError_t err = cudaErrorUnknown;
-  const float one = 1.f, beta = accumulate ? 1.f : 0.f;
-  cublasLtMatmulHeuristicResult_t heur = {};
-  int found = 0;
-  if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS)
-    goto done;
-  if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, P, dm, P) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, dm, ne, dm) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatrixLayoutCreate(&lc, CUDA_R_32F, P, ne, P) != CUBLAS_STATUS_SUCCESS)
-    goto done;
-  if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS) goto done;
-  cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
-                                       &lt_ws_bytes, sizeof lt_ws_bytes);
-  if (cublasLtMatmulAlgoGetHeuristic(t_lt, op, la, lb, lc, lc, pref, 1, &heur, &found) !=
-          CUBLAS_STATUS_SUCCESS ||
-      found < 1)
-    goto done;
-  if (cublasLtMatmul(t_lt, op, &one, W, la, X, lb, &beta, Y, lc, Y, lc, &heur.algo, lt_ws,
-                     lt_ws_bytes, stream) == CUBLAS_STATUS_SUCCESS)
-    err = cudaSuccess;
-done:
-  if (pref) cublasLtMatmulPreferenceDestroy(pref);
-  if (lc) cublasLtMatrixLayoutDestroy(lc);
-  if (lb) cublasLtMatrixLayoutDestroy(lb);
-  if (la) cublasLtMatrixLayoutDestroy(la);
-  if (op) cublasLtMatmulDescDestroy(op);
-  return err;
-}
-
 }  // namespace
+
+size_t hidden_part_bytes(size_t ce, int dm) { return (ce * dm * 2 + 255) / 256 * 256; }
 
 size_t hidden_chunk_entries(int64_t total) { return total < kHiddenChunk ? total : kHiddenChunk; }
 
 size_t hidden_workspace_bytes(int64_t total, int dm, int P) {
+  (void)P;
   const size_t ce = hidden_chunk_entries(total);
-  auto up = [](size_t n) { return (n + 255) / 256 * 256; };
-  return 2 * up(ce * dm * 2) + up(ce * P * 4) + kHiddenLtWorkspace;
+  return 2 * hidden_part_bytes(ce, dm);
 }
 
+int hidden_ik_cols(int dI) { return dI <= 0 ? 0 : (dI + 63) / 64 * 64; }
+
 cudaError_t launch_compress_hidden(const HiddenArgs& a, void* ws, int num_sms,
-                                   cudaStream_t stream) {
+                                   const CUtensorMap& tm_ah, const CUtensorMap& tm_al,
+                                   const CUtensorMap& tm_w, int* status, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(a.B) * (a.j_end - a.j_begin);
   if (total <= 0) return cudaSuccess;
   const int64_t ce = static_cast<int64_t>(hidden_chunk_entries(total));
-  auto up = [](size_t n) { return (n + 255) / 256 * 256; };
   uint8_t* p = static_cast<uint8_t*>(ws);
   __nv_bfloat16* xh = reinterpret_cast<__nv_bfloat16*>(p);
-  p += up((size_t)ce * a.dm * 2);
-  __nv_bfloat16* xl = reinterpret_cast<__nv_bfloat16*>(p);
-  p += up((size_t)ce * a.dm * 2);
-  float* Y = reinterpret_cast<float*>(p);
-  p += up((size_t)ce * (a.D + a.dI) * 4);
-  void* lt_ws = p;
+  __nv_bfloat16* xl = reinterpret_cast<__nv_bfloat16*>(p + hidden_part_bytes(ce, a.dm));
+  const int n_kv = a.D, n_ik = hidden_ik_cols(a.dI);
+  // each column group's plan fits one CTA; the launch gives the larger
+  const size_t s_kv = proj_plan(n_kv).smem_bytes;
+  const size_t s_ik = n_ik > 0 ? proj_plan(n_ik).smem_bytes : 0;
+  const size_t smem = s_kv > s_ik ? s_kv : s_ik;
+  cudaError_t e = cudaFuncSetAttribute(project_entries_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   for (int64_t e0 = 0; e0 < total; e0 += ce) {
     const int64_t ne = (total - e0) < ce ? (total - e0) : ce;
     const int64_t grid = ne < (int64_t)num_sms * 8 ? ne : (int64_t)num_sms * 8;
     pool_hidden_kernel<<<static_cast<unsigned>(grid), kPoolThreads, 0, stream>>>(a, e0, ne, xh,
                                                                                xl);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = project(xh, a.W, Y, ne, a.dm, a.D + a.dI, false, lt_ws, kHiddenLtWorkspace, stream);
-    if (e != cudaSuccess) return e;
-    e = project(xl, a.W, Y, ne, a.dm, a.D + a.dI, true, lt_ws, kHiddenLtWorkspace, stream);
-    if (e != cudaSuccess) return e;
-    entry_norm_rope_kernel<<<static_cast<unsigned>((ne + 7) / 8), 256, 0, stream>>>(a, e0, ne, Y);
+    // one CTA per (128-entry tile, column group); the shared memory of the
+    // larger group serves both
+    const dim3 g(static_cast<unsigned>((ne + 127) / 128), n_ik > 0 ? 2u : 1u, 1u);
+    project_entries_kernel<<<g, kProjThreads, smem, stream>>>(tm_ah, tm_al, tm_w, a, e0, ne, n_kv,
+                                                              n_ik, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -91,11 +91,16 @@ struct HiddenArgs {
   RopeCoef rope;
 };
 constexpr int64_t kHiddenChunk = 16384;          // entries pooled and projected per pass
-constexpr size_t kHiddenLtWorkspace = 32u << 20;  // the GEMM's scratch
 size_t hidden_chunk_entries(int64_t total);
+size_t hidden_part_bytes(size_t ce, int dm);      // one pooled part (hi or lo) of a chunk
 size_t hidden_workspace_bytes(int64_t total, int dm, int P);
+int hidden_ik_cols(int dI);                       // accumulator columns of the indexer-key group
+// tm_ah / tm_al: the pooled parts [chunk entries][dm] bf16 in the workspace
+// (boxes {64, 128}); tm_w: W [dm][D + dI] (boxes {64 columns, 64 rows});
+// all 128-byte swizzled.
 cudaError_t launch_compress_hidden(const HiddenArgs& a, void* ws, int num_sms,
-                                   cudaStream_t stream);
+                                   const CUtensorMap& tm_ah, const CUtensorMap& tm_al,
+                                   const CUtensorMap& tm_w, int* status, cudaStream_t stream);
 
 // ------------------------------------------------------------ E4M3 rows
 // rows x n bf16 -> E4M3 codes [rows][n] and row scales [rows]; n % 4 == 0.

@@ -81,6 +81,8 @@ def test_csa_compress(B, L, D, dI, r, j0, j1):
     (2, 1024, 512, 512, 128, 4, 8, 64, 0, 256),      # a CSA cache build
     (1, 1030, 1024, 512, 128, 4, 8, 64, 200, 257),   # an entry range, ragged length
     (2, 1024, 512, 512, 0, 128, 128, 64, 0, 8),      # HCA: no indexer key
+    (1, 600, 200, 64, 32, 4, 8, 16, 0, 150),         # a ragged last K block; a narrow key group
+    (1, 520, 128, 256, 64, 4, 8, 32, 3, 130),        # mid-size D: one 256-column product
 ])
 def test_compress_hidden(B, L, dm, D, dI, m, w, r, j0, j1):
     """Entries from hidden states (pooled, then projected once) against the

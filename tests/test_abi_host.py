@@ -256,8 +256,10 @@ def test_ring_and_hidden_validation(L):
     rc = L.hattn_compress_hidden(FAKE, FAKE, FAKE, N, 1, 1024, 512, 512, 128, 4, 8, 64, 1e4, 1e-6,
                                  0, 256, FAKE, N, 256, FAKE, 1 << 30, s)
     assert rc == hattn.INVALID_ARG and "ik_out" in _err(L)
+    # the two bf16 parts (hi, lo) of each pooled row; the projection keeps
+    # its fp32 result in tensor memory
     need = L.hattn_compress_hidden_workspace_bytes(1, 0, 256, 512, 512, 128)
-    assert need > 256 * 512 * 4
+    assert need == 2 * 256 * 512 * 2
     rc = L.hattn_compress_hidden(FAKE, FAKE, FAKE, N, 1, 1024, 512, 512, 128, 4, 8, 64, 1e4, 1e-6,
                                  0, 256, FAKE, FAKE, 256, FAKE, need - 1, s)
     assert rc == hattn.INVALID_ARG and "workspace" in _err(L)

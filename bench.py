@@ -826,10 +826,11 @@ def run_stack(args, world, rank, local):
 
 def run_cache_build(args, world, rank, local):
     """The cache build of one sequence from hidden states: the CSA entries
-    (with indexer keys) and the HCA entries of L tokens, each by
-    hattn_compress_hidden (pool the window's hidden states, project once per
-    entry, norm and rope).  Hidden states and weights are seeded N(0,1) bf16
-    (weights scaled by 1/sqrt(d_model))."""
+    (with indexer keys) and the HCA entries of L tokens in one call,
+    hattn_compress_hidden_pair (one read of the hidden states: pool each
+    window, project once per entry on the tensor cores, norm and rope).
+    Hidden states and weights are seeded N(0,1) bf16 (weights scaled by
+    1/sqrt(d_model))."""
     import torch
     from sparse_attention_26_b300 import hattn
 
@@ -849,14 +850,13 @@ def run_cache_build(args, world, rank, local):
     kv_c = torch.empty((1, L // 4, D), dtype=torch.bfloat16, device=dev)
     ik_c = torch.empty((1, L // 4, dI), dtype=torch.bfloat16, device=dev)
     kv_h = torch.empty((1, L // 128, D), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(max(hattn.lib().hattn_compress_hidden_workspace_bytes(1, 0, L // 4, dm, D, dI),
-                         hattn.lib().hattn_compress_hidden_workspace_bytes(1, 0, L // 128, dm, D, 0)),
+    ws = torch.empty(hattn.lib().hattn_compress_hidden_pair_workspace_bytes(1, L, L // 4, L // 128,
+                                                                           dm),
                      dtype=torch.uint8, device=dev)
 
     def build():
-        hattn.compress_hidden(x, W_c, g_c, D=D, r=r, m=4, w=8, kv_out=kv_c, ik_out=ik_c,
-                              workspace=ws)
-        hattn.compress_hidden(x, W_h, g_h, D=D, r=r, m=128, w=128, kv_out=kv_h, workspace=ws)
+        hattn.compress_hidden_pair(x, W_c, g_c, W_h, g_h, D=D, r=r, kv_c=kv_c, ik_c=ik_c,
+                                   kv_h=kv_h, workspace=ws)
 
     for _ in range(args.warmup):
         build()
@@ -876,9 +876,9 @@ def run_cache_build(args, world, rank, local):
     hbm, _, src = peaks()
     x_bytes = L * dm * 2
     n_c, n_h = L // 4, L // 128
-    # both passes read the hidden states once (the CSA windows overlap by
-    # half: their second read is of rows just read), write their entries
-    alg_bytes = 2 * x_bytes + n_c * (D + dI) * 2 + n_h * D * 2 + 2 * L * 2
+    # one read of the hidden states (the overlapping CSA windows and the HCA
+    # window of a block re-read rows just read), the two gate rows, the entries
+    alg_bytes = x_bytes + n_c * (D + dI) * 2 + n_h * D * 2 + 2 * L * 2
     # the projections: pooled rows (two bf16 parts each) times W
     flops = 2 * 2.0 * dm * (n_c * (D + dI) + n_h * D)
     achieved = alg_bytes / (ms / 1e3) / 1e9
@@ -889,7 +889,7 @@ def run_cache_build(args, world, rank, local):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "cache_build_1m_from_hidden", "context_tokens": L, "d_model": dm,
                    "head_dim": D, "indexer_dim": dI, "csa_entries": n_c, "hca_entries": n_h},
-        "roofline": {"bound": "hbm", "kernel": "whole build (pool, project, norm)",
+        "roofline": {"bound": "hbm", "kernel": "whole build (pool both caches, project, norm)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": None, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes": alg_bytes, "projection_flops": flops,

@@ -137,6 +137,29 @@ HATTN_API int hattn_compress_hidden(const void* x, const void* W, const void* ga
                                     int64_t N_cap, void* workspace, size_t ws_bytes,
                                     hattn_stream_t stream);
 
+/* Both caches of a layer from hidden states in one read of them ([DD]
+ * "Infrastructure and Deployment": fewer passes over the data): the CSA
+ * entries C(4, 8) with their indexer keys (W_c [dm][D + dI], gate_c) and the
+ * HCA entries C(128, 128) (W_h [dm][D], gate_h) of the first L tokens of each
+ * sequence, as hattn_compress_hidden computes each (same pooling, projection,
+ * RMSNorm with gamma_kv, RoPE at the entry's last token):
+ *   kv_c [B][N_c][D], ik_c [B][N_c][dI] (NULL when dI == 0), entries
+ *   j < min(N_c, L/4); kv_h [B][N_h][D], entries j < min(N_h, L/128), which
+ *   need min(N_c, L/4) >= 32 * (HCA entries - 1) + 1 (full caches do).
+ * Each 128-token block's hidden states come from HBM once: its CSA windows
+ * read them, and its HCA window, pooled right after, finds them in L2.
+ * Workspace: hattn_compress_hidden_pair_workspace_bytes() bytes (the pooled
+ * rows of one pass of 16,384 CSA entries, then those of every HCA entry). */
+HATTN_API size_t hattn_compress_hidden_pair_workspace_bytes(int B, int64_t L, int64_t N_c,
+                                                            int64_t N_h, int dm);
+HATTN_API int hattn_compress_hidden_pair(const void* x, const void* W_c, const void* gate_c,
+                                         const void* W_h, const void* gate_h,
+                                         const float* gamma_kv, int B, int64_t L_cap, int64_t L,
+                                         int dm, int D, int dI, int r, float rope_base, float eps,
+                                         void* kv_c, void* ik_c, int64_t N_c, void* kv_h,
+                                         int64_t N_h, void* workspace, size_t ws_bytes,
+                                         hattn_stream_t stream);
+
 /* Ring-buffer raw caches.  A decode loop needs only the newest raw tokens:
  * the compressors read the window of the entry the newest token completes
  * (8 tokens for CSA, 128 for HCA) and the window keys the last W tokens.  In

@@ -622,6 +622,110 @@ int hattn_compress_hidden(const void* x, const void* W, const void* gate, const 
   return ok();
 }
 
+size_t hattn_compress_hidden_pair_workspace_bytes(int B, int64_t L, int64_t N_c, int64_t N_h,
+                                                  int dm) {
+  if (B < 1 || L < 1 || dm < 8) return 0;
+  const int64_t nc = N_c < L / 4 ? N_c : L / 4, nh = N_h < L / 128 ? N_h : L / 128;
+  if (nc <= 0) return 0;
+  return hidden_pair_workspace_bytes(B, nc, nh, dm);
+}
+
+int hattn_compress_hidden_pair(const void* x, const void* W_c, const void* gate_c,
+                               const void* W_h, const void* gate_h, const float* gamma_kv, int B,
+                               int64_t L_cap, int64_t L, int dm, int D, int dI, int r,
+                               float rope_base, float eps, void* kv_c, void* ik_c, int64_t N_c,
+                               void* kv_h, int64_t N_h, void* workspace, size_t ws_bytes,
+                               hattn_stream_t stream) {
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(W_c);
+  REQUIRE_PTR(gate_c);
+  REQUIRE_PTR(W_h);
+  REQUIRE_PTR(gate_h);
+  REQUIRE_PTR(kv_c);
+  REQUIRE_PTR(kv_h);
+  REQUIRE_F32(gamma_kv);
+  REQUIRE((ik_c == nullptr) == (dI == 0), "ik_c must be given exactly when dI > 0");
+  if (ik_c) REQUIRE_PTR(ik_c);
+  REQUIRE(B >= 1 && L_cap >= 1 && N_c >= 1 && N_h >= 1, "B, L_cap, N_c and N_h must be >= 1");
+  REQUIRE(L >= 0 && L <= L_cap, "L=%lld must be in [0, L_cap=%lld]", (long long)L,
+          (long long)L_cap);
+  REQUIRE(dm >= 8 && dm % 8 == 0, "dm=%d must be a positive multiple of 8", dm);
+  REQUIRE(D >= 64 && D <= 512 && D % 64 == 0, "D=%d must be a multiple of 64 in [64, 512]", D);
+  REQUIRE(dI == 0 || (dI >= 8 && dI <= 128 && dI % 8 == 0),
+          "dI=%d must be 0 or a multiple of 8 in [8, 128]", dI);
+  int rc = check_rope(D, r, rope_base, eps);
+  if (rc) return rc;
+  const int64_t nc = N_c < L / 4 ? N_c : L / 4, nh = N_h < L / 128 ? N_h : L / 128;
+  // the HCA entries ride on the CSA pass's 128-token blocks
+  REQUIRE(nh <= (nc + 31) / 32, "N_c=%lld holds too few CSA entries for the %lld HCA entries",
+          (long long)N_c, (long long)nh);
+  if (nc == 0) return ok();
+  const size_t need = hidden_pair_workspace_bytes(B, nc, nh, dm);
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  HiddenArgs ac;
+  ac.x = static_cast<const __nv_bfloat16*>(x);
+  ac.W = static_cast<const __nv_bfloat16*>(W_c);
+  ac.gate = static_cast<const __nv_bfloat16*>(gate_c);
+  ac.gamma = gamma_kv;
+  ac.kv_out = static_cast<__nv_bfloat16*>(kv_c);
+  ac.ik_out = static_cast<__nv_bfloat16*>(ik_c);
+  ac.B = B;
+  ac.dm = dm;
+  ac.D = D;
+  ac.dI = dI;
+  ac.m = 4;
+  ac.w = 8;
+  ac.r = r;
+  ac.L_cap = L_cap;
+  ac.N_cap = N_c;
+  ac.j_begin = 0;
+  ac.j_end = nc;
+  ac.eps = eps;
+  make_rope_coef(rope_base, r, &ac.rope);
+  HiddenArgs ah = ac;
+  ah.W = static_cast<const __nv_bfloat16*>(W_h);
+  ah.gate = static_cast<const __nv_bfloat16*>(gate_h);
+  ah.kv_out = static_cast<__nv_bfloat16*>(kv_h);
+  ah.ik_out = nullptr;
+  ah.dI = 0;
+  ah.m = 128;
+  ah.w = 128;
+  ah.N_cap = N_h;
+  ah.j_end = nh;
+  int sms = 0;
+  int* status = nullptr;
+  if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
+  const int64_t rows_c = (int64_t)B * nc < kHiddenChunk ? (int64_t)B * nc : kHiddenChunk;
+  const int64_t rows_h = (int64_t)B * nh;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  CUtensorMap tm_ch, tm_cl, tm_wc, tm_hh, tm_hl, tm_wh;
+  auto part_map = [&](CUtensorMap* m, const void* base, int64_t rows, const char* what) {
+    const uint64_t dims[2] = {(uint64_t)dm, (uint64_t)(rows > 0 ? rows : 1)};
+    const uint64_t strides[1] = {(uint64_t)dm * 2};
+    const uint32_t box[2] = {64, 128};
+    return make_tmap(m, base, 2, dims, strides, box, what);
+  };
+  auto w_map = [&](CUtensorMap* m, const void* base, int P, const char* what) {
+    const uint64_t dims[2] = {(uint64_t)P, (uint64_t)dm};
+    const uint64_t strides[1] = {(uint64_t)P * 2};
+    const uint32_t box[2] = {64, 64};
+    return make_tmap(m, base, 2, dims, strides, box, what);
+  };
+  const size_t pc = hidden_part_bytes(rows_c, dm), ph = hidden_part_bytes(rows_h, dm);
+  if ((rc = part_map(&tm_ch, wsb, rows_c, "CSA pooled hi")) ||
+      (rc = part_map(&tm_cl, wsb + pc, rows_c, "CSA pooled lo")) ||
+      (rc = part_map(&tm_hh, wsb + 2 * pc, rows_h, "HCA pooled hi")) ||
+      (rc = part_map(&tm_hl, wsb + 2 * pc + ph, rows_h, "HCA pooled lo")) ||
+      (rc = w_map(&tm_wc, W_c, D + dI, "W_c")) || (rc = w_map(&tm_wh, W_h, D, "W_h")))
+    return rc;
+  cudaError_t e = launch_compress_hidden_pair(ac, ah, workspace, sms, tm_ch, tm_cl, tm_wc, tm_hh,
+                                              tm_hl, tm_wh, status,
+                                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "compress pair from hidden states");
+  return ok();
+}
+
 int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* codes, float* scales,
                         hattn_stream_t stream) {
   REQUIRE(rows >= 0, "rows must be >= 0");

@@ -101,6 +101,19 @@ int hidden_ik_cols(int dI);                       // accumulator columns of the 
 cudaError_t launch_compress_hidden(const HiddenArgs& a, void* ws, int num_sms,
                                    const CUtensorMap& tm_ah, const CUtensorMap& tm_al,
                                    const CUtensorMap& tm_w, int* status, cudaStream_t stream);
+// Both caches in one read of the hidden states: ac the CSA pass (C(4, 8),
+// entries [0, ac.j_end) per sequence, dI > 0 allowed), ah the HCA pass
+// (C(128, 128), entries [0, ah.j_end), dI = 0), sharing x, dm and D.
+// Workspace (hidden_pair_workspace_bytes): the CSA parts of one pass, then
+// the HCA parts of every entry; tm_ch/tm_cl and tm_hh/tm_hl map them,
+// tm_wc / tm_wh the two projections.
+size_t hidden_pair_workspace_bytes(int B, int64_t nc, int64_t nh, int dm);
+cudaError_t launch_compress_hidden_pair(const HiddenArgs& ac, const HiddenArgs& ah, void* ws,
+                                        int num_sms, const CUtensorMap& tm_ch,
+                                        const CUtensorMap& tm_cl, const CUtensorMap& tm_wc,
+                                        const CUtensorMap& tm_hh, const CUtensorMap& tm_hl,
+                                        const CUtensorMap& tm_wh, int* status,
+                                        cudaStream_t stream);
 
 // ------------------------------------------------------------ E4M3 rows
 // rows x n bf16 -> E4M3 codes [rows][n] and row scales [rows]; n % 4 == 0.

@@ -77,6 +77,10 @@ _SIGS = {
                                  _vp, _vp, _vp, _sz, _i32, _vp]),
     "hattn_hybrid_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                                 _i32, _i32, _i32]),
+    "hattn_compress_hidden_pair_workspace_bytes": (_sz, [_i32, _i64, _i64, _i64, _i32]),
+    "hattn_compress_hidden_pair": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32,
+                                          _i32, _i32, _i32, _f32, _f32, _vp, _vp, _i64, _vp, _i64,
+                                          _vp, _sz, _vp]),
     "hattn_hybrid_attn_out": (_i32, [_vp, _vp, _i32, _vp, _vp, _i64, _i32, _vp, _i64, _i32, _vp,
                                      _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32,
                                      _i32, _i32, _vp, _vp, _vp, _vp, _sz, _i32, _vp]),
@@ -336,6 +340,44 @@ def compress_hidden(x, W, gate, *, D, r, m=4, w=8, j_begin=0, j_end=None, kv_out
                                        _ptr(ik_out), N_cap, _ptr(workspace), wsb,
                                        _stream(stream)))
     return kv_out, ik_out
+
+
+
+def compress_hidden_pair(x, W_c, gate_c, W_h, gate_h, *, D, r, L=None, kv_c=None, ik_c=None,
+                         kv_h=None, N_c=None, N_h=None, gamma_kv=None, rope_base=10000.0,
+                         eps=1e-6, workspace=None, stream=None):
+    """Both caches of a layer from hidden states in one read of them: the CSA
+    entries C(4, 8) with indexer keys (W_c [dm, D + dI]) and the HCA entries
+    C(128, 128) (W_h [dm, D]) of the first L tokens; returns (kv_c, ik_c or
+    None, kv_h)."""
+    _need(x, "x", torch.bfloat16, 3)
+    _need(W_c, "W_c", torch.bfloat16, 2)
+    _need(W_h, "W_h", torch.bfloat16, 2)
+    _need(gate_c, "gate_c", torch.bfloat16, 2)
+    _need(gate_h, "gate_h", torch.bfloat16, 2)
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    B, L_cap, dm = x.shape
+    L = L_cap if L is None else L
+    dI = W_c.shape[1] - D
+    dev = x.device
+    N_c = (kv_c.shape[1] if kv_c is not None else L_cap // 4) if N_c is None else N_c
+    N_h = (kv_h.shape[1] if kv_h is not None else max(1, L_cap // 128)) if N_h is None else N_h
+    if kv_c is None:
+        kv_c = torch.zeros((B, N_c, D), dtype=torch.bfloat16, device=dev)
+    if ik_c is None and dI > 0:
+        ik_c = torch.zeros((B, N_c, dI), dtype=torch.bfloat16, device=dev)
+    if kv_h is None:
+        kv_h = torch.zeros((B, N_h, D), dtype=torch.bfloat16, device=dev)
+    need = lib().hattn_compress_hidden_pair_workspace_bytes(B, L, N_c, N_h, dm)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wsb = workspace.numel() if workspace is not None else 0
+    _check(lib().hattn_compress_hidden_pair(_ptr(x), _ptr(W_c), _ptr(gate_c), _ptr(W_h),
+                                            _ptr(gate_h), _ptr(gamma_kv), B, L_cap, L, dm, D, dI,
+                                            r, rope_base, eps, _ptr(kv_c), _ptr(ik_c), N_c,
+                                            _ptr(kv_h), N_h, _ptr(workspace), wsb,
+                                            _stream(stream)))
+    return kv_c, ik_c, kv_h
 
 
 def quantize_e4m3(x, *, codes=None, scales=None, stream=None):

@@ -118,6 +118,38 @@ def test_compress_hidden_across_chunks():
         assert rel_l2(ik[:, j0:j1], ref_ik) <= KV_REL_L2, (j0, j1)
 
 
+@pytest.mark.parametrize("B,L,L_cap,dm,D,dI,r", [
+    (2, 1024, 1024, 512, 512, 128, 64),   # whole blocks: 256 CSA and 8 HCA entries each
+    (1, 1000, 1030, 200, 64, 32, 16),     # a ragged tail block (no HCA entry), ragged K
+])
+def test_compress_hidden_pair(B, L, L_cap, dm, D, dI, r):
+    """Both caches from one read of the hidden states equal the oracle's two
+    compressions (the same as two hattn_compress_hidden calls)."""
+    x = randn_bf16((B, L_cap, dm), 76)
+    W_c = (randn_f32((dm, D + dI), 77) / math.sqrt(dm)).to(torch.bfloat16)
+    W_h = (randn_f32((dm, D), 78) / math.sqrt(dm)).to(torch.bfloat16)
+    g_c = randn_bf16((B, L_cap), 79)
+    g_h = randn_bf16((B, L_cap), 80)
+    gamma = 1.0 + 0.1 * randn_f32((D,), 81)
+    N_c, N_h = L_cap // 4, max(1, L_cap // 128)
+    kv_c = torch.full((B, N_c, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    kv_h = torch.full((B, N_h, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    kv_c, ik_c, kv_h = hattn.compress_hidden_pair(x.to(DEV), W_c.to(DEV), g_c.to(DEV),
+                                                  W_h.to(DEV), g_h.to(DEV), D=D, r=r, L=L,
+                                                  kv_c=kv_c, kv_h=kv_h, gamma_kv=gamma.to(DEV))
+    hattn.check_status()
+    nc, nh = L // 4, L // 128
+    ref_kv, ref_ik = orc.compress_hidden(bits(x), bits(W_c), bits(g_c), 4, 8, r, 0, nc, D,
+                                         gamma=gamma.numpy())
+    assert rel_l2(kv_c[:, :nc], ref_kv) <= KV_REL_L2
+    assert rel_l2(ik_c[:, :nc], ref_ik) <= KV_REL_L2
+    ref_h, _ = orc.compress_hidden(bits(x), bits(W_h), bits(g_h), 128, 128, r, 0, nh, D,
+                                   gamma=gamma.numpy())
+    assert rel_l2(kv_h[:, :nh], ref_h) <= KV_REL_L2
+    # entries past L are untouched
+    assert torch.isnan(kv_c[:, nc:].float()).all() and torch.isnan(kv_h[:, nh:].float()).all()
+
+
 @pytest.mark.parametrize("B,L,D,r", [(2, 1024, 512, 64), (1, 300, 64, 16)])
 def test_hca_compress(B, L, D, r):
     kv = randn_bf16((B, L, D), 5)

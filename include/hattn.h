@@ -227,6 +227,31 @@ HATTN_API int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* code
 HATTN_API int hattn_quantize_mxfp4(const void* x, int64_t rows, int n, void* codes, void* scales,
                                    hattn_stream_t stream);
 
+/* Indexer scores over MXFP4 keys ([AT] "Inference efficiency": the indexer's
+ * QK path in FP4): ik4 [B][N_cap][64] code bytes and ik4_scale [B][N_cap][4]
+ * E8M0 bytes as hattn_quantize_mxfp4 writes them (dI must be 128; N_cap a
+ * multiple of 4, so that a block's scales are whole 16-byte rows).  Each bf16
+ * query row iq[b][t][h] takes the same MXFP4 round trip inside the kernel,
+ * and the score is the plain definition over the decoded values,
+ *   I[j] = sum_h w[b][t][h] * max(0, q~[b][t][h] . k~[b][j]),
+ * with fp32 accumulation.  A key costs 68 bytes of HBM (against 256 for
+ * bf16); every decoded element is exact in bf16, so the products run on the
+ * bf16 tensor-core path after the keys are decoded in shared memory.  The
+ * other arguments, limits and flags are hattn_indexer_scores_ex's. */
+HATTN_API int hattn_indexer_scores_mxfp4(const void* iq, const float* w, const void* ik4,
+                                         const void* ik4_scale, const int32_t* pos, int B, int T,
+                                         int HI, int dI, int64_t N_cap, int m, int n_sms,
+                                         int64_t fresh_from, float* score_out, int flags,
+                                         hattn_stream_t stream);
+/* hattn_indexer_topk_ex over MXFP4 keys (scores as hattn_indexer_scores_mxfp4;
+ * the workspace is hattn_indexer_topk_workspace_bytes()). */
+HATTN_API int hattn_indexer_topk_mxfp4(const void* iq, const float* w, const void* ik4,
+                                       const void* ik4_scale, const int32_t* pos, int B, int T,
+                                       int HI, int dI, int64_t N_cap, int k, int m, int n_sms,
+                                       int64_t fresh_from, int32_t* idx_out, float* score_out,
+                                       void* workspace, size_t ws_bytes, int flags,
+                                       void* split_event, hattn_stream_t stream);
+
 HATTN_API int hattn_csa_compress_fp8(const void* kv_raw, const void* ik_raw, const void* gate,
                                      const float* gamma_kv, int B, int64_t L_cap, int D, int dI,
                                      int m, int w, int r, float rope_base, float eps,

@@ -771,14 +771,17 @@ int hattn_hca_compress(const void* kv_raw, const void* gate, const float* gamma_
 namespace {
 
 // Scores of bf16 indexer keys (ik_c), or of E4M3 keys when k_scale is given
-// (ik_c then holds the codes, [B][N_cap][128] bytes).
+// (ik_c then holds the codes, [B][N_cap][128] bytes), or with mx of MXFP4
+// keys (ik_c the codes [B][N_cap][64] bytes, k_scale the E8M0 scales
+// [B][N_cap][4] bytes).
 // hist_part: the folded first selection pass (IndexerArgs::hist_part; the
 // caller has checked fold_plan), else nullptr.  grid_out: the CTAs launched.
 int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const int32_t* pos,
                         int B, int T, int HI, int dI, int64_t N_cap, int m, float* scores,
                         hattn_stream_t stream, int n_sms = 0, int64_t fresh_from = -1,
-                        const float* k_scale = nullptr, int flags = 0,
-                        uint16_t* hist_part = nullptr, int64_t* grid_out = nullptr) {
+                        const void* k_scale = nullptr, int flags = 0,
+                        uint16_t* hist_part = nullptr, int64_t* grid_out = nullptr,
+                        bool mx = false) {
   if (int rcf = check_flags(flags)) return rcf;
   REQUIRE_PTR(iq);
   REQUIRE_PTR(w);
@@ -791,20 +794,37 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   REQUIRE(m >= 1, "m must be >= 1");
   REQUIRE((int64_t)B * T * HI < (1ll << 31), "too many query heads");
   REQUIRE(n_sms >= 0, "n_sms=%d must be >= 0", n_sms);
-  const bool f8 = k_scale != nullptr;
-  if (f8) {
-    REQUIRE(dI == 128, "FP8 indexer keys need dI = 128 (one 128-byte row), got %d", dI);
-    REQUIRE(N_cap % 4 == 0, "FP8 indexer keys need N_cap %% 4 == 0 (16-byte scale rows), got %lld",
-            (long long)N_cap);
+  const bool f8 = k_scale != nullptr && !mx;
+  if (f8 || mx) {
+    REQUIRE_PTR(k_scale);
+    REQUIRE(dI == 128, "%s indexer keys need dI = 128, got %d", mx ? "MXFP4" : "FP8", dI);
+    REQUIRE(N_cap % 4 == 0, "%s indexer keys need N_cap %% 4 == 0 (16-byte scale rows), got %lld",
+            mx ? "MXFP4" : "FP8", (long long)N_cap);
   }
+  const int keys = mx ? kIdxKeysMx4 : (f8 ? kIdxKeysE4m3 : kIdxKeysBf16);
   IndexerPlan ip;
-  if (!plan_indexer(T, HI, dI, f8, hist_part != nullptr, &ip))
+  if (!plan_indexer(T, HI, dI, keys, hist_part != nullptr, &ip))
     return fail(HATTN_ERR_UNSUPPORTED, "no indexer kernel for HI=%d dI=%d", HI, dI);
   int sms = 0;
   int* status = nullptr;
   if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
   CUtensorMap tm_ik, tm_iq, tm_ks;
-  if (f8) {
+  if (mx) {
+    // a key block: 128 rows of 64 code bytes; its scales as 32 rows of 16
+    // bytes (4 keys each)
+    const uint64_t dims[3] = {64, (uint64_t)N_cap, (uint64_t)B};
+    const uint64_t strides[2] = {64, (uint64_t)N_cap * 64};
+    const uint32_t box[3] = {64, 128, 1};
+    int rc = make_tmap(&tm_ik, ik_c, 3, dims, strides, box, "ik4", CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+    const uint64_t sdims[3] = {16, (uint64_t)N_cap / 4, (uint64_t)B};
+    const uint64_t sstrides[2] = {16, (uint64_t)N_cap * 4};
+    const uint32_t sbox[3] = {16, 32, 1};
+    rc = make_tmap(&tm_ks, k_scale, 3, sdims, sstrides, sbox, "ik4_scale",
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  } else if (f8) {
     const uint64_t dims[3] = {128, (uint64_t)N_cap, (uint64_t)B};
     const uint64_t strides[2] = {128, (uint64_t)N_cap * 128};
     const uint32_t box[3] = {128, 128, 1};
@@ -846,6 +866,7 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   a.NQ = ip.NQ;
   a.KC = ip.KC;
   a.stages = ip.stages;
+  a.mx_stages = ip.mx_stages;
   a.nacc = ip.nacc;
   a.groups_per_seq = (T + ip.G - 1) / ip.G;
   a.nblk = static_cast<int>((N_cap + 127) / 128);
@@ -860,7 +881,7 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   a.hist_part = hist_part;
   if (grid_out) *grid_out = grid;
   cudaError_t e =
-      launch_indexer_score(tm_ik, tm_iq, tm_ks, a, ip, f8, grid, static_cast<cudaStream_t>(stream));
+      launch_indexer_score(tm_ik, tm_iq, tm_ks, a, ip, keys, grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
   return ok();
 }
@@ -964,9 +985,10 @@ size_t part_bytes(int64_t grid) { return round256((size_t)grid * 2 * kSelBins * 
 // scores (one query per indexer group, each CTA's slots within two rows and
 // at most 65,535 entries, and the cluster path of the selection), for an
 // indexer grid of `grid` CTAs.
-bool fold_plan(int T, int HI, int dI, bool f8, int64_t rows, int64_t N_cap, int k, int64_t grid) {
+bool fold_plan(int T, int HI, int dI, int keys, int64_t rows, int64_t N_cap, int k,
+               int64_t grid) {
   IndexerPlan ip;
-  if (!plan_indexer(T, HI, dI, f8, true, &ip)) return false;
+  if (!plan_indexer(T, HI, dI, keys, true, &ip)) return false;
   TopkPlan tp;
   if (!plan_topk(rows, N_cap, k, num_sms_or_default(), &tp) || !tp.slice_path) return false;
   const int64_t nblk = (N_cap + 127) / 128;
@@ -985,11 +1007,12 @@ int64_t indexer_grid(int64_t rows_times_nblk_groups, int n_sms, int sms) {
 // Scores, then selection (folded when fold_plan allows).  workspace layout:
 // [scores, unless score_out] [partial histograms, on the cluster path]
 // [selection scratch].
-int indexer_topk_impl(const void* iq, const float* w, const void* ik_c, const float* ik_scale,
+int indexer_topk_impl(const void* iq, const float* w, const void* ik_c, const void* ik_scale,
                       const int32_t* pos, int B, int T, int HI, int dI, int64_t N_cap, int k,
                       int m, int n_sms, int64_t fresh_from, int32_t* idx_out, float* score_out,
                       uint8_t* workspace, size_t ws_bytes, int flags, void* split_event,
-                      hattn_stream_t stream) {
+                      hattn_stream_t stream, bool mx = false) {
+  const int keys = mx ? kIdxKeysMx4 : (ik_scale ? kIdxKeysE4m3 : kIdxKeysBf16);
   const int64_t rows = (int64_t)B * T;
   float* scores = score_out;
   uint8_t* rest = workspace;
@@ -1006,7 +1029,7 @@ int indexer_topk_impl(const void* iq, const float* w, const void* ik_c, const fl
     int* status = nullptr;
     if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
     grid = indexer_grid(rows * ((N_cap + 127) / 128), n_sms, sms);
-    if (fold_plan(T, HI, dI, ik_scale != nullptr, rows, N_cap, k, grid) &&
+    if (fold_plan(T, HI, dI, keys, rows, N_cap, k, grid) &&
         part_bytes(grid) <= part_bytes(num_sms_or_default()))
       part = reinterpret_cast<uint16_t*>(rest);
     rest += part_bytes(num_sms_or_default());
@@ -1015,7 +1038,7 @@ int indexer_topk_impl(const void* iq, const float* w, const void* ik_c, const fl
   const size_t left = ws_bytes > used ? ws_bytes - used : 0;
   int64_t launched = 0;
   int rc = indexer_scores_impl(iq, w, ik_c, pos, B, T, HI, dI, N_cap, m, scores, stream, n_sms,
-                               fresh_from, ik_scale, flags, part, &launched);
+                               fresh_from, ik_scale, flags, part, &launched, mx);
   if (rc) return rc;
   if (split_event) {
     // external: an event record node when the stream is being captured
@@ -1065,6 +1088,16 @@ int hattn_indexer_scores_fp8(const void* iq, const float* w, const void* ik8,
   REQUIRE_PTR(ik_scale);
   return indexer_scores_impl(iq, w, ik8, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms,
                              fresh_from < 0 ? -1 : fresh_from, ik_scale, flags);
+}
+
+int hattn_indexer_scores_mxfp4(const void* iq, const float* w, const void* ik4,
+                               const void* ik4_scale, const int32_t* pos, int B, int T, int HI,
+                               int dI, int64_t N_cap, int m, int n_sms, int64_t fresh_from,
+                               float* score_out, int flags, hattn_stream_t stream) {
+  REQUIRE_PTR(ik4_scale);
+  return indexer_scores_impl(iq, w, ik4, pos, B, T, HI, dI, N_cap, m, score_out, stream, n_sms,
+                             fresh_from < 0 ? -1 : fresh_from, ik4_scale, flags, nullptr, nullptr,
+                             true);
 }
 
 size_t hattn_topk_workspace_bytes(int B, int T, int64_t N_cap, int k) {
@@ -1117,6 +1150,34 @@ int hattn_indexer_topk_ex(const void* iq, const float* w, const void* ik_c, cons
                            fresh_from < 0 ? -1 : fresh_from, idx_out, score_out,
                            static_cast<uint8_t*>(workspace), ws_bytes, flags, split_event,
                            stream);
+}
+
+int hattn_indexer_topk_mxfp4(const void* iq, const float* w, const void* ik4,
+                             const void* ik4_scale, const int32_t* pos, int B, int T, int HI,
+                             int dI, int64_t N_cap, int k, int m, int n_sms, int64_t fresh_from,
+                             int32_t* idx_out, float* score_out, void* workspace,
+                             size_t ws_bytes, int flags, void* split_event,
+                             hattn_stream_t stream) {
+  if (int rcf = check_flags(flags)) return rcf;
+  REQUIRE_PTR(iq);
+  REQUIRE_PTR(w);
+  REQUIRE_PTR(ik4);
+  REQUIRE_PTR(ik4_scale);
+  REQUIRE_PTR(pos);
+  REQUIRE(k >= 1 && k <= 2048, "k=%d must be in [1, 2048]", k);
+  REQUIRE_PTR(idx_out);
+  REQUIRE(dI == 128, "MXFP4 indexer keys need dI = 128, got %d", dI);
+  REQUIRE(B >= 1 && T >= 1 && N_cap >= 1, "B, T and N_cap must be >= 1");
+  REQUIRE(n_sms >= 0, "n_sms=%d must be >= 0", n_sms);
+  const size_t need = indexer_topk_ws(B, T, N_cap, k, score_out != nullptr);
+  if (need > 0) {
+    REQUIRE_PTR(workspace);
+    REQUIRE(ws_bytes >= need, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  }
+  return indexer_topk_impl(iq, w, ik4, ik4_scale, pos, B, T, HI, dI, N_cap, k, m, n_sms,
+                           fresh_from < 0 ? -1 : fresh_from, idx_out, score_out,
+                           static_cast<uint8_t*>(workspace), ws_bytes, flags, split_event,
+                           stream, true);
 }
 
 int hattn_indexer_topk_noalloc(const void* iq, const float* w, const void* ik_c,

@@ -46,6 +46,12 @@ constexpr int kBlockRows = 128;
 constexpr int kMaxStages = 12;
 constexpr int kMaxStagesBf16 = 8;
 constexpr int kMaxAcc = 4;  // accumulators in flight (TMEM columns permitting)
+// key formats of the score kernel
+constexpr int kKeyBf16 = kIdxKeysBf16, kKeyE4m3 = kIdxKeysE4m3, kKeyMx4 = kIdxKeysMx4;
+// MXFP4 keys (dI = 128): a block of 128 keys is 128 x 64 code bytes, then
+// its 128 x 4 E8M0 scale bytes
+constexpr uint32_t kMxRawBytes = 128 * 64 + 128 * 4;
+constexpr int kMaxMxStages = 8;
 constexpr int kHistWords = kSelBins / 2;  // a row's 16-bit bins, two per word
 
 struct IdxSmem {
@@ -142,6 +148,95 @@ struct SlotCursor {
   }
 };
 
+// ------------------------------------------------------------ MXFP4
+// The OCP MXFP4 element (E2M1 nibble, sign in bit 3) at scale 1: magnitudes
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_value(uint32_t n) {
+  const uint32_t m = n & 7u;
+  const float mag = m < 2u ? 0.5f * static_cast<float>(m)
+                           : __uint_as_float((((m >> 1) + 126u) << 23) | ((m & 1u) << 22));
+  return (n & 8u) ? -mag : mag;
+}
+
+// A bf16 pair of decoded elements at scale 1 (from the table) times the
+// block scale 2^s: exact.  For s >= -125 the exponent fields move by s (no
+// carry out of a half: a nonzero e2m1 half has exponent 126..129); the two
+// smallest scales go through fp32 (their products may be subnormal).
+__device__ __forceinline__ uint32_t mx_scale_pair(uint32_t v, int s) {
+  if (s >= -125) {
+    const uint32_t add = static_cast<uint32_t>(s * 128);
+    const uint32_t lo = (v & 0x7fffu) ? add : 0u;
+    const uint32_t hi = (v & 0x7fff0000u) ? (add << 16) : 0u;
+    return v + lo + hi;
+  }
+  const float f = s == -126 ? __uint_as_float(0x00800000u) : __uint_as_float(0x00400000u);
+  const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+  return pack_bf16x2(x.x * f, x.y * f);
+}
+
+// Decodes key row r of a raw MXFP4 stage (64 code bytes at r * 64, 4 scale
+// bytes at 8192 + r * 4) into row r of a bf16 stage (two 128B-swizzled
+// 64-dim chunks of 16 KB): one 16-byte piece (8 elements) per code word.
+__device__ __forceinline__ void mx_decode_row(const uint8_t* raw, const uint32_t* lut, uint8_t* A,
+                                              int r) {
+  const uint4* cw4 = reinterpret_cast<const uint4*>(raw + r * 64);
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(raw + 8192 + r * 4);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 c4 = cw4[q];  // block q: elements 32q .. 32q + 31
+    const int s = static_cast<int>((sc >> (8 * q)) & 0xffu) - 127;
+    const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t o[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) o[b] = mx_scale_pair(lut[(cw[k] >> (8 * b)) & 0xffu], s);
+      const int d = 32 * q + 8 * k;  // first element of the piece
+      *reinterpret_cast<uint4*>(A + (d >> 6) * 16384 + swz128(r, (d & 63) >> 3)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// The MXFP4 round trip of the group's bf16 query rows, in place (sQ,
+// 128B-swizzled 64-dim chunks): blocks of 32 dims share the scale
+// 2^(floor(log2 amax) - 2) (exponent at least -127), elements round to E2M1
+// (nearest, ties to even, saturating at 6) and decode back exactly.  Epilogue
+// warp e takes rows e, e + kEpiWarps, ...; lane l holds dims 4l .. 4l+3, so
+// lanes 8g .. 8g+7 hold block g.
+__device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ void mx_query_rows(uint8_t* sQ, int NQ, int ew, int lane) {
+  const int d = 4 * lane;
+  const uint32_t off = static_cast<uint32_t>(d >> 6) * NQ * 128u;
+  const uint32_t piece = (d & 63) >> 3, within = (d & 7) * 2;
+  for (int r = ew; r < NQ; r += kEpiWarps) {
+    uint2* cell = reinterpret_cast<uint2*>(sQ + off + swz128(r, piece) + within);
+    const uint2 u = *cell;
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    float amax = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int se = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 2;
+    se = se < -127 ? -127 : se;
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);  // 2^-se
+    const float sc = se >= -126 ? __uint_as_float(static_cast<uint32_t>(se + 127) << 23)
+                                : __uint_as_float(0x00400000u);          // 2^se
+    const uint32_t c0 = e2m1x2_code(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv));
+    const uint32_t c1 = e2m1x2_code(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv));
+    *cell = make_uint2(pack_bf16x2(e2m1_value(c0 & 15u) * sc, e2m1_value(c0 >> 4) * sc),
+                       pack_bf16x2(e2m1_value(c1 & 15u) * sc, e2m1_value(c1 >> 4) * sc));
+  }
+}
+
 // Quantises the group's bf16 query rows (sQ, 128B-swizzled 64-dim chunks)
 // to E4M3 codes in sQ8 (one 128-byte swizzled row each) and their scales;
 // epilogue warp e takes rows e, e + kEpiWarps, ...  Lane l holds dims
@@ -165,17 +260,20 @@ __device__ __forceinline__ void quantize_query_rows(const uint8_t* sQ, uint8_t* 
   }
 }
 
-template <bool F8>
+template <int KF>
 __global__ void __launch_bounds__(kIdxThreads, 1)
     indexer_score_kernel(const __grid_constant__ CUtensorMap tm_ik,
                          const __grid_constant__ CUtensorMap tm_iq,
                          const __grid_constant__ CUtensorMap tm_ks, const IndexerArgs a) {
+  constexpr bool F8 = KF == kKeyE4m3;  // E4M3 keys: kind::f8f6f4 products
+  constexpr bool MX = KF == kKeyMx4;   // MXFP4 keys: decoded to bf16 in shared memory
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128B-swizzled operand buffers
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   // [E4M3 query rows (FP8 keys)] [bf16 query rows] [key stages]
-  // [key scales of each stage (FP8 keys)] [IdxSmem]
+  // [key scales of each stage (FP8 keys) | raw MXFP4 stages and the decode
+  // table (MXFP4 keys)] [IdxSmem]
   const uint32_t q8_bytes = F8 ? static_cast<uint32_t>(a.NQ) * 128u : 0u;
   const uint32_t q_bytes = static_cast<uint32_t>(a.KC) * a.NQ * 128u;
   const uint32_t stage_bytes = F8 ? 16384u : static_cast<uint32_t>(a.KC) * 16384u;
@@ -183,8 +281,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   uint8_t* sQ = base + q8_bytes;
   uint8_t* sA = sQ + q_bytes;
   float* sScale = reinterpret_cast<float*>(sA + a.stages * stage_bytes);
-  IdxSmem* sm = reinterpret_cast<IdxSmem*>(sA + a.stages * stage_bytes +
-                                           (F8 ? a.stages * kBlockRows * 4 : 0));
+  uint8_t* sRaw = sA + a.stages * stage_bytes;  // MXFP4: raw stages, then the table
+  uint32_t* mxlut = reinterpret_cast<uint32_t*>(sRaw + (MX ? a.mx_stages * kMxRawBytes : 0));
+  IdxSmem* sm = reinterpret_cast<IdxSmem*>(
+      sA + a.stages * stage_bytes +
+      (F8 ? a.stages * kBlockRows * 4 : (MX ? a.mx_stages * kMxRawBytes + 1024 : 0)));
   const EpiLayout el = epi_layout(a.NQ, a.G, a.hist_part != nullptr);
   uint8_t* epi = reinterpret_cast<uint8_t*>(sm) + (sizeof(IdxSmem) + 15) / 16 * 16;
   float* qscale = reinterpret_cast<float*>(epi + el.qscale);
@@ -198,11 +299,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   const int64_t s1 = a.total_slots * (blockIdx.x + 1) / gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < a.stages; ++i) {
+    // MXFP4: full/sempty follow the raw stages (copy landed / decoded by
+    // the slot's MMA warp), empty the bf16 stages; else all three the stages
+    const int nfull = MX ? a.mx_stages : a.stages;
+    for (int i = 0; i < nfull; ++i) {
       mbar_init(smem_u32(&sm->full[i]), 1);
-      mbar_init(smem_u32(&sm->empty[i]), 1);
-      mbar_init(smem_u32(&sm->sempty[i]), 4);  // the four warps of the slot's epilogue group
+      // the four warps of the slot's epilogue group (FP8 scales), or the
+      // decoding MMA warp (MXFP4)
+      mbar_init(smem_u32(&sm->sempty[i]), MX ? 1 : 4);
     }
+    for (int i = 0; i < a.stages; ++i) mbar_init(smem_u32(&sm->empty[i]), 1);
     for (int i = 0; i < a.nacc; ++i) {
       mbar_init(smem_u32(&sm->tfull[i]), 1);
       mbar_init(smem_u32(&sm->tempty[i]), 128);  // the four warps of one epilogue group
@@ -210,13 +316,20 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     mbar_init(smem_u32(&sm->qfull), 1);
     mbar_init(smem_u32(&sm->qempty), 2);  // both MMA issuers leave the query block
     mbar_init(smem_u32(&sm->q8full), kEpiWarps);  // each epilogue warp quantised its rows
+  }
+  if (MX) {
+    // bf16 pair of each MXFP4 code byte at scale 1 (element 2i low nibble)
+    for (int i = threadIdx.x; i < 256; i += kIdxThreads)
+      mxlut[i] = pack_bf16x2(e2m1_value(i & 15), e2m1_value(i >> 4));
+  }
+  if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm->mma_done[0]), 1);
     mbar_init(smem_u32(&sm->mma_done[1]), 1);
     sm->abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_ik);
     tma_prefetch_desc(&tm_iq);
-    if (F8) tma_prefetch_desc(&tm_ks);
+    if (F8 || MX) tma_prefetch_desc(&tm_ks);
   }
   const int acc_cols = a.nacc * a.NQ;
   const uint32_t tmem_cols = acc_cols <= 32 ? 32 : (acc_cols <= 64 ? 64 : (acc_cols <= 128 ? 128 : (acc_cols <= 256 ? 256 : 512)));
@@ -242,6 +355,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       int64_t it = 0, qloads = 0, loaded = -1;
       bool keys_ready = false;  // the compressed keys of the previous kernel are visible
       const uint64_t once = l2_policy_evict_first();
+      const int nst = MX ? a.mx_stages : a.stages;  // the ring the copies fill
       for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
         if (!cur.live()) continue;
         if (cur.group != loaded) {
@@ -257,11 +371,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           loaded = cur.group;
         }
         // stage st was last filled `stages` uses ago, in phase ph ^ 1; with
-        // FP8 keys its scales are also read by the epilogue, which lags the MMAs
-        if (it >= a.stages &&
+        // FP8 keys its scales are also read by the epilogue, which lags the
+        // MMAs.  MXFP4: the raw stage is free once its slot's MMA warp has
+        // decoded it (the bf16 stages are that warp's own)
+        if (!MX && it >= a.stages &&
             !mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 11))
           break;
-        if (F8 && it >= a.stages &&
+        if ((F8 || MX) && it >= nst &&
             !mbar_wait(smem_u32(&sm->sempty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 20))
           break;
         if (!keys_ready &&
@@ -273,10 +389,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           keys_ready = true;
         }
         const uint32_t fb = smem_u32(&sm->full[st]);
-        mbar_arrive_expect_tx(fb, stage_bytes + (F8 ? kBlockRows * 4 : 0));
+        mbar_arrive_expect_tx(fb, MX ? kMxRawBytes : stage_bytes + (F8 ? kBlockRows * 4 : 0));
         // the keys are read once: first out of L2 (the scores written
         // meanwhile, and whatever the attention reads again, stay)
-        if (F8) {
+        if (MX) {
+          // 128 rows of 64 code bytes; their scales, 4 keys per 16-byte row
+          uint8_t* rs = sRaw + st * kMxRawBytes;
+          tma_load_3d_hint(smem_u32(rs), &tm_ik, 0, cur.blk * kBlockRows, cur.b, fb, once);
+          tma_load_3d_hint(smem_u32(rs + 8192), &tm_ks, 0, cur.blk * (kBlockRows / 4), cur.b, fb,
+                           once);
+        } else if (F8) {
           tma_load_3d_hint(smem_u32(sA + st * stage_bytes), &tm_ik, 0, cur.blk * kBlockRows,
                            cur.b, fb, once);
           tma_load_2d_hint(smem_u32(sScale + st * kBlockRows), &tm_ks, cur.blk * kBlockRows,
@@ -286,7 +408,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             tma_load_3d_hint(smem_u32(sA + st * stage_bytes + kc * 16384), &tm_ik, kc * 64,
                              cur.blk * kBlockRows, cur.b, fb, once);
         ++it;
-        if (++st == a.stages) { st = 0; ph ^= 1u; }
+        if (++st == nst) { st = 0; ph ^= 1u; }
       }
       if (*abort) {
         // let the copies already issued land before the CTA exits: the last
@@ -294,10 +416,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         // issued: the issuers had released it), then the key stages
         if (qloads > 0)
           mbar_wait(smem_u32(&sm->qfull), (qloads - 1) & 1, nullptr, nullptr, 10000000ull, 13);
-        const int64_t first = it > a.stages ? it - a.stages : 0;
+        const int64_t first = it > nst ? it - nst : 0;
         for (int64_t x = first; x < it; ++x)
-          mbar_wait(smem_u32(&sm->full[x % a.stages]), (x / a.stages) & 1, nullptr, nullptr,
-                    10000000ull, 12);
+          mbar_wait(smem_u32(&sm->full[x % nst]), (x / nst) & 1, nullptr, nullptr, 10000000ull,
+                    12);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -308,7 +430,78 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     // the tensor core ahead of it.  Slot `it` accumulates into accumulator
     // it % nacc, its (it / nacc)-th use.
     const int par = warp == 1 ? 0 : 1;
-    if (lane == 0) {
+    if (MX) {
+      // MXFP4 keys: the whole warp decodes its slot's raw stage into a bf16
+      // stage (lane l: key rows l, l + 32, l + 64, l + 96), then lane 0
+      // issues the bf16 products as for bf16 keys.  Both rings are even, so
+      // a raw stage and a bf16 stage each belong to one of the two warps.
+      const uint32_t idesc = idesc_bf16(128, a.NQ, 0, 0);
+      const uint32_t qbar = smem_u32(&sm->q8full);  // the queries after their MXFP4 round trip
+      SlotCursor cur;
+      int st = 0, rs = 0;
+      uint32_t ph = 0, rph = 0;
+      int64_t it = 0, qn = 0, loaded = -1;
+      bool ok = true;
+      for (cur.init(a, s0, s1); cur.slot < cur.end && ok && !*abort; cur.advance(a)) {
+        if (!cur.live()) continue;
+        if (cur.group != loaded) {
+          if (lane == 0 && qn > 0) mma_commit(smem_u32(&sm->qempty));
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(qbar, qn & 1, abort, a.status, kWaitLimitNs, 13));
+          if (!ok) break;
+          ++qn;
+          loaded = cur.group;
+        }
+        const int acc = static_cast<int>(it & acc_mask);
+        if (static_cast<int>(it & 1) == par) {
+          bool got = true;
+          // the accumulator's previous use has been drained by the epilogue
+          if (it >= a.nacc)
+            got = mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> acc_shift) + 1) & 1, abort,
+                            a.status, kWaitLimitNs, 14);
+          // the raw copy has landed
+          got = got && mbar_wait(smem_u32(&sm->full[rs]), rph, abort, a.status, kWaitLimitNs, 15);
+          // this warp's products of `stages` slots ago have read the bf16 stage
+          if (it >= a.stages)
+            got = got &&
+                  mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 56);
+          ok = __all_sync(0xffffffffu, got);
+          if (!ok) break;
+          const uint8_t* raw = sRaw + rs * kMxRawBytes;
+          uint8_t* Ast = sA + st * stage_bytes;
+          for (int r = lane; r < kBlockRows; r += 32) mx_decode_row(raw, mxlut, Ast, r);
+          fence_proxy_async_smem();  // the decoded rows are read by the tensor core
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&sm->sempty[rs]));  // the raw stage may be refilled
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + acc * a.NQ;
+            for (int kc = 0; kc < a.KC; ++kc) {
+              const uint32_t a_addr = smem_u32(Ast + kc * 16384);
+              const uint32_t b_addr = smem_u32(sQ + kc * a.NQ * 128);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ad = smem_desc(a_addr + ks * 32, 16, 1024, kSwizzle128B);
+                const uint64_t bd = smem_desc(b_addr + ks * 32, 16, 1024, kSwizzle128B);
+                mma_bf16_ss(d_tmem, ad, bd, idesc, (kc | ks) != 0);
+              }
+            }
+            mma_commit(smem_u32(&sm->empty[st]));
+            mma_commit(smem_u32(&sm->tfull[acc]));
+          }
+          __syncwarp();
+        }
+        ++it;
+        if (++st == a.stages) { st = 0; ph ^= 1u; }
+        if (++rs == a.mx_stages) { rs = 0; rph ^= 1u; }
+      }
+      // all issued MMAs complete before the accumulators are released
+      if (lane == 0) {
+        mma_commit(smem_u32(&sm->mma_done[par]));
+        mbar_wait(smem_u32(&sm->mma_done[par]), 0, nullptr, a.status, kWaitLimitNs, 16);
+      }
+      __syncwarp();
+    } else if (lane == 0) {
       const uint32_t idesc = F8 ? idesc_e4m3(128, a.NQ) : idesc_bf16(128, a.NQ, 0, 0);
       // the operand rows the products read: E4M3 codes, or the bf16 rows
       const uint64_t qbar = smem_u32(F8 ? &sm->q8full : &sm->qfull);
@@ -400,13 +593,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
       if (!cur.live()) continue;
       if (cur.group != wgroup) {
-        if (F8) {
+        if (F8 || MX) {
           // the group's bf16 query rows have landed: quantise this warp's
           // share, publish it to the MMA issuers, then wait for the others'
-          // row scales
+          // row scales (MXFP4: the rows' round trip, in place)
           bool got = mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 18);
           if (!__all_sync(0xffffffffu, got)) break;
-          quantize_query_rows(sQ, sQ8, qscale, a.NQ, ew, lane);
+          if (MX) mx_query_rows(sQ, a.NQ, ew, lane);
+          else quantize_query_rows(sQ, sQ8, qscale, a.NQ, ew, lane);
           fence_proxy_async_smem();  // visible to the tensor core's reads
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm->q8full));
@@ -546,9 +740,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
 }  // namespace
 
-bool plan_indexer(int T, int HI, int dI, bool f8, bool fold, IndexerPlan* p) {
+bool plan_indexer(int T, int HI, int dI, int kf, bool fold, IndexerPlan* p) {
   if (HI <= 0 || HI > 256 || dI <= 0 || dI > 128) return false;
-  if (f8 && dI != 128) return false;
+  const bool f8 = kf == kKeyE4m3, mx = kf == kKeyMx4;
+  if ((f8 || mx) && dI != 128) return false;
   int G = 256 / HI;
   if (G > T) G = T;
   if (G < 1) G = 1;
@@ -562,9 +757,13 @@ bool plan_indexer(int T, int HI, int dI, bool f8, bool fold, IndexerPlan* p) {
   const size_t stage_bytes = f8 ? 16384 + kBlockRows * 4 : (size_t)p->KC * 16384;
   if (fold && G != 1) return false;  // the folded pass counts one query per group
   const size_t fixed = (sizeof(IdxSmem) + 15) / 16 * 16 + epi_layout(NQ, G, fold).bytes;
-  const size_t budget = 227 * 1024 - 1024 - fixed - q_bytes;
+  // MXFP4: the raw stages the copies fill (the HBM stream in flight) and the
+  // decode table come first; the bf16 stages the products read get the rest
+  const int mx_stages = mx ? kMaxMxStages : 0;
+  const size_t mx_bytes = mx ? (size_t)mx_stages * kMxRawBytes + 1024 : 0;
+  const size_t budget = 227 * 1024 - 1024 - fixed - q_bytes - mx_bytes;
   int stages = static_cast<int>(budget / stage_bytes);
-  const int cap = f8 ? kMaxStages : kMaxStagesBf16;
+  const int cap = f8 ? kMaxStages : (mx ? 4 : kMaxStagesBf16);
   if (stages > cap) stages = cap;
   // An even ring: slot s uses stage s % stages and is issued by MMA warp
   // s % 2, so every stage (like every accumulator) belongs to one issuer and
@@ -575,19 +774,22 @@ bool plan_indexer(int T, int HI, int dI, bool f8, bool fold, IndexerPlan* p) {
   stages &= ~1;
   if (stages < 2) return false;
   p->stages = stages;
+  p->mx_stages = mx_stages;
   // as many accumulators as tensor memory holds, up to kMaxAcc (a power of 2)
   int nacc = 2;
   while (nacc * 2 <= kMaxAcc && nacc * 2 * NQ <= 512) nacc *= 2;
   p->nacc = nacc;
   p->tmem_cols = nacc * NQ;
-  p->smem_bytes = 1024 + q_bytes + stages * stage_bytes + fixed;
+  p->smem_bytes = 1024 + q_bytes + stages * stage_bytes + mx_bytes + fixed;
   return true;
 }
 
 cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm_iq,
                                  const CUtensorMap& tm_ks, const IndexerArgs& a,
-                                 const IndexerPlan& p, bool f8, int grid, cudaStream_t stream) {
-  auto kernel = f8 ? indexer_score_kernel<true> : indexer_score_kernel<false>;
+                                 const IndexerPlan& p, int kf, int grid, cudaStream_t stream) {
+  auto kernel = kf == kKeyE4m3 ? indexer_score_kernel<kKeyE4m3>
+                               : (kf == kKeyMx4 ? indexer_score_kernel<kKeyMx4>
+                                                : indexer_score_kernel<kKeyBf16>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(p.smem_bytes));
   if (e != cudaSuccess) return e;

@@ -51,6 +51,7 @@ struct IndexerArgs {
   int NQ;                // MMA N
   int KC;                // 64-wide K chunks of the bf16 operands
   int stages;
+  int mx_stages;         // MXFP4 keys: raw stages (else 0)
   int nacc;              // tensor-memory accumulators in flight (2, 4 or 8)
   int groups_per_seq;    // ceil(T / G)
   int nblk;              // ceil(N_cap / 128)
@@ -66,16 +67,20 @@ struct IndexerArgs {
   uint16_t* hist_part;
 };
 struct IndexerPlan {
-  int G, NQ, KC, stages, nacc, tmem_cols;
+  int G, NQ, KC, stages, mx_stages, nacc, tmem_cols;
   size_t smem_bytes;
 };
-// f8: E4M3 keys (dI = 128, one 128-byte row each) and queries quantised in
-// the kernel; else bf16 keys and queries.
-bool plan_indexer(int T, int HI, int dI, bool f8, bool fold, IndexerPlan* p);
-// tm_ks: the FP8 keys' row scales [B][N_cap] fp32, boxes of 128 (FP8 only).
+// Key formats: bf16 keys and queries; E4M3 keys (dI = 128, one 128-byte row
+// each) with the queries quantised in the kernel; MXFP4 keys (dI = 128: 64
+// code bytes and 4 E8M0 scale bytes each) decoded to bf16 in shared memory,
+// with the queries taken through the same round trip in the kernel.
+enum IndexerKeys { kIdxKeysBf16 = 0, kIdxKeysE4m3 = 1, kIdxKeysMx4 = 2 };
+bool plan_indexer(int T, int HI, int dI, int keys, bool fold, IndexerPlan* p);
+// tm_ks: the FP8 keys' row scales [B][N_cap] fp32, boxes of 128 (FP8); the
+// MXFP4 keys' scales as [B][N_cap / 4][16] bytes, boxes {16, 32} (MXFP4).
 cudaError_t launch_indexer_score(const CUtensorMap& tm_ik, const CUtensorMap& tm_iq,
                                  const CUtensorMap& tm_ks, const IndexerArgs& a,
-                                 const IndexerPlan& p, bool f8, int grid, cudaStream_t stream);
+                                 const IndexerPlan& p, int keys, int grid, cudaStream_t stream);
 
 // ------------------------------------------------------------ entries from hidden states
 struct HiddenArgs {

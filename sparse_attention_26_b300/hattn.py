@@ -49,6 +49,11 @@ _SIGS = {
                                    _vp, _vp]),
     "hattn_indexer_scores_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
                                         _i32, _i32, _i64, _vp, _i32, _vp]),
+    "hattn_indexer_scores_mxfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
+                                          _i32, _i32, _i64, _vp, _i32, _vp]),
+    "hattn_indexer_topk_mxfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
+                                        _i32, _i32, _i32, _i64, _vp, _vp, _vp, _sz, _i32, _vp,
+                                        _vp]),
     "hattn_indexer_topk": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i32, _i32,
                                   _vp, _vp, _vp, _sz, _vp]),
     "hattn_indexer_topk_workspace_bytes": (_sz, [_i32, _i32, _i64, _i32, _i32]),
@@ -531,6 +536,66 @@ def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, fresh_from
         _check(lib().hattn_indexer_scores(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
                                           N_cap, m, _ptr(score_out), _stream(stream)))
     return score_out
+
+
+def _mx_keys(ik4, ik4_scale, B, N_cap):
+    _need(ik4, "ik4", torch.uint8, 3)
+    _shape(ik4, "ik4", (B, N_cap, 64))
+    _need(ik4_scale, "ik4_scale", torch.uint8, 3)
+    _shape(ik4_scale, "ik4_scale", (B, N_cap, 4))
+
+
+def indexer_scores_mxfp4(iq, w, ik4, ik4_scale, pos, *, m=4, score_out=None, n_sms=0,
+                         fresh_from=-1, dependent=False, stream=None):
+    """indexer_scores over MXFP4 keys (codes ik4 uint8 [B, N_cap, 64] and E8M0
+    scales ik4_scale uint8 [B, N_cap, 4], as quantize_mxfp4 writes them); the
+    bf16 queries take the same round trip in the kernel."""
+    B, T, HI, dI = iq.shape
+    N_cap = ik4.shape[1]
+    _need(iq, "iq", torch.bfloat16, 4)
+    _need(w, "w", torch.float32, 3)
+    _shape(w, "w", (B, T, HI))
+    _need(pos, "pos", torch.int32, 2)
+    _shape(pos, "pos", (B, T))
+    _mx_keys(ik4, ik4_scale, B, N_cap)
+    if score_out is None:
+        score_out = torch.empty((B, T, N_cap), dtype=torch.float32, device=iq.device)
+    _need(score_out, "score_out", torch.float32, 3)
+    _shape(score_out, "score_out", (B, T, N_cap))
+    _check(lib().hattn_indexer_scores_mxfp4(_ptr(iq), _ptr(w), _ptr(ik4), _ptr(ik4_scale),
+                                            _ptr(pos), B, T, HI, dI, N_cap, m, n_sms, fresh_from,
+                                            _ptr(score_out), _flags(dependent), _stream(stream)))
+    return score_out
+
+
+def indexer_topk_mxfp4(iq, w, ik4, ik4_scale, pos, *, k, m=4, idx_out=None, score_out=None,
+                       workspace=None, n_sms=0, fresh_from=-1, dependent=False, split_event=None,
+                       split_external=False, stream=None):
+    """indexer_topk over MXFP4 keys (see indexer_scores_mxfp4)."""
+    B, T, HI, dI = iq.shape
+    N_cap = ik4.shape[1]
+    _need(iq, "iq", torch.bfloat16, 4)
+    _need(w, "w", torch.float32, 3)
+    _shape(w, "w", (B, T, HI))
+    _need(pos, "pos", torch.int32, 2)
+    _shape(pos, "pos", (B, T))
+    _mx_keys(ik4, ik4_scale, B, N_cap)
+    idx_out = _idx_out(idx_out, B, T, k, iq.device)
+    if score_out is not None:
+        _need(score_out, "score_out", torch.float32, 3)
+        _shape(score_out, "score_out", (B, T, N_cap))
+    need = indexer_topk_workspace_bytes(B, T, N_cap, k, score_out is not None)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=iq.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().hattn_indexer_topk_mxfp4(_ptr(iq), _ptr(w), _ptr(ik4), _ptr(ik4_scale),
+                                          _ptr(pos), B, T, HI, dI, N_cap, k, m, n_sms,
+                                          fresh_from, _ptr(idx_out), _ptr(score_out),
+                                          _ptr(workspace), ws_bytes,
+                                          _flags(dependent) | (EVENT_EXTERNAL if split_external
+                                                               else 0),
+                                          _event(split_event), _stream(stream)))
+    return idx_out
 
 
 def indexer_scores_fp8(iq, w, ik8, ik_scale, pos, *, m=4, score_out=None, n_sms=0,

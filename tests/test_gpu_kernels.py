@@ -255,6 +255,80 @@ def test_quantize_mxfp4_bit_exact(rows, n):
     assert e_codes.shape == (0, n // 2) and e_scales.shape == (0, n // 32)
 
 
+# ------------------------------------------------------------------ MXFP4 indexer keys
+def _mx(x):
+    """MXFP4 codes [.., 64] and scales [.., 4] of bf16 rows [.., 128] (the
+    library's quantiser, bit-exact against the oracle's)."""
+    lead = x.shape[:-1]
+    c, s = hattn.quantize_mxfp4(x.reshape(-1, 128).to(DEV))
+    return c.reshape(*lead, 64), s.reshape(*lead, 4)
+
+
+@pytest.mark.parametrize("B,T,N_cap,k,pos", [
+    (3, 1, 600, 16, [2, 599 * 4 + 3, 4 * 300 + 1]),          # nothing visible, full, ragged
+    (2, 5, 1300, 64, [[4 * 1000 + t for t in range(5)], [4 * 77 + 3 * t for t in range(5)]]),
+])
+def test_indexer_mxfp4(B, T, N_cap, k, pos):
+    """Scores over MXFP4 keys, per entry, against the oracle's definition over
+    the decoded keys and the decoded query round trip; top-k by the 1e-3
+    rule.  T = 5 runs groups of 4 queries (256 columns, a ragged group)."""
+    HI, dI = 64, 128
+    iq = randn_bf16((B, T, HI, dI), 140)
+    w = randn_f32((B, T, HI), 141)
+    ik = randn_bf16((B, N_cap, dI), 142)
+    ik4, iks = _mx(ik)
+    pos_t = torch.tensor(pos, dtype=torch.int32).reshape(B, T)
+    scores = torch.full((B, T, N_cap), float("nan"), device=DEV)
+    hattn.indexer_scores_mxfp4(iq.to(DEV), w.to(DEV), ik4, iks, pos_t.to(DEV), score_out=scores)
+    idx = hattn.indexer_topk_mxfp4(iq.to(DEV), w.to(DEV), ik4, iks, pos_t.to(DEV), k=k)
+    hattn.check_status()
+    ref = orc.indexer_scores_mxfp4(bits(iq), w.numpy(), _u8(ik4), _u8(iks), pos_t.numpy(), 4)
+    vis = ~np.isnan(ref)
+    got = f64(scores)
+    assert np.isfinite(got[vis]).all()
+    err = np.abs(got[vis] - ref[vis])
+    tol = 2e-3 * (np.abs(ref[vis]) + np.sqrt(HI * dI) * 0.05)
+    assert (err <= tol).all(), f"score error {err.max():.3e}"
+    check_topk(idx.cpu().numpy(), ref, pos_t.numpy(), 4, k)
+
+
+@pytest.mark.parametrize("N_cap,k", [(40000, 1024), (3000, 512)])
+def test_indexer_mxfp4_lossless_exact(N_cap, k):
+    """Rows on the E2M1 grid with a 4 in every block lose nothing to MXFP4
+    (block scale 1), and their products sum exactly in fp32: scores equal
+    the oracle's bit for bit and the selected sets (ties to the smaller
+    index) are identical.  40,000 entries take the cluster selection with
+    the folded first pass."""
+    B, T, HI, dI = 2, 1, 64, 128
+    g = torch.Generator().manual_seed(143)
+    grid = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+    def rows(*shape):
+        v = grid[torch.randint(0, 8, shape + (dI,), generator=g)]
+        v = v * (torch.randint(0, 2, v.shape, generator=g) * 2 - 1)
+        v.view(-1, dI // 32, 32)[:, :, 0] = 6.0   # each block's amax in [4, 8): scale 1
+        return v.to(torch.bfloat16)
+
+    iq, ik = rows(B, T, HI), rows(B, N_cap)
+    w = torch.ones((B, T, HI)) * 0.5
+    ik4, iks = _mx(ik)
+    assert (_u8(iks) == 127).all()
+    pos = torch.tensor([[4 * N_cap - 1], [4 * (N_cap // 2) + 1]], dtype=torch.int32)
+    scores = torch.zeros((B, T, N_cap), device=DEV)
+    idx = hattn.indexer_topk_mxfp4(iq.to(DEV), w.to(DEV), ik4, iks, pos.to(DEV), k=k,
+                                   score_out=scores)
+    hattn.check_status()
+    ref = orc.indexer_scores_mxfp4(bits(iq), w.numpy(), _u8(ik4), _u8(iks), pos.numpy(), 4)
+    vis = ~np.isnan(ref)
+    np.testing.assert_array_equal(f64(scores)[vis], ref[vis])
+    ref_idx = orc.topk(ref, pos.numpy(), 4, k)
+    got = idx.cpu().numpy()
+    for b in range(B):
+        assert sorted(got[b, 0][got[b, 0] >= 0].tolist()) == sorted(
+            ref_idx[b, 0][ref_idx[b, 0] >= 0].tolist())
+        assert (got[b, 0] == -1).sum() == (ref_idx[b, 0] == -1).sum()
+
+
 @pytest.mark.parametrize("B,L,D,dI,r,j0,j1", [
     (2, 1024, 512, 128, 64, 255, 256),   # one new entry per sequence: the small kernel
     (2, 4096, 512, 128, 64, 0, 1024),    # cache build: the grid-stride kernel

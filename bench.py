@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--workload", default="hybrid_decode_1m")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling only)")
     ap.add_argument("--context", type=int, default=0, help="override L (profiling only)")
-    ap.add_argument("--indexer-keys", default="bf16", choices=["bf16", "fp8"],
+    ap.add_argument("--indexer-keys", default="bf16", choices=["bf16", "fp8", "mxfp4"],
                     help="indexer key cache: bf16, or E4M3 codes with a row scale")
     ap.add_argument("--stack", type=int, default=0,
                     help="time the decode step of N attention layers in the pages' pattern "
@@ -104,7 +104,7 @@ def step_bytes(wl, keys="bf16"):
     n_csa, n_hca = L // wl.m_csa, L // wl.m_hca
     per = 0
     if "csa" in wl.branches:
-        key = dI * 2 if keys == "bf16" else dI + 4
+        key = key_bytes(dI, keys)
         per += n_csa * key + T * (min(wl.k, n_csa) * D * 2 + wl.HI * dI * 2 + wl.HI * 4)
         per += wl.w_csa * (D + dI + 1) * 2 + D * 2 + key
     if "hca" in wl.branches:
@@ -115,6 +115,16 @@ def step_bytes(wl, keys="bf16"):
     return B * per
 
 
+def key_bytes(dI, keys):
+    """HBM bytes of one indexer key: bf16 values, E4M3 codes and an fp32 row
+    scale, or MXFP4 codes (two per byte) and an E8M0 scale per 32."""
+    if keys == "bf16":
+        return dI * 2
+    if keys == "fp8":
+        return dI + 4
+    return dI // 2 + dI // 32
+
+
 def indexer_bytes(wl, keys="bf16"):
     """Algorithmic bytes of one indexer launch: every visible indexer key
     read once per sequence (its queries share the scan) -- dI bf16 values,
@@ -122,7 +132,7 @@ def indexer_bytes(wl, keys="bf16"):
     The fp32 scores the launch writes are implementation overhead (the
     selection's intermediate), counted apart by indexer_overhead_bytes."""
     n_csa = wl.L // wl.m_csa
-    key = wl.dI * 2 if keys == "bf16" else wl.dI + 4
+    key = key_bytes(wl.dI, keys)
     return wl.B * (n_csa * key + wl.T * (wl.HI * wl.dI * 2 + wl.HI * 4))
 
 
@@ -249,12 +259,13 @@ def indexer_traffic(wl, keys="bf16"):
             h.update(fh.read())
     if h.hexdigest() != INDEXER_TRAFFIC["sha256"]:
         return None
-    if wl.T != 1:
-        return None  # the capture is of one query per sequence
+    if wl.T != 1 or keys not in INDEXER_TRAFFIC["bytes_per_entry"]:
+        return None  # the capture is of one query per sequence, per key format
     return INDEXER_TRAFFIC["bytes_per_entry"][keys] * wl.B * (wl.L // wl.m_csa)
 
 
-INDEXER_KEYS = {"bf16": "bf16", "fp8": "e4m3 codes + fp32 row scale (queries quantised alike)"}
+INDEXER_KEYS = {"bf16": "bf16", "fp8": "e4m3 codes + fp32 row scale (queries quantised alike)",
+                "mxfp4": "mxfp4: e2m1 codes + e8m0 scale per 32 (queries quantised alike)"}
 
 
 class ClockSampler:
@@ -691,7 +702,8 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if keys == "bf16" else "bf16 (indexer QK: e4m3)", "data": "synthetic",
+        "dtype": {"bf16": "bf16", "fp8": "bf16 (indexer QK: e4m3)",
+                  "mxfp4": "bf16 (indexer QK: mxfp4)"}[keys], "data": "synthetic",
         "config": config_dict(wl, keys,
                               parallelism=f"replicas x{world}" if world > 1 else "1 GPU",
                               step_roofline=step_roof, indexer_keys=INDEXER_KEYS[keys],

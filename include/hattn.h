@@ -227,6 +227,14 @@ HATTN_API int hattn_quantize_e4m3(const void* x, int64_t rows, int n, void* code
 HATTN_API int hattn_quantize_mxfp4(const void* x, int64_t rows, int n, void* codes, void* scales,
                                    hattn_stream_t stream);
 
+/* hattn_quantize_mxfp4 over the entries [j_begin, j_end) of every sequence
+ * of a cache x [B][N_cap][n] bf16, into codes [B][N_cap][n/2] and scales
+ * [B][N_cap][n/32] (other entries untouched): keeps an MXFP4 key cache in
+ * step with the entries a decode step compresses. */
+HATTN_API int hattn_quantize_mxfp4_entries(const void* x, int B, int64_t N_cap, int n,
+                                           int64_t j_begin, int64_t j_end, void* codes,
+                                           void* scales, hattn_stream_t stream);
+
 /* Indexer scores over MXFP4 keys ([AT] "Inference efficiency": the indexer's
  * QK path in FP4): ik4 [B][N_cap][64] code bytes and ik4_scale [B][N_cap][4]
  * E8M0 bytes as hattn_quantize_mxfp4 writes them (dI must be 128; N_cap a

@@ -758,6 +758,26 @@ int hattn_quantize_mxfp4(const void* x, int64_t rows, int n, void* codes, void* 
   return ok();
 }
 
+int hattn_quantize_mxfp4_entries(const void* x, int B, int64_t N_cap, int n, int64_t j_begin,
+                                 int64_t j_end, void* codes, void* scales, hattn_stream_t stream) {
+  REQUIRE(B >= 1 && N_cap >= 1, "B and N_cap must be >= 1");
+  REQUIRE(n >= 32 && n % 32 == 0 && n <= (1 << 20), "n=%d must be a multiple of 32 in [32, 2^20]",
+          n);
+  REQUIRE(j_begin >= 0 && j_end >= j_begin && j_end <= N_cap,
+          "entry range [%lld, %lld) outside [0, N_cap=%lld)", (long long)j_begin,
+          (long long)j_end, (long long)N_cap);
+  if (j_end == j_begin) return ok();
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(codes);
+  REQUIRE_PTR(scales);
+  cudaError_t e = launch_quantize_mxfp4(
+      static_cast<const __nv_bfloat16*>(x), (int64_t)B * (j_end - j_begin), n,
+      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), num_sms_or_default(),
+      static_cast<cudaStream_t>(stream), j_end - j_begin, j_begin, N_cap);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return ok();
+}
+
 int hattn_hca_compress(const void* kv_raw, const void* gate, const float* gamma_kv, int B,
                        int64_t L_cap, int D, int m, int r, float rope_base, float eps,
                        int64_t j_begin, int64_t j_end, void* kv_h, int64_t N_cap,

@@ -103,48 +103,60 @@ __device__ __forceinline__ int64_t visible_entries(int32_t t, int m, int64_t cap
   return n < cap ? n : cap;
 }
 
-// Walks this CTA's slots in order.  Every role runs the same cursor, so all
-// of them skip the same blocks; the 64-bit divisions happen only when the
-// query group changes, never per slot.
+// Walks this CTA's live slots in order.  Every role runs the same cursor, so
+// all of them visit the same blocks: the blocks of a group that hold an entry
+// some query of the group sees (the later blocks of the group are dead).  A
+// step is one 32-bit compare; the 64-bit divisions and the visibility reads
+// happen only when the query group changes, which `fresh` flags.
 struct SlotCursor {
-  int64_t slot, end;
   int64_t group;   // b * groups_per_seq + query group within the sequence
+  int64_t last;    // the last group the CTA's slots reach
   int blk;         // 128-entry block within the sequence
+  int blk_end;     // one past the group's last live block within the CTA's slots
+  int last_end;    // one past the CTA's last block within group `last`
   int b, t0, gv;
-  int64_t nmax;    // largest visible-entry count among the group's queries
+  bool fresh;      // first live slot of its group
+  bool done;
 
   __device__ __forceinline__ void load_group(const IndexerArgs& a) {
     b = static_cast<int>(group / a.groups_per_seq);
     t0 = static_cast<int>(group - static_cast<int64_t>(b) * a.groups_per_seq) * a.G;
     gv = min(a.G, a.T - t0);
-    nmax = 0;
+    int64_t nmax = 0;  // largest visible-entry count among the group's queries
     for (int g = 0; g < gv; ++g) {
       const int64_t v = visible_entries(a.pos[(int64_t)b * a.T + t0 + g], a.m, a.N_cap);
       nmax = v > nmax ? v : nmax;
     }
+    const int cap = group == last ? last_end : a.nblk;
+    const int64_t live = (nmax + kBlockRows - 1) / kBlockRows;
+    blk_end = live < cap ? static_cast<int>(live) : cap;
+    fresh = true;
+  }
+  // the first live block of a later group, or done
+  __device__ __forceinline__ void next_group(const IndexerArgs& a) {
+    do {
+      if (group >= last) {
+        done = true;
+        return;
+      }
+      ++group;
+      blk = 0;
+      load_group(a);
+    } while (blk_end <= 0);
   }
   __device__ __forceinline__ void init(const IndexerArgs& a, int64_t s0, int64_t s1) {
-    slot = s0;
-    end = s1;
+    done = s0 >= s1;
+    if (done) return;
     group = s0 / a.nblk;
     blk = static_cast<int>(s0 - group * a.nblk);
-    if (slot < end) load_group(a);
+    last = (s1 - 1) / a.nblk;
+    last_end = static_cast<int>(s1 - last * a.nblk);
+    load_group(a);
+    if (blk >= blk_end) next_group(a);
   }
-  __device__ __forceinline__ bool live() const {
-    return static_cast<int64_t>(blk) * kBlockRows < nmax;
-  }
-  // next slot; a dead block ends its group (the later blocks are dead too)
   __device__ __forceinline__ void advance(const IndexerArgs& a) {
-    if (!live()) {
-      slot += a.nblk - 1 - blk;
-      blk = a.nblk - 1;
-    }
-    ++slot;
-    if (++blk == a.nblk) {
-      blk = 0;
-      ++group;
-      if (slot < end) load_group(a);
-    }
+    fresh = false;
+    if (++blk >= blk_end) next_group(a);
   }
 };
 
@@ -352,13 +364,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       SlotCursor cur;
       int st = 0;
       uint32_t ph = 0;
-      int64_t it = 0, qloads = 0, loaded = -1;
+      int64_t it = 0, qloads = 0;
       bool keys_ready = false;  // the compressed keys of the previous kernel are visible
       const uint64_t once = l2_policy_evict_first();
       const int nst = MX ? a.mx_stages : a.stages;  // the ring the copies fill
-      for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
-        if (!cur.live()) continue;
-        if (cur.group != loaded) {
+      for (cur.init(a, s0, s1); !cur.done && !*abort; cur.advance(a)) {
+        if (cur.fresh) {
           if (qloads > 0 &&
               !mbar_wait(smem_u32(&sm->qempty), (qloads - 1) & 1, abort, a.status, kWaitLimitNs, 10))
             break;
@@ -368,7 +379,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           for (int kc = 0; kc < a.KC; ++kc)
             tma_load_2d(smem_u32(sQ + kc * a.NQ * 128), &tm_iq, kc * 64, row0, qb);
           ++qloads;
-          loaded = cur.group;
         }
         // stage st was last filled `stages` uses ago, in phase ph ^ 1; with
         // FP8 keys its scales are also read by the epilogue, which lags the
@@ -440,17 +450,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       SlotCursor cur;
       int st = 0, rs = 0;
       uint32_t ph = 0, rph = 0;
-      int64_t it = 0, qn = 0, loaded = -1;
+      int64_t it = 0, qn = 0;
       bool ok = true;
-      for (cur.init(a, s0, s1); cur.slot < cur.end && ok && !*abort; cur.advance(a)) {
-        if (!cur.live()) continue;
-        if (cur.group != loaded) {
+      for (cur.init(a, s0, s1); !cur.done && ok && !*abort; cur.advance(a)) {
+        if (cur.fresh) {
           if (lane == 0 && qn > 0) mma_commit(smem_u32(&sm->qempty));
           ok = __all_sync(0xffffffffu,
                           mbar_wait(qbar, qn & 1, abort, a.status, kWaitLimitNs, 13));
           if (!ok) break;
           ++qn;
-          loaded = cur.group;
         }
         const int acc = static_cast<int>(it & acc_mask);
         if (static_cast<int>(it & 1) == par) {
@@ -508,15 +516,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       SlotCursor cur;
       int st = 0;
       uint32_t ph = 0;
-      int64_t it = 0, qn = 0, loaded = -1;
-      for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
-        if (!cur.live()) continue;
-        if (cur.group != loaded) {
+      int64_t it = 0, qn = 0;
+      for (cur.init(a, s0, s1); !cur.done && !*abort; cur.advance(a)) {
+        if (cur.fresh) {
           if (qn > 0) mma_commit(smem_u32(&sm->qempty));  // previous group's reads of sQ done
           if (!mbar_wait(static_cast<uint32_t>(qbar), qn & 1, abort, a.status, kWaitLimitNs, 13))
             break;
           ++qn;
-          loaded = cur.group;
         }
         const int acc = static_cast<int>(it & acc_mask);
         if (static_cast<int>(it & 1) == par) {
@@ -587,12 +593,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     const bool whole = (a.HI & 31) == 0;
     const int cpq = a.HI >> 5;
     SlotCursor cur;
-    int64_t it = 0, wgroup = -1, qn = 0;
+    int64_t it = 0, qn = 0;
     int st = 0;  // the slot's key stage (FP8: its scales are read from there)
     uint32_t ph = 0;
-    for (cur.init(a, s0, s1); cur.slot < cur.end && !*abort; cur.advance(a)) {
-      if (!cur.live()) continue;
-      if (cur.group != wgroup) {
+    float* sbase = nullptr;  // the group's first score row, at this thread's entry of block 0
+    int hoff = 0;            // the group's histogram (first or second row of the CTA)
+    static_assert((kEpiGroups & (kEpiGroups - 1)) == 0, "epilogue groups: a power of two");
+    for (cur.init(a, s0, s1); !cur.done && !*abort; cur.advance(a)) {
+      if (cur.fresh) {
+        sbase = a.scores + ((int64_t)cur.b * a.T + cur.t0) * a.N_cap + row;
+        hoff = cur.group == row0 ? 0 : kHistWords;
         if (F8 || MX) {
           // the group's bf16 query rows have landed: quantise this warp's
           // share, publish it to the MMA issuers, then wait for the others'
@@ -619,17 +629,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                                     a.pos[(int64_t)cur.b * a.T + cur.t0 + g], a.m, a.N_cap))
                               : 0;
         __syncwarp();
-        wgroup = cur.group;
       }
       const int sst = st;
       const uint32_t sph = ph;
       if (++st == a.stages) { st = 0; ph ^= 1u; }
-      if (static_cast<int>(it % kEpiGroups) != eg) {
+      if (static_cast<int>(it & (kEpiGroups - 1)) != eg) {
         ++it;
         continue;  // the other epilogue group's slot
       }
       const int acc = static_cast<int>(it & acc_mask);
-      const int64_t j = static_cast<int64_t>(cur.blk) * kBlockRows + row;
+      const int j = cur.blk * kBlockRows + row;
       const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), (it >> acc_shift) & 1, abort,
                                  a.status, kWaitLimitNs, 17);
       if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: tcgen05.ld follows
@@ -645,7 +654,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&sm->sempty[sst]));
       }
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * a.NQ;
-      float* srow = a.scores + ((int64_t)cur.b * a.T + cur.t0) * a.N_cap + j;
+      float* srow = sbase + cur.blk * kBlockRows;
       if (whole) {
         for (int g = 0; g < cur.gv; ++g) {
           // four independent partial sums (one per column of a float4), as
@@ -684,7 +693,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             st_global_hint(srow + (int64_t)g * a.N_cap, sc, keep);
             if (fold) {
               const uint32_t bin = score_key(sc) >> 21;
-              atomicAdd(&hist[(cur.group == row0 ? 0 : kHistWords) + (bin >> 1)],
+              atomicAdd(&hist[hoff + (bin >> 1)],
                         1u << ((bin & 1u) * 16u));
             }
           }
@@ -705,7 +714,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                 st_global_hint(srow + (int64_t)g * a.N_cap, sc, keep);
                 if (fold) {
                   const uint32_t bin = score_key(sc) >> 21;
-                  atomicAdd(&hist[(cur.group == row0 ? 0 : kHistWords) + (bin >> 1)],
+                  atomicAdd(&hist[hoff + (bin >> 1)],
                             1u << ((bin & 1u) * 16u));
                 }
               }

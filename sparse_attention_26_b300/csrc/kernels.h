@@ -129,7 +129,8 @@ cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, int64_t rows, int n, ui
 // rows x n bf16 -> E2M1 codes [rows][n/2] (element 2i in the low nibble of
 // byte i) and E8M0 block scales [rows][n/32]; n % 32 == 0.
 cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
-                                  uint8_t* scales, int num_sms, cudaStream_t stream);
+                                  uint8_t* scales, int num_sms, cudaStream_t stream, int64_t nj = 0,
+                                  int64_t j0 = 0, int64_t ncap = 0);
 
 // ------------------------------------------------------------ top-k select
 struct TopkArgs {

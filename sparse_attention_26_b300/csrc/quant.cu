@@ -79,10 +79,14 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
 
 // kN > 0: rows of exactly kN elements (row offsets become immediates); kN = 0:
 // any n, a multiple of 32.
+// Row r of the call is row (r / nj) * ncap + j0 + r % nj of x, codes and
+// scales (the identity for nj = ncap = rows, j0 = 0; an entry range
+// [j0, j0 + nj) of every sequence of a [B][ncap][n] cache otherwise).
 template <int kN>
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_mxfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int n_arg,
-                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int64_t nj,
+                          int64_t j0, int64_t ncap) {
   const int n = kN > 0 ? kN : n_arg;
   const int lane = threadIdx.x & 31;
   const int64_t warp = static_cast<int64_t>(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
@@ -91,9 +95,12 @@ __global__ void __launch_bounds__(kQuantThreads)
     // rows of this group that exist (warp-uniform); row k sits k * n
     // elements past the group's first
     const int nk = rows - row0 < kMxRows ? static_cast<int>(rows - row0) : kMxRows;
-    const __nv_bfloat16* xg = x + row0 * n;
-    uint8_t* cg = codes + row0 * (n / 2);
-    uint8_t* sg = scales + row0 * (n / 32);
+    int64_t rk[kMxRows];  // the rows' places in the cache
+#pragma unroll
+    for (int k = 0; k < kMxRows; ++k) {
+      const int64_t r = row0 + k;
+      rk[k] = (r / nj) * ncap + j0 + r % nj;
+    }
     for (int base = 0; base < n; base += 128) {
       const int i = base + lane * 4;
       const bool in = i < n;
@@ -101,7 +108,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 #pragma unroll
       for (int k = 0; k < kMxRows; ++k) {
         u[k] = make_uint2(0u, 0u);
-        if (in && k < nk) u[k] = *reinterpret_cast<const uint2*>(xg + k * n + i);
+        if (in && k < nk) u[k] = *reinterpret_cast<const uint2*>(x + rk[k] * n + i);
       }
 #pragma unroll
       for (int k = 0; k < kMxRows; ++k) {
@@ -118,8 +125,8 @@ __global__ void __launch_bounds__(kQuantThreads)
                        (e2m1x2(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv)) << 8);
           const uint32_t mag = w & 0x7777u;
           w = mag | (w & ((mag + 0x7777u) & 0x8888u));  // drop the sign of zero nibbles
-          *reinterpret_cast<uint16_t*>(cg + k * (n / 2) + i / 2) = static_cast<uint16_t>(w);
-          if ((lane & 7) == 0) sg[k * (n / 32) + i / 32] = static_cast<uint8_t>(se + 127);
+          *reinterpret_cast<uint16_t*>(codes + rk[k] * (n / 2) + i / 2) = static_cast<uint16_t>(w);
+          if ((lane & 7) == 0) scales[rk[k] * (n / 32) + i / 32] = static_cast<uint8_t>(se + 127);
         }
       }
     }
@@ -165,7 +172,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 }  // namespace
 
 cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* x, int64_t rows, int n, uint8_t* codes,
-                                  uint8_t* scales, int num_sms, cudaStream_t stream) {
+                                  uint8_t* scales, int num_sms, cudaStream_t stream, int64_t nj,
+                                  int64_t j0, int64_t ncap) {
   if (rows <= 0) return cudaSuccess;
   // one wave of resident CTAs, each striding over groups of rows
   auto kernel = n == 128 ? quantize_mxfp4_kernel<128> : quantize_mxfp4_kernel<0>;
@@ -176,7 +184,12 @@ cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* x, int64_t rows, int n, u
   const int64_t want = (rows + per_cta - 1) / per_cta;
   const int64_t cap = static_cast<int64_t>(num_sms) * (resident > 0 ? resident : 1);
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  kernel<<<grid, kQuantThreads, 0, stream>>>(x, rows, n, codes, scales);
+  if (nj <= 0) {  // plain rows
+    nj = rows;
+    j0 = 0;
+    ncap = rows;
+  }
+  kernel<<<grid, kQuantThreads, 0, stream>>>(x, rows, n, codes, scales, nj, j0, ncap);
   return cudaGetLastError();
 }
 

@@ -49,6 +49,7 @@ _SIGS = {
                                    _vp, _vp]),
     "hattn_indexer_scores_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
                                         _i32, _i32, _i64, _vp, _i32, _vp]),
+    "hattn_quantize_mxfp4_entries": (_i32, [_vp, _i32, _i64, _i32, _i64, _i64, _vp, _vp, _vp]),
     "hattn_indexer_scores_mxfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
                                           _i32, _i32, _i64, _vp, _i32, _vp]),
     "hattn_indexer_topk_mxfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64,
@@ -536,6 +537,20 @@ def indexer_scores(iq, w, ik_c, pos, *, m=4, score_out=None, n_sms=0, fresh_from
         _check(lib().hattn_indexer_scores(_ptr(iq), _ptr(w), _ptr(ik_c), _ptr(pos), B, T, HI, dI,
                                           N_cap, m, _ptr(score_out), _stream(stream)))
     return score_out
+
+
+def quantize_mxfp4_entries(x, codes, scales, *, j_begin, j_end, stream=None):
+    """quantize_mxfp4 of the entries [j_begin, j_end) of every sequence of a
+    cache x [B, N_cap, n] bf16 into codes [B, N_cap, n/2] and scales
+    [B, N_cap, n/32] (uint8)."""
+    _need(x, "x", torch.bfloat16, 3)
+    B, N_cap, n = x.shape
+    _need(codes, "codes", torch.uint8, 3)
+    _shape(codes, "codes", (B, N_cap, n // 2))
+    _need(scales, "scales", torch.uint8, 3)
+    _shape(scales, "scales", (B, N_cap, n // 32))
+    _check(lib().hattn_quantize_mxfp4_entries(_ptr(x), B, N_cap, n, j_begin, j_end, _ptr(codes),
+                                              _ptr(scales), _stream(stream)))
 
 
 def _mx_keys(ik4, ik4_scale, B, N_cap):

@@ -29,15 +29,19 @@ from . import hattn
 
 class HybridLayer:
     def __init__(self, wl, raw: dict, device="cuda", build_caches=True, indexer_keys="bf16"):
-        """indexer_keys: "bf16", or "fp8" to keep the indexer keys as E4M3
-        codes with a row scale (ik8, ik_scale) and score them on the FP8
-        tensor-core path."""
-        if indexer_keys not in ("bf16", "fp8"):
-            raise ValueError(f"indexer_keys must be 'bf16' or 'fp8', got {indexer_keys!r}")
+        """indexer_keys: "bf16"; "fp8" to keep the indexer keys as E4M3 codes
+        with a row scale (ik8, ik_scale) and score them on the FP8
+        tensor-core path; or "mxfp4" to keep them as MXFP4 codes and block
+        scales (ik4, ik4_scale, quantised from the bf16 keys as each entry is
+        compressed) and score them from those."""
+        if indexer_keys not in ("bf16", "fp8", "mxfp4"):
+            raise ValueError(f"indexer_keys must be 'bf16', 'fp8' or 'mxfp4', "
+                             f"got {indexer_keys!r}")
         self.wl = wl
         self.dev = device
         self.raw = raw  # kv_raw, ik_raw, gate_csa, gate_hca on device
         self.fp8 = indexer_keys == "fp8"
+        self.mx4 = indexer_keys == "mxfp4"
         B, L, D = raw["kv_raw"].shape
         self.B, self.L, self.D = B, L, D
         self.N_csa = L // wl.m_csa
@@ -51,6 +55,9 @@ class HybridLayer:
         if self.fp8:
             self.ik8 = torch.zeros((B, n_c, wl.dI), dtype=torch.uint8, device=device)
             self.ik_scale = torch.zeros((B, n_c), dtype=torch.float32, device=device)
+        if self.mx4:
+            self.ik4 = torch.zeros((B, n_c, wl.dI // 2), dtype=torch.uint8, device=device)
+            self.ik4_scale = torch.zeros((B, n_c, wl.dI // 32), dtype=torch.uint8, device=device)
         self.kv_h = torch.zeros((B, n_h, D), dtype=bf, device=device)
         self.override_dense_sms = 0  # > 0: HCA + SWA attention on that many SMs beside the indexer
         # fused step with a side stream: the indexer, top-k, attention and
@@ -203,6 +210,9 @@ class HybridLayer:
         else:
             hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j0,
                                j_end=j1, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c, ik_c=self.ik_c)
+            if self.mx4:
+                hattn.quantize_mxfp4_entries(self.ik_c, self.ik4, self.ik4_scale, j_begin=j0,
+                                             j_end=j1)
 
     def _indexer_topk(self, iq, w, pos, b, events=None, n_sms=0, fresh_from=-1, dependent=False):
         """Indexer scores and top-k as one call (the score kernel counts the
@@ -223,12 +233,19 @@ class HybridLayer:
                 self._split_event = torch.cuda.Event()
                 self._split_event.record(cur)  # creates its CUDA event
             split = self._split_event
-        keys = self.ik8 if self.fp8 else self.ik_c
-        hattn.indexer_topk(iq, w, keys, pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"],
-                           score_out=b["scores"], workspace=b["ws_topk"],
-                           ik_scale=self.ik_scale if self.fp8 else None, n_sms=n_sms,
-                           fresh_from=fresh_from, dependent=dependent, split_event=split,
-                           split_external=timed)
+        if self.mx4:
+            hattn.indexer_topk_mxfp4(iq, w, self.ik4, self.ik4_scale, pos, k=wl.k, m=wl.m_csa,
+                                     idx_out=b["idx"], score_out=b["scores"],
+                                     workspace=b["ws_topk"], n_sms=n_sms, fresh_from=fresh_from,
+                                     dependent=dependent, split_event=split,
+                                     split_external=timed)
+        else:
+            keys = self.ik8 if self.fp8 else self.ik_c
+            hattn.indexer_topk(iq, w, keys, pos, k=wl.k, m=wl.m_csa, idx_out=b["idx"],
+                               score_out=b["scores"], workspace=b["ws_topk"],
+                               ik_scale=self.ik_scale if self.fp8 else None, n_sms=n_sms,
+                               fresh_from=fresh_from, dependent=dependent, split_event=split,
+                               split_external=timed)
         if timed:
             events["topk"][1].record(cur)
         return split

@@ -329,6 +329,24 @@ def test_indexer_mxfp4_lossless_exact(N_cap, k):
         assert (got[b, 0] == -1).sum() == (ref_idx[b, 0] == -1).sum()
 
 
+@pytest.mark.parametrize("B,N_cap,j0,j1", [(3, 700, 0, 700), (2, 1000, 37, 613), (2, 64, 5, 5)])
+def test_quantize_mxfp4_entries(B, N_cap, j0, j1):
+    """Entries [j0, j1) of every sequence of a cache, bit-exact against the
+    oracle's quantiser; the codes and scales outside the range keep their
+    bytes (an empty range writes nothing)."""
+    x = (randn_bf16((B, N_cap, 128), 150).float() * 3.0).to(torch.bfloat16)
+    codes = torch.full((B, N_cap, 64), 0xA5, dtype=torch.uint8, device=DEV)
+    scales = torch.full((B, N_cap, 4), 0x5A, dtype=torch.uint8, device=DEV)
+    hattn.quantize_mxfp4_entries(x.to(DEV), codes, scales, j_begin=j0, j_end=j1)
+    hattn.check_status()
+    rc, rs = orc.quantize_mxfp4(bits(x[:, j0:j1].reshape(-1, 128)))
+    c, s = _u8(codes), _u8(scales)
+    np.testing.assert_array_equal(c[:, j0:j1].reshape(-1, 64), rc)
+    np.testing.assert_array_equal(s[:, j0:j1].reshape(-1, 4), rs)
+    assert (c[:, :j0] == 0xA5).all() and (c[:, j1:] == 0xA5).all()
+    assert (s[:, :j0] == 0x5A).all() and (s[:, j1:] == 0x5A).all()
+
+
 @pytest.mark.parametrize("B,L,D,dI,r,j0,j1", [
     (2, 1024, 512, 128, 64, 255, 256),   # one new entry per sequence: the small kernel
     (2, 4096, 512, 128, 64, 0, 1024),    # cache build: the grid-stride kernel

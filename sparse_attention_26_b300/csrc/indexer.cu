@@ -38,14 +38,14 @@ namespace {
 // warps: 0 producer, 1 and 2 MMA issuers (even / odd slots), then
 // kEpiGroups x 4 epilogue warps (any 4 consecutive warps cover the four
 // 32-lane quarters of tensor memory)
-constexpr int kEpiGroups = 2;
+constexpr int kEpiGroups = 3;
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kFirstEpiWarp = 3;
 constexpr int kIdxThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kBlockRows = 128;
 constexpr int kMaxStages = 12;
 constexpr int kMaxStagesBf16 = 8;
-constexpr int kMaxAcc = 4;  // accumulators in flight (TMEM columns permitting)
+constexpr int kMaxAcc = 8;  // accumulators in flight (TMEM columns permitting)
 // key formats of the score kernel
 constexpr int kKeyBf16 = kIdxKeysBf16, kKeyE4m3 = kIdxKeysE4m3, kKeyMx4 = kIdxKeysMx4;
 // MXFP4 keys (dI = 128): a block of 128 keys is 128 x 64 code bytes, then
@@ -345,7 +345,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   }
   const int acc_cols = a.nacc * a.NQ;
   const uint32_t tmem_cols = acc_cols <= 32 ? 32 : (acc_cols <= 64 ? 64 : (acc_cols <= 128 ? 128 : (acc_cols <= 256 ? 256 : 512)));
-  const int acc_mask = a.nacc - 1, acc_shift = a.nacc == 2 ? 1 : (a.nacc == 4 ? 2 : 3);
+  // Slot it accumulates into accumulator it % nacc, its (it / nacc)-th use;
+  // every role tracks (acc, parity of the use) as a counter pair.  With six
+  // accumulators three epilogue groups drain them (slot it to group it % 3,
+  // so each accumulator belongs to one group), else two.
+  const int egroups = a.nacc % 3 == 0 ? 3 : 2;
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm->tmem_base), tmem_cols);
     tmem_relinquish();
@@ -448,8 +452,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const uint32_t idesc = idesc_bf16(128, a.NQ, 0, 0);
       const uint32_t qbar = smem_u32(&sm->q8full);  // the queries after their MXFP4 round trip
       SlotCursor cur;
-      int st = 0, rs = 0;
-      uint32_t ph = 0, rph = 0;
+      int st = 0, rs = 0, acc = 0;
+      uint32_t ph = 0, rph = 0, aph = 0;
       int64_t it = 0, qn = 0;
       bool ok = true;
       for (cur.init(a, s0, s1); !cur.done && ok && !*abort; cur.advance(a)) {
@@ -460,13 +464,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           if (!ok) break;
           ++qn;
         }
-        const int acc = static_cast<int>(it & acc_mask);
         if (static_cast<int>(it & 1) == par) {
           bool got = true;
           // the accumulator's previous use has been drained by the epilogue
           if (it >= a.nacc)
-            got = mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> acc_shift) + 1) & 1, abort,
-                            a.status, kWaitLimitNs, 14);
+            got = mbar_wait(smem_u32(&sm->tempty[acc]), aph ^ 1u, abort, a.status, kWaitLimitNs,
+                            14);
           // the raw copy has landed
           got = got && mbar_wait(smem_u32(&sm->full[rs]), rph, abort, a.status, kWaitLimitNs, 15);
           // this warp's products of `stages` slots ago have read the bf16 stage
@@ -500,6 +503,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           __syncwarp();
         }
         ++it;
+        if (++acc == a.nacc) { acc = 0; aph ^= 1u; }
         if (++st == a.stages) { st = 0; ph ^= 1u; }
         if (++rs == a.mx_stages) { rs = 0; rph ^= 1u; }
       }
@@ -514,8 +518,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       // the operand rows the products read: E4M3 codes, or the bf16 rows
       const uint64_t qbar = smem_u32(F8 ? &sm->q8full : &sm->qfull);
       SlotCursor cur;
-      int st = 0;
-      uint32_t ph = 0;
+      int st = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
       int64_t it = 0, qn = 0;
       for (cur.init(a, s0, s1); !cur.done && !*abort; cur.advance(a)) {
         if (cur.fresh) {
@@ -524,12 +528,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             break;
           ++qn;
         }
-        const int acc = static_cast<int>(it & acc_mask);
         if (static_cast<int>(it & 1) == par) {
           // the accumulator's previous use has been drained by the epilogue
           if (it >= a.nacc &&
-              !mbar_wait(smem_u32(&sm->tempty[acc]), ((it >> acc_shift) + 1) & 1, abort,
-                         a.status, kWaitLimitNs, 14))
+              !mbar_wait(smem_u32(&sm->tempty[acc]), aph ^ 1u, abort, a.status, kWaitLimitNs, 14))
             break;
           if (!mbar_wait(smem_u32(&sm->full[st]), ph, abort, a.status, kWaitLimitNs, 15)) break;
           tc_fence_after();
@@ -560,6 +562,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           mma_commit(smem_u32(&sm->tfull[acc]));
         }
         ++it;
+        if (++acc == a.nacc) { acc = 0; aph ^= 1u; }
         if (++st == a.stages) { st = 0; ph ^= 1u; }
       }
       // all issued MMAs complete before the accumulators are released
@@ -575,6 +578,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     float* wcol = reinterpret_cast<float*>(epi + el.wcol) + ew * a.NQ;
+    const uint32_t wcol_s = smem_u32(wcol);
     int* ntv = reinterpret_cast<int*>(epi + el.nt) + ew * a.G;
     // Folded first selection pass (one query per group): the top 11 bits of
     // each visible score's key are counted per row, for the first and the
@@ -598,49 +602,81 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     uint32_t ph = 0;
     float* sbase = nullptr;  // the group's first score row, at this thread's entry of block 0
     int hoff = 0;            // the group's histogram (first or second row of the CTA)
-    static_assert((kEpiGroups & (kEpiGroups - 1)) == 0, "epilogue groups: a power of two");
-    for (cur.init(a, s0, s1); !cur.done && !*abort; cur.advance(a)) {
-      if (cur.fresh) {
-        sbase = a.scores + ((int64_t)cur.b * a.T + cur.t0) * a.N_cap + row;
-        hoff = cur.group == row0 ? 0 : kHistWords;
-        if (F8 || MX) {
-          // the group's bf16 query rows have landed: quantise this warp's
-          // share, publish it to the MMA issuers, then wait for the others'
-          // row scales (MXFP4: the rows' round trip, in place)
-          bool got = mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 18);
-          if (!__all_sync(0xffffffffu, got)) break;
-          if (MX) mx_query_rows(sQ, a.NQ, ew, lane);
-          else quantize_query_rows(sQ, sQ8, qscale, a.NQ, ew, lane);
-          fence_proxy_async_smem();  // visible to the tensor core's reads
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sm->q8full));
-          got = mbar_wait(smem_u32(&sm->q8full), qn & 1, abort, a.status, kWaitLimitNs, 19);
-          if (!__all_sync(0xffffffffu, got)) break;
-          ++qn;
-        }
+    int rot = 0;             // it % egroups: the epilogue group of slot it
+    int acc = 0;             // it % nacc
+    uint32_t aph = 0;        // parity of (it / nacc)
+    // A new query group: its weights and visible counts, and (FP8, MXFP4)
+    // this warp's share of the query rows' quantisation.  Every epilogue warp
+    // enters every group, in order.  False when a wait gave up.
+    auto enter_group = [&]() -> bool {
+      sbase = a.scores + ((int64_t)cur.b * a.T + cur.t0) * a.N_cap + row;
+      hoff = cur.group == row0 ? 0 : kHistWords;
+      if (F8 || MX) {
+        // the group's bf16 query rows have landed: quantise this warp's
+        // share, publish it to the MMA issuers, then wait for the others'
+        // row scales (MXFP4: the rows' round trip, in place)
+        bool got = mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 18);
+        if (!__all_sync(0xffffffffu, got)) return false;
+        if (MX) mx_query_rows(sQ, a.NQ, ew, lane);
+        else quantize_query_rows(sQ, sQ8, qscale, a.NQ, ew, lane);
+        fence_proxy_async_smem();  // visible to the tensor core's reads
         __syncwarp();
-        for (int c = lane; c < a.NQ; c += 32) {
-          const int g = c / a.HI, h = c % a.HI;
-          const float wv = (g < cur.gv) ? a.w[((int64_t)cur.b * a.T + cur.t0 + g) * a.HI + h] : 0.f;
-          wcol[c] = F8 ? wv * qscale[c] : wv;
-        }
-        for (int g = lane; g < a.G; g += 32)
-          ntv[g] = g < cur.gv ? static_cast<int>(visible_entries(
-                                    a.pos[(int64_t)cur.b * a.T + cur.t0 + g], a.m, a.N_cap))
-                              : 0;
-        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->q8full));
+        got = mbar_wait(smem_u32(&sm->q8full), qn & 1, abort, a.status, kWaitLimitNs, 19);
+        if (!__all_sync(0xffffffffu, got)) return false;
+        ++qn;
       }
+      __syncwarp();
+      for (int c = lane; c < a.NQ; c += 32) {
+        const int g = c / a.HI, h = c % a.HI;
+        const float wv = (g < cur.gv) ? a.w[((int64_t)cur.b * a.T + cur.t0 + g) * a.HI + h] : 0.f;
+        wcol[c] = F8 ? wv * qscale[c] : wv;
+      }
+      for (int g = lane; g < a.G; g += 32)
+        ntv[g] = g < cur.gv ? static_cast<int>(visible_entries(
+                                  a.pos[(int64_t)cur.b * a.T + cur.t0 + g], a.m, a.N_cap))
+                            : 0;
+      __syncwarp();
+      return true;
+    };
+    // on to the next live slot (entering its group); false at the end
+    auto step = [&]() -> bool {
+      cur.advance(a);
+      ++it;
+      if (++rot == egroups) rot = 0;
+      if (++acc == a.nacc) { acc = 0; aph ^= 1u; }
+      if (++st == a.stages) { st = 0; ph ^= 1u; }
+      return !cur.done && (!cur.fresh || enter_group());
+    };
+    // this group's next slot, egroups slots on: plain arithmetic while they
+    // stay in the current query group (the common case), else slot by slot
+    // (every warp enters every group)
+    const bool leap = a.stages >= egroups;  // a leap wraps each ring at most once
+    auto next_own = [&]() -> bool {
+      if (leap && cur.blk + egroups < cur.blk_end) {
+        cur.blk += egroups;
+        it += egroups;
+        acc += egroups;
+        if (acc >= a.nacc) { acc -= a.nacc; aph ^= 1u; }
+        st += egroups;
+        if (st >= a.stages) { st -= a.stages; ph ^= 1u; }
+        return true;
+      }
+      bool m = true;
+      for (int k = 0; k < egroups && m; ++k) m = step();
+      return m;
+    };
+    cur.init(a, s0, s1);
+    bool more = !cur.done && enter_group();  // a first slot always opens its group
+    while (more && rot != eg) more = step();
+    // one pass per slot of this group: the slots of the other groups are
+    // stepped over between passes
+    while (more) {
       const int sst = st;
       const uint32_t sph = ph;
-      if (++st == a.stages) { st = 0; ph ^= 1u; }
-      if (static_cast<int>(it & (kEpiGroups - 1)) != eg) {
-        ++it;
-        continue;  // the other epilogue group's slot
-      }
-      const int acc = static_cast<int>(it & acc_mask);
       const int j = cur.blk * kBlockRows + row;
-      const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), (it >> acc_shift) & 1, abort,
-                                 a.status, kWaitLimitNs, 17);
+      const bool got =
+          mbar_wait(smem_u32(&sm->tfull[acc]), aph, abort, a.status, kWaitLimitNs, 17);
       if (!__all_sync(0xffffffffu, got)) break;  // warp-uniform: tcgen05.ld follows
       tc_fence_after();
       float ks = 1.f;
@@ -657,37 +693,37 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       float* srow = sbase + cur.blk * kBlockRows;
       if (whole) {
         for (int g = 0; g < cur.gv; ++g) {
-          // four independent partial sums (one per column of a float4), as
-          // two packed pairs, so the FMAs do not wait on one another
-          float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+          // four independent partial sums (one per column of a float4), so
+          // the FMAs do not wait on one another; scalar FMAs, which take the
+          // maxima from any register (a packed FMA wants them as a pair)
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
           for (int c = 0; c < cpq; c += 2) {
             const int col = (g * cpq + c) * 32;
             float x0[32], x1[32];
             tmem_ld32(taddr + col, x0);
             if (c + 1 < cpq) tmem_ld32(taddr + col + 32, x1);
             tmem_wait_ld();
-            const float4* w0 = reinterpret_cast<const float4*>(wcol + col);
+            const uint32_t w0 = wcol_s + col * 4;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float4 wv = w0[i];
-              s01 = ffma2(make_float2(wv.x, wv.y),
-                          make_float2(fmaxf(x0[4 * i], 0.f), fmaxf(x0[4 * i + 1], 0.f)), s01);
-              s23 = ffma2(make_float2(wv.z, wv.w),
-                          make_float2(fmaxf(x0[4 * i + 2], 0.f), fmaxf(x0[4 * i + 3], 0.f)), s23);
+              const float4 wv = lds_f4(w0 + 16 * i);
+              p0 = fmaf(wv.x, fmaxf(x0[4 * i], 0.f), p0);
+              p1 = fmaf(wv.y, fmaxf(x0[4 * i + 1], 0.f), p1);
+              p2 = fmaf(wv.z, fmaxf(x0[4 * i + 2], 0.f), p2);
+              p3 = fmaf(wv.w, fmaxf(x0[4 * i + 3], 0.f), p3);
             }
             if (c + 1 < cpq) {
-              const float4* w1 = reinterpret_cast<const float4*>(wcol + col + 32);
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                const float4 wv = w1[i];
-                s01 = ffma2(make_float2(wv.x, wv.y),
-                            make_float2(fmaxf(x1[4 * i], 0.f), fmaxf(x1[4 * i + 1], 0.f)), s01);
-                s23 = ffma2(make_float2(wv.z, wv.w),
-                            make_float2(fmaxf(x1[4 * i + 2], 0.f), fmaxf(x1[4 * i + 3], 0.f)), s23);
+                const float4 wv = lds_f4(w0 + 128 + 16 * i);
+                p0 = fmaf(wv.x, fmaxf(x1[4 * i], 0.f), p0);
+                p1 = fmaf(wv.y, fmaxf(x1[4 * i + 1], 0.f), p1);
+                p2 = fmaf(wv.z, fmaxf(x1[4 * i + 2], 0.f), p2);
+                p3 = fmaf(wv.w, fmaxf(x1[4 * i + 3], 0.f), p3);
               }
             }
           }
-          const float sum = (s01.x + s01.y) + (s23.x + s23.y);
+          const float sum = (p0 + p1) + (p2 + p3);
           if (j < ntv[g]) {
             const float sc = F8 ? sum * ks : sum;
             st_global_hint(srow + (int64_t)g * a.N_cap, sc, keep);
@@ -727,7 +763,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&sm->tempty[acc]));
-      ++it;
+      more = next_own();
     }
     if (fold) {
       // this CTA's partial histograms, part[cta][0] for its first row and
@@ -774,19 +810,28 @@ bool plan_indexer(int T, int HI, int dI, int kf, bool fold, IndexerPlan* p) {
   int stages = static_cast<int>(budget / stage_bytes);
   const int cap = f8 ? kMaxStages : (mx ? 4 : kMaxStagesBf16);
   if (stages > cap) stages = cap;
-  // An even ring: slot s uses stage s % stages and is issued by MMA warp
-  // s % 2, so every stage (like every accumulator) belongs to one issuer and
-  // one epilogue group, and each waits on a barrier's phases in order.  With
-  // an odd ring a stage alternates between the issuers, and an issuer that
-  // runs a lap ahead of the other would wait on the parity of a phase whose
-  // predecessor is still pending -- a parity wait that passes at once.
-  stages &= ~1;
-  if (stages < 2) return false;
-  p->stages = stages;
-  p->mx_stages = mx_stages;
-  // as many accumulators as tensor memory holds, up to kMaxAcc (a power of 2)
+  // Accumulators: six when tensor memory holds them (three epilogue groups
+  // drain them, slot s to group s % 3), else as many as it holds up to
+  // kMaxAcc, a power of 2 (two epilogue groups).
   int nacc = 2;
   while (nacc * 2 <= kMaxAcc && nacc * 2 * NQ <= 512) nacc *= 2;
+  if (6 * NQ <= 512) nacc = 6;
+  const int egroups = nacc % 3 == 0 ? 3 : 2;
+  // Slot s uses stage s % stages and accumulator s % nacc, is issued by MMA
+  // warp s % 2 and drained by epilogue group s % egroups.  A ring whose
+  // length is a multiple of the roles sharing it gives each stage (each
+  // accumulator) to one issuer and one group, so each waits on a barrier's
+  // phases in order.  Otherwise a stage alternates between, say, the
+  // issuers, and an issuer that runs a lap ahead of the other would wait on
+  // the parity of a phase whose predecessor is still pending -- a parity
+  // wait that passes at once.  The stages of bf16 keys (and the bf16 stages
+  // of MXFP4 keys) are the issuers' alone; the epilogue reads the FP8 key
+  // scales from its slot's stage.
+  const int ring = f8 ? 2 * egroups : 2;
+  stages -= stages % ring;
+  if (stages < ring) return false;
+  p->stages = stages;
+  p->mx_stages = mx_stages;
   p->nacc = nacc;
   p->tmem_cols = nacc * NQ;
   p->smem_bytes = 1024 + q_bytes + stages * stage_bytes + mx_bytes + fixed;

@@ -11,11 +11,16 @@ scales that travel with each stage (sempty releases them).
 
 An mbarrier parity wait passes when the barrier's current phase has the other
 parity, so a waiter must never get a full phase ahead of the barrier.  The
-kernel keeps the ring even so that a stage, like an accumulator, always
-belongs to one issuer and one epilogue group.  This test runs the protocol
-(as the kernel runs it) under thousands of random interleavings: with even
-rings no schedule deadlocks or reads a stale stage, accumulator or query
-block; with an odd ring and two epilogue groups some schedule does.
+kernel sizes each ring as a multiple of the roles that share it, so that a
+stage, like an accumulator, always belongs to one issuer and one epilogue
+group: two groups with an even number of accumulators, three groups with
+six; FP8 stages a multiple of 2 x groups (the epilogue reads their scales).
+With two groups, a third group's warps still enter every query group (they
+quantise their share of the query rows) but drain nothing.  This test runs
+the protocol (as the kernel runs it) under thousands of random
+interleavings: with such rings no schedule deadlocks or reads a stale stage,
+accumulator or query block; with an odd ring, or accumulators shared between
+groups, some schedule does.
 """
 import random
 
@@ -47,9 +52,10 @@ class Barrier:
             self.pending = self.count
 
 
-def simulate(slots, stages, nacc, groups, f8, seed):
+def simulate(slots, stages, nacc, groups, f8, seed, idle=0):
     """One random schedule of one CTA over `slots` ((query group, block)
-    pairs).  Returns (finished, errors)."""
+    pairs); `groups` epilogue groups drain, `idle` more only enter the query
+    groups.  Returns (finished, errors)."""
     rnd = random.Random(seed)
     bars = {}
 
@@ -65,7 +71,7 @@ def simulate(slots, stages, nacc, groups, f8, seed):
         bar(f"tempty{i}", 4)
     bar("qfull", 1)
     bar("qempty", 2)
-    bar("q8full", 4 * groups)
+    bar("q8full", 4 * (groups + idle))
     bar("done0", 1)
     bar("done1", 1)
     copies = []
@@ -138,7 +144,7 @@ def simulate(slots, stages, nacc, groups, f8, seed):
             st += 1
             if st == stages:
                 st, ph = 0, ph ^ 1
-            if it % groups != g:
+            if g >= groups or it % groups != g:
                 it += 1
                 continue
             acc = it % nacc
@@ -154,7 +160,7 @@ def simulate(slots, stages, nacc, groups, f8, seed):
             it += 1
 
     roles = {"producer": producer(), "mma0": issuer(0), "mma1": issuer(1)}
-    for g in range(groups):
+    for g in range(groups + idle):
         for w in range(4):
             roles[f"epilogue{g}.{w}"] = epilogue(g, w)
     waiting = dict.fromkeys(roles)
@@ -240,6 +246,38 @@ def test_an_odd_ring_with_two_epilogue_groups_fails():
     for seed in range(400):
         try:
             ok, errors = simulate(_slots(seed), 5, 4, 2, False, seed)
+        except AssertionError:
+            ok, errors = False, ["barrier accounting broken"]
+        failures += (not ok) or bool(errors)
+    assert failures > 0
+
+
+def test_three_epilogue_groups_with_six_accumulators():
+    """Six accumulators (slot s to accumulator s % 6 and group s % 3); FP8
+    stage rings a multiple of six, bf16 rings even (the epilogue does not
+    read those stages)."""
+    for f8, rings in ((True, (6, 12)), (False, (2, 4, 8))):
+        for stages in rings:
+            for seed in range(100):
+                ok, errors = simulate(_slots(seed), stages, 6, 3, f8, seed)
+                assert ok and not errors, (f8, stages, seed, errors[:2])
+
+
+def test_two_draining_groups_and_an_idle_one():
+    for stages in (4, 12):
+        for seed in range(100):
+            ok, errors = simulate(_slots(seed), stages, 4, 2, seed % 2 == 1, seed, idle=1)
+            assert ok and not errors, (stages, seed, errors[:2])
+
+
+def test_accumulators_shared_between_three_groups_fail():
+    """Four accumulators and three groups: accumulator s % 4 passes from
+    group to group, and a group that runs ahead waits on the parity of a use
+    whose predecessor is still pending."""
+    failures = 0
+    for seed in range(400):
+        try:
+            ok, errors = simulate(_slots(seed), 4, 4, 3, False, seed)
         except AssertionError:
             ok, errors = False, ["barrier accounting broken"]
         failures += (not ok) or bool(errors)

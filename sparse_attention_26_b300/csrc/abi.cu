@@ -830,13 +830,14 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   if (!device_info(nullptr, &status, &sms)) return fail(HATTN_ERR_CUDA, "no CUDA device");
   CUtensorMap tm_ik, tm_iq, tm_ks;
   if (mx) {
-    // a key block: 128 rows of 64 code bytes; its scales as 32 rows of 16
-    // bytes (4 keys each)
+    // a key block: 128 rows of 64 code bytes, 64-byte swizzled (the layout
+    // the block-scaled products read); its scales as 32 rows of 16 bytes
+    // (4 keys each)
     const uint64_t dims[3] = {64, (uint64_t)N_cap, (uint64_t)B};
     const uint64_t strides[2] = {64, (uint64_t)N_cap * 64};
     const uint32_t box[3] = {64, 128, 1};
     int rc = make_tmap(&tm_ik, ik_c, 3, dims, strides, box, "ik4", CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+                       CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc) return rc;
     const uint64_t sdims[3] = {16, (uint64_t)N_cap / 4, (uint64_t)B};
     const uint64_t sstrides[2] = {16, (uint64_t)N_cap * 4};
@@ -886,7 +887,6 @@ int indexer_scores_impl(const void* iq, const float* w, const void* ik_c, const 
   a.NQ = ip.NQ;
   a.KC = ip.KC;
   a.stages = ip.stages;
-  a.mx_stages = ip.mx_stages;
   a.nacc = ip.nacc;
   a.groups_per_seq = (T + ip.G - 1) / ip.G;
   a.nblk = static_cast<int>((N_cap + 127) / 128);

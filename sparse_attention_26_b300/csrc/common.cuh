@@ -419,6 +419,34 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::mxf4 with block scales: A (M=128
+// rows) and B (N rows) hold K = 64 packed E2M1 elements per row (two per
+// byte, the even element in the low nibble) and each 32-element block of a
+// row has a UE8M0 scale 2^(e - 127) in tensor memory (sfa, sfb; the scale
+// vector of two blocks per row starts at the byte the descriptor's scale
+// IDs name).  The products are exact; D accumulates in fp32.
+__device__ __forceinline__ void mma_mxf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies 32 rows of 16 bytes from shared memory (s_desc: no swizzle, rows
+// 16 bytes apart) into 4 tensor-memory columns starting at taddr, for lanes
+// 0..31 of each of the four 32-lane quarters: lane r, column c + j gets
+// bytes 4j .. 4j+3 of row r.  Ordered with the issuing thread's later
+// tcgen05.mma; tcgen05.commit covers its read of shared memory.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc)
+               : "memory");
+}
+
 // Arrive (once) on an mbarrier when all previously issued tcgen05 async
 // operations of this thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -489,6 +517,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
   return d;
 }
 constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle64B = 4;
+constexpr uint32_t kSwizzleNone = 0;
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: 1 if the operand is MN-major in shared memory (else K-major).
@@ -509,6 +539,22 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_m
          | (static_cast<uint32_t>(b_mn) << 16)       // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor, kind::mxf4 (block-scaled): A and B E2M1 (format
+// 1), K-major, UE8M0 scales (bit 23), N / 8 in bits 17-22, M / 128 in bits
+// 27-28, and the byte of the scales' 32-bit tensor-memory word where this
+// product's two-block scale vector starts, for B (bits 4-5) and A (bits
+// 29-30): 0 for K elements 0..63 of a 128-element row, 2 for 64..127.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, uint32_t sfa_id,
+                                                  uint32_t sfb_id) {
+  return ((sfb_id & 3u) << 4)                        // B scale vector: byte
+         | (1u << 7)                                 // A format: E2M1
+         | (1u << 10)                                // B format: E2M1
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale format: UE8M0
+         | (static_cast<uint32_t>(M >> 7) << 27)     // M / 128
+         | ((sfa_id & 3u) << 29);                    // A scale vector: byte
 }
 
 // Instruction descriptor, kind::f8f6f4 with E4M3 A/B (format code 0), fp32

@@ -50,8 +50,7 @@ constexpr int kMaxAcc = 8;  // accumulators in flight (TMEM columns permitting)
 constexpr int kKeyBf16 = kIdxKeysBf16, kKeyE4m3 = kIdxKeysE4m3, kKeyMx4 = kIdxKeysMx4;
 // MXFP4 keys (dI = 128): a block of 128 keys is 128 x 64 code bytes, then
 // its 128 x 4 E8M0 scale bytes
-constexpr uint32_t kMxRawBytes = 128 * 64 + 128 * 4;
-constexpr int kMaxMxStages = 8;
+constexpr uint32_t kMxStageBytes = 128 * 64 + 128 * 4;
 constexpr int kHistWords = kSelBins / 2;  // a row's 16-bit bins, two per word
 
 struct IdxSmem {
@@ -77,6 +76,15 @@ struct IdxSmem {
 struct EpiLayout {
   uint32_t wcol, qscale, nt, hist, bytes;
 };
+// The bytes before the bf16 query rows: E4M3 query rows (FP8 keys), or the
+// E2M1 query rows and their 512-byte scale atom (MXFP4 keys), a multiple of
+// 1024 so the bf16 rows keep their 128-byte swizzle atoms aligned.
+__host__ __device__ __forceinline__ uint32_t indexer_q8_bytes(int kf, int NQ) {
+  if (kf == kIdxKeysE4m3) return static_cast<uint32_t>(NQ) * 128u;
+  if (kf == kIdxKeysMx4) return (static_cast<uint32_t>(NQ) * 64u + 512u + 1023u) / 1024u * 1024u;
+  return 0u;
+}
+
 __host__ __device__ __forceinline__ EpiLayout epi_layout(int NQ, int G, bool hist) {
   EpiLayout l;
   uint32_t o = 0;
@@ -161,61 +169,22 @@ struct SlotCursor {
 };
 
 // ------------------------------------------------------------ MXFP4
-// The OCP MXFP4 element (E2M1 nibble, sign in bit 3) at scale 1: magnitudes
-// 0, 0.5, 1, 1.5, 2, 3, 4, 6.
-__device__ __forceinline__ float e2m1_value(uint32_t n) {
-  const uint32_t m = n & 7u;
-  const float mag = m < 2u ? 0.5f * static_cast<float>(m)
-                           : __uint_as_float((((m >> 1) + 126u) << 23) | ((m & 1u) << 22));
-  return (n & 8u) ? -mag : mag;
+// MXFP4 operands of the block-scaled products.  The codes of a row (128
+// elements, 64 bytes) sit in 64-byte-swizzled rows: 16-byte piece c of row r
+// at r * 64 + ((c ^ ((r >> 1) & 3)) << 4), eight rows to a 512-byte atom (the
+// layout TMA writes for a 64-byte box row under 64-byte swizzle).  The block
+// scales of 128 rows sit in a 512-byte scale atom: byte r * 16 + j * 4 + k
+// holds block k of row 32 j + r, the layout tensor memory takes them in (one
+// 32-bit word per row, four rows per lane) by tcgen05.cp.32x128b.warpx4.
+__device__ __forceinline__ uint32_t swz64(uint32_t row, uint32_t piece) {
+  return row * 64u + ((piece ^ ((row >> 1) & 3u)) << 4);
+}
+__device__ __forceinline__ uint32_t scale_atom_byte(uint32_t row, uint32_t block) {
+  return (row & 31u) * 16u + (row >> 5) * 4u + block;
 }
 
-// A bf16 pair of decoded elements at scale 1 (from the table) times the
-// block scale 2^s: exact.  For s >= -125 the exponent fields move by s (no
-// carry out of a half: a nonzero e2m1 half has exponent 126..129); the two
-// smallest scales go through fp32 (their products may be subnormal).
-__device__ __forceinline__ uint32_t mx_scale_pair(uint32_t v, int s) {
-  if (s >= -125) {
-    const uint32_t add = static_cast<uint32_t>(s * 128);
-    const uint32_t lo = (v & 0x7fffu) ? add : 0u;
-    const uint32_t hi = (v & 0x7fff0000u) ? (add << 16) : 0u;
-    return v + lo + hi;
-  }
-  const float f = s == -126 ? __uint_as_float(0x00800000u) : __uint_as_float(0x00400000u);
-  const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
-  return pack_bf16x2(x.x * f, x.y * f);
-}
-
-// Decodes key row r of a raw MXFP4 stage (64 code bytes at r * 64, 4 scale
-// bytes at 8192 + r * 4) into row r of a bf16 stage (two 128B-swizzled
-// 64-dim chunks of 16 KB): one 16-byte piece (8 elements) per code word.
-__device__ __forceinline__ void mx_decode_row(const uint8_t* raw, const uint32_t* lut, uint8_t* A,
-                                              int r) {
-  const uint4* cw4 = reinterpret_cast<const uint4*>(raw + r * 64);
-  const uint32_t sc = *reinterpret_cast<const uint32_t*>(raw + 8192 + r * 4);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 c4 = cw4[q];  // block q: elements 32q .. 32q + 31
-    const int s = static_cast<int>((sc >> (8 * q)) & 0xffu) - 127;
-    const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t o[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) o[b] = mx_scale_pair(lut[(cw[k] >> (8 * b)) & 0xffu], s);
-      const int d = 32 * q + 8 * k;  // first element of the piece
-      *reinterpret_cast<uint4*>(A + (d >> 6) * 16384 + swz128(r, (d & 63) >> 3)) =
-          make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-}
-
-// The MXFP4 round trip of the group's bf16 query rows, in place (sQ,
-// 128B-swizzled 64-dim chunks): blocks of 32 dims share the scale
-// 2^(floor(log2 amax) - 2) (exponent at least -127), elements round to E2M1
-// (nearest, ties to even, saturating at 6) and decode back exactly.  Epilogue
-// warp e takes rows e, e + kEpiWarps, ...; lane l holds dims 4l .. 4l+3, so
-// lanes 8g .. 8g+7 hold block g.
+// E2M1 codes of two floats (nearest, ties to even, saturating at 6): lo in
+// the low nibble.
 __device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
   uint32_t r;
   asm("{\n\t.reg .b8 t;\n\t"
@@ -225,13 +194,21 @@ __device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
       : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ void mx_query_rows(uint8_t* sQ, int NQ, int ew, int lane) {
+
+// MXFP4 quantisation of the group's bf16 query rows (sQ, 128B-swizzled
+// 64-dim chunks) into E2M1 codes (sQ4, 64-byte-swizzled rows) and block
+// scales (the scale atom sfb): blocks of 32 dims share the scale
+// 2^(floor(log2 amax) - 2) (exponent at least -127), elements round to E2M1
+// (nearest, ties to even, saturating at 6).  Epilogue warp e takes rows e,
+// e + kEpiWarps, ...; lane l holds dims 4l .. 4l+3, so lanes 8g .. 8g+7 hold
+// block g.
+__device__ __forceinline__ void mx_query_codes(const uint8_t* sQ, uint8_t* sQ4, uint8_t* sfb,
+                                               int NQ, int ew, int lane) {
   const int d = 4 * lane;
   const uint32_t off = static_cast<uint32_t>(d >> 6) * NQ * 128u;
   const uint32_t piece = (d & 63) >> 3, within = (d & 7) * 2;
   for (int r = ew; r < NQ; r += kEpiWarps) {
-    uint2* cell = reinterpret_cast<uint2*>(sQ + off + swz128(r, piece) + within);
-    const uint2 u = *cell;
+    const uint2 u = *reinterpret_cast<const uint2*>(sQ + off + swz128(r, piece) + within);
     const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
     const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
     float amax = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
@@ -240,12 +217,12 @@ __device__ __forceinline__ void mx_query_rows(uint8_t* sQ, int NQ, int ew, int l
     int se = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 2;
     se = se < -127 ? -127 : se;
     const float inv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);  // 2^-se
-    const float sc = se >= -126 ? __uint_as_float(static_cast<uint32_t>(se + 127) << 23)
-                                : __uint_as_float(0x00400000u);          // 2^se
     const uint32_t c0 = e2m1x2_code(__fmul_rn(f0.x, inv), __fmul_rn(f0.y, inv));
     const uint32_t c1 = e2m1x2_code(__fmul_rn(f1.x, inv), __fmul_rn(f1.y, inv));
-    *cell = make_uint2(pack_bf16x2(e2m1_value(c0 & 15u) * sc, e2m1_value(c0 >> 4) * sc),
-                       pack_bf16x2(e2m1_value(c1 & 15u) * sc, e2m1_value(c1 >> 4) * sc));
+    // dims 4l .. 4l+3 are code bytes 2l, 2l+1: piece l / 8, byte 2 (l % 8)
+    *reinterpret_cast<uint16_t*>(sQ4 + swz64(r, lane >> 3) + 2 * (lane & 7)) =
+        static_cast<uint16_t>(c0 | (c1 << 8));
+    if ((lane & 7) == 0) sfb[scale_atom_byte(r, lane >> 3)] = static_cast<uint8_t>(se + 127);
   }
 }
 
@@ -278,26 +255,28 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                          const __grid_constant__ CUtensorMap tm_iq,
                          const __grid_constant__ CUtensorMap tm_ks, const IndexerArgs a) {
   constexpr bool F8 = KF == kKeyE4m3;  // E4M3 keys: kind::f8f6f4 products
-  constexpr bool MX = KF == kKeyMx4;   // MXFP4 keys: decoded to bf16 in shared memory
+  constexpr bool MX = KF == kKeyMx4;   // MXFP4 keys: kind::mxf4 block-scaled products
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128B-swizzled operand buffers
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  // [E4M3 query rows (FP8 keys)] [bf16 query rows] [key stages]
-  // [key scales of each stage (FP8 keys) | raw MXFP4 stages and the decode
-  // table (MXFP4 keys)] [IdxSmem]
-  const uint32_t q8_bytes = F8 ? static_cast<uint32_t>(a.NQ) * 128u : 0u;
+  // [E4M3 query rows (FP8 keys) | E2M1 query rows and their scale atom
+  // (MXFP4 keys)] [bf16 query rows] [key stages] [key scales of each stage
+  // (FP8 keys) | a scale atom per accumulator (MXFP4 keys)] [IdxSmem]
+  const uint32_t q8_bytes = indexer_q8_bytes(KF, a.NQ);
   const uint32_t q_bytes = static_cast<uint32_t>(a.KC) * a.NQ * 128u;
-  const uint32_t stage_bytes = F8 ? 16384u : static_cast<uint32_t>(a.KC) * 16384u;
-  uint8_t* sQ8 = base;
+  const uint32_t stage_bytes =
+      F8 ? 16384u : (MX ? kMxStageBytes : static_cast<uint32_t>(a.KC) * 16384u);
+  uint8_t* sQ8 = base;  // FP8: E4M3 rows; MXFP4: E2M1 rows, then their scale atom
+  uint8_t* sQ4 = base;
+  uint8_t* sfb_atom = base + static_cast<uint32_t>(a.NQ) * 64u;
   uint8_t* sQ = base + q8_bytes;
   uint8_t* sA = sQ + q_bytes;
   float* sScale = reinterpret_cast<float*>(sA + a.stages * stage_bytes);
-  uint8_t* sRaw = sA + a.stages * stage_bytes;  // MXFP4: raw stages, then the table
-  uint32_t* mxlut = reinterpret_cast<uint32_t*>(sRaw + (MX ? a.mx_stages * kMxRawBytes : 0));
+  uint8_t* sfa_atoms = sA + a.stages * stage_bytes;  // MXFP4: 512 bytes per accumulator
   IdxSmem* sm = reinterpret_cast<IdxSmem*>(
       sA + a.stages * stage_bytes +
-      (F8 ? a.stages * kBlockRows * 4 : (MX ? a.mx_stages * kMxRawBytes + 1024 : 0)));
+      (F8 ? a.stages * kBlockRows * 4 : (MX ? a.nacc * 512 : 0)));
   const EpiLayout el = epi_layout(a.NQ, a.G, a.hist_part != nullptr);
   uint8_t* epi = reinterpret_cast<uint8_t*>(sm) + (sizeof(IdxSmem) + 15) / 16 * 16;
   float* qscale = reinterpret_cast<float*>(epi + el.qscale);
@@ -311,16 +290,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   const int64_t s1 = a.total_slots * (blockIdx.x + 1) / gridDim.x;
 
   if (threadIdx.x == 0) {
-    // MXFP4: full/sempty follow the raw stages (copy landed / decoded by
-    // the slot's MMA warp), empty the bf16 stages; else all three the stages
-    const int nfull = MX ? a.mx_stages : a.stages;
-    for (int i = 0; i < nfull; ++i) {
+    for (int i = 0; i < a.stages; ++i) {
       mbar_init(smem_u32(&sm->full[i]), 1);
-      // the four warps of the slot's epilogue group (FP8 scales), or the
-      // decoding MMA warp (MXFP4)
-      mbar_init(smem_u32(&sm->sempty[i]), MX ? 1 : 4);
+      mbar_init(smem_u32(&sm->empty[i]), 1);
+      // FP8: the four warps of the slot's epilogue group read its scales
+      mbar_init(smem_u32(&sm->sempty[i]), 4);
     }
-    for (int i = 0; i < a.stages; ++i) mbar_init(smem_u32(&sm->empty[i]), 1);
     for (int i = 0; i < a.nacc; ++i) {
       mbar_init(smem_u32(&sm->tfull[i]), 1);
       mbar_init(smem_u32(&sm->tempty[i]), 128);  // the four warps of one epilogue group
@@ -330,9 +305,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     mbar_init(smem_u32(&sm->q8full), kEpiWarps);  // each epilogue warp quantised its rows
   }
   if (MX) {
-    // bf16 pair of each MXFP4 code byte at scale 1 (element 2i low nibble)
-    for (int i = threadIdx.x; i < 256; i += kIdxThreads)
-      mxlut[i] = pack_bf16x2(e2m1_value(i & 15), e2m1_value(i >> 4));
+    // the query scale atom's rows past NQ (never written per group): 2^0
+    for (int i = threadIdx.x; i < 512; i += kIdxThreads) sfb_atom[i] = 127;
+    fence_proxy_async_smem();  // read by tcgen05.cp
   }
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm->mma_done[0]), 1);
@@ -343,7 +318,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     tma_prefetch_desc(&tm_iq);
     if (F8 || MX) tma_prefetch_desc(&tm_ks);
   }
-  const int acc_cols = a.nacc * a.NQ;
+  const int acc_cols = a.nacc * a.NQ + (MX ? 4 * a.nacc + 8 : 0);  // MXFP4: scale columns too
   const uint32_t tmem_cols = acc_cols <= 32 ? 32 : (acc_cols <= 64 ? 64 : (acc_cols <= 128 ? 128 : (acc_cols <= 256 ? 256 : 512)));
   // Slot it accumulates into accumulator it % nacc, its (it / nacc)-th use;
   // every role tracks (acc, parity of the use) as a counter pair.  With six
@@ -371,7 +346,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       int64_t it = 0, qloads = 0;
       bool keys_ready = false;  // the compressed keys of the previous kernel are visible
       const uint64_t once = l2_policy_evict_first();
-      const int nst = MX ? a.mx_stages : a.stages;  // the ring the copies fill
+      const int nst = a.stages;
       for (cur.init(a, s0, s1); !cur.done && !*abort; cur.advance(a)) {
         if (cur.fresh) {
           if (qloads > 0 &&
@@ -386,12 +361,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         }
         // stage st was last filled `stages` uses ago, in phase ph ^ 1; with
         // FP8 keys its scales are also read by the epilogue, which lags the
-        // MMAs.  MXFP4: the raw stage is free once its slot's MMA warp has
-        // decoded it (the bf16 stages are that warp's own)
-        if (!MX && it >= a.stages &&
+        // MMAs (MXFP4: the slot's MMA warp reads the scales before its
+        // products, which release the stage)
+        if (it >= a.stages &&
             !mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 11))
           break;
-        if ((F8 || MX) && it >= nst &&
+        if (F8 && it >= nst &&
             !mbar_wait(smem_u32(&sm->sempty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 20))
           break;
         if (!keys_ready &&
@@ -403,12 +378,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           keys_ready = true;
         }
         const uint32_t fb = smem_u32(&sm->full[st]);
-        mbar_arrive_expect_tx(fb, MX ? kMxRawBytes : stage_bytes + (F8 ? kBlockRows * 4 : 0));
+        mbar_arrive_expect_tx(fb, stage_bytes + (F8 ? kBlockRows * 4 : 0));
         // the keys are read once: first out of L2 (the scores written
         // meanwhile, and whatever the attention reads again, stay)
         if (MX) {
-          // 128 rows of 64 code bytes; their scales, 4 keys per 16-byte row
-          uint8_t* rs = sRaw + st * kMxRawBytes;
+          // 128 rows of 64 code bytes (64-byte swizzle); their scales, 4 keys
+          // per 16-byte row
+          uint8_t* rs = sA + st * stage_bytes;
           tma_load_3d_hint(smem_u32(rs), &tm_ik, 0, cur.blk * kBlockRows, cur.b, fb, once);
           tma_load_3d_hint(smem_u32(rs + 8192), &tm_ks, 0, cur.blk * (kBlockRows / 4), cur.b, fb,
                            once);
@@ -445,15 +421,20 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     // it % nacc, its (it / nacc)-th use.
     const int par = warp == 1 ? 0 : 1;
     if (MX) {
-      // MXFP4 keys: the whole warp decodes its slot's raw stage into a bf16
-      // stage (lane l: key rows l, l + 32, l + 64, l + 96), then lane 0
-      // issues the bf16 products as for bf16 keys.  Both rings are even, so
-      // a raw stage and a bf16 stage each belong to one of the two warps.
-      const uint32_t idesc = idesc_bf16(128, a.NQ, 0, 0);
-      const uint32_t qbar = smem_u32(&sm->q8full);  // the queries after their MXFP4 round trip
+      // MXFP4 keys: block-scaled products (kind::mxf4, K = 64 per call, two
+      // per slot) of the key codes, as the copy lands them, and the group's
+      // E2M1 query rows.  The scales reach tensor memory by tcgen05.cp from
+      // 512-byte scale atoms: the query atom (the epilogue warps write it) at
+      // each group change into this warp's own four columns, and per slot
+      // the keys' scales, which travel with the stage key by key and which
+      // the warp lays out as the atom of the slot's accumulator (lane r:
+      // keys r, r + 32, r + 64, r + 96), into that accumulator's columns.
+      const uint32_t sfa_col = tmem + static_cast<uint32_t>(a.nacc * a.NQ);
+      const uint32_t sfb_col = sfa_col + 4u * a.nacc + 4u * par;
+      const uint32_t qbar = smem_u32(&sm->q8full);  // the group's E2M1 rows and scales
       SlotCursor cur;
-      int st = 0, rs = 0, acc = 0;
-      uint32_t ph = 0, rph = 0, aph = 0;
+      int st = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
       int64_t it = 0, qn = 0;
       bool ok = true;
       for (cur.init(a, s0, s1); !cur.done && ok && !*abort; cur.advance(a)) {
@@ -463,39 +444,41 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                           mbar_wait(qbar, qn & 1, abort, a.status, kWaitLimitNs, 13));
           if (!ok) break;
           ++qn;
+          if (lane == 0) {
+            tc_fence_after();
+            tmem_cp_32x128b_x4(sfb_col, smem_desc(smem_u32(sfb_atom), 128, 128, kSwizzleNone));
+          }
         }
         if (static_cast<int>(it & 1) == par) {
           bool got = true;
           // the accumulator's previous use has been drained by the epilogue
+          // (its products and the copy of its scale atom are complete)
           if (it >= a.nacc)
             got = mbar_wait(smem_u32(&sm->tempty[acc]), aph ^ 1u, abort, a.status, kWaitLimitNs,
                             14);
-          // the raw copy has landed
-          got = got && mbar_wait(smem_u32(&sm->full[rs]), rph, abort, a.status, kWaitLimitNs, 15);
-          // this warp's products of `stages` slots ago have read the bf16 stage
-          if (it >= a.stages)
-            got = got &&
-                  mbar_wait(smem_u32(&sm->empty[st]), ph ^ 1u, abort, a.status, kWaitLimitNs, 56);
+          // the copy has landed
+          got = got && mbar_wait(smem_u32(&sm->full[st]), ph, abort, a.status, kWaitLimitNs, 15);
           ok = __all_sync(0xffffffffu, got);
           if (!ok) break;
-          const uint8_t* raw = sRaw + rs * kMxRawBytes;
-          uint8_t* Ast = sA + st * stage_bytes;
-          for (int r = lane; r < kBlockRows; r += 32) mx_decode_row(raw, mxlut, Ast, r);
-          fence_proxy_async_smem();  // the decoded rows are read by the tensor core
+          const uint8_t* stage = sA + st * stage_bytes;
+          const uint32_t* ks = reinterpret_cast<const uint32_t*>(stage + 8192);
+          uint8_t* atom = sfa_atoms + acc * 512;
+          *reinterpret_cast<uint4*>(atom + lane * 16) =
+              make_uint4(ks[lane], ks[32 + lane], ks[64 + lane], ks[96 + lane]);
+          fence_proxy_async_smem();  // read by tcgen05.cp
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_u32(&sm->sempty[rs]));  // the raw stage may be refilled
             tc_fence_after();
+            const uint32_t sfa = sfa_col + 4u * acc;
+            tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(atom), 128, 128, kSwizzleNone));
             const uint32_t d_tmem = tmem + acc * a.NQ;
-            for (int kc = 0; kc < a.KC; ++kc) {
-              const uint32_t a_addr = smem_u32(Ast + kc * 16384);
-              const uint32_t b_addr = smem_u32(sQ + kc * a.NQ * 128);
+            const uint32_t a_addr = smem_u32(stage), b_addr = smem_u32(sQ4);
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ad = smem_desc(a_addr + ks * 32, 16, 1024, kSwizzle128B);
-                const uint64_t bd = smem_desc(b_addr + ks * 32, 16, 1024, kSwizzle128B);
-                mma_bf16_ss(d_tmem, ad, bd, idesc, (kc | ks) != 0);
-              }
+            for (int kh = 0; kh < 2; ++kh) {  // elements 64 kh .. 64 kh + 63: 32 bytes a row
+              const uint64_t ad = smem_desc(a_addr + kh * 32, 16, 512, kSwizzle64B);
+              const uint64_t bd = smem_desc(b_addr + kh * 32, 16, 512, kSwizzle64B);
+              mma_mxf4_ss(d_tmem, ad, bd, idesc_mxf4(128, a.NQ, 2u * kh, 2u * kh), sfa, sfb_col,
+                          kh);
             }
             mma_commit(smem_u32(&sm->empty[st]));
             mma_commit(smem_u32(&sm->tfull[acc]));
@@ -505,7 +488,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         ++it;
         if (++acc == a.nacc) { acc = 0; aph ^= 1u; }
         if (++st == a.stages) { st = 0; ph ^= 1u; }
-        if (++rs == a.mx_stages) { rs = 0; rph ^= 1u; }
       }
       // all issued MMAs complete before the accumulators are released
       if (lane == 0) {
@@ -617,7 +599,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         // row scales (MXFP4: the rows' round trip, in place)
         bool got = mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 18);
         if (!__all_sync(0xffffffffu, got)) return false;
-        if (MX) mx_query_rows(sQ, a.NQ, ew, lane);
+        if (MX) mx_query_codes(sQ, sQ4, sfb_atom, a.NQ, ew, lane);
         else quantize_query_rows(sQ, sQ8, qscale, a.NQ, ew, lane);
         fence_proxy_async_smem();  // visible to the tensor core's reads
         __syncwarp();
@@ -789,34 +771,39 @@ bool plan_indexer(int T, int HI, int dI, int kf, bool fold, IndexerPlan* p) {
   if (HI <= 0 || HI > 256 || dI <= 0 || dI > 128) return false;
   const bool f8 = kf == kKeyE4m3, mx = kf == kKeyMx4;
   if ((f8 || mx) && dI != 128) return false;
-  int G = 256 / HI;
+  // MXFP4: at most 128 query rows a group, so that two accumulators and the
+  // scale columns fit in tensor memory
+  const int max_nq = mx ? 128 : 256;
+  int G = max_nq / HI;
   if (G > T) G = T;
   if (G < 1) G = 1;
   int NQ = ((G * HI + 31) / 32) * 32;
-  if (NQ > 256) return false;
+  if (NQ > max_nq) return false;
   p->G = G;
   p->NQ = NQ;
   p->KC = (dI + 63) / 64;
-  const size_t q_bytes = (size_t)p->KC * NQ * 128 + (f8 ? (size_t)NQ * 128 : 0);
-  // FP8: 16 KB of codes plus the block's 128 fp32 scales per stage
-  const size_t stage_bytes = f8 ? 16384 + kBlockRows * 4 : (size_t)p->KC * 16384;
+  const size_t q_bytes = (size_t)p->KC * NQ * 128 + indexer_q8_bytes(kf, NQ);
+  // FP8: 16 KB of codes plus the block's 128 fp32 scales per stage; MXFP4:
+  // 8 KB of codes plus 512 bytes of scales
+  const size_t stage_bytes =
+      f8 ? 16384 + kBlockRows * 4 : (mx ? kMxStageBytes : (size_t)p->KC * 16384);
   if (fold && G != 1) return false;  // the folded pass counts one query per group
-  const size_t fixed = (sizeof(IdxSmem) + 15) / 16 * 16 + epi_layout(NQ, G, fold).bytes;
-  // MXFP4: the raw stages the copies fill (the HBM stream in flight) and the
-  // decode table come first; the bf16 stages the products read get the rest
-  const int mx_stages = mx ? kMaxMxStages : 0;
-  const size_t mx_bytes = mx ? (size_t)mx_stages * kMxRawBytes + 1024 : 0;
-  const size_t budget = 227 * 1024 - 1024 - fixed - q_bytes - mx_bytes;
-  int stages = static_cast<int>(budget / stage_bytes);
-  const int cap = f8 ? kMaxStages : (mx ? 4 : kMaxStagesBf16);
-  if (stages > cap) stages = cap;
   // Accumulators: six when tensor memory holds them (three epilogue groups
   // drain them, slot s to group s % 3), else as many as it holds up to
-  // kMaxAcc, a power of 2 (two epilogue groups).
+  // kMaxAcc, a power of 2 (two epilogue groups).  MXFP4 also keeps four
+  // scale columns per accumulator and four per MMA issuer.
+  auto cols = [&](int n) { return n * NQ + (mx ? 4 * n + 8 : 0); };
   int nacc = 2;
-  while (nacc * 2 <= kMaxAcc && nacc * 2 * NQ <= 512) nacc *= 2;
-  if (6 * NQ <= 512) nacc = 6;
+  while (nacc * 2 <= kMaxAcc && cols(nacc * 2) <= 512) nacc *= 2;
+  if (cols(6) <= 512) nacc = 6;
+  if (cols(nacc) > 512) return false;
   const int egroups = nacc % 3 == 0 ? 3 : 2;
+  const size_t fixed = (sizeof(IdxSmem) + 15) / 16 * 16 + epi_layout(NQ, G, fold).bytes +
+                       (mx ? (size_t)nacc * 512 : 0);
+  const size_t budget = 227 * 1024 - 1024 - fixed - q_bytes;
+  int stages = static_cast<int>(budget / stage_bytes);
+  const int cap = (f8 || mx) ? kMaxStages : kMaxStagesBf16;
+  if (stages > cap) stages = cap;
   // Slot s uses stage s % stages and accumulator s % nacc, is issued by MMA
   // warp s % 2 and drained by epilogue group s % egroups.  A ring whose
   // length is a multiple of the roles sharing it gives each stage (each
@@ -824,17 +811,16 @@ bool plan_indexer(int T, int HI, int dI, int kf, bool fold, IndexerPlan* p) {
   // phases in order.  Otherwise a stage alternates between, say, the
   // issuers, and an issuer that runs a lap ahead of the other would wait on
   // the parity of a phase whose predecessor is still pending -- a parity
-  // wait that passes at once.  The stages of bf16 keys (and the bf16 stages
-  // of MXFP4 keys) are the issuers' alone; the epilogue reads the FP8 key
-  // scales from its slot's stage.
+  // wait that passes at once.  The stages of bf16 and MXFP4 keys are the
+  // issuers' alone; the epilogue reads the FP8 key scales from its slot's
+  // stage.
   const int ring = f8 ? 2 * egroups : 2;
   stages -= stages % ring;
   if (stages < ring) return false;
   p->stages = stages;
-  p->mx_stages = mx_stages;
   p->nacc = nacc;
-  p->tmem_cols = nacc * NQ;
-  p->smem_bytes = 1024 + q_bytes + stages * stage_bytes + mx_bytes + fixed;
+  p->tmem_cols = cols(nacc);
+  p->smem_bytes = 1024 + q_bytes + stages * stage_bytes + fixed;
   return true;
 }
 

@@ -51,7 +51,6 @@ struct IndexerArgs {
   int NQ;                // MMA N
   int KC;                // 64-wide K chunks of the bf16 operands
   int stages;
-  int mx_stages;         // MXFP4 keys: raw stages (else 0)
   int nacc;              // tensor-memory accumulators in flight (2, 4 or 8)
   int groups_per_seq;    // ceil(T / G)
   int nblk;              // ceil(N_cap / 128)
@@ -67,7 +66,7 @@ struct IndexerArgs {
   uint16_t* hist_part;
 };
 struct IndexerPlan {
-  int G, NQ, KC, stages, mx_stages, nacc, tmem_cols;
+  int G, NQ, KC, stages, nacc, tmem_cols;
   size_t smem_bytes;
 };
 // Key formats: bf16 keys and queries; E4M3 keys (dI = 128, one 128-byte row

@@ -35,13 +35,14 @@ namespace hattn {
 
 namespace {
 
-// warps: 0 producer, 1 and 2 MMA issuers (even / odd slots), then
-// kEpiGroups x 4 epilogue warps (any 4 consecutive warps cover the four
-// 32-lane quarters of tensor memory)
+// warps: 0 producer (even slots), 1 and 2 MMA issuers (even / odd slots),
+// then kEpiGroups x 4 epilogue warps (any 4 consecutive warps cover the four
+// 32-lane quarters of tensor memory), then the producer of the odd slots
 constexpr int kEpiGroups = 3;
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kFirstEpiWarp = 3;
-constexpr int kIdxThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kProducer2 = kFirstEpiWarp + kEpiWarps;  // the second producer, last warp
+constexpr int kIdxThreads = 32 * (kProducer2 + 1);
 constexpr int kBlockRows = 128;
 constexpr int kMaxStages = 12;
 constexpr int kMaxStagesBf16 = 8;
@@ -165,6 +166,41 @@ struct SlotCursor {
   __device__ __forceinline__ void advance(const IndexerArgs& a) {
     fresh = false;
     if (++blk >= blk_end) next_group(a);
+  }
+};
+
+// A role's walk over the CTA's live slots together with the rings they
+// index: slot it uses stage it % stages (phase bit ph) and accumulator
+// it % nacc (phase bit aph).
+struct SlotWalk {
+  SlotCursor cur;
+  int64_t it;
+  int st, acc;
+  uint32_t ph, aph;
+  __device__ __forceinline__ void init(const IndexerArgs& a, int64_t s0, int64_t s1) {
+    cur.init(a, s0, s1);
+    it = 0;
+    st = acc = 0;
+    ph = aph = 0;
+  }
+  // one slot on (the cursor may enter a new query group: cur.fresh)
+  __device__ __forceinline__ void step(const IndexerArgs& a) {
+    cur.advance(a);
+    ++it;
+    if (++st == a.stages) { st = 0; ph ^= 1u; }
+    if (++acc == a.nacc) { acc = 0; aph ^= 1u; }
+  }
+  // n slots on by plain arithmetic when they stay in the current group
+  // (n <= stages and n <= nacc: each ring wraps at most once); else false
+  __device__ __forceinline__ bool leap(const IndexerArgs& a, int n) {
+    if (cur.blk + n >= cur.blk_end) return false;
+    cur.blk += n;
+    it += n;
+    st += n;
+    if (st >= a.stages) { st -= a.stages; ph ^= 1u; }
+    acc += n;
+    if (acc >= a.nacc) { acc -= a.nacc; aph ^= 1u; }
+    return true;
   }
 };
 
@@ -337,28 +373,47 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
   // Ring positions are tracked as (stage, phase) pairs advanced by one per
   // use, so the loops below divide nothing per slot.
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kProducer2) {
+    // ------------------------------------------------------------ producers
+    // Two producer threads (warp 0 and the last warp) issue the copies of
+    // the even and the odd live slots: a single thread issues a slot's
+    // copies only every ~0.45 us, less than the key stream needs.  The ring
+    // is even, so each stage belongs to one of them.  Producer 0 also loads
+    // each group's query rows.
     if (lane == 0) {
+      const int ppar = warp == 0 ? 0 : 1;
       SlotCursor cur;
       int st = 0;
       uint32_t ph = 0;
-      int64_t it = 0, qloads = 0;
+      int64_t it = 0, qloads = 0, hi = 0;  // hi: one past the last slot this thread issued
       bool keys_ready = false;  // the compressed keys of the previous kernel are visible
       const uint64_t once = l2_policy_evict_first();
       const int nst = a.stages;
-      for (cur.init(a, s0, s1); !cur.done && !*abort; cur.advance(a)) {
-        if (cur.fresh) {
-          if (qloads > 0 &&
-              !mbar_wait(smem_u32(&sm->qempty), (qloads - 1) & 1, abort, a.status, kWaitLimitNs, 10))
-            break;
-          const uint32_t qb = smem_u32(&sm->qfull);
-          mbar_arrive_expect_tx(qb, q_bytes);
-          const int row0 = ((cur.b * a.T) + cur.t0) * a.HI;
-          for (int kc = 0; kc < a.KC; ++kc)
-            tma_load_2d(smem_u32(sQ + kc * a.NQ * 128), &tm_iq, kc * 64, row0, qb);
-          ++qloads;
-        }
+      // a new query group: producer 0 loads its query rows once the MMA
+      // issuers have left the previous group's
+      auto enter_group = [&]() -> bool {
+        if (ppar != 0) return true;
+        if (qloads > 0 &&
+            !mbar_wait(smem_u32(&sm->qempty), (qloads - 1) & 1, abort, a.status, kWaitLimitNs, 10))
+          return false;
+        const uint32_t qb = smem_u32(&sm->qfull);
+        mbar_arrive_expect_tx(qb, q_bytes);
+        const int row0 = ((cur.b * a.T) + cur.t0) * a.HI;
+        for (int kc = 0; kc < a.KC; ++kc)
+          tma_load_2d(smem_u32(sQ + kc * a.NQ * 128), &tm_iq, kc * 64, row0, qb);
+        ++qloads;
+        return true;
+      };
+      auto step = [&]() -> bool {
+        cur.advance(a);
+        ++it;
+        if (++st == nst) { st = 0; ph ^= 1u; }
+        return !cur.done && (!cur.fresh || enter_group());
+      };
+      cur.init(a, s0, s1);
+      bool more = !cur.done && enter_group();
+      if (more && static_cast<int>(it & 1) != ppar) more = step();
+      while (more && !*abort) {
         // stage st was last filled `stages` uses ago, in phase ph ^ 1; with
         // FP8 keys its scales are also read by the epilogue, which lags the
         // MMAs (MXFP4: the slot's MMA warp reads the scales before its
@@ -397,19 +452,28 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           for (int kc = 0; kc < a.KC; ++kc)
             tma_load_3d_hint(smem_u32(sA + st * stage_bytes + kc * 16384), &tm_ik, kc * 64,
                              cur.blk * kBlockRows, cur.b, fb, once);
-        ++it;
-        if (++st == nst) { st = 0; ph ^= 1u; }
+        hi = it + 1;
+        // this thread's next slot, two on: plain arithmetic within the group
+        if (cur.blk + 2 < cur.blk_end) {
+          cur.blk += 2;
+          it += 2;
+          st += 2;
+          if (st >= nst) { st -= nst; ph ^= 1u; }
+        } else {
+          more = step() && step();
+        }
       }
       if (*abort) {
         // let the copies already issued land before the CTA exits: the last
         // query block (its predecessor's phase completed before it was
-        // issued: the issuers had released it), then the key stages
+        // issued: the issuers had released it), then this thread's key
+        // stages among the last `stages` slots
         if (qloads > 0)
           mbar_wait(smem_u32(&sm->qfull), (qloads - 1) & 1, nullptr, nullptr, 10000000ull, 13);
-        const int64_t first = it > nst ? it - nst : 0;
-        for (int64_t x = first; x < it; ++x)
-          mbar_wait(smem_u32(&sm->full[x % nst]), (x / nst) & 1, nullptr, nullptr, 10000000ull,
-                    12);
+        for (int64_t x = hi > nst ? hi - nst : 0; x < hi; ++x)
+          if (static_cast<int>(x & 1) == ppar)
+            mbar_wait(smem_u32(&sm->full[x % nst]), (x / nst) & 1, nullptr, nullptr, 10000000ull,
+                      12);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -432,62 +496,65 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const uint32_t sfa_col = tmem + static_cast<uint32_t>(a.nacc * a.NQ);
       const uint32_t sfb_col = sfa_col + 4u * a.nacc + 4u * par;
       const uint32_t qbar = smem_u32(&sm->q8full);  // the group's E2M1 rows and scales
-      SlotCursor cur;
-      int st = 0, acc = 0;
-      uint32_t ph = 0, aph = 0;
-      int64_t it = 0, qn = 0;
-      bool ok = true;
-      for (cur.init(a, s0, s1); !cur.done && ok && !*abort; cur.advance(a)) {
-        if (cur.fresh) {
-          if (lane == 0 && qn > 0) mma_commit(smem_u32(&sm->qempty));
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(qbar, qn & 1, abort, a.status, kWaitLimitNs, 13));
-          if (!ok) break;
-          ++qn;
-          if (lane == 0) {
-            tc_fence_after();
-            tmem_cp_32x128b_x4(sfb_col, smem_desc(smem_u32(sfb_atom), 128, 128, kSwizzleNone));
-          }
+      SlotWalk w;
+      int64_t qn = 0;
+      // a new query group: the previous group's rows are released, this
+      // group's are ready, and their scales go to this warp's columns
+      auto enter_group = [&]() -> bool {
+        if (lane == 0 && qn > 0) mma_commit(smem_u32(&sm->qempty));
+        if (!__all_sync(0xffffffffu, mbar_wait(qbar, qn & 1, abort, a.status, kWaitLimitNs, 13)))
+          return false;
+        ++qn;
+        if (lane == 0) {
+          tc_fence_after();
+          tmem_cp_32x128b_x4(sfb_col, smem_desc(smem_u32(sfb_atom), 128, 128, kSwizzleNone));
         }
-        if (static_cast<int>(it & 1) == par) {
-          bool got = true;
-          // the accumulator's previous use has been drained by the epilogue
-          // (its products and the copy of its scale atom are complete)
-          if (it >= a.nacc)
-            got = mbar_wait(smem_u32(&sm->tempty[acc]), aph ^ 1u, abort, a.status, kWaitLimitNs,
-                            14);
-          // the copy has landed
-          got = got && mbar_wait(smem_u32(&sm->full[st]), ph, abort, a.status, kWaitLimitNs, 15);
-          ok = __all_sync(0xffffffffu, got);
-          if (!ok) break;
-          const uint8_t* stage = sA + st * stage_bytes;
-          const uint32_t* ks = reinterpret_cast<const uint32_t*>(stage + 8192);
-          uint8_t* atom = sfa_atoms + acc * 512;
-          *reinterpret_cast<uint4*>(atom + lane * 16) =
-              make_uint4(ks[lane], ks[32 + lane], ks[64 + lane], ks[96 + lane]);
-          fence_proxy_async_smem();  // read by tcgen05.cp
-          __syncwarp();
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t sfa = sfa_col + 4u * acc;
-            tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(atom), 128, 128, kSwizzleNone));
-            const uint32_t d_tmem = tmem + acc * a.NQ;
-            const uint32_t a_addr = smem_u32(stage), b_addr = smem_u32(sQ4);
+        return true;
+      };
+      auto step = [&]() -> bool {
+        w.step(a);
+        return !w.cur.done && (!w.cur.fresh || enter_group());
+      };
+      w.init(a, s0, s1);
+      bool more = !w.cur.done && enter_group();
+      if (more && static_cast<int>(w.it & 1) != par) more = step();
+      while (more && !*abort) {
+        const int st = w.st, acc = w.acc;
+        bool got = true;
+        // the accumulator's previous use has been drained by the epilogue
+        // (its products and the copy of its scale atom are complete)
+        if (w.it >= a.nacc)
+          got = mbar_wait(smem_u32(&sm->tempty[acc]), w.aph ^ 1u, abort, a.status, kWaitLimitNs,
+                          14);
+        // the copy has landed
+        got = got && mbar_wait(smem_u32(&sm->full[st]), w.ph, abort, a.status, kWaitLimitNs, 15);
+        if (!__all_sync(0xffffffffu, got)) break;
+        const uint8_t* stage = sA + st * stage_bytes;
+        const uint32_t* ks = reinterpret_cast<const uint32_t*>(stage + 8192);
+        uint8_t* atom = sfa_atoms + acc * 512;
+        *reinterpret_cast<uint4*>(atom + lane * 16) =
+            make_uint4(ks[lane], ks[32 + lane], ks[64 + lane], ks[96 + lane]);
+        fence_proxy_async_smem();  // read by tcgen05.cp
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sfa = sfa_col + 4u * acc;
+          tmem_cp_32x128b_x4(sfa, smem_desc(smem_u32(atom), 128, 128, kSwizzleNone));
+          const uint32_t d_tmem = tmem + acc * a.NQ;
+          const uint32_t a_addr = smem_u32(stage), b_addr = smem_u32(sQ4);
 #pragma unroll
-            for (int kh = 0; kh < 2; ++kh) {  // elements 64 kh .. 64 kh + 63: 32 bytes a row
-              const uint64_t ad = smem_desc(a_addr + kh * 32, 16, 512, kSwizzle64B);
-              const uint64_t bd = smem_desc(b_addr + kh * 32, 16, 512, kSwizzle64B);
-              mma_mxf4_ss(d_tmem, ad, bd, idesc_mxf4(128, a.NQ, 2u * kh, 2u * kh), sfa, sfb_col,
-                          kh);
-            }
-            mma_commit(smem_u32(&sm->empty[st]));
-            mma_commit(smem_u32(&sm->tfull[acc]));
+          for (int kh = 0; kh < 2; ++kh) {  // elements 64 kh .. 64 kh + 63: 32 bytes a row
+            const uint64_t ad = smem_desc(a_addr + kh * 32, 16, 512, kSwizzle64B);
+            const uint64_t bd = smem_desc(b_addr + kh * 32, 16, 512, kSwizzle64B);
+            mma_mxf4_ss(d_tmem, ad, bd, idesc_mxf4(128, a.NQ, 2u * kh, 2u * kh), sfa, sfb_col,
+                        kh);
           }
-          __syncwarp();
+          mma_commit(smem_u32(&sm->empty[st]));
+          mma_commit(smem_u32(&sm->tfull[acc]));
         }
-        ++it;
-        if (++acc == a.nacc) { acc = 0; aph ^= 1u; }
-        if (++st == a.stages) { st = 0; ph ^= 1u; }
+        __syncwarp();
+        // this warp's next slot, two on
+        if (!w.leap(a, 2)) more = step() && step();
       }
       // all issued MMAs complete before the accumulators are released
       if (lane == 0) {
@@ -495,63 +562,77 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         mbar_wait(smem_u32(&sm->mma_done[par]), 0, nullptr, a.status, kWaitLimitNs, 16);
       }
       __syncwarp();
-    } else if (lane == 0) {
+    } else {
+      // bf16 or E4M3 keys.  The whole warp walks the slots and computes the
+      // operand descriptors (warp-uniform values, so they stay in uniform
+      // registers); lane 0 issues the products.
       const uint32_t idesc = F8 ? idesc_e4m3(128, a.NQ) : idesc_bf16(128, a.NQ, 0, 0);
       // the operand rows the products read: E4M3 codes, or the bf16 rows
-      const uint64_t qbar = smem_u32(F8 ? &sm->q8full : &sm->qfull);
-      SlotCursor cur;
-      int st = 0, acc = 0;
-      uint32_t ph = 0, aph = 0;
-      int64_t it = 0, qn = 0;
-      for (cur.init(a, s0, s1); !cur.done && !*abort; cur.advance(a)) {
-        if (cur.fresh) {
-          if (qn > 0) mma_commit(smem_u32(&sm->qempty));  // previous group's reads of sQ done
-          if (!mbar_wait(static_cast<uint32_t>(qbar), qn & 1, abort, a.status, kWaitLimitNs, 13))
-            break;
-          ++qn;
-        }
-        if (static_cast<int>(it & 1) == par) {
-          // the accumulator's previous use has been drained by the epilogue
-          if (it >= a.nacc &&
-              !mbar_wait(smem_u32(&sm->tempty[acc]), aph ^ 1u, abort, a.status, kWaitLimitNs, 14))
-            break;
-          if (!mbar_wait(smem_u32(&sm->full[st]), ph, abort, a.status, kWaitLimitNs, 15)) break;
+      const uint32_t qbar = smem_u32(F8 ? &sm->q8full : &sm->qfull);
+      // descriptors: 128-byte swizzle, 8-row atoms 1024 bytes apart; a K
+      // step of 32 bytes adds 2 to the start address field, a 64-dim chunk
+      // (16 KB of keys, NQ x 128 bytes of queries) adds its size / 16
+      const uint64_t q_desc = smem_desc(smem_u32(F8 ? sQ8 : sQ), 16, 1024, kSwizzle128B);
+      const uint64_t k_desc0 = smem_desc(smem_u32(sA), 16, 1024, kSwizzle128B);
+      SlotWalk w;
+      int64_t qn = 0;
+      // a new query group: the previous group's reads of the query rows are
+      // released and this group's are ready
+      auto enter_group = [&]() -> bool {
+        if (lane == 0 && qn > 0) mma_commit(smem_u32(&sm->qempty));
+        if (!__all_sync(0xffffffffu, mbar_wait(qbar, qn & 1, abort, a.status, kWaitLimitNs, 13)))
+          return false;
+        ++qn;
+        return true;
+      };
+      auto step = [&]() -> bool {
+        w.step(a);
+        return !w.cur.done && (!w.cur.fresh || enter_group());
+      };
+      w.init(a, s0, s1);
+      bool more = !w.cur.done && enter_group();
+      if (more && static_cast<int>(w.it & 1) != par) more = step();
+      while (more && !*abort) {
+        const int st = w.st, acc = w.acc;
+        bool got = true;
+        // the accumulator's previous use has been drained by the epilogue
+        if (w.it >= a.nacc)
+          got = mbar_wait(smem_u32(&sm->tempty[acc]), w.aph ^ 1u, abort, a.status, kWaitLimitNs,
+                          14);
+        got = got && mbar_wait(smem_u32(&sm->full[st]), w.ph, abort, a.status, kWaitLimitNs, 15);
+        if (!__all_sync(0xffffffffu, got)) break;
+        const uint32_t d_tmem = tmem + acc * a.NQ;
+        const uint64_t k_desc = k_desc0 + static_cast<uint64_t>(st * (stage_bytes >> 4));
+        if (lane == 0) {
           tc_fence_after();
-          const uint32_t d_tmem = tmem + acc * a.NQ;
           if (F8) {
             // one 128-byte row per key and per query: 4 steps of K = 32
-            const uint32_t a_addr = smem_u32(sA + st * stage_bytes);
-            const uint32_t b_addr = smem_u32(sQ8);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = smem_desc(a_addr + ks * 32, 16, 1024, kSwizzle128B);
-              const uint64_t bd = smem_desc(b_addr + ks * 32, 16, 1024, kSwizzle128B);
-              mma_f8_ss(d_tmem, ad, bd, idesc, ks != 0);
-            }
+            for (int ks = 0; ks < 4; ++ks) mma_f8_ss(d_tmem, k_desc + 2 * ks, q_desc + 2 * ks, idesc, ks != 0);
           } else {
             for (int kc = 0; kc < a.KC; ++kc) {
-              const uint32_t a_addr = smem_u32(sA + st * stage_bytes + kc * 16384);
-              const uint32_t b_addr = smem_u32(sQ + kc * a.NQ * 128);
+              const uint64_t kd = k_desc + kc * (16384 >> 4);
+              const uint64_t qd = q_desc + static_cast<uint64_t>(kc * a.NQ * (128 >> 4));
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ad = smem_desc(a_addr + ks * 32, 16, 1024, kSwizzle128B);
-                const uint64_t bd = smem_desc(b_addr + ks * 32, 16, 1024, kSwizzle128B);
-                mma_bf16_ss(d_tmem, ad, bd, idesc, (kc | ks) != 0);
-              }
+              for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ss(d_tmem, kd + 2 * ks, qd + 2 * ks, idesc, (kc | ks) != 0);
             }
           }
           mma_commit(smem_u32(&sm->empty[st]));
           mma_commit(smem_u32(&sm->tfull[acc]));
         }
-        ++it;
-        if (++acc == a.nacc) { acc = 0; aph ^= 1u; }
-        if (++st == a.stages) { st = 0; ph ^= 1u; }
+        __syncwarp();
+        // this warp's next slot, two on
+        if (!w.leap(a, 2)) more = step() && step();
       }
       // all issued MMAs complete before the accumulators are released
-      mma_commit(smem_u32(&sm->mma_done[par]));
-      mbar_wait(smem_u32(&sm->mma_done[par]), 0, nullptr, a.status, kWaitLimitNs, 16);
+      if (lane == 0) {
+        mma_commit(smem_u32(&sm->mma_done[par]));
+        mbar_wait(smem_u32(&sm->mma_done[par]), 0, nullptr, a.status, kWaitLimitNs, 16);
+      }
+      __syncwarp();
     }
-  } else {
+  } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     // Group eg drains the slots it with it % kEpiGroups == eg; its warp for
     // tensor-memory lanes quad*32 .. quad*32+31 handles those 32 entries.

@@ -1,8 +1,9 @@
 """A model of the indexer kernel's mbarrier protocol, run under random schedules.
 
-The score kernel is warp-specialised: a producer issues TMA copies of key
-blocks into a ring of `stages` buffers (and, at each query-group change, the
-group's query rows), two MMA issuers take alternate slots into a ring of
+The score kernel is warp-specialised: two producers issue TMA copies of the
+key blocks of alternate slots into a ring of `stages` buffers (and the first,
+at each query-group change, the group's query rows), two MMA issuers take
+alternate slots into a ring of
 `nacc` tensor-memory accumulators, and epilogue groups drain alternate
 accumulators.  Copies land and MMAs complete asynchronously; a commit
 arrives once the issuing thread's earlier MMAs are done.  With FP8 keys the
@@ -79,17 +80,24 @@ def simulate(slots, stages, nacc, groups, f8, seed, idle=0):
     mem = {"q": None, "q8": None, "stage": [None] * stages, "acc": [None] * nacc}
     errors = []
 
-    def producer():
+    def producer(par):
         st = ph = it = qloads = 0
         loaded = None
         for grp, blk in slots:
             if grp != loaded:
-                if qloads:
-                    yield "qempty", (qloads - 1) & 1
-                bars["qfull"].expect_tx(1)
-                copies.append(lambda g=grp: (mem.__setitem__("q", g), bars["qfull"].land(1)))
-                qloads += 1
+                if par == 0:
+                    if qloads:
+                        yield "qempty", (qloads - 1) & 1
+                    bars["qfull"].expect_tx(1)
+                    copies.append(lambda g=grp: (mem.__setitem__("q", g), bars["qfull"].land(1)))
+                    qloads += 1
                 loaded = grp
+            if it % 2 != par:
+                it += 1
+                st += 1
+                if st == stages:
+                    st, ph = 0, ph ^ 1
+                continue
             if it >= stages:
                 yield f"empty{st}", ph ^ 1
                 if f8:
@@ -159,7 +167,8 @@ def simulate(slots, stages, nacc, groups, f8, seed, idle=0):
             bars[f"tempty{acc}"].arrive()
             it += 1
 
-    roles = {"producer": producer(), "mma0": issuer(0), "mma1": issuer(1)}
+    roles = {"producer0": producer(0), "producer1": producer(1), "mma0": issuer(0),
+             "mma1": issuer(1)}
     for g in range(groups + idle):
         for w in range(4):
             roles[f"epilogue{g}.{w}"] = epilogue(g, w)

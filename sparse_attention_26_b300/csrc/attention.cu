@@ -49,7 +49,7 @@ struct AttnShared {
   uint64_t empty[kMaxSlots];
   uint64_t s_full[kNSB];
   uint64_t s_free[kNSB];    // PV of the tile that last used this S/P buffer is done
-  uint64_t p_full;
+  uint64_t p_full[kNSB];    // P of the tile using this S/P buffer is in tensor memory
   uint64_t o_full;
   uint64_t q_full;
   uint64_t q_tmem;          // the other half of Q is in tensor memory
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&sm->drain[0]), 1);
     mbar_init(smem_u32(&sm->drain[1]), 1);
-    mbar_init(smem_u32(&sm->p_full), 128);
+    for (int i = 0; i < kNSB; ++i) mbar_init(smem_u32(&sm->p_full[i]), 128);
     mbar_init(smem_u32(&sm->o_full), 1);
     mbar_init(smem_u32(&sm->q_full), 1);
     mbar_init(smem_u32(&sm->q_tmem), 128);
@@ -612,18 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, got);  // warp-uniform
         if (!ok) break;
         // gathered rows were written by cp.async (generic proxy); the MMA
-        // reads through the async proxy
+        // reads through the async proxy.  (The invalid key rows of a streamed
+        // tail tile may hold anything: their S columns are masked, and the
+        // PV issuer zeroes them as values.)
         if (KIND == kSparse || KIND == kFused) fence_proxy_async_smem();
-        if ((KIND == kHca || (KIND == kFused && seg != 0)) && nvalid < kTile) {
-          // a streamed tail tile: zero its invalid key rows (they may hold
-          // anything, and P = 0 times a NaN would still be NaN)
-          uint8_t* dst = sRing + gsl * gsz * 8192;
-          for (int pc = nvalid * 8 + lane; pc < kTile * 8; pc += 32)
-            for (int e = 0; e < gsz; ++e)
-              *reinterpret_cast<uint4*>(dst + e * 8192 + swz128(pc >> 3, pc & 7)) =
-                  make_uint4(0, 0, 0, 0);
-          fence_proxy_async_smem();
-        }
         __syncwarp();
         if (lane == 0) {
           tc_fence_after();
@@ -668,17 +660,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sRa = smem_u32(sRing);
     bool ok = true;
     for (int i = 0; i < nt && ok; ++i) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->p_full), i & 1, abort, a.status,
+      // one barrier per S/P buffer: the softmax of tile i + kNSB needs
+      // S(i + kNSB), whose QK waited for PV(i), so no phase is skipped
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm->p_full[i % kNSB]), (i / kNSB) & 1,
+                                             abort, a.status,
                                              kWaitLimitNs, 23));
       if (!ok) break;
       const int64_t g = (int64_t)i * ngt + (ngt - 1);  // the tile's own group
       const int gsl = static_cast<int>(g % ng);
-      if (KIND == kSparse || KIND == kFused) {
-        // this warp's view of the gathered rows, for the async proxy
+      int seg, nvalid;
+      int64_t kt;
+      tile_of(i, seg, kt, nvalid);
+      // a streamed tail tile: its invalid key rows may hold anything (even
+      // NaN, and P = 0 times NaN is NaN), so this warp zeroes them as values
+      // before its product reads the group
+      const bool zero_tail = (KIND == kHca || (KIND == kFused && seg != 0)) && nvalid < kTile;
+      if (KIND == kSparse || KIND == kFused || zero_tail) {
+        // this warp's view of the copied rows (the copy landed before QK(i)
+        // read them), for the zeroing and for the async proxy
         ok = __all_sync(0xffffffffu,
                         mbar_wait(smem_u32(&sm->full[gsl]), static_cast<uint32_t>((g / ng) & 1),
                                   abort, a.status, kWaitLimitNs, 38));
         if (!ok) break;
+        if (zero_tail) {
+          uint8_t* dst = sRing + gsl * gsz * 8192;
+          for (int pc = nvalid * 8 + lane; pc < kTile * 8; pc += 32)
+            for (int e = 0; e < gsz; ++e)
+              *reinterpret_cast<uint4*>(dst + e * 8192 + swz128(pc >> 3, pc & 7)) =
+                  make_uint4(0, 0, 0, 0);
+        }
         fence_proxy_async_smem();
         __syncwarp();
       }
@@ -873,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tS + lane_base + sb * 64, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&sm->p_full));
+      mbar_arrive(smem_u32(&sm->p_full[sb]));
     }
     // ------------------------------------------------------------ epilogue
     // O rows go through shared memory (the Q area and the ring, free once

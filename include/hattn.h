@@ -235,6 +235,18 @@ HATTN_API int hattn_quantize_mxfp4_entries(const void* x, int B, int64_t N_cap, 
                                            int64_t j_begin, int64_t j_end, void* codes,
                                            void* scales, hattn_stream_t stream);
 
+/* hattn_csa_compress that also writes each entry's indexer key as MXFP4:
+ * codes ik4 [B][N_cap][dI/2] and E8M0 scales ik4_scale [B][N_cap][dI/32],
+ * quantised from the bf16-rounded key (the value ik_c holds) exactly as
+ * hattn_quantize_mxfp4 does; dI a multiple of 32.  One launch instead of the
+ * compression and a quantisation of its entries. */
+HATTN_API int hattn_csa_compress_mxfp4(const void* kv_raw, const void* ik_raw, const void* gate,
+                                       const float* gamma_kv, int B, int64_t L_cap, int D, int dI,
+                                       int m, int w, int r, float rope_base, float eps,
+                                       int64_t j_begin, int64_t j_end, void* kv_c, void* ik_c,
+                                       void* ik4, void* ik4_scale, int64_t N_cap,
+                                       hattn_stream_t stream);
+
 /* Indexer scores over MXFP4 keys ([AT] "Inference efficiency": the indexer's
  * QK path in FP4): ik4 [B][N_cap][64] code bytes and ik4_scale [B][N_cap][4]
  * E8M0 bytes as hattn_quantize_mxfp4 writes them (dI must be 128; N_cap a
@@ -243,9 +255,11 @@ HATTN_API int hattn_quantize_mxfp4_entries(const void* x, int B, int64_t N_cap, 
  * and the score is the plain definition over the decoded values,
  *   I[j] = sum_h w[b][t][h] * max(0, q~[b][t][h] . k~[b][j]),
  * with fp32 accumulation.  A key costs 68 bytes of HBM (against 256 for
- * bf16); every decoded element is exact in bf16, so the products run on the
- * bf16 tensor-core path after the keys are decoded in shared memory.  The
- * other arguments, limits and flags are hattn_indexer_scores_ex's. */
+ * bf16).  The products run on the block-scaled FP4 tensor-core path
+ * (kind::mxf4): the E2M1 codes of keys and queries are the operands and
+ * their E8M0 scales the block scales, so no key is decoded.  The other
+ * arguments, limits and flags are hattn_indexer_scores_ex's; queries go in
+ * groups of at most 128 rows (G * HI <= 128). */
 HATTN_API int hattn_indexer_scores_mxfp4(const void* iq, const float* w, const void* ik4,
                                          const void* ik4_scale, const int32_t* pos, int B, int T,
                                          int HI, int dI, int64_t N_cap, int m, int n_sms,

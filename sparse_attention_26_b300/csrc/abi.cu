@@ -146,12 +146,15 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
                     const float* gamma_kv, int B, int64_t L_cap, int D, int dI, int m, int w,
                     int r, float rope_base, float eps, int64_t j_begin, int64_t j_end, void* kv_c,
                     void* ik_c, int64_t N_cap, hattn_stream_t stream, void* ik8 = nullptr,
-                    float* ik_scale = nullptr, int64_t ring = 0) {
+                    float* ik_scale = nullptr, int64_t ring = 0, void* ik4 = nullptr,
+                    void* ik4_scale = nullptr) {
   REQUIRE_PTR(kv_raw);
   REQUIRE_PTR(gate);
   REQUIRE_PTR(kv_c);
   REQUIRE_F32(gamma_kv);
   REQUIRE((ik8 == nullptr) == (ik_scale == nullptr), "ik8 and ik_scale must both be given or both NULL");
+  REQUIRE((ik4 == nullptr) == (ik4_scale == nullptr),
+          "ik4 and ik4_scale must both be given or both NULL");
   REQUIRE((ik_raw == nullptr) == (ik_c == nullptr && ik8 == nullptr),
           "ik_raw needs an indexer-key output (ik_c or ik8), and an output needs ik_raw");
   if (ik_raw) {
@@ -160,6 +163,11 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
     if (ik8) {
       REQUIRE_PTR(ik8);
       REQUIRE_PTR(ik_scale);
+    }
+    if (ik4) {
+      REQUIRE_PTR(ik4);
+      REQUIRE_PTR(ik4_scale);
+      REQUIRE(dI % 32 == 0, "MXFP4 indexer keys need dI a multiple of 32, got %d", dI);
     }
     REQUIRE(dI >= 8 && dI <= 128 && dI % 8 == 0, "dI=%d must be a multiple of 8 in [8, 128]", dI);
   }
@@ -192,6 +200,8 @@ int compress_common(const void* kv_raw, const void* ik_raw, const void* gate,
   a.ik_out = static_cast<__nv_bfloat16*>(ik_c);
   a.ik8_out = static_cast<uint8_t*>(ik8);
   a.ik_scale_out = ik_scale;
+  a.ik4_out = static_cast<uint8_t*>(ik4);
+  a.ik4_scale_out = static_cast<uint8_t*>(ik4_scale);
   a.B = B;
   a.D = D;
   a.dI = ik_raw ? dI : 0;
@@ -514,6 +524,20 @@ int hattn_csa_compress_fp8(const void* kv_raw, const void* ik_raw, const void* g
   REQUIRE_PTR(ik_scale);
   return compress_common(kv_raw, ik_raw, gate, gamma_kv, B, L_cap, D, dI, m, w, r, rope_base, eps,
                          j_begin, j_end, kv_c, ik_c, N_cap, stream, ik8, ik_scale);
+}
+
+int hattn_csa_compress_mxfp4(const void* kv_raw, const void* ik_raw, const void* gate,
+                             const float* gamma_kv, int B, int64_t L_cap, int D, int dI, int m,
+                             int w, int r, float rope_base, float eps, int64_t j_begin,
+                             int64_t j_end, void* kv_c, void* ik_c, void* ik4, void* ik4_scale,
+                             int64_t N_cap, hattn_stream_t stream) {
+  REQUIRE_PTR(ik_raw);
+  REQUIRE_PTR(ik_c);
+  REQUIRE_PTR(ik4);
+  REQUIRE_PTR(ik4_scale);
+  return compress_common(kv_raw, ik_raw, gate, gamma_kv, B, L_cap, D, dI, m, w, r, rope_base, eps,
+                         j_begin, j_end, kv_c, ik_c, N_cap, stream, nullptr, nullptr, 0, ik4,
+                         ik4_scale);
 }
 
 int hattn_csa_compress_ring(const void* kv_ring, const void* ik_ring, const void* gate_ring,

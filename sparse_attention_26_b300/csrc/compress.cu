@@ -73,6 +73,47 @@ __device__ __forceinline__ void store8_e4m3(uint8_t* p, const float (&y)[8], flo
   *reinterpret_cast<uint2*>(p) = u;
 }
 
+// MXFP4 codes and block scale of the bf16-rounded values of an 8-wide piece
+// of the indexer key (the values the bf16 key holds), as the row quantiser
+// writes them: a block of 32 elements is the pieces of 4 consecutive lanes
+// (piece p on a lane with lane % 4 == p % 4), its scale 2^se with se =
+// floor(log2 amax) - 2 (at least -127), elements x * 2^-se rounded to E2M1
+// (nearest, ties to even, saturating), the low nibble the even element, a
+// zero stored as +0.  Every lane of the warp calls it (the block's amax is
+// reduced by shuffles); `valid` marks the lanes that hold a piece.
+__device__ __forceinline__ void store8_mxfp4(bool valid, const float (&y)[8], uint8_t* codes,
+                                             uint8_t* scales, int piece) {
+  float r[8];
+  float am = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    r[e] = bf16_round(y[e]);
+    am = fmaxf(am, fabsf(r[e]));
+  }
+  if (!valid) am = 0.f;
+  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+  if (!valid) return;
+  int se = static_cast<int>((__float_as_uint(am) >> 23) & 0xffu) - 127 - 2;
+  se = se < -127 ? -127 : se;
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);  // 2^-se
+  uint32_t w = 0;
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    uint32_t c;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(c)
+        : "f"(__fmul_rn(r[e + 1], inv)), "f"(__fmul_rn(r[e], inv)));
+    w |= c << (4 * e);
+  }
+  const uint32_t mag = w & 0x77777777u;
+  w = mag | (w & ((mag + 0x77777777u) & 0x88888888u));  // drop the sign of zero nibbles
+  *reinterpret_cast<uint32_t*>(codes + piece * 4) = w;
+  if ((piece & 3) == 0) scales[piece >> 2] = static_cast<uint8_t>(se + 127);
+}
+
 __global__ void __launch_bounds__(kCompressThreads)
     compress_kernel(const __grid_constant__ CompressArgs a) {
   __shared__ float alpha[kMaxW];
@@ -195,10 +236,10 @@ __global__ void __launch_bounds__(kCompressThreads)
     // reduce the slices (fixed order), RMS over the KV part, largest
     // magnitude of the indexer key (for its E4M3 codes)
     float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.f;
     float ss = 0.f, am = 0.f;
     if (tid < NC) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = 0.f;
       for (int s = 0; s < S; ++s)
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] += partial[s * width + tid * 8 + e];
@@ -260,6 +301,11 @@ __global__ void __launch_bounds__(kCompressThreads)
         store8_e4m3(a.ik8_out + row * a.dI + (tid - NCk) * 8, v, q.inv);
         if (tid == NCk) a.ik_scale_out[row] = q.scale;
       }
+    }
+    if (a.ik4_out) {
+      const int64_t row = (int64_t)b * a.N_cap + j;
+      store8_mxfp4(tid >= NCk && tid < NC, v, a.ik4_out + row * (a.dI / 2),
+                   a.ik4_scale_out + row * (a.dI / 32), tid - NCk);
     }
     __syncthreads();
   }
@@ -392,6 +438,11 @@ __global__ void __launch_bounds__(kSmallThreads)
         store8_e4m3(a.ik8_out + row * a.dI + (tid - NCk) * 8, acc, q.inv);
         if (tid == NCk) a.ik_scale_out[row] = q.scale;
       }
+    }
+    if (a.ik4_out) {
+      const int64_t row = (int64_t)b * a.N_cap + j;
+      store8_mxfp4(tid >= NCk && tid < NC, acc, a.ik4_out + row * (a.dI / 2),
+                   a.ik4_scale_out + row * (a.dI / 32), tid - NCk);
     }
     __syncthreads();  // alpha and red are rewritten by the next entry
   }

@@ -28,6 +28,8 @@ struct CompressArgs {
   __nv_bfloat16* ik_out;        // [B][N_cap][dI] or null
   uint8_t* ik8_out;             // [B][N_cap][dI] E4M3 codes of the indexer key, or null
   float* ik_scale_out;          // [B][N_cap] their row scales (with ik8_out)
+  uint8_t* ik4_out;             // [B][N_cap][dI/2] MXFP4 codes of the indexer key, or null
+  uint8_t* ik4_scale_out;       // [B][N_cap][dI/32] their E8M0 block scales (with ik4_out)
   int B, D, dI, m, w, r;
   int64_t L_cap, N_cap, j_begin, j_end;
   int64_t ring;                 // 0: token u in row u; else row u mod ring (L_cap == ring)

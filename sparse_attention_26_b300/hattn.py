@@ -35,6 +35,9 @@ _SIGS = {
     "hattn_csa_compress_fp8": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
                                       _i32, _f32, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _i64,
                                       _vp]),
+    "hattn_csa_compress_mxfp4": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32, _i32,
+                                        _i32, _f32, _f32, _i64, _i64, _vp, _vp, _vp, _vp, _i64,
+                                        _vp]),
     "hattn_quantize_e4m3": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp]),
     "hattn_quantize_mxfp4": (_i32, [_vp, _i64, _i32, _vp, _vp, _vp]),
     "hattn_compress_hidden_workspace_bytes": (_sz, [_i32, _i64, _i64, _i32, _i32, _i32]),
@@ -264,6 +267,34 @@ def csa_compress_fp8(kv_raw, ik_raw, gate, *, r, j_begin=0, j_end=None, m=4, w=8
                                         _ptr(kv_c), _ptr(ik_c), _ptr(ik8), _ptr(ik_scale), N_cap,
                                         _stream(stream)))
     return kv_c, ik8, ik_scale
+
+
+def csa_compress_mxfp4(kv_raw, ik_raw, gate, *, r, kv_c, ik_c, ik4, ik4_scale, j_begin=0,
+                       j_end=None, m=4, w=8, gamma_kv=None, rope_base=10000.0, eps=1e-6,
+                       stream=None):
+    """csa_compress that also writes each entry's indexer key as MXFP4
+    (codes ik4 uint8 [B, N_cap, dI/2], E8M0 scales ik4_scale uint8
+    [B, N_cap, dI/32]), bit for bit what quantize_mxfp4 makes of ik_c."""
+    _need(kv_raw, "kv_raw", torch.bfloat16, 3)
+    _need(ik_raw, "ik_raw", torch.bfloat16, 3)
+    _need(gate, "gate", torch.bfloat16, 2)
+    B, L, D = kv_raw.shape
+    dI = ik_raw.shape[2]
+    N_cap = kv_c.shape[1]
+    if j_end is None:
+        j_end = min(N_cap, L // m)
+    _need(kv_c, "kv_c", torch.bfloat16, 3)
+    _need(ik_c, "ik_c", torch.bfloat16, 3)
+    _need(ik4, "ik4", torch.uint8, 3)
+    _shape(ik4, "ik4", (B, N_cap, dI // 2))
+    _need(ik4_scale, "ik4_scale", torch.uint8, 3)
+    _shape(ik4_scale, "ik4_scale", (B, N_cap, dI // 32))
+    _opt(gamma_kv, "gamma_kv", torch.float32)
+    _check(lib().hattn_csa_compress_mxfp4(_ptr(kv_raw), _ptr(ik_raw), _ptr(gate), _ptr(gamma_kv),
+                                          B, L, D, dI, m, w, r, rope_base, eps, j_begin, j_end,
+                                          _ptr(kv_c), _ptr(ik_c), _ptr(ik4), _ptr(ik4_scale),
+                                          N_cap, _stream(stream)))
+    return kv_c, ik_c, ik4, ik4_scale
 
 
 def csa_compress_ring(kv_ring, ik_ring, gate_ring, *, r, j_begin, j_end, kv_c, ik_c, m=4, w=8,

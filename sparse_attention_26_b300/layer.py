@@ -207,12 +207,14 @@ class HybridLayer:
             hattn.csa_compress_fp8(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j0,
                                    j_end=j1, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c,
                                    ik8=self.ik8, ik_scale=self.ik_scale)
+        elif self.mx4:
+            # one launch: the entries and their MXFP4 indexer keys
+            hattn.csa_compress_mxfp4(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j0,
+                                     j_end=j1, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c,
+                                     ik_c=self.ik_c, ik4=self.ik4, ik4_scale=self.ik4_scale)
         else:
             hattn.csa_compress(r["kv_raw"], r["ik_raw"], r["gate_csa"], r=wl.r, j_begin=j0,
                                j_end=j1, m=wl.m_csa, w=wl.w_csa, kv_c=self.kv_c, ik_c=self.ik_c)
-            if self.mx4:
-                hattn.quantize_mxfp4_entries(self.ik_c, self.ik4, self.ik4_scale, j_begin=j0,
-                                             j_end=j1)
 
     def _indexer_topk(self, iq, w, pos, b, events=None, n_sms=0, fresh_from=-1, dependent=False):
         """Indexer scores and top-k as one call (the score kernel counts the

@@ -385,6 +385,35 @@ def test_csa_compress_fp8(B, L, D, dI, r, j0, j1):
     assert (ik8[:, :j0] == 0).all() and (ik8[:, j1:] == 0).all()
 
 
+@pytest.mark.parametrize("B,L,D,dI,r,j0,j1", [
+    (2, 1024, 512, 128, 64, 255, 256),   # one new entry per sequence: the small kernel
+    (2, 4096, 512, 128, 64, 0, 1024),    # cache build: the grid-stride kernel
+])
+def test_csa_compress_mxfp4(B, L, D, dI, r, j0, j1):
+    """The MXFP4 indexer key the compressor writes is, byte for byte, the
+    oracle's quantisation of the bf16 key it writes beside it; the KV entries
+    and bf16 keys are those of the plain call, the other entries untouched."""
+    kv = randn_bf16((B, L, D), 51)
+    ik = randn_bf16((B, L, dI), 52)
+    gate = randn_bf16((B, L), 53)
+    N_cap = L // 4
+    d = dict(kv=kv.to(DEV), ik=ik.to(DEV), gate=gate.to(DEV))
+    kv_c, ik_c = hattn.csa_compress(d["kv"], d["ik"], d["gate"], r=r, j_begin=j0, j_end=j1)
+    kv_c4 = torch.zeros_like(kv_c)
+    ik_c4 = torch.zeros_like(ik_c)
+    ik4 = torch.full((B, N_cap, dI // 2), 0xA5, dtype=torch.uint8, device=DEV)
+    ik4s = torch.full((B, N_cap, dI // 32), 0x5A, dtype=torch.uint8, device=DEV)
+    hattn.csa_compress_mxfp4(d["kv"], d["ik"], d["gate"], r=r, j_begin=j0, j_end=j1, kv_c=kv_c4,
+                             ik_c=ik_c4, ik4=ik4, ik4_scale=ik4s)
+    hattn.check_status()
+    assert torch.equal(kv_c4, kv_c) and torch.equal(ik_c4, ik_c)
+    rc, rs = orc.quantize_mxfp4(bits(ik_c[:, j0:j1].reshape(-1, dI).cpu()))
+    np.testing.assert_array_equal(_u8(ik4[:, j0:j1]).reshape(-1, dI // 2), rc)
+    np.testing.assert_array_equal(_u8(ik4s[:, j0:j1]).reshape(-1, dI // 32), rs)
+    assert (ik4[:, :j0] == 0xA5).all() and (ik4[:, j1:] == 0xA5).all()
+    assert (ik4s[:, :j0] == 0x5A).all() and (ik4s[:, j1:] == 0x5A).all()
+
+
 def _indexer_fp8_case(B, T, HI, N_cap, k, pos, seed, m=4):
     dI = 128
     iq = randn_bf16((B, T, HI, dI), seed)

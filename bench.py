@@ -143,13 +143,15 @@ def indexer_overhead_bytes(wl):
 
 # DRAM traffic of indexer_score_kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum) from one ncu capture of an 8 x 65,536-entry launch
-# per key format (bf16 keys: 137.65 MB; E4M3 keys: 69.91 MB), per entry
-# processed; it applies only to the kernel sources it was taken on, checked
-# by hash, and to one query per sequence, else the bench reports null.
+# per key format (bf16 keys: 137.39 MB; E4M3 keys: 70.47 MB; MXFP4 keys:
+# 35.94 MB), per entry processed; it applies only to the kernel sources it
+# was taken on, checked by hash, and to one query per sequence, else the
+# bench reports null.
 INDEXER_TRAFFIC = {
-    "bytes_per_entry": {"bf16": 137.655e6 / (8 * 65536), "fp8": 69.911e6 / (8 * 65536)},
+    "bytes_per_entry": {"bf16": 137.392e6 / (8 * 65536), "fp8": 70.469e6 / (8 * 65536),
+                        "mxfp4": 35.942e6 / (8 * 65536)},
     "sources": ["indexer.cu", "common.cuh"],
-    "sha256": "775364c0e4fd8fce93517a370578c464a7333d6f85a71a513fdfa841b63fdbe5",
+    "sha256": "23cfb5f256c44eb372970b4e7e26a639960d782376ed8a8df010ac792f654f25",
     "profile": "profiles/indexer_score_kernel_decode_8x65536.md",
 }
 

@@ -95,11 +95,17 @@ __global__ void __launch_bounds__(kQuantThreads)
     // rows of this group that exist (warp-uniform); row k sits k * n
     // elements past the group's first
     const int nk = rows - row0 < kMxRows ? static_cast<int>(rows - row0) : kMxRows;
-    int64_t rk[kMxRows];  // the rows' places in the cache
+    int64_t rk[kMxRows];  // the rows' places in the cache: one division per group
+    {
+      int64_t q = row0 / nj, rem = row0 - q * nj;
 #pragma unroll
-    for (int k = 0; k < kMxRows; ++k) {
-      const int64_t r = row0 + k;
-      rk[k] = (r / nj) * ncap + j0 + r % nj;
+      for (int k = 0; k < kMxRows; ++k) {
+        rk[k] = q * ncap + j0 + rem;
+        if (++rem == nj) {
+          rem = 0;
+          ++q;
+        }
+      }
     }
     for (int base = 0; base < n; base += 128) {
       const int i = base + lane * 4;

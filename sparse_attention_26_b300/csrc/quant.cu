@@ -79,10 +79,11 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
 
 // kN > 0: rows of exactly kN elements (row offsets become immediates); kN = 0:
 // any n, a multiple of 32.
-// Row r of the call is row (r / nj) * ncap + j0 + r % nj of x, codes and
-// scales (the identity for nj = ncap = rows, j0 = 0; an entry range
-// [j0, j0 + nj) of every sequence of a [B][ncap][n] cache otherwise).
-template <int kN>
+// kMapped: row r of the call is row (r / nj) * ncap + j0 + r % nj of x,
+// codes and scales (an entry range [j0, j0 + nj) of every sequence of a
+// [B][ncap][n] cache); else row r is row r (the offsets of a group's rows
+// are then immediates).
+template <int kN, bool kMapped>
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_mxfp4_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int n_arg,
                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int64_t nj,
@@ -95,8 +96,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     // rows of this group that exist (warp-uniform); row k sits k * n
     // elements past the group's first
     const int nk = rows - row0 < kMxRows ? static_cast<int>(rows - row0) : kMxRows;
-    int64_t rk[kMxRows];  // the rows' places in the cache: one division per group
-    {
+    int64_t rk[kMxRows];  // the rows' places: one division per group when mapped
+    if (kMapped) {
       int64_t q = row0 / nj, rem = row0 - q * nj;
 #pragma unroll
       for (int k = 0; k < kMxRows; ++k) {
@@ -106,6 +107,9 @@ __global__ void __launch_bounds__(kQuantThreads)
           ++q;
         }
       }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kMxRows; ++k) rk[k] = row0 + k;
     }
     for (int base = 0; base < n; base += 128) {
       const int i = base + lane * 4;
@@ -182,7 +186,10 @@ cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* x, int64_t rows, int n, u
                                   int64_t j0, int64_t ncap) {
   if (rows <= 0) return cudaSuccess;
   // one wave of resident CTAs, each striding over groups of rows
-  auto kernel = n == 128 ? quantize_mxfp4_kernel<128> : quantize_mxfp4_kernel<0>;
+  const bool mapped = nj > 0;
+  auto kernel = n == 128 ? (mapped ? quantize_mxfp4_kernel<128, true>
+                                   : quantize_mxfp4_kernel<128, false>)
+                         : (mapped ? quantize_mxfp4_kernel<0, true> : quantize_mxfp4_kernel<0, false>);
   int resident = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, kQuantThreads, 0);
   if (e != cudaSuccess) return e;
@@ -190,7 +197,7 @@ cudaError_t launch_quantize_mxfp4(const __nv_bfloat16* x, int64_t rows, int n, u
   const int64_t want = (rows + per_cta - 1) / per_cta;
   const int64_t cap = static_cast<int64_t>(num_sms) * (resident > 0 ? resident : 1);
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  if (nj <= 0) {  // plain rows
+  if (!mapped) {  // plain rows
     nj = rows;
     j0 = 0;
     ncap = rows;

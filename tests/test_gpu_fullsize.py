@@ -88,6 +88,12 @@ def _check_compress(wl, inp, layer, b, entries, kind):
             assert (np.abs(deq - ref) <= bound).all(), f"FP8 indexer key {j}"
         elif kind == "csa":
             assert rel_l2(layer.ik_c[b, j], ri[0, 0]) <= KV_REL_L2, f"indexer key {j}"
+            if layer.mx4:
+                # the MXFP4 key is, byte for byte, the oracle's quantisation
+                # of the bf16 key beside it
+                rc, rs = orc.quantize_mxfp4(_bits(layer.ik_c[b, j:j + 1]))
+                np.testing.assert_array_equal(layer.ik4[b, j].cpu().numpy(), rc[0])
+                np.testing.assert_array_equal(layer.ik4_scale[b, j].cpu().numpy(), rs[0])
 
 
 def _check_sequence(wl, inp, layer, res_b, res, b, ts):
@@ -107,6 +113,10 @@ def _check_sequence(wl, inp, layer, res_b, res, b, ts):
         if layer.fp8:
             ref_sc = orc.indexer_scores_e4m3(iq, w, layer.ik8[b:b + 1].cpu().numpy(),
                                              layer.ik_scale[b:b + 1].cpu().numpy(), pos, wl.m_csa)
+        elif layer.mx4:
+            ref_sc = orc.indexer_scores_mxfp4(iq, w, layer.ik4[b:b + 1].cpu().numpy(),
+                                              layer.ik4_scale[b:b + 1].cpu().numpy(), pos,
+                                              wl.m_csa)
         else:
             ref_sc = orc.indexer_scores(iq, w, _bits(layer.ik_c[b:b + 1]), pos, wl.m_csa)
         got_sc = f64(bufs["scores"][b:b + 1, tsel])
@@ -173,6 +183,19 @@ def test_hybrid_decode_1m_fp8_keys():
     n = wl.L // wl.m_csa
     _check_compress(wl, inp, layer, 3, [0, 1, 123457, n - 1], "csa")
     _check_sequence(wl, inp, layer, res_b, res, 3, [0])
+    assert torch.isfinite(res[0].float()).all()
+
+
+def test_hybrid_decode_1m_mxfp4_keys():
+    """The 1M decode step with the indexer keys held as MXFP4 codes and block
+    scales: the compressor's MXFP4 keys (bit for bit the oracle's
+    quantisation of its bf16 keys), the block-scaled indexer scores (against
+    the oracle's decoded definition), top-k, and the attention and merge."""
+    wl = synth.WORKLOADS["hybrid_decode_1m"]
+    inp, layer, res_b, res = _run(wl, t_new=wl.L - 1, side=True, indexer_keys="mxfp4")
+    n = wl.L // wl.m_csa
+    _check_compress(wl, inp, layer, 5, [0, 1, 123457, n - 1], "csa")
+    _check_sequence(wl, inp, layer, res_b, res, 5, [0])
     assert torch.isfinite(res[0].float()).all()
 
 

@@ -151,7 +151,7 @@ INDEXER_TRAFFIC = {
     "bytes_per_entry": {"bf16": 137.392e6 / (8 * 65536), "fp8": 70.469e6 / (8 * 65536),
                         "mxfp4": 35.942e6 / (8 * 65536)},
     "sources": ["indexer.cu", "common.cuh"],
-    "sha256": "23cfb5f256c44eb372970b4e7e26a639960d782376ed8a8df010ac792f654f25",
+    "sha256": "f203c562db1d20ac7d7eb0198a42b71a9a11a59abfcc873e0b437daaa8690a3f",
     "profile": "profiles/indexer_score_kernel_decode_8x65536.md",
 }
 

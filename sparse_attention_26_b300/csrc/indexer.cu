@@ -11,13 +11,14 @@
 // epilogue applies ReLU, the per-head weights and the per-query head sum.
 //
 // Work = (query group, 128-entry block) slots, flattened and split evenly
-// over a grid of one CTA per SM.  Roles: warp 0 issues TMA loads of key
-// blocks (128B-swizzled, a ring of `stages` buffers) and of the group's
-// queries; warps 1 and 2 issue the MMAs (M=128, N=NQ) of alternate slots
-// into a ring of `nacc` tensor-memory accumulators; kEpiGroups groups of
-// four warps drain alternate accumulators (tcgen05.ld), reduce them and
-// write fp32 scores with coalesced stores.  HBM traffic is the key blocks
-// once plus the scores.
+// over a grid of one CTA per SM.  Roles: two producer threads (warp 0 and
+// the last warp) issue the TMA loads of the key blocks of even and odd slots
+// into a ring of `stages` buffers (and warp 0 the group's queries); warps 1
+// and 2 issue the MMAs (M=128, N=NQ) of alternate slots into a ring of
+// `nacc` tensor-memory accumulators; three groups of four warps (two when
+// nacc is not a multiple of 3) drain the accumulators in turn (tcgen05.ld),
+// reduce them and write fp32 scores with coalesced stores.  HBM traffic is
+// the key blocks once plus the scores.
 //
 // FP8 keys ("DeepSeek-V4" atlas spec sheet, "Inference efficiency": the
 // indexer QK path runs in low precision): each key is 128 E4M3 codes (one
@@ -28,6 +29,13 @@
 //     I(t, j) = s_j * sum_h (w[t,h] * s_h) * max(0, q8_h . k8_j),
 // so the scales cost one multiply per column weight and one per score.
 // A key costs 128 + 4 bytes instead of 256.
+//
+// MXFP4 keys (the same spec sheet names MXFP4 for that path): 64 bytes of
+// E2M1 codes and 4 E8M0 block scales per key.  The epilogue warps quantise
+// the query rows to E2M1 codes and block scales; the MMAs run
+// kind::mxf4 with block scaling (K = 64 per call, 2 calls per block), the
+// scales of both operands copied into tensor memory, so the product is the
+// score's dot product over the decoded values.  A key costs 68 bytes.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -677,7 +685,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (F8 || MX) {
         // the group's bf16 query rows have landed: quantise this warp's
         // share, publish it to the MMA issuers, then wait for the others'
-        // row scales (MXFP4: the rows' round trip, in place)
+        // row scales (MXFP4: the rows' E2M1 codes and their scale atom)
         bool got = mbar_wait(smem_u32(&sm->qfull), qn & 1, abort, a.status, kWaitLimitNs, 18);
         if (!__all_sync(0xffffffffu, got)) return false;
         if (MX) mx_query_codes(sQ, sQ4, sfb_atom, a.NQ, ew, lane);

@@ -595,10 +595,11 @@ def indexer_scores_mxfp4(iq, w, ik4, ik4_scale, pos, *, m=4, score_out=None, n_s
                          fresh_from=-1, dependent=False, stream=None):
     """indexer_scores over MXFP4 keys (codes ik4 uint8 [B, N_cap, 64] and E8M0
     scales ik4_scale uint8 [B, N_cap, 4], as quantize_mxfp4 writes them); the
-    bf16 queries take the same round trip in the kernel."""
+    kernel quantises the bf16 queries the same way, and the score is the
+    definition over the decoded values (block-scaled FP4 products)."""
+    _need(iq, "iq", torch.bfloat16, 4)
     B, T, HI, dI = iq.shape
     N_cap = ik4.shape[1]
-    _need(iq, "iq", torch.bfloat16, 4)
     _need(w, "w", torch.float32, 3)
     _shape(w, "w", (B, T, HI))
     _need(pos, "pos", torch.int32, 2)
@@ -618,9 +619,9 @@ def indexer_topk_mxfp4(iq, w, ik4, ik4_scale, pos, *, k, m=4, idx_out=None, scor
                        workspace=None, n_sms=0, fresh_from=-1, dependent=False, split_event=None,
                        split_external=False, stream=None):
     """indexer_topk over MXFP4 keys (see indexer_scores_mxfp4)."""
+    _need(iq, "iq", torch.bfloat16, 4)
     B, T, HI, dI = iq.shape
     N_cap = ik4.shape[1]
-    _need(iq, "iq", torch.bfloat16, 4)
     _need(w, "w", torch.float32, 3)
     _shape(w, "w", (B, T, HI))
     _need(pos, "pos", torch.int32, 2)

@@ -151,7 +151,7 @@ INDEXER_TRAFFIC = {
     "bytes_per_entry": {"bf16": 137.392e6 / (8 * 65536), "fp8": 70.469e6 / (8 * 65536),
                         "mxfp4": 35.942e6 / (8 * 65536)},
     "sources": ["indexer.cu", "common.cuh"],
-    "sha256": "f203c562db1d20ac7d7eb0198a42b71a9a11a59abfcc873e0b437daaa8690a3f",
+    "sha256": "bb3161b662091452e42a3d6f15e8f8ddc0b63598163f6dc1bd11b66ec3ccb335",
     "profile": "profiles/indexer_score_kernel_decode_8x65536.md",
 }
 

@@ -487,9 +487,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
     // Warp 1 issues the products of the even live slots and warp 2 those of
-    // the odd ones: a single thread issues a chained tcgen05.mma only every
-    // ~64 ns, close to a slot's share of the key stream, so two issuers keep
-    // the tensor core ahead of it.  Slot `it` accumulates into accumulator
+    // the odd ones, so that one issuer's waits and per-slot bookkeeping
+    // overlap the other's products.  Slot `it` accumulates into accumulator
     // it % nacc, its (it / nacc)-th use.
     const int par = warp == 1 ? 0 : 1;
     if (MX) {
@@ -642,8 +641,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
   } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
-    // Group eg drains the slots it with it % kEpiGroups == eg; its warp for
-    // tensor-memory lanes quad*32 .. quad*32+31 handles those 32 entries.
+    // Group eg drains the slots it with it % egroups == eg (a group past
+    // egroups drains none but still quantises its share of each group's
+    // query rows); its warp for tensor-memory lanes quad*32 .. quad*32+31
+    // handles those 32 entries.
     const int ew = warp - kFirstEpiWarp;
     const int eg = ew >> 2;
     const int quad = warp & 3;

@@ -231,6 +231,27 @@ def test_mxfp4_validation(L):
     # no rows: nothing is read or written, so null pointers (an empty tensor's) pass
     assert L.hattn_quantize_mxfp4(N, 0, 128, N, N, s) == hattn.OK
     assert L.hattn_quantize_e4m3(N, 0, 128, N, N, s) == hattn.OK
+    # an entry range of a cache: inside [0, N_cap); an empty one touches nothing
+    rc = L.hattn_quantize_mxfp4_entries(FAKE, 2, 100, 128, 90, 101, FAKE, FAKE, s)
+    assert rc == hattn.INVALID_ARG and "entry range" in _err(L)
+    rc = L.hattn_quantize_mxfp4_entries(FAKE, 2, 100, 48, 0, 10, FAKE, FAKE, s)
+    assert rc == hattn.INVALID_ARG and "n=48" in _err(L)
+    assert L.hattn_quantize_mxfp4_entries(N, 2, 100, 128, 5, 5, N, N, s) == hattn.OK
+    # the compressor's MXFP4 key needs the bf16 key, the codes and the scales,
+    # and whole 32-element blocks
+    rc = L.hattn_csa_compress_mxfp4(FAKE, FAKE, FAKE, N, 1, 64, 64, 32, 4, 8, 16, 1e4, 1e-6, 0,
+                                    4, FAKE, FAKE, FAKE, N, 16, s)
+    assert rc == hattn.INVALID_ARG and "ik4_scale" in _err(L)
+    rc = L.hattn_csa_compress_mxfp4(FAKE, FAKE, FAKE, N, 1, 64, 64, 32, 4, 8, 16, 1e4, 1e-6, 0,
+                                    4, FAKE, N, FAKE, FAKE, 16, s)
+    assert rc == hattn.INVALID_ARG and "ik_c" in _err(L)
+    rc = L.hattn_csa_compress_mxfp4(FAKE, FAKE, FAKE, N, 1, 64, 64, 40, 4, 8, 16, 1e4, 1e-6, 0,
+                                    4, FAKE, FAKE, FAKE, FAKE, 16, s)
+    assert rc == hattn.INVALID_ARG and "multiple of 32" in _err(L)
+    # MXFP4 scoring: dI = 128, and queries in groups of at most 128 rows
+    rc = L.hattn_indexer_scores_mxfp4(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 100, 4, 0, -1,
+                                      FAKE, 0, s)
+    assert rc == hattn.INVALID_ARG and "dI = 128" in _err(L)
 
 
 def test_ring_and_hidden_validation(L):
